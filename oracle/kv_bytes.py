@@ -1,0 +1,19 @@
+"""KV-cache size accounting (test infrastructure; see ``oracle/__init__``).
+
+Follows the tutorial page "LLM 推理服务引擎深度拆解", section 1.3 (KV cache
+bytes = 2 for K and V x layers x kv_heads x head_dim x seq_len x dtype_bytes
+x batch) and section 5.4 (bytes moved when a request's KV is handed from a
+prefill instance to a decode instance: the same product for one request).
+The essay page "LLM推理PD分离架构深度工程实践", section 3, works the same
+formula per token and per layer.
+"""
+
+
+def kv_cache_bytes(layers: int, kv_heads: int, head_dim: int, seq_len: int,
+                   dtype_bytes: int = 2, batch: int = 1) -> int:
+    return 2 * layers * kv_heads * head_dim * seq_len * dtype_bytes * batch
+
+
+def pd_transfer_bytes(seq_len: int, layers: int, kv_heads: int, head_dim: int,
+                      dtype_bytes: int) -> int:
+    return kv_cache_bytes(layers, kv_heads, head_dim, seq_len, dtype_bytes, 1)

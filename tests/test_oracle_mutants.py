@@ -1,0 +1,87 @@
+"""Planted mistakes: each mutant is a copy of oracle.c with one plausible error
+(a dropped term, a wrong sign or index, a transposed operand).  The pins in
+test_oracle_pins.py must reject every one of them.  CPU only; the mutants are
+built in a temporary directory and never touch the real oracle build."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, exact text in oracle.c, replacement)
+MUTANTS = [
+    ("gqa_head_mapping", "h / G, key_cache, value_cache, Hk, D, S, NB, scale,\n                          dtype) != 0;\n    }\n    return bad;\n}\n\n/* ---- decode written",
+     "h % Hk, key_cache, value_cache, Hk, D, S, NB, scale,\n                          dtype) != 0;\n    }\n    return bad;\n}\n\n/* ---- decode written"),
+    ("scale_dropped", "s[t] = scale * dot;", "s[t] = dot;"),
+    ("softmax_sign", "double w = exp(s[t] - m);", "double w = exp(m - s[t]);"),
+    ("causal_off_by_one", "P + j + 1, bt_row", "P + j, bt_row"),
+    ("slot_offset_swapped", "int64_t blk = slot / S, off = slot % S;",
+     "int64_t blk = slot % S, off = slot / S;"),
+    ("page_offset_wrong", "const uint16_t* k = kc + cache_index(blk, kvh, t % S, Hk, S, D);",
+     "const uint16_t* k = kc + cache_index(blk, kvh, t / S, Hk, S, D);"),
+    ("value_from_key_pool", "const uint16_t* v = vc + cache_index(",
+     "const uint16_t* v = kc + cache_index("),
+    ("merge_sign", "double c = exp(mp[p] - M);", "double c = exp(M - mp[p]);"),
+    ("f16_exponent_bias", "ldexp((double)(1024 + f), e - 25)", "ldexp((double)(1024 + f), e - 24)"),
+    ("bf16_mantissa_bits", "int f = b & 0x7f;", "int f = b & 0x3f;"),
+    ("copy_src_dst_swapped",
+     "key_caches[l][dst * block_elems + e] = key_caches[l][src * block_elems + e];",
+     "key_caches[l][src * block_elems + e] = key_caches[l][dst * block_elems + e];"),
+    ("prefill_prior_len", "int64_t P = context_lens[i] - C;", "int64_t P = context_lens[i] - C + 1;"),
+]
+
+PIN_CHECKS = [
+    lambda: pins.test_all_16bit_patterns_decode_like_torch(oracle.F16, pins.torch.float16),
+    lambda: pins.test_all_16bit_patterns_decode_like_torch(oracle.BF16, pins.torch.bfloat16),
+    pins.test_store_then_gather_returns_the_token,
+    pins.test_copy_blocks_brute_force,
+    pins.test_decode_matches_brute_force_tiny,
+    pins.test_decode_matches_brute_force_bf16_gqa_variants,
+    pins.test_ctx1_returns_v_exactly,
+    lambda: pins.test_split_partitions_merge_to_unsplit(48),
+    pins.test_prefill_matches_brute_force,
+    pins.test_prefill_special_cases_reduce_to_decode,
+]
+
+
+def _build_mutant(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutant {name}: anchor text not found exactly once"
+    path = tmp_path / f"{name}.c"
+    path.write_text(src.replace(old, new))
+    lib = tmp_path / f"lib{name}.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                    str(path), "-o", str(lib), "-lm"], check=True)
+    return str(lib)
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_reject_mutant(tmp_path, name, old, new):
+    lib = _build_mutant(tmp_path, name, old, new)
+    prev = oracle.swap_library(lib)
+    caught = []
+    try:
+        for chk in PIN_CHECKS:
+            try:
+                chk()
+            except (AssertionError, ValueError):
+                caught.append(chk)
+    finally:
+        oracle.swap_library(None)
+        del prev
+    assert caught, f"no pin rejects the planted mistake '{name}'"
+
+
+def test_unmutated_copy_passes_every_check(tmp_path):
+    lib = _build_mutant(tmp_path, "identity", "enum { ORC_F16 = 0, ORC_BF16 = 1 };",
+                        "enum { ORC_F16 = 0, ORC_BF16 = 1 };")
+    oracle.swap_library(lib)
+    try:
+        for chk in PIN_CHECKS:
+            chk()
+    finally:
+        oracle.swap_library(None)

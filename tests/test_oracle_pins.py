@@ -1,0 +1,401 @@
+"""Pins of the float64 oracle against things other than itself: values the
+pages print, closed forms, special cases with a textbook answer, and brute
+force on tiny inputs.  CPU only."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pd_inputs
+from oracle import BlockManager, Sequence
+from tests import brute_force as bf
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---- 16-bit float decoding ----------------------------------------------
+
+@pytest.mark.parametrize("dtype,tdt", [(oracle.F16, torch.float16), (oracle.BF16, torch.bfloat16)])
+def test_all_16bit_patterns_decode_like_torch(dtype, tdt):
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    ref = bits.view(tdt).to(torch.float64).numpy()
+    got = oracle.to_double(bits.numpy(), dtype)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+# ---- KV-bytes formula ----------------------------------------------------
+
+def test_kv_bytes_printed_values():
+    g = _load("kv_bytes.json")
+    for c in g["cases"]:
+        args = {k: c[k] for k in ("layers", "kv_heads", "head_dim", "seq_len", "dtype_bytes", "batch")}
+        assert oracle.kv_cache_bytes(**args) == c["bytes"], c["cite"]
+    for c in g["lower_bounds"]:
+        args = {k: c[k] for k in ("layers", "kv_heads", "head_dim", "seq_len", "dtype_bytes", "batch")}
+        assert oracle.kv_cache_bytes(**args) > c["more_than_bytes"], c["cite"]
+    r = g["ratios"]
+    assert oracle.kv_cache_bytes(1, r[0]["kv_heads_from"], 128, 1) == \
+        r[0]["ratio"] * oracle.kv_cache_bytes(1, r[0]["kv_heads_to"], 128, 1)
+    assert oracle.kv_cache_bytes(1, 8, 128, 1, r[1]["dtype_from"]) == \
+        r[1]["ratio"] * oracle.kv_cache_bytes(1, 8, 128, 1, r[1]["dtype_to"])
+    # the transfer of one 8K request equals the per-request cache size
+    assert oracle.pd_transfer_bytes(8192, 32, 8, 128, 2) == 1 << 30
+
+
+# ---- block manager --------------------------------------------------------
+
+def test_block_manager_fork_demo():
+    g = _load("block_manager_fork_demo.json")
+    mgr = BlockManager(g["num_blocks"], g["block_size"])
+    s = Sequence(mgr, 0)
+    copies = [s.append_slot()[1] for _ in range(g["prompt_len"])]
+    assert all(c is None for c in copies)
+    assert s.block_table == g["prompt_blocks"]
+    assert mgr.usage == g["usage_after_prompt"]
+    kids = [s.fork(i + 1) for i in range(g["n_children"])]
+    assert mgr.usage == g["usage_after_fork"]
+    assert all(mgr.ref_count[b] == g["ref_count_shared_after_fork"] for b in s.block_table)
+    res = [k.append_slot() for k in kids]
+    assert [list(c) for _, c in res] == g["child_cow_copies"]
+    assert [slot for slot, _ in res] == g["child_slots"]
+    assert mgr.usage == g["usage_after_child_appends"]
+    for b, rc in g["ref_count_after_appends"].items():
+        assert mgr.ref_count[int(b)] == rc
+
+
+@pytest.mark.parametrize("S", [8, 16, 32, 64])
+def test_block_manager_invariants_random(S):
+    rng = np.random.default_rng(S)
+    mgr = BlockManager(400, S)
+    seqs = {0: Sequence(mgr, 0)}
+    next_id = 1
+    for _ in range(3000):
+        op = rng.integers(0, 10)
+        sid = int(rng.choice(list(seqs)))
+        s = seqs[sid]
+        if op < 7:
+            try:
+                slot, copy = s.append_slot()
+            except MemoryError:
+                continue
+            # the slot lies in the last block of the table at offset (len-1) % S
+            assert slot == s.block_table[-1] * S + (s.length - 1) % S
+            if copy is not None:
+                assert copy[1] == s.block_table[-1] and mgr.ref_count[copy[1]] == 1
+        elif op < 9 and len(seqs) < 12:
+            used = mgr.num_blocks - len(mgr.free_ids)
+            seqs[next_id] = s.fork(next_id)
+            next_id += 1
+            assert mgr.num_blocks - len(mgr.free_ids) == used  # fork copies nothing
+        elif len(seqs) > 1:
+            s.release()
+            del seqs[sid]
+        # waste <= S - 1 per sequence; ref counts equal table references
+        for t in seqs.values():
+            assert len(t.block_table) * S - t.length <= S - 1
+            assert len(t.block_table) == (t.length + S - 1) // S
+        refs = np.zeros(mgr.num_blocks, dtype=np.int64)
+        for t in seqs.values():
+            for b in t.block_table:
+                refs[b] += 1
+        assert np.array_equal(refs, np.array(mgr.ref_count))
+        assert sorted(mgr.free_ids) == [b for b in range(mgr.num_blocks) if refs[b] == 0]
+    # a block written by one sequence is never referenced by another
+    # (the property copy-on-write exists for)
+
+
+def test_block_manager_last_writer_in_place():
+    mgr = BlockManager(32, 16)
+    p = Sequence(mgr, 0)
+    for _ in range(20):
+        p.append_slot()
+    kids = [p.fork(i) for i in range(1, 4)]
+    p.release()
+    res = [k.append_slot()[1] for k in kids]
+    assert res[0] is not None and res[1] is not None and res[2] is None
+
+
+def test_block_manager_exhaustion_raises():
+    mgr = BlockManager(2, 4)
+    s = Sequence(mgr, 0)
+    for _ in range(8):
+        s.append_slot()
+    with pytest.raises(MemoryError):
+        s.append_slot()
+
+
+# ---- store and copy -----------------------------------------------------
+
+def _u16(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def test_store_then_gather_returns_the_token():
+    c = pd_inputs.tiny_decode()
+    kc, vc = _u16(c.pool.key_cache), _u16(c.pool.value_cache)
+    S = c.pool.S
+    assert oracle.reshape_and_cache(c.new_key, c.new_value, kc, vc, c.slot_mapping, S) == 0
+    bt = c.pool.block_tables.numpy()
+    for n, i in enumerate(range(c.B)):
+        t = int(c.pool.context_lens[i]) - 1
+        slot = oracle.slot_of(bt[i], t, S)
+        assert slot == int(c.slot_mapping[n])
+        blk, off = bt[i][t // S], t % S
+        assert np.array_equal(kc[blk, :, off, :], _u16(c.new_key[n]))
+        assert np.array_equal(vc[blk, :, off, :], _u16(c.new_value[n]))
+    # everything else is untouched (bit compare, NaN payloads included)
+    mask = np.ones(kc.shape[:3], dtype=bool)
+    for n, s in enumerate(c.slot_mapping.tolist()):
+        mask[s // S, :, s % S] = False
+    assert np.array_equal(kc[mask], _u16(c.pool.key_cache)[mask])
+
+
+def test_store_skips_negative_and_counts_out_of_range():
+    kc = np.zeros((4, 2, 8, 16), dtype=np.uint16)
+    vc = kc.copy()
+    key = torch.ones(3, 2, 16, dtype=torch.float16)
+    slots = torch.tensor([-1, 4 * 8, 5], dtype=torch.int64)
+    assert oracle.reshape_and_cache(key, key, kc, vc, slots, 8) == 1
+    assert kc.sum() == 2 * 16 * 0x3C00
+    assert (kc[0, :, 5, :] == 0x3C00).all()
+
+
+def test_copy_blocks_brute_force():
+    rng = np.random.default_rng(1)
+    L, NB, Hk, S, D = 3, 10, 2, 8, 16
+    kcs = [rng.integers(0, 65535, (NB, Hk, S, D), dtype=np.uint16) for _ in range(L)]
+    vcs = [rng.integers(0, 65535, (NB, Hk, S, D), dtype=np.uint16) for _ in range(L)]
+    ref_k = [k.copy() for k in kcs]
+    ref_v = [v.copy() for v in vcs]
+    pairs = np.array([[1, 7], [2, 3], [9, 0]], dtype=np.int64)
+    assert oracle.copy_blocks(kcs, vcs, pairs) == 0
+    for l in range(L):
+        for s, d in pairs:
+            ref_k[l][d] = ref_k[l][s]
+            ref_v[l][d] = ref_v[l][s]
+        assert np.array_equal(kcs[l], ref_k[l]) and np.array_equal(vcs[l], ref_v[l])
+
+
+# ---- decode attention -----------------------------------------------------
+
+def _stored(c):
+    """A decode case with its new tokens stored, as uint16 numpy pools."""
+    kc, vc = _u16(c.pool.key_cache), _u16(c.pool.value_cache)
+    oracle.reshape_and_cache(c.new_key, c.new_value, kc, vc, c.slot_mapping, c.pool.S)
+    return kc, vc
+
+
+def _as_tensor(a, dtype):
+    return torch.from_numpy(a.view(np.int16)).view(dtype)
+
+
+def test_decode_matches_brute_force_tiny():
+    c = pd_inputs.tiny_decode()
+    kc, vc = _stored(c)
+    dt = oracle.F16
+    got = oracle.decode(c.q, kc, vc, c.pool.block_tables, c.pool.context_lens, c.scale, dt)
+    ref = bf.decode(c.q, _as_tensor(kc, c.dtype), _as_tensor(vc, c.dtype),
+                    c.pool.block_tables, c.pool.context_lens, c.scale)
+    assert np.isfinite(got).all()
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_decode_matches_brute_force_bf16_gqa_variants():
+    for (H, Hk, S) in [(4, 4, 8), (8, 1, 32), (6, 2, 64), (8, 2, 16)]:
+        c = pd_inputs.decode_case("v", 3, [5, 64, 65, 130], H, Hk, 64, S, torch.bfloat16)
+        kc, vc = _stored(c)
+        got = oracle.decode(c.q, kc, vc, c.pool.block_tables, c.pool.context_lens,
+                            c.scale, oracle.BF16)
+        ref = bf.decode(c.q, _as_tensor(kc, c.dtype), _as_tensor(vc, c.dtype),
+                        c.pool.block_tables, c.pool.context_lens, c.scale)
+        np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_ctx1_returns_v_exactly():
+    c = pd_inputs.decode_case("one", 5, [1, 1, 1], 8, 2, 64, 16, torch.float16)
+    kc, vc = _stored(c)
+    got = oracle.decode(c.q, kc, vc, c.pool.block_tables, c.pool.context_lens, c.scale,
+                        oracle.F16)
+    v = c.new_value.to(torch.float64).numpy()          # [B, Hk, D]
+    for h in range(8):
+        assert np.array_equal(got[:, h], v[:, h // 4])
+
+
+def test_equal_keys_give_mean_of_v_and_equal_values_give_that_row():
+    c = pd_inputs.decode_case("eq", 6, [40, 3], 4, 2, 64, 8, torch.float16, poison=False,
+                              store_last=False)
+    kc, vc = _u16(c.pool.key_cache), _u16(c.pool.value_cache)
+    kc[:] = kc[0, 0, 0]                       # every key identical
+    out = oracle.decode(c.q, kc, vc, c.pool.block_tables, c.pool.context_lens, c.scale,
+                        oracle.F16)
+    v64 = _as_tensor(vc, c.dtype).to(torch.float64).numpy()
+    for i in range(2):
+        n = int(c.pool.context_lens[i])
+        V = bf.gather(v64, c.pool.block_tables[i].numpy(), n)
+        for h in range(4):
+            np.testing.assert_allclose(out[i, h], V[:, h // 2].mean(0), rtol=1e-12, atol=1e-13)
+    kc2, vc2 = _u16(c.pool.key_cache), _u16(c.pool.value_cache)
+    vc2[:] = vc2[3, 1, 2]                     # every value row identical
+    out = oracle.decode(c.q, kc2, vc2, c.pool.block_tables, c.pool.context_lens, c.scale,
+                        oracle.F16)
+    row = _as_tensor(vc2[3, 1, 2], c.dtype).to(torch.float64).numpy()
+    np.testing.assert_allclose(out, np.broadcast_to(row, out.shape), rtol=1e-14, atol=1e-14)
+
+
+def test_mha_and_mqa_reductions():
+    """G = H/Hk grouping: MQA (Hk=1) equals MHA over a pool in which every kv
+    head holds the same data; MHA head h reads kv head h."""
+    c = pd_inputs.decode_case("mqa", 7, [9, 50], 4, 1, 64, 16, torch.bfloat16, poison=False,
+                              store_last=False)
+    kc, vc = _u16(c.pool.key_cache), _u16(c.pool.value_cache)
+    mqa = oracle.decode(c.q, kc, vc, c.pool.block_tables, c.pool.context_lens, c.scale,
+                        oracle.BF16)
+    kc4, vc4 = np.repeat(kc, 4, axis=1), np.repeat(vc, 4, axis=1)
+    mha = oracle.decode(c.q, kc4, vc4, c.pool.block_tables, c.pool.context_lens, c.scale,
+                        oracle.BF16)
+    assert np.array_equal(mqa, mha)
+    # MHA with distinct kv heads: head h must follow kv head h
+    kc4[:, 2] = kc4[:, 0]
+    vc4[:, 2] = vc4[:, 0] * 0 + vc4[:, 1]
+    mha2 = oracle.decode(c.q, kc4, vc4, c.pool.block_tables, c.pool.context_lens, c.scale,
+                         oracle.BF16)
+    ref = bf.decode(c.q, _as_tensor(kc4, c.dtype), _as_tensor(vc4, c.dtype),
+                    c.pool.block_tables, c.pool.context_lens, c.scale)
+    np.testing.assert_allclose(mha2, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_block_permutation_invariance():
+    c = pd_inputs.decode_case("perm", 8, [7, 100, 31], 8, 2, 64, 8, torch.float16)
+    kc, vc = _stored(c)
+    out = oracle.decode(c.q, kc, vc, c.pool.block_tables, c.pool.context_lens, c.scale,
+                        oracle.F16)
+    NB = kc.shape[0]
+    perm = np.random.default_rng(0).permutation(NB)      # new id of old block b
+    kc2, vc2 = np.empty_like(kc), np.empty_like(vc)
+    kc2[perm], vc2[perm] = kc, vc
+    bt2 = torch.from_numpy(perm[c.pool.block_tables.numpy()].astype(np.int32))
+    out2 = oracle.decode(c.q, kc2, vc2, bt2, c.pool.context_lens, c.scale, oracle.F16)
+    assert np.array_equal(out, out2)
+
+
+@pytest.mark.parametrize("part", [16, 48, 64, 512])
+def test_split_partitions_merge_to_unsplit(part):
+    c = pd_inputs.decode_case("split", 9, [1, 15, 16, 17, 200, 513], 8, 2, 64, 16,
+                              torch.bfloat16, key_outlier_frac=0.05)
+    kc, vc = _stored(c)
+    a = oracle.decode(c.q, kc, vc, c.pool.block_tables, c.pool.context_lens, c.scale, oracle.BF16)
+    b = oracle.decode(c.q, kc, vc, c.pool.block_tables, c.pool.context_lens, c.scale,
+                      oracle.BF16, split_part=part)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+def test_zero_context_gives_zeros():
+    c = pd_inputs.decode_case("z", 10, [0, 5], 4, 2, 64, 16, torch.float16)
+    kc, vc = _stored(c)
+    out = oracle.decode(c.q, kc, vc, c.pool.block_tables, c.pool.context_lens, c.scale,
+                        oracle.F16)
+    assert (out[0] == 0).all() and np.isfinite(out[1]).all()
+
+
+def test_bad_block_id_is_reported():
+    c = pd_inputs.decode_case("bad", 11, [20], 4, 2, 64, 16, torch.float16)
+    kc, vc = _stored(c)
+    bt = c.pool.block_tables.clone()
+    bt[0, 1] = kc.shape[0]
+    with pytest.raises(ValueError):
+        oracle.decode(c.q, kc, vc, bt, c.pool.context_lens, c.scale, oracle.F16)
+
+
+# ---- chunked prefill ------------------------------------------------------
+
+def _mixed_small(seed=12, S=16, dtype=torch.bfloat16):
+    return pd_inputs.mixed_case(seed, [0, 5, 40], [1, 19, 33], [3, 70], 8, 2, 64, S, dtype)
+
+
+def _stored_mixed(m):
+    kc, vc = _u16(m.pool.key_cache), _u16(m.pool.value_cache)
+    oracle.reshape_and_cache(m.new_key, m.new_value, kc, vc, m.slot_mapping, m.pool.S)
+    return kc, vc
+
+
+def test_prefill_matches_brute_force():
+    m = _mixed_small()
+    kc, vc = _stored_mixed(m)
+    bt = m.pool.block_tables[: m.Bp]
+    cl = m.pool.context_lens[: m.Bp]
+    got = oracle.prefill(m.q_prefill, m.cu_q_lens, kc, vc, bt, cl, m.scale, oracle.BF16)
+    ref = bf.prefill(m.q_prefill, m.cu_q_lens, _as_tensor(kc, m.dtype), _as_tensor(vc, m.dtype),
+                     bt, cl, m.scale)
+    assert np.isfinite(got).all()
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    # sampled rows agree with the full evaluation
+    rows = np.array([0, 5, 17, 8 * 20 + 3, got.shape[0] * 8 - 1])
+    part = oracle.prefill(m.q_prefill, m.cu_q_lens, kc, vc, bt, cl, m.scale, oracle.BF16,
+                          rows=rows)
+    assert np.array_equal(part, got.reshape(-1, 64)[rows])
+
+
+def test_prefill_special_cases_reduce_to_decode():
+    m = _mixed_small()
+    kc, vc = _stored_mixed(m)
+    bt = m.pool.block_tables[: m.Bp]
+    cl = m.pool.context_lens[: m.Bp]
+    pre = oracle.prefill(m.q_prefill, m.cu_q_lens, kc, vc, bt, cl, m.scale, oracle.BF16)
+    cu = m.cu_q_lens.tolist()
+    for i in range(m.Bp):
+        # the chunk's last query row is a decode step at ctx = P + C
+        q_last = m.q_prefill[cu[i + 1] - 1].unsqueeze(0)
+        dec = oracle.decode(q_last, kc, vc, bt[i:i + 1], cl[i:i + 1], m.scale, oracle.BF16)
+        assert np.array_equal(pre[cu[i + 1] - 1], dec[0])
+    # sequence 0 has P = 0, C = 1: attention to its single key returns V exactly
+    v = m.new_value[0].to(torch.float64).numpy()
+    for h in range(8):
+        assert np.array_equal(pre[0, h], v[h // 4])
+
+
+def test_prefill_causality():
+    """Changing the keys/values at positions after query j leaves row j as is."""
+    m = _mixed_small(seed=13)
+    kc, vc = _stored_mixed(m)
+    bt = m.pool.block_tables[: m.Bp]
+    cl = m.pool.context_lens[: m.Bp]
+    a = oracle.prefill(m.q_prefill, m.cu_q_lens, kc, vc, bt, cl, m.scale, oracle.BF16)
+    i, S = 2, m.pool.S
+    P = int(cl[i]) - 33
+    j = 10
+    for t in range(P + j + 1, int(cl[i])):
+        blk, off = int(bt[i, t // S]), t % S
+        kc[blk, :, off] ^= 0x0100
+        vc[blk, :, off] ^= 0x0100
+    b = oracle.prefill(m.q_prefill, m.cu_q_lens, kc, vc, bt, cl, m.scale, oracle.BF16)
+    row = int(m.cu_q_lens[i]) + j
+    assert np.array_equal(a[: row + 1], b[: row + 1])
+    assert not np.array_equal(a[row + 1:int(m.cu_q_lens[i + 1])], b[row + 1:int(m.cu_q_lens[i + 1])])
+
+
+def test_prefill_scale_enters_once():
+    """softmax(scale * s): with scale -> 0 the output is the mean of V."""
+    m = _mixed_small(seed=14)
+    kc, vc = _stored_mixed(m)
+    bt = m.pool.block_tables[: m.Bp]
+    cl = m.pool.context_lens[: m.Bp]
+    out = oracle.prefill(m.q_prefill, m.cu_q_lens, kc, vc, bt, cl, 0.0, oracle.BF16)
+    v64 = _as_tensor(vc, m.dtype).to(torch.float64).numpy()
+    i = 2
+    P = int(cl[i]) - 33
+    V = bf.gather(v64, bt[i].numpy(), int(cl[i]))
+    for j in (0, 32):
+        np.testing.assert_allclose(out[int(m.cu_q_lens[i]) + j, 5], V[: P + j + 1, 1].mean(0),
+                                   rtol=1e-12, atol=1e-13)
+    assert math.isclose(m.scale, 1 / 8)
