@@ -1,0 +1,222 @@
+/*
+ * pd_attn.h -- C ABI of the paged KV-cache attention library (GB300, sm_103a).
+ *
+ * The operations are those of a prefill/decode-disaggregated serving engine
+ * whose KV cache is paged (nanoPD page "nanoPD：从零实现的LLM预填充/解码分离推
+ * 理引擎", sections "分页KV缓存", "分块预填充", "自定义CUDA分页注意力内核" and
+ * "模块结构与代码组织": paged KV store op and paged multi-head attention
+ * kernel), with the paging scheme of the tutorial page "LLM 推理服务引擎深度拆
+ * 解", section 2.2: fixed-size blocks of S tokens, a per-sequence block table
+ * mapping logical block i to a physical block, and one indirection per KV read.
+ *
+ * Conventions shared by every device entry point
+ * - Cache layout, one pool per layer and per K/V: [NB][Hk][S][D] elements,
+ *   contiguous (block-major, then kv head, then token offset, then dim).
+ *   Logical token t of sequence i lives in physical block
+ *   block_tables[i * max_blocks_per_seq + t / S] at offset t % S; its slot
+ *   number is block * S + t % S.
+ * - All tensor pointers are CALLER-OWNED DEVICE memory, 16-byte aligned;
+ *   the library allocates nothing on the device and never synchronises: work
+ *   is enqueued on `stream` (NULL = legacy default stream) and returns.
+ * - Element types: K, V, Q and outputs share one `pd_dtype` (fp16 or bf16).
+ *   Attention accumulates in fp32 and rounds its output to the element type
+ *   with round-to-nearest-even.
+ * - Supported shapes: D in {64, 128}; S in {8, 16, 32, 64}; H % Hk == 0.
+ *   Other values return PD_ERR_UNSUPPORTED; bad pointers, negative sizes or
+ *   inconsistent arguments return PD_ERR_INVALID_ARG.  Nothing is launched
+ *   when a call returns an error.
+ * - Device-side faults are never trapped.  Kernels check every slot, block
+ *   id and context length they read against the sizes given; an offender is
+ *   skipped and a bit is OR-ed into *dev_err (caller-owned device int32,
+ *   may be NULL to ignore).  Results touched by a flagged input are
+ *   unspecified.  Every wait inside a kernel is bounded in time; a wait that
+ *   runs out sets PD_DEVERR_TIMEOUT and the kernel returns.
+ * - PD_ERR_CUDA means a launch failed; pd_last_cuda_error() returns the
+ *   cudaError_t value of the last failure in this thread.
+ */
+#ifndef PD_ATTN_H
+#define PD_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+/* Exported symbols keep default visibility when the library is built with
+ * -fvisibility=hidden. */
+#if defined(__GNUC__)
+#define PD_API __attribute__((visibility("default")))
+#else
+#define PD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pd_status {
+    PD_OK = 0,
+    PD_ERR_INVALID_ARG = 1,
+    PD_ERR_UNSUPPORTED = 2,
+    PD_ERR_CUDA = 3,
+    PD_ERR_NO_FREE_BLOCK = 4,
+    PD_ERR_WORKSPACE_TOO_SMALL = 5,
+    PD_ERR_NOT_FOUND = 6
+} pd_status;
+
+typedef enum pd_dtype { PD_F16 = 0, PD_BF16 = 1 } pd_dtype;
+
+/* Bits OR-ed into the caller's device error word. */
+#define PD_DEVERR_SLOT_RANGE 0x1  /* slot >= NB * S in a store               */
+#define PD_DEVERR_BLOCK_RANGE 0x2 /* block id outside [0, NB)                */
+#define PD_DEVERR_CTX_RANGE 0x4   /* context longer than table / promise     */
+#define PD_DEVERR_TIMEOUT 0x8     /* a bounded wait inside a kernel expired  */
+
+/* Text for a status code (static storage). */
+PD_API const char* pd_status_string(pd_status s);
+/* cudaError_t of the last PD_ERR_CUDA returned to this thread (0 if none). */
+PD_API int pd_last_cuda_error(void);
+/* Number of kernels this library has launched in this process (a counter
+ * for accounting; every successful launch increments it by one). */
+PD_API uint64_t pd_launch_count(void);
+
+/* ---------------------------------------------------------------------- */
+/* Store new tokens' K/V into their cache slots (nanoPD page, "模块结构与代码
+ * 组织": the paged KV store op; slots come from the block manager, tutorial
+ * page section 2.3, Sequence.append_token).
+ *   key, value    [T][Hk][D] (token stride key_stride_tok / value_stride_tok
+ *                 elements, heads contiguous at stride D)
+ *   key_cache, value_cache   [NB][Hk][S][D], written in place
+ *   slot_mapping  int64 [T]; slot < 0 skips the token (padding);
+ *                 slot >= NB*S is skipped and flags PD_DEVERR_SLOT_RANGE.
+ * A bit copy: no conversion.  Two tokens mapped to one slot race. */
+PD_API pd_status pd_reshape_and_cache(const void* key, const void* value,
+                               void* key_cache, void* value_cache,
+                               const int64_t* slot_mapping, int T, int Hk,
+                               int D, int S, int NB, int64_t key_stride_tok,
+                               int64_t value_stride_tok, pd_dtype dt,
+                               int32_t* dev_err, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Decode attention: one query token per sequence over its paged context
+ * (nanoPD page, "自定义CUDA分页注意力内核": gather attention over
+ * non-contiguous KV blocks; GQA as in the essay page "LLM推理PD分离架构深度
+ * 工程实践", section 6.2: q head h reads kv head h / (H / Hk)).
+ *   out[i][h][:] = sum_{t < ctx_i} softmax_t(scale * q[i][h] . k_t) v_t
+ * with ctx_i = context_lens[i] (it counts any token stored this step) and
+ * ctx_i == 0 giving zeros.
+ *   out, q        [B][H][D]
+ *   block_tables  int32 [B][max_blocks_per_seq]
+ *   context_lens  int32 [B], each <= max_context_len (the caller's promise,
+ *                 checked on device: PD_DEVERR_CTX_RANGE, the context is
+ *                 then cut to what the table and workspace hold)
+ * Long contexts are split into partitions of a fixed number of tokens that
+ * are processed in parallel (online softmax per partition, results kept in
+ * `workspace`), then merged by a second kernel; a batch whose
+ * max_context_len fits one partition is written directly.
+ *   workspace     device scratch of at least
+ *                 pd_decode_workspace_bytes(B, H, D, max_context_len) bytes
+ *                 (may be NULL when that size is 0); 256-byte aligned.
+ *                 Overwritten; callers sharing one workspace on two streams
+ *                 race.  PD_ERR_WORKSPACE_TOO_SMALL if it is short. */
+PD_API size_t pd_decode_workspace_bytes(int B, int H, int D, int max_context_len);
+/* Tokens per partition used for a given max_context_len (exposed for
+ * accounting and tests). */
+PD_API int pd_decode_partition_tokens(int max_context_len);
+PD_API pd_status pd_paged_attention_decode(void* out, const void* q,
+                                    const void* key_cache,
+                                    const void* value_cache,
+                                    const int32_t* block_tables,
+                                    int max_blocks_per_seq,
+                                    const int32_t* context_lens, int B, int H,
+                                    int Hk, int D, int S, int NB,
+                                    int max_context_len, float scale,
+                                    void* workspace, size_t workspace_bytes,
+                                    pd_dtype dt, int32_t* dev_err,
+                                    cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Copy-on-write block copies for fork (parallel sampling, beam search):
+ * tutorial page section 2.3, BlockManager.cow(): a shared block that is about
+ * to be written is duplicated into a fresh block first; nanoPD page "分页KV
+ * 缓存": CoW for beam-search and speculative branches.
+ *   key_caches, value_caches  DEVICE arrays of L device pointers, one pool
+ *                             [NB][Hk][S][D] per layer
+ *   block_mapping  DEVICE int64 [npairs][2] = (src, dst); for every pair and
+ *                  every layer the whole block (all heads, all S offsets) of
+ *                  K and of V is copied.  Ids outside [0, NB) skip the pair
+ *                  and flag PD_DEVERR_BLOCK_RANGE.  A dst that is also a src
+ *                  of another pair, or two pairs with one dst, race.
+ * A bit copy.  npairs == 0 or L == 0 launches nothing. */
+PD_API pd_status pd_copy_blocks(void* const* key_caches, void* const* value_caches,
+                         int L, const int64_t* block_mapping, int npairs,
+                         int Hk, int D, int S, int NB, pd_dtype dt,
+                         int32_t* dev_err, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Chunked-prefill attention (nanoPD page "分块预填充": long prompts are cut
+ * into chunks interleaved with decode; tutorial page section 5.2): sequence
+ * i appends a chunk of C_i query tokens after P_i cached tokens; its chunk
+ * K/V are stored beforehand (pd_reshape_and_cache), so the context holds
+ * ctx_i = P_i + C_i tokens.  Query j of the chunk (position P_i + j) attends
+ * causally to keys 0 .. P_i + j:
+ *   out[tok][h][:] = sum_{t <= P_i + j} softmax_t(scale * q[tok][h] . k_t) v_t
+ *   q, out        packed [sum_i C_i][H][D]; sequence i's tokens are rows
+ *                 cu_q_lens[i] .. cu_q_lens[i+1]-1
+ *   cu_q_lens     int32 [B + 1], cu_q_lens[0] = 0, non-decreasing
+ *   max_q_len     >= every C_i (sizes the launch grid)
+ *   context_lens  int32 [B] = P_i + C_i (>= C_i; checked on device)
+ * QK^T and PV run on the tensor cores (tcgen05, fp32 accumulation in tensor
+ * memory); probabilities are rounded to the element type before PV. */
+PD_API pd_status pd_paged_prefill_chunk(void* out, const void* q,
+                                 const int32_t* cu_q_lens, int max_q_len,
+                                 const void* key_cache, const void* value_cache,
+                                 const int32_t* block_tables,
+                                 int max_blocks_per_seq,
+                                 const int32_t* context_lens, int B, int H,
+                                 int Hk, int D, int S, int NB, float scale,
+                                 pd_dtype dt, int32_t* dev_err,
+                                 cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Host-side block manager (tutorial page section 2.3, BlockManager and
+ * Sequence): ref-counted physical blocks, copy-on-write and fork.  Pure host
+ * code, no CUDA calls; not thread-safe (one manager per thread).
+ * Allocation order is part of the contract: the free list starts as
+ * 0 .. num_blocks-1, allocation takes its last id, freeing appends. */
+typedef struct pd_bm pd_bm;
+
+/* NULL on bad sizes (num_blocks < 1, block_size < 1) or out of memory. */
+PD_API pd_bm* pd_bm_create(int num_blocks, int block_size);
+PD_API void pd_bm_destroy(pd_bm* bm);
+/* New empty sequence.  PD_ERR_INVALID_ARG if seq_id is in use or < 0. */
+PD_API pd_status pd_bm_add_seq(pd_bm* bm, int seq_id);
+/* Reserve the slot of the sequence's next token: a new block at a block
+ * boundary, else copy-on-write of a shared last block.  *slot_out gets
+ * block*S + offset; *cow_src_out / *cow_dst_out get the block copy the
+ * caller must apply on the device (pd_copy_blocks) before storing, or -1.
+ * PD_ERR_NO_FREE_BLOCK leaves the sequence unchanged. */
+PD_API pd_status pd_bm_append_slot(pd_bm* bm, int seq_id, int64_t* slot_out,
+                            int32_t* cow_src_out, int32_t* cow_dst_out);
+/* Child shares every block of the parent (ref count + 1), copying nothing. */
+PD_API pd_status pd_bm_fork(pd_bm* bm, int parent_id, int child_id);
+/* Drop the sequence, one reference from each of its blocks. */
+PD_API pd_status pd_bm_release(pd_bm* bm, int seq_id);
+/* Copy the sequence's block table into out[0 .. cap); *n_out = its length
+ * (PD_ERR_INVALID_ARG if cap is too small; *n_out still set). */
+PD_API pd_status pd_bm_block_table(const pd_bm* bm, int seq_id, int32_t* out,
+                            int cap, int* n_out);
+/* Number of tokens of a sequence (-1 if unknown). */
+PD_API int64_t pd_bm_seq_len(const pd_bm* bm, int seq_id);
+/* Blocks in use / pool size. */
+PD_API double pd_bm_usage(const pd_bm* bm);
+/* Ref count of a block (-1 if out of range). */
+PD_API int pd_bm_ref_count(const pd_bm* bm, int block_id);
+/* Free blocks left. */
+PD_API int pd_bm_num_free(const pd_bm* bm);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PD_ATTN_H */

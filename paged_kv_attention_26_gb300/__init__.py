@@ -1,0 +1,335 @@
+"""Paged KV-cache attention for GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over the C ABI of ``include/pd_attn.h``: it checks tensor
+dtypes, devices and contiguity, marshals ``data_ptr()`` values and the current
+CUDA stream, and raises on a non-OK status.  Every step of the computation
+runs in the library's CUDA kernels; there is no other code path.  The library
+must have been built (``paged_kv_attention_26_gb300.build.build()``); loading
+fails loudly otherwise.
+
+Functions carry the C names: ``pd_reshape_and_cache``,
+``pd_paged_attention_decode`` (+ ``pd_decode_workspace_bytes``),
+``pd_copy_blocks``, ``pd_paged_prefill_chunk``; ``BlockManager`` wraps the
+host-side ``pd_bm_*`` calls.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+LIB_PATH = _build.LIB
+
+PD_OK = 0
+PD_F16, PD_BF16 = 0, 1
+PD_DEVERR_SLOT_RANGE = 0x1
+PD_DEVERR_BLOCK_RANGE = 0x2
+PD_DEVERR_CTX_RANGE = 0x4
+PD_DEVERR_TIMEOUT = 0x8
+
+STATUS_NAMES = {0: "PD_OK", 1: "PD_ERR_INVALID_ARG", 2: "PD_ERR_UNSUPPORTED", 3: "PD_ERR_CUDA",
+                4: "PD_ERR_NO_FREE_BLOCK", 5: "PD_ERR_WORKSPACE_TOO_SMALL",
+                6: "PD_ERR_NOT_FOUND"}
+
+# Every symbol include/pd_attn.h exports: name -> (restype, argtypes)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+SIGNATURES = {
+    "pd_status_string": (ctypes.c_char_p, [_I]),
+    "pd_last_cuda_error": (_I, []),
+    "pd_launch_count": (ctypes.c_uint64, []),
+    "pd_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I64, _I64, _I, _P, _P]),
+    "pd_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "pd_decode_partition_tokens": (_I, [_I]),
+    "pd_paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I,
+                                       _F, _P, _SZ, _I, _P, _P]),
+    "pd_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "pd_paged_prefill_chunk": (_I, [_P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I,
+                                    _F, _I, _P, _P]),
+    "pd_bm_create": (_P, [_I, _I]),
+    "pd_bm_destroy": (None, [_P]),
+    "pd_bm_add_seq": (_I, [_P, _I]),
+    "pd_bm_append_slot": (_I, [_P, _I, ctypes.POINTER(ctypes.c_int64),
+                               ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]),
+    "pd_bm_fork": (_I, [_P, _I, _I]),
+    "pd_bm_release": (_I, [_P, _I]),
+    "pd_bm_block_table": (_I, [_P, _I, ctypes.POINTER(ctypes.c_int32), _I,
+                               ctypes.POINTER(ctypes.c_int)]),
+    "pd_bm_seq_len": (_I64, [_P, _I]),
+    "pd_bm_usage": (ctypes.c_double, [_P]),
+    "pd_bm_ref_count": (_I, [_P, _I]),
+    "pd_bm_num_free": (_I, [_P]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PDError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        name = STATUS_NAMES.get(status, str(status))
+        extra = ""
+        if status == 3 and _lib is not None:
+            extra = f" (cudaError {_lib.pd_last_cuda_error()})"
+        super().__init__(f"{fn}: {name}{extra}")
+
+
+def load():
+    """Load the built library (raises FileNotFoundError if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise FileNotFoundError(
+                f"{LIB_PATH} is missing: build it with paged_kv_attention_26_gb300.build.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int):
+    if status != PD_OK:
+        raise PDError(fn, status)
+
+
+def launch_count() -> int:
+    return int(load().pd_launch_count())
+
+
+# ---- tensor helpers ---------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dt(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float16:
+        return PD_F16
+    if t.dtype == torch.bfloat16:
+        return PD_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _dev(t, name, dtype=None, contiguous=True):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _opt(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+# ---- ops -------------------------------------------------------------------------------
+
+def pd_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, dev_err=None,
+                         stream=None):
+    """Store key/value [T, Hk, D] (token-strided, heads contiguous) into the
+    paged caches [NB, Hk, S, D] at ``slot_mapping`` (int64 [T])."""
+    torch = _torch()
+    T, Hk, D = key.shape
+    NB, Hk2, S, D2 = key_cache.shape
+    if (Hk2, D2) != (Hk, D) or value.shape != key.shape or value_cache.shape != key_cache.shape:
+        raise ValueError("shape mismatch")
+    for t, n in ((key, "key"), (value, "value")):
+        if t.stride(2) != 1 or t.stride(1) != D:
+            raise ValueError(f"{n} must have contiguous heads and dims")
+    dt = _dt(key_cache)
+    if key.dtype != key_cache.dtype or value.dtype != key_cache.dtype:
+        raise TypeError("dtype mismatch")
+    st = load().pd_reshape_and_cache(
+        _dev(key, "key", contiguous=False), _dev(value, "value", contiguous=False),
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+        _dev(slot_mapping, "slot_mapping", torch.int64), T, Hk, D, S, NB,
+        key.stride(0), value.stride(0), dt, _opt(dev_err), _stream(stream))
+    _check("pd_reshape_and_cache", st)
+
+
+def pd_decode_workspace_bytes(B: int, H: int, D: int, max_context_len: int) -> int:
+    return int(load().pd_decode_workspace_bytes(B, H, D, max_context_len))
+
+
+def pd_decode_partition_tokens(max_context_len: int) -> int:
+    return int(load().pd_decode_partition_tokens(max_context_len))
+
+
+def decode_workspace(B, H, D, max_context_len, device="cuda"):
+    """Allocate a workspace of the required size (uint8, 256-byte aligned)."""
+    torch = _torch()
+    n = pd_decode_workspace_bytes(B, H, D, max_context_len)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def pd_paged_attention_decode(out, q, key_cache, value_cache, block_tables, context_lens,
+                              max_context_len: int, scale: float, workspace=None,
+                              dev_err=None, stream=None):
+    """out, q [B, H, D]; caches [NB, Hk, S, D]; block_tables int32 [B, max_blocks];
+    context_lens int32 [B].  ``workspace`` (uint8 CUDA tensor) must hold
+    ``pd_decode_workspace_bytes`` bytes when that is non-zero."""
+    torch = _torch()
+    B, H, D = q.shape
+    NB, Hk, S, D2 = key_cache.shape
+    if out.shape != q.shape or D2 != D or value_cache.shape != key_cache.shape:
+        raise ValueError("shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables / context_lens shape")
+    dt = _dt(key_cache)
+    for t in (q, out, value_cache):
+        if t.dtype != key_cache.dtype:
+            raise TypeError("dtype mismatch")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    st = load().pd_paged_attention_decode(
+        _dev(out, "out"), _dev(q, "q"), _dev(key_cache, "key_cache"),
+        _dev(value_cache, "value_cache"), _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), B, H, Hk, D, S,
+        NB, int(max_context_len), float(scale), ws_ptr, ws_bytes, dt, _opt(dev_err),
+        _stream(stream))
+    _check("pd_paged_attention_decode", st)
+
+
+_ptr_arrays: dict = {}
+
+
+def pointer_array(tensors, device=None):
+    """Device int64 array of the tensors' data pointers (cached per pointer tuple)."""
+    torch = _torch()
+    key = tuple(t.data_ptr() for t in tensors)
+    arr = _ptr_arrays.get(key)
+    if arr is None:
+        dev = device or tensors[0].device
+        arr = torch.tensor(key, dtype=torch.int64).to(dev)
+        _ptr_arrays[key] = arr
+    return arr
+
+
+def pd_copy_blocks(key_caches, value_caches, block_mapping, dev_err=None, stream=None):
+    """Copy whole blocks src -> dst for every (src, dst) row of ``block_mapping``
+    (int64 CUDA [npairs, 2]) in every layer's K and V pool (lists of [NB, Hk, S, D])."""
+    torch = _torch()
+    L = len(key_caches)
+    if L == 0 or L != len(value_caches):
+        raise ValueError("need the same number (> 0) of key and value pools")
+    NB, Hk, S, D = key_caches[0].shape
+    for t in list(key_caches) + list(value_caches):
+        if t.shape != key_caches[0].shape or t.dtype != key_caches[0].dtype:
+            raise ValueError("all pools must share shape and dtype")
+        _dev(t, "cache")
+    if block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
+        raise ValueError("block_mapping must be [npairs, 2]")
+    kp = pointer_array(key_caches)
+    vp = pointer_array(value_caches)
+    st = load().pd_copy_blocks(kp.data_ptr(), vp.data_ptr(), L,
+                               _dev(block_mapping, "block_mapping", torch.int64),
+                               block_mapping.shape[0], Hk, D, S, NB, _dt(key_caches[0]),
+                               _opt(dev_err), _stream(stream))
+    _check("pd_copy_blocks", st)
+
+
+def pd_paged_prefill_chunk(out, q, cu_q_lens, max_q_len: int, key_cache, value_cache,
+                           block_tables, context_lens, scale: float, dev_err=None, stream=None):
+    """out, q packed [sumC, H, D]; cu_q_lens int32 [B+1]; context_lens int32 [B]
+    (= prior + chunk length); caches [NB, Hk, S, D]; block_tables int32 [B, max_blocks]."""
+    torch = _torch()
+    NT, H, D = q.shape
+    NB, Hk, S, D2 = key_cache.shape
+    B = cu_q_lens.shape[0] - 1
+    if out.shape != q.shape or D2 != D or value_cache.shape != key_cache.shape:
+        raise ValueError("shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables / context_lens shape")
+    for t in (q, out, value_cache):
+        if t.dtype != key_cache.dtype:
+            raise TypeError("dtype mismatch")
+    st = load().pd_paged_prefill_chunk(
+        _dev(out, "out"), _dev(q, "q"), _dev(cu_q_lens, "cu_q_lens", torch.int32),
+        int(max_q_len), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), B, H, Hk, D, S, NB, float(scale),
+        _dt(key_cache), _opt(dev_err), _stream(stream))
+    _check("pd_paged_prefill_chunk", st)
+
+
+class BlockManager:
+    """Host block manager (pd_bm_*): ref-counted blocks, copy-on-write, fork."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self._lib = load()
+        self._h = self._lib.pd_bm_create(num_blocks, block_size)
+        if not self._h:
+            raise ValueError("pd_bm_create failed")
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            self._lib.pd_bm_destroy(h)
+            self._h = None
+
+    def add_seq(self, seq_id: int):
+        _check("pd_bm_add_seq", self._lib.pd_bm_add_seq(self._h, seq_id))
+
+    def append_slot(self, seq_id: int):
+        """Returns (slot, (src, dst) copy or None)."""
+        slot = ctypes.c_int64()
+        src = ctypes.c_int32()
+        dst = ctypes.c_int32()
+        _check("pd_bm_append_slot", self._lib.pd_bm_append_slot(
+            self._h, seq_id, ctypes.byref(slot), ctypes.byref(src), ctypes.byref(dst)))
+        return slot.value, (None if src.value < 0 else (src.value, dst.value))
+
+    def fork(self, parent_id: int, child_id: int):
+        _check("pd_bm_fork", self._lib.pd_bm_fork(self._h, parent_id, child_id))
+
+    def release(self, seq_id: int):
+        _check("pd_bm_release", self._lib.pd_bm_release(self._h, seq_id))
+
+    def block_table(self, seq_id: int) -> list:
+        n = ctypes.c_int()
+        st = self._lib.pd_bm_block_table(self._h, seq_id, None, 0, ctypes.byref(n))
+        if st not in (PD_OK, 1):
+            _check("pd_bm_block_table", st)
+        buf = (ctypes.c_int32 * max(1, n.value))()
+        _check("pd_bm_block_table", self._lib.pd_bm_block_table(self._h, seq_id, buf, n.value,
+                                                                ctypes.byref(n)))
+        return list(buf[: n.value])
+
+    def seq_len(self, seq_id: int) -> int:
+        return int(self._lib.pd_bm_seq_len(self._h, seq_id))
+
+    @property
+    def usage(self) -> float:
+        return float(self._lib.pd_bm_usage(self._h))
+
+    def ref_count(self, block_id: int) -> int:
+        return int(self._lib.pd_bm_ref_count(self._h, block_id))
+
+    @property
+    def num_free(self) -> int:
+        return int(self._lib.pd_bm_num_free(self._h))

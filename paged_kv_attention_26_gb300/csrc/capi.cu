@@ -1,0 +1,142 @@
+// capi.cu -- the extern "C" entry points of pd_attn.h: argument validation,
+// status codes and launch accounting around the per-op launchers.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "pd_attn.h"
+#include "pd_internal.h"
+
+namespace pd {
+namespace {
+thread_local int g_last_cuda_error = 0;
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+
+pd_status launch_result(cudaError_t e) {
+    if (e == cudaSuccess) {
+        count_launch();
+        return PD_OK;
+    }
+    g_last_cuda_error = int(e);
+    return PD_ERR_CUDA;
+}
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+}  // namespace pd
+
+using namespace pd;
+
+extern "C" {
+
+const char* pd_status_string(pd_status s) {
+    switch (s) {
+        case PD_OK: return "ok";
+        case PD_ERR_INVALID_ARG: return "invalid argument";
+        case PD_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case PD_ERR_CUDA: return "CUDA launch error (see pd_last_cuda_error)";
+        case PD_ERR_NO_FREE_BLOCK: return "no free block in the pool";
+        case PD_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case PD_ERR_NOT_FOUND: return "unknown sequence id";
+    }
+    return "unknown status";
+}
+
+int pd_last_cuda_error(void) { return g_last_cuda_error; }
+
+uint64_t pd_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+pd_status pd_reshape_and_cache(const void* key, const void* value, void* key_cache,
+                               void* value_cache, const int64_t* slot_mapping, int T, int Hk,
+                               int D, int S, int NB, int64_t key_stride_tok,
+                               int64_t value_stride_tok, pd_dtype dt, int32_t* dev_err,
+                               cudaStream_t stream) {
+    if (T < 0 || Hk < 1 || NB < 1) return PD_ERR_INVALID_ARG;
+    if (!supported_D(D) || !supported_S(S) || !supported_dt(dt)) return PD_ERR_UNSUPPORTED;
+    if (!key_cache || !value_cache || !aligned16(key_cache) || !aligned16(value_cache))
+        return PD_ERR_INVALID_ARG;
+    if (T == 0) return PD_OK;
+    if (!key || !value || !slot_mapping || !aligned16(key) || !aligned16(value))
+        return PD_ERR_INVALID_ARG;
+    if (key_stride_tok < int64_t(Hk) * D || value_stride_tok < int64_t(Hk) * D ||
+        key_stride_tok % 8 || value_stride_tok % 8)
+        return PD_ERR_INVALID_ARG;
+    return launch_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, T, Hk, D,
+                                    S, NB, key_stride_tok, value_stride_tok, dev_err, stream);
+}
+
+size_t pd_decode_workspace_bytes(int B, int H, int D, int max_context_len) {
+    if (B < 1 || H < 1 || !supported_D(D) || max_context_len < 0) return 0;
+    return decode_workspace_bytes(B, H, D, max_context_len);
+}
+
+int pd_decode_partition_tokens(int max_context_len) {
+    return decode_partition_tokens(max_context_len);
+}
+
+pd_status pd_paged_attention_decode(void* out, const void* q, const void* key_cache,
+                                    const void* value_cache, const int32_t* block_tables,
+                                    int max_blocks_per_seq, const int32_t* context_lens, int B,
+                                    int H, int Hk, int D, int S, int NB, int max_context_len,
+                                    float scale, void* workspace, size_t workspace_bytes,
+                                    pd_dtype dt, int32_t* dev_err, cudaStream_t stream) {
+    if (B < 0 || H < 1 || Hk < 1 || NB < 1 || max_blocks_per_seq < 1 || max_context_len < 0)
+        return PD_ERR_INVALID_ARG;
+    if (H % Hk != 0) return PD_ERR_INVALID_ARG;
+    if (!supported_D(D) || !supported_S(S) || !supported_dt(dt)) return PD_ERR_UNSUPPORTED;
+    if (B == 0) return PD_OK;
+    if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens)
+        return PD_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
+        return PD_ERR_INVALID_ARG;
+    if (B > 65535 || int64_t(max_blocks_per_seq) * S > (int64_t(1) << 30))
+        return PD_ERR_UNSUPPORTED;
+    const size_t need = decode_workspace_bytes(B, H, D, max_context_len);
+    if (need > 0) {
+        if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+            return PD_ERR_INVALID_ARG;
+        if (workspace_bytes < need) return PD_ERR_WORKSPACE_TOO_SMALL;
+    }
+    DecodeArgs a{out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
+                 B, H, Hk, D, S, NB, max_context_len, scale, workspace, dt, dev_err, stream};
+    return launch_decode(a);
+}
+
+pd_status pd_copy_blocks(void* const* key_caches, void* const* value_caches, int L,
+                         const int64_t* block_mapping, int npairs, int Hk, int D, int S, int NB,
+                         pd_dtype dt, int32_t* dev_err, cudaStream_t stream) {
+    if (L < 0 || npairs < 0 || Hk < 1 || NB < 1) return PD_ERR_INVALID_ARG;
+    if (!supported_D(D) || !supported_S(S) || !supported_dt(dt)) return PD_ERR_UNSUPPORTED;
+    if (L == 0 || npairs == 0) return PD_OK;
+    if (!key_caches || !value_caches || !block_mapping) return PD_ERR_INVALID_ARG;
+    if (L > 65535) return PD_ERR_UNSUPPORTED;
+    return launch_copy_blocks(key_caches, value_caches, L, block_mapping, npairs, Hk, D, S, NB,
+                              dev_err, stream);
+}
+
+pd_status pd_paged_prefill_chunk(void* out, const void* q, const int32_t* cu_q_lens,
+                                 int max_q_len, const void* key_cache, const void* value_cache,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* context_lens, int B, int H, int Hk, int D, int S,
+                                 int NB, float scale, pd_dtype dt, int32_t* dev_err,
+                                 cudaStream_t stream) {
+    if (B < 0 || H < 1 || Hk < 1 || NB < 1 || max_blocks_per_seq < 1 || max_q_len < 0)
+        return PD_ERR_INVALID_ARG;
+    if (H % Hk != 0) return PD_ERR_INVALID_ARG;
+    if (!supported_D(D) || !supported_S(S) || !supported_dt(dt)) return PD_ERR_UNSUPPORTED;
+    if (B == 0 || max_q_len == 0) return PD_OK;
+    if (!out || !q || !cu_q_lens || !key_cache || !value_cache || !block_tables || !context_lens)
+        return PD_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
+        return PD_ERR_INVALID_ARG;
+    if (B > 65535 || int64_t(max_blocks_per_seq) * S > (int64_t(1) << 30))
+        return PD_ERR_UNSUPPORTED;
+    PrefillArgs a{out, q, cu_q_lens, max_q_len, key_cache, value_cache, block_tables,
+                  max_blocks_per_seq, context_lens, B, H, Hk, D, S, NB, scale, dt, dev_err,
+                  stream};
+    return launch_prefill(a);
+}
+
+}  // extern "C"

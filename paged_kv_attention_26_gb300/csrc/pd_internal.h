@@ -1,0 +1,76 @@
+// pd_internal.h -- host-side declarations shared by the library's translation
+// units (validation helpers, launch accounting, per-op launchers).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "pd_attn.h"
+
+namespace pd {
+
+// Record a kernel launch result; returns PD_OK or PD_ERR_CUDA (and keeps
+// the cudaError_t for pd_last_cuda_error()).
+pd_status launch_result(cudaError_t e);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool supported_D(int D) { return D == 64 || D == 128; }
+inline bool supported_S(int S) { return S == 8 || S == 16 || S == 32 || S == 64; }
+inline bool supported_dt(pd_dtype dt) { return dt == PD_F16 || dt == PD_BF16; }
+
+// ---- decode ------------------------------------------------------------------
+// Partition length chosen for a batch; a multiple of 64 tokens.
+int decode_partition_tokens(int max_context_len);
+int decode_num_partitions(int max_context_len);
+size_t decode_workspace_bytes(int B, int H, int D, int max_context_len);
+
+struct DecodeArgs {
+    void* out;
+    const void* q;
+    const void* key_cache;
+    const void* value_cache;
+    const int32_t* block_tables;
+    int max_blocks_per_seq;
+    const int32_t* context_lens;
+    int B, H, Hk, D, S, NB;
+    int max_context_len;
+    float scale;
+    void* workspace;
+    pd_dtype dt;
+    int32_t* dev_err;
+    cudaStream_t stream;
+};
+pd_status launch_decode(const DecodeArgs& a);
+
+// ---- store / copy ----------------------------------------------------------------
+pd_status launch_reshape_and_cache(const void* key, const void* value, void* key_cache,
+                                   void* value_cache, const int64_t* slot_mapping, int T,
+                                   int Hk, int D, int S, int NB, int64_t key_stride_tok,
+                                   int64_t value_stride_tok, int32_t* dev_err,
+                                   cudaStream_t stream);
+pd_status launch_copy_blocks(void* const* key_caches, void* const* value_caches, int L,
+                             const int64_t* block_mapping, int npairs, int Hk, int D, int S,
+                             int NB, int32_t* dev_err, cudaStream_t stream);
+
+// ---- prefill -------------------------------------------------------------------------
+struct PrefillArgs {
+    void* out;
+    const void* q;
+    const int32_t* cu_q_lens;
+    int max_q_len;
+    const void* key_cache;
+    const void* value_cache;
+    const int32_t* block_tables;
+    int max_blocks_per_seq;
+    const int32_t* context_lens;
+    int B, H, Hk, D, S, NB;
+    float scale;
+    pd_dtype dt;
+    int32_t* dev_err;
+    cudaStream_t stream;
+};
+pd_status launch_prefill(const PrefillArgs& a);
+
+void count_launch();
+
+}  // namespace pd

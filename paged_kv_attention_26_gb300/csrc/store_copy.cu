@@ -1,0 +1,109 @@
+// store_copy.cu -- the two cache-maintenance kernels: storing new tokens into
+// their slots (nanoPD page, "模块结构与代码组织": the paged KV store op) and
+// copy-on-write block copies (tutorial page "LLM 推理服务引擎深度拆解",
+// section 2.3, BlockManager.cow()).  Both are HBM-bound bit copies moved in
+// 16-byte vectors; neither looks at the element type.
+#include <cuda_runtime.h>
+
+#include "pd_device.cuh"
+#include "pd_internal.h"
+
+namespace pd {
+namespace {
+
+constexpr int kStoreThreads = 256;
+
+// One (token, kv head) row of D elements = D/8 16-byte vectors per row; each
+// thread moves one vector of K and one of V.
+__global__ void __launch_bounds__(kStoreThreads)
+reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict__ value,
+                         uint4* __restrict__ key_cache, uint4* __restrict__ value_cache,
+                         const int64_t* __restrict__ slot_mapping, int T, int Hk, int D,
+                         int S, int NB, int64_t key_stride_vec, int64_t value_stride_vec,
+                         int32_t* dev_err) {
+    const int vec_per_row = D / 8;
+    const int64_t g = int64_t(blockIdx.x) * kStoreThreads + threadIdx.x;
+    const int64_t row = g / vec_per_row;
+    const int c = int(g % vec_per_row);
+    if (row >= int64_t(T) * Hk) return;
+    const int64_t n = row / Hk;
+    const int h = int(row % Hk);
+    const int64_t slot = __ldg(slot_mapping + n);
+    if (slot < 0) return;                       // padding token
+    if (slot >= int64_t(NB) * S) {
+        if (c == 0) flag_error(dev_err, PD_DEVERR_SLOT_RANGE);
+        return;
+    }
+    const int64_t blk = slot / S, off = slot % S;
+    const int64_t dst = ((blk * Hk + h) * S + off) * vec_per_row + c;
+    const uint4 kv = __ldg(key + n * key_stride_vec + int64_t(h) * vec_per_row + c);
+    const uint4 vv = __ldg(value + n * value_stride_vec + int64_t(h) * vec_per_row + c);
+    key_cache[dst] = kv;
+    value_cache[dst] = vv;
+}
+
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;
+
+// blockIdx.x = pair, blockIdx.y = layer, blockIdx.z = 0 for K, 1 for V.
+// The whole block (Hk * S * D elements) is contiguous in the pool.
+__global__ void __launch_bounds__(kCopyThreads)
+copy_blocks_kernel(void* const* __restrict__ key_caches, void* const* __restrict__ value_caches,
+                   const int64_t* __restrict__ block_mapping, int NB, int64_t block_vecs,
+                   int32_t* dev_err) {
+    const int64_t src = __ldg(block_mapping + 2 * blockIdx.x);
+    const int64_t dst = __ldg(block_mapping + 2 * blockIdx.x + 1);
+    if (src < 0 || src >= NB || dst < 0 || dst >= NB) {
+        if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+            flag_error(dev_err, PD_DEVERR_BLOCK_RANGE);
+        return;
+    }
+    void* const* pools = blockIdx.z == 0 ? key_caches : value_caches;
+    uint4* pool = static_cast<uint4*>(pools[blockIdx.y]);
+    const uint4* s = pool + src * block_vecs;
+    uint4* d = pool + dst * block_vecs;
+    for (int64_t base = threadIdx.x; base < block_vecs; base += kCopyThreads * kCopyUnroll) {
+        uint4 r[kCopyUnroll];
+#pragma unroll
+        for (int k = 0; k < kCopyUnroll; ++k) {
+            const int64_t i = base + int64_t(k) * kCopyThreads;
+            if (i < block_vecs) r[k] = s[i];
+        }
+#pragma unroll
+        for (int k = 0; k < kCopyUnroll; ++k) {
+            const int64_t i = base + int64_t(k) * kCopyThreads;
+            if (i < block_vecs) d[i] = r[k];
+        }
+    }
+}
+
+}  // namespace
+
+pd_status launch_reshape_and_cache(const void* key, const void* value, void* key_cache,
+                                   void* value_cache, const int64_t* slot_mapping, int T,
+                                   int Hk, int D, int S, int NB, int64_t key_stride_tok,
+                                   int64_t value_stride_tok, int32_t* dev_err,
+                                   cudaStream_t stream) {
+    if (T == 0) return PD_OK;
+    const int64_t threads = int64_t(T) * Hk * (D / 8);
+    const int64_t blocks = (threads + kStoreThreads - 1) / kStoreThreads;
+    reshape_and_cache_kernel<<<unsigned(blocks), kStoreThreads, 0, stream>>>(
+        static_cast<const uint4*>(key), static_cast<const uint4*>(value),
+        static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache), slot_mapping, T, Hk,
+        D, S, NB, key_stride_tok / 8, value_stride_tok / 8, dev_err);
+    return launch_result(cudaGetLastError());
+}
+
+pd_status launch_copy_blocks(void* const* key_caches, void* const* value_caches, int L,
+                             const int64_t* block_mapping, int npairs, int Hk, int D, int S,
+                             int NB, int32_t* dev_err, cudaStream_t stream) {
+    if (npairs == 0 || L == 0) return PD_OK;
+    const int64_t block_vecs = int64_t(Hk) * S * D / 8;
+    dim3 grid(unsigned(npairs), unsigned(L), 2);
+    copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(key_caches, value_caches,
+                                                          block_mapping, NB, block_vecs,
+                                                          dev_err);
+    return launch_result(cudaGetLastError());
+}
+
+}  // namespace pd

@@ -4,13 +4,14 @@ test_oracle_pins.py must reject every one of them.  CPU only; the mutants are
 built in a temporary directory and never touch the real oracle build."""
 import os
 import subprocess
-
-import pytest
+import sys
+from concurrent.futures import ThreadPoolExecutor
 
 import oracle
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 # (name, exact text in oracle.c, replacement)
 MUTANTS = [
@@ -59,29 +60,38 @@ def _build_mutant(tmp_path, name, old, new):
     return str(lib)
 
 
-@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pins_reject_mutant(tmp_path, name, old, new):
-    lib = _build_mutant(tmp_path, name, old, new)
-    prev = oracle.swap_library(lib)
-    caught = []
-    try:
-        for chk in PIN_CHECKS:
-            try:
-                chk()
-            except (AssertionError, ValueError):
-                caught.append(chk)
-    finally:
-        oracle.swap_library(None)
-        del prev
-    assert caught, f"no pin rejects the planted mistake '{name}'"
+def run_checks(lib_path: str) -> int:
+    """Run every pin check against the oracle build at ``lib_path``; the number
+    of checks that reject it."""
+    oracle.swap_library(lib_path)
+    caught = 0
+    for chk in PIN_CHECKS:
+        try:
+            chk()
+        except (AssertionError, ValueError):
+            caught += 1
+    return caught
+
+
+def _child(lib_path: str) -> subprocess.CompletedProcess:
+    # A mutant may write out of bounds, so each one runs in its own process;
+    # a crash counts as caught.
+    code = ("import sys; from tests import test_oracle_mutants as m; "
+            f"sys.exit(1 if m.run_checks({lib_path!r}) else 0)")
+    return subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True,
+                          timeout=600)
+
+
+def test_pins_reject_every_mutant(tmp_path):
+    libs = {name: _build_mutant(tmp_path, name, old, new) for name, old, new in MUTANTS}
+    with ThreadPoolExecutor(max(1, min(8, os.cpu_count() or 1))) as ex:
+        res = dict(zip(libs, ex.map(_child, libs.values())))
+    missed = [n for n, r in res.items() if r.returncode == 0]
+    assert not missed, f"no pin rejects the planted mistakes {missed}"
 
 
 def test_unmutated_copy_passes_every_check(tmp_path):
     lib = _build_mutant(tmp_path, "identity", "enum { ORC_F16 = 0, ORC_BF16 = 1 };",
                         "enum { ORC_F16 = 0, ORC_BF16 = 1 };")
-    oracle.swap_library(lib)
-    try:
-        for chk in PIN_CHECKS:
-            chk()
-    finally:
-        oracle.swap_library(None)
+    r = _child(lib)
+    assert r.returncode == 0, r.stderr.decode()[-2000:]
