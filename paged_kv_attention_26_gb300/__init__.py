@@ -239,7 +239,8 @@ def pd_copy_blocks(key_caches, value_caches, block_mapping, dev_err=None, stream
     for t in list(key_caches) + list(value_caches):
         if t.shape != key_caches[0].shape or t.dtype != key_caches[0].dtype:
             raise ValueError("all pools must share shape and dtype")
-        _dev(t, "cache")
+        if _dev(t, "cache") % 16:
+            raise ValueError("cache pools must be 16-byte aligned")
     if block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
         raise ValueError("block_mapping must be [npairs, 2]")
     kp = pointer_array(key_caches)

@@ -91,7 +91,8 @@ pd_status pd_paged_attention_decode(void* out, const void* q, const void* key_ca
         return PD_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
         return PD_ERR_INVALID_ARG;
-    if (B > 65535 || int64_t(max_blocks_per_seq) * S > (int64_t(1) << 30))
+    if (B > 65535 || int64_t(max_blocks_per_seq) * S > (int64_t(1) << 30) ||
+        decode_num_partitions(max_context_len) > 65535)
         return PD_ERR_UNSUPPORTED;
     const size_t need = decode_workspace_bytes(B, H, D, max_context_len);
     if (need > 0) {

@@ -60,6 +60,10 @@ copy_blocks_kernel(void* const* __restrict__ key_caches, void* const* __restrict
     }
     void* const* pools = blockIdx.z == 0 ? key_caches : value_caches;
     uint4* pool = static_cast<uint4*>(pools[blockIdx.y]);
+    if (reinterpret_cast<uintptr_t>(pool) & 15u) {     // pointer table is device data
+        if (threadIdx.x == 0) flag_error(dev_err, PD_DEVERR_BLOCK_RANGE);
+        return;
+    }
     const uint4* s = pool + src * block_vecs;
     uint4* d = pool + dst * block_vecs;
     for (int64_t base = threadIdx.x; base < block_vecs; base += kCopyThreads * kCopyUnroll) {
