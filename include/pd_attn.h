@@ -161,14 +161,16 @@ PD_API pd_status pd_copy_blocks(void* const* key_caches, void* const* value_cach
  * ctx_i = P_i + C_i tokens.  Query j of the chunk (position P_i + j) attends
  * causally to keys 0 .. P_i + j:
  *   out[tok][h][:] = sum_{t <= P_i + j} softmax_t(scale * q[tok][h] . k_t) v_t
- *   q, out        packed [sum_i C_i][H][D]; sequence i's tokens are rows
+ *   q, out        packed [total_q][H][D]; sequence i's tokens are rows
  *                 cu_q_lens[i] .. cu_q_lens[i+1]-1
- *   cu_q_lens     int32 [B + 1], cu_q_lens[0] = 0, non-decreasing
+ *   cu_q_lens     int32 [B + 1], non-decreasing, cu_q_lens[B] <= total_q
+ *                 (checked on device: PD_DEVERR_CTX_RANGE, sequence skipped)
  *   max_q_len     >= every C_i (sizes the launch grid)
  *   context_lens  int32 [B] = P_i + C_i (>= C_i; checked on device)
  * QK^T and PV run on the tensor cores (tcgen05, fp32 accumulation in tensor
- * memory); probabilities are rounded to the element type before PV. */
-PD_API pd_status pd_paged_prefill_chunk(void* out, const void* q,
+ * memory); probabilities are rounded to the element type before PV.
+ * scale must be positive and finite. */
+PD_API pd_status pd_paged_prefill_chunk(void* out, const void* q, int total_q,
                                  const int32_t* cu_q_lens, int max_q_len,
                                  const void* key_cache, const void* value_cache,
                                  const int32_t* block_tables,

@@ -49,8 +49,8 @@ SIGNATURES = {
     "pd_paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I,
                                        _F, _P, _SZ, _I, _P, _P]),
     "pd_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
-    "pd_paged_prefill_chunk": (_I, [_P, _P, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I,
-                                    _F, _I, _P, _P]),
+    "pd_paged_prefill_chunk": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
+                                    _I, _F, _I, _P, _P]),
     "pd_bm_create": (_P, [_I, _I]),
     "pd_bm_destroy": (None, [_P]),
     "pd_bm_add_seq": (_I, [_P, _I]),
@@ -268,7 +268,7 @@ def pd_paged_prefill_chunk(out, q, cu_q_lens, max_q_len: int, key_cache, value_c
         if t.dtype != key_cache.dtype:
             raise TypeError("dtype mismatch")
     st = load().pd_paged_prefill_chunk(
-        _dev(out, "out"), _dev(q, "q"), _dev(cu_q_lens, "cu_q_lens", torch.int32),
+        _dev(out, "out"), _dev(q, "q"), NT, _dev(cu_q_lens, "cu_q_lens", torch.int32),
         int(max_q_len), _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
         _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
         _dev(context_lens, "context_lens", torch.int32), B, H, Hk, D, S, NB, float(scale),

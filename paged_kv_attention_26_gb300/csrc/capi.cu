@@ -3,7 +3,9 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdint>
+#include <cstdlib>
 
 #include "pd_attn.h"
 #include "pd_internal.h"
@@ -24,6 +26,16 @@ pd_status launch_result(cudaError_t e) {
 }
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+// PD_PREFILL_P_IN_SMEM=1 stages the softmax probabilities in shared memory
+// (two shared-memory operands) instead of tensor memory; read once.
+bool prefill_p_in_smem() {
+    static const bool v = [] {
+        const char* e = std::getenv("PD_PREFILL_P_IN_SMEM");
+        return e != nullptr && e[0] == '1';
+    }();
+    return v;
+}
 
 }  // namespace pd
 
@@ -117,26 +129,30 @@ pd_status pd_copy_blocks(void* const* key_caches, void* const* value_caches, int
                               dev_err, stream);
 }
 
-pd_status pd_paged_prefill_chunk(void* out, const void* q, const int32_t* cu_q_lens,
-                                 int max_q_len, const void* key_cache, const void* value_cache,
+pd_status pd_paged_prefill_chunk(void* out, const void* q, int total_q,
+                                 const int32_t* cu_q_lens, int max_q_len,
+                                 const void* key_cache, const void* value_cache,
                                  const int32_t* block_tables, int max_blocks_per_seq,
                                  const int32_t* context_lens, int B, int H, int Hk, int D, int S,
                                  int NB, float scale, pd_dtype dt, int32_t* dev_err,
                                  cudaStream_t stream) {
-    if (B < 0 || H < 1 || Hk < 1 || NB < 1 || max_blocks_per_seq < 1 || max_q_len < 0)
+    if (B < 0 || H < 1 || Hk < 1 || NB < 1 || max_blocks_per_seq < 1 || max_q_len < 0 ||
+        total_q < 0)
         return PD_ERR_INVALID_ARG;
-    if (H % Hk != 0) return PD_ERR_INVALID_ARG;
+    if (H % Hk != 0 || !(scale > 0.f) || !std::isfinite(scale)) return PD_ERR_INVALID_ARG;
     if (!supported_D(D) || !supported_S(S) || !supported_dt(dt)) return PD_ERR_UNSUPPORTED;
-    if (B == 0 || max_q_len == 0) return PD_OK;
+    if (B == 0 || max_q_len == 0 || total_q == 0) return PD_OK;
     if (!out || !q || !cu_q_lens || !key_cache || !value_cache || !block_tables || !context_lens)
         return PD_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
         return PD_ERR_INVALID_ARG;
     if (B > 65535 || int64_t(max_blocks_per_seq) * S > (int64_t(1) << 30))
         return PD_ERR_UNSUPPORTED;
-    PrefillArgs a{out, q, cu_q_lens, max_q_len, key_cache, value_cache, block_tables,
+    if (int64_t(max_q_len) > int64_t(65535) * 128 || int64_t(NB) * Hk * S > (int64_t(1) << 31))
+        return PD_ERR_UNSUPPORTED;
+    PrefillArgs a{out, q, total_q, cu_q_lens, max_q_len, key_cache, value_cache, block_tables,
                   max_blocks_per_seq, context_lens, B, H, Hk, D, S, NB, scale, dt, dev_err,
-                  stream};
+                  stream, prefill_p_in_smem()};
     return launch_prefill(a);
 }
 

@@ -323,6 +323,9 @@ paged_decode_split_kernel(T* __restrict__ out, const T* __restrict__ q,
         float m_mine = m_run[0];
 #pragma unroll
         for (int h = 1; h < GH; ++h) if (h == my_h) m_mine = m_run[h];
+        // A warp that has not seen a valid token yet keeps max -inf; its
+        // scores are all -inf too and must give p = 0, not 2^(-inf + inf).
+        if (m_mine == -INFINITY) m_mine = 0.f;
 #pragma unroll
         for (int qd = 0; qd < L::kQuadsPerWarp; ++qd) {
             const float p = ex2(s[qd] - m_mine);   // 0 for masked tokens

@@ -56,6 +56,7 @@ pd_status launch_copy_blocks(void* const* key_caches, void* const* value_caches,
 struct PrefillArgs {
     void* out;
     const void* q;
+    int total_q;
     const int32_t* cu_q_lens;
     int max_q_len;
     const void* key_cache;
@@ -68,9 +69,11 @@ struct PrefillArgs {
     pd_dtype dt;
     int32_t* dev_err;
     cudaStream_t stream;
+    bool p_in_smem;   // probabilities staged in shared memory instead of tensor memory
 };
 pd_status launch_prefill(const PrefillArgs& a);
 
 void count_launch();
+bool prefill_p_in_smem();
 
 }  // namespace pd

@@ -1,8 +1,498 @@
-// prefill.cu -- chunked-prefill attention (tcgen05 / TMEM / TMA).
+// prefill.cu -- chunked-prefill attention over the paged cache on the 5th-gen
+// tensor cores (tcgen05 MMA, accumulators in tensor memory, operands staged by
+// TMA).
+//
+// Operation (nanoPD page "分块预填充"; tutorial page "LLM 推理服务引擎深度拆解"
+// section 5.2): sequence i appends a chunk of C_i queries after P_i cached
+// tokens; query j sees keys 0 .. P_i + j of its own paged context:
+//   out = softmax(scale * q K^T) V, causal, GQA head h -> kv head h / G.
+// Prefill is a dense contraction (tensor-core bound, essay page
+// "LLM推理PD分离架构深度工程实践" section 1), so QK^T and PV run as
+// tcgen05.mma with fp32 accumulation in tensor memory.
+//
+// Tiling.  A CTA owns one 128-row query tile and streams 128-key tiles:
+//  * GQA packing: the G' = min(G, 16) query heads that share a kv head are
+//    interleaved into the tile (rows = 128/G' tokens x G' heads), so every
+//    K/V tile is loaded once for all of them and the causal band is narrow;
+//  * warp 0 issues TMA loads: the Q tile once (3-D map over [tokens][heads][D]),
+//    then per key tile one 2-D box [S rows][64 dims] per K and per V block,
+//    gathered through the block table into a 2-stage ring, 128-byte swizzle;
+//  * warp 1 allocates tensor memory and issues the MMAs from one thread:
+//    S = Q K^T into one of two S buffers (so QK^T of tile t+1 overlaps the
+//    softmax of tile t), then O += P V with P read straight from tensor
+//    memory where the softmax wrote it over S;
+//  * warps 2-5 (one query row per thread) run the online softmax in the
+//    log2 domain with lazy rescaling (the accumulator O is rescaled only when
+//    a row max grows by more than 2^8), write P as 16-bit values, and finally
+//    normalise O and store it.
+// Every wait is bounded; a wait that runs out flags PD_DEVERR_TIMEOUT and the
+// CTA drains its in-flight copies and MMAs, frees tensor memory and leaves.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <cmath>
+
+#include "pd_device.cuh"
 #include "pd_internal.h"
+#include "pd_tcgen05.cuh"
 
 namespace pd {
-pd_status launch_prefill(const PrefillArgs&) { return PD_ERR_UNSUPPORTED; }
+namespace {
+
+constexpr int kTileM = 128;            // query rows per tile (MMA M)
+constexpr int kTileN = 128;            // keys per tile
+constexpr int kKVStages = 2;
+constexpr int kPrefillThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kSoftmaxThreads = 128;
+constexpr uint32_t kTmemCols = 512;    // S0 [0,128) S1 [128,256) O [256, 256+D)
+constexpr uint32_t kTmemO = 256;
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D, bool kPInTmem>
+struct PrefillSmem {
+    static constexpr int kAtom = kTileM * 128;          // 128 rows x 128 B (64 16-bit values)
+    static constexpr int kTile = (D / 64) * kAtom;      // a [128][D] tile
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + kTile;                // kKVStages tiles
+    static constexpr int kV = kK + kKVStages * kTile;
+    static constexpr int kP = kV + kKVStages * kTile;    // P tiles [128][128] (smem variant)
+    static constexpr int kPBytes = kPInTmem ? 0 : 2 * kTileM * kTileN * 2;
+    static constexpr int kBar = kP + kPBytes;
+    // barriers: q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], pv_done, drain
+    static constexpr int kNumBars = 11;
+    static constexpr int kMisc = kBar + kNumBars * 8;   // tmem base, abort flag, issued count
+    static constexpr int kBytes = kMisc + 16;
+    // room to align the base to 1 KB; at least 116 KB so a second CTA never
+    // shares the SM (each CTA takes all 512 tensor-memory columns)
+    static constexpr int kAlloc = kBytes + 1024 > 116 * 1024 ? kBytes + 1024 : 116 * 1024;
+};
+
+template <typename T, int D, bool kPInTmem>
+__global__ void __launch_bounds__(kPrefillThreads, 1)
+paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, T* __restrict__ out, int total_q,
+                     const int32_t* __restrict__ cu_q_lens,
+                     const int32_t* __restrict__ block_tables, int max_blocks_per_seq,
+                     const int32_t* __restrict__ context_lens, int H, int Hk, int S, int NB,
+                     int GP, float scale_log2, int32_t* dev_err) {
+    using L = PrefillSmem<D, kPInTmem>;
+    using E = Elem<T>;
+    constexpr bool kBf16 = E::kDtype == PD_BF16;
+    constexpr uint32_t kIdescQK = tc::idesc_f16(kBf16, kTileM, kTileN, false, false);
+    constexpr uint32_t kIdescPV = tc::idesc_f16(kBf16, kTileM, D, false, true);
+    constexpr int kAtoms = D / 64;
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+    uint64_t* q_full = bars + 0;
+    uint64_t* kv_full = bars + 1;     // [2]
+    uint64_t* kv_empty = bars + 3;    // [2]
+    uint64_t* s_full = bars + 5;      // [2]
+    uint64_t* p_full = bars + 7;      // [2]
+    uint64_t* pv_done = bars + 9;
+    uint64_t* drain = bars + 10;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L::kMisc);
+    volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kMisc + 4);
+    volatile int32_t* issued = reinterpret_cast<volatile int32_t*>(smem + L::kMisc + 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int seq = blockIdx.z;
+    const int TQ = kTileM / GP;                       // query tokens per tile
+    const int q_begin = __ldg(cu_q_lens + seq);
+    const int C = __ldg(cu_q_lens + seq + 1) - q_begin;
+    const int q0 = blockIdx.x * TQ;                   // first chunk token of this tile
+    if (q0 >= C) return;
+    const int ctx = __ldg(context_lens + seq);
+    const int P = ctx - C;
+    if (C < 0 || P < 0 || ctx > max_blocks_per_seq * S || q_begin < 0 ||
+        q_begin + C > total_q) {
+        if (threadIdx.x == 0) flag_error(dev_err, PD_DEVERR_CTX_RANGE);
+        return;
+    }
+    const int G = H / Hk;
+    const int sub = G / GP;
+    const int kvh = blockIdx.y / sub;
+    const int head0 = kvh * G + (blockIdx.y % sub) * GP;
+    const int q_last = min(C, q0 + TQ) - 1;
+    const int n_keys = P + q_last + 1;
+    const int n_tiles = (n_keys + kTileN - 1) / kTileN;
+    const int n_blocks_ctx = (ctx + S - 1) / S;
+    const int32_t* bt_row = block_tables + (int64_t)seq * max_blocks_per_seq;
+
+    const uint32_t sQ = smem_u32(smem + L::kQ);
+    const uint32_t sK = smem_u32(smem + L::kK);
+    const uint32_t sV = smem_u32(smem + L::kV);
+    const uint32_t sP = smem_u32(smem + L::kP);
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < kKVStages; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+            mbar_init(&s_full[s], 1);
+            mbar_init(&p_full[s], kSoftmaxThreads);
+        }
+        mbar_init(pv_done, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        *issued = 0;
+        fence_mbar_init();
+        tc::prefetch_tmap(&tm_q);
+        tc::prefetch_tmap(&tm_k);
+        tc::prefetch_tmap(&tm_v);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(const_cast<uint32_t*>(tmem_slot), kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            mbar_arrive_expect_tx(q_full, uint32_t(kTileM) * D * 2);
+            for (int a = 0; a < kAtoms; ++a)
+                tc::tma_load_3d(smem + L::kQ + a * L::kAtom, &tm_q, a * 64, head0, q_begin + q0,
+                                q_full);
+        }
+        const int blocks_per_tile = kTileN / S;            // 2 .. 16
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t & 1;
+            const bool ok = __all_sync(0xffffffffu,
+                                       t < kKVStages || mbar_wait(&kv_empty[st], ((t >> 1) - 1) & 1));
+            if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) {
+                if (lane == 0 && !ok) {
+                    flag_error(dev_err, PD_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            int64_t row = -1;
+            if (lane < blocks_per_tile) {
+                const int lb = t * blocks_per_tile + lane;
+                if (lb < n_blocks_ctx) {
+                    const int blk = __ldg(bt_row + lb);
+                    if (blk >= 0 && blk < NB) {
+                        row = ((int64_t)blk * Hk + kvh) * S;
+                    } else {
+                        flag_error(dev_err, PD_DEVERR_BLOCK_RANGE);
+                    }
+                }
+            }
+            const uint32_t ok_mask = __ballot_sync(0xffffffffu, row >= 0);
+            if (lane == 0)
+                mbar_arrive_expect_tx(&kv_full[st], uint32_t(__popc(ok_mask)) * S * D * 2 * 2);
+            __syncwarp();
+            if (row >= 0) {
+                for (int a = 0; a < kAtoms; ++a) {
+                    const int off = st * L::kTile + a * L::kAtom + lane * S * 128;
+                    tc::tma_load_2d(smem + L::kK + off, &tm_k, a * 64, int32_t(row), &kv_full[st]);
+                    tc::tma_load_2d(smem + L::kV + off, &tm_v, a * 64, int32_t(row), &kv_full[st]);
+                }
+            }
+            if (lane == 0) *issued = t + 1;
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer --------------------------------
+        if (lane == 0) {
+            bool ok = mbar_wait(q_full, 0);
+            for (int t = 0; ok && t <= n_tiles; ++t) {
+                if (*abort_flag) { ok = false; break; }
+                if (t < n_tiles) {
+                    const int st = t & 1;
+                    if (!(ok = mbar_wait(&kv_full[st], (t >> 1) & 1))) break;
+                    tc::fence_after_sync();
+                    const uint32_t d_s = tmem + uint32_t(st) * kTileN;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t koff = (kk >> 2) * L::kAtom + (kk & 3) * 32;
+                        const uint64_t a = tc::smem_desc_sw128(sQ + koff, 16, 1024);
+                        const uint64_t b = tc::smem_desc_sw128(sK + st * L::kTile + koff, 16, 1024);
+                        tc::mma_ss(d_s, a, b, kIdescQK, kk > 0);
+                    }
+                    tc::commit(&s_full[st]);
+                }
+                if (t > 0) {
+                    const int u = t - 1, su = u & 1;
+                    if (!(ok = mbar_wait(&p_full[su], (u >> 1) & 1))) break;
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < kTileN / 16; ++kk) {
+                        // V tile as an MN-major operand: N = D contiguous in 64-wide
+                        // atoms (LBO between them), K = keys at 128 B (SBO per 8 keys)
+                        const uint64_t b = tc::smem_desc_sw128(sV + su * L::kTile + kk * 16 * 128,
+                                                               L::kAtom, 1024);
+                        if constexpr (kPInTmem) {
+                            tc::mma_ts(tmem + kTmemO, tmem + uint32_t(su) * kTileN + kk * 8, b,
+                                       kIdescPV, (u > 0 || kk > 0));
+                        } else {
+                            const uint32_t poff = (kk >> 2) * L::kAtom + (kk & 3) * 32;
+                            const uint64_t a = tc::smem_desc_sw128(
+                                sP + su * (kTileM * kTileN * 2) + poff, 16, 1024);
+                            tc::mma_ss(tmem + kTmemO, a, b, kIdescPV, (u > 0 || kk > 0));
+                        }
+                    }
+                    tc::commit(pv_done);
+                    tc::commit(&kv_empty[su]);
+                }
+            }
+            if (!ok) {
+                flag_error(dev_err, PD_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+        __syncwarp();
+    } else {
+        // --------------------------- softmax + epilogue ---------------------------
+        const int quarter = warp & 3;                  // tensor-memory lane quarter
+        const int r = quarter * 32 + lane;             // tile row
+        const int tok = r / GP;                        // token within the tile
+        const int g = r % GP;
+        const int pos = P + q0 + tok;                  // position of this query
+        const int lim = min(pos, ctx - 1);             // last visible key
+        const bool row_valid = q0 + tok < C;
+        const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[st], (t >> 1) & 1));
+            if (!ok || *abort_flag) break;
+            tc::fence_after_sync();
+            uint32_t sr[kTileN];
+#pragma unroll
+            for (int c = 0; c < kTileN / 32; ++c)
+                tc::tmem_ld32(tmem + lane_base + uint32_t(st) * kTileN + c * 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+            tc::tmem_ld_wait();
+            const int kbase = t * kTileN;
+            float mx = -INFINITY;
+            if (kbase + kTileN - 1 > lim) {            // tile crosses this row's limit
+#pragma unroll
+                for (int c = 0; c < kTileN; ++c) {
+                    const float s = kbase + c <= lim ? __uint_as_float(sr[c]) : -INFINITY;
+                    sr[c] = __float_as_uint(s);
+                    mx = fmaxf(mx, s);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kTileN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+            }
+            const float m_tile = mx * scale_log2;
+            if (m_tile > m_run + kRescaleThreshold) {
+                const float alpha = ex2(m_run - m_tile);   // 0 on the first tile
+                if (t > 0) {
+                    // O holds PV of tiles < t; wait for the last of them, then scale.
+                    ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (t - 1) & 1));
+                    if (!ok) break;
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tc::tmem_ld32(tmem + lane_base + kTmemO + c * 32, o);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tc::tmem_st32(tmem + lane_base + kTmemO + c * 32, o);
+                    }
+                    tc::tmem_st_wait();
+                }
+                l_run *= alpha;
+                m_run = m_tile;
+            }
+            // p = 2^(s * scale_log2 - m), rounded to the element type
+            uint32_t pk[kTileN / 2];
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < kTileN / 2; ++c) {
+                const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), scale_log2, -m_run));
+                const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), scale_log2, -m_run));
+                lsum += p0 + p1;
+                pk[c] = E::pack2(p0, p1);
+            }
+            l_run += lsum;
+            if constexpr (kPInTmem) {
+#pragma unroll
+                for (int c = 0; c < kTileN / 64; ++c)
+                    tc::tmem_st32(tmem + lane_base + uint32_t(st) * kTileN + c * 32,
+                                  *reinterpret_cast<const uint32_t(*)[32]>(&pk[c * 32]));
+                tc::tmem_st_wait();
+            } else {
+                unsigned char* prow = smem + L::kP + st * (kTileM * kTileN * 2) + r * 128;
+#pragma unroll
+                for (int a = 0; a < 2; ++a)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(prow + a * L::kAtom + ((c ^ (r & 7)) * 16)) =
+                            make_uint4(pk[a * 32 + c * 4], pk[a * 32 + c * 4 + 1],
+                                       pk[a * 32 + c * 4 + 2], pk[a * 32 + c * 4 + 3]);
+            }
+            if (kbase + kTileN > ctx) {
+                // Keys past the context in the last tile: their V rows hold other
+                // data (or were never loaded); zero them so 0 * v stays 0.
+                ok = __all_sync(0xffffffffu, mbar_wait(&kv_full[st], (t >> 1) & 1));
+                if (!ok) break;
+                if (kbase + r >= ctx) {
+                    unsigned char* vrow = smem + L::kV + st * L::kTile + r * 128;
+#pragma unroll
+                    for (int a = 0; a < kAtoms; ++a)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<uint4*>(vrow + a * L::kAtom + c * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            if (!kPInTmem || kbase + kTileN > ctx) tc::fence_proxy_async_smem();
+            tc::fence_before_sync();
+            mbar_arrive(&p_full[st]);
+        }
+        if (ok && !*abort_flag) {
+            ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (n_tiles - 1) & 1));
+            if (ok) {
+                tc::fence_after_sync();
+                const float inv = 1.f / l_run;
+                T* orow = out + ((int64_t)(q_begin + q0 + tok) * H + head0 + g) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(tmem + lane_base + kTmemO + c * 32, o);
+                    tc::tmem_ld_wait();
+                    uint32_t pk2[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk2[e] = E::pack2(__uint_as_float(o[2 * e]) * inv,
+                                          __uint_as_float(o[2 * e + 1]) * inv);
+                    if (row_valid) {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            dst[e] = make_uint4(pk2[4 * e], pk2[4 * e + 1], pk2[4 * e + 2],
+                                                pk2[4 * e + 3]);
+                    }
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            flag_error(dev_err, PD_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+    }
+
+    __syncthreads();
+    if (*abort_flag) {
+        // Drain: no MMA may still be writing tensor memory, no TMA shared memory.
+        if (warp == 1 && lane == 0) {
+            tc::commit(drain);
+            mbar_wait(drain, 0);
+        }
+        if (warp == 0 && lane == 0) {
+            const int n = *issued;
+            for (int t = max(0, n - kKVStages); t < n; ++t)
+                if (!mbar_wait(&kv_full[t & 1], (t >> 1) & 1)) break;
+            mbar_wait(q_full, 0);
+        }
+        __syncthreads();
+    }
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---- host side --------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+template <typename T, int D, bool kPInTmem>
+pd_status launch_prefill_t(const PrefillArgs& a) {
+    using L = PrefillSmem<D, kPInTmem>;
+    auto encode = encode_fn();
+    if (!encode) return launch_result(cudaErrorNotSupported);
+    const CUtensorMapDataType dt =
+        Elem<T>::kDtype == PD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const int G = a.H / a.Hk;
+    int GP = 1;
+    while (GP * 2 <= 16 && G % (GP * 2) == 0) GP *= 2;
+    const int TQ = kTileM / GP;
+
+    CUtensorMap tm_q, tm_k, tm_v;
+    {
+        cuuint64_t dims[3] = {cuuint64_t(a.D), cuuint64_t(a.H), cuuint64_t(a.total_q)};
+        cuuint64_t strides[2] = {cuuint64_t(a.D) * 2, cuuint64_t(a.H) * a.D * 2};
+        cuuint32_t box[3] = {64u, cuuint32_t(GP), cuuint32_t(TQ)};
+        cuuint32_t es[3] = {1u, 1u, 1u};
+        CUresult r = encode(&tm_q, dt, 3, const_cast<void*>(a.q), dims, strides, box, es,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return launch_result(cudaErrorInvalidValue);
+    }
+    {
+        cuuint64_t dims[2] = {cuuint64_t(a.D), cuuint64_t(a.NB) * a.Hk * a.S};
+        cuuint64_t strides[1] = {cuuint64_t(a.D) * 2};
+        cuuint32_t box[2] = {64u, cuuint32_t(a.S)};
+        cuuint32_t es[2] = {1u, 1u};
+        CUresult r = encode(&tm_k, dt, 2, const_cast<void*>(a.key_cache), dims, strides, box, es,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return launch_result(cudaErrorInvalidValue);
+        r = encode(&tm_v, dt, 2, const_cast<void*>(a.value_cache), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return launch_result(cudaErrorInvalidValue);
+    }
+    auto kern = paged_prefill_kernel<T, D, kPInTmem>;
+    static uint64_t attr_set = 0;   // one bit per device
+    int dev = 0;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return launch_result(e0);
+    if (dev >= 64 || !((attr_set >> dev) & 1)) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             L::kAlloc);
+        if (e != cudaSuccess) return launch_result(e);
+        if (dev < 64) attr_set |= uint64_t(1) << dev;
+    }
+    dim3 grid(unsigned((a.max_q_len + TQ - 1) / TQ), unsigned(a.Hk * (G / GP)), unsigned(a.B));
+    kern<<<grid, kPrefillThreads, L::kAlloc, a.stream>>>(
+        tm_q, tm_k, tm_v, static_cast<T*>(a.out), a.total_q, a.cu_q_lens, a.block_tables,
+        a.max_blocks_per_seq, a.context_lens, a.H, a.Hk, a.S, a.NB, GP, a.scale * kLog2e,
+        a.dev_err);
+    return launch_result(cudaGetLastError());
+}
+
+template <bool kPInTmem>
+pd_status launch_prefill_p(const PrefillArgs& a) {
+    if (a.dt == PD_BF16)
+        return a.D == 128 ? launch_prefill_t<__nv_bfloat16, 128, kPInTmem>(a)
+                          : launch_prefill_t<__nv_bfloat16, 64, kPInTmem>(a);
+    return a.D == 128 ? launch_prefill_t<__half, 128, kPInTmem>(a)
+                      : launch_prefill_t<__half, 64, kPInTmem>(a);
+}
+
+}  // namespace
+
+pd_status launch_prefill(const PrefillArgs& a) {
+    return a.p_in_smem ? launch_prefill_p<false>(a) : launch_prefill_p<true>(a);
+}
+
 }  // namespace pd

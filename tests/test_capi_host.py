@@ -125,16 +125,18 @@ def test_copy_and_prefill_validation(lib):
     assert lib.pd_copy_blocks(P, P, 1, P, 0, 8, 128, 16, 10, 1, None, None) == 0
     assert lib.pd_launch_count() == n0
     f = lib.pd_paged_prefill_chunk
-    base = [P, P, P, 16, P, P, P, 8, P, 2, 8, 2, 64, 16, 64, 0.125, pd.PD_BF16, None, None]
-    a = list(base)
-    a[10] = 3
-    assert f(*a) == 1
-    a = list(base)
-    a[12] = 256
-    assert f(*a) == 2
-    a = list(base)
-    a[3] = -1
-    assert f(*a) == 1
+    base = [P, P, 40, P, 16, P, P, P, 8, P, 2, 8, 2, 64, 16, 64, 0.125, pd.PD_BF16, None, None]
+    for change, want in [({11: 3}, 1),        # H % Hk
+                         ({13: 256}, 2),      # D
+                         ({4: -1}, 1),        # max_q_len
+                         ({2: -5}, 1),        # total_q
+                         ({16: 0.0}, 1),      # scale must be positive
+                         ({16: float("nan")}, 1),
+                         ({1: P + 4}, 1)]:    # misaligned q
+        a = list(base)
+        for k, v in change.items():
+            a[k] = v
+        assert f(*a) == want, change
 
 
 # ---- block manager: C++ against the oracle ------------------------------------
