@@ -1,0 +1,572 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged KV-cache attention hot path on GB300.
+
+Headline (one JSON line on stdout, rank 0): the Qwen3-8B-shaped single-layer
+decode step -- batch 64, 32 Q heads, 8 KV heads, head_dim 128, block 16,
+bf16, context lengths uniform on [128, 2048], pool 1.5x the blocks needed --
+where one step is the store of the 64 new tokens (pd_reshape_and_cache) and
+split-context decode attention with its reduce (pd_paged_attention_decode).
+``value`` is the step's algorithmic bytes (K/V read once, q, out, tables and
+the stored tokens) per second of device time, inputs resident in HBM, L2
+flushed (256 MiB write) before every timed step.
+
+The same line carries: the roofline of the dominant kernel (decode) against
+the measured HBM copy bandwidth, the end-to-end figure through the public API
+with host buffers, the float64 oracle timed on the host cores, launch count,
+clocks sampled during the run, and (N=1) the other workloads: the 32-layer
+long-context stack, the chunked-prefill mix (prefill TFLOP/s on the tensor
+cores) and the copy-on-write fork stress.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+N > 1 runs under torch.distributed.run, one process per GPU, each on its own
+replica of the batch (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("Paged decode-attn achieved HBM GB/s (% of GB300 peak); KV tokens/s; "
+          "prefill TFLOP/s")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true", help="headline workload only")
+    ap.add_argument("--extra-steps", type=int, default=10)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return (float(p["hbm_gbs"]), float(p["bf16_tflops"]),
+                float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured")
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def source_sha(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "paged_kv_attention_26_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, sha: str):
+    """DRAM bytes per launch recorded from an ncu capture in profiles/*.md
+    (line 'traffic: kernel=<k> source_sha=<sha> bytes_per_launch=<n>'); None
+    when absent or when the kernel source changed since the capture."""
+    pat = re.compile(r"traffic: kernel=(\S+) source_sha=(\S+) bytes_per_launch=(\d+)")
+    d = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(d):
+        return None
+    for n in sorted(os.listdir(d)):
+        if not n.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(d, n)) as f:
+            for line in f:
+                m = pat.search(line)
+                if m and m.group(1) == kernel and m.group(2) == sha:
+                    return int(m.group(3))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        sm.sort()
+        loaded = [s for s in sm if s > 0.5 * mx] or sm
+        return {"sm_mhz": loaded[len(loaded) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------
+# workload accounting
+
+def decode_alg_bytes(ctx, B, H, Hk, D, S, elem=2):
+    """K/V read once + q read + out written + block-table entries read."""
+    kv = int(sum(ctx)) * Hk * D * elem * 2
+    qo = 2 * B * H * D * elem
+    tables = sum((c + S - 1) // S for c in ctx) * 4
+    return kv, kv + qo + tables
+
+
+def store_alg_bytes(T, Hk, D, elem=2):
+    return 2 * (2 * T * Hk * D * elem) + T * 8     # K,V read + written, slots read
+
+
+# ---------------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import paged_kv_attention_26_gb300 as pd
+    import pd_inputs
+
+    pd.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+
+    stream = torch.cuda.current_stream()
+
+    # ---- headline: Qwen3-8B-shaped decode step --------------------------------------
+    c = pd_inputs.qwen3_8b_decode(seed=rank)
+    B, H, Hk, D, S = c.B, c.H, c.Hk, c.D, c.pool.S
+    ctx = c.pool.context_lens.tolist()
+    mcl = c.max_context_len
+    kc, vc = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
+    q = c.q.to(dev)
+    bt = c.pool.block_tables.to(dev)
+    cl = c.pool.context_lens.to(dev)
+    nk, nv = c.new_key.to(dev), c.new_value.to(dev)
+    slots = c.slot_mapping.to(dev)
+    out = torch.empty_like(q)
+    ws = pd.decode_workspace(B, H, D, mcl, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    kv_bytes, dec_bytes = decode_alg_bytes(ctx, B, H, Hk, D, S)
+    st_bytes = store_alg_bytes(B, Hk, D)
+    step_bytes = dec_bytes + st_bytes
+
+    def step():
+        pd.pd_reshape_and_cache(nk, nv, kc, vc, slots, dev_err=err)
+        pd.pd_paged_attention_decode(out, q, kc, vc, bt, cl, mcl, c.scale, ws, dev_err=err)
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = pd.launch_count()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush()
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        pd.pd_reshape_and_cache(nk, nv, kc, vc, slots, dev_err=err)
+        e1.record(stream)
+        pd.pd_paged_attention_decode(out, q, kc, vc, bt, cl, mcl, c.scale, ws, dev_err=err)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    launches = pd.launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    step_s = sum(a.elapsed_time(b2) for a, _, b2 in ev) * 1e-3
+    dec_s = sum(b1.elapsed_time(b2) for _, b1, b2 in ev) * 1e-3
+    if world > 1:
+        t = torch.tensor([step_s], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_s = float(t.item())
+    assert err.item() == 0, f"device error word {err.item()}"
+    value = world * step_bytes * args.steps / step_s / 1e9
+    ms_per_step = step_s / args.steps * 1e3
+    dec_avg = dec_s / args.steps
+    achieved = dec_bytes / dec_avg / 1e9
+    sha = source_sha("decode.cu", "pd_device.cuh")
+    traffic = profiled_traffic("paged_decode", sha)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "qwen3_8b_decode_step", "batch": B, "q_heads": H, "kv_heads": Hk,
+                   "head_dim": D, "block_size": S, "context_lens": "uniform [128, 2048], seed 0",
+                   "kv_tokens": int(sum(ctx)), "pool_blocks": c.pool.NB,
+                   "step": "store 64 tokens + split-context decode + reduce",
+                   "l2": "flushed before every timed step (256 MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_hbm_peak": round(100 * value / world / hbm_peak, 2),
+        "kv_tokens_per_s": round(world * sum(ctx) * args.steps / step_s, 1),
+        "roofline": {"kernel": "paged_decode (split + reduce)", "bound": "hbm",
+                     "achieved": round(achieved, 2), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
+                     "alg_bytes_per_launch": dec_bytes,
+                     "traffic": traffic, "traffic_source_sha": sha},
+        "gpu_launches": launches,
+        "wall_s_timed_loop": round(t_wall, 4),
+    }
+
+    if rank == 0 and world == 1:
+        result["e2e"] = e2e_decode(pd, c, dev, args, step_bytes)
+        result["cpu_baseline"] = cpu_baseline_decode(c, step_bytes, budget_s=10.0)
+    if world == 1 and not args.no_extras:
+        extras = {}
+        del kc, vc
+        torch.cuda.empty_cache()
+        extras["chunked_prefill_mix"] = bench_prefill_mix(pd, pd_inputs, dev, args, flush,
+                                                          bf16_peak, hbm_peak, peak_src)
+        extras["long_context_32_layers"] = bench_long_context(pd, pd_inputs, dev, args, flush,
+                                                               hbm_peak)
+        extras["cow_fork_stress"] = bench_cow(pd, pd_inputs, dev, args, flush, hbm_peak)
+        result["extras"] = extras
+        pm = extras["chunked_prefill_mix"]
+        result["prefill_tflops"] = pm["prefill_tflops"]
+        result["prefill_pct_of_bf16_peak"] = round(100 * pm["prefill_frac"], 2)
+    if sampler is not None:
+        result["clocks"] = sampler.stop()
+    return result
+
+
+def e2e_decode(pd, c, dev, args, step_bytes):
+    """The same step through the public API from pinned host buffers: per step
+    the inputs go host -> device, the step runs, the output comes back."""
+    import torch
+    pin = lambda t: t.contiguous().pin_memory()
+    h_in = [pin(c.q), pin(c.new_key), pin(c.new_value), pin(c.slot_mapping),
+            pin(c.pool.block_tables), pin(c.pool.context_lens)]
+    d_in = [torch.empty_like(t, device=dev) for t in h_in]
+    kc, vc = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
+    out = torch.empty_like(d_in[0])
+    h_out = torch.empty_like(c.q).pin_memory()
+    ws = pd.decode_workspace(c.B, c.H, c.D, c.max_context_len, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = h_out.numel() * h_out.element_size()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def one():
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        q, nk, nv, sl, bt, cl = d_in
+        pd.pd_reshape_and_cache(nk, nv, kc, vc, sl)
+        pd.pd_paged_attention_decode(out, q, kc, vc, bt, cl, c.max_context_len, c.scale, ws)
+        h_out.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(args.warmup):
+        one()
+    total = 0.0
+    for _ in range(args.steps):
+        flush_buf.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        one()
+        total += time.perf_counter() - t0
+    return {"value": round(step_bytes * args.steps / total / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(total / args.steps * 1e3, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "path": "pinned host -> device copies, pd_reshape_and_cache, "
+                    "pd_paged_attention_decode, device -> host copy, synchronize"}
+
+
+def cpu_baseline_decode(c, step_bytes, budget_s=10.0):
+    """The float64 oracle (as it stands) on this host's cores, on the same step:
+    store + decode of all 64 sequences, repeated until ``budget_s`` elapsed."""
+    import numpy as np
+    import torch
+    import oracle
+    threads = oracle.default_threads()
+    kc0 = c.pool.key_cache.view(torch.int16).numpy().view(np.uint16)
+    vc0 = c.pool.value_cache.view(torch.int16).numpy().view(np.uint16)
+    reps, total = 0, 0.0
+    while total < budget_s and reps < 50:
+        kc, vc = kc0.copy(), vc0.copy()
+        t0 = time.perf_counter()
+        oracle.reshape_and_cache(c.new_key, c.new_value, kc, vc, c.slot_mapping, c.pool.S)
+        oracle.decode(c.q, kc, vc, c.pool.block_tables, c.pool.context_lens, c.scale,
+                      oracle.BF16, threads=threads)
+        total += time.perf_counter() - t0
+        reps += 1
+    return {"value": round(step_bytes * reps / total / 1e9, 4), "unit": "GB/s",
+            "cores": threads, "kind": "oracle",
+            "sample": f"{reps} full steps (store + decode of all 64 sequences), "
+                      f"{total:.1f} s on {threads} threads"}
+
+
+def _time_calls(fn, n, flush, warm=3):
+    import torch
+    for _ in range(warm):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    tot = 0.0
+    for _ in range(n):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        tot += a.elapsed_time(b) * 1e-3
+    return tot / n
+
+
+def bench_prefill_mix(pd, pd_inputs, dev, args, flush, bf16_peak, hbm_peak, peak_src):
+    import torch
+    m = pd_inputs.chunked_prefill_mixed()
+    kc, vc = m.pool.key_cache.to(dev), m.pool.value_cache.to(dev)
+    nk, nv, sl = m.new_key.to(dev), m.new_value.to(dev), m.slot_mapping.to(dev)
+    q = m.q_prefill.to(dev)
+    out = torch.empty_like(q)
+    cu = m.cu_q_lens.to(dev)
+    btp, clp = m.pool.block_tables[:m.Bp].to(dev), m.pool.context_lens[:m.Bp].to(dev)
+    btd, cld = m.pool.block_tables[m.Bp:].to(dev), m.pool.context_lens[m.Bp:].to(dev)
+    qd = m.q_decode.to(dev)
+    od = torch.empty_like(qd)
+    mcl = int(cld.max())
+    ws = pd.decode_workspace(m.Bd, m.H, m.D, mcl, device=dev)
+    P = m.prior_lens.double()
+    C = (m.cu_q_lens[1:] - m.cu_q_lens[:-1]).double()
+    flops = float(4 * m.D * m.H * (C * P + C * (C + 1) / 2).sum())
+    dctx = m.pool.context_lens[m.Bp:].tolist()
+    _, dbytes = decode_alg_bytes(dctx, m.Bd, m.H, m.Hk, m.D, m.pool.S)
+    sbytes = store_alg_bytes(sl.numel(), m.Hk, m.D)
+    n = args.extra_steps
+    t_store = _time_calls(lambda: pd.pd_reshape_and_cache(nk, nv, kc, vc, sl), n, flush)
+    t_pre = _time_calls(lambda: pd.pd_paged_prefill_chunk(out, q, cu, m.max_q_len, kc, vc, btp,
+                                                          clp, m.scale), n, flush)
+    t_dec = _time_calls(lambda: pd.pd_paged_attention_decode(od, qd, kc, vc, btd, cld, mcl,
+                                                             m.scale, ws), n, flush)
+
+    def whole():
+        pd.pd_reshape_and_cache(nk, nv, kc, vc, sl)
+        pd.pd_paged_prefill_chunk(out, q, cu, m.max_q_len, kc, vc, btp, clp, m.scale)
+        pd.pd_paged_attention_decode(od, qd, kc, vc, btd, cld, mcl, m.scale, ws)
+
+    t_step = _time_calls(whole, n, flush)
+    return {"workload": "16 prefill chunks of 512 (prior U[0,8192]) + 48 decode (ctx U[256,4096])",
+            "step_ms": round(t_step * 1e3, 4),
+            "prefill_ms": round(t_pre * 1e3, 4), "prefill_gflop": round(flops / 1e9, 2),
+            "prefill_tflops": round(flops / t_pre / 1e12, 2),
+            "prefill_frac": round(flops / t_pre / 1e12 / bf16_peak, 4),
+            "prefill_peak_tflops": bf16_peak, "peak_source": peak_src,
+            "store_tokens": sl.numel(), "store_gbs": round(sbytes / t_store / 1e9, 1),
+            "decode_ms": round(t_dec * 1e3, 4), "decode_gbs": round(dbytes / t_dec / 1e9, 1),
+            "decode_frac": round(dbytes / t_dec / 1e9 / hbm_peak, 4)}
+
+
+def bench_long_context(pd, pd_inputs, dev, args, flush, hbm_peak):
+    import torch
+    res = {}
+    for point, (B, ctx) in enumerate(pd_inputs.LONG_CONTEXT_POINTS):
+        layers = []
+        for layer in range(32):
+            lc = pd_inputs.long_context_layer(point, layer, device=dev)
+            layers.append((lc.pool.key_cache, lc.pool.value_cache, lc.q))
+        bt = lc.pool.block_tables.to(dev)
+        cl = lc.pool.context_lens.to(dev)
+        outs = [torch.empty_like(x[2]) for x in layers]
+        ws = pd.decode_workspace(B, lc.H, lc.D, ctx, device=dev)
+
+        def step():
+            for (k, v, q), o in zip(layers, outs):
+                pd.pd_paged_attention_decode(o, q, k, v, bt, cl, ctx, lc.scale, ws)
+
+        t = _time_calls(step, max(3, args.extra_steps // 2), flush, warm=2)
+        kv, alg = decode_alg_bytes([ctx] * B, B, lc.H, lc.Hk, lc.D, lc.pool.S)
+        res[f"{B}x{ctx}"] = {"step_ms": round(t * 1e3, 3),
+                             "gbs": round(32 * alg / t / 1e9, 1),
+                             "frac": round(32 * alg / t / 1e9 / hbm_peak, 4),
+                             "kv_tokens_per_s": round(32 * B * ctx / t, 1),
+                             "partitions": -(-ctx // pd.pd_decode_partition_tokens(ctx))}
+        del layers, outs
+        torch.cuda.empty_cache()
+    return res
+
+
+def bench_cow(pd, pd_inputs, dev, args, flush, hbm_peak):
+    import torch
+    res = {}
+    for S in (8, 16, 32, 64):
+        fc = pd_inputs.cow_fork_stress(S)
+        bm = pd.BlockManager(fc.NB, S)
+        tables, ctxs, slots, pairs = [], [], [], []
+        nid = 0
+        for L in fc.prompt_lens.tolist():
+            parent = nid
+            nid += 1
+            bm.add_seq(parent)
+            for _ in range(L):
+                bm.append_slot(parent)
+            kids = list(range(nid, nid + fc.n_fork))
+            nid += fc.n_fork
+            for k in kids:
+                bm.fork(parent, k)
+            bm.release(parent)
+            for k in kids:
+                s, cp = bm.append_slot(k)
+                slots.append(s)
+                if cp:
+                    pairs.append(cp)
+                tables.append(bm.block_table(k))
+                ctxs.append(L + 1)
+        kc, vc = fc.key_cache.to(dev), fc.value_cache.to(dev)
+        mb = max(len(t) for t in tables)
+        bt = torch.zeros(len(tables), mb, dtype=torch.int32)
+        for i, t in enumerate(tables):
+            bt[i, :len(t)] = torch.tensor(t, dtype=torch.int32)
+        bt, cl = bt.to(dev), torch.tensor(ctxs, dtype=torch.int32, device=dev)
+        pr = torch.tensor(pairs, dtype=torch.int64, device=dev).view(-1, 2)
+        sl = torch.tensor(slots, dtype=torch.int64, device=dev)
+        nk, nv, q = fc.new_key.to(dev), fc.new_value.to(dev), fc.q.to(dev)
+        out = torch.empty_like(q)
+        mcl = max(ctxs)
+        ws = pd.decode_workspace(len(tables), fc.H, fc.D, mcl, device=dev)
+        n = args.extra_steps
+        t_copy = _time_calls(lambda: pd.pd_copy_blocks([kc], [vc], pr), n, flush)
+        t_dec = _time_calls(lambda: pd.pd_paged_attention_decode(out, q, kc, vc, bt, cl, mcl,
+                                                                 fc.scale, ws), n, flush)
+
+        def whole():
+            pd.pd_copy_blocks([kc], [vc], pr)
+            pd.pd_reshape_and_cache(nk, nv, kc, vc, sl)
+            pd.pd_paged_attention_decode(out, q, kc, vc, bt, cl, mcl, fc.scale, ws)
+
+        t_step = _time_calls(whole, n, flush)
+        _, logical = decode_alg_bytes(ctxs, len(tables), fc.H, fc.Hk, fc.D, S)
+        unique_blocks = len({b for t in tables for b in t})
+        unique = unique_blocks * S * fc.Hk * fc.D * 2 * 2
+        copy_bytes = 2 * len(pairs) * 2 * fc.Hk * S * fc.D * 2
+        res[f"S{S}"] = {"pairs": len(pairs), "step_ms": round(t_step * 1e3, 4),
+                        "copy_ms": round(t_copy * 1e3, 4),
+                        "copy_gbs": round(copy_bytes / t_copy / 1e9, 1),
+                        "decode_ms": round(t_dec * 1e3, 4),
+                        "decode_logical_gbs": round(logical / t_dec / 1e9, 1),
+                        "decode_unique_gbs": round(unique / t_dec / 1e9, 1),
+                        "decode_unique_frac": round(unique / t_dec / 1e9 / hbm_peak, 4)}
+    return res
+
+
+def run_reference(args, rank, world):
+    """The oracle (as it stands) on the host cores, on the headline workload; a
+    step = store + decode of a bounded sample of the batch's sequences."""
+    import numpy as np
+    import torch
+    import oracle
+    import pd_inputs
+    if rank != 0:
+        return None
+    c = pd_inputs.qwen3_8b_decode()
+    threads = oracle.default_threads()
+    n_seq = 16                                     # sample: the first 16 of 64 sequences
+    ctx = c.pool.context_lens[:n_seq].tolist()
+    _, dbytes = decode_alg_bytes(ctx, n_seq, c.H, c.Hk, c.D, c.pool.S)
+    sbytes = store_alg_bytes(n_seq, c.Hk, c.D)
+    kc0 = c.pool.key_cache.view(torch.int16).numpy().view(np.uint16)
+    vc0 = c.pool.value_cache.view(torch.int16).numpy().view(np.uint16)
+
+    def step():
+        kc, vc = kc0.copy(), vc0.copy()
+        t0 = time.perf_counter()
+        oracle.reshape_and_cache(c.new_key[:n_seq], c.new_value[:n_seq], kc, vc,
+                                 c.slot_mapping[:n_seq], c.pool.S)
+        oracle.decode(c.q, kc, vc, c.pool.block_tables, c.pool.context_lens, c.scale,
+                      oracle.BF16, threads=threads, rows=(0, n_seq * c.H))
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        step()
+    total = sum(step() for _ in range(args.steps))
+    value = (dbytes + sbytes) * args.steps / total / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "qwen3_8b_decode_step", "batch": 64, "q_heads": 32,
+                       "kv_heads": 8, "head_dim": 128, "block_size": 16,
+                       "context_lens": "uniform [128, 2048], seed 0",
+                       "step": f"store + decode of the first {n_seq} of 64 sequences"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle",
+                             "sample": f"first {n_seq} of 64 sequences per step"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    return line
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        result = run_ours(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(result), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
