@@ -135,6 +135,36 @@ PD_API pd_status pd_paged_attention_decode(void* out, const void* q,
                                     pd_dtype dt, int32_t* dev_err,
                                     cudaStream_t stream);
 
+/* Decode attention without any device allocation by the caller: same
+ * operation, arguments and results as pd_paged_attention_decode, minus the
+ * workspace.  The pages describe no such call; it exists for callers that
+ * cannot allocate device memory on the call path (engines that reserve all
+ * device memory at start-up and forbid later allocations, or code that must
+ * not pay cudaMalloc's implicit synchronisation).
+ * - The partition scratch is a fixed 32 MiB array inside the library; every
+ *   GPU that loads the library keeps it until the process exits.  A batch
+ *   whose pd_decode_workspace_bytes(B, H, D, max_context_len) exceeds
+ *   32 MiB (33554432 bytes) is rejected with PD_ERR_WORKSPACE_TOO_SMALL and
+ *   nothing is launched.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture on the device.
+ * - Nothing in the scratch needs to start at zero: every entry a launch
+ *   reads was written earlier in the same launch.
+ * - All calls share the one array: calls that may overlap on the GPU (other
+ *   streams, other host threads) race and must be serialised by the caller.
+ * - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+PD_API pd_status pd_paged_attention_decode_noalloc(void* out, const void* q,
+                                           const void* key_cache,
+                                           const void* value_cache,
+                                           const int32_t* block_tables,
+                                           int max_blocks_per_seq,
+                                           const int32_t* context_lens, int B,
+                                           int H, int Hk, int D, int S, int NB,
+                                           int max_context_len, float scale,
+                                           pd_dtype dt, int32_t* dev_err,
+                                           cudaStream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* Copy-on-write block copies for fork (parallel sampling, beam search):
  * tutorial page section 2.3, BlockManager.cow(): a shared block that is about

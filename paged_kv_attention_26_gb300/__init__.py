@@ -48,6 +48,8 @@ SIGNATURES = {
     "pd_decode_partition_tokens": (_I, [_I]),
     "pd_paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I,
                                        _F, _P, _SZ, _I, _P, _P]),
+    "pd_paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
+                                               _I, _I, _F, _I, _P, _P]),
     "pd_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pd_paged_prefill_chunk": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
                                     _I, _F, _I, _P, _P]),
@@ -211,6 +213,33 @@ def pd_paged_attention_decode(out, q, key_cache, value_cache, block_tables, cont
         NB, int(max_context_len), float(scale), ws_ptr, ws_bytes, dt, _opt(dev_err),
         _stream(stream))
     _check("pd_paged_attention_decode", st)
+
+
+def pd_paged_attention_decode_noalloc(out, q, key_cache, value_cache, block_tables,
+                                      context_lens, max_context_len: int, scale: float,
+                                      dev_err=None, stream=None):
+    """Decode attention that needs no workspace from the caller: the library
+    keeps a fixed 32 MiB scratch array per GPU for the partition results.
+    For callers that cannot allocate device memory on the call path.  Batches
+    whose workspace would exceed 32 MiB raise (PD_ERR_WORKSPACE_TOO_SMALL);
+    calls that overlap on the GPU share the scratch and race."""
+    torch = _torch()
+    B, H, D = q.shape
+    NB, Hk, S, D2 = key_cache.shape
+    if out.shape != q.shape or D2 != D or value_cache.shape != key_cache.shape:
+        raise ValueError("shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables / context_lens shape")
+    dt = _dt(key_cache)
+    for t in (q, out, value_cache):
+        if t.dtype != key_cache.dtype:
+            raise TypeError("dtype mismatch")
+    st = load().pd_paged_attention_decode_noalloc(
+        _dev(out, "out"), _dev(q, "q"), _dev(key_cache, "key_cache"),
+        _dev(value_cache, "value_cache"), _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), B, H, Hk, D, S,
+        NB, int(max_context_len), float(scale), dt, _opt(dev_err), _stream(stream))
+    _check("pd_paged_attention_decode_noalloc", st)
 
 
 _ptr_arrays: dict = {}
