@@ -5,7 +5,6 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
-#include <cstdlib>
 
 #include "pd_attn.h"
 #include "pd_internal.h"
@@ -26,16 +25,6 @@ pd_status launch_result(cudaError_t e) {
 }
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
-
-// PD_PREFILL_P_IN_SMEM=1 stages the softmax probabilities in shared memory
-// (two shared-memory operands) instead of tensor memory; read once.
-bool prefill_p_in_smem() {
-    static const bool v = [] {
-        const char* e = std::getenv("PD_PREFILL_P_IN_SMEM");
-        return e != nullptr && e[0] == '1';
-    }();
-    return v;
-}
 
 }  // namespace pd
 
@@ -152,7 +141,7 @@ pd_status pd_paged_prefill_chunk(void* out, const void* q, int total_q,
         return PD_ERR_UNSUPPORTED;
     PrefillArgs a{out, q, total_q, cu_q_lens, max_q_len, key_cache, value_cache, block_tables,
                   max_blocks_per_seq, context_lens, B, H, Hk, D, S, NB, scale, dt, dev_err,
-                  stream, prefill_p_in_smem()};
+                  stream};
     return launch_prefill(a);
 }
 

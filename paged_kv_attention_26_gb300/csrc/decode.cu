@@ -6,28 +6,30 @@
 //   out[i][h] = sum_{t < ctx_i} softmax_t(scale * q[i][h] . k_t) v_t,
 //   k_t, v_t read from kv head h / G through block_tables[i][t / S].
 //
-// Decode is HBM-bound (arithmetic intensity ~1 FLOP/byte per query head,
-// tutorial page section 1.1), so the design is about streaming every K/V
-// byte exactly once at full bandwidth:
-//   * grid = (kv head x head group, sequence, partition); a partition is a
-//     fixed run of PART logical tokens, so long contexts spread over many SMs;
-//   * one producer warp streams the partition's K and V block slabs (each a
-//     contiguous [S][D] run of the pool) into a 4-stage shared-memory ring
-//     with bulk copies (TMA engine, mbarrier completion): up to 64 KB in
-//     flight per CTA, three CTAs per SM;
-//   * four consumer warps share each stage: q . k with 8 lanes per token
-//     (16-byte conflict-free shared loads), a 3-step shuffle reduction that
-//     leaves each lane with one (token, head) score, online softmax in the
-//     log2 domain with lazy rescaling, and p * v with 32 lanes across D;
-//     all fp32 with packed two-wide FMAs;
-//   * the G query heads that share a kv head are processed together, so K/V
-//     are read once per kv head;
-//   * the four warps' partial results are merged in shared memory; a batch
-//     that fits one partition writes `out` directly, otherwise partial
-//     (max, sum, unnormalised output) triples go to the workspace and a
-//     reduce kernel (launched programmatically dependent) merges them in
-//     fixed partition order.  No atomics touch results: outputs are
-//     bit-identical for any placement of blocks in the pool.
+// Decode is HBM-bound (about one FLOP per byte per query head, tutorial page
+// section 1.1): the design streams every K/V byte once and keeps the
+// instruction count per byte low enough that issue never caps bandwidth.
+//  * grid = (kv head x head group, sequence, partition); a partition is a
+//    fixed run of kPart logical tokens, so long contexts spread over SMs;
+//  * one producer warp gathers the partition's K and V blocks with 2-D TMA
+//    boxes ([S tokens][64 dims], 128-byte swizzle) through the block table
+//    into a 3-stage shared-memory ring of 64-token stages (two CTAs per SM);
+//  * four consumer warps take 16 tokens of each stage.  The G query heads
+//    that share the kv head form the N = 8 side of warp-level tensor-core
+//    products (mma.sync m16n8k16, fp32 accumulation): S^T = K q^T for 16
+//    tokens, then O^T += V^T P^T.  The fragment layouts line up so each lane
+//    owns the same two heads in S and in O: the online softmax (log2 domain,
+//    lazy rescaling when a max grows by more than 2^8) needs only three
+//    shuffle steps per head pair and no broadcasts; P is transposed into
+//    operand layout with movmatrix;
+//  * P enters the product as an unevaluated pair of 16-bit values
+//    (hi = rn(p), lo = rn(p - hi)), two MMAs per tile, so P carries about
+//    2^-17 relative error instead of the 2^-9 of a single bf16;
+//  * the four warps merge in shared memory; a batch that fits one partition
+//    writes `out` directly, otherwise partial (max, sum, unnormalised o) go
+//    to the workspace and a reduce kernel, launched programmatically
+//    dependent, merges them in fixed partition order.  No atomics touch
+//    results: outputs are bit-identical for any placement of blocks.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -35,96 +37,115 @@
 
 #include "pd_device.cuh"
 #include "pd_internal.h"
+#include "pd_mma.cuh"
+#include "pd_tcgen05.cuh"
+#include "pd_tmap.h"
 
 namespace pd {
 namespace {
 
-constexpr int kPart = 256;          // tokens per partition (multiple of 64)
-constexpr int kStageTokens = 32;    // tokens per pipeline stage
-constexpr int kStages = 4;          // ring depth
-constexpr int kConsumerWarps = 4;
+constexpr int kPart = 256;          // tokens per partition (multiple of the stage)
+constexpr int kStageTokens = 64;    // tokens per pipeline stage
+constexpr int kStages = 3;          // ring depth
+constexpr int kConsumerWarps = 4;   // 16 tokens of each stage per warp
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kHeadsN = 8;          // MMA N: query heads per CTA, padded
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows > 2^8
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D, int GH>
+template <int D>
 struct DecodeSmem {
-    static constexpr int kStageBytes = kStageTokens * D * 2;
-    static constexpr int kQuadsPerWarp = kStageTokens / 4 / kConsumerWarps;
-    static constexpr int kTokPerWarp = kQuadsPerWarp * 4;
-    // layout (bytes)
+    static constexpr int kAtom = kStageTokens * 128;   // [64 tokens][64 values], 8 KB
+    static constexpr int kTile = (D / 64) * kAtom;     // one stage of K (or of V)
+    static constexpr int kFrag = (D / 16) * 4 + 4;     // per-lane merge record: o, m[2], l[2]
     static constexpr int kK = 0;
-    static constexpr int kV = kK + kStages * kStageBytes;
-    static constexpr int kP = kV + kStages * kStageBytes;             // float2 [warps][tok][GH]
-    static constexpr int kPBytes = kConsumerWarps * kTokPerWarp * GH * 8;
-    static constexpr int kM = kP + kPBytes;                           // float [warps][GH]
-    static constexpr int kL = kM + kConsumerWarps * GH * 4;           // float [warps][GH]
-    static constexpr int kBar = (kL + kConsumerWarps * GH * 4 + 15) / 16 * 16;
-    static constexpr int kMisc = kBar + 2 * kStages * 8;              // int32 flags
+    static constexpr int kV = kK + kStages * kTile;
+    static constexpr int kX = kV + kStages * kTile;    // merge exchange float [2][kFrag][32]
+    static constexpr int kBar = kX + 2 * kFrag * 32 * 4;
+    static constexpr int kMisc = kBar + 2 * kStages * 8;   // abort flag, issued count
     static constexpr int kBytes = kMisc + 16;
-    // merge buffer float [warps][GH][D] aliases the K ring after the loop
-    static_assert(kConsumerWarps * GH * D * 4 <= kStages * kStageBytes, "merge alias");
+    static constexpr int kAlloc = kBytes + 1024;           // base aligned to 1 KB in-kernel
 };
 
-template <typename T, int D, int GH>
-__global__ void __launch_bounds__(kDecodeThreads, 3)
-paged_decode_split_kernel(T* __restrict__ out, const T* __restrict__ q,
-                          const T* __restrict__ key_cache, const T* __restrict__ value_cache,
-                          const int32_t* __restrict__ block_tables, int max_blocks_per_seq,
-                          const int32_t* __restrict__ context_lens, int H, int Hk, int S,
-                          int NB, int max_context_len, float scale_log2, int num_parts_max,
-                          float* __restrict__ ws_o, float* __restrict__ ws_m,
-                          float* __restrict__ ws_l, int32_t* dev_err) {
-    using L = DecodeSmem<D, GH>;
+// Shared address of 16-byte chunk `chunk` (of D/8) of token row `tok` in a
+// stage laid out as 64-value swizzle atoms ([64 rows][128 B], chunk c of row
+// r stored at position c ^ (r % 8)).
+template <int D>
+__device__ __forceinline__ uint32_t swz(uint32_t base, int tok, int chunk) {
+    return base + (chunk >> 3) * DecodeSmem<D>::kAtom + tok * 128 +
+           (((chunk & 7) ^ (tok & 7)) << 4);
+}
+
+// A work item is (partition, sequence, unit) with unit = (kv head, head group);
+// the same enumeration drives the producer and the consumers.
+struct Item {
+    int part, seq, unit, t_begin, t_end, n_stages;
+};
+
+__device__ __forceinline__ Item decode_item(long item, int units, int B,
+                                            const int32_t* __restrict__ context_lens, int cap,
+                                            int32_t* dev_err, bool flag) {
+    Item it;
+    it.unit = int(item % units);
+    const long rest = item / units;
+    it.seq = int(rest % B);
+    it.part = int(rest / B);
+    int ctx = __ldg(context_lens + it.seq);
+    if (ctx > cap || ctx < 0) {
+        // context longer than the table / workspace promise: cut to what they hold
+        if (flag && it.part == 0 && it.unit == 0) flag_error(dev_err, PD_DEVERR_CTX_RANGE);
+        ctx = ctx < 0 ? 0 : cap;
+    }
+    it.t_begin = it.part * kPart;
+    it.t_end = min(ctx, it.t_begin + kPart);
+    it.n_stages = it.t_end > it.t_begin ? (it.t_end - it.t_begin + kStageTokens - 1) / kStageTokens
+                                        : 0;
+    return it;
+}
+
+// OR of `pred` over the consumer warps (named barrier 1), uniform result.
+__device__ __forceinline__ bool consumers_any(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r) : "r"(uint32_t(pred)), "n"(kConsumerWarps * 32) : "memory");
+    return r != 0;
+}
+
+// Persistent: each CTA walks items blockIdx.x, blockIdx.x + gridDim.x, ...
+template <typename T, int D>
+__global__ void __launch_bounds__(kDecodeThreads, 2)
+paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, T* __restrict__ out,
+                          const T* __restrict__ q, const int32_t* __restrict__ block_tables,
+                          int max_blocks_per_seq, const int32_t* __restrict__ context_lens,
+                          int B, int H, int Hk, int S, int NB, int GH, float scale_log2,
+                          int num_parts_max, float* __restrict__ ws_o,
+                          float* __restrict__ ws_m, float* __restrict__ ws_l,
+                          int32_t* dev_err) {
+    using L = DecodeSmem<D>;
     using E = Elem<T>;
-    extern __shared__ __align__(128) unsigned char smem[];
-    T* k_ring = reinterpret_cast<T*>(smem + L::kK);
-    T* v_ring = reinterpret_cast<T*>(smem + L::kV);
-    float2* pbuf = reinterpret_cast<float2*>(smem + L::kP);
-    float* red_m = reinterpret_cast<float*>(smem + L::kM);
-    float* red_l = reinterpret_cast<float*>(smem + L::kL);
-    float* red_o = reinterpret_cast<float*>(smem + L::kK);
+    constexpr int kAtoms = D / 64;
+    constexpr int KS = D / 16;      // k-steps of q.k, m-tiles of p.v
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* xchg = reinterpret_cast<float*>(smem + L::kX);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
     uint64_t* empty = full + kStages;
     volatile int32_t* abort_flag = reinterpret_cast<int32_t*>(smem + L::kMisc);
-    int32_t* issued = reinterpret_cast<int32_t*>(smem + L::kMisc + 4);
+    volatile int32_t* issued = reinterpret_cast<int32_t*>(smem + L::kMisc + 4);
 
     pdl_launch_dependents();
 
     const int G = H / Hk;
     const int groups = G / GH;
-    const int kvh = blockIdx.x / groups;
-    const int h0 = kvh * G + (blockIdx.x % groups) * GH;   // first q head of this CTA
-    const int seq = blockIdx.y;
-    const int part = blockIdx.z;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // Context of this sequence, cut to what the table and the workspace hold.
-    int ctx = __ldg(context_lens + seq);
+    const int units = Hk * groups;
+    const long n_items = long(num_parts_max) * B * units;
     const int cap = min(max_blocks_per_seq * S, num_parts_max * kPart);
-    if (ctx > cap || ctx < 0) {
-        if (threadIdx.x == 0 && blockIdx.x == 0 && part == 0) flag_error(dev_err, PD_DEVERR_CTX_RANGE);
-        ctx = ctx < 0 ? 0 : cap;
-    }
-    const int t_begin = part * kPart;
     const bool direct = (num_parts_max == 1);
-    if (t_begin >= ctx) {
-        // Nothing to attend to.  A zero-length context still owes zeros.
-        if (part == 0 && direct) {
-            for (int idx = threadIdx.x; idx < GH * D / 2; idx += kDecodeThreads) {
-                const int h = idx / (D / 2), d2 = idx % (D / 2);
-                reinterpret_cast<uint32_t*>(out + ((int64_t)seq * H + h0 + h) * D)[d2] = 0u;
-            }
-        }
-        if (part == 0 && !direct && threadIdx.x < GH) {
-            const int64_t r = ((int64_t)seq * H + h0 + threadIdx.x) * num_parts_max;
-            ws_m[r] = -INFINITY;   // the reduce kernel sees an empty row
-            ws_l[r] = 0.f;
-        }
-        return;
-    }
-    const int t_end = min(ctx, t_begin + kPart);
-    const int n_stages = (t_end - t_begin + kStageTokens - 1) / kStageTokens;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -134,294 +155,297 @@ paged_decode_split_kernel(T* __restrict__ out, const T* __restrict__ q,
         *abort_flag = 0;
         *issued = 0;
         fence_mbar_init();
+        tc::prefetch_tmap(&tm_k);
+        tc::prefetch_tmap(&tm_v);
     }
     __syncthreads();
 
-    const int32_t* bt_row = block_tables + (int64_t)seq * max_blocks_per_seq;
-
     if (warp == kConsumerWarps) {
-        // ---------------- producer warp ----------------
-        const int chunk = S < kStageTokens ? S : kStageTokens;    // tokens per bulk copy
-        const uint32_t chunk_bytes = uint32_t(chunk) * D * 2;
-        for (int st = 0; st < n_stages; ++st) {
-            const int slot = st % kStages;
-            // every lane waits (acquire), then the warp agrees on the outcome
-            const bool ok = __all_sync(0xffffffffu, st < kStages ||
-                                       mbar_wait(&empty[slot], ((st / kStages) - 1) & 1));
-            if (!ok) {
-                if (lane == 0) {
-                    flag_error(dev_err, PD_DEVERR_TIMEOUT);
-                    *abort_flag = 1;
+        // ---------------- producer warp: streams stages across items ----------------
+        const uint32_t block_bytes = uint32_t(S) * D * 2;        // one [S][D] slab
+        uint32_t gs = 0;                                         // stages issued so far
+        bool stop = false;
+        for (long item = blockIdx.x; item < n_items && !stop; item += gridDim.x) {
+            const Item it = decode_item(item, units, B, context_lens, cap, dev_err, false);
+            if (it.n_stages == 0) continue;
+            const int kvh = it.unit / groups;
+            const int32_t* bt_row = block_tables + (int64_t)it.seq * max_blocks_per_seq;
+            for (int st = 0; st < it.n_stages; ++st, ++gs) {
+                const int slot = gs % kStages;
+                // every lane waits (acquire), then the warp agrees on the outcome
+                const bool ok = __all_sync(0xffffffffu, gs < kStages ||
+                                           mbar_wait(&empty[slot], ((gs / kStages) - 1) & 1));
+                if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) {
+                    if (lane == 0 && !ok) {
+                        flag_error(dev_err, PD_DEVERR_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    stop = true;
+                    break;
                 }
-                break;
-            }
-            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-            const int t0 = t_begin + st * kStageTokens;
-            const int nt = min(kStageTokens, t_end - t0);
-            const int nchunks = (nt + chunk - 1) / chunk;
-            int64_t src = -1;
-            if (lane < nchunks) {
-                const int t = t0 + lane * chunk;
-                const int blk = __ldg(bt_row + t / S);
-                if (blk >= 0 && blk < NB) {
-                    src = (((int64_t)blk * Hk + kvh) * S + (t % S)) * D;
-                } else {
-                    flag_error(dev_err, PD_DEVERR_BLOCK_RANGE);
+                const int t0 = it.t_begin + st * kStageTokens;
+                const int nt = min(kStageTokens, it.t_end - t0);
+                const int nblk = (nt + S - 1) / S;             // <= 64 / S <= 8
+                int row = -1;
+                if (lane < nblk) {
+                    const int blk = __ldg(bt_row + t0 / S + lane);
+                    if (blk >= 0 && blk < NB) {
+                        row = (blk * Hk + kvh) * S;
+                    } else {
+                        flag_error(dev_err, PD_DEVERR_BLOCK_RANGE);
+                    }
                 }
+                const uint32_t ok_mask = __ballot_sync(0xffffffffu, row >= 0);
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&full[slot], 2u * block_bytes * __popc(ok_mask));
+                __syncwarp();
+                if (row >= 0) {
+#pragma unroll
+                    for (int a = 0; a < kAtoms; ++a) {
+                        const int off = slot * L::kTile + a * L::kAtom + lane * S * 128;
+                        tc::tma_load_2d(smem + L::kK + off, &tm_k, a * 64, row, &full[slot]);
+                        tc::tma_load_2d(smem + L::kV + off, &tm_v, a * 64, row, &full[slot]);
+                    }
+                }
+                if (lane == 0) *issued = int(gs + 1);
             }
-            const uint32_t ok_mask = __ballot_sync(0xffffffffu, src >= 0);
-            if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2u * chunk_bytes * __popc(ok_mask));
-            __syncwarp();
-            if (src >= 0) {
-                bulk_g2s(k_ring + slot * kStageTokens * D + lane * chunk * D, key_cache + src,
-                         chunk_bytes, &full[slot]);
-                bulk_g2s(v_ring + slot * kStageTokens * D + lane * chunk * D, value_cache + src,
-                         chunk_bytes, &full[slot]);
-            }
-            if (lane == 0) *issued = st + 1;
         }
         return;
     }
 
     // ---------------- consumer warps ----------------
-    constexpr int DQ = D / 8;          // dims per lane for q . k
-    constexpr int CHQ = DQ / 8;        // 16-byte chunks per lane (2 or 1)
-    constexpr int DV = D / 32;         // dims per lane for p * v (4 or 2)
-    const int tg = lane >> 3;          // token within a quad
-    const int j = lane & 7;            // lane within the token group
+    const int j8 = lane >> 3, r8 = lane & 7;     // ldmatrix: matrix index, row within it
+    const int tb = warp * 16;                    // this warp's tokens within a stage
+    const uint32_t k_base0 = smem_u32(smem + L::kK);
+    const uint32_t v_base0 = smem_u32(smem + L::kV);
+    const float2 neg1 = make_float2(-1.f, -1.f);
+    uint32_t gs = 0;                             // stages consumed so far
+    bool aborted = false;
 
-    // q (scaled into the log2 domain) for this lane's dims: chunk c = j + 8k.
-    float2 qr[GH][CHQ][4];
+    for (long item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const Item it = decode_item(item, units, B, context_lens, cap, dev_err, warp == 0);
+        const int kvh = it.unit / groups;
+        const int h0 = kvh * G + (it.unit % groups) * GH;     // first q head of this unit
+        if (it.n_stages == 0) {
+            // Nothing to attend to.  A zero-length context still owes zeros.
+            if (it.part == 0 && warp == 0) {
+                if (direct) {
+                    for (int idx = lane; idx < GH * D / 2; idx += 32) {
+                        const int h = idx / (D / 2), d2 = idx % (D / 2);
+                        reinterpret_cast<uint32_t*>(out + ((int64_t)it.seq * H + h0 + h) * D)[d2] = 0u;
+                    }
+                } else if (lane < GH) {
+                    const int64_t r = ((int64_t)it.seq * H + h0 + lane) * num_parts_max;
+                    ws_m[r] = -INFINITY;     // the reduce kernel sees an empty row
+                    ws_l[r] = 0.f;
+                }
+            }
+            continue;
+        }
+        // q^T as the MMA B operand: lane holds head lane/4, dims 16ks + 2(lane%4) + {0,1}
+        // (register 0) and the same + 8 (register 1); heads past GH are zero.
+        uint32_t qb[KS][2];
+        {
+            const int n = lane >> 2;
+            const T* qrow = q + ((int64_t)it.seq * H + h0 + n) * D + 2 * (lane & 3);
 #pragma unroll
-    for (int h = 0; h < GH; ++h) {
-        const uint4* qrow = reinterpret_cast<const uint4*>(q + ((int64_t)seq * H + h0 + h) * D);
-#pragma unroll
-        for (int k = 0; k < CHQ; ++k) {
-            const uint4 w = __ldg(qrow + j + 8 * k);
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = E::unpack2(ww[e]);
-                qr[h][k][e] = make_float2(f.x * scale_log2, f.y * scale_log2);
+            for (int ks = 0; ks < KS; ++ks) {
+                qb[ks][0] = n < GH ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks)) : 0u;
+                qb[ks][1] =
+                    n < GH ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8)) : 0u;
             }
         }
-    }
-    // head whose full score this lane holds after the shuffle reduction
-    const int my_h = GH == 4 ? (((j >> 2) & 1) * 2 + ((j >> 1) & 1)) : (GH == 2 ? ((j >> 2) & 1) : 0);
-
-    float m_run[GH];
-    float2 acc[GH][DV / 2];
+        // O^T fragments: m-tile mt covers dims 16mt..16mt+15; lane holds dims
+        // 16mt + lane/4 (regs 0,1) and + 8 (regs 2,3), heads 2(lane%4) and + 1.
+        float o[KS][4];
 #pragma unroll
-    for (int h = 0; h < GH; ++h) {
-        m_run[h] = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < DV / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
-    }
-    float l_lane = 0.f;
-    float2* my_pbuf = pbuf + warp * L::kTokPerWarp * GH;
+        for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        float m_run[2] = {-INFINITY, -INFINITY};
+        float l_run[2] = {0.f, 0.f};
 
-    int st = 0;
-    for (; st < n_stages; ++st) {
-        const int slot = st % kStages;
-        if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (st / kStages) & 1))) {
-            if (lane == 0) {
-                flag_error(dev_err, PD_DEVERR_TIMEOUT);
-                *abort_flag = 1;
+        for (int st = 0; st < it.n_stages; ++st, ++gs) {
+            const int slot = gs % kStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (gs / kStages) & 1))) {
+                if (lane == 0) {
+                    flag_error(dev_err, PD_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                aborted = true;
+                break;                   // skip the item's other stages
             }
+            const int nt = min(kStageTokens, it.t_end - (it.t_begin + st * kStageTokens));
+            if (tb < nt) {
+                const uint32_t kb = k_base0 + slot * L::kTile;
+                const uint32_t vb = v_base0 + slot * L::kTile;
+                const bool partial = tb + 16 > nt;
+                if (partial) {
+                    // V rows past the partition end hold other data or were never
+                    // loaded this round: zero them so that 0 * v stays 0.
+                    unsigned char* vrow = smem + L::kV + slot * L::kTile;
+                    for (int i = lane; i < 16 * kAtoms * 8; i += 32) {
+                        const int tok = tb + i / (kAtoms * 8);
+                        if (tok >= nt) {
+                            const int a = (i / 8) % kAtoms, c = i % 8;
+                            *reinterpret_cast<uint4*>(vrow + a * L::kAtom + tok * 128 + c * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                    __syncwarp();
+                }
+                // ---- S^T[16 tokens][8 heads] = K q^T (two accumulators for ILP)
+                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    uint32_t a[4];
+                    wmma16::ldsm_x4(a, swz<D>(kb, tb + r8 + 8 * (j8 & 1), 2 * ks + (j8 >> 1)));
+                    wmma16::Mma<T>::run(acc[ks & 1], a, qb[ks][0], qb[ks][1]);
+                }
+                // lane holds tokens tb + lane/4 (0,1) and + 8 (2,3); heads 2(lane%4) + {0,1}
+                const int tok0 = tb + (lane >> 2);
+                float x[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int tok = tok0 + (i >> 1) * 8;
+                    x[i] = tok < nt ? (acc[0][i] + acc[1][i]) * scale_log2 : -INFINITY;
+                }
+                // ---- online softmax per head (lane-local state, 3 shuffles per head)
+                float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
+                    mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (mx[h] > m_run[h] + kRescaleThreshold) {
+                        const float alpha = ex2(m_run[h] - mx[h]);   // 0 the first time
+                        m_run[h] = mx[h];
+                        l_run[h] *= alpha;
+#pragma unroll
+                        for (int mt = 0; mt < KS; ++mt) {
+                            o[mt][h] *= alpha;
+                            o[mt][2 + h] *= alpha;
+                        }
+                    }
+                }
+                const float p0 = ex2(x[0] - m_run[0]), p1 = ex2(x[1] - m_run[1]);
+                const float p2 = ex2(x[2] - m_run[0]), p3 = ex2(x[3] - m_run[1]);
+                l_run[0] += p0 + p2;
+                l_run[1] += p1 + p3;
+                // P as hi + lo 16-bit pairs, transposed into B-operand layout
+                const uint32_t hi0 = E::pack2(p0, p1), hi1 = E::pack2(p2, p3);
+                const float2 lo0 = ffma2(E::unpack2(hi0), neg1, make_float2(p0, p1));
+                const float2 lo1 = ffma2(E::unpack2(hi1), neg1, make_float2(p2, p3));
+                const uint32_t bh0 = wmma16::movm_t(hi0), bh1 = wmma16::movm_t(hi1);
+                const uint32_t bl0 = wmma16::movm_t(E::pack2(lo0.x, lo0.y));
+                const uint32_t bl1 = wmma16::movm_t(E::pack2(lo1.x, lo1.y));
+                // ---- O^T[dims][heads] += V^T P^T
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    uint32_t a[4];
+                    wmma16::ldsm_x4_t(a, swz<D>(vb, tb + r8 + 8 * (j8 >> 1), 2 * mt + (j8 & 1)));
+                    wmma16::Mma<T>::run(o[mt], a, bh0, bh1);
+                    wmma16::Mma<T>::run(o[mt], a, bl0, bl1);
+                }
+                if (partial) tc::fence_proxy_async_smem();   // zeros before the next TMA write
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+        // All four consumer warps decide together whether to go on: a warp
+        // that gave up still arrives here, so named-barrier counts stay matched.
+        if (consumers_any(aborted || *abort_flag != 0)) {
+            aborted = true;
             break;
         }
-        const int nt = min(kStageTokens, t_end - (t_begin + st * kStageTokens));
-        const T* ks = k_ring + slot * kStageTokens * D;
-        const T* vs = v_ring + slot * kStageTokens * D;
 
-        // ---- scores for this warp's tokens: quads warp, warp + 4, ...
-        float s[L::kQuadsPerWarp];
+        // ---- merge the four warps in registers through a fragment-order buffer:
+        // warps 2, 3 hand over to 0, 1, then warp 1 to warp 0.
 #pragma unroll
-        for (int qd = 0; qd < L::kQuadsPerWarp; ++qd) {
-            const int tq = (warp + kConsumerWarps * qd) * 4 + tg;
-            float part_s[GH];
-            if ((warp + kConsumerWarps * qd) * 4 < nt) {
-                float2 a[GH];
+        for (int h = 0; h < 2; ++h) {
+            l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 4);
+            l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 8);
+            l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 16);
+        }
+        auto put = [&](int buf) {
+            float* x = xchg + buf * L::kFrag * 32 + lane;
 #pragma unroll
-                for (int h = 0; h < GH; ++h) a[h] = make_float2(0.f, 0.f);
-                const uint4* krow = reinterpret_cast<const uint4*>(ks + tq * D);
+            for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-                for (int k = 0; k < CHQ; ++k) {
-                    const uint4 w = krow[j + 8 * k];
-                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                for (int e = 0; e < 4; ++e) x[(mt * 4 + e) * 32] = o[mt][e];
+            x[(KS * 4 + 0) * 32] = m_run[0];
+            x[(KS * 4 + 1) * 32] = m_run[1];
+            x[(KS * 4 + 2) * 32] = l_run[0];
+            x[(KS * 4 + 3) * 32] = l_run[1];
+        };
+        auto take = [&](int buf) {
+            const float* x = xchg + buf * L::kFrag * 32 + lane;
+            float c_mine[2], c_other[2];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 kf = E::unpack2(ww[e]);
+            for (int h = 0; h < 2; ++h) {
+                const float mo = x[(KS * 4 + h) * 32], lo = x[(KS * 4 + 2 + h) * 32];
+                const float M = fmaxf(m_run[h], mo);
+                c_mine[h] = m_run[h] == -INFINITY ? 0.f : ex2(m_run[h] - M);
+                c_other[h] = mo == -INFINITY ? 0.f : ex2(mo - M);
+                l_run[h] = l_run[h] * c_mine[h] + lo * c_other[h];
+                m_run[h] = M;
+            }
 #pragma unroll
-                        for (int h = 0; h < GH; ++h) a[h] = ffma2(qr[h][k][e], kf, a[h]);
+            for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    o[mt][e] = o[mt][e] * c_mine[e & 1] + x[(mt * 4 + e) * 32] * c_other[e & 1];
+        };
+        if (warp >= 2) put(warp - 2);
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+        if (warp < 2) take(warp);
+        if (warp == 1) {
+            __syncwarp();
+            put(1);                      // own partner slot, already read by this warp
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+        if (warp == 0) {
+            take(1);
+            // lane: heads ha, ha + 1; dims 16mt + lane/4 and + 8
+            const int ha = 2 * (lane & 3), d0 = lane >> 2;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int hh = ha + h;
+                if (hh >= GH) continue;
+                const int hq = h0 + hh;
+                if (direct) {
+                    const float inv = 1.f / l_run[h];
+                    T* orow = out + ((int64_t)it.seq * H + hq) * D + d0;
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        orow[16 * mt] = T(o[mt][h] * inv);
+                        orow[16 * mt + 8] = T(o[mt][2 + h] * inv);
                     }
-                }
+                } else {
+                    const int64_t r = ((int64_t)it.seq * H + hq) * num_parts_max + it.part;
+                    float* wrow = ws_o + r * D + d0;
 #pragma unroll
-                for (int h = 0; h < GH; ++h) part_s[h] = a[h].x + a[h].y;
-            } else {
-#pragma unroll
-                for (int h = 0; h < GH; ++h) part_s[h] = 0.f;
-            }
-            // reduce over the 8 lanes of the token group; lane keeps head my_h
-            float r;
-            if constexpr (GH == 4) {
-                const bool b2 = (j >> 2) & 1, b1 = (j >> 1) & 1;
-                const float send0 = b2 ? part_s[0] : part_s[2];
-                const float send1 = b2 ? part_s[1] : part_s[3];
-                const float keep0 = b2 ? part_s[2] : part_s[0];
-                const float keep1 = b2 ? part_s[3] : part_s[1];
-                const float t0 = keep0 + __shfl_xor_sync(0xffffffffu, send0, 4);
-                const float t1 = keep1 + __shfl_xor_sync(0xffffffffu, send1, 4);
-                const float send = b1 ? t0 : t1;
-                const float keep = b1 ? t1 : t0;
-                r = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-                r += __shfl_xor_sync(0xffffffffu, r, 1);
-            } else if constexpr (GH == 2) {
-                const bool b2 = (j >> 2) & 1;
-                const float send = b2 ? part_s[0] : part_s[1];
-                const float keep = b2 ? part_s[1] : part_s[0];
-                r = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-                r += __shfl_xor_sync(0xffffffffu, r, 2);
-                r += __shfl_xor_sync(0xffffffffu, r, 1);
-            } else {
-                r = part_s[0];
-                r += __shfl_xor_sync(0xffffffffu, r, 4);
-                r += __shfl_xor_sync(0xffffffffu, r, 2);
-                r += __shfl_xor_sync(0xffffffffu, r, 1);
-            }
-            s[qd] = tq < nt ? r : -INFINITY;
-        }
-
-        // ---- online softmax (log2 domain), lazy rescale
-        float mx = s[0];
-#pragma unroll
-        for (int qd = 1; qd < L::kQuadsPerWarp; ++qd) mx = fmaxf(mx, s[qd]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        bool grow = false;
-        float m_new[GH];
-#pragma unroll
-        for (int h = 0; h < GH; ++h) {
-            const int src_lane = GH == 4 ? ((h >> 1) * 4 + (h & 1) * 2) : (GH == 2 ? h * 4 : 0);
-            const float mh = __shfl_sync(0xffffffffu, mx, src_lane);
-            m_new[h] = mh > m_run[h] + kRescaleThreshold ? mh : m_run[h];
-            grow |= m_new[h] != m_run[h];
-        }
-        if (grow) {   // warp-uniform: every lane holds the same m_run / m_new
-            float alpha_mine = 1.f;
-#pragma unroll
-            for (int h = 0; h < GH; ++h) {
-                const float alpha = ex2(m_run[h] - m_new[h]);
-                const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-                for (int e = 0; e < DV / 2; ++e) acc[h][e] = fmul2(acc[h][e], a2);
-                if (h == my_h) alpha_mine = alpha;
-                m_run[h] = m_new[h];
-            }
-            l_lane *= alpha_mine;
-        }
-        float m_mine = m_run[0];
-#pragma unroll
-        for (int h = 1; h < GH; ++h) if (h == my_h) m_mine = m_run[h];
-        // A warp that has not seen a valid token yet keeps max -inf; its
-        // scores are all -inf too and must give p = 0, not 2^(-inf + inf).
-        if (m_mine == -INFINITY) m_mine = 0.f;
-#pragma unroll
-        for (int qd = 0; qd < L::kQuadsPerWarp; ++qd) {
-            const float p = ex2(s[qd] - m_mine);   // 0 for masked tokens
-            l_lane += p;
-            if ((j & ((8 / GH) - 1)) == 0)
-                my_pbuf[(qd * 4 + tg) * GH + my_h] = make_float2(p, p);
-        }
-        __syncwarp();
-
-        // ---- p * v: lane owns dims [lane*DV, lane*DV + DV)
-#pragma unroll
-        for (int qd = 0; qd < L::kQuadsPerWarp; ++qd) {
-            const int tbase = (warp + kConsumerWarps * qd) * 4;
-            if (tbase >= nt) break;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (tbase + u < nt) {
-                    float2 vf[DV / 2];
-                    if constexpr (DV == 4) {
-                        const uint2 w = reinterpret_cast<const uint2*>(vs + (tbase + u) * D)[lane];
-                        vf[0] = E::unpack2(w.x);
-                        vf[1] = E::unpack2(w.y);
-                    } else {
-                        const uint32_t w = reinterpret_cast<const uint32_t*>(vs + (tbase + u) * D)[lane];
-                        vf[0] = E::unpack2(w);
+                    for (int mt = 0; mt < KS; ++mt) {
+                        wrow[16 * mt] = o[mt][h];
+                        wrow[16 * mt + 8] = o[mt][2 + h];
                     }
-                    const float2* pp = my_pbuf + (qd * 4 + u) * GH;
-#pragma unroll
-                    for (int h = 0; h < GH; ++h) {
-                        const float2 p2 = pp[h];
-#pragma unroll
-                        for (int e = 0; e < DV / 2; ++e) acc[h][e] = ffma2(p2, vf[e], acc[h][e]);
+                    if (d0 == 0) {
+                        ws_m[r] = m_run[h];
+                        ws_l[r] = l_run[h];
                     }
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
+        // the exchange buffer is rewritten by the next item's merge
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
     }
 
-    // Named barrier over the consumer warps only (the producer has left).
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-    if (*abort_flag) {
+    if (aborted) {
         // Let copies already issued into the ring land before the CTA exits.
         if (threadIdx.x == 0) {
             const int n_issued = *issued;
-            for (int s2 = st; s2 < n_issued; ++s2)
+            for (int s2 = int(gs); s2 < n_issued; ++s2)
                 if (!mbar_wait(&full[s2 % kStages], (s2 / kStages) & 1)) break;
-        }
-        return;
-    }
-
-    // ---- merge the four warps: m, l per head; o per (head, dim)
-    // l over the token groups (lanes xor 8, 16) for this lane's head
-    l_lane += __shfl_xor_sync(0xffffffffu, l_lane, 8);
-    l_lane += __shfl_xor_sync(0xffffffffu, l_lane, 16);
-    if (lane < 8 && (j & ((8 / GH) - 1)) == 0) red_l[warp * GH + my_h] = l_lane;
-    if (lane == 0) {
-#pragma unroll
-        for (int h = 0; h < GH; ++h) red_m[warp * GH + h] = m_run[h];
-    }
-#pragma unroll
-    for (int h = 0; h < GH; ++h) {
-#pragma unroll
-        for (int e = 0; e < DV / 2; ++e)
-            reinterpret_cast<float2*>(red_o + (warp * GH + h) * D + lane * DV)[e] = acc[h][e];
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-
-    for (int idx = threadIdx.x; idx < GH * D / 2; idx += kConsumerWarps * 32) {
-        const int h = idx / (D / 2), d = (idx % (D / 2)) * 2;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * GH + h]);
-        float lsum = 0.f, o0 = 0.f, o1 = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            const float mw = red_m[w * GH + h];
-            const float c = mw == -INFINITY ? 0.f : ex2(mw - M);
-            lsum += red_l[w * GH + h] * c;
-            const float2 ow = *reinterpret_cast<const float2*>(red_o + (w * GH + h) * D + d);
-            o0 += ow.x * c;
-            o1 += ow.y * c;
-        }
-        const int hq = h0 + h;
-        if (direct) {
-            const float inv = 1.f / lsum;
-            reinterpret_cast<uint32_t*>(out + ((int64_t)seq * H + hq) * D)[d / 2] =
-                E::pack2(o0 * inv, o1 * inv);
-        } else {
-            const int64_t r = ((int64_t)seq * H + hq) * num_parts_max + part;
-            *reinterpret_cast<float2*>(ws_o + r * D + d) = make_float2(o0, o1);
-            if (d == 0) {
-                ws_m[r] = M;
-                ws_l[r] = lsum;
-            }
         }
     }
 }
@@ -497,19 +521,41 @@ WsLayout ws_layout(int B, int H, int D, int P) {
     return w;
 }
 
-template <typename T, int D, int GH>
+int sm_count(int dev) {
+    static int counts[64] = {};
+    if (dev < 0 || dev >= 64) return 148;
+    if (counts[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
+template <typename T, int D>
 pd_status launch_decode_t(const DecodeArgs& a) {
-    using Lt = DecodeSmem<D, GH>;
+    using Lt = DecodeSmem<D>;
     const int P = decode_num_partitions(a.max_context_len);
-    const int groups = (a.H / a.Hk) / GH;
-    auto kern = paged_decode_split_kernel<T, D, GH>;
+    const int G = a.H / a.Hk;
+    int GH = 1;                          // largest divisor of G that fits N = 8
+    for (int g = std::min(G, kHeadsN); g >= 1; --g)
+        if (G % g == 0) { GH = g; break; }
+    const int groups = G / GH;
+    CUtensorMap tm_k, tm_v;
+    const unsigned long long rows = (unsigned long long)a.NB * a.Hk * a.S;
+    if (rows > 0x7fffffffull) return PD_ERR_UNSUPPORTED;   // TMA row coordinate is int32
+    if (!encode_pool_map(&tm_k, a.key_cache, D, rows, a.S, a.dt) ||
+        !encode_pool_map(&tm_v, a.value_cache, D, rows, a.S, a.dt))
+        return launch_result(cudaErrorInvalidValue);
+    auto kern = paged_decode_split_kernel<T, D>;
     static uint64_t attr_set = 0;   // one bit per device; benign if raced
     int dev = 0;
     cudaError_t e0 = cudaGetDevice(&dev);
     if (e0 != cudaSuccess) return launch_result(e0);
     if (dev >= 64 || !((attr_set >> dev) & 1)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Lt::kBytes);
+                                             Lt::kAlloc);
         if (e != cudaSuccess) return launch_result(e);
         if (dev < 64) attr_set |= uint64_t(1) << dev;
     }
@@ -524,12 +570,14 @@ pd_status launch_decode_t(const DecodeArgs& a) {
         ws_l = reinterpret_cast<float*>(base + w.l);
     }
     const float scale_log2 = a.scale * kLog2e;
-    dim3 grid(unsigned(a.Hk * groups), unsigned(a.B), unsigned(P));
-    kern<<<grid, kDecodeThreads, Lt::kBytes, a.stream>>>(
-        static_cast<T*>(a.out), static_cast<const T*>(a.q), static_cast<const T*>(a.key_cache),
-        static_cast<const T*>(a.value_cache), a.block_tables, a.max_blocks_per_seq,
-        a.context_lens, a.H, a.Hk, a.S, a.NB, a.max_context_len, scale_log2, P, ws_o, ws_m,
-        ws_l, a.dev_err);
+    // Persistent grid: two CTAs per SM (shared memory bound), never more CTAs
+    // than work items.
+    const long n_items = long(P) * a.B * a.Hk * groups;
+    const long grid = std::min<long>(n_items, 2L * sm_count(dev));
+    kern<<<unsigned(grid), kDecodeThreads, Lt::kAlloc, a.stream>>>(
+        tm_k, tm_v, static_cast<T*>(a.out), static_cast<const T*>(a.q), a.block_tables,
+        a.max_blocks_per_seq, a.context_lens, a.B, a.H, a.Hk, a.S, a.NB, GH, scale_log2, P,
+        ws_o, ws_m, ws_l, a.dev_err);
     pd_status st = launch_result(cudaGetLastError());
     if (st != PD_OK || P == 1) return st;
 
@@ -537,8 +585,8 @@ pd_status launch_decode_t(const DecodeArgs& a) {
     // launch overlaps the split kernel's tail.
     const int cap = std::min(a.max_blocks_per_seq * a.S, P * kPart);
     cudaLaunchConfig_t cfg = {};
-    const int64_t rows = int64_t(a.B) * a.H;
-    cfg.gridDim = dim3(unsigned((rows + kReduceWarps - 1) / kReduceWarps));
+    const int64_t nrows = int64_t(a.B) * a.H;
+    cfg.gridDim = dim3(unsigned((nrows + kReduceWarps - 1) / kReduceWarps));
     cfg.blockDim = dim3(kReduceWarps * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = a.stream;
@@ -553,14 +601,6 @@ pd_status launch_decode_t(const DecodeArgs& a) {
                                        static_cast<const float*>(ws_m),
                                        static_cast<const float*>(ws_l));
     return launch_result(e);
-}
-
-template <typename T, int D>
-pd_status launch_decode_d(const DecodeArgs& a) {
-    const int G = a.H / a.Hk;
-    if (G % 4 == 0) return launch_decode_t<T, D, 4>(a);
-    if (G % 2 == 0) return launch_decode_t<T, D, 2>(a);
-    return launch_decode_t<T, D, 1>(a);
 }
 
 }  // namespace
@@ -583,10 +623,10 @@ size_t decode_workspace_bytes(int B, int H, int D, int max_context_len) {
 
 pd_status launch_decode(const DecodeArgs& a) {
     if (a.dt == PD_BF16) {
-        return a.D == 128 ? launch_decode_d<__nv_bfloat16, 128>(a)
-                          : launch_decode_d<__nv_bfloat16, 64>(a);
+        return a.D == 128 ? launch_decode_t<__nv_bfloat16, 128>(a)
+                          : launch_decode_t<__nv_bfloat16, 64>(a);
     }
-    return a.D == 128 ? launch_decode_d<__half, 128>(a) : launch_decode_d<__half, 64>(a);
+    return a.D == 128 ? launch_decode_t<__half, 128>(a) : launch_decode_t<__half, 64>(a);
 }
 
 }  // namespace pd

@@ -69,11 +69,9 @@ struct PrefillArgs {
     pd_dtype dt;
     int32_t* dev_err;
     cudaStream_t stream;
-    bool p_in_smem;   // probabilities staged in shared memory instead of tensor memory
 };
 pd_status launch_prefill(const PrefillArgs& a);
 
 void count_launch();
-bool prefill_p_in_smem();
 
 }  // namespace pd

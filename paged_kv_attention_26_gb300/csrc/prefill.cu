@@ -23,8 +23,12 @@
 //    memory where the softmax wrote it over S;
 //  * warps 2-5 (one query row per thread) run the online softmax in the
 //    log2 domain with lazy rescaling (the accumulator O is rescaled only when
-//    a row max grows by more than 2^8), write P as 16-bit values, and finally
-//    normalise O and store it.
+//    a row max grows by more than 2^8) and finally normalise O and store it;
+//  * P is carried as an unevaluated sum of two 16-bit values, hi = rn(p) and
+//    lo = rn(p - hi), both written over the S row (64 + 64 columns) and
+//    applied by two PV passes.  A single 16-bit P carries a relative error of
+//    up to 2^-9 (bf16), which near-zero outputs of short contexts cannot
+//    absorb; the pair brings it to about 2^-17.
 // Every wait is bounded; a wait that runs out flags PD_DEVERR_TIMEOUT and the
 // CTA drains its in-flight copies and MMAs, frees tensor memory and leaves.
 #include <cuda.h>
@@ -37,6 +41,7 @@
 #include "pd_device.cuh"
 #include "pd_internal.h"
 #include "pd_tcgen05.cuh"
+#include "pd_tmap.h"
 
 namespace pd {
 namespace {
@@ -51,18 +56,16 @@ constexpr uint32_t kTmemO = 256;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D, bool kPInTmem>
+template <int D>
 struct PrefillSmem {
     static constexpr int kAtom = kTileM * 128;          // 128 rows x 128 B (64 16-bit values)
     static constexpr int kTile = (D / 64) * kAtom;      // a [128][D] tile
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + kTile;                // kKVStages tiles
     static constexpr int kV = kK + kKVStages * kTile;
-    static constexpr int kP = kV + kKVStages * kTile;    // P tiles [128][128] (smem variant)
-    static constexpr int kPBytes = kPInTmem ? 0 : 2 * kTileM * kTileN * 2;
-    static constexpr int kBar = kP + kPBytes;
-    // barriers: q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], pv_done, drain
-    static constexpr int kNumBars = 11;
+    static constexpr int kBar = kV + kKVStages * kTile;
+    // barriers: q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], pv_done[2], drain
+    static constexpr int kNumBars = 12;
     static constexpr int kMisc = kBar + kNumBars * 8;   // tmem base, abort flag, issued count
     static constexpr int kBytes = kMisc + 16;
     // room to align the base to 1 KB; at least 116 KB so a second CTA never
@@ -70,7 +73,7 @@ struct PrefillSmem {
     static constexpr int kAlloc = kBytes + 1024 > 116 * 1024 ? kBytes + 1024 : 116 * 1024;
 };
 
-template <typename T, int D, bool kPInTmem>
+template <typename T, int D>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -79,7 +82,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const int32_t* __restrict__ block_tables, int max_blocks_per_seq,
                      const int32_t* __restrict__ context_lens, int H, int Hk, int S, int NB,
                      int GP, float scale_log2, int32_t* dev_err) {
-    using L = PrefillSmem<D, kPInTmem>;
+    using L = PrefillSmem<D>;
     using E = Elem<T>;
     constexpr bool kBf16 = E::kDtype == PD_BF16;
     constexpr uint32_t kIdescQK = tc::idesc_f16(kBf16, kTileM, kTileN, false, false);
@@ -95,8 +98,12 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
     uint64_t* kv_empty = bars + 3;    // [2]
     uint64_t* s_full = bars + 5;      // [2]
     uint64_t* p_full = bars + 7;      // [2]
-    uint64_t* pv_done = bars + 9;
-    uint64_t* drain = bars + 10;
+    // pv_done[u & 1] completes when PV of tile u (and every earlier MMA) is
+    // done.  One barrier per tile parity keeps each wait within one phase of
+    // the barrier's state, which parity waits need (a barrier two phases
+    // behind would read as already complete).
+    uint64_t* pv_done = bars + 9;     // [2]
+    uint64_t* drain = bars + 11;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L::kMisc);
     volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kMisc + 4);
     volatile int32_t* issued = reinterpret_cast<volatile int32_t*>(smem + L::kMisc + 8);
@@ -128,7 +135,6 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t sQ = smem_u32(smem + L::kQ);
     const uint32_t sK = smem_u32(smem + L::kK);
     const uint32_t sV = smem_u32(smem + L::kV);
-    const uint32_t sP = smem_u32(smem + L::kP);
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -138,7 +144,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
             mbar_init(&s_full[s], 1);
             mbar_init(&p_full[s], kSoftmaxThreads);
         }
-        mbar_init(pv_done, 1);
+        mbar_init(&pv_done[0], 1);
+        mbar_init(&pv_done[1], 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         *issued = 0;
@@ -225,23 +232,21 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const int u = t - 1, su = u & 1;
                     if (!(ok = mbar_wait(&p_full[su], (u >> 1) & 1))) break;
                     tc::fence_after_sync();
+                    // P_hi in columns [0, 64) of the S buffer, P_lo in [64, 128)
 #pragma unroll
-                    for (int kk = 0; kk < kTileN / 16; ++kk) {
-                        // V tile as an MN-major operand: N = D contiguous in 64-wide
-                        // atoms (LBO between them), K = keys at 128 B (SBO per 8 keys)
-                        const uint64_t b = tc::smem_desc_sw128(sV + su * L::kTile + kk * 16 * 128,
-                                                               L::kAtom, 1024);
-                        if constexpr (kPInTmem) {
-                            tc::mma_ts(tmem + kTmemO, tmem + uint32_t(su) * kTileN + kk * 8, b,
-                                       kIdescPV, (u > 0 || kk > 0));
-                        } else {
-                            const uint32_t poff = (kk >> 2) * L::kAtom + (kk & 3) * 32;
-                            const uint64_t a = tc::smem_desc_sw128(
-                                sP + su * (kTileM * kTileN * 2) + poff, 16, 1024);
-                            tc::mma_ss(tmem + kTmemO, a, b, kIdescPV, (u > 0 || kk > 0));
+                    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                        for (int kk = 0; kk < kTileN / 16; ++kk) {
+                            // V tile as an MN-major operand: N = D contiguous in 64-wide
+                            // atoms (LBO between them), K = keys at 128 B (SBO per 8 keys)
+                            const uint64_t b = tc::smem_desc_sw128(
+                                sV + su * L::kTile + kk * 16 * 128, L::kAtom, 1024);
+                            tc::mma_ts(tmem + kTmemO,
+                                       tmem + uint32_t(su) * kTileN + half * 64 + kk * 8, b,
+                                       kIdescPV, (u > 0 || kk > 0 || half > 0));
                         }
                     }
-                    tc::commit(pv_done);
+                    tc::commit(&pv_done[su]);
                     tc::commit(&kv_empty[su]);
                 }
             }
@@ -266,7 +271,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int t = 0; t < n_tiles; ++t) {
             const int st = t & 1;
             ok = __all_sync(0xffffffffu, mbar_wait(&s_full[st], (t >> 1) & 1));
-            if (!ok || *abort_flag) break;
+            if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) break;
             tc::fence_after_sync();
             uint32_t sr[kTileN];
 #pragma unroll
@@ -275,24 +280,29 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                               *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
             tc::tmem_ld_wait();
             const int kbase = t * kTileN;
-            float mx = -INFINITY;
             if (kbase + kTileN - 1 > lim) {            // tile crosses this row's limit
 #pragma unroll
-                for (int c = 0; c < kTileN; ++c) {
-                    const float s = kbase + c <= lim ? __uint_as_float(sr[c]) : -INFINITY;
-                    sr[c] = __float_as_uint(s);
-                    mx = fmaxf(mx, s);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < kTileN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+                for (int c = 0; c < kTileN; ++c)
+                    if (kbase + c > lim) sr[c] = __float_as_uint(-INFINITY);
             }
+            float mxs[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mxs[k] = __uint_as_float(sr[k]);
+#pragma unroll
+            for (int c = 8; c < kTileN; ++c) mxs[c & 7] = fmaxf(mxs[c & 7], __uint_as_float(sr[c]));
+            const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                                   fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
             const float m_tile = mx * scale_log2;
-            if (m_tile > m_run + kRescaleThreshold) {
-                const float alpha = ex2(m_run - m_tile);   // 0 on the first tile
+            // The tensor-memory loads and stores below are warp-collective, so
+            // the warp rescales together when any of its rows needs it; each
+            // row uses its own exact factor (1 when its max did not grow).
+            if (__any_sync(0xffffffffu, m_tile > m_run + kRescaleThreshold)) {
+                const float m_new = fmaxf(m_run, m_tile);
+                const float alpha = ex2(m_run - m_new);    // 0 on the first tile
                 if (t > 0) {
                     // O holds PV of tiles < t; wait for the last of them, then scale.
-                    ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (t - 1) & 1));
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1));
                     if (!ok) break;
                     tc::fence_after_sync();
 #pragma unroll
@@ -308,35 +318,36 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                     tc::tmem_st_wait();
                 }
                 l_run *= alpha;
-                m_run = m_tile;
+                m_run = m_new;
             }
-            // p = 2^(s * scale_log2 - m), rounded to the element type
-            uint32_t pk[kTileN / 2];
-            float lsum = 0.f;
+            // p = 2^(s * scale_log2 - m) as hi + lo 16-bit values
+            uint32_t phi[kTileN / 2], plo[kTileN / 2];
+            float2 lsum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                              make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            const float2 sc2 = make_float2(scale_log2, scale_log2);
+            const float2 nm2 = make_float2(-m_run, -m_run);
+            const float2 neg1 = make_float2(-1.f, -1.f);
+            const float2 one2 = make_float2(1.f, 1.f);
 #pragma unroll
             for (int c = 0; c < kTileN / 2; ++c) {
-                const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), scale_log2, -m_run));
-                const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), scale_log2, -m_run));
-                lsum += p0 + p1;
-                pk[c] = E::pack2(p0, p1);
+                const float2 x = ffma2(make_float2(__uint_as_float(sr[2 * c]),
+                                                   __uint_as_float(sr[2 * c + 1])), sc2, nm2);
+                const float2 p = make_float2(ex2(x.x), ex2(x.y));
+                lsum[c & 3] = ffma2(p, one2, lsum[c & 3]);
+                phi[c] = E::pack2(p.x, p.y);
+                const float2 lo = ffma2(E::unpack2(phi[c]), neg1, p);   // p - hi, exact
+                plo[c] = E::pack2(lo.x, lo.y);
             }
-            l_run += lsum;
-            if constexpr (kPInTmem) {
+            l_run += ((lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y)) +
+                     ((lsum[2].x + lsum[2].y) + (lsum[3].x + lsum[3].y));
 #pragma unroll
-                for (int c = 0; c < kTileN / 64; ++c)
-                    tc::tmem_st32(tmem + lane_base + uint32_t(st) * kTileN + c * 32,
-                                  *reinterpret_cast<const uint32_t(*)[32]>(&pk[c * 32]));
-                tc::tmem_st_wait();
-            } else {
-                unsigned char* prow = smem + L::kP + st * (kTileM * kTileN * 2) + r * 128;
-#pragma unroll
-                for (int a = 0; a < 2; ++a)
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(prow + a * L::kAtom + ((c ^ (r & 7)) * 16)) =
-                            make_uint4(pk[a * 32 + c * 4], pk[a * 32 + c * 4 + 1],
-                                       pk[a * 32 + c * 4 + 2], pk[a * 32 + c * 4 + 3]);
+            for (int c = 0; c < kTileN / 64; ++c) {
+                tc::tmem_st32(tmem + lane_base + uint32_t(st) * kTileN + c * 32,
+                              *reinterpret_cast<const uint32_t(*)[32]>(&phi[c * 32]));
+                tc::tmem_st32(tmem + lane_base + uint32_t(st) * kTileN + 64 + c * 32,
+                              *reinterpret_cast<const uint32_t(*)[32]>(&plo[c * 32]));
             }
+            tc::tmem_st_wait();
             if (kbase + kTileN > ctx) {
                 // Keys past the context in the last tile: their V rows hold other
                 // data (or were never loaded); zero them so 0 * v stays 0.
@@ -352,12 +363,13 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                                 make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            if (!kPInTmem || kbase + kTileN > ctx) tc::fence_proxy_async_smem();
+            if (kbase + kTileN > ctx) tc::fence_proxy_async_smem();
             tc::fence_before_sync();
             mbar_arrive(&p_full[st]);
         }
-        if (ok && !*abort_flag) {
-            ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (n_tiles - 1) & 1));
+        if (ok && !__any_sync(0xffffffffu, *abort_flag != 0)) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(n_tiles - 1) & 1],
+                                                   ((n_tiles - 1) >> 1) & 1));
             if (ok) {
                 tc::fence_after_sync();
                 const float inv = 1.f / l_run;
@@ -411,57 +423,21 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
 
 // ---- host side --------------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-template <typename T, int D, bool kPInTmem>
+template <typename T, int D>
 pd_status launch_prefill_t(const PrefillArgs& a) {
-    using L = PrefillSmem<D, kPInTmem>;
-    auto encode = encode_fn();
-    if (!encode) return launch_result(cudaErrorNotSupported);
-    const CUtensorMapDataType dt =
-        Elem<T>::kDtype == PD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    using L = PrefillSmem<D>;
     const int G = a.H / a.Hk;
     int GP = 1;
     while (GP * 2 <= 16 && G % (GP * 2) == 0) GP *= 2;
     const int TQ = kTileM / GP;
-
     CUtensorMap tm_q, tm_k, tm_v;
-    {
-        cuuint64_t dims[3] = {cuuint64_t(a.D), cuuint64_t(a.H), cuuint64_t(a.total_q)};
-        cuuint64_t strides[2] = {cuuint64_t(a.D) * 2, cuuint64_t(a.H) * a.D * 2};
-        cuuint32_t box[3] = {64u, cuuint32_t(GP), cuuint32_t(TQ)};
-        cuuint32_t es[3] = {1u, 1u, 1u};
-        CUresult r = encode(&tm_q, dt, 3, const_cast<void*>(a.q), dims, strides, box, es,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return launch_result(cudaErrorInvalidValue);
-    }
-    {
-        cuuint64_t dims[2] = {cuuint64_t(a.D), cuuint64_t(a.NB) * a.Hk * a.S};
-        cuuint64_t strides[1] = {cuuint64_t(a.D) * 2};
-        cuuint32_t box[2] = {64u, cuuint32_t(a.S)};
-        cuuint32_t es[2] = {1u, 1u};
-        CUresult r = encode(&tm_k, dt, 2, const_cast<void*>(a.key_cache), dims, strides, box, es,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return launch_result(cudaErrorInvalidValue);
-        r = encode(&tm_v, dt, 2, const_cast<void*>(a.value_cache), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return launch_result(cudaErrorInvalidValue);
-    }
-    auto kern = paged_prefill_kernel<T, D, kPInTmem>;
+    const unsigned long long rows = (unsigned long long)a.NB * a.Hk * a.S;
+    if (rows > 0x7fffffffull) return PD_ERR_UNSUPPORTED;   // TMA row coordinate is int32
+    if (!encode_q_map(&tm_q, a.q, D, a.H, a.total_q, GP, TQ, a.dt) ||
+        !encode_pool_map(&tm_k, a.key_cache, D, rows, a.S, a.dt) ||
+        !encode_pool_map(&tm_v, a.value_cache, D, rows, a.S, a.dt))
+        return launch_result(cudaErrorInvalidValue);
+    auto kern = paged_prefill_kernel<T, D>;
     static uint64_t attr_set = 0;   // one bit per device
     int dev = 0;
     cudaError_t e0 = cudaGetDevice(&dev);
@@ -480,19 +456,13 @@ pd_status launch_prefill_t(const PrefillArgs& a) {
     return launch_result(cudaGetLastError());
 }
 
-template <bool kPInTmem>
-pd_status launch_prefill_p(const PrefillArgs& a) {
-    if (a.dt == PD_BF16)
-        return a.D == 128 ? launch_prefill_t<__nv_bfloat16, 128, kPInTmem>(a)
-                          : launch_prefill_t<__nv_bfloat16, 64, kPInTmem>(a);
-    return a.D == 128 ? launch_prefill_t<__half, 128, kPInTmem>(a)
-                      : launch_prefill_t<__half, 64, kPInTmem>(a);
-}
-
 }  // namespace
 
 pd_status launch_prefill(const PrefillArgs& a) {
-    return a.p_in_smem ? launch_prefill_p<false>(a) : launch_prefill_p<true>(a);
+    if (a.dt == PD_BF16)
+        return a.D == 128 ? launch_prefill_t<__nv_bfloat16, 128>(a)
+                          : launch_prefill_t<__nv_bfloat16, 64>(a);
+    return a.D == 128 ? launch_prefill_t<__half, 128>(a) : launch_prefill_t<__half, 64>(a);
 }
 
 }  // namespace pd

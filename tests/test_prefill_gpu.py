@@ -160,3 +160,16 @@ def test_bad_inputs_flagged(cuda_lib):
     err = device_err()
     _run(pd, m2, dev_err=err)
     assert err.item() & pd.PD_DEVERR_CTX_RANGE
+
+
+def test_repeat_runs_identical(cuda_lib):
+    """Same inputs, same bits, run after run: catches reads of tensor memory
+    that race the MMAs still accumulating into it.  Chunks end in query tiles
+    with one valid token, over 1, 2 and 3 key tiles."""
+    pd = cuda_lib
+    m = pd_inputs.mixed_case(95, [0, 127, 300], [97, 129, 65], [], 8, 2, 128, 16, torch.bfloat16)
+    first, kc, vc = _run(pd, m)
+    for _ in range(8):
+        again, _, _ = _run(pd, m, kc=kc, vc=vc)
+        assert torch.equal(first.view(torch.int16), again.view(torch.int16))
+    assert_close(first.cpu(), _oracle(m), "repeat mix")
