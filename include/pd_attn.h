@@ -109,19 +109,20 @@ PD_API pd_status pd_reshape_and_cache(const void* key, const void* value,
  *   block_tables  int32 [B][max_blocks_per_seq]
  *   context_lens  int32 [B], each <= max_context_len (the caller's promise,
  *                 checked on device: PD_DEVERR_CTX_RANGE, the context is
- *                 then cut to what the table and workspace hold)
- * Long contexts are split into partitions of a fixed number of tokens that
- * are processed in parallel (online softmax per partition, results kept in
- * `workspace`), then merged by a second kernel; a batch whose
- * max_context_len fits one partition is written directly.
+ *                 then cut to max_context_len and to what the table holds)
+ * The batch's work is cut into equal contiguous runs of 64-token stages, one
+ * per resident CTA, so a long context may be split across CTAs (online
+ * softmax per piece, pieces kept in `workspace`) and merged by a second
+ * kernel; a context that one CTA finishes is written directly.
  *   workspace     device scratch of at least
  *                 pd_decode_workspace_bytes(B, H, D, max_context_len) bytes
- *                 (may be NULL when that size is 0); 256-byte aligned.
- *                 Overwritten; callers sharing one workspace on two streams
- *                 race.  PD_ERR_WORKSPACE_TOO_SMALL if it is short. */
+ *                 (always > 0), 256-byte aligned.  Nothing in it needs to
+ *                 start at zero.  Overwritten; callers sharing one workspace
+ *                 on two streams race.  PD_ERR_WORKSPACE_TOO_SMALL if short. */
 PD_API size_t pd_decode_workspace_bytes(int B, int H, int D, int max_context_len);
-/* Tokens per partition used for a given max_context_len (exposed for
- * accounting and tests). */
+/* Token granule of the work split: a CTA takes at least this many tokens
+ * before another CTA shares a context, so one context is cut into at most
+ * ceil(ctx / granule) + 1 pieces (exposed for accounting and tests). */
 PD_API int pd_decode_partition_tokens(int max_context_len);
 PD_API pd_status pd_paged_attention_decode(void* out, const void* q,
                                     const void* key_cache,

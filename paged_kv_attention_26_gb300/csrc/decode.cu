@@ -9,11 +9,15 @@
 // Decode is HBM-bound (about one FLOP per byte per query head, tutorial page
 // section 1.1): the design streams every K/V byte once and keeps the
 // instruction count per byte low enough that issue never caps bandwidth.
-//  * grid = (kv head x head group, sequence, partition); a partition is a
-//    fixed run of kPart logical tokens, so long contexts spread over SMs;
-//  * one producer warp gathers the partition's K and V blocks with 2-D TMA
-//    boxes ([S tokens][64 dims], 128-byte swizzle) through the block table
-//    into a 3-stage shared-memory ring of 64-token stages (two CTAs per SM);
+//  * work split (stream-K): each (sequence, kv head group) is a stream of
+//    64-token stages; the streams laid end to end are cut into equal
+//    contiguous ranges, one per persistent CTA (two per SM, at least 4
+//    stages each), so every CTA streams the same number of bytes.  A stream
+//    that fits inside one CTA's range is finished there; one that crosses
+//    range boundaries leaves one partial result per CTA for the reduce;
+//  * one producer warp gathers K and V blocks with 2-D TMA boxes
+//    ([S tokens][64 dims], 128-byte swizzle) through the block table into a
+//    3-stage shared-memory ring, running ahead across stream boundaries;
 //  * four consumer warps take 16 tokens of each stage.  The G query heads
 //    that share the kv head form the N = 8 side of warp-level tensor-core
 //    products (mma.sync m16n8k16, fp32 accumulation): S^T = K q^T for 16
@@ -25,11 +29,12 @@
 //  * P enters the product as an unevaluated pair of 16-bit values
 //    (hi = rn(p), lo = rn(p - hi)), two MMAs per tile, so P carries about
 //    2^-17 relative error instead of the 2^-9 of a single bf16;
-//  * the four warps merge in shared memory; a batch that fits one partition
-//    writes `out` directly, otherwise partial (max, sum, unnormalised o) go
-//    to the workspace and a reduce kernel, launched programmatically
-//    dependent, merges them in fixed partition order.  No atomics touch
-//    results: outputs are bit-identical for any placement of blocks.
+//  * at the end of each stream piece the four warps merge through a small
+//    exchange buffer; a whole stream is normalised and written to `out`,
+//    a piece leaves (max, sum, unnormalised o) in the workspace, and a
+//    reduce kernel (programmatic dependent launch) merges the pieces in
+//    fixed order.  No atomics touch results: outputs are bit-identical for
+//    any placement of blocks in the pool.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -44,7 +49,8 @@
 namespace pd {
 namespace {
 
-constexpr int kPart = 256;          // tokens per partition (multiple of the stage)
+constexpr int kMinStagesPerCta = 4; // a CTA's range never ends before 4 stages
+constexpr int kSegTokens = kMinStagesPerCta * 64;   // bounds pieces per stream
 constexpr int kStageTokens = 64;    // tokens per pipeline stage
 constexpr int kStages = 3;          // ring depth
 constexpr int kConsumerWarps = 4;   // 16 tokens of each stage per warp
@@ -76,31 +82,84 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int tok, int chunk) {
            (((chunk & 7) ^ (tok & 7)) << 4);
 }
 
-// A work item is (partition, sequence, unit) with unit = (kv head, head group);
-// the same enumeration drives the producer and the consumers.
-struct Item {
-    int part, seq, unit, t_begin, t_end, n_stages;
+// Stream walk shared by the producer and the consumers.  Streams are ordered
+// sequence-major, unit-minor; stream (s, u) has L_s = ceil(ctx_s / 64) stages
+// and starts at global stage units * (sum of L over earlier sequences) + u * L_s.
+struct Walk {
+    int s, u, L, ctx;     // current stream and its sequence's stage count / tokens
+    long start;           // global stage index of the stream's first stage
+    int off;              // next stage within the stream
+    long pos, end;        // next global stage; end of this CTA's range
+    long per_cta;
 };
 
-__device__ __forceinline__ Item decode_item(long item, int units, int B,
-                                            const int32_t* __restrict__ context_lens, int cap,
-                                            int32_t* dev_err, bool flag) {
-    Item it;
-    it.unit = int(item % units);
-    const long rest = item / units;
-    it.seq = int(rest % B);
-    it.part = int(rest / B);
-    int ctx = __ldg(context_lens + it.seq);
-    if (ctx > cap || ctx < 0) {
-        // context longer than the table / workspace promise: cut to what they hold
-        if (flag && it.part == 0 && it.unit == 0) flag_error(dev_err, PD_DEVERR_CTX_RANGE);
-        ctx = ctx < 0 ? 0 : cap;
+__device__ __forceinline__ int stream_ctx(const int32_t* __restrict__ context_lens, int s,
+                                          int cap) {
+    const int c = __ldg(context_lens + s);
+    return c < 0 ? 0 : (c > cap ? cap : c);
+}
+
+// Position the walk at the start of this CTA's range (every warp computes it).
+__device__ __forceinline__ bool walk_begin(Walk& w, const int32_t* __restrict__ context_lens,
+                                           int B, int units, int cap) {
+    const int lane = threadIdx.x & 31;
+    long total = 0;
+    for (int base = 0; base < B; base += 32) {
+        const int s = base + lane;
+        const long v = s < B ? long(units) * ((stream_ctx(context_lens, s, cap) + 63) / 64) : 0;
+        total += v;
     }
-    it.t_begin = it.part * kPart;
-    it.t_end = min(ctx, it.t_begin + kPart);
-    it.n_stages = it.t_end > it.t_begin ? (it.t_end - it.t_begin + kStageTokens - 1) / kStageTokens
-                                        : 0;
-    return it;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+    const long even = (total + gridDim.x - 1) / gridDim.x;
+    w.per_cta = even > kMinStagesPerCta ? even : long(kMinStagesPerCta);
+    const long r0 = long(blockIdx.x) * w.per_cta;
+    w.end = total < r0 + w.per_cta ? total : r0 + w.per_cta;
+    if (r0 >= total) return false;
+    // find the sequence whose streams contain r0
+    long prefix = 0;
+    for (int base = 0; base < B; base += 32) {
+        const int s = base + lane;
+        const int ctx = s < B ? stream_ctx(context_lens, s, cap) : 0;
+        const long v = long(units) * ((ctx + 63) / 64);
+        long incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const bool hit = s < B && v > 0 && prefix + incl > r0 && prefix + incl - v <= r0;
+        const uint32_t m = __ballot_sync(0xffffffffu, hit);
+        if (m) {
+            const int src = __ffs(m) - 1;
+            w.s = base + src;
+            w.ctx = __shfl_sync(0xffffffffu, ctx, src);
+            const long before = prefix + __shfl_sync(0xffffffffu, incl - v, src);
+            w.L = (w.ctx + 63) / 64;
+            w.u = int((r0 - before) / w.L);
+            w.start = before + long(w.u) * w.L;
+            w.off = int(r0 - w.start);
+            w.pos = r0;
+            return true;
+        }
+        prefix += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return false;
+}
+
+// After the current stream is exhausted, move to the next non-empty one.
+__device__ __forceinline__ void walk_next_stream(Walk& w, const int32_t* __restrict__ context_lens,
+                                                 int B, int units, int cap) {
+    w.start += w.L;
+    w.off = 0;
+    if (++w.u == units) {
+        w.u = 0;
+        do {
+            ++w.s;
+            w.ctx = w.s < B ? stream_ctx(context_lens, w.s, cap) : 0;
+        } while (w.s < B && w.ctx == 0);
+        w.L = (w.ctx + 63) / 64;
+    }
 }
 
 // OR of `pred` over the consumer warps (named barrier 1), uniform result.
@@ -113,7 +172,6 @@ __device__ __forceinline__ bool consumers_any(bool pred) {
     return r != 0;
 }
 
-// Persistent: each CTA walks items blockIdx.x, blockIdx.x + gridDim.x, ...
 template <typename T, int D>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -121,9 +179,9 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const T* __restrict__ q, const int32_t* __restrict__ block_tables,
                           int max_blocks_per_seq, const int32_t* __restrict__ context_lens,
                           int B, int H, int Hk, int S, int NB, int GH, float scale_log2,
-                          int num_parts_max, float* __restrict__ ws_o,
+                          int max_segs, int cap, float* __restrict__ ws_o,
                           float* __restrict__ ws_m, float* __restrict__ ws_l,
-                          int32_t* dev_err) {
+                          int2* __restrict__ ws_seg, int32_t* dev_err) {
     using L = DecodeSmem<D>;
     using E = Elem<T>;
     constexpr int kAtoms = D / 64;
@@ -142,9 +200,6 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int G = H / Hk;
     const int groups = G / GH;
     const int units = Hk * groups;
-    const long n_items = long(num_parts_max) * B * units;
-    const int cap = min(max_blocks_per_seq * S, num_parts_max * kPart);
-    const bool direct = (num_parts_max == 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -160,55 +215,53 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     __syncthreads();
 
+    Walk w;
+    if (!walk_begin(w, context_lens, B, units, cap)) return;   // uniform: no range
+
     if (warp == kConsumerWarps) {
-        // ---------------- producer warp: streams stages across items ----------------
+        // ---------------- producer warp: streams stages across stream pieces ----------------
         const uint32_t block_bytes = uint32_t(S) * D * 2;        // one [S][D] slab
-        uint32_t gs = 0;                                         // stages issued so far
-        bool stop = false;
-        for (long item = blockIdx.x; item < n_items && !stop; item += gridDim.x) {
-            const Item it = decode_item(item, units, B, context_lens, cap, dev_err, false);
-            if (it.n_stages == 0) continue;
-            const int kvh = it.unit / groups;
-            const int32_t* bt_row = block_tables + (int64_t)it.seq * max_blocks_per_seq;
-            for (int st = 0; st < it.n_stages; ++st, ++gs) {
-                const int slot = gs % kStages;
-                // every lane waits (acquire), then the warp agrees on the outcome
-                const bool ok = __all_sync(0xffffffffu, gs < kStages ||
-                                           mbar_wait(&empty[slot], ((gs / kStages) - 1) & 1));
-                if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) {
-                    if (lane == 0 && !ok) {
-                        flag_error(dev_err, PD_DEVERR_TIMEOUT);
-                        *abort_flag = 1;
-                    }
-                    stop = true;
-                    break;
+        for (uint32_t gs = 0; w.pos < w.end; ++gs) {
+            const int slot = gs % kStages;
+            // every lane waits (acquire), then the warp agrees on the outcome
+            const bool ok = __all_sync(0xffffffffu, gs < kStages ||
+                                       mbar_wait(&empty[slot], ((gs / kStages) - 1) & 1));
+            if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) {
+                if (lane == 0 && !ok) {
+                    flag_error(dev_err, PD_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
                 }
-                const int t0 = it.t_begin + st * kStageTokens;
-                const int nt = min(kStageTokens, it.t_end - t0);
-                const int nblk = (nt + S - 1) / S;             // <= 64 / S <= 8
-                int row = -1;
-                if (lane < nblk) {
-                    const int blk = __ldg(bt_row + t0 / S + lane);
-                    if (blk >= 0 && blk < NB) {
-                        row = (blk * Hk + kvh) * S;
-                    } else {
-                        flag_error(dev_err, PD_DEVERR_BLOCK_RANGE);
-                    }
-                }
-                const uint32_t ok_mask = __ballot_sync(0xffffffffu, row >= 0);
-                if (lane == 0)
-                    mbar_arrive_expect_tx(&full[slot], 2u * block_bytes * __popc(ok_mask));
-                __syncwarp();
-                if (row >= 0) {
-#pragma unroll
-                    for (int a = 0; a < kAtoms; ++a) {
-                        const int off = slot * L::kTile + a * L::kAtom + lane * S * 128;
-                        tc::tma_load_2d(smem + L::kK + off, &tm_k, a * 64, row, &full[slot]);
-                        tc::tma_load_2d(smem + L::kV + off, &tm_v, a * 64, row, &full[slot]);
-                    }
-                }
-                if (lane == 0) *issued = int(gs + 1);
+                break;
             }
+            const int kvh = w.u / groups;
+            const int32_t* bt_row = block_tables + (int64_t)w.s * max_blocks_per_seq;
+            const int t0 = w.off * kStageTokens;
+            const int nt = min(kStageTokens, w.ctx - t0);
+            const int nblk = (nt + S - 1) / S;             // <= 64 / S <= 8
+            int row = -1;
+            if (lane < nblk) {
+                const int blk = __ldg(bt_row + t0 / S + lane);
+                if (blk >= 0 && blk < NB) {
+                    row = (blk * Hk + kvh) * S;
+                } else {
+                    flag_error(dev_err, PD_DEVERR_BLOCK_RANGE);
+                }
+            }
+            const uint32_t ok_mask = __ballot_sync(0xffffffffu, row >= 0);
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2u * block_bytes * __popc(ok_mask));
+            __syncwarp();
+            if (row >= 0) {
+#pragma unroll
+                for (int a = 0; a < kAtoms; ++a) {
+                    const int off = slot * L::kTile + a * L::kAtom + lane * S * 128;
+                    tc::tma_load_2d(smem + L::kK + off, &tm_k, a * 64, row, &full[slot]);
+                    tc::tma_load_2d(smem + L::kV + off, &tm_v, a * 64, row, &full[slot]);
+                }
+            }
+            if (lane == 0) *issued = int(gs + 1);
+            ++w.off;
+            ++w.pos;
+            if (w.off == w.L && w.pos < w.end) walk_next_stream(w, context_lens, B, units, cap);
         }
         return;
     }
@@ -222,32 +275,22 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     uint32_t gs = 0;                             // stages consumed so far
     bool aborted = false;
 
-    for (long item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const Item it = decode_item(item, units, B, context_lens, cap, dev_err, warp == 0);
-        const int kvh = it.unit / groups;
-        const int h0 = kvh * G + (it.unit % groups) * GH;     // first q head of this unit
-        if (it.n_stages == 0) {
-            // Nothing to attend to.  A zero-length context still owes zeros.
-            if (it.part == 0 && warp == 0) {
-                if (direct) {
-                    for (int idx = lane; idx < GH * D / 2; idx += 32) {
-                        const int h = idx / (D / 2), d2 = idx % (D / 2);
-                        reinterpret_cast<uint32_t*>(out + ((int64_t)it.seq * H + h0 + h) * D)[d2] = 0u;
-                    }
-                } else if (lane < GH) {
-                    const int64_t r = ((int64_t)it.seq * H + h0 + lane) * num_parts_max;
-                    ws_m[r] = -INFINITY;     // the reduce kernel sees an empty row
-                    ws_l[r] = 0.f;
-                }
-            }
-            continue;
-        }
+    while (w.pos < w.end) {
+        // ---- one stream piece: stages [w.off, min(w.L, w.off + w.end - w.pos)) of (s, u)
+        const int kvh = w.u / groups;
+        const int h0 = kvh * G + (w.u % groups) * GH;     // first q head of this unit
+        const long left = w.end - w.pos;
+        const int piece_stages = int(left < long(w.L - w.off) ? left : long(w.L - w.off));
+        const long c_first = w.start / w.per_cta;
+        const long c_last = (w.start + w.L - 1) / w.per_cta;
+        const int nseg = int(c_last - c_first + 1);
+        const int seg = int(long(blockIdx.x) - c_first);
         // q^T as the MMA B operand: lane holds head lane/4, dims 16ks + 2(lane%4) + {0,1}
         // (register 0) and the same + 8 (register 1); heads past GH are zero.
         uint32_t qb[KS][2];
         {
             const int n = lane >> 2;
-            const T* qrow = q + ((int64_t)it.seq * H + h0 + n) * D + 2 * (lane & 3);
+            const T* qrow = q + ((int64_t)w.s * H + h0 + n) * D + 2 * (lane & 3);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 qb[ks][0] = n < GH ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks)) : 0u;
@@ -263,7 +306,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         float m_run[2] = {-INFINITY, -INFINITY};
         float l_run[2] = {0.f, 0.f};
 
-        for (int st = 0; st < it.n_stages; ++st, ++gs) {
+        for (int st = 0; st < piece_stages; ++st, ++gs) {
             const int slot = gs % kStages;
             if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (gs / kStages) & 1))) {
                 if (lane == 0) {
@@ -271,15 +314,15 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                     *abort_flag = 1;
                 }
                 aborted = true;
-                break;                   // skip the item's other stages
+                break;                   // skip the piece's other stages
             }
-            const int nt = min(kStageTokens, it.t_end - (it.t_begin + st * kStageTokens));
+            const int nt = min(kStageTokens, w.ctx - (w.off + st) * kStageTokens);
             if (tb < nt) {
                 const uint32_t kb = k_base0 + slot * L::kTile;
                 const uint32_t vb = v_base0 + slot * L::kTile;
                 const bool partial = tb + 16 > nt;
                 if (partial) {
-                    // V rows past the partition end hold other data or were never
+                    // V rows past the context end hold other data or were never
                     // loaded this round: zero them so that 0 * v stays 0.
                     unsigned char* vrow = smem + L::kV + slot * L::kTile;
                     for (int i = lane; i < 16 * kAtoms * 8; i += 32) {
@@ -412,17 +455,19 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             for (int h = 0; h < 2; ++h) {
                 const int hh = ha + h;
                 if (hh >= GH) continue;
-                const int hq = h0 + hh;
-                if (direct) {
+                const int64_t row = (int64_t)w.s * H + h0 + hh;
+                if (seg == 0 && d0 == 0) ws_seg[row] = make_int2(int(c_first), nseg);
+                if (nseg == 1) {
+                    // the whole stream was here: final, normalised output
                     const float inv = 1.f / l_run[h];
-                    T* orow = out + ((int64_t)it.seq * H + hq) * D + d0;
+                    T* orow = out + row * D + d0;
 #pragma unroll
                     for (int mt = 0; mt < KS; ++mt) {
                         orow[16 * mt] = T(o[mt][h] * inv);
                         orow[16 * mt + 8] = T(o[mt][2 + h] * inv);
                     }
                 } else {
-                    const int64_t r = ((int64_t)it.seq * H + hq) * num_parts_max + it.part;
+                    const int64_t r = row * max_segs + seg;
                     float* wrow = ws_o + r * D + d0;
 #pragma unroll
                     for (int mt = 0; mt < KS; ++mt) {
@@ -436,8 +481,11 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
             }
         }
-        // the exchange buffer is rewritten by the next item's merge
+        // the exchange buffer is rewritten by the next piece's merge
         asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+        w.off += piece_stages;
+        w.pos += piece_stages;
+        if (w.off == w.L && w.pos < w.end) walk_next_stream(w, context_lens, B, units, cap);
     }
 
     if (aborted) {
@@ -450,16 +498,19 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
 }
 
-// Merge the partitions of each (sequence, q head): one warp per row, fixed
-// partition order.  M = max_p m_p; out = sum_p o_p 2^(m_p - M) / sum_p l_p 2^(m_p - M).
+// Merge the pieces of each (sequence, q head) stream: one warp per row, fixed
+// order.  M = max_k m_k; out = sum_k o_k 2^(m_k - M) / sum_k l_k 2^(m_k - M).
+// Rows whose stream was finished in one CTA were written by the split
+// kernel; empty contexts give zeros.
 constexpr int kReduceWarps = 4;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kReduceWarps * 32)
 paged_decode_reduce_kernel(T* __restrict__ out, const int32_t* __restrict__ context_lens,
-                           int B, int H, int num_parts_max, int cap,
+                           int B, int H, int max_segs, int cap,
                            const float* __restrict__ ws_o, const float* __restrict__ ws_m,
-                           const float* __restrict__ ws_l) {
+                           const float* __restrict__ ws_l, const int2* __restrict__ ws_seg,
+                           int32_t* dev_err) {
     using E = Elem<T>;
     constexpr int DV = D / 32;
     pdl_wait_primary();
@@ -468,10 +519,21 @@ paged_decode_reduce_kernel(T* __restrict__ out, const int32_t* __restrict__ cont
     if (row >= int64_t(B) * H) return;
     const int seq = int(row / H);
     int ctx = __ldg(context_lens + seq);
-    ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
-    const int np = (ctx + kPart - 1) / kPart;
-    const float* m = ws_m + row * num_parts_max;
-    const float* l = ws_l + row * num_parts_max;
+    if (ctx < 0 || ctx > cap) {
+        // longer than the table or the caller's max_context_len: it was cut
+        if (lane == 0 && row % H == 0) flag_error(dev_err, PD_DEVERR_CTX_RANGE);
+        ctx = ctx < 0 ? 0 : cap;
+    }
+    uint32_t* dst = reinterpret_cast<uint32_t*>(out + row * D + lane * DV);
+    if (ctx == 0) {
+#pragma unroll
+        for (int e = 0; e < DV / 2; ++e) dst[e] = 0u;
+        return;
+    }
+    const int np = ws_seg[row].y;
+    if (np <= 1 || np > max_segs) return;     // finished by the split kernel
+    const float* m = ws_m + row * max_segs;
+    const float* l = ws_l + row * max_segs;
     float M = -INFINITY;
     for (int p = lane; p < np; p += 32) M = fmaxf(M, m[p]);
 #pragma unroll
@@ -482,12 +544,12 @@ paged_decode_reduce_kernel(T* __restrict__ out, const int32_t* __restrict__ cont
     float lsum = 0.f;
     for (int p0 = 0; p0 < np; p0 += 32) {
         const int p = p0 + lane;
-        const float w = p < np ? ex2(m[p] - M) : 0.f;
+        const float w = p < np && m[p] != -INFINITY ? ex2(m[p] - M) : 0.f;
         lsum += p < np ? l[p] * w : 0.f;
         const int n = min(32, np - p0);
         for (int u = 0; u < n; ++u) {
             const float wu = __shfl_sync(0xffffffffu, w, u);
-            const float* o = ws_o + (row * num_parts_max + p0 + u) * D + lane * DV;
+            const float* o = ws_o + (row * max_segs + p0 + u) * D + lane * DV;
             if constexpr (DV == 4) {
                 const float4 v = *reinterpret_cast<const float4*>(o);
                 acc[0] += v.x * wu; acc[1] += v.y * wu; acc[2] += v.z * wu; acc[3] += v.w * wu;
@@ -499,8 +561,7 @@ paged_decode_reduce_kernel(T* __restrict__ out, const int32_t* __restrict__ cont
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-    const float inv = np > 0 ? 1.f / lsum : 0.f;
-    uint32_t* dst = reinterpret_cast<uint32_t*>(out + row * D + lane * DV);
+    const float inv = 1.f / lsum;
 #pragma unroll
     for (int e = 0; e < DV / 2; ++e) dst[e] = E::pack2(acc[2 * e] * inv, acc[2 * e + 1] * inv);
 }
@@ -508,16 +569,17 @@ paged_decode_reduce_kernel(T* __restrict__ out, const int32_t* __restrict__ cont
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-    size_t o, m, l, total;
+    size_t o, m, l, seg, total;
 };
 
 WsLayout ws_layout(int B, int H, int D, int P) {
     WsLayout w;
-    const size_t rows = size_t(B) * H * P;
+    const size_t rows = size_t(B) * H;
     w.o = 0;
-    w.m = align256(rows * D * sizeof(float));
-    w.l = w.m + align256(rows * sizeof(float));
-    w.total = w.l + align256(rows * sizeof(float));
+    w.m = align256(rows * P * D * sizeof(float));
+    w.l = w.m + align256(rows * P * sizeof(float));
+    w.seg = w.l + align256(rows * P * sizeof(float));
+    w.total = w.seg + align256(rows * sizeof(int2));
     return w;
 }
 
@@ -536,12 +598,10 @@ int sm_count(int dev) {
 template <typename T, int D>
 pd_status launch_decode_t(const DecodeArgs& a) {
     using Lt = DecodeSmem<D>;
-    const int P = decode_num_partitions(a.max_context_len);
     const int G = a.H / a.Hk;
     int GH = 1;                          // largest divisor of G that fits N = 8
     for (int g = std::min(G, kHeadsN); g >= 1; --g)
         if (G % g == 0) { GH = g; break; }
-    const int groups = G / GH;
     CUtensorMap tm_k, tm_v;
     const unsigned long long rows = (unsigned long long)a.NB * a.Hk * a.S;
     if (rows > 0x7fffffffull) return PD_ERR_UNSUPPORTED;   // TMA row coordinate is int32
@@ -559,31 +619,27 @@ pd_status launch_decode_t(const DecodeArgs& a) {
         if (e != cudaSuccess) return launch_result(e);
         if (dev < 64) attr_set |= uint64_t(1) << dev;
     }
-    float* ws_o = nullptr;
-    float* ws_m = nullptr;
-    float* ws_l = nullptr;
-    if (P > 1) {
-        const WsLayout w = ws_layout(a.B, a.H, a.D, P);
-        char* base = static_cast<char*>(a.workspace);
-        ws_o = reinterpret_cast<float*>(base + w.o);
-        ws_m = reinterpret_cast<float*>(base + w.m);
-        ws_l = reinterpret_cast<float*>(base + w.l);
-    }
+    const int P = decode_num_partitions(a.max_context_len);   // pieces per stream, at most
+    const WsLayout w = ws_layout(a.B, a.H, a.D, P);
+    char* base = static_cast<char*>(a.workspace);
+    float* ws_o = reinterpret_cast<float*>(base + w.o);
+    float* ws_m = reinterpret_cast<float*>(base + w.m);
+    float* ws_l = reinterpret_cast<float*>(base + w.l);
+    int2* ws_seg = reinterpret_cast<int2*>(base + w.seg);
     const float scale_log2 = a.scale * kLog2e;
-    // Persistent grid: two CTAs per SM (shared memory bound), never more CTAs
-    // than work items.
-    const long n_items = long(P) * a.B * a.Hk * groups;
-    const long grid = std::min<long>(n_items, 2L * sm_count(dev));
-    kern<<<unsigned(grid), kDecodeThreads, Lt::kAlloc, a.stream>>>(
+    // contexts are cut to what the table holds and to the caller's promise
+    const int cap = int(std::min<long>(long(a.max_blocks_per_seq) * a.S, a.max_context_len));
+    // persistent grid: two CTAs per SM (shared memory bound)
+    const unsigned grid = unsigned(2 * sm_count(dev));
+    kern<<<grid, kDecodeThreads, Lt::kAlloc, a.stream>>>(
         tm_k, tm_v, static_cast<T*>(a.out), static_cast<const T*>(a.q), a.block_tables,
-        a.max_blocks_per_seq, a.context_lens, a.B, a.H, a.Hk, a.S, a.NB, GH, scale_log2, P,
-        ws_o, ws_m, ws_l, a.dev_err);
+        a.max_blocks_per_seq, a.context_lens, a.B, a.H, a.Hk, a.S, a.NB, GH, scale_log2, P, cap,
+        ws_o, ws_m, ws_l, ws_seg, a.dev_err);
     pd_status st = launch_result(cudaGetLastError());
-    if (st != PD_OK || P == 1) return st;
+    if (st != PD_OK) return st;
 
     // Reduce, launched as a programmatic dependent of the split kernel so its
     // launch overlaps the split kernel's tail.
-    const int cap = std::min(a.max_blocks_per_seq * a.S, P * kPart);
     cudaLaunchConfig_t cfg = {};
     const int64_t nrows = int64_t(a.B) * a.H;
     cfg.gridDim = dim3(unsigned((nrows + kReduceWarps - 1) / kReduceWarps));
@@ -599,7 +655,8 @@ pd_status launch_decode_t(const DecodeArgs& a) {
                                        static_cast<T*>(a.out), a.context_lens, a.B, a.H, P, cap,
                                        static_cast<const float*>(ws_o),
                                        static_cast<const float*>(ws_m),
-                                       static_cast<const float*>(ws_l));
+                                       static_cast<const float*>(ws_l),
+                                       static_cast<const int2*>(ws_seg), a.dev_err);
     return launch_result(e);
 }
 
@@ -607,18 +664,19 @@ pd_status launch_decode_t(const DecodeArgs& a) {
 
 int decode_partition_tokens(int max_context_len) {
     (void)max_context_len;
-    return kPart;
+    return kSegTokens;
 }
 
+// Most pieces one stream can be cut into: a CTA's range holds at least
+// kMinStagesPerCta stages, so a stream of L stages meets at most
+// ceil(L / kMinStagesPerCta) + 1 ranges.
 int decode_num_partitions(int max_context_len) {
     if (max_context_len <= 0) return 1;
-    return (max_context_len + kPart - 1) / kPart;
+    return (max_context_len + kSegTokens - 1) / kSegTokens + 1;
 }
 
 size_t decode_workspace_bytes(int B, int H, int D, int max_context_len) {
-    const int P = decode_num_partitions(max_context_len);
-    if (P <= 1) return 0;
-    return ws_layout(B, H, D, P).total;
+    return ws_layout(B, H, D, decode_num_partitions(max_context_len)).total;
 }
 
 pd_status launch_decode(const DecodeArgs& a) {
