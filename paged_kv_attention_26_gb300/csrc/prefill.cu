@@ -10,25 +10,30 @@
 // "LLM推理PD分离架构深度工程实践" section 1), so QK^T and PV run as
 // tcgen05.mma with fp32 accumulation in tensor memory.
 //
-// Tiling.  A CTA owns one 128-row query tile and streams 128-key tiles:
+// Tiling.  A CTA owns two 128-row query tiles (A, B) of one kv head group and
+// streams 128-key tiles shared by both:
 //  * GQA packing: the G' = min(G, 16) query heads that share a kv head are
-//    interleaved into the tile (rows = 128/G' tokens x G' heads), so every
+//    interleaved into each tile (rows = 128/G' tokens x G' heads), so every
 //    K/V tile is loaded once for all of them and the causal band is narrow;
-//  * warp 0 issues TMA loads: the Q tile once (3-D map over [tokens][heads][D]),
-//    then per key tile one 2-D box [S rows][64 dims] per K and per V block,
-//    gathered through the block table into a 2-stage ring, 128-byte swizzle;
-//  * warp 1 allocates tensor memory and issues the MMAs from one thread:
-//    S = Q K^T into one of two S buffers (so QK^T of tile t+1 overlaps the
-//    softmax of tile t), then O += P V with P read straight from tensor
-//    memory where the softmax wrote it over S;
-//  * warps 2-5 (one query row per thread) run the online softmax in the
-//    log2 domain with lazy rescaling (the accumulator O is rescaled only when
-//    a row max grows by more than 2^8) and finally normalise O and store it;
-//  * P is carried as an unevaluated sum of two 16-bit values, hi = rn(p) and
-//    lo = rn(p - hi), both written over the S row (64 + 64 columns) and
-//    applied by two PV passes.  A single 16-bit P carries a relative error of
-//    up to 2^-9 (bf16), which near-zero outputs of short contexts cannot
-//    absorb; the pair brings it to about 2^-17.
+//  * warp 0 issues TMA loads: the two Q tiles once (3-D map over
+//    [tokens][heads][D]), then per key tile one 2-D box [S rows][64 dims] per
+//    K and per V block, gathered through the block table into a 2-stage ring
+//    with 128-byte swizzle;
+//  * warp 1 allocates all 512 tensor-memory columns (S_A, O_A, S_B, O_B) and
+//    issues every MMA from one thread, alternating the two tiles: PV_A(t),
+//    QK_A(t+1), PV_B(t), QK_B(t+1).  While one softmax warpgroup works on
+//    its tile, the tensor cores run the other tile's products;
+//  * warps 4-7 (tile A) and 8-11 (tile B), one query row per thread, run the
+//    online softmax in the log2 domain with lazy rescaling (the accumulator
+//    O is rescaled only when a row max grows by more than 2^8), reading the
+//    S row from tensor memory in 32-column chunks (a max pass, then an
+//    exponential pass), and write P over S for the PV product;
+//  * P is rounded to 16 bits for the tensor cores.  Where one key can carry a
+//    large share of a row's softmax mass (its weight may exceed 1/64), the
+//    16-bit rounding error (2^-9 relative for bf16) is not averaged away, so
+//    that tile also gets the residual lo = rn(p - hi) as a second PV pass;
+//    rows vote per warp, and the MMA issuer runs the second pass only when
+//    some row of the tile asked for it.
 // Every wait is bounded; a wait that runs out flags PD_DEVERR_TIMEOUT and the
 // CTA drains its in-flight copies and MMAs, frees tensor memory and leaves.
 #include <cuda.h>
@@ -49,27 +54,27 @@ namespace {
 constexpr int kTileM = 128;            // query rows per tile (MMA M)
 constexpr int kTileN = 128;            // keys per tile
 constexpr int kKVStages = 2;
-constexpr int kPrefillThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kPrefillThreads = 384;   // warp 0 TMA, 1 MMA, 2-3 spare, 4-7 / 8-11 softmax A / B
 constexpr int kSoftmaxThreads = 128;
-constexpr uint32_t kTmemCols = 512;    // S0 [0,128) S1 [128,256) O [256, 256+D)
-constexpr uint32_t kTmemO = 256;
+constexpr uint32_t kTmemCols = 512;    // S_A [0,128) O_A [128,256) S_B [256,384) O_B [384,512)
 constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLoWeight = 1.0f / 64.0f;   // weight above which P's rounding is corrected
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct PrefillSmem {
     static constexpr int kAtom = kTileM * 128;          // 128 rows x 128 B (64 16-bit values)
     static constexpr int kTile = (D / 64) * kAtom;      // a [128][D] tile
-    static constexpr int kQ = 0;
-    static constexpr int kK = kQ + kTile;                // kKVStages tiles
+    static constexpr int kQ = 0;                         // Q_A, Q_B
+    static constexpr int kK = kQ + 2 * kTile;            // kKVStages tiles
     static constexpr int kV = kK + kKVStages * kTile;
     static constexpr int kBar = kV + kKVStages * kTile;
-    // barriers: q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], pv_done[2], drain
-    static constexpr int kNumBars = 12;
-    static constexpr int kMisc = kBar + kNumBars * 8;   // tmem base, abort flag, issued count
+    // barriers: q_full, kv_full[2], kv_empty[2], s_full[A,B], p_full[A,B],
+    // pv_done[A0,A1,B0,B1], drain
+    static constexpr int kNumBars = 14;
+    static constexpr int kFlags = kBar + kNumBars * 8;  // int lo_flag[2 tiles][2 parity][4 warps]
+    static constexpr int kMisc = kFlags + 16 * 4;       // tmem base, abort flag, issued count
     static constexpr int kBytes = kMisc + 16;
-    // room to align the base to 1 KB; at least 116 KB so a second CTA never
-    // shares the SM (each CTA takes all 512 tensor-memory columns)
     static constexpr int kAlloc = kBytes + 1024 > 116 * 1024 ? kBytes + 1024 : 116 * 1024;
 };
 
@@ -94,16 +99,16 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
     uint64_t* q_full = bars + 0;
-    uint64_t* kv_full = bars + 1;     // [2]
-    uint64_t* kv_empty = bars + 3;    // [2]
-    uint64_t* s_full = bars + 5;      // [2]
-    uint64_t* p_full = bars + 7;      // [2]
-    // pv_done[u & 1] completes when PV of tile u (and every earlier MMA) is
-    // done.  One barrier per tile parity keeps each wait within one phase of
-    // the barrier's state, which parity waits need (a barrier two phases
-    // behind would read as already complete).
-    uint64_t* pv_done = bars + 9;     // [2]
-    uint64_t* drain = bars + 11;
+    uint64_t* kv_full = bars + 1;     // [stage]
+    uint64_t* kv_empty = bars + 3;    // [stage]
+    uint64_t* s_full = bars + 5;      // [tile]
+    uint64_t* p_full = bars + 7;      // [tile]
+    // pv_done[tile * 2 + (u & 1)] completes when PV of key tile u (and every
+    // earlier MMA) is done.  One barrier per parity keeps each wait within one
+    // phase of the barrier's state, which parity waits need.
+    uint64_t* pv_done = bars + 9;     // [4]
+    uint64_t* drain = bars + 13;
+    volatile int32_t* lo_flag = reinterpret_cast<volatile int32_t*>(smem + L::kFlags);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L::kMisc);
     volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kMisc + 4);
     volatile int32_t* issued = reinterpret_cast<volatile int32_t*>(smem + L::kMisc + 8);
@@ -113,7 +118,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int TQ = kTileM / GP;                       // query tokens per tile
     const int q_begin = __ldg(cu_q_lens + seq);
     const int C = __ldg(cu_q_lens + seq + 1) - q_begin;
-    const int q0 = blockIdx.x * TQ;                   // first chunk token of this tile
+    const int q0 = blockIdx.x * 2 * TQ;               // first chunk token of tile A
     if (q0 >= C) return;
     const int ctx = __ldg(context_lens + seq);
     const int P = ctx - C;
@@ -126,9 +131,10 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int sub = G / GP;
     const int kvh = blockIdx.y / sub;
     const int head0 = kvh * G + (blockIdx.y % sub) * GP;
-    const int q_last = min(C, q0 + TQ) - 1;
-    const int n_keys = P + q_last + 1;
-    const int n_tiles = (n_keys + kTileN - 1) / kTileN;
+    const bool has_b = q0 + TQ < C;
+    const int n_a = (P + min(C, q0 + TQ) + kTileN - 1) / kTileN;            // key tiles of A
+    const int n_b = has_b ? (P + min(C, q0 + 2 * TQ) + kTileN - 1) / kTileN : 0;
+    const int n_tiles = max(n_a, n_b);
     const int n_blocks_ctx = (ctx + S - 1) / S;
     const int32_t* bt_row = block_tables + (int64_t)seq * max_blocks_per_seq;
 
@@ -138,14 +144,13 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < kKVStages; ++s) {
+        for (int s = 0; s < 2; ++s) {
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
             mbar_init(&s_full[s], 1);
             mbar_init(&p_full[s], kSoftmaxThreads);
         }
-        mbar_init(&pv_done[0], 1);
-        mbar_init(&pv_done[1], 1);
+        for (int s = 0; s < 4; ++s) mbar_init(&pv_done[s], 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         *issued = 0;
@@ -166,10 +171,14 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
-            mbar_arrive_expect_tx(q_full, uint32_t(kTileM) * D * 2);
-            for (int a = 0; a < kAtoms; ++a)
+            mbar_arrive_expect_tx(q_full, uint32_t(has_b ? 2 : 1) * kTileM * D * 2);
+            for (int a = 0; a < kAtoms; ++a) {
                 tc::tma_load_3d(smem + L::kQ + a * L::kAtom, &tm_q, a * 64, head0, q_begin + q0,
                                 q_full);
+                if (has_b)
+                    tc::tma_load_3d(smem + L::kQ + L::kTile + a * L::kAtom, &tm_q, a * 64, head0,
+                                    q_begin + q0 + TQ, q_full);
+            }
         }
         const int blocks_per_tile = kTileN / S;            // 2 .. 16
         for (int t = 0; t < n_tiles; ++t) {
@@ -211,44 +220,61 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
     } else if (warp == 1) {
         // ------------------------------ MMA issuer --------------------------------
         if (lane == 0) {
+            auto qk = [&](int x, int t) {
+                const uint32_t d_s = tmem + uint32_t(x) * 256;
+                const int st = t & 1;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * L::kAtom + (kk & 3) * 32;
+                    const uint64_t a = tc::smem_desc_sw128(sQ + x * L::kTile + koff, 16, 1024);
+                    const uint64_t b = tc::smem_desc_sw128(sK + st * L::kTile + koff, 16, 1024);
+                    tc::mma_ss(d_s, a, b, kIdescQK, kk > 0);
+                }
+                tc::commit(&s_full[x]);
+            };
+            auto pv = [&](int x, int t) {
+                const int st = t & 1;
+                const bool lo = (lo_flag[x * 8 + st * 4 + 0] | lo_flag[x * 8 + st * 4 + 1] |
+                                 lo_flag[x * 8 + st * 4 + 2] | lo_flag[x * 8 + st * 4 + 3]) != 0;
+                const uint32_t d_o = tmem + uint32_t(x) * 256 + 128;
+                // P over S: chunk c (keys 32c..32c+31) holds hi in columns
+                // 32c..32c+15 and lo in 32c+16..32c+31
+                for (int pass = 0; pass < (lo ? 2 : 1); ++pass) {
+#pragma unroll
+                    for (int kk = 0; kk < kTileN / 16; ++kk) {
+                        // V tile as an MN-major operand: N = D contiguous in 64-wide
+                        // atoms (LBO between them), K = keys at 128 B (SBO per 8 keys)
+                        const uint64_t b = tc::smem_desc_sw128(
+                            sV + st * L::kTile + kk * 16 * 128, L::kAtom, 1024);
+                        tc::mma_ts(d_o,
+                                   tmem + uint32_t(x) * 256 + 32 * (kk >> 1) + 16 * pass +
+                                       8 * (kk & 1),
+                                   b, kIdescPV, (t > 0 || kk > 0 || pass > 0));
+                    }
+                }
+                tc::commit(&pv_done[x * 2 + (t & 1)]);
+            };
             bool ok = mbar_wait(q_full, 0);
-            for (int t = 0; ok && t <= n_tiles; ++t) {
+            if (ok && (ok = mbar_wait(&kv_full[0], 0))) {
+                tc::fence_after_sync();
+                if (n_a > 0) qk(0, 0);
+                if (n_b > 0) qk(1, 0);
+            }
+            for (int t = 0; ok && t < n_tiles; ++t) {
                 if (*abort_flag) { ok = false; break; }
-                if (t < n_tiles) {
-                    const int st = t & 1;
-                    if (!(ok = mbar_wait(&kv_full[st], (t >> 1) & 1))) break;
+                for (int x = 0; x < 2 && ok; ++x) {
+                    const int nx = x == 0 ? n_a : n_b;
+                    if (t >= nx) continue;
+                    if (!(ok = mbar_wait(&p_full[x], t & 1))) break;
                     tc::fence_after_sync();
-                    const uint32_t d_s = tmem + uint32_t(st) * kTileN;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t koff = (kk >> 2) * L::kAtom + (kk & 3) * 32;
-                        const uint64_t a = tc::smem_desc_sw128(sQ + koff, 16, 1024);
-                        const uint64_t b = tc::smem_desc_sw128(sK + st * L::kTile + koff, 16, 1024);
-                        tc::mma_ss(d_s, a, b, kIdescQK, kk > 0);
+                    pv(x, t);
+                    if (t + 1 < nx) {
+                        if (!(ok = mbar_wait(&kv_full[(t + 1) & 1], ((t + 1) >> 1) & 1))) break;
+                        tc::fence_after_sync();
+                        qk(x, t + 1);
                     }
-                    tc::commit(&s_full[st]);
                 }
-                if (t > 0) {
-                    const int u = t - 1, su = u & 1;
-                    if (!(ok = mbar_wait(&p_full[su], (u >> 1) & 1))) break;
-                    tc::fence_after_sync();
-                    // P_hi in columns [0, 64) of the S buffer, P_lo in [64, 128)
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-#pragma unroll
-                        for (int kk = 0; kk < kTileN / 16; ++kk) {
-                            // V tile as an MN-major operand: N = D contiguous in 64-wide
-                            // atoms (LBO between them), K = keys at 128 B (SBO per 8 keys)
-                            const uint64_t b = tc::smem_desc_sw128(
-                                sV + su * L::kTile + kk * 16 * 128, L::kAtom, 1024);
-                            tc::mma_ts(tmem + kTmemO,
-                                       tmem + uint32_t(su) * kTileN + half * 64 + kk * 8, b,
-                                       kIdescPV, (u > 0 || kk > 0 || half > 0));
-                        }
-                    }
-                    tc::commit(&pv_done[su]);
-                    tc::commit(&kv_empty[su]);
-                }
+                if (ok) tc::commit(&kv_empty[t & 1]);
             }
             if (!ok) {
                 flag_error(dev_err, PD_DEVERR_TIMEOUT);
@@ -256,43 +282,45 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp >= 4) {
         // --------------------------- softmax + epilogue ---------------------------
+        const int x = warp >= 8 ? 1 : 0;               // tile A or B
+        const int nx = x == 0 ? n_a : n_b;
         const int quarter = warp & 3;                  // tensor-memory lane quarter
         const int r = quarter * 32 + lane;             // tile row
         const int tok = r / GP;                        // token within the tile
         const int g = r % GP;
-        const int pos = P + q0 + tok;                  // position of this query
+        const int qx0 = q0 + x * TQ;                   // first chunk token of this tile
+        const int pos = P + qx0 + tok;                 // position of this query
         const int lim = min(pos, ctx - 1);             // last visible key
-        const bool row_valid = q0 + tok < C;
+        const bool row_valid = qx0 + tok < C;
         const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+        const uint32_t s_cols = tmem + lane_base + uint32_t(x) * 256;
+        const uint32_t o_cols = s_cols + 128;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        for (int t = 0; t < n_tiles; ++t) {
+        for (int t = 0; t < nx; ++t) {
             const int st = t & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[st], (t >> 1) & 1));
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], t & 1));
             if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) break;
             tc::fence_after_sync();
-            uint32_t sr[kTileN];
-#pragma unroll
-            for (int c = 0; c < kTileN / 32; ++c)
-                tc::tmem_ld32(tmem + lane_base + uint32_t(st) * kTileN + c * 32,
-                              *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-            tc::tmem_ld_wait();
             const int kbase = t * kTileN;
-            if (kbase + kTileN - 1 > lim) {            // tile crosses this row's limit
+            const bool masked = kbase + kTileN - 1 > lim;     // tile crosses this row's limit
+            // ---- pass 1: row max
+            float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int c = 0; c < kTileN; ++c)
-                    if (kbase + c > lim) sr[c] = __float_as_uint(-INFINITY);
+            for (int c = 0; c < kTileN / 32; ++c) {
+                uint32_t sr[32];
+                tc::tmem_ld32(s_cols + c * 32, sr);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    float v = __uint_as_float(sr[e]);
+                    if (masked && kbase + c * 32 + e > lim) v = -INFINITY;
+                    mxs[e & 3] = fmaxf(mxs[e & 3], v);
+                }
             }
-            float mxs[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) mxs[k] = __uint_as_float(sr[k]);
-#pragma unroll
-            for (int c = 8; c < kTileN; ++c) mxs[c & 7] = fmaxf(mxs[c & 7], __uint_as_float(sr[c]));
-            const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
-                                   fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
-            const float m_tile = mx * scale_log2;
+            const float m_tile = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])) * scale_log2;
             // The tensor-memory loads and stores below are warp-collective, so
             // the warp rescales together when any of its rows needs it; each
             // row uses its own exact factor (1 when its max did not grow).
@@ -300,57 +328,70 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                 const float m_new = fmaxf(m_run, m_tile);
                 const float alpha = ex2(m_run - m_new);    // 0 on the first tile
                 if (t > 0) {
-                    // O holds PV of tiles < t; wait for the last of them, then scale.
-                    ok = __all_sync(0xffffffffu,
-                                    mbar_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1));
+                    // O holds PV of tiles < t (already complete: QK of tile t
+                    // was issued after PV of tile t-1); wait anyway, cheaply.
+                    ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[x * 2 + ((t - 1) & 1)],
+                                                           ((t - 1) >> 1) & 1));
                     if (!ok) break;
                     tc::fence_after_sync();
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t o[32];
-                        tc::tmem_ld32(tmem + lane_base + kTmemO + c * 32, o);
+                        tc::tmem_ld32(o_cols + c * 32, o);
                         tc::tmem_ld_wait();
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tc::tmem_st32(tmem + lane_base + kTmemO + c * 32, o);
+                        tc::tmem_st32(o_cols + c * 32, o);
                     }
                     tc::tmem_st_wait();
                 }
                 l_run *= alpha;
                 m_run = m_new;
             }
-            // p = 2^(s * scale_log2 - m) as hi + lo 16-bit values
-            uint32_t phi[kTileN / 2], plo[kTileN / 2];
-            float2 lsum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                              make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            // Does some key of this tile carry a weight that may exceed
+            // kLoWeight?  max weight <= p_max / (l_before + p_max).
+            const float p_max = m_tile == -INFINITY ? 0.f : ex2(m_tile - m_run);
+            const bool need_lo = __any_sync(0xffffffffu, p_max > kLoWeight * (l_run + p_max));
+            // ---- pass 2: p = 2^(s * scale_log2 - m), written over S as hi (+ lo)
             const float2 sc2 = make_float2(scale_log2, scale_log2);
             const float2 nm2 = make_float2(-m_run, -m_run);
             const float2 neg1 = make_float2(-1.f, -1.f);
             const float2 one2 = make_float2(1.f, 1.f);
+            float2 lsum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll 1
+            for (int c = 0; c < kTileN / 32; ++c) {
+                uint32_t sr[32];
+                tc::tmem_ld32(s_cols + c * 32, sr);
+                tc::tmem_ld_wait();
+                uint32_t hi[16], lo[16];
 #pragma unroll
-            for (int c = 0; c < kTileN / 2; ++c) {
-                const float2 x = ffma2(make_float2(__uint_as_float(sr[2 * c]),
-                                                   __uint_as_float(sr[2 * c + 1])), sc2, nm2);
-                const float2 p = make_float2(ex2(x.x), ex2(x.y));
-                lsum[c & 3] = ffma2(p, one2, lsum[c & 3]);
-                phi[c] = E::pack2(p.x, p.y);
-                const float2 lo = ffma2(E::unpack2(phi[c]), neg1, p);   // p - hi, exact
-                plo[c] = E::pack2(lo.x, lo.y);
+                for (int e = 0; e < 16; ++e) {
+                    float s0 = __uint_as_float(sr[2 * e]), s1 = __uint_as_float(sr[2 * e + 1]);
+                    if (masked && kbase + c * 32 + 2 * e > lim) s0 = -INFINITY;
+                    if (masked && kbase + c * 32 + 2 * e + 1 > lim) s1 = -INFINITY;
+                    const float2 xx = ffma2(make_float2(s0, s1), sc2, nm2);
+                    const float2 p = make_float2(ex2(xx.x), ex2(xx.y));
+                    lsum[e & 1] = ffma2(p, one2, lsum[e & 1]);
+                    hi[e] = E::pack2(p.x, p.y);
+                    if (need_lo) {
+                        const float2 d = ffma2(E::unpack2(hi[e]), neg1, p);   // p - hi, exact
+                        lo[e] = E::pack2(d.x, d.y);
+                    } else {
+                        lo[e] = 0u;
+                    }
+                }
+                tc::tmem_st16(s_cols + c * 32, hi);
+                tc::tmem_st16(s_cols + c * 32 + 16, lo);
             }
-            l_run += ((lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y)) +
-                     ((lsum[2].x + lsum[2].y) + (lsum[3].x + lsum[3].y));
-#pragma unroll
-            for (int c = 0; c < kTileN / 64; ++c) {
-                tc::tmem_st32(tmem + lane_base + uint32_t(st) * kTileN + c * 32,
-                              *reinterpret_cast<const uint32_t(*)[32]>(&phi[c * 32]));
-                tc::tmem_st32(tmem + lane_base + uint32_t(st) * kTileN + 64 + c * 32,
-                              *reinterpret_cast<const uint32_t(*)[32]>(&plo[c * 32]));
-            }
+            l_run += (lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y);
             tc::tmem_st_wait();
-            if (kbase + kTileN > ctx) {
-                // Keys past the context in the last tile: their V rows hold other
-                // data (or were never loaded); zero them so 0 * v stays 0.
+            if (lane == 0) lo_flag[x * 8 + st * 4 + quarter] = need_lo ? 1 : 0;
+            // Keys past the context in the last tile: their V rows hold other
+            // data (or were never loaded); zero them so 0 * v stays 0.  The
+            // first tile to use this stage does it.
+            const bool zero_v = kbase + kTileN > ctx && (x == 0 || t >= n_a);
+            if (zero_v) {
                 ok = __all_sync(0xffffffffu, mbar_wait(&kv_full[st], (t >> 1) & 1));
                 if (!ok) break;
                 if (kbase + r >= ctx) {
@@ -362,22 +403,22 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                             *reinterpret_cast<uint4*>(vrow + a * L::kAtom + c * 16) =
                                 make_uint4(0u, 0u, 0u, 0u);
                 }
+                tc::fence_proxy_async_smem();
             }
-            if (kbase + kTileN > ctx) tc::fence_proxy_async_smem();
             tc::fence_before_sync();
-            mbar_arrive(&p_full[st]);
+            mbar_arrive(&p_full[x]);
         }
-        if (ok && !__any_sync(0xffffffffu, *abort_flag != 0)) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(n_tiles - 1) & 1],
-                                                   ((n_tiles - 1) >> 1) & 1));
+        if (ok && nx > 0 && !__any_sync(0xffffffffu, *abort_flag != 0)) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[x * 2 + ((nx - 1) & 1)],
+                                                   ((nx - 1) >> 1) & 1));
             if (ok) {
                 tc::fence_after_sync();
                 const float inv = 1.f / l_run;
-                T* orow = out + ((int64_t)(q_begin + q0 + tok) * H + head0 + g) * D;
+                T* orow = out + ((int64_t)(q_begin + qx0 + tok) * H + head0 + g) * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
-                    tc::tmem_ld32(tmem + lane_base + kTmemO + c * 32, o);
+                    tc::tmem_ld32(o_cols + c * 32, o);
                     tc::tmem_ld_wait();
                     uint32_t pk2[16];
 #pragma unroll
@@ -448,7 +489,8 @@ pd_status launch_prefill_t(const PrefillArgs& a) {
         if (e != cudaSuccess) return launch_result(e);
         if (dev < 64) attr_set |= uint64_t(1) << dev;
     }
-    dim3 grid(unsigned((a.max_q_len + TQ - 1) / TQ), unsigned(a.Hk * (G / GP)), unsigned(a.B));
+    dim3 grid(unsigned((a.max_q_len + 2 * TQ - 1) / (2 * TQ)), unsigned(a.Hk * (G / GP)),
+              unsigned(a.B));
     kern<<<grid, kPrefillThreads, L::kAlloc, a.stream>>>(
         tm_q, tm_k, tm_v, static_cast<T*>(a.out), a.total_q, a.cu_q_lens, a.block_tables,
         a.max_blocks_per_seq, a.context_lens, a.H, a.Hk, a.S, a.NB, GP, a.scale * kLog2e,
