@@ -60,6 +60,11 @@ constexpr uint32_t kTmemCols = 512;    // S_A [0,128) O_A [128,256) S_B [256,384
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLoWeight = 1.0f / 64.0f;   // weight above which P's rounding is corrected
 constexpr float kLog2e = 1.4426950408889634f;
+// Register split (384 threads launched at 168 each = 64512): the TMA/MMA
+// warpgroup keeps 64, the two softmax warpgroups take 216, which holds a
+// whole 128-column S row in registers.  128*64 + 256*216 = 63488 <= 64512.
+constexpr uint32_t kRegsControl = 64;
+constexpr uint32_t kRegsSoftmax = 216;
 
 template <int D>
 struct PrefillSmem {
@@ -168,6 +173,10 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
+    if (warp < 4) {
+    // One register release for the whole control warpgroup (setmaxnreg is
+    // warpgroup-aligned), then the warps take their roles.
+    tc::regs_dec<kRegsControl>();
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
@@ -282,8 +291,10 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    }                                                  // warps 2, 3: spare
+    } else {
         // --------------------------- softmax + epilogue ---------------------------
+        tc::regs_inc<kRegsSoftmax>();
         const int x = warp >= 8 ? 1 : 0;               // tile A or B
         const int nx = x == 0 ? n_a : n_b;
         const int quarter = warp & 3;                  // tensor-memory lane quarter
@@ -306,19 +317,24 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
             tc::fence_after_sync();
             const int kbase = t * kTileN;
             const bool masked = kbase + kTileN - 1 > lim;     // tile crosses this row's limit
-            // ---- pass 1: row max
+            // ---- the whole S row into registers (one burst of loads)
+            uint32_t sr[kTileN];
+#pragma unroll
+            for (int c = 0; c < kTileN / 32; ++c)
+                tc::tmem_ld32(s_cols + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+            tc::tmem_ld_wait();
+            if (masked) {                              // only tiles that cross the limit
+#pragma unroll
+                for (int e = 0; e < kTileN; ++e)
+                    if (kbase + e > lim) sr[e] = __float_as_uint(-INFINITY);
+            }
             float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < kTileN / 32; ++c) {
-                uint32_t sr[32];
-                tc::tmem_ld32(s_cols + c * 32, sr);
-                tc::tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float v = __uint_as_float(sr[e]);
-                    if (masked && kbase + c * 32 + e > lim) v = -INFINITY;
-                    mxs[e & 3] = fmaxf(mxs[e & 3], v);
-                }
+            for (int e = 0; e < kTileN; e += 8) {
+                mxs[0] = fmax3(mxs[0], __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+                mxs[1] = fmax3(mxs[1], __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
+                mxs[2] = fmax3(mxs[2], __uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5]));
+                mxs[3] = fmax3(mxs[3], __uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7]));
             }
             const float m_tile = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])) * scale_log2;
             // The tensor-memory loads and stores below are warp-collective, so
@@ -353,30 +369,23 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
             // kLoWeight?  max weight <= p_max / (l_before + p_max).
             const float p_max = m_tile == -INFINITY ? 0.f : ex2(m_tile - m_run);
             const bool need_lo = __any_sync(0xffffffffu, p_max > kLoWeight * (l_run + p_max));
-            // ---- pass 2: p = 2^(s * scale_log2 - m), written over S as hi (+ lo)
-            const float2 sc2 = make_float2(scale_log2, scale_log2);
-            const float2 nm2 = make_float2(-m_run, -m_run);
-            const float2 neg1 = make_float2(-1.f, -1.f);
-            const float2 one2 = make_float2(1.f, 1.f);
-            float2 lsum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll 1
+            // ---- p = 2^(s * scale_log2 - m), written over S as hi (+ lo) per
+            // 32-column chunk (keys 32c..32c+31 -> columns 32c.. hi, 32c+16.. lo)
+            const float nm = -m_run;
+            float lsum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
             for (int c = 0; c < kTileN / 32; ++c) {
-                uint32_t sr[32];
-                tc::tmem_ld32(s_cols + c * 32, sr);
-                tc::tmem_ld_wait();
                 uint32_t hi[16], lo[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    float s0 = __uint_as_float(sr[2 * e]), s1 = __uint_as_float(sr[2 * e + 1]);
-                    if (masked && kbase + c * 32 + 2 * e > lim) s0 = -INFINITY;
-                    if (masked && kbase + c * 32 + 2 * e + 1 > lim) s1 = -INFINITY;
-                    const float2 xx = ffma2(make_float2(s0, s1), sc2, nm2);
-                    const float2 p = make_float2(ex2(xx.x), ex2(xx.y));
-                    lsum[e & 1] = ffma2(p, one2, lsum[e & 1]);
-                    hi[e] = E::pack2(p.x, p.y);
+                    const float p0 = ex2(fmaf(__uint_as_float(sr[c * 32 + 2 * e]), scale_log2, nm));
+                    const float p1 =
+                        ex2(fmaf(__uint_as_float(sr[c * 32 + 2 * e + 1]), scale_log2, nm));
+                    lsum[e & 3] += p0 + p1;
+                    hi[e] = E::pack2(p0, p1);
                     if (need_lo) {
-                        const float2 d = ffma2(E::unpack2(hi[e]), neg1, p);   // p - hi, exact
-                        lo[e] = E::pack2(d.x, d.y);
+                        const float2 h = E::unpack2(hi[e]);
+                        lo[e] = E::pack2(p0 - h.x, p1 - h.y);   // exact differences
                     } else {
                         lo[e] = 0u;
                     }
@@ -384,7 +393,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                 tc::tmem_st16(s_cols + c * 32, hi);
                 tc::tmem_st16(s_cols + c * 32 + 16, lo);
             }
-            l_run += (lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y);
+            l_run += (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
             tc::tmem_st_wait();
             if (lane == 0) lo_flag[x * 8 + st * 4 + quarter] = need_lo ? 1 : 0;
             // Keys past the context in the last tile: their V rows hold other
