@@ -5,7 +5,7 @@ Headline (one JSON line on stdout, rank 0): the Qwen3-8B-shaped single-layer
 decode step -- batch 64, 32 Q heads, 8 KV heads, head_dim 128, block 16,
 bf16, context lengths uniform on [128, 2048], pool 1.5x the blocks needed --
 where one step is the store of the 64 new tokens (pd_reshape_and_cache) and
-split-context decode attention with its reduce (pd_paged_attention_decode).
+split-context decode attention, pieces merged in-kernel (pd_paged_attention_decode).
 ``value`` is the step's algorithmic bytes (K/V read once, q, out, tables and
 the stored tokens) per second of device time, inputs resident in HBM, L2
 flushed (256 MiB read) before every timed step.
@@ -247,13 +247,13 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": "qwen3_8b_decode_step", "batch": B, "q_heads": H, "kv_heads": Hk,
                    "head_dim": D, "block_size": S, "context_lens": "uniform [128, 2048], seed 0",
                    "kv_tokens": int(sum(ctx)), "pool_blocks": c.pool.NB,
-                   "step": "store 64 tokens + split-context decode + reduce",
+                   "step": "store 64 tokens + split-context decode (one launch, in-kernel merge)",
                    "l2": "inputs larger than L2 (KV 321 MB vs 129 MB L2), and L2 flushed "
                          "before every timed step by reading a 256 MiB buffer",
                    "parallelism": f"replicas x{world}"},
         "pct_of_hbm_peak": round(100 * value / world / hbm_peak, 2),
         "kv_tokens_per_s": round(world * sum(ctx) * args.steps / step_s, 1),
-        "roofline": {"kernel": "paged_decode (split + reduce)", "bound": "hbm",
+        "roofline": {"kernel": "paged_decode_split_kernel", "bound": "hbm",
                      "achieved": round(achieved, 2), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
                      "alg_bytes_per_launch": dec_bytes,

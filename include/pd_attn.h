@@ -110,15 +110,20 @@ PD_API pd_status pd_reshape_and_cache(const void* key, const void* value,
  *   context_lens  int32 [B], each <= max_context_len (the caller's promise,
  *                 checked on device: PD_DEVERR_CTX_RANGE, the context is
  *                 then cut to max_context_len and to what the table holds)
- * The batch's work is cut into equal contiguous runs of 64-token stages, one
- * per resident CTA, so a long context may be split across CTAs (online
- * softmax per piece, pieces kept in `workspace`) and merged by a second
- * kernel; a context that one CTA finishes is written directly.
+ * One kernel launch.  The batch's work is cut into equal contiguous runs of
+ * 64-token stages, one per resident CTA, so a long context may be split
+ * across CTAs (online softmax per piece, pieces kept in `workspace`); the
+ * CTA that finishes a context's last outstanding piece merges the pieces in
+ * fixed order.  A context that one CTA finishes is written directly.
  *   workspace     device scratch of at least
  *                 pd_decode_workspace_bytes(B, H, D, max_context_len) bytes
  *                 (always > 0), 256-byte aligned.  Nothing in it needs to
- *                 start at zero.  Overwritten; callers sharing one workspace
- *                 on two streams race.  PD_ERR_WORKSPACE_TOO_SMALL if short. */
+ *                 start at zero: pieces are written before they are read in
+ *                 the same launch, and the per-context arrival counters carry
+ *                 a per-launch tag, so whatever an earlier launch (or other
+ *                 data) left there counts as zero.  Overwritten; callers
+ *                 sharing one workspace on two streams race.
+ *                 PD_ERR_WORKSPACE_TOO_SMALL if short. */
 PD_API size_t pd_decode_workspace_bytes(int B, int H, int D, int max_context_len);
 /* Token granule of the work split: a CTA takes at least this many tokens
  * before another CTA shares a context, so one context is cut into at most
@@ -150,8 +155,8 @@ PD_API pd_status pd_paged_attention_decode(void* out, const void* q,
  * - The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call
  *   before any stream capture on the device.
- * - Nothing in the scratch needs to start at zero: every entry a launch
- *   reads was written earlier in the same launch.
+ * - Nothing in the scratch needs to start at zero (as for the workspace of
+ *   pd_paged_attention_decode).
  * - All calls share the one array: calls that may overlap on the GPU (other
  *   streams, other host threads) race and must be serialised by the caller.
  * - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */

@@ -30,14 +30,25 @@
 //    (hi = rn(p), lo = rn(p - hi)), two MMAs per tile, so P carries about
 //    2^-17 relative error instead of the 2^-9 of a single bf16;
 //  * at the end of each stream piece the four warps merge through a small
-//    exchange buffer; a whole stream is normalised and written to `out`,
-//    a piece leaves (max, sum, unnormalised o) in the workspace, and a
-//    reduce kernel (programmatic dependent launch) merges the pieces in
-//    fixed order.  No atomics touch results: outputs are bit-identical for
-//    any placement of blocks in the pool.
+//    exchange buffer; a whole stream is normalised and written to `out`.
+//    A piece of a longer stream leaves (max, sum, unnormalised o) in the
+//    workspace and counts itself on the stream's arrival counter; the CTA
+//    that brings the count to the number of pieces merges them all, in
+//    fixed piece order, and writes `out`.  No second kernel, and no atomics
+//    touch results: outputs are bit-identical for any placement of blocks
+//    in the pool and any order in which CTAs finish.
+//  * arrival counters need no clearing between calls: each 64-bit counter
+//    carries the tag of the launch that last counted on it (high 44 bits)
+//    beside its count (low 20 bits), and a counter holding another launch's
+//    tag reads as zero.  Tags are distinct per launch within a process and
+//    salted per process.
 #include <cuda_runtime.h>
 
+#include <unistd.h>
+
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cmath>
 
 #include "pd_device.cuh"
@@ -172,6 +183,65 @@ __device__ __forceinline__ bool consumers_any(bool pred) {
     return r != 0;
 }
 
+// Count one arrived piece on a stream's tagged counter; true for the piece
+// that completes the stream.  High 44 bits: launch tag; low 20: count.
+constexpr unsigned long long kCountBits = 20;
+constexpr unsigned long long kCountMask = (1ull << kCountBits) - 1;
+
+__device__ __forceinline__ bool arrive_piece(unsigned long long* cnt, unsigned long long tag,
+                                             int nseg) {
+    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(cnt);
+    for (;;) {
+        const unsigned long long next =
+            (cur >> kCountBits) == tag ? cur + 1 : (tag << kCountBits) | 1ull;
+        const unsigned long long seen = atomicCAS(cnt, cur, next);
+        if (seen == cur) return int(next & kCountMask) == nseg;
+        cur = seen;
+    }
+}
+
+// Merge the np pieces of one (sequence, q head) row, one warp, fixed order:
+// M = max_k m_k; out = sum_k o_k 2^(m_k - M) / sum_k l_k 2^(m_k - M).
+// Pieces of other CTAs are read through L2 (ld.global.cg).
+template <typename T, int D>
+__device__ __forceinline__ void merge_pieces(T* __restrict__ out_row, const float* o_rows,
+                                             const float* m, const float* l, int np, int lane) {
+    using E = Elem<T>;
+    constexpr int DV = D / 32;
+    float M = -INFINITY;
+    for (int p = lane; p < np; p += 32) M = fmaxf(M, __ldcg(m + p));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float acc[DV];
+#pragma unroll
+    for (int e = 0; e < DV; ++e) acc[e] = 0.f;
+    float lsum = 0.f;
+    for (int p0 = 0; p0 < np; p0 += 32) {
+        const int p = p0 + lane;
+        const float mp = p < np ? __ldcg(m + p) : -INFINITY;
+        const float w = mp != -INFINITY ? ex2(mp - M) : 0.f;
+        lsum += p < np ? __ldcg(l + p) * w : 0.f;
+        const int n = min(32, np - p0);
+        for (int u = 0; u < n; ++u) {
+            const float wu = __shfl_sync(0xffffffffu, w, u);
+            const float* o = o_rows + (p0 + u) * D + lane * DV;
+            if constexpr (DV == 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(o));
+                acc[0] += v.x * wu; acc[1] += v.y * wu; acc[2] += v.z * wu; acc[3] += v.w * wu;
+            } else {
+                const float2 v = __ldcg(reinterpret_cast<const float2*>(o));
+                acc[0] += v.x * wu; acc[1] += v.y * wu;
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    const float inv = 1.f / lsum;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(out_row + lane * DV);
+#pragma unroll
+    for (int e = 0; e < DV / 2; ++e) dst[e] = E::pack2(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -181,7 +251,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                           int B, int H, int Hk, int S, int NB, int GH, float scale_log2,
                           int max_segs, int cap, float* __restrict__ ws_o,
                           float* __restrict__ ws_m, float* __restrict__ ws_l,
-                          int2* __restrict__ ws_seg, int32_t* dev_err) {
+                          unsigned long long* __restrict__ ws_cnt, unsigned long long tag,
+                          int32_t* dev_err) {
     using L = DecodeSmem<D>;
     using E = Elem<T>;
     constexpr int kAtoms = D / 64;
@@ -194,8 +265,6 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     uint64_t* empty = full + kStages;
     volatile int32_t* abort_flag = reinterpret_cast<int32_t*>(smem + L::kMisc);
     volatile int32_t* issued = reinterpret_cast<int32_t*>(smem + L::kMisc + 4);
-
-    pdl_launch_dependents();
 
     const int G = H / Hk;
     const int groups = G / GH;
@@ -214,6 +283,18 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         tc::prefetch_tmap(&tm_v);
     }
     __syncthreads();
+
+    // Rows of empty contexts get zeros (no stream covers them); contexts
+    // outside [0, cap] are flagged (and cut to cap by the walk).
+    for (int s = blockIdx.x; s < B; s += gridDim.x) {
+        const int raw = __ldg(context_lens + s);
+        if ((raw < 0 || raw > cap) && threadIdx.x == 0) flag_error(dev_err, PD_DEVERR_CTX_RANGE);
+        if (raw <= 0) {
+            uint4* dst = reinterpret_cast<uint4*>(out + (int64_t)s * H * D);
+            for (int i = threadIdx.x; i < H * D * 2 / 16; i += blockDim.x)
+                dst[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
 
     Walk w;
     if (!walk_begin(w, context_lens, B, units, cap)) return;   // uniform: no range
@@ -456,7 +537,6 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 const int hh = ha + h;
                 if (hh >= GH) continue;
                 const int64_t row = (int64_t)w.s * H + h0 + hh;
-                if (seg == 0 && d0 == 0) ws_seg[row] = make_int2(int(c_first), nseg);
                 if (nseg == 1) {
                     // the whole stream was here: final, normalised output
                     const float inv = 1.f / l_run[h];
@@ -480,6 +560,25 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                     }
                 }
             }
+            if (nseg > 1) {
+                // publish this piece, count it; the last of the stream's
+                // pieces to arrive merges them all
+                __threadfence();
+                __syncwarp();
+                uint32_t last = 0;
+                if (lane == 0)
+                    last = arrive_piece(ws_cnt + (int64_t)w.s * units + w.u, tag, nseg) ? 1u : 0u;
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+                    for (int hh = 0; hh < GH; ++hh) {
+                        const int64_t row = (int64_t)w.s * H + h0 + hh;
+                        merge_pieces<T, D>(out + row * D, ws_o + row * max_segs * D,
+                                           ws_m + row * max_segs, ws_l + row * max_segs, nseg,
+                                           lane);
+                    }
+                }
+            }
         }
         // the exchange buffer is rewritten by the next piece's merge
         asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
@@ -498,78 +597,29 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
 }
 
-// Merge the pieces of each (sequence, q head) stream: one warp per row, fixed
-// order.  M = max_k m_k; out = sum_k o_k 2^(m_k - M) / sum_k l_k 2^(m_k - M).
-// Rows whose stream was finished in one CTA were written by the split
-// kernel; empty contexts give zeros.
-constexpr int kReduceWarps = 4;
-
-template <typename T, int D>
-__global__ void __launch_bounds__(kReduceWarps * 32)
-paged_decode_reduce_kernel(T* __restrict__ out, const int32_t* __restrict__ context_lens,
-                           int B, int H, int max_segs, int cap,
-                           const float* __restrict__ ws_o, const float* __restrict__ ws_m,
-                           const float* __restrict__ ws_l, const int2* __restrict__ ws_seg,
-                           int32_t* dev_err) {
-    using E = Elem<T>;
-    constexpr int DV = D / 32;
-    pdl_wait_primary();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t row = int64_t(blockIdx.x) * kReduceWarps + warp;
-    if (row >= int64_t(B) * H) return;
-    const int seq = int(row / H);
-    int ctx = __ldg(context_lens + seq);
-    if (ctx < 0 || ctx > cap) {
-        // longer than the table or the caller's max_context_len: it was cut
-        if (lane == 0 && row % H == 0) flag_error(dev_err, PD_DEVERR_CTX_RANGE);
-        ctx = ctx < 0 ? 0 : cap;
-    }
-    uint32_t* dst = reinterpret_cast<uint32_t*>(out + row * D + lane * DV);
-    if (ctx == 0) {
-#pragma unroll
-        for (int e = 0; e < DV / 2; ++e) dst[e] = 0u;
-        return;
-    }
-    const int np = ws_seg[row].y;
-    if (np <= 1 || np > max_segs) return;     // finished by the split kernel
-    const float* m = ws_m + row * max_segs;
-    const float* l = ws_l + row * max_segs;
-    float M = -INFINITY;
-    for (int p = lane; p < np; p += 32) M = fmaxf(M, m[p]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float acc[DV];
-#pragma unroll
-    for (int e = 0; e < DV; ++e) acc[e] = 0.f;
-    float lsum = 0.f;
-    for (int p0 = 0; p0 < np; p0 += 32) {
-        const int p = p0 + lane;
-        const float w = p < np && m[p] != -INFINITY ? ex2(m[p] - M) : 0.f;
-        lsum += p < np ? l[p] * w : 0.f;
-        const int n = min(32, np - p0);
-        for (int u = 0; u < n; ++u) {
-            const float wu = __shfl_sync(0xffffffffu, w, u);
-            const float* o = ws_o + (row * max_segs + p0 + u) * D + lane * DV;
-            if constexpr (DV == 4) {
-                const float4 v = *reinterpret_cast<const float4*>(o);
-                acc[0] += v.x * wu; acc[1] += v.y * wu; acc[2] += v.z * wu; acc[3] += v.w * wu;
-            } else {
-                const float2 v = *reinterpret_cast<const float2*>(o);
-                acc[0] += v.x * wu; acc[1] += v.y * wu;
-            }
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-    const float inv = 1.f / lsum;
-#pragma unroll
-    for (int e = 0; e < DV / 2; ++e) dst[e] = E::pack2(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+// Launch tags for the arrival counters: 44 bits, never 0, distinct for
+// every launch of this process (a salted counter).
+unsigned long long next_launch_tag() {
+    static const unsigned long long salt = [] {
+        unsigned long long x = uint64_t(std::chrono::steady_clock::now().time_since_epoch().count());
+        x ^= uint64_t(reinterpret_cast<uintptr_t>(&salt)) << 17;
+        x ^= uint64_t(getpid()) << 40;
+        // splitmix64 finaliser to spread the bits
+        x ^= x >> 30; x *= 0xbf58476d1ce4e5b9ull;
+        x ^= x >> 27; x *= 0x94d049bb133111ebull;
+        x ^= x >> 31;
+        return x;
+    }();
+    static std::atomic<unsigned long long> counter{0};
+    const unsigned long long t = (salt + counter.fetch_add(1, std::memory_order_relaxed)) &
+                                 ((1ull << (64 - kCountBits)) - 1);
+    return t == 0 ? 1 : t;
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-    size_t o, m, l, seg, total;
+    size_t o, m, l, cnt, total;
 };
 
 WsLayout ws_layout(int B, int H, int D, int P) {
@@ -578,8 +628,8 @@ WsLayout ws_layout(int B, int H, int D, int P) {
     w.o = 0;
     w.m = align256(rows * P * D * sizeof(float));
     w.l = w.m + align256(rows * P * sizeof(float));
-    w.seg = w.l + align256(rows * P * sizeof(float));
-    w.total = w.seg + align256(rows * sizeof(int2));
+    w.cnt = w.l + align256(rows * P * sizeof(float));
+    w.total = w.cnt + align256(rows * sizeof(unsigned long long));   // streams <= rows
     return w;
 }
 
@@ -625,7 +675,7 @@ pd_status launch_decode_t(const DecodeArgs& a) {
     float* ws_o = reinterpret_cast<float*>(base + w.o);
     float* ws_m = reinterpret_cast<float*>(base + w.m);
     float* ws_l = reinterpret_cast<float*>(base + w.l);
-    int2* ws_seg = reinterpret_cast<int2*>(base + w.seg);
+    unsigned long long* ws_cnt = reinterpret_cast<unsigned long long*>(base + w.cnt);
     const float scale_log2 = a.scale * kLog2e;
     // contexts are cut to what the table holds and to the caller's promise
     const int cap = int(std::min<long>(long(a.max_blocks_per_seq) * a.S, a.max_context_len));
@@ -634,30 +684,8 @@ pd_status launch_decode_t(const DecodeArgs& a) {
     kern<<<grid, kDecodeThreads, Lt::kAlloc, a.stream>>>(
         tm_k, tm_v, static_cast<T*>(a.out), static_cast<const T*>(a.q), a.block_tables,
         a.max_blocks_per_seq, a.context_lens, a.B, a.H, a.Hk, a.S, a.NB, GH, scale_log2, P, cap,
-        ws_o, ws_m, ws_l, ws_seg, a.dev_err);
-    pd_status st = launch_result(cudaGetLastError());
-    if (st != PD_OK) return st;
-
-    // Reduce, launched as a programmatic dependent of the split kernel so its
-    // launch overlaps the split kernel's tail.
-    cudaLaunchConfig_t cfg = {};
-    const int64_t nrows = int64_t(a.B) * a.H;
-    cfg.gridDim = dim3(unsigned((nrows + kReduceWarps - 1) / kReduceWarps));
-    cfg.blockDim = dim3(kReduceWarps * 32);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = a.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, paged_decode_reduce_kernel<T, D>,
-                                       static_cast<T*>(a.out), a.context_lens, a.B, a.H, P, cap,
-                                       static_cast<const float*>(ws_o),
-                                       static_cast<const float*>(ws_m),
-                                       static_cast<const float*>(ws_l),
-                                       static_cast<const int2*>(ws_seg), a.dev_err);
-    return launch_result(e);
+        ws_o, ws_m, ws_l, ws_cnt, next_launch_tag(), a.dev_err);
+    return launch_result(cudaGetLastError());
 }
 
 }  // namespace

@@ -17,8 +17,11 @@
 //    K/V tile is loaded once for all of them and the causal band is narrow;
 //  * warp 0 issues TMA loads: the two Q tiles once (3-D map over
 //    [tokens][heads][D]), then per key tile one 2-D box [S rows][64 dims] per
-//    K and per V block, gathered through the block table into a 2-stage ring
-//    with 128-byte swizzle;
+//    K and per V block, gathered through the block table with 128-byte
+//    swizzle.  K and V have rings of their own (3 and 2 stages) and K runs
+//    one tile ahead of V, matching the order the tensor cores use them in
+//    (K of tile t+1 is needed before V of tile t is done), so each load has
+//    more than a key tile's worth of time to land;
 //  * warp 1 allocates all 512 tensor-memory columns (S_A, O_A, S_B, O_B) and
 //    issues every MMA from one thread, alternating the two tiles: PV_A(t),
 //    QK_A(t+1), PV_B(t), QK_B(t+1).  While one softmax warpgroup works on
@@ -41,6 +44,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <cmath>
 
 #include "pd_device.cuh"
@@ -53,7 +57,8 @@ namespace {
 
 constexpr int kTileM = 128;            // query rows per tile (MMA M)
 constexpr int kTileN = 128;            // keys per tile
-constexpr int kKVStages = 2;
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;             // the MMA issuer indexes V stages as t & 1
 constexpr int kPrefillThreads = 384;   // warp 0 TMA, 1 MMA, 2-3 spare, 4-7 / 8-11 softmax A / B
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kTmemCols = 512;    // S_A [0,128) O_A [128,256) S_B [256,384) O_B [384,512)
@@ -65,20 +70,39 @@ constexpr float kLog2e = 1.4426950408889634f;
 // whole 128-column S row in registers.  128*64 + 256*216 = 63488 <= 64512.
 constexpr uint32_t kRegsControl = 64;
 constexpr uint32_t kRegsSoftmax = 216;
+// setmaxnreg.inc waits until enough registers are free: the split must fit
+// in what the CTA was launched with (168 per thread at 384 threads).
+static_assert(kRegsControl * 128 + kRegsSoftmax * 256 <= 168 * kPrefillThreads,
+              "register split exceeds the launch allocation");
+
+// OR of a predicate over one softmax warpgroup (128 threads, named
+// barrier 1 + x).  Every thread of the warpgroup must reach it.
+template <int kBar>
+__device__ __forceinline__ bool wg_any_on(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r) : "r"(uint32_t(pred)), "n"(kBar) : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ bool wg_any(bool pred, int x) {
+    return x == 0 ? wg_any_on<1>(pred) : wg_any_on<2>(pred);
+}
 
 template <int D>
 struct PrefillSmem {
     static constexpr int kAtom = kTileM * 128;          // 128 rows x 128 B (64 16-bit values)
     static constexpr int kTile = (D / 64) * kAtom;      // a [128][D] tile
     static constexpr int kQ = 0;                         // Q_A, Q_B
-    static constexpr int kK = kQ + 2 * kTile;            // kKVStages tiles
-    static constexpr int kV = kK + kKVStages * kTile;
-    static constexpr int kBar = kV + kKVStages * kTile;
-    // barriers: q_full, kv_full[2], kv_empty[2], s_full[A,B], p_full[A,B],
-    // pv_done[A0,A1,B0,B1], drain
-    static constexpr int kNumBars = 14;
+    static constexpr int kK = kQ + 2 * kTile;            // kKStages tiles
+    static constexpr int kV = kK + kKStages * kTile;     // kVStages tiles
+    static constexpr int kBar = kV + kVStages * kTile;
+    // barriers: q_full, k_full[3], k_empty[3], v_full[2], v_empty[2],
+    // s_full[A,B], p_full[A,B], pv_done[A0,A1,B0,B1], drain
+    static constexpr int kNumBars = 20;
     static constexpr int kFlags = kBar + kNumBars * 8;  // int lo_flag[2 tiles][2 parity][4 warps]
-    static constexpr int kMisc = kFlags + 16 * 4;       // tmem base, abort flag, issued count
+    static constexpr int kMisc = kFlags + 16 * 4;       // tmem base, abort flag, K / V issued
     static constexpr int kBytes = kMisc + 16;
     static constexpr int kAlloc = kBytes + 1024 > 116 * 1024 ? kBytes + 1024 : 116 * 1024;
 };
@@ -104,19 +128,22 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
     uint64_t* q_full = bars + 0;
-    uint64_t* kv_full = bars + 1;     // [stage]
-    uint64_t* kv_empty = bars + 3;    // [stage]
-    uint64_t* s_full = bars + 5;      // [tile]
-    uint64_t* p_full = bars + 7;      // [tile]
+    uint64_t* k_full = bars + 1;      // [K stage]
+    uint64_t* k_empty = bars + 4;     // [K stage]
+    uint64_t* v_full = bars + 7;      // [V stage]
+    uint64_t* v_empty = bars + 9;     // [V stage]
+    uint64_t* s_full = bars + 11;     // [tile]
+    uint64_t* p_full = bars + 13;     // [tile]
     // pv_done[tile * 2 + (u & 1)] completes when PV of key tile u (and every
     // earlier MMA) is done.  One barrier per parity keeps each wait within one
     // phase of the barrier's state, which parity waits need.
-    uint64_t* pv_done = bars + 9;     // [4]
-    uint64_t* drain = bars + 13;
+    uint64_t* pv_done = bars + 15;    // [4]
+    uint64_t* drain = bars + 19;
     volatile int32_t* lo_flag = reinterpret_cast<volatile int32_t*>(smem + L::kFlags);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + L::kMisc);
     volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kMisc + 4);
-    volatile int32_t* issued = reinterpret_cast<volatile int32_t*>(smem + L::kMisc + 8);
+    volatile int32_t* k_issued = reinterpret_cast<volatile int32_t*>(smem + L::kMisc + 8);
+    volatile int32_t* v_issued = reinterpret_cast<volatile int32_t*>(smem + L::kMisc + 12);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int seq = blockIdx.z;
@@ -149,16 +176,23 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
+        }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
             mbar_init(&s_full[s], 1);
             mbar_init(&p_full[s], kSoftmaxThreads);
         }
         for (int s = 0; s < 4; ++s) mbar_init(&pv_done[s], 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
-        *issued = 0;
+        *k_issued = 0;
+        *v_issued = 0;
         fence_mbar_init();
         tc::prefetch_tmap(&tm_q);
         tc::prefetch_tmap(&tm_k);
@@ -190,16 +224,21 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
         }
         const int blocks_per_tile = kTileN / S;            // 2 .. 16
-        for (int t = 0; t < n_tiles; ++t) {
-            const int st = t & 1;
+        // Load key tile t of K (is_v false) or V into its ring stage once the
+        // stage is free; false if the CTA must stop.
+        auto load = [&](bool is_v, int t) -> bool {
+            const int stages = is_v ? kVStages : kKStages;
+            const int st = t % stages;
+            uint64_t* empty = is_v ? &v_empty[st] : &k_empty[st];
+            uint64_t* full = is_v ? &v_full[st] : &k_full[st];
             const bool ok = __all_sync(0xffffffffu,
-                                       t < kKVStages || mbar_wait(&kv_empty[st], ((t >> 1) - 1) & 1));
+                                       t < stages || mbar_wait(empty, ((t / stages) - 1) & 1));
             if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) {
                 if (lane == 0 && !ok) {
                     flag_error(dev_err, PD_DEVERR_TIMEOUT);
                     *abort_flag = 1;
                 }
-                break;
+                return false;
             }
             int64_t row = -1;
             if (lane < blocks_per_tile) {
@@ -208,89 +247,112 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const int blk = __ldg(bt_row + lb);
                     if (blk >= 0 && blk < NB) {
                         row = ((int64_t)blk * Hk + kvh) * S;
-                    } else {
+                    } else if (!is_v) {
                         flag_error(dev_err, PD_DEVERR_BLOCK_RANGE);
                     }
                 }
             }
             const uint32_t ok_mask = __ballot_sync(0xffffffffu, row >= 0);
-            if (lane == 0)
-                mbar_arrive_expect_tx(&kv_full[st], uint32_t(__popc(ok_mask)) * S * D * 2 * 2);
+            if (lane == 0) mbar_arrive_expect_tx(full, uint32_t(__popc(ok_mask)) * S * D * 2);
             __syncwarp();
             if (row >= 0) {
-                for (int a = 0; a < kAtoms; ++a) {
-                    const int off = st * L::kTile + a * L::kAtom + lane * S * 128;
-                    tc::tma_load_2d(smem + L::kK + off, &tm_k, a * 64, int32_t(row), &kv_full[st]);
-                    tc::tma_load_2d(smem + L::kV + off, &tm_v, a * 64, int32_t(row), &kv_full[st]);
-                }
+                unsigned char* dst = smem + (is_v ? L::kV : L::kK) + st * L::kTile + lane * S * 128;
+                for (int a = 0; a < kAtoms; ++a)
+                    tc::tma_load_2d(dst + a * L::kAtom, is_v ? &tm_v : &tm_k, a * 64,
+                                    int32_t(row), full);
             }
-            if (lane == 0) *issued = t + 1;
+            if (lane == 0) *(is_v ? v_issued : k_issued) = t + 1;
+            return true;
+        };
+        // K runs one key tile ahead of V: K0, K1, V0, K2, V1, ...
+        if (n_tiles > 0 && load(false, 0)) {
+            for (int t = 0; t < n_tiles; ++t) {
+                if (t + 1 < n_tiles && !load(false, t + 1)) break;
+                if (!load(true, t)) break;
+            }
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer --------------------------------
-        if (lane == 0) {
-            auto qk = [&](int x, int t) {
-                const uint32_t d_s = tmem + uint32_t(x) * 256;
-                const int st = t & 1;
+        // The whole warp runs this loop in step (every decision warp-uniform);
+        // one elected lane issues each MMA and commit.
+        constexpr uint32_t kHi = tc::sw128_desc_hi(1024);
+        constexpr uint32_t kTile16 = uint32_t(L::kTile) >> 4;
+        // Descriptor low halves, built once: every operand below is one of
+        // these bases plus a constant (byte offset >> 4).
+        const uint32_t q_lo = tc::smem_desc_sw128_lo(sQ, 16);
+        const uint32_t k_lo = tc::smem_desc_sw128_lo(sK, 16);
+        // V as an MN-major operand: N = D contiguous in 64-wide atoms (LBO
+        // between them), K = keys at 128 B (SBO per 8 keys)
+        const uint32_t v_lo = tc::smem_desc_sw128_lo(sV, L::kAtom);
+        auto qk = [&](int x, uint32_t kst) {
+            const uint32_t d_s = tmem + uint32_t(x) * 256;
+            const uint32_t a0 = q_lo + uint32_t(x) * kTile16;
+            const uint32_t b0 = k_lo + kst * kTile16;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * L::kAtom + (kk & 3) * 32;
-                    const uint64_t a = tc::smem_desc_sw128(sQ + x * L::kTile + koff, 16, 1024);
-                    const uint64_t b = tc::smem_desc_sw128(sK + st * L::kTile + koff, 16, 1024);
-                    tc::mma_ss(d_s, a, b, kIdescQK, kk > 0);
-                }
-                tc::commit(&s_full[x]);
-            };
-            auto pv = [&](int x, int t) {
-                const int st = t & 1;
-                const bool lo = (lo_flag[x * 8 + st * 4 + 0] | lo_flag[x * 8 + st * 4 + 1] |
-                                 lo_flag[x * 8 + st * 4 + 2] | lo_flag[x * 8 + st * 4 + 3]) != 0;
-                const uint32_t d_o = tmem + uint32_t(x) * 256 + 128;
-                // P over S: chunk c (keys 32c..32c+31) holds hi in columns
-                // 32c..32c+15 and lo in 32c+16..32c+31
-                for (int pass = 0; pass < (lo ? 2 : 1); ++pass) {
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t koff = uint32_t((kk >> 2) * L::kAtom + (kk & 3) * 32) >> 4;
+                if (kk == 0)
+                    tc::mma_ss_warp<false>(d_s, a0 + koff, kHi, b0 + koff, kHi, kIdescQK);
+                else
+                    tc::mma_ss_warp<true>(d_s, a0 + koff, kHi, b0 + koff, kHi, kIdescQK);
+            }
+            tc::commit_warp(&s_full[x]);
+        };
+        auto pv = [&](int x, int t, uint32_t vst) {
+            // the lo pass is decided per tile, so one flag holds the answer
+            const bool lo = lo_flag[x * 8 + (t & 1) * 4] != 0;
+            const uint32_t d_o = tmem + uint32_t(x) * 256 + 128;
+            const uint32_t p0 = tmem + uint32_t(x) * 256;
+            const uint32_t b0 = v_lo + vst * kTile16;
+            // P over S: chunk c (keys 32c..32c+31) holds hi in columns
+            // 32c..32c+15 and lo in 32c+16..32c+31
+            for (int pass = 0; pass < (lo ? 2 : 1); ++pass) {
 #pragma unroll
-                    for (int kk = 0; kk < kTileN / 16; ++kk) {
-                        // V tile as an MN-major operand: N = D contiguous in 64-wide
-                        // atoms (LBO between them), K = keys at 128 B (SBO per 8 keys)
-                        const uint64_t b = tc::smem_desc_sw128(
-                            sV + st * L::kTile + kk * 16 * 128, L::kAtom, 1024);
-                        tc::mma_ts(d_o,
-                                   tmem + uint32_t(x) * 256 + 32 * (kk >> 1) + 16 * pass +
-                                       8 * (kk & 1),
-                                   b, kIdescPV, (t > 0 || kk > 0 || pass > 0));
-                    }
-                }
-                tc::commit(&pv_done[x * 2 + (t & 1)]);
-            };
-            bool ok = mbar_wait(q_full, 0);
-            if (ok && (ok = mbar_wait(&kv_full[0], 0))) {
-                tc::fence_after_sync();
-                if (n_a > 0) qk(0, 0);
-                if (n_b > 0) qk(1, 0);
+                for (int kk = 0; kk < kTileN / 16; ++kk)
+                    tc::mma_ts_warp(d_o, p0 + uint32_t(32 * (kk >> 1) + 8 * (kk & 1) + 16 * pass),
+                                    b0 + uint32_t(kk * 16 * 128 / 16), kHi, kIdescPV,
+                                    uint32_t(t > 0 || kk > 0 || pass > 0));
             }
-            for (int t = 0; ok && t < n_tiles; ++t) {
-                if (*abort_flag) { ok = false; break; }
-                for (int x = 0; x < 2 && ok; ++x) {
-                    const int nx = x == 0 ? n_a : n_b;
-                    if (t >= nx) continue;
-                    if (!(ok = mbar_wait(&p_full[x], t & 1))) break;
-                    tc::fence_after_sync();
-                    pv(x, t);
-                    if (t + 1 < nx) {
-                        if (!(ok = mbar_wait(&kv_full[(t + 1) & 1], ((t + 1) >> 1) & 1))) break;
-                        tc::fence_after_sync();
-                        qk(x, t + 1);
-                    }
-                }
-                if (ok) tc::commit(&kv_empty[t & 1]);
-            }
-            if (!ok) {
-                flag_error(dev_err, PD_DEVERR_TIMEOUT);
-                *abort_flag = 1;
-            }
+            tc::commit_warp(&pv_done[x * 2 + (t & 1)]);
+        };
+        bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0));
+        if (ok && n_tiles > 0 && (ok = __all_sync(0xffffffffu, mbar_wait(&k_full[0], 0)))) {
+            tc::fence_after_sync();
+            if (n_a > 0) qk(0, 0);
+            if (n_b > 0) qk(1, 0);
+            tc::commit_warp(&k_empty[0]);
         }
-        __syncwarp();
+        // Ring positions tracked incrementally: K of tile u = t + 1 in stage
+        // kst with phase parity kpar; V of tile t in stage t & 1, parity
+        // (t >> 1) & 1.  Waiting twice on a phase that completed is harmless:
+        // a stage is only refilled after this warp releases it.
+        uint32_t kst = 1 % kKStages, kpar = kKStages == 1 ? 1u : 0u;
+        for (int t = 0; ok && t < n_tiles; ++t) {
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
+            const uint32_t vst = uint32_t(t) & 1u, vpar = (uint32_t(t) >> 1) & 1u;
+            for (int x = 0; x < 2 && ok; ++x) {
+                const int nx = x == 0 ? n_a : n_b;
+                if (t >= nx) continue;
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(&p_full[x], uint32_t(t) & 1u)))) break;
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(&v_full[vst], vpar)))) break;
+                tc::fence_after_sync();
+                pv(x, t, vst);
+                if (t + 1 < nx) {
+                    if (!(ok = __all_sync(0xffffffffu, mbar_wait(&k_full[kst], kpar)))) break;
+                    tc::fence_after_sync();
+                    qk(x, kst);
+                }
+            }
+            if (ok) {
+                tc::commit_warp(&v_empty[vst]);
+                if (t + 1 < n_tiles) tc::commit_warp(&k_empty[kst]);
+            }
+            if (++kst == kKStages) { kst = 0; kpar ^= 1u; }
+        }
+        if (!ok && lane == 0) {
+            flag_error(dev_err, PD_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+        }
     }                                                  // warps 2, 3: spare
     } else {
         // --------------------------- softmax + epilogue ---------------------------
@@ -311,100 +373,122 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int t = 0; t < nx; ++t) {
-            const int st = t & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], t & 1));
-            if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) break;
-            tc::fence_after_sync();
+            const int par = t & 1;
+            // A warp that hits a failed wait carries ok = false to the vote
+            // below, the one place where the warpgroup leaves the loop (all
+            // four warps together, so the named barrier always completes).
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], par));
             const int kbase = t * kTileN;
-            const bool masked = kbase + kTileN - 1 > lim;     // tile crosses this row's limit
-            // ---- the whole S row into registers (one burst of loads)
             uint32_t sr[kTileN];
+            float m_tile = -INFINITY;
+            bool need_lo = false;
+            if (ok) {
+                tc::fence_after_sync();
+                // ---- the whole S row into registers (one burst of loads)
 #pragma unroll
-            for (int c = 0; c < kTileN / 32; ++c)
-                tc::tmem_ld32(s_cols + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-            tc::tmem_ld_wait();
-            if (masked) {                              // only tiles that cross the limit
+                for (int c = 0; c < kTileN / 32; ++c)
+                    tc::tmem_ld32(s_cols + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+                tc::tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < kTileN; ++e)
-                    if (kbase + e > lim) sr[e] = __float_as_uint(-INFINITY);
-            }
-            float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                for (int c = 0; c < kTileN / 32; ++c)
+                    tc::tmem_ld_fence(*reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+                if (kbase + kTileN - 1 > lim) {        // only tiles that cross the limit
 #pragma unroll
-            for (int e = 0; e < kTileN; e += 8) {
-                mxs[0] = fmax3(mxs[0], __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
-                mxs[1] = fmax3(mxs[1], __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
-                mxs[2] = fmax3(mxs[2], __uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5]));
-                mxs[3] = fmax3(mxs[3], __uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7]));
-            }
-            const float m_tile = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])) * scale_log2;
-            // The tensor-memory loads and stores below are warp-collective, so
-            // the warp rescales together when any of its rows needs it; each
-            // row uses its own exact factor (1 when its max did not grow).
-            if (__any_sync(0xffffffffu, m_tile > m_run + kRescaleThreshold)) {
-                const float m_new = fmaxf(m_run, m_tile);
-                const float alpha = ex2(m_run - m_new);    // 0 on the first tile
-                if (t > 0) {
-                    // O holds PV of tiles < t (already complete: QK of tile t
-                    // was issued after PV of tile t-1); wait anyway, cheaply.
-                    ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[x * 2 + ((t - 1) & 1)],
-                                                           ((t - 1) >> 1) & 1));
-                    if (!ok) break;
-                    tc::fence_after_sync();
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        tc::tmem_ld32(o_cols + c * 32, o);
-                        tc::tmem_ld_wait();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tc::tmem_st32(o_cols + c * 32, o);
-                    }
-                    tc::tmem_st_wait();
+                    for (int e = 0; e < kTileN; ++e)
+                        if (kbase + e > lim) sr[e] = __float_as_uint(-INFINITY);
                 }
-                l_run *= alpha;
-                m_run = m_new;
-            }
-            // Does some key of this tile carry a weight that may exceed
-            // kLoWeight?  max weight <= p_max / (l_before + p_max).
-            const float p_max = m_tile == -INFINITY ? 0.f : ex2(m_tile - m_run);
-            const bool need_lo = __any_sync(0xffffffffu, p_max > kLoWeight * (l_run + p_max));
-            // ---- p = 2^(s * scale_log2 - m), written over S as hi (+ lo) per
-            // 32-column chunk (keys 32c..32c+31 -> columns 32c.. hi, 32c+16.. lo)
-            const float nm = -m_run;
-            float lsum[4] = {0.f, 0.f, 0.f, 0.f};
+                float mxs[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < kTileN / 32; ++c) {
-                uint32_t hi[16], lo[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float p0 = ex2(fmaf(__uint_as_float(sr[c * 32 + 2 * e]), scale_log2, nm));
-                    const float p1 =
-                        ex2(fmaf(__uint_as_float(sr[c * 32 + 2 * e + 1]), scale_log2, nm));
-                    lsum[e & 3] += p0 + p1;
-                    hi[e] = E::pack2(p0, p1);
-                    if (need_lo) {
-                        const float2 h = E::unpack2(hi[e]);
-                        lo[e] = E::pack2(p0 - h.x, p1 - h.y);   // exact differences
-                    } else {
-                        lo[e] = 0u;
-                    }
+                for (int e = 0; e < kTileN; e += 8) {
+                    mxs[0] = fmax3(mxs[0], __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+                    mxs[1] = fmax3(mxs[1], __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
+                    mxs[2] = fmax3(mxs[2], __uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5]));
+                    mxs[3] = fmax3(mxs[3], __uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7]));
                 }
-                tc::tmem_st16(s_cols + c * 32, hi);
-                tc::tmem_st16(s_cols + c * 32 + 16, lo);
+                m_tile = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])) * scale_log2;
+                // The tensor-memory loads and stores below are warp-collective,
+                // so the warp rescales together when any of its rows needs it;
+                // each row uses its own exact factor (1 when its max did not grow).
+                if (__any_sync(0xffffffffu, m_tile > m_run + kRescaleThreshold)) {
+                    const float m_new = fmaxf(m_run, m_tile);
+                    const float alpha = ex2(m_run - m_new);    // 0 on the first tile
+                    if (t > 0) {
+                        // O holds PV of tiles < t (already complete: QK of tile t
+                        // was issued after PV of tile t-1); wait anyway, cheaply.
+                        ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[x * 2 + ((t - 1) & 1)],
+                                                               ((t - 1) >> 1) & 1));
+                        if (ok) {
+                            tc::fence_after_sync();
+#pragma unroll
+                            for (int c = 0; c < D / 16; ++c) {
+                                uint32_t o[16];
+                                tc::tmem_ld16(o_cols + c * 16, o);
+                                tc::tmem_ld_wait();
+                                tc::tmem_ld_fence(o);
+#pragma unroll
+                                for (int e = 0; e < 16; ++e)
+                                    o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                                tc::tmem_st16(o_cols + c * 16, o);
+                            }
+                            tc::tmem_st_wait();
+                        }
+                    }
+                    l_run *= alpha;
+                    m_run = m_new;
+                }
+                // Can some key of this tile carry a weight above kLoWeight?
+                // max weight <= p_max / (l_before + p_max).
+                const float p_max = m_tile == -INFINITY ? 0.f : ex2(m_tile - m_run);
+                need_lo = p_max > kLoWeight * (l_run + p_max);
             }
-            l_run += (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
+            if (wg_any(!ok || *abort_flag != 0, x)) {
+                ok = false;
+                break;
+            }
+            // The lo pass is decided for the whole tile, so every row writes
+            // its residuals when any row needs them.
+            const bool lo_any = wg_any(need_lo, x);
+            // ---- p = 2^(s * scale_log2 - m) over S: keys 32c..32c+31 -> hi in
+            // columns 32c..32c+15, lo (when taken) in 32c+16..32c+31
+            const float2 sc2 = make_float2(scale_log2, scale_log2);
+            const float2 nm2 = make_float2(-m_run, -m_run);
+            float2 lsum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            auto exp_pass = [&](auto with_lo) {
+                constexpr bool kLo = decltype(with_lo)::value;
+#pragma unroll
+                for (int c = 0; c < kTileN / 32; ++c) {
+                    uint32_t hi[16], lo[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 xv = ffma2(make_float2(__uint_as_float(sr[c * 32 + 2 * e]),
+                                                            __uint_as_float(sr[c * 32 + 2 * e + 1])),
+                                                sc2, nm2);
+                        const float2 pv = make_float2(ex2(xv.x), ex2(xv.y));
+                        lsum[e & 1] = fadd2(lsum[e & 1], pv);
+                        hi[e] = E::pack2(pv.x, pv.y);
+                        if (kLo) {
+                            const float2 d = fsub2(pv, E::unpack2(hi[e]));   // exact
+                            lo[e] = E::pack2(d.x, d.y);
+                        }
+                    }
+                    tc::tmem_st16(s_cols + c * 32, hi);
+                    if (kLo) tc::tmem_st16(s_cols + c * 32 + 16, lo);
+                }
+            };
+            if (lo_any) exp_pass(std::true_type{});
+            else exp_pass(std::false_type{});
+            l_run += (lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y);
             tc::tmem_st_wait();
-            if (lane == 0) lo_flag[x * 8 + st * 4 + quarter] = need_lo ? 1 : 0;
+            if (lane == 0) lo_flag[x * 8 + par * 4 + quarter] = lo_any ? 1 : 0;
             // Keys past the context in the last tile: their V rows hold other
             // data (or were never loaded); zero them so 0 * v stays 0.  The
             // first tile to use this stage does it.
             const bool zero_v = kbase + kTileN > ctx && (x == 0 || t >= n_a);
             if (zero_v) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&kv_full[st], (t >> 1) & 1));
-                if (!ok) break;
-                if (kbase + r >= ctx) {
-                    unsigned char* vrow = smem + L::kV + st * L::kTile + r * 128;
+                const int vst = t % kVStages;
+                ok = __all_sync(0xffffffffu, mbar_wait(&v_full[vst], (t / kVStages) & 1));
+                if (ok && kbase + r >= ctx) {
+                    unsigned char* vrow = smem + L::kV + vst * L::kTile + r * 128;
 #pragma unroll
                     for (int a = 0; a < kAtoms; ++a)
 #pragma unroll
@@ -429,6 +513,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                     uint32_t o[32];
                     tc::tmem_ld32(o_cols + c * 32, o);
                     tc::tmem_ld_wait();
+                    tc::tmem_ld_fence(o);
                     uint32_t pk2[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
@@ -458,9 +543,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
             mbar_wait(drain, 0);
         }
         if (warp == 0 && lane == 0) {
-            const int n = *issued;
-            for (int t = max(0, n - kKVStages); t < n; ++t)
-                if (!mbar_wait(&kv_full[t & 1], (t >> 1) & 1)) break;
+            const int nk = *k_issued, nv = *v_issued;
+            for (int t = max(0, nk - kKStages); t < nk; ++t)
+                if (!mbar_wait(&k_full[t % kKStages], (t / kKStages) & 1)) break;
+            for (int t = max(0, nv - kVStages); t < nv; ++t)
+                if (!mbar_wait(&v_full[t % kVStages], (t / kVStages) & 1)) break;
             mbar_wait(q_full, 0);
         }
         __syncthreads();

@@ -28,6 +28,10 @@ reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict_
     if (row >= int64_t(T) * Hk) return;
     const int64_t n = row / Hk;
     const int h = int(row % Hk);
+    // the token's vectors and its slot are independent loads: issue all three
+    // before acting on the slot, so they overlap
+    const uint4 kv = __ldg(key + n * key_stride_vec + int64_t(h) * vec_per_row + c);
+    const uint4 vv = __ldg(value + n * value_stride_vec + int64_t(h) * vec_per_row + c);
     const int64_t slot = __ldg(slot_mapping + n);
     if (slot < 0) return;                       // padding token
     if (slot >= int64_t(NB) * S) {
@@ -36,8 +40,6 @@ reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict_
     }
     const int64_t blk = slot / S, off = slot % S;
     const int64_t dst = ((blk * Hk + h) * S + off) * vec_per_row + c;
-    const uint4 kv = __ldg(key + n * key_stride_vec + int64_t(h) * vec_per_row + c);
-    const uint4 vv = __ldg(value + n * value_stride_vec + int64_t(h) * vec_per_row + c);
     key_cache[dst] = kv;
     value_cache[dst] = vv;
 }

@@ -1,4 +1,4 @@
-"""GPU parity of paged decode attention (split-context + reduce) against the
+"""GPU parity of paged decode attention (split context, pieces merged in-kernel) against the
 float64 oracle, over the five workloads and the edge cases: ragged and empty
 contexts, partition boundaries, every GQA grouping, head dims, block sizes
 and element types, block-permutation invariance (bit-identical), a
@@ -183,3 +183,38 @@ def test_workspace_too_small_is_an_error(cuda_lib):
     with pytest.raises(cuda_lib.PDError) as e:
         gpu_store_and_decode(cuda_lib, c, workspace=small)
     assert e.value.status == 5
+
+
+def test_workspace_contents_do_not_matter(cuda_lib):
+    """The arrival counters in the workspace carry a per-launch tag: results
+    are the same bits whatever the workspace held before (fresh, random
+    bytes, all ones, or the counters of an earlier launch on the same batch)."""
+    pd = cuda_lib
+    c = pd_inputs.qwen3_8b_decode(seed=3, B=16)
+    dev = torch.device("cuda")
+    kc, vc = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
+    pd.pd_reshape_and_cache(c.new_key.to(dev), c.new_value.to(dev), kc, vc,
+                            c.slot_mapping.to(dev))
+    q = c.q.to(dev)
+    bt, cl = c.pool.block_tables.to(dev), c.pool.context_lens.to(dev)
+    mcl = c.max_context_len
+    nbytes = pd.pd_decode_workspace_bytes(c.B, c.H, c.D, mcl)
+    g = torch.Generator(device="cpu").manual_seed(5)
+    fills = [None,
+             torch.randint(0, 256, (nbytes,), dtype=torch.uint8, generator=g),
+             torch.full((nbytes,), 255, dtype=torch.uint8)]
+    outs = []
+    for fill in fills:
+        ws = pd.decode_workspace(c.B, c.H, c.D, mcl)
+        if fill is not None:
+            ws.view(torch.uint8)[:nbytes].copy_(fill.to(dev))
+        for _ in range(2):               # the second call meets the first's counters
+            out = torch.full_like(q, float("nan"))
+            err = device_err()
+            pd.pd_paged_attention_decode(out, q, kc, vc, bt, cl, mcl, c.scale, ws, dev_err=err)
+            torch.cuda.synchronize()
+            assert err.item() == 0
+            outs.append(u16(out.cpu()))
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+    assert torch.isfinite(out.float()).all()
