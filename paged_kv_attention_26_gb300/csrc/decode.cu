@@ -200,46 +200,84 @@ __device__ __forceinline__ bool arrive_piece(unsigned long long* cnt, unsigned l
     }
 }
 
-// Merge the np pieces of one (sequence, q head) row, one warp, fixed order:
+// Merge the np pieces of a stream's GH rows (one warp, fixed piece order):
 // M = max_k m_k; out = sum_k o_k 2^(m_k - M) / sum_k l_k 2^(m_k - M).
+// Four lanes per row (row = lane / 4, a quarter of D each), so every row is
+// merged at once and the loads of all pieces are in flight together.
 // Pieces of other CTAs are read through L2 (ld.global.cg).
 template <typename T, int D>
-__device__ __forceinline__ void merge_pieces(T* __restrict__ out_row, const float* o_rows,
-                                             const float* m, const float* l, int np, int lane) {
+__device__ __forceinline__ void merge_stream(T* __restrict__ out, const float* ws_o,
+                                             const float* ws_m, const float* ws_l, int64_t row0,
+                                             int GH, int max_segs, int np, int lane) {
     using E = Elem<T>;
-    constexpr int DV = D / 32;
+    constexpr int kDpl = D / 4;          // values per lane
+    constexpr int kCache = 8;            // pieces whose (m, l) stay in registers
+    const int h = lane >> 2;
+    if (h >= GH) return;
+    const int64_t row = row0 + h;
+    const float* m = ws_m + row * max_segs;
+    const float* l = ws_l + row * max_segs;
+    const float* o = ws_o + row * max_segs * D + (lane & 3) * kDpl;
+    float mc[kCache], lc[kCache];
     float M = -INFINITY;
-    for (int p = lane; p < np; p += 32) M = fmaxf(M, __ldcg(m + p));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float acc[DV];
+    for (int p = 0; p < kCache; ++p) {
+        mc[p] = p < np ? __ldcg(m + p) : -INFINITY;
+        lc[p] = p < np ? __ldcg(l + p) : 0.f;
+        M = fmaxf(M, mc[p]);
+    }
+    for (int p = kCache; p < np; ++p) M = fmaxf(M, __ldcg(m + p));
+    float acc[kDpl];
 #pragma unroll
-    for (int e = 0; e < DV; ++e) acc[e] = 0.f;
+    for (int e = 0; e < kDpl; ++e) acc[e] = 0.f;
     float lsum = 0.f;
-    for (int p0 = 0; p0 < np; p0 += 32) {
-        const int p = p0 + lane;
-        const float mp = p < np ? __ldcg(m + p) : -INFINITY;
+    for (int p = 0; p < np; ++p) {
+        float mp, lp;
+        if (p < kCache) {
+#pragma unroll
+            for (int k = 0; k < kCache; ++k)
+                if (k == p) { mp = mc[k]; lp = lc[k]; }
+        } else {
+            mp = __ldcg(m + p);
+            lp = __ldcg(l + p);
+        }
         const float w = mp != -INFINITY ? ex2(mp - M) : 0.f;
-        lsum += p < np ? __ldcg(l + p) * w : 0.f;
-        const int n = min(32, np - p0);
-        for (int u = 0; u < n; ++u) {
-            const float wu = __shfl_sync(0xffffffffu, w, u);
-            const float* o = o_rows + (p0 + u) * D + lane * DV;
-            if constexpr (DV == 4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(o));
-                acc[0] += v.x * wu; acc[1] += v.y * wu; acc[2] += v.z * wu; acc[3] += v.w * wu;
-            } else {
-                const float2 v = __ldcg(reinterpret_cast<const float2*>(o));
-                acc[0] += v.x * wu; acc[1] += v.y * wu;
-            }
+        lsum += lp * w;
+        const float4* src = reinterpret_cast<const float4*>(o + int64_t(p) * D);
+#pragma unroll
+        for (int c = 0; c < kDpl / 4; ++c) {
+            const float4 v = __ldcg(src + c);
+            acc[4 * c + 0] += v.x * w;
+            acc[4 * c + 1] += v.y * w;
+            acc[4 * c + 2] += v.z * w;
+            acc[4 * c + 3] += v.w * w;
         }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
     const float inv = 1.f / lsum;
-    uint32_t* dst = reinterpret_cast<uint32_t*>(out_row + lane * DV);
+    uint4* dst = reinterpret_cast<uint4*>(out + row * D + (lane & 3) * kDpl);
 #pragma unroll
-    for (int e = 0; e < DV / 2; ++e) dst[e] = E::pack2(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+    for (int c = 0; c < kDpl / 8; ++c)
+        dst[c] = make_uint4(E::pack2(acc[8 * c + 0] * inv, acc[8 * c + 1] * inv),
+                            E::pack2(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv),
+                            E::pack2(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv),
+                            E::pack2(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv));
+}
+
+// Rows of empty contexts get zeros (no stream covers them); contexts outside
+// [0, cap] are flagged (the walk cuts them to cap).  CTA b takes sequences
+// b, b + grid, ...; called by one warp.
+template <typename T, int D>
+__device__ __forceinline__ void zero_empty_rows(T* __restrict__ out,
+                                                const int32_t* __restrict__ context_lens, int B,
+                                                int H, int cap, int32_t* dev_err, int lane) {
+    for (int s = blockIdx.x; s < B; s += gridDim.x) {
+        const int raw = __ldg(context_lens + s);
+        if ((raw < 0 || raw > cap) && lane == 0) flag_error(dev_err, PD_DEVERR_CTX_RANGE);
+        if (raw <= 0) {
+            uint4* dst = reinterpret_cast<uint4*>(out + (int64_t)s * H * D);
+            for (int i = lane; i < H * D * 2 / 16; i += 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
 }
 
 template <typename T, int D>
@@ -284,20 +322,11 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     }
     __syncthreads();
 
-    // Rows of empty contexts get zeros (no stream covers them); contexts
-    // outside [0, cap] are flagged (and cut to cap by the walk).
-    for (int s = blockIdx.x; s < B; s += gridDim.x) {
-        const int raw = __ldg(context_lens + s);
-        if ((raw < 0 || raw > cap) && threadIdx.x == 0) flag_error(dev_err, PD_DEVERR_CTX_RANGE);
-        if (raw <= 0) {
-            uint4* dst = reinterpret_cast<uint4*>(out + (int64_t)s * H * D);
-            for (int i = threadIdx.x; i < H * D * 2 / 16; i += blockDim.x)
-                dst[i] = make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
-
     Walk w;
-    if (!walk_begin(w, context_lens, B, units, cap)) return;   // uniform: no range
+    if (!walk_begin(w, context_lens, B, units, cap)) {          // uniform: no range
+        if (warp == 0) zero_empty_rows<T, D>(out, context_lens, B, H, cap, dev_err, lane);
+        return;
+    }
 
     if (warp == kConsumerWarps) {
         // ---------------- producer warp: streams stages across stream pieces ----------------
@@ -344,6 +373,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             ++w.pos;
             if (w.off == w.L && w.pos < w.end) walk_next_stream(w, context_lens, B, units, cap);
         }
+        // all loads are issued: the producer has time for the empty rows
+        zero_empty_rows<T, D>(out, context_lens, B, H, cap, dev_err, lane);
         return;
     }
 
@@ -571,12 +602,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
                     __threadfence();
-                    for (int hh = 0; hh < GH; ++hh) {
-                        const int64_t row = (int64_t)w.s * H + h0 + hh;
-                        merge_pieces<T, D>(out + row * D, ws_o + row * max_segs * D,
-                                           ws_m + row * max_segs, ws_l + row * max_segs, nseg,
-                                           lane);
-                    }
+                    merge_stream<T, D>(out, ws_o, ws_m, ws_l, (int64_t)w.s * H + h0, GH, max_segs,
+                                       nseg, lane);
                 }
             }
         }

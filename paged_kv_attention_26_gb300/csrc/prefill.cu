@@ -75,21 +75,6 @@ constexpr uint32_t kRegsSoftmax = 216;
 static_assert(kRegsControl * 128 + kRegsSoftmax * 256 <= 168 * kPrefillThreads,
               "register split exceeds the launch allocation");
 
-// OR of a predicate over one softmax warpgroup (128 threads, named
-// barrier 1 + x).  Every thread of the warpgroup must reach it.
-template <int kBar>
-__device__ __forceinline__ bool wg_any_on(bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r) : "r"(uint32_t(pred)), "n"(kBar) : "memory");
-    return r != 0;
-}
-__device__ __forceinline__ bool wg_any(bool pred, int x) {
-    return x == 0 ? wg_any_on<1>(pred) : wg_any_on<2>(pred);
-}
-
 template <int D>
 struct PrefillSmem {
     static constexpr int kAtom = kTileM * 128;          // 128 rows x 128 B (64 16-bit values)
@@ -299,8 +284,9 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
             tc::commit_warp(&s_full[x]);
         };
         auto pv = [&](int x, int t, uint32_t vst) {
-            // the lo pass is decided per tile, so one flag holds the answer
-            const bool lo = lo_flag[x * 8 + (t & 1) * 4] != 0;
+            // second pass when any of the four softmax warps asked for it
+            const int32_t* f = const_cast<const int32_t*>(lo_flag) + x * 8 + (t & 1) * 4;
+            const bool lo = (f[0] | f[1] | f[2] | f[3]) != 0;
             const uint32_t d_o = tmem + uint32_t(x) * 256 + 128;
             const uint32_t p0 = tmem + uint32_t(x) * 256;
             const uint32_t b0 = v_lo + vst * kTile16;
@@ -374,15 +360,12 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
         bool ok = true;
         for (int t = 0; t < nx; ++t) {
             const int par = t & 1;
-            // A warp that hits a failed wait carries ok = false to the vote
-            // below, the one place where the warpgroup leaves the loop (all
-            // four warps together, so the named barrier always completes).
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], par));
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], par));
+            if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) break;
             const int kbase = t * kTileN;
             uint32_t sr[kTileN];
-            float m_tile = -INFINITY;
-            bool need_lo = false;
-            if (ok) {
+            float p_max;
+            {
                 tc::fence_after_sync();
                 // ---- the whole S row into registers (one burst of loads)
 #pragma unroll
@@ -405,7 +388,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                     mxs[2] = fmax3(mxs[2], __uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5]));
                     mxs[3] = fmax3(mxs[3], __uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7]));
                 }
-                m_tile = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])) * scale_log2;
+                const float m_tile = fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])) * scale_log2;
                 // The tensor-memory loads and stores below are warp-collective,
                 // so the warp rescales together when any of its rows needs it;
                 // each row uses its own exact factor (1 when its max did not grow).
@@ -417,7 +400,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                         // was issued after PV of tile t-1); wait anyway, cheaply.
                         ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[x * 2 + ((t - 1) & 1)],
                                                                ((t - 1) >> 1) & 1));
-                        if (ok) {
+                        if (!ok) break;
+                        {
                             tc::fence_after_sync();
 #pragma unroll
                             for (int c = 0; c < D / 16; ++c) {
@@ -438,16 +422,12 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                 }
                 // Can some key of this tile carry a weight above kLoWeight?
                 // max weight <= p_max / (l_before + p_max).
-                const float p_max = m_tile == -INFINITY ? 0.f : ex2(m_tile - m_run);
-                need_lo = p_max > kLoWeight * (l_run + p_max);
+                p_max = m_tile == -INFINITY ? 0.f : ex2(m_tile - m_run);
             }
-            if (wg_any(!ok || *abort_flag != 0, x)) {
-                ok = false;
-                break;
-            }
-            // The lo pass is decided for the whole tile, so every row writes
-            // its residuals when any row needs them.
-            const bool lo_any = wg_any(need_lo, x);
+            // The warp stores residuals when one of its rows needs them, and
+            // zeros otherwise, so the MMA issuer can run the lo pass for the
+            // whole tile when any warp asks for it.
+            const bool need_lo = __any_sync(0xffffffffu, p_max > kLoWeight * (l_run + p_max));
             // ---- p = 2^(s * scale_log2 - m) over S: keys 32c..32c+31 -> hi in
             // columns 32c..32c+15, lo (when taken) in 32c+16..32c+31
             const float2 sc2 = make_float2(scale_log2, scale_log2);
@@ -473,13 +453,14 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                     }
                     tc::tmem_st16(s_cols + c * 32, hi);
                     if (kLo) tc::tmem_st16(s_cols + c * 32 + 16, lo);
+                    else tc::tmem_st16_zero(s_cols + c * 32 + 16);
                 }
             };
-            if (lo_any) exp_pass(std::true_type{});
+            if (need_lo) exp_pass(std::true_type{});
             else exp_pass(std::false_type{});
             l_run += (lsum[0].x + lsum[0].y) + (lsum[1].x + lsum[1].y);
             tc::tmem_st_wait();
-            if (lane == 0) lo_flag[x * 8 + par * 4 + quarter] = lo_any ? 1 : 0;
+            if (lane == 0) lo_flag[x * 8 + par * 4 + quarter] = need_lo ? 1 : 0;
             // Keys past the context in the last tile: their V rows hold other
             // data (or were never loaded); zero them so 0 * v stays 0.  The
             // first tile to use this stage does it.
@@ -487,7 +468,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (zero_v) {
                 const int vst = t % kVStages;
                 ok = __all_sync(0xffffffffu, mbar_wait(&v_full[vst], (t / kVStages) & 1));
-                if (ok && kbase + r >= ctx) {
+                if (!ok) break;
+                if (kbase + r >= ctx) {
                     unsigned char* vrow = smem + L::kV + vst * L::kTile + r * 128;
 #pragma unroll
                     for (int a = 0; a < kAtoms; ++a)
