@@ -50,7 +50,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
-    ap.add_argument("--extras", default="chunked_prefill_mix,long_context_32_layers,cow_fork_stress",
+    ap.add_argument("--extras", default="chunked_prefill_mix,long_context_32_layers,cow_fork_stress,spec_verify,"
+                    "kv_handover",
                     help="comma-separated extra workloads to run after the headline")
     ap.add_argument("--extra-steps", type=int, default=10)
     return ap.parse_args()
@@ -281,6 +282,11 @@ def run_ours(args, rank, world, local_rank):
                                                                    flush, hbm_peak)
         if "cow_fork_stress" in wanted:
             extras["cow_fork_stress"] = bench_cow(pd, pd_inputs, dev, args, flush, hbm_peak)
+        if "spec_verify" in wanted:
+            extras["spec_verify"] = bench_spec_verify(pd, pd_inputs, dev, args, flush, hbm_peak,
+                                                      bf16_peak)
+        if "kv_handover" in wanted:
+            extras["kv_handover"] = bench_kv_handover(pd, pd_inputs, dev, args, flush, hbm_peak)
         result["extras"] = extras
     if sampler is not None:
         result["clocks"] = sampler.stop()
@@ -440,6 +446,62 @@ def bench_long_context(pd, pd_inputs, dev, args, flush, hbm_peak):
                              "partitions": -(-ctx // pd.pd_decode_partition_tokens(ctx))}
         del layers, outs
         torch.cuda.empty_cache()
+    return res
+
+
+def bench_spec_verify(pd, pd_inputs, dev, args, flush, hbm_peak, bf16_peak):
+    """Speculative verification of 4 tokens per sequence (64 sequences, prior
+    context U[128, 2048], Qwen3-8B shape) through the chunked-prefill kernel:
+    K/V bytes read per second (the bound) and causal TFLOP/s."""
+    import torch
+    m = pd_inputs.spec_verify()
+    kc, vc = m.pool.key_cache.to(dev), m.pool.value_cache.to(dev)
+    pd.pd_reshape_and_cache(m.new_key.to(dev), m.new_value.to(dev), kc, vc,
+                            m.slot_mapping.to(dev))
+    q = m.q_prefill.to(dev)
+    out = torch.empty_like(q)
+    cu = m.cu_q_lens.to(dev)
+    bt = m.pool.block_tables[:m.Bp].to(dev)
+    cl = m.pool.context_lens[:m.Bp].to(dev)
+    t = _time_calls(lambda: pd.pd_paged_prefill_chunk(out, q, cu, m.max_q_len, kc, vc, bt, cl,
+                                                      m.scale), args.extra_steps, flush)
+    ctx = m.pool.context_lens[:m.Bp].double()
+    kv = float(ctx.sum()) * m.Hk * m.D * 2 * 2
+    nq = m.max_q_len
+    P = m.prior_lens.double()
+    flops = float(4 * m.D * m.H * (nq * P + nq * (nq + 1) / 2).sum())
+    res = {"workload": f"{m.Bp} sequences x {nq} query tokens, prior U[128, 2048], bf16",
+           "ms": round(t * 1e3, 4), "kv_gbs": round(kv / t / 1e9, 1),
+           "kv_frac": round(kv / t / 1e9 / hbm_peak, 4), "tflops": round(flops / t / 1e12, 2),
+           "query_tokens_per_s": round(m.Bp * nq / t, 1)}
+    del kc, vc
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_kv_handover(pd, pd_inputs, dev, args, flush, hbm_peak):
+    """KV hand-over of 4 sequences x 2048 tokens, 32 layers, Qwen3-8B kv shape:
+    pack on the sending side, unpack into the receiving pool (1 GiB of KV each
+    way; bytes = read + written)."""
+    import torch
+    c = pd_inputs.kv_transfer(seed=0, device=dev)
+    send = c.block_ids(c.send_tables).to(dev)
+    recv = c.block_ids(c.recv_tables).to(dev)
+    st = pd.kv_staging(c.L, send.numel(), c.key_caches[0])
+    rk = [torch.empty(c.NB_recv, c.Hk, c.S, c.D, dtype=c.dtype, device=dev) for _ in range(c.L)]
+    rv = [torch.empty_like(t) for t in rk]
+    n = args.extra_steps
+    t_pack = _time_calls(lambda: pd.pd_kv_pack(st, c.key_caches, c.value_caches, send), n, flush)
+    t_unpack = _time_calls(lambda: pd.pd_kv_unpack(st, rk, rv, recv), n, flush)
+    kv = st.numel() * st.element_size()
+    res = {"workload": "32 layers, 4 x 2048 tokens, 8 kv heads x 128, S 16, bf16",
+           "kv_bytes": kv,
+           "pack_ms": round(t_pack * 1e3, 4), "pack_gbs": round(2 * kv / t_pack / 1e9, 1),
+           "pack_frac": round(2 * kv / t_pack / 1e9 / hbm_peak, 4),
+           "unpack_ms": round(t_unpack * 1e3, 4), "unpack_gbs": round(2 * kv / t_unpack / 1e9, 1),
+           "unpack_frac": round(2 * kv / t_unpack / 1e9 / hbm_peak, 4)}
+    del c, st, rk, rv
+    torch.cuda.empty_cache()
     return res
 
 

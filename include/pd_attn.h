@@ -190,6 +190,36 @@ PD_API pd_status pd_copy_blocks(void* const* key_caches, void* const* value_cach
                          int32_t* dev_err, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------- */
+/* KV hand-over between a prefill worker and a decode worker (nanoPD page,
+ * "异步KV传输": the KV of a finished prefill moves to the decode side on a
+ * stream of its own; essay page "LLM推理PD分离架构深度工程实践", section 3.1:
+ * layer-by-layer transfer, so the receiver can start on the first layers while
+ * later ones are in flight).
+ * pd_kv_pack gathers whole blocks of every layer into one contiguous staging
+ * buffer, layer-major:
+ *   staging[l][0 = K, 1 = V][i][Hk][S][D] = pool_l[block_ids[i]]
+ * so layer l is the run of 2 * nblk * Hk*S*D elements that starts at element
+ * l * 2 * nblk * Hk*S*D.  pd_kv_unpack is the inverse: it writes each staged
+ * slab into block block_ids[i] of the (receiving) pools.
+ *   staging       device, 16-byte aligned, L * 2 * nblk * Hk*S*D elements
+ *   key_caches, value_caches  DEVICE arrays of L device pointers, one pool
+ *                 [NB][Hk][S][D] per layer (as for pd_copy_blocks)
+ *   block_ids     DEVICE int32 [nblk]; an id outside [0, NB) skips its slabs
+ *                 (pack leaves them untouched, unpack does not read them) and
+ *                 flags PD_DEVERR_BLOCK_RANGE.  For unpack, two equal ids race.
+ * Bit copies.  nblk == 0 or L == 0 launches nothing. */
+PD_API pd_status pd_kv_pack(void* staging, void* const* key_caches,
+                            void* const* value_caches, int L,
+                            const int32_t* block_ids, int nblk, int Hk, int D,
+                            int S, int NB, pd_dtype dt, int32_t* dev_err,
+                            cudaStream_t stream);
+PD_API pd_status pd_kv_unpack(const void* staging, void* const* key_caches,
+                              void* const* value_caches, int L,
+                              const int32_t* block_ids, int nblk, int Hk, int D,
+                              int S, int NB, pd_dtype dt, int32_t* dev_err,
+                              cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
 /* Chunked-prefill attention (nanoPD page "分块预填充": long prompts are cut
  * into chunks interleaved with decode; tutorial page section 5.2): sequence
  * i appends a chunk of C_i query tokens after P_i cached tokens; its chunk

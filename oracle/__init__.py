@@ -84,6 +84,8 @@ def _bind(lib):
                                           i32, i64, i64]
     lib.orc_copy_blocks.restype = i32
     lib.orc_copy_blocks.argtypes = [P, P, i32, P, i32, i32, i32, i32, i32]
+    lib.orc_kv_pack.restype = i32
+    lib.orc_kv_pack.argtypes = [i32, P, P, P, i32, P, i32, i32, i32, i32, i32]
     lib.orc_decode.restype = i32
     lib.orc_decode.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32,
                                i32, i32, dbl, i32, i64, i64]
@@ -166,6 +168,30 @@ def copy_blocks(key_caches: list, value_caches: list, block_mapping) -> int:
     kp = (ctypes.c_void_p * L)(*[_ptr(c) for c in key_caches])
     vp = (ctypes.c_void_p * L)(*[_ptr(c) for c in value_caches])
     return _load().orc_copy_blocks(kp, vp, L, _ptr(bm), bm.shape[0], Hk, D, S, NB)
+
+
+def kv_pack(key_caches: list, value_caches: list, block_ids) -> tuple[np.ndarray, int]:
+    """Staging buffer [L][2][nblk][Hk][S][D] (uint16) gathered from the pools, and
+    the number of skipped (out-of-range) ids."""
+    ids = np.ascontiguousarray(np.asarray(block_ids, dtype=np.int32))
+    L = len(key_caches)
+    NB, Hk, S, D = key_caches[0].shape
+    st = np.zeros((L, 2, ids.shape[0], Hk, S, D), dtype=np.uint16)
+    kp = (ctypes.c_void_p * L)(*[_ptr(c) for c in key_caches])
+    vp = (ctypes.c_void_p * L)(*[_ptr(c) for c in value_caches])
+    bad = _load().orc_kv_pack(0, _ptr(st), kp, vp, L, _ptr(ids), ids.shape[0], Hk, D, S, NB)
+    return st, bad
+
+
+def kv_unpack(staging: np.ndarray, key_caches: list, value_caches: list, block_ids) -> int:
+    """In place: scatter a staging buffer into the pools' blocks ``block_ids``."""
+    ids = np.ascontiguousarray(np.asarray(block_ids, dtype=np.int32))
+    st = np.ascontiguousarray(staging, dtype=np.uint16)
+    L = len(key_caches)
+    NB, Hk, S, D = key_caches[0].shape
+    kp = (ctypes.c_void_p * L)(*[_ptr(c) for c in key_caches])
+    vp = (ctypes.c_void_p * L)(*[_ptr(c) for c in value_caches])
+    return _load().orc_kv_pack(1, _ptr(st), kp, vp, L, _ptr(ids), ids.shape[0], Hk, D, S, NB)
 
 
 def _run_rows(fn, nrows: int, threads: int):

@@ -136,6 +136,34 @@ int orc_copy_blocks(uint16_t* const* key_caches, uint16_t* const* value_caches,
     return bad;
 }
 
+/* ---- KV pack / unpack ----------------------------------------------------
+ * nanoPD page, "异步KV传输"; essay page "LLM推理PD分离架构深度工程实践",
+ * section 3.1 (layer-by-layer KV transfer).  Staging layout, layer-major:
+ *   staging[l][kv][i][Hk][S][D] = pool_{l,kv}[block_ids[i]]   (kv 0 = K, 1 = V)
+ * pack copies pool -> staging, unpack staging -> pool.  Ids outside [0, NB)
+ * are skipped; the count of skipped ids is returned. */
+int orc_kv_pack(int unpack, uint16_t* staging, uint16_t* const* key_caches,
+                uint16_t* const* value_caches, int L, const int32_t* block_ids, int nblk,
+                int Hk, int D, int S, int NB) {
+    int bad = 0;
+    int64_t slab = (int64_t)Hk * S * D;
+    for (int i = 0; i < nblk; ++i) {
+        int32_t b = block_ids[i];
+        if (b < 0 || b >= NB) { ++bad; continue; }
+        for (int l = 0; l < L; ++l) {
+            for (int kv = 0; kv < 2; ++kv) {
+                uint16_t* pool = kv == 0 ? key_caches[l] : value_caches[l];
+                uint16_t* st = staging + (((int64_t)l * 2 + kv) * nblk + i) * slab;
+                for (int64_t e = 0; e < slab; ++e) {
+                    if (unpack) pool[(int64_t)b * slab + e] = st[e];
+                    else st[e] = pool[(int64_t)b * slab + e];
+                }
+            }
+        }
+    }
+    return bad;
+}
+
 /* ---- attention of one query row over keys [0, n_keys) ------------------ */
 /* out[d] = sum_t softmax_t(scale * q.k_t) * v_t[d], in float64, two passes
  * (max, then exponentials) for a well-defined result.  n_keys <= 0 gives

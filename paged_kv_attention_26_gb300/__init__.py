@@ -51,6 +51,8 @@ SIGNATURES = {
     "pd_paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
                                                _I, _I, _F, _I, _P, _P]),
     "pd_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "pd_kv_pack": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "pd_kv_unpack": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pd_paged_prefill_chunk": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
                                     _I, _F, _I, _P, _P]),
     "pd_bm_create": (_P, [_I, _I]),
@@ -279,6 +281,58 @@ def pd_copy_blocks(key_caches, value_caches, block_mapping, dev_err=None, stream
                                block_mapping.shape[0], Hk, D, S, NB, _dt(key_caches[0]),
                                _opt(dev_err), _stream(stream))
     _check("pd_copy_blocks", st)
+
+
+def _pools_check(key_caches, value_caches):
+    L = len(key_caches)
+    if L == 0 or L != len(value_caches):
+        raise ValueError("need the same number (> 0) of key and value pools")
+    for t in list(key_caches) + list(value_caches):
+        if t.shape != key_caches[0].shape or t.dtype != key_caches[0].dtype:
+            raise ValueError("all pools must share shape and dtype")
+        if _dev(t, "cache") % 16:
+            raise ValueError("cache pools must be 16-byte aligned")
+    return L
+
+
+def kv_staging(L: int, nblk: int, key_cache, device=None):
+    """Allocate a staging buffer [L, 2, nblk, Hk, S, D] for ``pd_kv_pack``."""
+    torch = _torch()
+    NB, Hk, S, D = key_cache.shape
+    return torch.empty((L, 2, nblk, Hk, S, D), dtype=key_cache.dtype,
+                       device=device or key_cache.device)
+
+
+def pd_kv_pack(staging, key_caches, value_caches, block_ids, dev_err=None, stream=None):
+    """Gather blocks ``block_ids`` (int32 CUDA [nblk]) of every layer's K and V pool
+    into ``staging`` ([L, 2, nblk, Hk, S, D], layer-major)."""
+    torch = _torch()
+    L = _pools_check(key_caches, value_caches)
+    NB, Hk, S, D = key_caches[0].shape
+    nblk = block_ids.shape[0]
+    if tuple(staging.shape) != (L, 2, nblk, Hk, S, D) or staging.dtype != key_caches[0].dtype:
+        raise ValueError("staging must be [L, 2, nblk, Hk, S, D] of the pools' dtype")
+    st = load().pd_kv_pack(_dev(staging, "staging"), pointer_array(key_caches).data_ptr(),
+                           pointer_array(value_caches).data_ptr(), L,
+                           _dev(block_ids, "block_ids", torch.int32), nblk, Hk, D, S, NB,
+                           _dt(key_caches[0]), _opt(dev_err), _stream(stream))
+    _check("pd_kv_pack", st)
+
+
+def pd_kv_unpack(staging, key_caches, value_caches, block_ids, dev_err=None, stream=None):
+    """Scatter ``staging`` ([L, 2, nblk, Hk, S, D]) into blocks ``block_ids`` of the
+    pools (the receiver's ids)."""
+    torch = _torch()
+    L = _pools_check(key_caches, value_caches)
+    NB, Hk, S, D = key_caches[0].shape
+    nblk = block_ids.shape[0]
+    if tuple(staging.shape) != (L, 2, nblk, Hk, S, D) or staging.dtype != key_caches[0].dtype:
+        raise ValueError("staging must be [L, 2, nblk, Hk, S, D] of the pools' dtype")
+    st = load().pd_kv_unpack(_dev(staging, "staging"), pointer_array(key_caches).data_ptr(),
+                             pointer_array(value_caches).data_ptr(), L,
+                             _dev(block_ids, "block_ids", torch.int32), nblk, Hk, D, S, NB,
+                             _dt(key_caches[0]), _opt(dev_err), _stream(stream))
+    _check("pd_kv_unpack", st)
 
 
 def pd_paged_prefill_chunk(out, q, cu_q_lens, max_q_len: int, key_cache, value_cache,

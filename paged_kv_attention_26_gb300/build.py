@@ -15,7 +15,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libpd_attn.so")
 
-CUDA_SOURCES = ["capi.cu", "store_copy.cu", "decode.cu", "decode_static.cu", "prefill.cu"]
+CUDA_SOURCES = ["capi.cu", "store_copy.cu", "kv_pack.cu", "decode.cu", "decode_static.cu",
+                "prefill.cu"]
 CXX_SOURCES = ["block_manager.cpp"]
 HEADERS = ["pd_device.cuh", "pd_internal.h", "pd_tcgen05.cuh", "pd_mma.cuh", "pd_tmap.h"]
 

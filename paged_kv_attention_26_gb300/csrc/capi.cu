@@ -118,6 +118,34 @@ pd_status pd_copy_blocks(void* const* key_caches, void* const* value_caches, int
                               dev_err, stream);
 }
 
+static pd_status kv_pack_common(bool unpack, void* staging, void* const* key_caches,
+                                void* const* value_caches, int L, const int32_t* block_ids,
+                                int nblk, int Hk, int D, int S, int NB, pd_dtype dt,
+                                int32_t* dev_err, cudaStream_t stream) {
+    if (L < 0 || nblk < 0 || Hk < 1 || NB < 1) return PD_ERR_INVALID_ARG;
+    if (!supported_D(D) || !supported_S(S) || !supported_dt(dt)) return PD_ERR_UNSUPPORTED;
+    if (L == 0 || nblk == 0) return PD_OK;
+    if (!staging || !key_caches || !value_caches || !block_ids || !aligned16(staging))
+        return PD_ERR_INVALID_ARG;
+    if (L > 65535) return PD_ERR_UNSUPPORTED;
+    return launch_kv_pack(unpack, staging, key_caches, value_caches, L, block_ids, nblk, Hk, D,
+                          S, NB, dev_err, stream);
+}
+
+pd_status pd_kv_pack(void* staging, void* const* key_caches, void* const* value_caches, int L,
+                     const int32_t* block_ids, int nblk, int Hk, int D, int S, int NB,
+                     pd_dtype dt, int32_t* dev_err, cudaStream_t stream) {
+    return kv_pack_common(false, staging, key_caches, value_caches, L, block_ids, nblk, Hk, D, S,
+                          NB, dt, dev_err, stream);
+}
+
+pd_status pd_kv_unpack(const void* staging, void* const* key_caches, void* const* value_caches,
+                       int L, const int32_t* block_ids, int nblk, int Hk, int D, int S, int NB,
+                       pd_dtype dt, int32_t* dev_err, cudaStream_t stream) {
+    return kv_pack_common(true, const_cast<void*>(staging), key_caches, value_caches, L,
+                          block_ids, nblk, Hk, D, S, NB, dt, dev_err, stream);
+}
+
 pd_status pd_paged_prefill_chunk(void* out, const void* q, int total_q,
                                  const int32_t* cu_q_lens, int max_q_len,
                                  const void* key_cache, const void* value_cache,

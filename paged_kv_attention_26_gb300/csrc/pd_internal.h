@@ -52,6 +52,11 @@ pd_status launch_copy_blocks(void* const* key_caches, void* const* value_caches,
                              const int64_t* block_mapping, int npairs, int Hk, int D, int S,
                              int NB, int32_t* dev_err, cudaStream_t stream);
 
+// ---- KV pack / unpack ------------------------------------------------------------------
+pd_status launch_kv_pack(bool unpack, void* staging, void* const* key_caches,
+                         void* const* value_caches, int L, const int32_t* block_ids, int nblk,
+                         int Hk, int D, int S, int NB, int32_t* dev_err, cudaStream_t stream);
+
 // ---- prefill -------------------------------------------------------------------------
 struct PrefillArgs {
     void* out;

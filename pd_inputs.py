@@ -325,3 +325,62 @@ def cow_fork_stress(S: int, seed: int = 0, n_prompts: int = 32, n_fork: int = 8,
     nv = torch.randn(n, Hk, D, generator=gd).to(dtype)
     return ForkCase(lens, n_fork, S, NB, k, v, q, nk, nv, H, Hk, D,
                     1.0 / math.sqrt(D), dtype)
+
+
+@dataclass
+class TransferCase:
+    """A paged cache on the sending side and the block ids the same sequences
+    get on the receiving side (prefill -> decode hand-over)."""
+    key_caches: list                 # L sender pools [NB, Hk, S, D]
+    value_caches: list
+    send_tables: torch.Tensor        # int32 [B, max_blocks], sender block ids
+    recv_tables: torch.Tensor        # int32 [B, max_blocks], receiver block ids
+    context_lens: torch.Tensor       # int32 [B]
+    NB: int                          # sender pool size
+    NB_recv: int                     # receiver pool size
+    S: int
+    Hk: int
+    D: int
+    dtype: torch.dtype
+
+    @property
+    def L(self):
+        return len(self.key_caches)
+
+    def block_ids(self, tables: torch.Tensor) -> torch.Tensor:
+        """The sequences' blocks in order (sequence-major), int32 [nblk]."""
+        nb = blocks_needed(self.context_lens.long(), self.S)
+        return torch.cat([tables[i, :n] for i, n in enumerate(nb.tolist())])
+
+
+def kv_transfer(seed: int = 0, L: int = 32, B: int = 4, ctx: int = 2048, Hk: int = 8,
+                D: int = 128, S: int = 16, dtype=torch.bfloat16, pool_factor: float = 1.25,
+                device="cpu") -> TransferCase:
+    """L layers, B sequences of ``ctx`` tokens (Qwen3-8B kv shape by default:
+    8 KV heads, head_dim 128, block size 16, bf16).  Each side scatters the
+    sequences' blocks over a random permutation of its own pool (1.25x the
+    blocks needed); K, V ~ N(0, 1).  One block table serves every layer."""
+    g = _gen(seed + 6000)
+    ctxs = torch.full((B,), ctx, dtype=torch.int64)
+    send, NB, _ = make_block_tables(g, ctxs, S, None, pool_factor)
+    recv, NB_recv, _ = make_block_tables(g, ctxs, S, None, pool_factor)
+    gd = _gen(seed + 6100, device)
+    kcs, vcs = [], []
+    for _ in range(L):
+        k, v = fill_pool(gd, NB, Hk, S, D, dtype, device=device)
+        kcs.append(k)
+        vcs.append(v)
+    return TransferCase(kcs, vcs, send, recv, ctxs.to(torch.int32), NB, NB_recv, S, Hk, D,
+                        dtype)
+
+
+def spec_verify(seed: int = 0, B: int = 64, n_q: int = 4, lo: int = 128, hi: int = 2048,
+                H: int = 32, Hk: int = 8, D: int = 128, S: int = 16,
+                dtype=torch.bfloat16) -> MixedCase:
+    """Speculative verification: each of B sequences with a prior context
+    uniform on [lo, hi] appends n_q tokens (the last accepted token plus
+    n_q - 1 drafted ones) whose queries attend causally; Qwen3-8B shape by
+    default.  A prefill-chunk case with every C_i = n_q and no decode part."""
+    g = _gen(seed + 7000)
+    P = randint(g, lo, hi, B)
+    return mixed_case(seed + 7100, P, [n_q] * B, [], H, Hk, D, S, dtype)

@@ -216,3 +216,29 @@ def test_bm_errors(lib):
         bm.fork(7, 8)
     assert lib.pd_bm_create(0, 16) is None
     assert lib.pd_bm_ref_count(bm._h, 99) == -1
+
+
+def test_kv_pack_validation(lib):
+    for f in (lib.pd_kv_pack, lib.pd_kv_unpack):
+        # staging, key_caches, value_caches, L, block_ids, nblk, Hk, D, S, NB, dt
+        base = [P, P, P, 4, P, 10, 8, 128, 16, 100, pd.PD_BF16, None, None]
+        for change, want in [({6: 0}, 1),          # Hk
+                             ({7: 96}, 2),          # D
+                             ({8: 12}, 2),          # S
+                             ({10: 7}, 2),          # dtype
+                             ({0: None}, 1),        # staging
+                             ({0: P + 8}, 1),       # misaligned staging
+                             ({4: None}, 1),        # block ids
+                             ({3: 70000}, 2)]:      # too many layers for the grid
+            a = list(base)
+            for k, v in change.items():
+                a[k] = v
+            assert f(*a) == want, change
+        n0 = lib.pd_launch_count()
+        a = list(base)
+        a[5] = 0                                    # nothing to move
+        assert f(*a) == 0
+        a = list(base)
+        a[3] = 0                                    # no layers
+        assert f(*a) == 0
+        assert lib.pd_launch_count() == n0

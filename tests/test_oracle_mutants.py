@@ -33,6 +33,10 @@ MUTANTS = [
      "key_caches[l][dst * block_elems + e] = key_caches[l][src * block_elems + e];",
      "key_caches[l][src * block_elems + e] = key_caches[l][dst * block_elems + e];"),
     ("prefill_prior_len", "int64_t P = context_lens[i] - C;", "int64_t P = context_lens[i] - C + 1;"),
+    ("pack_layer_kv_swapped", "uint16_t* st = staging + (((int64_t)l * 2 + kv) * nblk + i) * slab;",
+     "uint16_t* st = staging + (((int64_t)kv * L + l) * nblk + i) * slab;"),
+    ("unpack_direction", "if (unpack) pool[(int64_t)b * slab + e] = st[e];",
+     "if (!unpack) pool[(int64_t)b * slab + e] = st[e];"),
 ]
 
 PIN_CHECKS = [
@@ -40,6 +44,8 @@ PIN_CHECKS = [
     lambda: pins.test_all_16bit_patterns_decode_like_torch(oracle.BF16, pins.torch.bfloat16),
     pins.test_store_then_gather_returns_the_token,
     pins.test_copy_blocks_brute_force,
+    pins.test_kv_pack_closed_form,
+    pins.test_kv_pack_unpack_moves_blocks_between_pools,
     pins.test_decode_matches_brute_force_tiny,
     pins.test_decode_matches_brute_force_bf16_gqa_variants,
     pins.test_ctx1_returns_v_exactly,

@@ -187,6 +187,68 @@ def test_copy_blocks_brute_force():
         assert np.array_equal(kcs[l], ref_k[l]) and np.array_equal(vcs[l], ref_v[l])
 
 
+def _coded_pools(L, NB, Hk, S, D):
+    """Pools whose every element encodes its own (layer, K/V, block, head,
+    offset, dim) coordinates, so a wrong index shows up as a wrong code."""
+    idx = np.arange(L * 2 * NB * Hk * S * D, dtype=np.int64).reshape(L, 2, NB, Hk, S, D)
+    assert idx.max() < 65536
+    code = idx.astype(np.uint16)
+    return [code[l, 0].copy() for l in range(L)], [code[l, 1].copy() for l in range(L)], code
+
+
+def test_kv_pack_closed_form():
+    """staging[l][kv][i] is block ids[i] of layer l's K (kv 0) or V (kv 1) pool,
+    element for element: a closed form of the layer-major layout."""
+    L, NB, Hk, S, D = 3, 7, 2, 4, 8
+    kcs, vcs, code = _coded_pools(L, NB, Hk, S, D)
+    ids = np.array([5, 0, 3, 6], dtype=np.int32)
+    st, bad = oracle.kv_pack(kcs, vcs, ids)
+    assert bad == 0 and st.shape == (L, 2, len(ids), Hk, S, D)
+    for l in range(L):
+        for kv in range(2):
+            for i, b in enumerate(ids):
+                base = (((l * 2 + kv) * NB + int(b)) * Hk) * S * D
+                expect = base + np.arange(Hk * S * D).reshape(Hk, S, D)
+                assert np.array_equal(st[l, kv, i].astype(np.int64), expect)
+    # layer l's part is one contiguous run starting at l * 2 * nblk * Hk*S*D
+    flat = st.reshape(-1)
+    run = 2 * len(ids) * Hk * S * D
+    assert np.array_equal(flat[run:2 * run], st[1].reshape(-1))
+
+
+def test_kv_pack_unpack_moves_blocks_between_pools():
+    """Pack from one pool's blocks, unpack into another pool's different
+    blocks: the receiving blocks hold the sender's data bit for bit, every
+    other receiving block is untouched, and out-of-range ids are skipped."""
+    rng = np.random.default_rng(3)
+    L, NB, Hk, S, D = 2, 9, 2, 8, 16
+    src_k = [rng.integers(0, 65535, (NB, Hk, S, D), dtype=np.uint16) for _ in range(L)]
+    src_v = [rng.integers(0, 65535, (NB, Hk, S, D), dtype=np.uint16) for _ in range(L)]
+    dst_k = [rng.integers(0, 65535, (NB, Hk, S, D), dtype=np.uint16) for _ in range(L)]
+    dst_v = [rng.integers(0, 65535, (NB, Hk, S, D), dtype=np.uint16) for _ in range(L)]
+    before_k = [k.copy() for k in dst_k]
+    before_v = [v.copy() for v in dst_v]
+    send = np.array([4, 1, 8], dtype=np.int32)
+    recv = np.array([0, 7, 2], dtype=np.int32)
+    st, bad = oracle.kv_pack(src_k, src_v, send)
+    assert bad == 0
+    assert oracle.kv_unpack(st, dst_k, dst_v, recv) == 0
+    for l in range(L):
+        for b in range(NB):
+            if b in recv:
+                j = list(recv).index(b)
+                assert np.array_equal(dst_k[l][b], src_k[l][send[j]])
+                assert np.array_equal(dst_v[l][b], src_v[l][send[j]])
+            else:
+                assert np.array_equal(dst_k[l][b], before_k[l][b])
+                assert np.array_equal(dst_v[l][b], before_v[l][b])
+    st2, bad2 = oracle.kv_pack(src_k, src_v, np.array([2, -1, NB], dtype=np.int32))
+    assert bad2 == 2
+    for l in range(L):
+        assert np.array_equal(st2[l, 0, 0], src_k[l][2]) and np.array_equal(st2[l, 1, 0], src_v[l][2])
+    assert not st2[:, :, 1:].any()               # skipped slabs stay as allocated (zeros)
+
+
 # ---- decode attention -----------------------------------------------------
 
 def _stored(c):
