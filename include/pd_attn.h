@@ -282,6 +282,53 @@ PD_API double pd_bm_usage(const pd_bm* bm);
 PD_API int pd_bm_ref_count(const pd_bm* bm, int block_id);
 /* Free blocks left. */
 PD_API int pd_bm_num_free(const pd_bm* bm);
+/* A new sequence whose first nblocks blocks are existing blocks (a cached
+ * prefix, tutorial page section 4): each gets one more reference, nothing is
+ * copied; its length is `length` tokens (within the last given block).  The
+ * blocks must be in use (ref count >= 1).  Later appends follow the usual
+ * rules (a shared, partly filled last block is copied on write). */
+PD_API pd_status pd_bm_add_seq_shared(pd_bm* bm, int seq_id,
+                                      const int32_t* blocks, int nblocks,
+                                      int64_t length);
+/* One more / one fewer reference on a block in use, held by a holder that
+ * is not a sequence (the prefix cache); the last drop frees the block. */
+PD_API pd_status pd_bm_retain(pd_bm* bm, int block_id);
+PD_API pd_status pd_bm_drop(pd_bm* bm, int block_id);
+
+/* ---------------------------------------------------------------------- */
+/* Prefix cache: the hash chain of the tutorial page "LLM 推理服务引擎深度拆
+ * 解", section 4.2 / 4.3.  A prompt is cut into full blocks of block_size
+ * tokens; block i's key is the first 32 hex digits of
+ *   sha256(parent + tokens + extra)
+ * with parent = key of block i-1 ("ROOT" for block 0), tokens = the block's
+ * ids in decimal joined by ",", extra = caller string (NULL = "").  The table
+ * maps key -> physical block id, holds at most capacity_blocks entries and
+ * evicts the least recently used key.  Host only. */
+typedef struct pd_pc pd_pc;
+PD_API pd_pc* pd_pc_create(int capacity_blocks, int block_size);
+PD_API void pd_pc_destroy(pd_pc* pc);
+/* Keys of every full block of token_ids[0..n) and the longest cached prefix.
+ *   hit_tokens      tokens of the longest cached prefix (multiple of
+ *                   block_size): blocks up to the first key not in the table
+ *   chain_out       [n / block_size][33]: all n / block_size keys,
+ *                   NUL-terminated (*n_chain = n / block_size), so that one
+ *                   pd_pc_insert can cache the whole prompt
+ *   hit_blocks_out  [n / block_size] (may be NULL): block ids of the hits
+ * Touches every hit key; counts one hit (hit_tokens > 0) or one miss. */
+PD_API pd_status pd_pc_lookup(pd_pc* pc, const int32_t* token_ids, int n,
+                              const char* extra, int* hit_tokens,
+                              char* chain_out, int32_t* hit_blocks_out,
+                              int* n_chain);
+/* Map chain[i] -> block_ids[i] for keys not yet held (evicting the least
+ * recently used key when full) and touch every key of the chain.  The ids
+ * of evicted entries go to evicted_out ([n_chain], may be NULL), their count
+ * to *n_evicted: the caller drops its references on them. */
+PD_API pd_status pd_pc_insert(pd_pc* pc, const char* chain, int n_chain,
+                              const int32_t* block_ids, int32_t* evicted_out,
+                              int* n_evicted);
+PD_API int pd_pc_size(const pd_pc* pc);
+PD_API int64_t pd_pc_hits(const pd_pc* pc);
+PD_API int64_t pd_pc_misses(const pd_pc* pc);
 
 #ifdef __cplusplus
 }

@@ -11,6 +11,10 @@ Contents
 - ``block_manager.py``: the ref-counted block manager with copy-on-write fork,
   following the tutorial page "LLM 推理服务引擎深度拆解", section 2.3.
 - ``kv_bytes.py``: the KV-cache size formula of the same page, section 1.3.
+- ``prefix_cache.py``: the block hash chain prefix cache of the same page,
+  sections 4.2 and 4.3.
+- ``oracle.c`` also holds the KV pack/unpack staging layout for the
+  prefill -> decode hand-over.
 
 Parity pins for every function here live in ``tests/test_oracle_*.py``.
 """
@@ -25,6 +29,7 @@ from concurrent.futures import ThreadPoolExecutor
 import numpy as np
 
 from .block_manager import BlockManager, Sequence  # noqa: F401
+from .prefix_cache import PrefixCache, block_key  # noqa: F401
 from .kv_bytes import kv_cache_bytes, pd_transfer_bytes  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

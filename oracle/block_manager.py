@@ -97,3 +97,22 @@ class Sequence:
         for bid in self.block_table:
             self.mgr.free(bid)
         self.block_table = []
+
+    @classmethod
+    def shared(cls, mgr: BlockManager, seq_id: int, blocks, length: int) -> "Sequence":
+        """A sequence whose first blocks are existing ones (a cached prefix):
+        each gets one more reference, nothing is copied."""
+        S = mgr.block_size
+        if blocks and not (len(blocks) - 1) * S < length <= len(blocks) * S:
+            raise ValueError("length must end inside the last shared block")
+        if not blocks and length != 0:
+            raise ValueError("no blocks, no tokens")
+        for bid in blocks:
+            if mgr.ref_count[bid] < 1:
+                raise ValueError(f"block {bid} is not in use")
+        seq = cls(mgr, seq_id)
+        seq.block_table = list(blocks)
+        seq.length = length
+        for bid in blocks:
+            mgr.incref(bid)
+        return seq

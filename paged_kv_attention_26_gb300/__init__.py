@@ -68,6 +68,19 @@ SIGNATURES = {
     "pd_bm_usage": (ctypes.c_double, [_P]),
     "pd_bm_ref_count": (_I, [_P, _I]),
     "pd_bm_num_free": (_I, [_P]),
+    "pd_bm_add_seq_shared": (_I, [_P, _I, ctypes.POINTER(ctypes.c_int32), _I, _I64]),
+    "pd_bm_retain": (_I, [_P, _I]),
+    "pd_bm_drop": (_I, [_P, _I]),
+    "pd_pc_create": (_P, [_I, _I]),
+    "pd_pc_destroy": (None, [_P]),
+    "pd_pc_lookup": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _I, ctypes.c_char_p,
+                          ctypes.POINTER(ctypes.c_int), ctypes.c_char_p,
+                          ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int)]),
+    "pd_pc_insert": (_I, [_P, ctypes.c_char_p, _I, ctypes.POINTER(ctypes.c_int32),
+                          ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int)]),
+    "pd_pc_size": (_I, [_P]),
+    "pd_pc_hits": (_I64, [_P]),
+    "pd_pc_misses": (_I64, [_P]),
 }
 
 _lock = threading.Lock()
@@ -417,3 +430,80 @@ class BlockManager:
     @property
     def num_free(self) -> int:
         return int(self._lib.pd_bm_num_free(self._h))
+
+    def add_seq_shared(self, seq_id: int, blocks, length: int):
+        """New sequence starting on existing blocks (a cached prefix)."""
+        arr = (ctypes.c_int32 * max(1, len(blocks)))(*blocks)
+        _check("pd_bm_add_seq_shared", self._lib.pd_bm_add_seq_shared(
+            self._h, seq_id, arr, len(blocks), int(length)))
+
+    def retain(self, block_id: int):
+        _check("pd_bm_retain", self._lib.pd_bm_retain(self._h, block_id))
+
+    def drop(self, block_id: int):
+        _check("pd_bm_drop", self._lib.pd_bm_drop(self._h, block_id))
+
+
+class PrefixCache:
+    """Host prefix cache (pd_pc_*): block hash chain -> physical block, LRU."""
+
+    KEY = 32
+
+    def __init__(self, capacity_blocks: int, block_size: int):
+        self._lib = load()
+        self._h = self._lib.pd_pc_create(capacity_blocks, block_size)
+        if not self._h:
+            raise ValueError("pd_pc_create failed")
+        self.block_size = block_size
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            self._lib.pd_pc_destroy(h)
+            self._h = None
+
+    def lookup(self, token_ids, extra: str = ""):
+        """Returns (hit tokens, chain of block keys walked, block ids of the hits)."""
+        n = len(token_ids)
+        nfull = n // self.block_size
+        toks = (ctypes.c_int32 * max(1, n))(*token_ids)
+        chain = ctypes.create_string_buffer(max(1, nfull) * (self.KEY + 1))
+        hits = (ctypes.c_int32 * max(1, nfull))()
+        hit = ctypes.c_int()
+        nc = ctypes.c_int()
+        _check("pd_pc_lookup", self._lib.pd_pc_lookup(self._h, toks, n, extra.encode(),
+                                                      ctypes.byref(hit), chain, hits,
+                                                      ctypes.byref(nc)))
+        raw = chain.raw
+        keys = [raw[i * (self.KEY + 1): i * (self.KEY + 1) + self.KEY].decode()
+                for i in range(nc.value)]
+        return hit.value, keys, list(hits[: hit.value // self.block_size])
+
+    def insert(self, chain, block_ids):
+        """Returns the block ids of the entries evicted to make room."""
+        n = len(chain)
+        if len(block_ids) < n:
+            raise ValueError("need a block id per chain key")
+        buf = b"".join(k.encode()[: self.KEY].ljust(self.KEY + 1, b"\0") for k in chain)
+        ids = (ctypes.c_int32 * max(1, n))(*block_ids[:n])
+        ev = (ctypes.c_int32 * max(1, n))()
+        ne = ctypes.c_int()
+        _check("pd_pc_insert", self._lib.pd_pc_insert(self._h, buf if n else None, n, ids, ev,
+                                                      ctypes.byref(ne)))
+        return list(ev[: ne.value])
+
+    def __len__(self):
+        return int(self._lib.pd_pc_size(self._h))
+
+    @property
+    def hits(self) -> int:
+        return int(self._lib.pd_pc_hits(self._h))
+
+    @property
+    def misses(self) -> int:
+        return int(self._lib.pd_pc_misses(self._h))
+
+    @property
+    def hit_rate(self) -> float:
+        tot = self.hits + self.misses
+        return self.hits / tot if tot else 0.0

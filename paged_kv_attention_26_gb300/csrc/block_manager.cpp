@@ -143,4 +143,41 @@ int pd_bm_ref_count(const pd_bm* bm, int block_id) {
 
 int pd_bm_num_free(const pd_bm* bm) { return bm ? int(bm->free_ids.size()) : -1; }
 
+pd_status pd_bm_add_seq_shared(pd_bm* bm, int seq_id, const int32_t* blocks, int nblocks,
+                               int64_t length) {
+    if (!bm || seq_id < 0 || nblocks < 0 || (nblocks > 0 && !blocks) || bm->seqs.count(seq_id))
+        return PD_ERR_INVALID_ARG;
+    const int S = bm->block_size;
+    if (length < 0 || length > int64_t(nblocks) * S ||
+        (nblocks > 0 && length <= int64_t(nblocks - 1) * S))
+        return PD_ERR_INVALID_ARG;
+    for (int i = 0; i < nblocks; ++i) {
+        const int32_t b = blocks[i];
+        if (b < 0 || size_t(b) >= bm->ref_count.size() || bm->ref_count[size_t(b)] < 1)
+            return PD_ERR_INVALID_ARG;     // only a block in use holds data to share
+    }
+    pd_bm::Seq s;
+    s.table.assign(blocks, blocks + nblocks);
+    s.length = length;
+    for (int32_t b : s.table) bm->ref_count[size_t(b)] += 1;
+    bm->seqs.emplace(seq_id, std::move(s));
+    return PD_OK;
+}
+
+pd_status pd_bm_retain(pd_bm* bm, int block_id) {
+    if (!bm || block_id < 0 || size_t(block_id) >= bm->ref_count.size() ||
+        bm->ref_count[size_t(block_id)] < 1)
+        return PD_ERR_INVALID_ARG;
+    bm->ref_count[size_t(block_id)] += 1;
+    return PD_OK;
+}
+
+pd_status pd_bm_drop(pd_bm* bm, int block_id) {
+    if (!bm || block_id < 0 || size_t(block_id) >= bm->ref_count.size() ||
+        bm->ref_count[size_t(block_id)] < 1)
+        return PD_ERR_INVALID_ARG;
+    bm->drop(block_id);
+    return PD_OK;
+}
+
 }  // extern "C"

@@ -384,3 +384,16 @@ def spec_verify(seed: int = 0, B: int = 64, n_q: int = 4, lo: int = 128, hi: int
     g = _gen(seed + 7000)
     P = randint(g, lo, hi, B)
     return mixed_case(seed + 7100, P, [n_q] * B, [], H, Hk, D, S, dtype)
+
+
+def token_kv(positions, token_ids, Hk: int = 8, D: int = 128, dtype=torch.bfloat16,
+             seed: int = 0):
+    """K and V [T, Hk, D] of tokens given by (position, token id): each pair
+    draws N(0, 1) values from its own seeded generator, so equal prefixes give
+    equal K/V (as a deterministic model would) whatever request they sit in."""
+    ks, vs = [], []
+    for p, t in zip(list(positions), list(token_ids)):
+        g = _gen((seed * 1_000_003 + int(p) * 7919 + int(t)) % (2 ** 62))
+        ks.append(torch.randn(Hk, D, generator=g))
+        vs.append(torch.randn(Hk, D, generator=g))
+    return torch.stack(ks).to(dtype), torch.stack(vs).to(dtype)
