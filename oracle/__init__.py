@@ -30,7 +30,7 @@ import numpy as np
 
 from .block_manager import BlockManager, Sequence  # noqa: F401
 from .prefix_cache import PrefixCache, block_key  # noqa: F401
-from .kv_bytes import kv_cache_bytes, pd_transfer_bytes  # noqa: F401
+from .kv_bytes import concurrency_limit, kv_cache_bytes, pd_transfer_bytes  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
@@ -91,6 +91,15 @@ def _bind(lib):
     lib.orc_copy_blocks.argtypes = [P, P, i32, P, i32, i32, i32, i32, i32]
     lib.orc_kv_pack.restype = i32
     lib.orc_kv_pack.argtypes = [i32, P, P, P, i32, P, i32, i32, i32, i32, i32]
+    lib.orc_e4m3_to_double.restype = dbl
+    lib.orc_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.orc_e4m3_encode.restype = ctypes.c_uint8
+    lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.orc_reshape_and_cache_fp8.restype = i32
+    lib.orc_reshape_and_cache_fp8.argtypes = [P, P, i32, P, P, P, i32, i32, i32, i32, i32, P, P]
+    lib.orc_decode_fp8.restype = i32
+    lib.orc_decode_fp8.argtypes = [P, P, i32, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
+                                   dbl, i64, i64]
     lib.orc_decode.restype = i32
     lib.orc_decode.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32,
                                i32, i32, dbl, i32, i64, i64]
@@ -197,6 +206,65 @@ def kv_unpack(staging: np.ndarray, key_caches: list, value_caches: list, block_i
     kp = (ctypes.c_void_p * L)(*[_ptr(c) for c in key_caches])
     vp = (ctypes.c_void_p * L)(*[_ptr(c) for c in value_caches])
     return _load().orc_kv_pack(1, _ptr(st), kp, vp, L, _ptr(ids), ids.shape[0], Hk, D, S, NB)
+
+
+def e4m3_to_double(code: int) -> float:
+    return float(_load().orc_e4m3_to_double(int(code) & 0xFF))
+
+
+def e4m3_encode(y: float) -> int:
+    """Nearest E4M3 code of a float32 value (ties to even, saturating at 448)."""
+    return int(_load().orc_e4m3_encode(float(np.float32(y))))
+
+
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+def _u8(a) -> np.ndarray:
+    if hasattr(a, "detach"):
+        import torch
+        a = a.detach().contiguous().view(torch.uint8).numpy()
+    return np.ascontiguousarray(a, dtype=np.uint8)
+
+
+def reshape_and_cache_fp8(key, value, dtype: int, key_cache: np.ndarray,
+                          value_cache: np.ndarray, slot_mapping, k_scale, v_scale,
+                          S: int) -> int:
+    """In place on uint8 pools [NB, Hk, S, D]; key/value are fp16/bf16 [T, Hk, D]."""
+    k, v = _u16(key), _u16(value)
+    T, Hk, D = k.shape
+    sm = _i64(slot_mapping)
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    NB = key_cache.shape[0]
+    return _load().orc_reshape_and_cache_fp8(_ptr(k), _ptr(v), dtype, _ptr(key_cache),
+                                             _ptr(value_cache), _ptr(sm), T, Hk, D, S, NB,
+                                             _ptr(ks), _ptr(vs))
+
+
+def decode_fp8(q, qdtype: int, key_cache, value_cache, k_scale, v_scale, block_tables,
+               context_lens, scale: float, threads: int | None = None,
+               rows: tuple[int, int] | None = None) -> np.ndarray:
+    """Decode attention over FP8 pools in float64 -> [B, H, D] (or the row range)."""
+    qa = _u16(q)
+    B, H, D = qa.shape
+    kc, vc = _u8(key_cache), _u8(value_cache)
+    NB, Hk, S, _ = kc.shape
+    bt, cl = _i32(block_tables), _i32(context_lens)
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    r0, r1 = rows if rows is not None else (0, B * H)
+    out = np.zeros((B * H, D), dtype=np.float64)
+    lib = _load()
+
+    def work(a, b):
+        return lib.orc_decode_fp8(_ptr(out), _ptr(qa), qdtype, _ptr(kc), _ptr(vc), _ptr(ks),
+                                  _ptr(vs), _ptr(bt), bt.shape[1], _ptr(cl), H, Hk, D, S, NB,
+                                  float(scale), a, b)
+    bad = _run_rows(lambda a, b: work(r0 + a, r0 + b), r1 - r0, threads or os.cpu_count() or 1)
+    if bad:
+        raise ValueError(f"{bad} rows named a block outside the pool")
+    res = out[r0:r1]
+    return res.reshape(B, H, D) if rows is None else res
 
 
 def _run_rows(fn, nrows: int, threads: int):

@@ -17,3 +17,12 @@ def kv_cache_bytes(layers: int, kv_heads: int, head_dim: int, seq_len: int,
 def pd_transfer_bytes(seq_len: int, layers: int, kv_heads: int, head_dim: int,
                       dtype_bytes: int) -> int:
     return kv_cache_bytes(layers, kv_heads, head_dim, seq_len, dtype_bytes, 1)
+
+
+def concurrency_limit(kv_gb_per_request: float, weights_gb: float, total_gb: float,
+                      reserve_gb: float = 4.0) -> int:
+    """Requests whose KV fits beside the weights and a reserve for activations
+    and fragmentation (tutorial page, section 8.1: quantising the KV cache
+    raises this limit): floor(free / per-request KV)."""
+    free = total_gb - weights_gb - reserve_gb
+    return int(free // kv_gb_per_request)

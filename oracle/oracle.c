@@ -228,6 +228,117 @@ int orc_decode(double* out, const uint16_t* q, const uint16_t* key_cache,
     return bad;
 }
 
+/* ---- FP8 (E4M3) KV cache ------------------------------------------------
+ * Essay page "LLM推理PD分离架构深度工程实践", section 6.2 and tutorial page
+ * "LLM 推理服务引擎深度拆解", section 8.1: the KV cache stored in FP8 E4M3
+ * (one byte per value) instead of BF16 halves its memory and bandwidth.
+ * E4M3: 1 sign, 4 exponent (bias 7) and 3 fraction bits; exponent field 0 is
+ * subnormal (f * 2^-9); S.1111.111 is NaN; no infinities; largest 448.
+ * Each (layer, kv head) has a scale for K and one for V: a stored code c
+ * stands for e4m3(c) * scale.  Storing rounds y = x * (1 / scale), both
+ * products formed in float32, to the nearest code (ties to the even code),
+ * values beyond 448 in magnitude saturate to 448, NaN stays NaN. */
+double orc_e4m3_to_double(uint8_t c) {
+    int sign = c >> 7, e = (c >> 3) & 15, f = c & 7;
+    if (e == 15 && f == 7) return NAN;
+    double v = e == 0 ? ldexp((double)f, -9) : ldexp((double)(8 + f), e - 10);
+    return sign ? -v : v;
+}
+
+uint8_t orc_e4m3_encode(float y) {
+    if (isnan(y)) return 0x7F;
+    uint8_t sign = signbit(y) ? 0x80 : 0;
+    double a = fabs((double)y);
+    if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    /* nearest of the non-negative finite codes 0x00 .. 0x7E (values rise
+     * with the code); ties go to the even code */
+    uint8_t best = 0;
+    double best_d = a;
+    for (int c = 1; c <= 0x7E; ++c) {
+        double d = fabs(orc_e4m3_to_double((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = (uint8_t)c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* Store new tokens into FP8 pools: code = encode(x * (1 / scale[h])). */
+int orc_reshape_and_cache_fp8(const uint16_t* key, const uint16_t* value, int dtype,
+                              uint8_t* key_cache, uint8_t* value_cache,
+                              const int64_t* slot_mapping, int T, int Hk, int D, int S,
+                              int NB, const float* k_scale, const float* v_scale) {
+    int bad = 0;
+    for (int n = 0; n < T; ++n) {
+        int64_t slot = slot_mapping[n];
+        if (slot < 0) continue;
+        if (slot >= (int64_t)NB * S) { ++bad; continue; }
+        int64_t blk = slot / S, off = slot % S;
+        for (int h = 0; h < Hk; ++h) {
+            float kinv = 1.0f / k_scale[h], vinv = 1.0f / v_scale[h];
+            for (int d = 0; d < D; ++d) {
+                int64_t src = ((int64_t)n * Hk + h) * D + d;
+                int64_t dst = ((blk * Hk + h) * S + off) * D + d;
+                float kx = (float)orc_to_double(key[src], dtype);
+                float vx = (float)orc_to_double(value[src], dtype);
+                key_cache[dst] = orc_e4m3_encode(kx * kinv);
+                value_cache[dst] = orc_e4m3_encode(vx * vinv);
+            }
+        }
+    }
+    return bad;
+}
+
+/* Decode attention over FP8 pools: k = e4m3(code) * k_scale[kv head], the
+ * same for v; q and the result as for orc_decode. */
+int orc_decode_fp8(double* out, const uint16_t* q, int qdtype, const uint8_t* key_cache,
+                   const uint8_t* value_cache, const float* k_scale, const float* v_scale,
+                   const int32_t* block_tables, int max_blocks_per_seq,
+                   const int32_t* context_lens, int H, int Hk, int D, int S, int NB,
+                   double scale, int64_t row_begin, int64_t row_end) {
+    int G = H / Hk, bad = 0;
+    double* qd = (double*)malloc(sizeof(double) * D);
+    for (int64_t r = row_begin; r < row_end; ++r) {
+        int64_t i = r / H;
+        int h = (int)(r % H), kvh = h / G;
+        const int32_t* bt = block_tables + i * (int64_t)max_blocks_per_seq;
+        int64_t n = context_lens[i];
+        double* o = out + r * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        if (n <= 0) continue;
+        for (int d = 0; d < D; ++d) qd[d] = orc_to_double(q[r * D + d], qdtype);
+        double* sc = (double*)malloc(sizeof(double) * n);
+        int err = 0;
+        for (int64_t t = 0; t < n && !err; ++t) {
+            int64_t blk = bt[t / S];
+            if (blk < 0 || blk >= NB) { err = 1; break; }
+            const uint8_t* k = key_cache + ((blk * Hk + kvh) * S + t % S) * D;
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += qd[d] * (orc_e4m3_to_double(k[d]) * k_scale[kvh]);
+            sc[t] = scale * dot;
+        }
+        if (err) {
+            for (int d = 0; d < D; ++d) o[d] = NAN;
+            free(sc);
+            ++bad;
+            continue;
+        }
+        double m = -INFINITY, l = 0.0;
+        for (int64_t t = 0; t < n; ++t) if (sc[t] > m) m = sc[t];
+        for (int64_t t = 0; t < n; ++t) {
+            double w = exp(sc[t] - m);
+            l += w;
+            const uint8_t* v = value_cache + ((bt[t / S] * (int64_t)Hk + kvh) * S + t % S) * D;
+            for (int d = 0; d < D; ++d) o[d] += w * (orc_e4m3_to_double(v[d]) * v_scale[kvh]);
+        }
+        for (int d = 0; d < D; ++d) o[d] /= l;
+        free(sc);
+    }
+    free(qd);
+    return bad;
+}
+
 /* ---- decode written as split-context partitions plus a merge ----------- */
 /* The same result as orc_decode, reached the way the split-context kernel
  * organises it: partition p covers tokens [p*part, min(ctx, (p+1)*part));

@@ -15,13 +15,15 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 # (name, exact text in oracle.c, replacement)
 MUTANTS = [
-    ("gqa_head_mapping", "h / G, key_cache, value_cache, Hk, D, S, NB, scale,\n                          dtype) != 0;\n    }\n    return bad;\n}\n\n/* ---- decode written",
-     "h % Hk, key_cache, value_cache, Hk, D, S, NB, scale,\n                          dtype) != 0;\n    }\n    return bad;\n}\n\n/* ---- decode written"),
+    ("gqa_head_mapping", "h / G, key_cache, value_cache, Hk, D, S, NB, scale,\n                          dtype) != 0;\n    }\n    return bad;\n}\n\n/* ---- FP8 (E4M3) KV cache",
+     "h % Hk, key_cache, value_cache, Hk, D, S, NB, scale,\n                          dtype) != 0;\n    }\n    return bad;\n}\n\n/* ---- FP8 (E4M3) KV cache"),
     ("scale_dropped", "s[t] = scale * dot;", "s[t] = dot;"),
     ("softmax_sign", "double w = exp(s[t] - m);", "double w = exp(m - s[t]);"),
     ("causal_off_by_one", "P + j + 1, bt_row", "P + j, bt_row"),
-    ("slot_offset_swapped", "int64_t blk = slot / S, off = slot % S;",
-     "int64_t blk = slot % S, off = slot / S;"),
+    ("slot_offset_swapped", "int64_t blk = slot / S, off = slot % S;\n        for (int h = 0; h < Hk; ++h) {\n            for (int d",
+     "int64_t blk = slot % S, off = slot / S;\n        for (int h = 0; h < Hk; ++h) {\n            for (int d"),
+    ("fp8_slot_offset_swapped", "int64_t blk = slot / S, off = slot % S;\n        for (int h = 0; h < Hk; ++h) {\n            float kinv",
+     "int64_t blk = slot % S, off = slot / S;\n        for (int h = 0; h < Hk; ++h) {\n            float kinv"),
     ("page_offset_wrong", "const uint16_t* k = kc + cache_index(blk, kvh, t % S, Hk, S, D);",
      "const uint16_t* k = kc + cache_index(blk, kvh, t / S, Hk, S, D);"),
     ("value_from_key_pool", "const uint16_t* v = vc + cache_index(",
@@ -37,6 +39,13 @@ MUTANTS = [
      "uint16_t* st = staging + (((int64_t)kv * L + l) * nblk + i) * slab;"),
     ("unpack_direction", "if (unpack) pool[(int64_t)b * slab + e] = st[e];",
      "if (!unpack) pool[(int64_t)b * slab + e] = st[e];"),
+    ("e4m3_exponent_bias", "ldexp((double)(8 + f), e - 10)", "ldexp((double)(8 + f), e - 9)"),
+    ("e4m3_ties_to_odd", "if (d < best_d || (d == best_d && (c & 1) == 0)) {",
+     "if (d < best_d || (d == best_d && (c & 1) == 1)) {"),
+    ("fp8_store_scale_not_inverted", "float kinv = 1.0f / k_scale[h], vinv = 1.0f / v_scale[h];",
+     "float kinv = k_scale[h], vinv = v_scale[h];"),
+    ("fp8_decode_v_scale_from_k", "(orc_e4m3_to_double(v[d]) * v_scale[kvh])",
+     "(orc_e4m3_to_double(v[d]) * k_scale[kvh])"),
 ]
 
 PIN_CHECKS = [
@@ -45,6 +54,10 @@ PIN_CHECKS = [
     pins.test_store_then_gather_returns_the_token,
     pins.test_copy_blocks_brute_force,
     pins.test_kv_pack_closed_form,
+    pins.test_e4m3_codes_decode_like_torch,
+    pins.test_e4m3_encode_round_trip_ties_and_saturation,
+    pins.test_fp8_store_matches_torch_quantisation,
+    pins.test_fp8_decode_reduces_to_bf16_decode,
     pins.test_kv_pack_unpack_moves_blocks_between_pools,
     pins.test_decode_matches_brute_force_tiny,
     pins.test_decode_matches_brute_force_bf16_gqa_variants,

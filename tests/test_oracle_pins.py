@@ -461,3 +461,102 @@ def test_prefill_scale_enters_once():
         np.testing.assert_allclose(out[int(m.cu_q_lens[i]) + j, 5], V[: P + j + 1, 1].mean(0),
                                    rtol=1e-12, atol=1e-13)
     assert math.isclose(m.scale, 1 / 8)
+
+
+# ---- FP8 (E4M3) KV cache -----------------------------------------------------
+
+def test_e4m3_codes_decode_like_torch():
+    """All 256 codes against torch's float8_e4m3fn (a library decoder), plus
+    the format's fixed points: +-0, NaN at S.1111.111, largest 448, smallest
+    subnormal 2^-9."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_to_double(c) for c in range(256)])
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert np.array_equal(got[~both_nan], ref[~both_nan]) and np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.isnan(got[0x7F]) and np.isnan(got[0xFF]) and np.isnan(got).sum() == 2
+    assert got[0x7E] == 448.0 and got[0xFE] == -448.0 and got[1] == 2.0 ** -9
+    assert got[0] == 0.0 and math.copysign(1, got[0x80]) == -1
+
+
+def test_e4m3_encode_round_trip_ties_and_saturation():
+    finite = [c for c in range(256) if c not in (0x7F, 0xFF)]
+    for c in finite:                                    # every value maps to its own code
+        assert oracle.e4m3_encode(oracle.e4m3_to_double(c)) == c, c
+    for c in range(0x7E):                               # midpoints go to the even code
+        lo, hi = oracle.e4m3_to_double(c), oracle.e4m3_to_double(c + 1)
+        mid = np.float32((lo + hi) / 2)
+        if float(mid) != (lo + hi) / 2:
+            continue                                    # midpoint not a float32: no tie
+        assert oracle.e4m3_encode(mid) == (c if c % 2 == 0 else c + 1), (c, lo, hi)
+    assert oracle.e4m3_encode(1e6) == 0x7E and oracle.e4m3_encode(-1e6) == 0xFE
+    assert oracle.e4m3_encode(float("inf")) == 0x7E and oracle.e4m3_encode(float("nan")) == 0x7F
+    # within range, rounding agrees with torch's float32 -> float8_e4m3fn cast
+    g = torch.Generator().manual_seed(11)
+    y = (torch.randn(4000, generator=g) * torch.exp2(torch.randint(-12, 9, (4000,), generator=g).float()))
+    y = y.clamp(-448, 448)
+    ref = y.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(v)) for v in y.numpy()], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def test_fp8_store_matches_torch_quantisation():
+    """Stored code = the float32 product x * (1 / scale[h]) cast to E4M3 (torch
+    as the reference cast), at the slot the paging rule names."""
+    g = torch.Generator().manual_seed(12)
+    T, Hk, D, S, NB = 10, 3, 16, 8, 6
+    key = torch.randn(T, Hk, D, generator=g).to(torch.bfloat16)
+    value = (3 * torch.randn(T, Hk, D, generator=g)).to(torch.bfloat16)
+    ks = torch.tensor([0.01, 0.5, 2.0], dtype=torch.float32)
+    vs = torch.tensor([0.03, 0.125, 1.0], dtype=torch.float32)
+    slots = torch.randperm(NB * S, generator=g)[:T].to(torch.int64)
+    slots[4] = -1
+    kc = np.zeros((NB, Hk, S, D), dtype=np.uint8)
+    vc = np.zeros_like(kc)
+    assert oracle.reshape_and_cache_fp8(key, value, oracle.BF16, kc, vc, slots, ks, vs, S) == 0
+    for n in range(T):
+        s = int(slots[n])
+        if s < 0:
+            continue
+        for h in range(Hk):
+            for x, sc, pool in ((key, ks, kc), (value, vs, vc)):
+                y = x[n, h].float() * (torch.tensor(1.0) / sc[h])
+                ref = y.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+                assert np.array_equal(pool[s // S, h, s % S], ref)
+
+
+def test_fp8_decode_reduces_to_bf16_decode():
+    """With scales 1 every E4M3 value is exactly a bf16 value: FP8 decode must
+    equal the 16-bit decode oracle over the same values; a K scale of 2 equals
+    doubling q, a V scale of 2 doubles the output."""
+    c = pd_inputs.decode_case("fp8pin", 3, [1, 9, 40, 70], 8, 2, 16, 8, torch.bfloat16,
+                              poison=False, store_last=False)
+    g = torch.Generator().manual_seed(13)
+    NB, Hk, S, D = c.pool.key_cache.shape
+    kc8 = torch.randint(0, 256, (NB, Hk, S, D), generator=g, dtype=torch.int32).to(torch.uint8)
+    vc8 = torch.randint(0, 256, (NB, Hk, S, D), generator=g, dtype=torch.int32).to(torch.uint8)
+    for t in (kc8, vc8):
+        t[(t & 0x7F) == 0x7F] = 0x38                    # no NaN codes
+    kb = kc8.view(torch.float8_e4m3fn).to(torch.bfloat16)
+    vb = vc8.view(torch.float8_e4m3fn).to(torch.bfloat16)
+    assert torch.equal(kb.float(), kc8.view(torch.float8_e4m3fn).float())   # exact in bf16
+    one = np.ones(Hk, dtype=np.float32)
+    bt, cl = c.pool.block_tables, c.pool.context_lens
+    ref = oracle.decode(c.q, kb, vb, bt, cl, c.scale, oracle.BF16)
+    got = oracle.decode_fp8(c.q, oracle.BF16, kc8.numpy(), vc8.numpy(), one, one, bt, cl, c.scale)
+    assert np.allclose(got, ref, rtol=0, atol=1e-12)
+    got2 = oracle.decode_fp8(c.q, oracle.BF16, kc8.numpy(), vc8.numpy(), 2 * one, 2 * one, bt, cl,
+                             c.scale)
+    ref2 = oracle.decode((c.q.float() * 2).to(torch.bfloat16), kb, vb, bt, cl, c.scale, oracle.BF16)
+    assert np.allclose(got2, 2 * ref2, rtol=0, atol=1e-12)
+    got3 = oracle.decode_fp8(c.q, oracle.BF16, kc8.numpy(), vc8.numpy(), one, 4 * one, bt, cl,
+                             c.scale)
+    assert np.allclose(got3, 4 * ref, rtol=0, atol=1e-12)
+
+
+def test_fp8_concurrency_golden():
+    d = json.load(open(os.path.join(GOLDEN, "kv_bytes.json")))
+    for case in d["concurrency"]:
+        args = (case["weights_gb"], case["total_gb"], case["reserve_gb"])
+        assert oracle.concurrency_limit(case["kv_gb_fp16"], *args) == case["fp16"]
+        assert oracle.concurrency_limit(case["kv_gb_fp16"] / 2, *args) == case["fp8"]
