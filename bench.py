@@ -50,8 +50,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
-    ap.add_argument("--extras", default="chunked_prefill_mix,long_context_32_layers,cow_fork_stress,spec_verify,"
-                    "kv_handover",
+    ap.add_argument("--extras", default="chunked_prefill_mix,long_context_32_layers,cow_fork_stress,fp8_decode,"
+                    "spec_verify,kv_handover",
                     help="comma-separated extra workloads to run after the headline")
     ap.add_argument("--extra-steps", type=int, default=10)
     return ap.parse_args()
@@ -282,6 +282,8 @@ def run_ours(args, rank, world, local_rank):
                                                                    flush, hbm_peak)
         if "cow_fork_stress" in wanted:
             extras["cow_fork_stress"] = bench_cow(pd, pd_inputs, dev, args, flush, hbm_peak)
+        if "fp8_decode" in wanted:
+            extras["fp8_decode"] = bench_fp8_decode(pd, pd_inputs, dev, args, flush, hbm_peak)
         if "spec_verify" in wanted:
             extras["spec_verify"] = bench_spec_verify(pd, pd_inputs, dev, args, flush, hbm_peak,
                                                       bf16_peak)
@@ -446,6 +448,34 @@ def bench_long_context(pd, pd_inputs, dev, args, flush, hbm_peak):
                              "partitions": -(-ctx // pd.pd_decode_partition_tokens(ctx))}
         del layers, outs
         torch.cuda.empty_cache()
+    return res
+
+
+def bench_fp8_decode(pd, pd_inputs, dev, args, flush, hbm_peak):
+    """The headline Qwen3-8B batch with E4M3 pools (one byte per K/V value, per-head
+    scales): algorithmic bytes = FP8 K/V + q + out + block tables."""
+    import torch
+    c = pd_inputs.qwen3_8b_decode(seed=0)
+    kc8, vc8, ks, vs = pd_inputs.fp8_pools(c.pool.key_cache, c.pool.value_cache)
+    kc8, vc8, ks, vs = kc8.to(dev), vc8.to(dev), ks.to(dev), vs.to(dev)
+    q = c.q.to(dev)
+    out = torch.empty_like(q)
+    bt, cl = c.pool.block_tables.to(dev), c.pool.context_lens.to(dev)
+    mcl = c.max_context_len
+    ws = pd.decode_workspace(c.B, c.H, c.D, mcl, device=dev)
+    pd.pd_reshape_and_cache_fp8(c.new_key.to(dev), c.new_value.to(dev), kc8, vc8,
+                                c.slot_mapping.to(dev), ks, vs)
+    t = _time_calls(lambda: pd.pd_paged_attention_decode_fp8(out, q, kc8, vc8, ks, vs, bt, cl, mcl,
+                                                             c.scale, ws), args.extra_steps, flush)
+    ctx = c.pool.context_lens.tolist()
+    kv = sum(ctx) * c.Hk * c.D * 2                 # one byte per K and per V value
+    other = 2 * c.B * c.H * c.D * 2 + sum(4 * -(-x // c.pool.S) for x in ctx)
+    res = {"workload": "qwen3_8b_decode_step, E4M3 K/V with per-head scales",
+           "ms": round(t * 1e3, 4), "gbs": round((kv + other) / t / 1e9, 1),
+           "frac": round((kv + other) / t / 1e9 / hbm_peak, 4),
+           "kv_tokens_per_s": round(sum(ctx) / t, 1)}
+    del kc8, vc8
+    torch.cuda.empty_cache()
     return res
 
 

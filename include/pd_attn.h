@@ -64,7 +64,7 @@ typedef enum pd_status {
     PD_ERR_NOT_FOUND = 6
 } pd_status;
 
-typedef enum pd_dtype { PD_F16 = 0, PD_BF16 = 1 } pd_dtype;
+typedef enum pd_dtype { PD_F16 = 0, PD_BF16 = 1, PD_FP8_E4M3 = 2 } pd_dtype;
 
 /* Bits OR-ed into the caller's device error word. */
 #define PD_DEVERR_SLOT_RANGE 0x1  /* slot >= NB * S in a store               */
@@ -172,6 +172,49 @@ PD_API pd_status pd_paged_attention_decode_noalloc(void* out, const void* q,
                                            cudaStream_t stream);
 
 /* ---------------------------------------------------------------------- */
+/* FP8 (E4M3) KV cache (essay page "LLM推理PD分离架构深度工程实践", section
+ * 6.2; tutorial page "LLM 推理服务引擎深度拆解", section 8.1): pools hold one
+ * E4M3 byte per value (1 sign, 4 exponent bits with bias 7, 3 fraction bits;
+ * largest 448), half the bytes of BF16.  Each kv head h has a K scale
+ * k_scale[h] and a V scale v_scale[h] (DEVICE float32 [Hk], > 0 and finite):
+ * a stored code c stands for e4m3(c) * scale.
+ *
+ * pd_reshape_and_cache_fp8: as pd_reshape_and_cache, with key/value of type
+ * in_dt (fp16 or bf16) and pools of E4M3 bytes [NB][Hk][S][D]: the code
+ * stored is y = float(x) * (1.0f / scale[h]) (float32 product) rounded to the
+ * nearest E4M3 value, ties to even, magnitudes beyond 448 saturating to 448.
+ * A NaN input stores a NaN code. */
+PD_API pd_status pd_reshape_and_cache_fp8(const void* key, const void* value,
+                                          void* key_cache, void* value_cache,
+                                          const int64_t* slot_mapping, int T,
+                                          int Hk, int D, int S, int NB,
+                                          int64_t key_stride_tok,
+                                          int64_t value_stride_tok,
+                                          const float* k_scale,
+                                          const float* v_scale, pd_dtype in_dt,
+                                          int32_t* dev_err, cudaStream_t stream);
+/* pd_paged_attention_decode_fp8: decode attention over E4M3 pools:
+ *   out[i][h] = sum_t softmax_t(scale * q . (k_t * k_scale[g])) v_t * v_scale[g]
+ * with g = h / (H / Hk); q and out are of type dt (fp16 or bf16), every other
+ * argument as for pd_paged_attention_decode (same workspace size).  The
+ * tensor-core products run on fp16 operands: K and V are widened exactly, q
+ * is rounded to fp16 (|q| must stay below 65504); the scales are applied in
+ * float32. */
+PD_API pd_status pd_paged_attention_decode_fp8(void* out, const void* q,
+                                               const void* key_cache,
+                                               const void* value_cache,
+                                               const float* k_scale,
+                                               const float* v_scale,
+                                               const int32_t* block_tables,
+                                               int max_blocks_per_seq,
+                                               const int32_t* context_lens,
+                                               int B, int H, int Hk, int D, int S,
+                                               int NB, int max_context_len,
+                                               float scale, void* workspace,
+                                               size_t workspace_bytes, pd_dtype dt,
+                                               int32_t* dev_err, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
 /* Copy-on-write block copies for fork (parallel sampling, beam search):
  * tutorial page section 2.3, BlockManager.cow(): a shared block that is about
  * to be written is duplicated into a fresh block first; nanoPD page "分页KV
@@ -183,6 +226,7 @@ PD_API pd_status pd_paged_attention_decode_noalloc(void* out, const void* q,
  *                  K and of V is copied.  Ids outside [0, NB) skip the pair
  *                  and flag PD_DEVERR_BLOCK_RANGE.  A dst that is also a src
  *                  of another pair, or two pairs with one dst, race.
+ * dt may also be PD_FP8_E4M3 (one-byte pools).
  * A bit copy.  npairs == 0 or L == 0 launches nothing. */
 PD_API pd_status pd_copy_blocks(void* const* key_caches, void* const* value_caches,
                          int L, const int64_t* block_mapping, int npairs,
@@ -207,6 +251,7 @@ PD_API pd_status pd_copy_blocks(void* const* key_caches, void* const* value_cach
  *   block_ids     DEVICE int32 [nblk]; an id outside [0, NB) skips its slabs
  *                 (pack leaves them untouched, unpack does not read them) and
  *                 flags PD_DEVERR_BLOCK_RANGE.  For unpack, two equal ids race.
+ * dt may also be PD_FP8_E4M3 (one-byte pools and staging).
  * Bit copies.  nblk == 0 or L == 0 launches nothing. */
 PD_API pd_status pd_kv_pack(void* staging, void* const* key_caches,
                             void* const* value_caches, int L,

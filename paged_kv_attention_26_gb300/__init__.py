@@ -23,7 +23,7 @@ from . import build as _build
 LIB_PATH = _build.LIB
 
 PD_OK = 0
-PD_F16, PD_BF16 = 0, 1
+PD_F16, PD_BF16, PD_FP8_E4M3 = 0, 1, 2
 PD_DEVERR_SLOT_RANGE = 0x1
 PD_DEVERR_BLOCK_RANGE = 0x2
 PD_DEVERR_CTX_RANGE = 0x4
@@ -51,6 +51,10 @@ SIGNATURES = {
     "pd_paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
                                                _I, _I, _F, _I, _P, _P]),
     "pd_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "pd_reshape_and_cache_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I64, _I64,
+                                      _P, _P, _I, _P, _P]),
+    "pd_paged_attention_decode_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I,
+                                           _I, _I, _I, _F, _P, _SZ, _I, _P, _P]),
     "pd_kv_pack": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pd_kv_unpack": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pd_paged_prefill_chunk": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
@@ -137,7 +141,13 @@ def _dt(t) -> int:
         return PD_F16
     if t.dtype == torch.bfloat16:
         return PD_BF16
+    if t.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        return PD_FP8_E4M3
     raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _is_fp8(t) -> bool:
+    return _dt(t) == PD_FP8_E4M3
 
 
 def _dev(t, name, dtype=None, contiguous=True):
@@ -184,6 +194,68 @@ def pd_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, dev_e
         _dev(slot_mapping, "slot_mapping", torch.int64), T, Hk, D, S, NB,
         key.stride(0), value.stride(0), dt, _opt(dev_err), _stream(stream))
     _check("pd_reshape_and_cache", st)
+
+
+def pd_reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping, k_scale, v_scale,
+                             dev_err=None, stream=None):
+    """Quantise key/value [T, Hk, D] (fp16/bf16) to E4M3 and store them into the
+    one-byte pools [NB, Hk, S, D] at ``slot_mapping``; ``k_scale``/``v_scale``
+    are float32 CUDA [Hk] (a code c stands for e4m3(c) * scale)."""
+    torch = _torch()
+    T, Hk, D = key.shape
+    NB, Hk2, S, D2 = key_cache.shape
+    if (Hk2, D2) != (Hk, D) or value.shape != key.shape or value_cache.shape != key_cache.shape:
+        raise ValueError("shape mismatch")
+    if not (_is_fp8(key_cache) and _is_fp8(value_cache)):
+        raise TypeError("the pools must be one-byte (uint8 or float8_e4m3fn)")
+    for t, n in ((key, "key"), (value, "value")):
+        if t.stride(2) != 1 or t.stride(1) != D:
+            raise ValueError(f"{n} must have contiguous heads and dims")
+    if value.dtype != key.dtype:
+        raise TypeError("dtype mismatch")
+    for sc in (k_scale, v_scale):
+        if sc.shape != (Hk,):
+            raise ValueError("scales must be [Hk]")
+    st = load().pd_reshape_and_cache_fp8(
+        _dev(key, "key", contiguous=False), _dev(value, "value", contiguous=False),
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+        _dev(slot_mapping, "slot_mapping", torch.int64), T, Hk, D, S, NB,
+        key.stride(0), value.stride(0), _dev(k_scale, "k_scale", torch.float32),
+        _dev(v_scale, "v_scale", torch.float32), _dt(key), _opt(dev_err), _stream(stream))
+    _check("pd_reshape_and_cache_fp8", st)
+
+
+def pd_paged_attention_decode_fp8(out, q, key_cache, value_cache, k_scale, v_scale, block_tables,
+                                  context_lens, max_context_len: int, scale: float,
+                                  workspace=None, dev_err=None, stream=None):
+    """Decode over E4M3 pools [NB, Hk, S, D] (uint8 or float8_e4m3fn) with float32
+    scales [Hk]; out, q [B, H, D] fp16/bf16."""
+    torch = _torch()
+    B, H, D = q.shape
+    NB, Hk, S, D2 = key_cache.shape
+    if out.shape != q.shape or D2 != D or value_cache.shape != key_cache.shape:
+        raise ValueError("shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables / context_lens shape")
+    if not (_is_fp8(key_cache) and _is_fp8(value_cache)):
+        raise TypeError("the pools must be one-byte (uint8 or float8_e4m3fn)")
+    if out.dtype != q.dtype:
+        raise TypeError("dtype mismatch")
+    for sc in (k_scale, v_scale):
+        if sc.shape != (Hk,):
+            raise ValueError("scales must be [Hk]")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    st = load().pd_paged_attention_decode_fp8(
+        _dev(out, "out"), _dev(q, "q"), _dev(key_cache, "key_cache"),
+        _dev(value_cache, "value_cache"), _dev(k_scale, "k_scale", torch.float32),
+        _dev(v_scale, "v_scale", torch.float32),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), B, H, Hk, D, S, NB,
+        int(max_context_len), float(scale), ws_ptr, ws_bytes, _dt(q), _opt(dev_err),
+        _stream(stream))
+    _check("pd_paged_attention_decode_fp8", st)
 
 
 def pd_decode_workspace_bytes(B: int, H: int, D: int, max_context_len: int) -> int:

@@ -77,12 +77,13 @@ int pd_decode_partition_tokens(int max_context_len) {
     return decode_partition_tokens(max_context_len);
 }
 
-pd_status pd_paged_attention_decode(void* out, const void* q, const void* key_cache,
-                                    const void* value_cache, const int32_t* block_tables,
-                                    int max_blocks_per_seq, const int32_t* context_lens, int B,
-                                    int H, int Hk, int D, int S, int NB, int max_context_len,
-                                    float scale, void* workspace, size_t workspace_bytes,
-                                    pd_dtype dt, int32_t* dev_err, cudaStream_t stream) {
+static pd_status decode_common(void* out, const void* q, const void* key_cache,
+                               const void* value_cache, const float* k_scale,
+                               const float* v_scale, bool fp8, const int32_t* block_tables,
+                               int max_blocks_per_seq, const int32_t* context_lens, int B, int H,
+                               int Hk, int D, int S, int NB, int max_context_len, float scale,
+                               void* workspace, size_t workspace_bytes, pd_dtype dt,
+                               int32_t* dev_err, cudaStream_t stream) {
     if (B < 0 || H < 1 || Hk < 1 || NB < 1 || max_blocks_per_seq < 1 || max_context_len < 0)
         return PD_ERR_INVALID_ARG;
     if (H % Hk != 0) return PD_ERR_INVALID_ARG;
@@ -101,21 +102,71 @@ pd_status pd_paged_attention_decode(void* out, const void* q, const void* key_ca
             return PD_ERR_INVALID_ARG;
         if (workspace_bytes < need) return PD_ERR_WORKSPACE_TOO_SMALL;
     }
+    if (fp8 && (!k_scale || !v_scale)) return PD_ERR_INVALID_ARG;
     DecodeArgs a{out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
                  B, H, Hk, D, S, NB, max_context_len, scale, workspace, dt, dev_err, stream};
+    a.fp8 = fp8;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     return launch_decode(a);
+}
+
+pd_status pd_paged_attention_decode(void* out, const void* q, const void* key_cache,
+                                    const void* value_cache, const int32_t* block_tables,
+                                    int max_blocks_per_seq, const int32_t* context_lens, int B,
+                                    int H, int Hk, int D, int S, int NB, int max_context_len,
+                                    float scale, void* workspace, size_t workspace_bytes,
+                                    pd_dtype dt, int32_t* dev_err, cudaStream_t stream) {
+    return decode_common(out, q, key_cache, value_cache, nullptr, nullptr, false, block_tables,
+                         max_blocks_per_seq, context_lens, B, H, Hk, D, S, NB, max_context_len,
+                         scale, workspace, workspace_bytes, dt, dev_err, stream);
+}
+
+pd_status pd_paged_attention_decode_fp8(void* out, const void* q, const void* key_cache,
+                                        const void* value_cache, const float* k_scale,
+                                        const float* v_scale, const int32_t* block_tables,
+                                        int max_blocks_per_seq, const int32_t* context_lens,
+                                        int B, int H, int Hk, int D, int S, int NB,
+                                        int max_context_len, float scale, void* workspace,
+                                        size_t workspace_bytes, pd_dtype dt, int32_t* dev_err,
+                                        cudaStream_t stream) {
+    return decode_common(out, q, key_cache, value_cache, k_scale, v_scale, true, block_tables,
+                         max_blocks_per_seq, context_lens, B, H, Hk, D, S, NB, max_context_len,
+                         scale, workspace, workspace_bytes, dt, dev_err, stream);
+}
+
+pd_status pd_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,
+                                   void* value_cache, const int64_t* slot_mapping, int T, int Hk,
+                                   int D, int S, int NB, int64_t key_stride_tok,
+                                   int64_t value_stride_tok, const float* k_scale,
+                                   const float* v_scale, pd_dtype in_dt, int32_t* dev_err,
+                                   cudaStream_t stream) {
+    if (T < 0 || Hk < 1 || NB < 1) return PD_ERR_INVALID_ARG;
+    if (!supported_D(D) || !supported_S(S) || !supported_dt(in_dt)) return PD_ERR_UNSUPPORTED;
+    if (!key_cache || !value_cache || !aligned16(key_cache) || !aligned16(value_cache))
+        return PD_ERR_INVALID_ARG;
+    if (T == 0) return PD_OK;
+    if (!key || !value || !slot_mapping || !k_scale || !v_scale || !aligned16(key) ||
+        !aligned16(value))
+        return PD_ERR_INVALID_ARG;
+    if (key_stride_tok < int64_t(Hk) * D || value_stride_tok < int64_t(Hk) * D ||
+        key_stride_tok % 8 || value_stride_tok % 8)
+        return PD_ERR_INVALID_ARG;
+    return launch_reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping, T, Hk,
+                                        D, S, NB, key_stride_tok, value_stride_tok, k_scale,
+                                        v_scale, in_dt, dev_err, stream);
 }
 
 pd_status pd_copy_blocks(void* const* key_caches, void* const* value_caches, int L,
                          const int64_t* block_mapping, int npairs, int Hk, int D, int S, int NB,
                          pd_dtype dt, int32_t* dev_err, cudaStream_t stream) {
     if (L < 0 || npairs < 0 || Hk < 1 || NB < 1) return PD_ERR_INVALID_ARG;
-    if (!supported_D(D) || !supported_S(S) || !supported_dt(dt)) return PD_ERR_UNSUPPORTED;
+    if (!supported_D(D) || !supported_S(S) || !supported_pool_dt(dt)) return PD_ERR_UNSUPPORTED;
     if (L == 0 || npairs == 0) return PD_OK;
     if (!key_caches || !value_caches || !block_mapping) return PD_ERR_INVALID_ARG;
     if (L > 65535) return PD_ERR_UNSUPPORTED;
     return launch_copy_blocks(key_caches, value_caches, L, block_mapping, npairs, Hk, D, S, NB,
-                              dev_err, stream);
+                              elem_bytes(dt), dev_err, stream);
 }
 
 static pd_status kv_pack_common(bool unpack, void* staging, void* const* key_caches,
@@ -123,13 +174,13 @@ static pd_status kv_pack_common(bool unpack, void* staging, void* const* key_cac
                                 int nblk, int Hk, int D, int S, int NB, pd_dtype dt,
                                 int32_t* dev_err, cudaStream_t stream) {
     if (L < 0 || nblk < 0 || Hk < 1 || NB < 1) return PD_ERR_INVALID_ARG;
-    if (!supported_D(D) || !supported_S(S) || !supported_dt(dt)) return PD_ERR_UNSUPPORTED;
+    if (!supported_D(D) || !supported_S(S) || !supported_pool_dt(dt)) return PD_ERR_UNSUPPORTED;
     if (L == 0 || nblk == 0) return PD_OK;
     if (!staging || !key_caches || !value_caches || !block_ids || !aligned16(staging))
         return PD_ERR_INVALID_ARG;
     if (L > 65535) return PD_ERR_UNSUPPORTED;
     return launch_kv_pack(unpack, staging, key_caches, value_caches, L, block_ids, nblk, Hk, D,
-                          S, NB, dev_err, stream);
+                          S, NB, elem_bytes(dt), dev_err, stream);
 }
 
 pd_status pd_kv_pack(void* staging, void* const* key_caches, void* const* value_caches, int L,

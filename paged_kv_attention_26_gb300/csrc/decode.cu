@@ -48,6 +48,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 #include <chrono>
 #include <cmath>
 
@@ -63,23 +64,33 @@ namespace {
 constexpr int kMinStagesPerCta = 4; // a CTA's range never ends before 4 stages
 constexpr int kSegTokens = kMinStagesPerCta * 64;   // bounds pieces per stream
 constexpr int kStageTokens = 64;    // tokens per pipeline stage
-constexpr int kStages = 3;          // ring depth
 constexpr int kConsumerWarps = 4;   // 16 tokens of each stage per warp
+constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
 constexpr int kHeadsN = 8;          // MMA N: query heads per CTA, padded
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows > 2^8
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
+// 16-bit pools: TMA fills a 3-stage ring of 16-bit tiles that the consumers
+// read.  FP8 pools: TMA fills a 4-stage ring of raw E4M3 tiles (half the
+// bytes); each consumer warp widens its own 16 rows of a stage (exactly) to
+// fp16 into one 16-bit tile of the same layout, releases the raw stage at
+// once, and runs the 16-bit code on fp16 operands.
+template <int D, bool kF8 = false>
 struct DecodeSmem {
+    static constexpr int kRing = kF8 ? 4 : 3;          // stages TMA fills
+    static constexpr int kTiles16 = kF8 ? 1 : kRing;   // 16-bit tiles the consumers read
     static constexpr int kAtom = kStageTokens * 128;   // [64 tokens][64 values], 8 KB
     static constexpr int kTile = (D / 64) * kAtom;     // one stage of K (or of V)
+    static constexpr int kTile8 = kStageTokens * D;    // one FP8 stage of K (or of V)
     static constexpr int kFrag = (D / 16) * 4 + 4;     // per-lane merge record: o, m[2], l[2]
     static constexpr int kK = 0;
-    static constexpr int kV = kK + kStages * kTile;
-    static constexpr int kX = kV + kStages * kTile;    // merge exchange float [2][kFrag][32]
+    static constexpr int kV = kK + kTiles16 * kTile;
+    static constexpr int kK8 = kV + kTiles16 * kTile;
+    static constexpr int kV8 = kK8 + (kF8 ? kRing * kTile8 : 0);
+    static constexpr int kX = kV8 + (kF8 ? kRing * kTile8 : 0);    // merge exchange [2][kFrag][32]
     static constexpr int kBar = kX + 2 * kFrag * 32 * 4;
-    static constexpr int kMisc = kBar + 2 * kStages * 8;   // abort flag, issued count
+    static constexpr int kMisc = kBar + 2 * kRing * 8;     // abort flag, issued count
     static constexpr int kBytes = kMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;           // base aligned to 1 KB in-kernel
 };
@@ -280,7 +291,36 @@ __device__ __forceinline__ void zero_empty_rows(T* __restrict__ out,
     }
 }
 
-template <typename T, int D>
+// Two E4M3 codes (low byte = lower index) -> two fp16 values, exactly (every
+// E4M3 value is an fp16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+
+// Two E4M3 codes -> two fp16 values times 2^-8, exactly, with integer
+// operations only (no conversion unit): an E4M3 code s.eeee.mmm placed as
+// fp16 bits s.0eeee.mmm0000000 reads as its value times 2^-8 (the exponent
+// biases differ by 8; subnormal codes land on fp16 subnormals).  sel picks
+// the two bytes of w (0x1404: bytes 0, 1; 0x3424: bytes 2, 3).
+template <uint32_t kSel>
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t w) {
+    uint32_t t;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(t) : "r"(w), "n"(kSel));
+    return (t & 0x80008000u) | ((t >> 1) & 0x3F803F80u);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                 ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// T: type of q and out.  kF8: the pools hold E4M3 codes with a K and a V scale
+// per kv head; the tensor-core products then run on fp16 (K and V widened
+// exactly, q rounded to fp16), and the scales are applied in fp32.
+template <typename T, int D, bool kF8>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, T* __restrict__ out,
@@ -290,9 +330,12 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                           int max_segs, int cap, float* __restrict__ ws_o,
                           float* __restrict__ ws_m, float* __restrict__ ws_l,
                           unsigned long long* __restrict__ ws_cnt, unsigned long long tag,
+                          const float* __restrict__ k_scale, const float* __restrict__ v_scale,
                           int32_t* dev_err) {
-    using L = DecodeSmem<D>;
-    using E = Elem<T>;
+    using L = DecodeSmem<D, kF8>;
+    using TM = typename std::conditional<kF8, __half, T>::type;   // tensor-core operand type
+    using E = Elem<TM>;
+    constexpr int kStages = L::kRing;
     constexpr int kAtoms = D / 64;
     constexpr int KS = D / 16;      // k-steps of q.k, m-tiles of p.v
     extern __shared__ unsigned char smem_raw[];
@@ -328,14 +371,30 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         return;
     }
 
-    if (warp == kConsumerWarps) {
+    if (warp == kProducerWarp) {
         // ---------------- producer warp: streams stages across stream pieces ----------------
-        const uint32_t block_bytes = uint32_t(S) * D * 2;        // one [S][D] slab
+        constexpr int kRingP = kStages;
+        uint64_t* p_full = full;
+        uint64_t* p_empty = empty;
+        const uint32_t block_bytes = uint32_t(S) * D * (kF8 ? 1 : 2);   // one [S][D] slab
+        // Block ids of one stage: lane i < (blocks in the stage) loads the id of
+        // block i (unchecked), other lanes -2.  The ids of stage gs + 1 are
+        // loaded while stage gs is issued, so the table's latency overlaps the
+        // copies instead of sitting in front of every stage.
+        auto stage_blk = [&](const Walk& x) -> int {
+            const int t0 = x.off * kStageTokens;
+            const int nt = min(kStageTokens, x.ctx - t0);
+            const int nblk = (nt + S - 1) / S;             // <= 64 / S <= 8
+            const int32_t* bt_row = block_tables + (int64_t)x.s * max_blocks_per_seq;
+            return lane < nblk ? __ldg(bt_row + t0 / S + lane) : -2;
+        };
+        Walk wn = w;                                       // one stage ahead of w
+        int blk_cur = stage_blk(w);
         for (uint32_t gs = 0; w.pos < w.end; ++gs) {
-            const int slot = gs % kStages;
+            const int slot = gs % kRingP;
             // every lane waits (acquire), then the warp agrees on the outcome
-            const bool ok = __all_sync(0xffffffffu, gs < kStages ||
-                                       mbar_wait(&empty[slot], ((gs / kStages) - 1) & 1));
+            const bool ok = __all_sync(0xffffffffu, gs < uint32_t(kRingP) ||
+                                       mbar_wait(&p_empty[slot], ((gs / kRingP) - 1) & 1));
             if (!ok || __any_sync(0xffffffffu, *abort_flag != 0)) {
                 if (lane == 0 && !ok) {
                     flag_error(dev_err, PD_DEVERR_TIMEOUT);
@@ -343,35 +402,41 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
                 break;
             }
+            // start loading the next stage's block ids
+            ++wn.off;
+            ++wn.pos;
+            if (wn.off == wn.L && wn.pos < wn.end) walk_next_stream(wn, context_lens, B, units, cap);
+            const int blk_next = wn.pos < wn.end ? stage_blk(wn) : -2;
             const int kvh = w.u / groups;
-            const int32_t* bt_row = block_tables + (int64_t)w.s * max_blocks_per_seq;
-            const int t0 = w.off * kStageTokens;
-            const int nt = min(kStageTokens, w.ctx - t0);
-            const int nblk = (nt + S - 1) / S;             // <= 64 / S <= 8
             int row = -1;
-            if (lane < nblk) {
-                const int blk = __ldg(bt_row + t0 / S + lane);
-                if (blk >= 0 && blk < NB) {
-                    row = (blk * Hk + kvh) * S;
+            if (blk_cur != -2) {
+                if (blk_cur >= 0 && blk_cur < NB) {
+                    row = (blk_cur * Hk + kvh) * S;
                 } else {
                     flag_error(dev_err, PD_DEVERR_BLOCK_RANGE);
                 }
             }
             const uint32_t ok_mask = __ballot_sync(0xffffffffu, row >= 0);
-            if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2u * block_bytes * __popc(ok_mask));
+            if (lane == 0) mbar_arrive_expect_tx(&p_full[slot], 2u * block_bytes * __popc(ok_mask));
             __syncwarp();
             if (row >= 0) {
+                if constexpr (kF8) {
+                    // one [S tokens][D bytes] box per block, rows packed
+                    const int off = slot * L::kTile8 + lane * S * D;
+                    tc::tma_load_2d(smem + L::kK8 + off, &tm_k, 0, row, &p_full[slot]);
+                    tc::tma_load_2d(smem + L::kV8 + off, &tm_v, 0, row, &p_full[slot]);
+                } else {
 #pragma unroll
-                for (int a = 0; a < kAtoms; ++a) {
-                    const int off = slot * L::kTile + a * L::kAtom + lane * S * 128;
-                    tc::tma_load_2d(smem + L::kK + off, &tm_k, a * 64, row, &full[slot]);
-                    tc::tma_load_2d(smem + L::kV + off, &tm_v, a * 64, row, &full[slot]);
+                    for (int a = 0; a < kAtoms; ++a) {
+                        const int off = slot * L::kTile + a * L::kAtom + lane * S * 128;
+                        tc::tma_load_2d(smem + L::kK + off, &tm_k, a * 64, row, &p_full[slot]);
+                        tc::tma_load_2d(smem + L::kV + off, &tm_v, a * 64, row, &p_full[slot]);
+                    }
                 }
             }
             if (lane == 0) *issued = int(gs + 1);
-            ++w.off;
-            ++w.pos;
-            if (w.off == w.L && w.pos < w.end) walk_next_stream(w, context_lens, B, units, cap);
+            w = wn;
+            blk_cur = blk_next;
         }
         // all loads are issued: the producer has time for the empty rows
         zero_empty_rows<T, D>(out, context_lens, B, H, cap, dev_err, lane);
@@ -408,8 +473,19 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 qb[ks][0] = n < GH ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks)) : 0u;
                 qb[ks][1] =
                     n < GH ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8)) : 0u;
+                if constexpr (kF8 && !std::is_same<T, __half>::value) {
+                    // q rounded to the fp16 operand type of the FP8 path
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const float2 f = Elem<T>::unpack2(qb[ks][r]);
+                        qb[ks][r] = Elem<__half>::pack2(f.x, f.y);
+                    }
+                }
             }
         }
+        // FP8 pools: the K scale joins the softmax scale, the V scale the output
+        // (K is widened to fp16 scaled by 2^-8: the 2^8 comes back here)
+        const float sl2 = kF8 ? scale_log2 * 256.f * __ldg(k_scale + kvh) : scale_log2;
         // O^T fragments: m-tile mt covers dims 16mt..16mt+15; lane holds dims
         // 16mt + lane/4 (regs 0,1) and + 8 (regs 2,3), heads 2(lane%4) and + 1.
         float o[KS][4];
@@ -429,14 +505,59 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 break;                   // skip the piece's other stages
             }
             const int nt = min(kStageTokens, w.ctx - (w.off + st) * kStageTokens);
+            // FP8 pools: this warp widens its own 16 rows of K and V to fp16 in
+            // the one 16-bit tile (no other warp reads them), then frees the raw
+            // stage for the next copy right away.
+            const int tslot = kF8 ? 0 : slot;
+            if constexpr (kF8) {
+                if (tb < nt) {
+                    // K through integer operations (times 2^-8), V through the
+                    // conversion unit (exact): the two halves run on different pipes.
+                    constexpr int kChunks = D / 16;          // 16-byte chunks per FP8 row
+                    const unsigned char* srck = smem + L::kK8 + slot * L::kTile8 + tb * D;
+                    const unsigned char* srcv = smem + L::kV8 + slot * L::kTile8 + tb * D;
+                    // (16 rows x kChunks) chunks, 32 per pass: a fixed trip count, so
+                    // every load of the stage is issued up front
+                    uint4 rk[16 * kChunks / 32], rv[16 * kChunks / 32];
+#pragma unroll
+                    for (int it = 0; it < 16 * kChunks / 32; ++it) {
+                        const int i = it * 32 + lane;
+                        rk[it] = *reinterpret_cast<const uint4*>(srck + i * 16);
+                        rv[it] = *reinterpret_cast<const uint4*>(srcv + i * 16);
+                    }
+#pragma unroll
+                    for (int it = 0; it < 16 * kChunks / 32; ++it) {
+                        const int i = it * 32 + lane;
+                        const int row = i / kChunks, c8 = i % kChunks;
+                        const uint32_t wk[4] = {rk[it].x, rk[it].y, rk[it].z, rk[it].w};
+                        const uint32_t wv[4] = {rv[it].x, rv[it].y, rv[it].z, rv[it].w};
+                        uint32_t hk[8], hv[8];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            hk[2 * j] = e4m3x2_to_f16x2_scaled<0x1404u>(wk[j]);
+                            hk[2 * j + 1] = e4m3x2_to_f16x2_scaled<0x3424u>(wk[j]);
+                            hv[2 * j] = e4m3x2_to_f16x2(uint16_t(wv[j] & 0xffffu));
+                            hv[2 * j + 1] = e4m3x2_to_f16x2(uint16_t(wv[j] >> 16));
+                        }
+                        st_shared_v4(swz<D>(k_base0, tb + row, 2 * c8), hk[0], hk[1], hk[2], hk[3]);
+                        st_shared_v4(swz<D>(k_base0, tb + row, 2 * c8 + 1), hk[4], hk[5], hk[6],
+                                     hk[7]);
+                        st_shared_v4(swz<D>(v_base0, tb + row, 2 * c8), hv[0], hv[1], hv[2], hv[3]);
+                        st_shared_v4(swz<D>(v_base0, tb + row, 2 * c8 + 1), hv[4], hv[5], hv[6],
+                                     hv[7]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+            }
             if (tb < nt) {
-                const uint32_t kb = k_base0 + slot * L::kTile;
-                const uint32_t vb = v_base0 + slot * L::kTile;
+                const uint32_t kb = k_base0 + tslot * L::kTile;
+                const uint32_t vb = v_base0 + tslot * L::kTile;
                 const bool partial = tb + 16 > nt;
                 if (partial) {
                     // V rows past the context end hold other data or were never
                     // loaded this round: zero them so that 0 * v stays 0.
-                    unsigned char* vrow = smem + L::kV + slot * L::kTile;
+                    unsigned char* vrow = smem + L::kV + tslot * L::kTile;
                     for (int i = lane; i < 16 * kAtoms * 8; i += 32) {
                         const int tok = tb + i / (kAtoms * 8);
                         if (tok >= nt) {
@@ -453,7 +574,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 for (int ks = 0; ks < KS; ++ks) {
                     uint32_t a[4];
                     wmma16::ldsm_x4(a, swz<D>(kb, tb + r8 + 8 * (j8 & 1), 2 * ks + (j8 >> 1)));
-                    wmma16::Mma<T>::run(acc[ks & 1], a, qb[ks][0], qb[ks][1]);
+                    wmma16::Mma<TM>::run(acc[ks & 1], a, qb[ks][0], qb[ks][1]);
                 }
                 // lane holds tokens tb + lane/4 (0,1) and + 8 (2,3); heads 2(lane%4) + {0,1}
                 const int tok0 = tb + (lane >> 2);
@@ -461,7 +582,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int tok = tok0 + (i >> 1) * 8;
-                    x[i] = tok < nt ? (acc[0][i] + acc[1][i]) * scale_log2 : -INFINITY;
+                    x[i] = tok < nt ? (acc[0][i] + acc[1][i]) * sl2 : -INFINITY;
                 }
                 // ---- online softmax per head (lane-local state, 3 shuffles per head)
                 float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
@@ -499,13 +620,13 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 for (int mt = 0; mt < KS; ++mt) {
                     uint32_t a[4];
                     wmma16::ldsm_x4_t(a, swz<D>(vb, tb + r8 + 8 * (j8 >> 1), 2 * mt + (j8 & 1)));
-                    wmma16::Mma<T>::run(o[mt], a, bh0, bh1);
-                    wmma16::Mma<T>::run(o[mt], a, bl0, bl1);
+                    wmma16::Mma<TM>::run(o[mt], a, bh0, bh1);
+                    wmma16::Mma<TM>::run(o[mt], a, bl0, bl1);
                 }
-                if (partial) tc::fence_proxy_async_smem();   // zeros before the next TMA write
+                if (partial && !kF8) tc::fence_proxy_async_smem();   // zeros before the next TMA write
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (!kF8 && lane == 0) mbar_arrive(&empty[slot]);
         }
         // All four consumer warps decide together whether to go on: a warp
         // that gave up still arrives here, so named-barrier counts stay matched.
@@ -561,6 +682,13 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
         if (warp == 0) {
             take(1);
+            if constexpr (kF8) {
+                const float vs = __ldg(v_scale + kvh);
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[mt][e] *= vs;
+            }
             // lane: heads ha, ha + 1; dims 16mt + lane/4 and + 8
             const int ha = 2 * (lane & 3), d0 = lane >> 2;
 #pragma unroll
@@ -672,9 +800,9 @@ int sm_count(int dev) {
     return counts[dev];
 }
 
-template <typename T, int D>
+template <typename T, int D, bool kF8>
 pd_status launch_decode_t(const DecodeArgs& a) {
-    using Lt = DecodeSmem<D>;
+    using Lt = DecodeSmem<D, kF8>;
     const int G = a.H / a.Hk;
     int GH = 1;                          // largest divisor of G that fits N = 8
     for (int g = std::min(G, kHeadsN); g >= 1; --g)
@@ -682,10 +810,12 @@ pd_status launch_decode_t(const DecodeArgs& a) {
     CUtensorMap tm_k, tm_v;
     const unsigned long long rows = (unsigned long long)a.NB * a.Hk * a.S;
     if (rows > 0x7fffffffull) return PD_ERR_UNSUPPORTED;   // TMA row coordinate is int32
-    if (!encode_pool_map(&tm_k, a.key_cache, D, rows, a.S, a.dt) ||
-        !encode_pool_map(&tm_v, a.value_cache, D, rows, a.S, a.dt))
-        return launch_result(cudaErrorInvalidValue);
-    auto kern = paged_decode_split_kernel<T, D>;
+    const bool maps_ok = kF8 ? (encode_pool_map_u8(&tm_k, a.key_cache, D, rows, a.S) &&
+                                encode_pool_map_u8(&tm_v, a.value_cache, D, rows, a.S))
+                             : (encode_pool_map(&tm_k, a.key_cache, D, rows, a.S, a.dt) &&
+                                encode_pool_map(&tm_v, a.value_cache, D, rows, a.S, a.dt));
+    if (!maps_ok) return launch_result(cudaErrorInvalidValue);
+    auto kern = paged_decode_split_kernel<T, D, kF8>;
     static uint64_t attr_set = 0;   // one bit per device; benign if raced
     int dev = 0;
     cudaError_t e0 = cudaGetDevice(&dev);
@@ -711,8 +841,16 @@ pd_status launch_decode_t(const DecodeArgs& a) {
     kern<<<grid, kDecodeThreads, Lt::kAlloc, a.stream>>>(
         tm_k, tm_v, static_cast<T*>(a.out), static_cast<const T*>(a.q), a.block_tables,
         a.max_blocks_per_seq, a.context_lens, a.B, a.H, a.Hk, a.S, a.NB, GH, scale_log2, P, cap,
-        ws_o, ws_m, ws_l, ws_cnt, next_launch_tag(), a.dev_err);
+        ws_o, ws_m, ws_l, ws_cnt, next_launch_tag(), a.k_scale, a.v_scale, a.dev_err);
     return launch_result(cudaGetLastError());
+}
+
+template <bool kF8>
+pd_status launch_decode_dt(const DecodeArgs& a) {
+    if (a.dt == PD_BF16)
+        return a.D == 128 ? launch_decode_t<__nv_bfloat16, 128, kF8>(a)
+                          : launch_decode_t<__nv_bfloat16, 64, kF8>(a);
+    return a.D == 128 ? launch_decode_t<__half, 128, kF8>(a) : launch_decode_t<__half, 64, kF8>(a);
 }
 
 }  // namespace
@@ -735,11 +873,7 @@ size_t decode_workspace_bytes(int B, int H, int D, int max_context_len) {
 }
 
 pd_status launch_decode(const DecodeArgs& a) {
-    if (a.dt == PD_BF16) {
-        return a.D == 128 ? launch_decode_t<__nv_bfloat16, 128>(a)
-                          : launch_decode_t<__nv_bfloat16, 64>(a);
-    }
-    return a.D == 128 ? launch_decode_t<__half, 128>(a) : launch_decode_t<__half, 64>(a);
+    return a.fp8 ? launch_decode_dt<true>(a) : launch_decode_dt<false>(a);
 }
 
 }  // namespace pd

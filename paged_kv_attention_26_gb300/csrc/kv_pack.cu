@@ -62,9 +62,10 @@ kv_pack_kernel(uint4* __restrict__ staging, void* const* __restrict__ key_caches
 
 pd_status launch_kv_pack(bool unpack, void* staging, void* const* key_caches,
                          void* const* value_caches, int L, const int32_t* block_ids, int nblk,
-                         int Hk, int D, int S, int NB, int32_t* dev_err, cudaStream_t stream) {
+                         int Hk, int D, int S, int NB, int esize, int32_t* dev_err,
+                         cudaStream_t stream) {
     if (nblk == 0 || L == 0) return PD_OK;
-    const int64_t slab_vecs = int64_t(Hk) * S * D / 8;
+    const int64_t slab_vecs = int64_t(Hk) * S * D * esize / 16;
     dim3 grid(unsigned(nblk), unsigned(L), 2);
     if (unpack)
         kv_pack_kernel<true><<<grid, kPackThreads, 0, stream>>>(

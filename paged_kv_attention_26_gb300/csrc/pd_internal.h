@@ -17,6 +17,8 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline bool supported_D(int D) { return D == 64 || D == 128; }
 inline bool supported_S(int S) { return S == 8 || S == 16 || S == 32 || S == 64; }
 inline bool supported_dt(pd_dtype dt) { return dt == PD_F16 || dt == PD_BF16; }
+inline bool supported_pool_dt(pd_dtype dt) { return supported_dt(dt) || dt == PD_FP8_E4M3; }
+inline int elem_bytes(pd_dtype dt) { return dt == PD_FP8_E4M3 ? 1 : 2; }
 
 // ---- decode ------------------------------------------------------------------
 // Partition length chosen for a batch; a multiple of 64 tokens.
@@ -36,9 +38,12 @@ struct DecodeArgs {
     int max_context_len;
     float scale;
     void* workspace;
-    pd_dtype dt;
+    pd_dtype dt;                 // q and out
     int32_t* dev_err;
     cudaStream_t stream;
+    bool fp8 = false;            // pools hold E4M3 codes ...
+    const float* k_scale = nullptr;   // ... standing for code * scale[kv head]
+    const float* v_scale = nullptr;
 };
 pd_status launch_decode(const DecodeArgs& a);
 
@@ -48,14 +53,21 @@ pd_status launch_reshape_and_cache(const void* key, const void* value, void* key
                                    int Hk, int D, int S, int NB, int64_t key_stride_tok,
                                    int64_t value_stride_tok, int32_t* dev_err,
                                    cudaStream_t stream);
+pd_status launch_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,
+                                       void* value_cache, const int64_t* slot_mapping, int T,
+                                       int Hk, int D, int S, int NB, int64_t key_stride_tok,
+                                       int64_t value_stride_tok, const float* k_scale,
+                                       const float* v_scale, pd_dtype in_dt, int32_t* dev_err,
+                                       cudaStream_t stream);
 pd_status launch_copy_blocks(void* const* key_caches, void* const* value_caches, int L,
                              const int64_t* block_mapping, int npairs, int Hk, int D, int S,
-                             int NB, int32_t* dev_err, cudaStream_t stream);
+                             int NB, int esize, int32_t* dev_err, cudaStream_t stream);
 
 // ---- KV pack / unpack ------------------------------------------------------------------
 pd_status launch_kv_pack(bool unpack, void* staging, void* const* key_caches,
                          void* const* value_caches, int L, const int32_t* block_ids, int nblk,
-                         int Hk, int D, int S, int NB, int32_t* dev_err, cudaStream_t stream);
+                         int Hk, int D, int S, int NB, int esize, int32_t* dev_err,
+                         cudaStream_t stream);
 
 // ---- prefill -------------------------------------------------------------------------
 struct PrefillArgs {

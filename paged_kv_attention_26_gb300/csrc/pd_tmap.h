@@ -43,6 +43,22 @@ inline bool encode_pool_map(CUtensorMap* m, const void* pool, int D, unsigned lo
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// FP8 pool viewed as rows of D bytes; box = one [box_rows][D] slab, packed
+// rows, no swizzle.
+inline bool encode_pool_map_u8(CUtensorMap* m, const void* pool, int D, unsigned long long rows,
+                               int box_rows) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return false;
+    cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(D)};
+    cuuint32_t box[2] = {cuuint32_t(D), cuuint32_t(box_rows)};
+    cuuint32_t es[2] = {1u, 1u};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Packed queries [total_q][H][D]; box = 64 values x heads x tokens.
 inline bool encode_q_map(CUtensorMap* m, const void* q, int D, int H, int total_q,
                          int box_heads, int box_tokens, pd_dtype dt) {

@@ -397,3 +397,21 @@ def token_kv(positions, token_ids, Hk: int = 8, D: int = 128, dtype=torch.bfloat
         ks.append(torch.randn(Hk, D, generator=g))
         vs.append(torch.randn(Hk, D, generator=g))
     return torch.stack(ks).to(dtype), torch.stack(vs).to(dtype)
+
+
+def fp8_pools(key_cache: torch.Tensor, value_cache: torch.Tensor):
+    """One-byte E4M3 copies of 16-bit pools [NB, Hk, S, D] for FP8-cache tests:
+    per kv head, scale = (largest finite magnitude) / 448 and code = the
+    float32 value / scale cast by torch to float8_e4m3fn (NaN stays NaN).
+    Returns (key codes, value codes, k_scale, v_scale), uint8 and float32 [Hk]."""
+    out = []
+    for pool in (key_cache, value_cache):
+        x = pool.float()
+        finite = torch.where(torch.isfinite(x), x.abs(), torch.zeros_like(x))
+        amax = finite.amax(dim=(0, 2, 3)).clamp_min(1e-6)
+        scale = (amax / 448.0).to(torch.float32)
+        y = x / scale.view(1, -1, 1, 1)
+        codes = y.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        codes = torch.where(torch.isnan(x), torch.full_like(codes, 0x7F), codes)
+        out.append((codes.contiguous(), scale))
+    return out[0][0], out[1][0], out[0][1], out[1][1]
