@@ -78,8 +78,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 // once, and runs the 16-bit code on fp16 operands.
 template <int D, bool kF8 = false>
 struct DecodeSmem {
-    static constexpr int kRing = kF8 ? 4 : 3;          // stages TMA fills
-    static constexpr int kTiles16 = kF8 ? 1 : kRing;   // 16-bit tiles the consumers read
+    // FP8 with D = 128: consumers take MMA fragments straight from the raw
+    // (128-byte swizzled) tiles, so there is no 16-bit tile and the ring is deeper.
+    static constexpr bool kNative = kF8 && D == 128;
+    static constexpr int kRing = kNative ? 6 : (kF8 ? 4 : 3);   // stages TMA fills
+    static constexpr int kTiles16 = kNative ? 0 : (kF8 ? 1 : kRing);   // 16-bit tiles read
     static constexpr int kAtom = kStageTokens * 128;   // [64 tokens][64 values], 8 KB
     static constexpr int kTile = (D / 64) * kAtom;     // one stage of K (or of V)
     static constexpr int kTile8 = kStageTokens * D;    // one FP8 stage of K (or of V)
@@ -311,6 +314,20 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t w) {
     return (t & 0x80008000u) | ((t >> 1) & 0x3F803F80u);
 }
 
+// Two E4M3 codes at bytes (i, j) of w -> fp16x2 exactly (byte i low).
+template <uint32_t kSel>
+__device__ __forceinline__ uint32_t e4m3_pair_to_f16x2(uint32_t w) {
+    uint32_t t;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(t) : "r"(w), "n"(kSel));
+    return e4m3x2_to_f16x2(uint16_t(t));
+}
+
+// Address of 16-byte chunk c of row r in a stage of 128-byte rows written by
+// TMA with 128-byte swizzle (chunk c of row r at position c ^ (r % 8)).
+__device__ __forceinline__ uint32_t swz128(uint32_t base, int r, int c) {
+    return base + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
@@ -333,6 +350,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const float* __restrict__ k_scale, const float* __restrict__ v_scale,
                           int32_t* dev_err) {
     using L = DecodeSmem<D, kF8>;
+    constexpr bool kNative = L::kNative;
     using TM = typename std::conditional<kF8, __half, T>::type;   // tensor-core operand type
     using E = Elem<TM>;
     constexpr int kStages = L::kRing;
@@ -381,12 +399,17 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         // block i (unchecked), other lanes -2.  The ids of stage gs + 1 are
         // loaded while stage gs is issued, so the table's latency overlaps the
         // copies instead of sitting in front of every stage.
+        const int log2S = __ffs(S) - 1;                    // S is a power of two
         auto stage_blk = [&](const Walk& x) -> int {
             const int t0 = x.off * kStageTokens;
             const int nt = min(kStageTokens, x.ctx - t0);
-            const int nblk = (nt + S - 1) / S;             // <= 64 / S <= 8
-            const int32_t* bt_row = block_tables + (int64_t)x.s * max_blocks_per_seq;
-            return lane < nblk ? __ldg(bt_row + t0 / S + lane) : -2;
+            const int nblk = (nt + S - 1) >> log2S;        // <= 64 / S <= 8
+            const int32_t* p = block_tables + (int64_t)x.s * max_blocks_per_seq +
+                               (t0 >> log2S) + lane;
+            int v = -2;
+            // issued here, consumed one stage later
+            if (lane < nblk) asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+            return v;
         };
         Walk wn = w;                                       // one stage ahead of w
         int blk_cur = stage_blk(w);
@@ -470,9 +493,21 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             const T* qrow = q + ((int64_t)w.s * H + h0 + n) * D + 2 * (lane & 3);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                qb[ks][0] = n < GH ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks)) : 0u;
-                qb[ks][1] =
-                    n < GH ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8)) : 0u;
+                if constexpr (kNative) {
+                    // native FP8 path: k step ks pairs dims 16ks + 4t, +1 (register 0)
+                    // and 16ks + 4t + 2, +3 (register 1), t = lane % 4, the order in
+                    // which K comes out of its byte fragments
+                    const T* qr = q + ((int64_t)w.s * H + h0 + n) * D + 16 * ks + 4 * (lane & 3);
+                    const uint2 v = n < GH ? __ldg(reinterpret_cast<const uint2*>(qr))
+                                           : make_uint2(0u, 0u);
+                    qb[ks][0] = v.x;
+                    qb[ks][1] = v.y;
+                } else {
+                    qb[ks][0] =
+                        n < GH ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks)) : 0u;
+                    qb[ks][1] =
+                        n < GH ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8)) : 0u;
+                }
                 if constexpr (kF8 && !std::is_same<T, __half>::value) {
                     // q rounded to the fp16 operand type of the FP8 path
 #pragma unroll
@@ -509,7 +544,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             // the one 16-bit tile (no other warp reads them), then frees the raw
             // stage for the next copy right away.
             const int tslot = kF8 ? 0 : slot;
-            if constexpr (kF8) {
+            if constexpr (kF8 && !kNative) {
                 if (tb < nt) {
                     // K through integer operations (times 2^-8), V through the
                     // conversion unit (exact): the two halves run on different pipes.
@@ -550,7 +585,108 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[slot]);
             }
-            if (tb < nt) {
+            if constexpr (kNative) {
+              if (tb < nt) {
+                // ---- fragments straight from the raw E4M3 stage (128-byte rows,
+                // swizzled): ldmatrix moves bytes, the conversion happens in registers
+                const uint32_t k8 = smem_u32(smem + L::kK8 + slot * L::kTile8);
+                const uint32_t v8 = smem_u32(smem + L::kV8 + slot * L::kTile8);
+                const int lrow = tb + r8 + 8 * (j8 & 1);
+                uint32_t kr[D / 32][4], vr[D / 32][4];
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    wmma16::ldsm_x4(kr[c], swz128(k8, lrow, 2 * c + (j8 >> 1)));
+                    wmma16::ldsm_x4_t(vr[c], swz128(v8, lrow, 2 * c + (j8 >> 1)));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);     // the raw stage is free
+                // ---- S^T = K q^T: register j of block c holds row g (+8 for odd j),
+                // bytes 4t..4t+3 of dims 32c + 16 (j / 2) ..; K is widened as 2^-8 K
+                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        uint32_t a[4];
+                        a[0] = e4m3x2_to_f16x2_scaled<0x1404u>(kr[c][2 * h2]);
+                        a[1] = e4m3x2_to_f16x2_scaled<0x1404u>(kr[c][2 * h2 + 1]);
+                        a[2] = e4m3x2_to_f16x2_scaled<0x3424u>(kr[c][2 * h2]);
+                        a[3] = e4m3x2_to_f16x2_scaled<0x3424u>(kr[c][2 * h2 + 1]);
+                        const int ks = 2 * c + h2;
+                        wmma16::Mma<TM>::run(acc[ks & 1], a, qb[ks][0], qb[ks][1]);
+                    }
+                }
+                const int tok0 = tb + (lane >> 2);
+                float x[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int tok = tok0 + (i >> 1) * 8;
+                    x[i] = tok < nt ? (acc[0][i] + acc[1][i]) * sl2 : -INFINITY;
+                }
+                float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
+                    mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (mx[h] > m_run[h] + kRescaleThreshold) {
+                        const float alpha = ex2(m_run[h] - mx[h]);   // 0 the first time
+                        m_run[h] = mx[h];
+                        l_run[h] *= alpha;
+#pragma unroll
+                        for (int mt = 0; mt < KS; ++mt) {
+                            o[mt][h] *= alpha;
+                            o[mt][2 + h] *= alpha;
+                        }
+                    }
+                }
+                const float p0 = ex2(x[0] - m_run[0]), p1 = ex2(x[1] - m_run[1]);
+                const float p2 = ex2(x[2] - m_run[0]), p3 = ex2(x[3] - m_run[1]);
+                l_run[0] += p0 + p2;
+                l_run[1] += p1 + p3;
+                const uint32_t hi0 = E::pack2(p0, p1), hi1 = E::pack2(p2, p3);
+                const float2 lo0 = ffma2(E::unpack2(hi0), neg1, make_float2(p0, p1));
+                const float2 lo1 = ffma2(E::unpack2(hi1), neg1, make_float2(p2, p3));
+                const uint32_t bh0 = wmma16::movm_t(hi0), bh1 = wmma16::movm_t(hi1);
+                const uint32_t bl0 = wmma16::movm_t(E::pack2(lo0.x, lo0.y));
+                const uint32_t bl1 = wmma16::movm_t(E::pack2(lo1.x, lo1.y));
+                // ---- O^T += V^T P^T: register j of block c holds tokens 2t, 2t+1
+                // (+8 for odd j) x dims 2g, 2g+1 of chunk 2c + j / 2; m-tile 2c + j/2
+                // has rows g -> dim 2g and g + 8 -> dim 2g + 1 of that chunk
+                const bool partial = tb + 16 > nt;
+                const int tk = tb + 2 * (lane & 3);
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        uint32_t a[4];
+                        a[0] = e4m3_pair_to_f16x2<0x4420u>(vr[c][2 * h2]);
+                        a[1] = e4m3_pair_to_f16x2<0x4431u>(vr[c][2 * h2]);
+                        a[2] = e4m3_pair_to_f16x2<0x4420u>(vr[c][2 * h2 + 1]);
+                        a[3] = e4m3_pair_to_f16x2<0x4431u>(vr[c][2 * h2 + 1]);
+                        if (partial) {
+                            // tokens past the context: their V bytes are other data
+                            const uint32_t m01 = (tk < nt ? 0xffffu : 0u) |
+                                                 (tk + 1 < nt ? 0xffff0000u : 0u);
+                            const uint32_t m23 = (tk + 8 < nt ? 0xffffu : 0u) |
+                                                 (tk + 9 < nt ? 0xffff0000u : 0u);
+                            a[0] &= m01;
+                            a[1] &= m01;
+                            a[2] &= m23;
+                            a[3] &= m23;
+                        }
+                        const int mt = 2 * c + h2;
+                        wmma16::Mma<TM>::run(o[mt], a, bh0, bh1);
+                        wmma16::Mma<TM>::run(o[mt], a, bl0, bl1);
+                    }
+                }
+              } else {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+              }
+            } else if (tb < nt) {
                 const uint32_t kb = k_base0 + tslot * L::kTile;
                 const uint32_t vb = v_base0 + tslot * L::kTile;
                 const bool partial = tb + 16 > nt;
@@ -689,8 +825,11 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
                     for (int e = 0; e < 4; ++e) o[mt][e] *= vs;
             }
-            // lane: heads ha, ha + 1; dims 16mt + lane/4 and + 8
-            const int ha = 2 * (lane & 3), d0 = lane >> 2;
+            // lane: heads ha, ha + 1; dims 16mt + lane/4 and + 8 (native FP8: the
+            // m-tile rows g, g + 8 are dims 2g, 2g + 1)
+            const int ha = 2 * (lane & 3);
+            const int d0 = kNative ? 2 * (lane >> 2) : (lane >> 2);
+            constexpr int kDd = kNative ? 1 : 8;     // dim step of registers 2, 3
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int hh = ha + h;
@@ -703,7 +842,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
                     for (int mt = 0; mt < KS; ++mt) {
                         orow[16 * mt] = T(o[mt][h] * inv);
-                        orow[16 * mt + 8] = T(o[mt][2 + h] * inv);
+                        orow[16 * mt + kDd] = T(o[mt][2 + h] * inv);
                     }
                 } else {
                     const int64_t r = row * max_segs + seg;
@@ -711,7 +850,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
                     for (int mt = 0; mt < KS; ++mt) {
                         wrow[16 * mt] = o[mt][h];
-                        wrow[16 * mt + 8] = o[mt][2 + h];
+                        wrow[16 * mt + kDd] = o[mt][2 + h];
                     }
                     if (d0 == 0) {
                         ws_m[r] = m_run[h];
@@ -810,8 +949,8 @@ pd_status launch_decode_t(const DecodeArgs& a) {
     CUtensorMap tm_k, tm_v;
     const unsigned long long rows = (unsigned long long)a.NB * a.Hk * a.S;
     if (rows > 0x7fffffffull) return PD_ERR_UNSUPPORTED;   // TMA row coordinate is int32
-    const bool maps_ok = kF8 ? (encode_pool_map_u8(&tm_k, a.key_cache, D, rows, a.S) &&
-                                encode_pool_map_u8(&tm_v, a.value_cache, D, rows, a.S))
+    const bool maps_ok = kF8 ? (encode_pool_map_u8(&tm_k, a.key_cache, D, rows, a.S, Lt::kNative) &&
+                                encode_pool_map_u8(&tm_v, a.value_cache, D, rows, a.S, Lt::kNative))
                              : (encode_pool_map(&tm_k, a.key_cache, D, rows, a.S, a.dt) &&
                                 encode_pool_map(&tm_v, a.value_cache, D, rows, a.S, a.dt));
     if (!maps_ok) return launch_result(cudaErrorInvalidValue);

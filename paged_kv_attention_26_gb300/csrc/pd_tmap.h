@@ -44,9 +44,9 @@ inline bool encode_pool_map(CUtensorMap* m, const void* pool, int D, unsigned lo
 }
 
 // FP8 pool viewed as rows of D bytes; box = one [box_rows][D] slab, packed
-// rows, no swizzle.
+// rows, no swizzle, or 128-byte swizzle when swizzled (D must be 128).
 inline bool encode_pool_map_u8(CUtensorMap* m, const void* pool, int D, unsigned long long rows,
-                               int box_rows) {
+                               int box_rows, bool swizzled = false) {
     auto encode = tensor_map_encoder();
     if (!encode) return false;
     cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(rows)};
@@ -54,7 +54,8 @@ inline bool encode_pool_map_u8(CUtensorMap* m, const void* pool, int D, unsigned
     cuuint32_t box[2] = {cuuint32_t(D), cuuint32_t(box_rows)};
     cuuint32_t es[2] = {1u, 1u};
     return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
