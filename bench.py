@@ -199,35 +199,44 @@ def run_ours(args, rank, world, local_rank):
     step_bytes = dec_bytes + st_bytes
 
     def step():
-        pd.pd_reshape_and_cache(nk, nv, kc, vc, slots, dev_err=err)
+        pd.pd_decode_step(out, q, kc, vc, bt, cl, mcl, c.scale, nk, nv, slots, workspace=ws,
+                          dev_err=err)
+
+    def decode_only():
         pd.pd_paged_attention_decode(out, q, kc, vc, bt, cl, mcl, c.scale, ws, dev_err=err)
 
     for _ in range(args.warmup):
         flush()
         step()
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    launches0 = pd.launch_count()
-    t_wall0 = time.perf_counter()
-    for i in range(args.steps):
+
+    def timed(fn):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        n0 = pd.launch_count()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush()
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        n = pd.launch_count() - n0
+        if world > 1:
+            torch.distributed.barrier()
+        return sum(a.elapsed_time(b) for a, b in ev) * 1e-3, wall, n
+
+    # the headline: whole decode steps (store, then decode as a dependent grid)
+    step_s, t_wall, launches = timed(step)
+    # the roofline's kernel alone: the same decode launched by itself
+    for _ in range(args.warmup):
         flush()
-        e0, e1, e2 = ev[i]
-        e0.record(stream)
-        pd.pd_reshape_and_cache(nk, nv, kc, vc, slots, dev_err=err)
-        e1.record(stream)
-        pd.pd_paged_attention_decode(out, q, kc, vc, bt, cl, mcl, c.scale, ws, dev_err=err)
-        e2.record(stream)
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall0
-    launches = pd.launch_count() - launches0
-    if world > 1:
-        torch.distributed.barrier()
-    step_s = sum(a.elapsed_time(b2) for a, _, b2 in ev) * 1e-3
-    dec_s = sum(b1.elapsed_time(b2) for _, b1, b2 in ev) * 1e-3
+        decode_only()
+    dec_s, _, _ = timed(decode_only)
     if world > 1:
         t = torch.tensor([step_s], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -248,7 +257,8 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": "qwen3_8b_decode_step", "batch": B, "q_heads": H, "kv_heads": Hk,
                    "head_dim": D, "block_size": S, "context_lens": "uniform [128, 2048], seed 0",
                    "kv_tokens": int(sum(ctx)), "pool_blocks": c.pool.NB,
-                   "step": "store 64 tokens + split-context decode (one launch, in-kernel merge)",
+                   "step": "pd_decode_step: store 64 tokens, then split-context decode (one "
+                           "launch, in-kernel merge) as a programmatic dependent of the store",
                    "l2": "inputs larger than L2 (KV 321 MB vs 129 MB L2), and L2 flushed "
                          "before every timed step by reading a 256 MiB buffer",
                    "parallelism": f"replicas x{world}"},
@@ -258,6 +268,8 @@ def run_ours(args, rank, world, local_rank):
                      "achieved": round(achieved, 2), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
                      "alg_bytes_per_launch": dec_bytes,
+                     "timing": "the decode launched alone, steps x (L2 flush, launch), CUDA "
+                               "events on the launching stream",
                      "traffic": traffic, "traffic_source_sha": sha},
         "gpu_launches": launches,
         "wall_s_timed_loop": round(t_wall, 4),
@@ -296,44 +308,47 @@ def run_ours(args, rank, world, local_rank):
 
 
 def e2e_decode(pd, c, dev, args, step_bytes):
-    """The same step through the public API from pinned host buffers: per step
-    the inputs go host -> device, the step runs, the output comes back."""
+    """The same step through the public API from pinned host memory:
+    ``DecodeStep`` (one pinned staging buffer holding q, the new K/V, slots,
+    block tables and context lengths; one copy in, ``pd_decode_step``, one copy
+    of ``out`` back, synchronize), replayed from a CUDA graph; the same object
+    run eagerly is reported beside it."""
     import torch
-    pin = lambda t: t.contiguous().pin_memory()
-    h_in = [pin(c.q), pin(c.new_key), pin(c.new_value), pin(c.slot_mapping),
-            pin(c.pool.block_tables), pin(c.pool.context_lens)]
-    d_in = [torch.empty_like(t, device=dev) for t in h_in]
     kc, vc = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
-    out = torch.empty_like(d_in[0])
-    h_out = torch.empty_like(c.q).pin_memory()
-    ws = pd.decode_workspace(c.B, c.H, c.D, c.max_context_len, device=dev)
-    h2d = sum(t.numel() * t.element_size() for t in h_in)
-    d2h = h_out.numel() * h_out.element_size()
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-
-    def one():
-        for h, d in zip(h_in, d_in):
-            d.copy_(h, non_blocking=True)
-        q, nk, nv, sl, bt, cl = d_in
-        pd.pd_reshape_and_cache(nk, nv, kc, vc, sl)
-        pd.pd_paged_attention_decode(out, q, kc, vc, bt, cl, c.max_context_len, c.scale, ws)
-        h_out.copy_(out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-
-    for _ in range(args.warmup):
-        one()
-    total = 0.0
-    for _ in range(args.steps):
-        flush_buf.sum()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        one()
-        total += time.perf_counter() - t0
+    res = {}
+    for graph in (True, False):
+        st = pd.DecodeStep(kc, vc, c.B, c.H, c.B, c.pool.block_tables.shape[1],
+                           c.max_context_len, c.scale, c.dtype, graph=graph)
+        h = st.host
+        h["q"].copy_(c.q)
+        h["key"].copy_(c.new_key)
+        h["value"].copy_(c.new_value)
+        h["slot_mapping"].copy_(c.slot_mapping)
+        h["block_tables"].copy_(c.pool.block_tables)
+        h["context_lens"].copy_(c.pool.context_lens)
+        for _ in range(args.warmup):
+            st()
+        total = 0.0
+        for _ in range(args.steps):
+            flush_buf.sum()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            st()
+            total += time.perf_counter() - t0
+        assert st.dev_err.item() == 0
+        res[graph] = (total, st.h2d_bytes, st.d2h_bytes)
+        del st
+    total, h2d, d2h = res[True]
+    eager = res[False][0]
     return {"value": round(step_bytes * args.steps / total / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(total / args.steps * 1e3, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "path": "pinned host -> device copies, pd_reshape_and_cache, "
-                    "pd_paged_attention_decode, device -> host copy, synchronize"}
+            "path": "DecodeStep replayed from a CUDA graph: one pinned host -> device copy of "
+                    "the step's inputs, pd_decode_step, device -> host copy of out, "
+                    "synchronize; host wall clock per step, L2 flushed before each",
+            "eager_value": round(step_bytes * args.steps / eager / 1e9, 2),
+            "eager_ms_per_step": round(eager / args.steps * 1e3, 4)}
 
 
 def cpu_baseline_decode(c, step_bytes, budget_s=10.0):
@@ -467,13 +482,20 @@ def bench_fp8_decode(pd, pd_inputs, dev, args, flush, hbm_peak):
                                 c.slot_mapping.to(dev), ks, vs)
     t = _time_calls(lambda: pd.pd_paged_attention_decode_fp8(out, q, kc8, vc8, ks, vs, bt, cl, mcl,
                                                              c.scale, ws), args.extra_steps, flush)
+    nk, nv, sl = c.new_key.to(dev), c.new_value.to(dev), c.slot_mapping.to(dev)
+    ts = _time_calls(lambda: pd.pd_decode_step(out, q, kc8, vc8, bt, cl, mcl, c.scale, nk, nv, sl,
+                                               workspace=ws, k_scale=ks, v_scale=vs),
+                     args.extra_steps, flush)
     ctx = c.pool.context_lens.tolist()
     kv = sum(ctx) * c.Hk * c.D * 2                 # one byte per K and per V value
     other = 2 * c.B * c.H * c.D * 2 + sum(4 * -(-x // c.pool.S) for x in ctx)
     res = {"workload": "qwen3_8b_decode_step, E4M3 K/V with per-head scales",
            "ms": round(t * 1e3, 4), "gbs": round((kv + other) / t / 1e9, 1),
            "frac": round((kv + other) / t / 1e9 / hbm_peak, 4),
-           "kv_tokens_per_s": round(sum(ctx) / t, 1)}
+           "kv_tokens_per_s": round(sum(ctx) / t, 1),
+           "step_ms": round(ts * 1e3, 4),
+           "step_kv_tokens_per_s": round(sum(ctx) / ts, 1),
+           "step": "pd_decode_step_fp8 (quantising store of 64 tokens, then the decode)"}
     del kc8, vc8
     torch.cuda.empty_cache()
     return res

@@ -121,8 +121,13 @@ PD_API pd_status pd_reshape_and_cache(const void* key, const void* value,
  *                 start at zero: pieces are written before they are read in
  *                 the same launch, and the per-context arrival counters carry
  *                 a per-launch tag, so whatever an earlier launch (or other
- *                 data) left there counts as zero.  Overwritten; callers
- *                 sharing one workspace on two streams race.
+ *                 data) left there counts as zero.  The arrival that
+ *                 completes a context writes its counter back to zero, so a
+ *                 launch captured in a CUDA graph (tag fixed at capture)
+ *                 may be replayed any number of times; after a replay that
+ *                 flagged PD_DEVERR_TIMEOUT, zero the workspace before the
+ *                 next replay.  Overwritten; callers sharing one workspace
+ *                 on two streams race.
  *                 PD_ERR_WORKSPACE_TOO_SMALL if short. */
 PD_API size_t pd_decode_workspace_bytes(int B, int H, int D, int max_context_len);
 /* Token granule of the work split: a CTA takes at least this many tokens
@@ -213,6 +218,49 @@ PD_API pd_status pd_paged_attention_decode_fp8(void* out, const void* q,
                                                float scale, void* workspace,
                                                size_t workspace_bytes, pd_dtype dt,
                                                int32_t* dev_err, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* One decode step of one layer: store the step's new K/V rows, then decode
+ * attention that already sees them (nanoPD page, "模块结构与代码组织": the
+ * attention layer writes the new token into its slot, then attends over the
+ * whole paged context).  The result is exactly that of pd_reshape_and_cache
+ * (or pd_reshape_and_cache_fp8) followed by pd_paged_attention_decode (or
+ * pd_paged_attention_decode_fp8) on the same stream; the arguments are the
+ * union of theirs, with key/value/slot_mapping/T/strides those of the store
+ * and dt the type of key, value, q and out.
+ * Difference: the decode grid is launched as a programmatic dependent of the
+ * store grid, so its prologue (work split, context lengths, first block ids)
+ * overlaps the store; every read of the pools waits for the store grid.
+ * Ordering with earlier work on the stream is ordinary stream order.  Reads
+ * of q, block_tables and context_lens may happen while the store runs, so the
+ * store's inputs must not alias them (they never do in a decode step).
+ * All checks of both calls are made before anything is launched; on an error
+ * nothing is launched.  T == 0 skips the store (the decode then launches
+ * normally); B == 0 skips the decode. */
+PD_API pd_status pd_decode_step(const void* key, const void* value,
+                                const int64_t* slot_mapping, int T,
+                                int64_t key_stride_tok, int64_t value_stride_tok,
+                                void* out, const void* q, void* key_cache,
+                                void* value_cache, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* context_lens,
+                                int B, int H, int Hk, int D, int S, int NB,
+                                int max_context_len, float scale, void* workspace,
+                                size_t workspace_bytes, pd_dtype dt,
+                                int32_t* dev_err, cudaStream_t stream);
+/* pd_decode_step_fp8: the same over E4M3 pools with per-kv-head float32
+ * k_scale / v_scale [Hk] (DEVICE), used by both the store and the decode. */
+PD_API pd_status pd_decode_step_fp8(const void* key, const void* value,
+                                    const int64_t* slot_mapping, int T,
+                                    int64_t key_stride_tok, int64_t value_stride_tok,
+                                    void* out, const void* q, void* key_cache,
+                                    void* value_cache, const float* k_scale,
+                                    const float* v_scale, const int32_t* block_tables,
+                                    int max_blocks_per_seq,
+                                    const int32_t* context_lens, int B, int H, int Hk,
+                                    int D, int S, int NB, int max_context_len,
+                                    float scale, void* workspace,
+                                    size_t workspace_bytes, pd_dtype dt,
+                                    int32_t* dev_err, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------- */
 /* Copy-on-write block copies for fork (parallel sampling, beam search):

@@ -9,8 +9,11 @@ fails loudly otherwise.
 
 Functions carry the C names: ``pd_reshape_and_cache``,
 ``pd_paged_attention_decode`` (+ ``pd_decode_workspace_bytes``),
-``pd_copy_blocks``, ``pd_paged_prefill_chunk``; ``BlockManager`` wraps the
-host-side ``pd_bm_*`` calls.
+``pd_decode_step`` (store + decode), the ``_fp8`` variants, ``pd_copy_blocks``,
+``pd_kv_pack``/``pd_kv_unpack``, ``pd_paged_prefill_chunk``; ``BlockManager``
+and ``PrefixCache`` wrap the host-side ``pd_bm_*`` and ``pd_pc_*`` calls;
+``DecodeStep`` runs one host-to-host decode step (one copy in, the fused
+step, one copy out), optionally replayed from a CUDA graph.
 """
 from __future__ import annotations
 
@@ -55,6 +58,10 @@ SIGNATURES = {
                                       _P, _P, _I, _P, _P]),
     "pd_paged_attention_decode_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I,
                                            _I, _I, _I, _F, _P, _SZ, _I, _P, _P]),
+    "pd_decode_step": (_I, [_P, _P, _P, _I, _I64, _I64, _P, _P, _P, _P, _P, _I, _P, _I, _I,
+                            _I, _I, _I, _I, _I, _F, _P, _SZ, _I, _P, _P]),
+    "pd_decode_step_fp8": (_I, [_P, _P, _P, _I, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _I,
+                                _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _I, _P, _P]),
     "pd_kv_pack": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pd_kv_unpack": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pd_paged_prefill_chunk": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
@@ -300,6 +307,144 @@ def pd_paged_attention_decode(out, q, key_cache, value_cache, block_tables, cont
         NB, int(max_context_len), float(scale), ws_ptr, ws_bytes, dt, _opt(dev_err),
         _stream(stream))
     _check("pd_paged_attention_decode", st)
+
+
+def pd_decode_step(out, q, key_cache, value_cache, block_tables, context_lens,
+                   max_context_len: int, scale: float, key, value, slot_mapping,
+                   workspace=None, k_scale=None, v_scale=None, dev_err=None, stream=None):
+    """One decode step of one layer: store ``key``/``value`` [T, Hk, D] at
+    ``slot_mapping``, then decode ``q`` [B, H, D] over the paged caches into
+    ``out``.  The same result as ``pd_reshape_and_cache`` (``_fp8`` with
+    scales) followed by ``pd_paged_attention_decode`` (``_fp8``); the decode
+    grid's prologue overlaps the store.  One-byte pools need ``k_scale`` and
+    ``v_scale`` (float32 [Hk])."""
+    torch = _torch()
+    B, H, D = q.shape
+    NB, Hk, S, D2 = key_cache.shape
+    T = key.shape[0]
+    if out.shape != q.shape or D2 != D or value_cache.shape != key_cache.shape:
+        raise ValueError("shape mismatch")
+    if key.shape != (T, Hk, D) or value.shape != key.shape or slot_mapping.shape != (T,):
+        raise ValueError("key / value / slot_mapping shape")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables / context_lens shape")
+    for t, n in ((key, "key"), (value, "value")):
+        if t.stride(2) != 1 or t.stride(1) != D:
+            raise ValueError(f"{n} must have contiguous heads and dims")
+    fp8 = _is_fp8(key_cache)
+    if fp8 != _is_fp8(value_cache):
+        raise TypeError("dtype mismatch")
+    for t in (q, key, value):
+        if t.dtype != out.dtype or (not fp8 and t.dtype != key_cache.dtype):
+            raise TypeError("dtype mismatch")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    head = (_dev(key, "key", contiguous=False), _dev(value, "value", contiguous=False),
+            _dev(slot_mapping, "slot_mapping", torch.int64), T, key.stride(0), value.stride(0),
+            _dev(out, "out"), _dev(q, "q"), _dev(key_cache, "key_cache"),
+            _dev(value_cache, "value_cache"))
+    tail = (_dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+            _dev(context_lens, "context_lens", torch.int32), B, H, Hk, D, S, NB,
+            int(max_context_len), float(scale), ws_ptr, ws_bytes, _dt(q), _opt(dev_err),
+            _stream(stream))
+    if fp8:
+        if k_scale is None or v_scale is None:
+            raise ValueError("one-byte pools need k_scale and v_scale")
+        for sc in (k_scale, v_scale):
+            if sc.shape != (Hk,):
+                raise ValueError("scales must be [Hk]")
+        st = load().pd_decode_step_fp8(*head, _dev(k_scale, "k_scale", torch.float32),
+                                       _dev(v_scale, "v_scale", torch.float32), *tail)
+        _check("pd_decode_step_fp8", st)
+    else:
+        st = load().pd_decode_step(*head, *tail)
+        _check("pd_decode_step", st)
+
+
+class DecodeStep:
+    """One layer's decode step from host memory to host memory.
+
+    The step's inputs live in one pinned host buffer, exposed as views in
+    ``host`` (``q`` [B, H, D], ``key``/``value`` [T, Hk, D], ``slot_mapping``
+    int64 [T], ``block_tables`` int32 [B, max_blocks_per_seq],
+    ``context_lens`` int32 [B]).  A call copies that buffer to the device in
+    one transfer, runs ``pd_decode_step`` (store, then decode as a dependent
+    grid) and copies ``out`` back into the pinned ``host_out``.  With
+    ``graph=True`` those three operations are captured once in a CUDA graph
+    and each call replays it; ``max_context_len`` and ``scale`` are fixed at
+    construction (contexts may vary per call up to that bound).  One-byte
+    pools take ``k_scale``/``v_scale`` (float32 CUDA [Hk]).  The device error
+    word of the last call is ``dev_err``."""
+
+    def __init__(self, key_cache, value_cache, B: int, H: int, T: int, max_blocks_per_seq: int,
+                 max_context_len: int, scale: float, dtype, k_scale=None, v_scale=None,
+                 graph: bool = True):
+        torch = _torch()
+        dev = key_cache.device
+        NB, Hk, S, D = key_cache.shape
+        fields = (("q", (B, H, D), dtype), ("key", (T, Hk, D), dtype),
+                  ("value", (T, Hk, D), dtype), ("slot_mapping", (T,), torch.int64),
+                  ("block_tables", (B, max_blocks_per_seq), torch.int32),
+                  ("context_lens", (B,), torch.int32))
+        spans, off = [], 0
+        for name, shape, dt in fields:
+            n = torch.empty(shape, dtype=dt, device="meta").numel() * \
+                torch.empty((), dtype=dt, device="meta").element_size()
+            spans.append((name, shape, dt, off, n))
+            off += (n + 255) // 256 * 256
+        self.host_buf = torch.zeros(max(off, 256), dtype=torch.uint8).pin_memory()
+        self.dev_buf = torch.zeros(self.host_buf.shape, dtype=torch.uint8, device=dev)
+        self.host = {n: self.host_buf[o:o + b].view(dt).view(shape) for n, shape, dt, o, b in spans}
+        self.dev = {n: self.dev_buf[o:o + b].view(dt).view(shape) for n, shape, dt, o, b in spans}
+        self.host["slot_mapping"].fill_(-1)      # until the caller writes it: store nothing
+        self.out = torch.zeros((B, H, D), dtype=dtype, device=dev)
+        self.host_out = torch.zeros((B, H, D), dtype=dtype).pin_memory()
+        self.workspace = decode_workspace(B, H, D, max_context_len, device=dev)
+        self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.key_cache, self.value_cache = key_cache, value_cache
+        self.k_scale, self.v_scale = k_scale, v_scale
+        self.max_context_len, self.scale = int(max_context_len), float(scale)
+        self.device = dev
+        self.graph = None
+        # one eager run on the harmless initial inputs (no slot stored, empty
+        # contexts) sets up the launch attributes before any capture
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            self._body()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        if graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self._body()
+            self.graph = g
+
+    def _body(self):
+        d = self.dev
+        self.dev_buf.copy_(self.host_buf, non_blocking=True)
+        pd_decode_step(self.out, d["q"], self.key_cache, self.value_cache, d["block_tables"],
+                       d["context_lens"], self.max_context_len, self.scale, d["key"], d["value"],
+                       d["slot_mapping"], workspace=self.workspace, k_scale=self.k_scale,
+                       v_scale=self.v_scale, dev_err=self.dev_err)
+        self.host_out.copy_(self.out, non_blocking=True)
+
+    def __call__(self):
+        torch = _torch()
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self._body()
+        torch.cuda.current_stream(self.device).synchronize()
+        return self.host_out
+
+    @property
+    def h2d_bytes(self) -> int:
+        return self.host_buf.numel()
+
+    @property
+    def d2h_bytes(self) -> int:
+        return self.host_out.numel() * self.host_out.element_size()
 
 
 def pd_paged_attention_decode_noalloc(out, q, key_cache, value_cache, block_tables,

@@ -77,18 +77,25 @@ int pd_decode_partition_tokens(int max_context_len) {
     return decode_partition_tokens(max_context_len);
 }
 
-static pd_status decode_common(void* out, const void* q, const void* key_cache,
-                               const void* value_cache, const float* k_scale,
-                               const float* v_scale, bool fp8, const int32_t* block_tables,
-                               int max_blocks_per_seq, const int32_t* context_lens, int B, int H,
-                               int Hk, int D, int S, int NB, int max_context_len, float scale,
-                               void* workspace, size_t workspace_bytes, pd_dtype dt,
-                               int32_t* dev_err, cudaStream_t stream) {
+// Checks the decode arguments and fills *a; *skip is set when there is
+// nothing to launch (B == 0).
+static pd_status decode_prepare(void* out, const void* q, const void* key_cache,
+                                const void* value_cache, const float* k_scale,
+                                const float* v_scale, bool fp8, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* context_lens, int B, int H,
+                                int Hk, int D, int S, int NB, int max_context_len, float scale,
+                                void* workspace, size_t workspace_bytes, pd_dtype dt,
+                                int32_t* dev_err, cudaStream_t stream, DecodeArgs* a,
+                                bool* skip) {
+    *skip = false;
     if (B < 0 || H < 1 || Hk < 1 || NB < 1 || max_blocks_per_seq < 1 || max_context_len < 0)
         return PD_ERR_INVALID_ARG;
     if (H % Hk != 0) return PD_ERR_INVALID_ARG;
     if (!supported_D(D) || !supported_S(S) || !supported_dt(dt)) return PD_ERR_UNSUPPORTED;
-    if (B == 0) return PD_OK;
+    if (B == 0) {
+        *skip = true;
+        return PD_OK;
+    }
     if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens)
         return PD_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
@@ -103,11 +110,92 @@ static pd_status decode_common(void* out, const void* q, const void* key_cache,
         if (workspace_bytes < need) return PD_ERR_WORKSPACE_TOO_SMALL;
     }
     if (fp8 && (!k_scale || !v_scale)) return PD_ERR_INVALID_ARG;
-    DecodeArgs a{out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
-                 B, H, Hk, D, S, NB, max_context_len, scale, workspace, dt, dev_err, stream};
-    a.fp8 = fp8;
-    a.k_scale = k_scale;
-    a.v_scale = v_scale;
+    *a = DecodeArgs{out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                    context_lens, B, H, Hk, D, S, NB, max_context_len, scale, workspace, dt,
+                    dev_err, stream};
+    a->fp8 = fp8;
+    a->k_scale = k_scale;
+    a->v_scale = v_scale;
+    return PD_OK;
+}
+
+static pd_status decode_common(void* out, const void* q, const void* key_cache,
+                               const void* value_cache, const float* k_scale,
+                               const float* v_scale, bool fp8, const int32_t* block_tables,
+                               int max_blocks_per_seq, const int32_t* context_lens, int B, int H,
+                               int Hk, int D, int S, int NB, int max_context_len, float scale,
+                               void* workspace, size_t workspace_bytes, pd_dtype dt,
+                               int32_t* dev_err, cudaStream_t stream) {
+    DecodeArgs a{};
+    bool skip = false;
+    const pd_status st = decode_prepare(out, q, key_cache, value_cache, k_scale, v_scale, fp8,
+                                        block_tables, max_blocks_per_seq, context_lens, B, H, Hk,
+                                        D, S, NB, max_context_len, scale, workspace,
+                                        workspace_bytes, dt, dev_err, stream, &a, &skip);
+    if (st != PD_OK || skip) return st;
+    return launch_decode(a);
+}
+
+// Argument checks of the store (16-bit or FP8 pools); *skip when T == 0.
+static pd_status store_check(const void* key, const void* value, const void* key_cache,
+                             const void* value_cache, const int64_t* slot_mapping, int T, int Hk,
+                             int D, int S, int NB, int64_t key_stride_tok,
+                             int64_t value_stride_tok, bool fp8, const float* k_scale,
+                             const float* v_scale, pd_dtype dt, bool* skip) {
+    *skip = false;
+    if (T < 0 || Hk < 1 || NB < 1) return PD_ERR_INVALID_ARG;
+    if (!supported_D(D) || !supported_S(S) || !supported_dt(dt)) return PD_ERR_UNSUPPORTED;
+    if (!key_cache || !value_cache || !aligned16(key_cache) || !aligned16(value_cache))
+        return PD_ERR_INVALID_ARG;
+    if (T == 0) {
+        *skip = true;
+        return PD_OK;
+    }
+    if (!key || !value || !slot_mapping || !aligned16(key) || !aligned16(value))
+        return PD_ERR_INVALID_ARG;
+    if (fp8 && (!k_scale || !v_scale)) return PD_ERR_INVALID_ARG;
+    if (key_stride_tok < int64_t(Hk) * D || value_stride_tok < int64_t(Hk) * D ||
+        key_stride_tok % 8 || value_stride_tok % 8)
+        return PD_ERR_INVALID_ARG;
+    return PD_OK;
+}
+
+// Store then decode on one stream.  The decode grid is launched as a
+// programmatic dependent of the store grid: its CTAs start while the store
+// runs, do everything that does not read the pools (barriers, tensor-map
+// prefetch, context lengths, work split, first block ids), and wait for the
+// store grid's writes before their first K/V copy.  Both kernels follow
+// ordinary stream order with respect to everything launched before the store.
+static pd_status step_common(const void* key, const void* value, const int64_t* slot_mapping,
+                             int T, int64_t key_stride_tok, int64_t value_stride_tok, void* out,
+                             const void* q, void* key_cache, void* value_cache,
+                             const float* k_scale, const float* v_scale, bool fp8,
+                             const int32_t* block_tables, int max_blocks_per_seq,
+                             const int32_t* context_lens, int B, int H, int Hk, int D, int S,
+                             int NB, int max_context_len, float scale, void* workspace,
+                             size_t workspace_bytes, pd_dtype dt, int32_t* dev_err,
+                             cudaStream_t stream) {
+    DecodeArgs a{};
+    bool skip_dec = false, skip_store = false;
+    pd_status st = decode_prepare(out, q, key_cache, value_cache, k_scale, v_scale, fp8,
+                                  block_tables, max_blocks_per_seq, context_lens, B, H, Hk, D, S,
+                                  NB, max_context_len, scale, workspace, workspace_bytes, dt,
+                                  dev_err, stream, &a, &skip_dec);
+    if (st != PD_OK) return st;
+    st = store_check(key, value, key_cache, value_cache, slot_mapping, T, Hk, D, S, NB,
+                     key_stride_tok, value_stride_tok, fp8, k_scale, v_scale, dt, &skip_store);
+    if (st != PD_OK) return st;
+    if (!skip_store) {
+        st = fp8 ? launch_reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping,
+                                                T, Hk, D, S, NB, key_stride_tok, value_stride_tok,
+                                                k_scale, v_scale, dt, dev_err, stream)
+                 : launch_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, T,
+                                            Hk, D, S, NB, key_stride_tok, value_stride_tok,
+                                            dev_err, stream);
+        if (st != PD_OK) return st;
+    }
+    if (skip_dec) return PD_OK;
+    a.pdl = !skip_store;    // only ever dependent on our own store grid
     return launch_decode(a);
 }
 
@@ -133,6 +221,35 @@ pd_status pd_paged_attention_decode_fp8(void* out, const void* q, const void* ke
     return decode_common(out, q, key_cache, value_cache, k_scale, v_scale, true, block_tables,
                          max_blocks_per_seq, context_lens, B, H, Hk, D, S, NB, max_context_len,
                          scale, workspace, workspace_bytes, dt, dev_err, stream);
+}
+
+pd_status pd_decode_step(const void* key, const void* value, const int64_t* slot_mapping, int T,
+                         int64_t key_stride_tok, int64_t value_stride_tok, void* out,
+                         const void* q, void* key_cache, void* value_cache,
+                         const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* context_lens, int B, int H, int Hk, int D, int S, int NB,
+                         int max_context_len, float scale, void* workspace,
+                         size_t workspace_bytes, pd_dtype dt, int32_t* dev_err,
+                         cudaStream_t stream) {
+    return step_common(key, value, slot_mapping, T, key_stride_tok, value_stride_tok, out, q,
+                       key_cache, value_cache, nullptr, nullptr, false, block_tables,
+                       max_blocks_per_seq, context_lens, B, H, Hk, D, S, NB, max_context_len,
+                       scale, workspace, workspace_bytes, dt, dev_err, stream);
+}
+
+pd_status pd_decode_step_fp8(const void* key, const void* value, const int64_t* slot_mapping,
+                             int T, int64_t key_stride_tok, int64_t value_stride_tok, void* out,
+                             const void* q, void* key_cache, void* value_cache,
+                             const float* k_scale, const float* v_scale,
+                             const int32_t* block_tables, int max_blocks_per_seq,
+                             const int32_t* context_lens, int B, int H, int Hk, int D, int S,
+                             int NB, int max_context_len, float scale, void* workspace,
+                             size_t workspace_bytes, pd_dtype dt, int32_t* dev_err,
+                             cudaStream_t stream) {
+    return step_common(key, value, slot_mapping, T, key_stride_tok, value_stride_tok, out, q,
+                       key_cache, value_cache, k_scale, v_scale, true, block_tables,
+                       max_blocks_per_seq, context_lens, B, H, Hk, D, S, NB, max_context_len,
+                       scale, workspace, workspace_bytes, dt, dev_err, stream);
 }
 
 pd_status pd_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,

@@ -41,7 +41,9 @@
 //    carries the tag of the launch that last counted on it (high 44 bits)
 //    beside its count (low 20 bits), and a counter holding another launch's
 //    tag reads as zero.  Tags are distinct per launch within a process and
-//    salted per process.
+//    salted per process.  The arrival that completes a stream writes the
+//    counter back to zero, so a launch replayed with its tag unchanged (a
+//    captured CUDA graph) also finds its counters at zero.
 #include <cuda_runtime.h>
 
 #include <unistd.h>
@@ -198,7 +200,9 @@ __device__ __forceinline__ bool consumers_any(bool pred) {
 }
 
 // Count one arrived piece on a stream's tagged counter; true for the piece
-// that completes the stream.  High 44 bits: launch tag; low 20: count.
+// that completes the stream, which leaves the counter at zero (no other
+// piece of this launch touches it afterwards).  High 44 bits: launch tag;
+// low 20: count.
 constexpr unsigned long long kCountBits = 20;
 constexpr unsigned long long kCountMask = (1ull << kCountBits) - 1;
 
@@ -208,8 +212,9 @@ __device__ __forceinline__ bool arrive_piece(unsigned long long* cnt, unsigned l
     for (;;) {
         const unsigned long long next =
             (cur >> kCountBits) == tag ? cur + 1 : (tag << kCountBits) | 1ull;
-        const unsigned long long seen = atomicCAS(cnt, cur, next);
-        if (seen == cur) return int(next & kCountMask) == nseg;
+        const bool done = int(next & kCountMask) == nseg;
+        const unsigned long long seen = atomicCAS(cnt, cur, done ? 0ull : next);
+        if (seen == cur) return done;
         cur = seen;
     }
 }
@@ -413,6 +418,11 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         };
         Walk wn = w;                                       // one stage ahead of w
         int blk_cur = stage_blk(w);
+        // Launched as a dependent of the store grid, the CTA got here while
+        // the store may still run: wait for its writes before the first K/V
+        // copy (returns at once for an ordinary launch).
+        pdl_wait_primary();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
         for (uint32_t gs = 0; w.pos < w.end; ++gs) {
             const int slot = gs % kRingP;
             // every lane waits (acquire), then the warp agrees on the outcome
@@ -977,11 +987,21 @@ pd_status launch_decode_t(const DecodeArgs& a) {
     const int cap = int(std::min<long>(long(a.max_blocks_per_seq) * a.S, a.max_context_len));
     // persistent grid: two CTAs per SM (shared memory bound)
     const unsigned grid = unsigned(2 * sm_count(dev));
-    kern<<<grid, kDecodeThreads, Lt::kAlloc, a.stream>>>(
-        tm_k, tm_v, static_cast<T*>(a.out), static_cast<const T*>(a.q), a.block_tables,
-        a.max_blocks_per_seq, a.context_lens, a.B, a.H, a.Hk, a.S, a.NB, GH, scale_log2, P, cap,
-        ws_o, ws_m, ws_l, ws_cnt, next_launch_tag(), a.k_scale, a.v_scale, a.dev_err);
-    return launch_result(cudaGetLastError());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kDecodeThreads);
+    cfg.dynamicSmemBytes = Lt::kAlloc;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.pdl ? 1 : 0;
+    return launch_result(cudaLaunchKernelEx(
+        &cfg, kern, tm_k, tm_v, static_cast<T*>(a.out), static_cast<const T*>(a.q),
+        a.block_tables, a.max_blocks_per_seq, a.context_lens, a.B, a.H, a.Hk, a.S, a.NB, GH,
+        scale_log2, P, cap, ws_o, ws_m, ws_l, ws_cnt, next_launch_tag(), a.k_scale, a.v_scale,
+        a.dev_err));
 }
 
 template <bool kF8>

@@ -44,6 +44,7 @@ struct DecodeArgs {
     bool fp8 = false;            // pools hold E4M3 codes ...
     const float* k_scale = nullptr;   // ... standing for code * scale[kv head]
     const float* v_scale = nullptr;
+    bool pdl = false;            // launch as a programmatic dependent of the previous grid
 };
 pd_status launch_decode(const DecodeArgs& a);
 

@@ -21,6 +21,9 @@ reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict_
                          const int64_t* __restrict__ slot_mapping, int T, int Hk, int D,
                          int S, int NB, int64_t key_stride_vec, int64_t value_stride_vec,
                          int32_t* dev_err) {
+    // a decode grid launched as our dependent may start its prologue now; it
+    // waits for this grid's completion before reading the pools
+    pdl_launch_dependents();
     const int vec_per_row = D / 8;
     const int64_t g = int64_t(blockIdx.x) * kStoreThreads + threadIdx.x;
     const int64_t row = g / vec_per_row;
@@ -56,6 +59,7 @@ reshape_and_cache_fp8_kernel(const uint4* __restrict__ key, const uint4* __restr
                              const float* __restrict__ k_scale, const float* __restrict__ v_scale,
                              int32_t* dev_err) {
     using E = Elem<T>;
+    pdl_launch_dependents();
     const int vec8 = D / 16;                    // 16-byte FP8 vectors per row
     const int64_t g = int64_t(blockIdx.x) * kStoreThreads + threadIdx.x;
     const int64_t row = g / vec8;

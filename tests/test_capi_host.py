@@ -107,6 +107,43 @@ def test_decode_validation(lib):
     assert f(*a) == 1                          # not 256-byte aligned
 
 
+def test_decode_step_validation(lib):
+    """The fused store + decode call checks both halves before launching
+    anything: an error in either leaves the launch count unchanged."""
+    f = lib.pd_decode_step
+    base = [P, P, P, 4, 128, 128,            # key, value, slots, T, strides
+            P, P, P, P,                      # out, q, key_cache, value_cache
+            P, 8, P, 4, 8, 2, 64, 16, 64,    # tables, mbps, lens, B, H, Hk, D, S, NB
+            100, 0.125, None, 0, pd.PD_F16, None, None]
+    cases = [
+        ({3: -1}, 1),          # T < 0 (store half)
+        ({4: 100}, 1),         # key stride shorter than a token
+        ({0: P + 4}, 1),       # misaligned key
+        ({15: 3}, 1),          # H % Hk (decode half)
+        ({16: 80}, 2),         # D
+        ({6: 0}, 1),           # null out
+        ({19: 5000}, 1),       # long context without a workspace
+        ({23: 9}, 2),          # dtype
+    ]
+    n0 = lib.pd_launch_count()
+    for change, want in cases:
+        a = list(base)
+        for k, v in change.items():
+            a[k] = v
+        assert f(*a) == want, change
+    a = list(base)
+    a[3], a[13] = 0, 0         # nothing to store, nothing to decode
+    assert f(*a) == 0
+    assert lib.pd_launch_count() == n0
+    g = lib.pd_decode_step_fp8
+    a = list(base)
+    a[10:10] = [None, P]       # k_scale missing
+    assert g(*a) == 1
+    a[10], a[11] = P, None     # v_scale missing
+    assert g(*a) == 1
+    assert lib.pd_launch_count() == n0
+
+
 def test_workspace_size_formula(lib):
     part = lib.pd_decode_partition_tokens(10000)
     assert part % 64 == 0

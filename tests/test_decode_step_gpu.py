@@ -1,0 +1,206 @@
+"""GPU parity of the fused decode step (store the step's new K/V, then decode
+with the decode grid launched as a programmatic dependent of the store grid):
+bit-identical to the two separate calls, equal to the oracle's store then
+decode, and, over many consecutive steps with every stored slot poisoned
+beforehand, never reading a slot before the store grid wrote it."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pd_inputs
+from tests.parity import (assert_close, device_err, gpu_store_and_decode, odt,
+                          oracle_store_and_decode, u16)
+
+pytestmark = pytest.mark.gpu
+
+
+def _step(pd, c, kc, vc, dev_err=None, k_scale=None, v_scale=None):
+    dev = torch.device("cuda")
+    q = c.q.to(dev)
+    out = torch.empty_like(q)
+    ws = pd.decode_workspace(c.B, c.H, c.D, c.max_context_len)
+    pd.pd_decode_step(out, q, kc, vc, c.pool.block_tables.to(dev), c.pool.context_lens.to(dev),
+                      c.max_context_len, c.scale, c.new_key.to(dev), c.new_value.to(dev),
+                      c.slot_mapping.to(dev), workspace=ws, k_scale=k_scale, v_scale=v_scale,
+                      dev_err=dev_err)
+    return out
+
+
+@pytest.mark.parametrize("which", ["tiny", "qwen3_8b", "ragged"])
+def test_step_equals_separate_calls_and_oracle(cuda_lib, which):
+    if which == "tiny":
+        c = pd_inputs.tiny_decode()
+    elif which == "qwen3_8b":
+        c = pd_inputs.qwen3_8b_decode()
+    else:
+        c = pd_inputs.decode_case("ragged", 61, [1, 0, 16, 17, 64, 65, 999, 2048, 5000], 16, 4,
+                                  128, 16, torch.bfloat16, key_outlier_frac=0.05)
+    dev = torch.device("cuda")
+    err = device_err()
+    kc, vc = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
+    out = _step(cuda_lib, c, kc, vc, dev_err=err)
+    sep, kc2, vc2 = gpu_store_and_decode(cuda_lib, c)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.equal(out.view(torch.int16), sep.view(torch.int16))
+    assert torch.equal(kc.view(torch.int16), kc2.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), vc2.view(torch.int16))
+    rows = (0, 64) if which == "qwen3_8b" else None     # sequences 0 and 1 of the batch
+    ref, rk, rv = oracle_store_and_decode(c, rows=rows)
+    g = out.cpu()
+    if rows:
+        g = g.reshape(-1, c.D)[rows[0]:rows[1]]
+        ref = ref.reshape(-1, c.D)[rows[0]:rows[1]]
+    assert_close(g, ref, f"step {which}")
+    assert np.array_equal(u16(kc), rk) and np.array_equal(u16(vc), rv)
+
+
+def test_consecutive_steps_see_their_own_tokens(cuda_lib):
+    """20 decode steps of 8 sequences, one new token each per step.  Every
+    slot a step stores is NaN in the pool until then, so a decode that read
+    it before the store grid finished would return NaN."""
+    steps = 20
+    ctx0 = torch.tensor([1, 15, 16, 17, 63, 64, 300, 1100])
+    H, Hk, D, S = 16, 4, 128, 16
+    c = pd_inputs.decode_case("steps", 62, (ctx0 + steps).tolist(), H, Hk, D, S,
+                              torch.bfloat16, store_last=False)
+    bt = c.pool.block_tables
+    B = ctx0.shape[0]
+    for i in range(steps):                      # poison every slot that a step stores
+        slots = pd_inputs.slot_mapping_for(bt, torch.arange(B), ctx0 - 1 + i, S)
+        c.pool.key_cache[slots // S, :, slots % S] = float("nan")
+        c.pool.value_cache[slots // S, :, slots % S] = float("nan")
+    dev = torch.device("cuda")
+    kc, vc = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
+    rk, rv = u16(c.pool.key_cache), u16(c.pool.value_cache)
+    btd = bt.to(dev)
+    g = torch.Generator().manual_seed(63)
+    err = device_err()
+    ws = cuda_lib.decode_workspace(B, H, D, int(ctx0.max()) + steps)
+    outs, refs = [], []
+    for i in range(steps):
+        lens = (ctx0 + i).to(torch.int32)
+        slots = pd_inputs.slot_mapping_for(bt, torch.arange(B), ctx0 - 1 + i, S)
+        nk = torch.randn(B, Hk, D, generator=g).to(torch.bfloat16)
+        nv = torch.randn(B, Hk, D, generator=g).to(torch.bfloat16)
+        q = torch.randn(B, H, D, generator=g).to(torch.bfloat16)
+        out = torch.empty(B, H, D, dtype=torch.bfloat16, device=dev)
+        cuda_lib.pd_decode_step(out, q.to(dev), kc, vc, btd, lens.to(dev), int(lens.max()),
+                                c.scale, nk.to(dev), nv.to(dev), slots.to(dev), workspace=ws,
+                                dev_err=err)
+        outs.append(out)
+        oracle.reshape_and_cache(nk, nv, rk, rv, slots, S)
+        refs.append(oracle.decode(q, rk, rv, bt, lens, c.scale, oracle.BF16))
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    for i in range(steps):
+        assert_close(outs[i].cpu(), refs[i], f"step {i}")
+    assert np.array_equal(u16(kc), rk) and np.array_equal(u16(vc), rv)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_fp8_step_equals_separate_calls_and_oracle(cuda_lib, D):
+    c = pd_inputs.decode_case("fp8step", 64 + D, [1, 17, 64, 65, 700, 2049], 32, 8, D, 16,
+                              torch.bfloat16, poison=False)
+    kc8, vc8, ks, vs = pd_inputs.fp8_pools(c.pool.key_cache, c.pool.value_cache)
+    dev = torch.device("cuda")
+    err = device_err()
+    ksd, vsd = ks.to(dev), vs.to(dev)
+    kg, vg = kc8.to(dev), vc8.to(dev)
+    out = _step(cuda_lib, c, kg, vg, dev_err=err, k_scale=ksd, v_scale=vsd)
+    kg2, vg2 = kc8.to(dev), vc8.to(dev)
+    cuda_lib.pd_reshape_and_cache_fp8(c.new_key.to(dev), c.new_value.to(dev), kg2, vg2,
+                                      c.slot_mapping.to(dev), ksd, vsd, dev_err=err)
+    sep = torch.empty_like(out)
+    cuda_lib.pd_paged_attention_decode_fp8(
+        sep, c.q.to(dev), kg2, vg2, ksd, vsd, c.pool.block_tables.to(dev),
+        c.pool.context_lens.to(dev), c.max_context_len, c.scale,
+        cuda_lib.decode_workspace(c.B, c.H, c.D, c.max_context_len), dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.equal(out.view(torch.int16), sep.view(torch.int16))
+    assert torch.equal(kg, kg2) and torch.equal(vg, vg2)
+    rk, rv = kc8.numpy().copy(), vc8.numpy().copy()
+    oracle.reshape_and_cache_fp8(c.new_key, c.new_value, odt(c.dtype), rk, rv, c.slot_mapping,
+                                 ks, vs, c.pool.S)
+    assert np.array_equal(kg.cpu().numpy(), rk) and np.array_equal(vg.cpu().numpy(), rv)
+    ref = oracle.decode_fp8(c.q, odt(c.dtype), rk, rv, ks, vs, c.pool.block_tables,
+                            c.pool.context_lens, c.scale)
+    assert_close(out, ref, f"fp8 step D{D}")
+
+
+def test_step_without_new_tokens_is_plain_decode(cuda_lib):
+    c = pd_inputs.decode_case("nostore", 65, [5, 80, 333], 8, 2, 64, 16, torch.float16,
+                              store_last=False)
+    dev = torch.device("cuda")
+    kc, vc = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
+    out = _step(cuda_lib, c, kc, vc)
+    sep, _, _ = gpu_store_and_decode(cuda_lib, c)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), sep.view(torch.int16))
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_host_decode_step_replays(cuda_lib, graph):
+    """DecodeStep: inputs written into its pinned views, one call per step.
+    Six steps with new tokens, queries and context lengths each time; with a
+    CUDA graph the decode replays with its launch tag fixed at capture, so
+    this also checks that the merge counters come back to zero."""
+    pd = cuda_lib
+    steps, B, H, Hk, D, S = 6, 8, 16, 4, 128, 16
+    ctx0 = torch.tensor([1, 40, 64, 65, 300, 700, 1500, 2100])
+    c = pd_inputs.decode_case("hoststep", 66, (ctx0 + steps).tolist(), H, Hk, D, S,
+                              torch.bfloat16, store_last=False, poison=False)
+    bt = c.pool.block_tables
+    dev = torch.device("cuda")
+    kc, vc = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
+    rk, rv = u16(c.pool.key_cache), u16(c.pool.value_cache)
+    mcl = int(ctx0.max()) + steps
+    st = pd.DecodeStep(kc, vc, B, H, B, bt.shape[1], mcl, c.scale, torch.bfloat16, graph=graph)
+    assert (graph and st.graph is not None) or (not graph and st.graph is None)
+    g = torch.Generator().manual_seed(67)
+    for i in range(steps):
+        lens = (ctx0 + i).to(torch.int32)
+        slots = pd_inputs.slot_mapping_for(bt, torch.arange(B), ctx0 - 1 + i, S)
+        nk = torch.randn(B, Hk, D, generator=g).to(torch.bfloat16)
+        nv = torch.randn(B, Hk, D, generator=g).to(torch.bfloat16)
+        q = torch.randn(B, H, D, generator=g).to(torch.bfloat16)
+        h = st.host
+        h["q"].copy_(q)
+        h["key"].copy_(nk)
+        h["value"].copy_(nv)
+        h["slot_mapping"].copy_(slots)
+        h["block_tables"].copy_(bt)
+        h["context_lens"].copy_(lens)
+        got = st().clone()
+        assert st.dev_err.item() == 0
+        oracle.reshape_and_cache(nk, nv, rk, rv, slots, S)
+        ref = oracle.decode(q, rk, rv, bt, lens, c.scale, oracle.BF16)
+        assert_close(got, ref, f"host step {i} graph={graph}")
+    assert np.array_equal(u16(kc), rk) and np.array_equal(u16(vc), rv)
+    assert st.h2d_bytes >= (B * H * D + 2 * B * Hk * D) * 2 + B * 8 + bt.numel() * 4 + B * 4
+    assert st.d2h_bytes == B * H * D * 2
+
+
+def test_graph_replayed_decode_matches_eager(cuda_lib):
+    """pd_paged_attention_decode captured once and replayed three times gives
+    the eager result every time (the tag is the same in every replay)."""
+    pd = cuda_lib
+    c = pd_inputs.decode_case("replay", 68, [3, 64, 65, 1000, 2500, 7000], 32, 8, 128, 16,
+                              torch.bfloat16, store_last=False)
+    dev = torch.device("cuda")
+    kc, vc = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
+    q, bt, cl = c.q.to(dev), c.pool.block_tables.to(dev), c.pool.context_lens.to(dev)
+    ws = pd.decode_workspace(c.B, c.H, c.D, c.max_context_len)
+    eager = torch.empty_like(q)
+    pd.pd_paged_attention_decode(eager, q, kc, vc, bt, cl, c.max_context_len, c.scale, ws)
+    out = torch.zeros_like(q)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        pd.pd_paged_attention_decode(out, q, kc, vc, bt, cl, c.max_context_len, c.scale, ws)
+    for _ in range(3):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
