@@ -515,17 +515,25 @@ def bench_spec_verify(pd, pd_inputs, dev, args, flush, hbm_peak, bf16_peak):
     cu = m.cu_q_lens.to(dev)
     bt = m.pool.block_tables[:m.Bp].to(dev)
     cl = m.pool.context_lens[:m.Bp].to(dev)
-    t = _time_calls(lambda: pd.pd_paged_prefill_chunk(out, q, cu, m.max_q_len, kc, vc, bt, cl,
-                                                      m.scale), args.extra_steps, flush)
+    tp = _time_calls(lambda: pd.pd_paged_prefill_chunk(out, q, cu, m.max_q_len, kc, vc, bt, cl,
+                                                       m.scale), args.extra_steps, flush)
+    nq = m.max_q_len
+    mcl = int(m.pool.context_lens[:m.Bp].max())
+    q4, o4 = q.view(m.Bp, nq, m.H, m.D), out.view(m.Bp, nq, m.H, m.D)
+    ws = pd.verify_workspace(m.Bp, nq, m.H, m.D, mcl, device=dev)
+    t = _time_calls(lambda: pd.pd_paged_attention_verify(o4, q4, kc, vc, bt, cl, mcl, m.scale, ws),
+                    args.extra_steps, flush)
     ctx = m.pool.context_lens[:m.Bp].double()
     kv = float(ctx.sum()) * m.Hk * m.D * 2 * 2
-    nq = m.max_q_len
     P = m.prior_lens.double()
     flops = float(4 * m.D * m.H * (nq * P + nq * (nq + 1) / 2).sum())
     res = {"workload": f"{m.Bp} sequences x {nq} query tokens, prior U[128, 2048], bf16",
+           "path": "pd_paged_attention_verify (decode kernel, (head, query) columns)",
            "ms": round(t * 1e3, 4), "kv_gbs": round(kv / t / 1e9, 1),
            "kv_frac": round(kv / t / 1e9 / hbm_peak, 4), "tflops": round(flops / t / 1e12, 2),
-           "query_tokens_per_s": round(m.Bp * nq / t, 1)}
+           "query_tokens_per_s": round(m.Bp * nq / t, 1),
+           "via_prefill_chunk": {"ms": round(tp * 1e3, 4), "kv_gbs": round(kv / tp / 1e9, 1),
+                                 "kv_frac": round(kv / tp / 1e9 / hbm_peak, 4)}}
     del kc, vc
     torch.cuda.empty_cache()
     return res

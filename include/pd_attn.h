@@ -220,6 +220,37 @@ PD_API pd_status pd_paged_attention_decode_fp8(void* out, const void* q,
                                                int32_t* dev_err, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------- */
+/* Speculative verification (tutorial page "LLM 推理服务引擎深度拆解",
+ * section 7.1, 投机解码: the k drafted tokens and the last accepted one go
+ * through the large model in a single forward pass, so the weights and the
+ * KV cache are read once for k + 1 positions).
+ * nq query tokens per sequence, the last nq positions of its context (their
+ * K/V already stored): query j of sequence i sits at position
+ * context_lens[i] - nq + j and attends to positions 0 .. that position
+ * (causal among the nq).
+ *   out, q        [B][nq][H][D] of type dt, contiguous
+ *   nq            1 .. 8 (1 is exactly pd_paged_attention_decode)
+ *   workspace     pd_decode_workspace_bytes(B * nq, H, D, max_context_len)
+ *                 bytes, same rules as for decode
+ * every other argument as for pd_paged_attention_decode (16-bit pools only).
+ * The decode kernel, with the 8 MMA columns of a stream holding (head, query
+ * token) pairs: the K/V of a kv head is read once for up to 8 / nq of its
+ * query heads.  A context shorter than nq (but not empty) flags
+ * PD_DEVERR_CTX_RANGE; queries that see no key then read 0.
+ * PD_ERR_UNSUPPORTED: nq outside 1..8, B * nq > 65535. */
+PD_API pd_status pd_paged_attention_verify(void* out, const void* q,
+                                           const void* key_cache,
+                                           const void* value_cache,
+                                           const int32_t* block_tables,
+                                           int max_blocks_per_seq,
+                                           const int32_t* context_lens, int B, int nq,
+                                           int H, int Hk, int D, int S, int NB,
+                                           int max_context_len, float scale,
+                                           void* workspace, size_t workspace_bytes,
+                                           pd_dtype dt, int32_t* dev_err,
+                                           cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
 /* One decode step of one layer: store the step's new K/V rows, then decode
  * attention that already sees them (nanoPD page, "模块结构与代码组织": the
  * attention layer writes the new token into its slot, then attends over the

@@ -9,7 +9,8 @@ fails loudly otherwise.
 
 Functions carry the C names: ``pd_reshape_and_cache``,
 ``pd_paged_attention_decode`` (+ ``pd_decode_workspace_bytes``),
-``pd_decode_step`` (store + decode), the ``_fp8`` variants, ``pd_copy_blocks``,
+``pd_decode_step`` (store + decode), ``pd_paged_attention_verify`` (several
+query tokens per sequence), the ``_fp8`` variants, ``pd_copy_blocks``,
 ``pd_kv_pack``/``pd_kv_unpack``, ``pd_paged_prefill_chunk``; ``BlockManager``
 and ``PrefixCache`` wrap the host-side ``pd_bm_*`` and ``pd_pc_*`` calls;
 ``DecodeStep`` runs one host-to-host decode step (one copy in, the fused
@@ -58,6 +59,8 @@ SIGNATURES = {
                                       _P, _P, _I, _P, _P]),
     "pd_paged_attention_decode_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I,
                                            _I, _I, _I, _F, _P, _SZ, _I, _P, _P]),
+    "pd_paged_attention_verify": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _I,
+                                       _I, _F, _P, _SZ, _I, _P, _P]),
     "pd_decode_step": (_I, [_P, _P, _P, _I, _I64, _I64, _P, _P, _P, _P, _P, _I, _P, _I, _I,
                             _I, _I, _I, _I, _I, _F, _P, _SZ, _I, _P, _P]),
     "pd_decode_step_fp8": (_I, [_P, _P, _P, _I, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _I,
@@ -307,6 +310,41 @@ def pd_paged_attention_decode(out, q, key_cache, value_cache, block_tables, cont
         NB, int(max_context_len), float(scale), ws_ptr, ws_bytes, dt, _opt(dev_err),
         _stream(stream))
     _check("pd_paged_attention_decode", st)
+
+
+def pd_paged_attention_verify(out, q, key_cache, value_cache, block_tables, context_lens,
+                              max_context_len: int, scale: float, workspace=None,
+                              dev_err=None, stream=None):
+    """Speculative verification: q, out [B, nq, H, D] (nq = 1..8), the last nq
+    positions of each context, causal among themselves; caches [NB, Hk, S, D]
+    (16-bit); ``workspace`` holds ``pd_decode_workspace_bytes(B * nq, ...)``
+    bytes (``verify_workspace``)."""
+    torch = _torch()
+    B, nq, H, D = q.shape
+    NB, Hk, S, D2 = key_cache.shape
+    if out.shape != q.shape or D2 != D or value_cache.shape != key_cache.shape:
+        raise ValueError("shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables / context_lens shape")
+    dt = _dt(key_cache)
+    for t in (q, out, value_cache):
+        if t.dtype != key_cache.dtype:
+            raise TypeError("dtype mismatch")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    st = load().pd_paged_attention_verify(
+        _dev(out, "out"), _dev(q, "q"), _dev(key_cache, "key_cache"),
+        _dev(value_cache, "value_cache"), _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), B, nq, H, Hk, D,
+        S, NB, int(max_context_len), float(scale), ws_ptr, ws_bytes, dt, _opt(dev_err),
+        _stream(stream))
+    _check("pd_paged_attention_verify", st)
+
+
+def verify_workspace(B, nq, H, D, max_context_len, device="cuda"):
+    """Workspace for ``pd_paged_attention_verify`` (B sequences of nq queries)."""
+    return decode_workspace(B * nq, H, D, max_context_len, device=device)
 
 
 def pd_decode_step(out, q, key_cache, value_cache, block_tables, context_lens,

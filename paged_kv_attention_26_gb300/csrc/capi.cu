@@ -86,8 +86,9 @@ static pd_status decode_prepare(void* out, const void* q, const void* key_cache,
                                 int Hk, int D, int S, int NB, int max_context_len, float scale,
                                 void* workspace, size_t workspace_bytes, pd_dtype dt,
                                 int32_t* dev_err, cudaStream_t stream, DecodeArgs* a,
-                                bool* skip) {
+                                bool* skip, int nq = 1) {
     *skip = false;
+    if (nq < 1 || nq > 8) return PD_ERR_UNSUPPORTED;
     if (B < 0 || H < 1 || Hk < 1 || NB < 1 || max_blocks_per_seq < 1 || max_context_len < 0)
         return PD_ERR_INVALID_ARG;
     if (H % Hk != 0) return PD_ERR_INVALID_ARG;
@@ -100,10 +101,10 @@ static pd_status decode_prepare(void* out, const void* q, const void* key_cache,
         return PD_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
         return PD_ERR_INVALID_ARG;
-    if (B > 65535 || int64_t(max_blocks_per_seq) * S > (int64_t(1) << 30) ||
+    if (int64_t(B) * nq > 65535 || int64_t(max_blocks_per_seq) * S > (int64_t(1) << 30) ||
         decode_num_partitions(max_context_len) > 65535)
         return PD_ERR_UNSUPPORTED;
-    const size_t need = decode_workspace_bytes(B, H, D, max_context_len);
+    const size_t need = decode_workspace_bytes(B * nq, H, D, max_context_len);
     if (need > 0) {
         if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
             return PD_ERR_INVALID_ARG;
@@ -116,6 +117,7 @@ static pd_status decode_prepare(void* out, const void* q, const void* key_cache,
     a->fp8 = fp8;
     a->k_scale = k_scale;
     a->v_scale = v_scale;
+    a->nq = nq;
     return PD_OK;
 }
 
@@ -250,6 +252,23 @@ pd_status pd_decode_step_fp8(const void* key, const void* value, const int64_t* 
                        key_cache, value_cache, k_scale, v_scale, true, block_tables,
                        max_blocks_per_seq, context_lens, B, H, Hk, D, S, NB, max_context_len,
                        scale, workspace, workspace_bytes, dt, dev_err, stream);
+}
+
+pd_status pd_paged_attention_verify(void* out, const void* q, const void* key_cache,
+                                    const void* value_cache, const int32_t* block_tables,
+                                    int max_blocks_per_seq, const int32_t* context_lens, int B,
+                                    int nq, int H, int Hk, int D, int S, int NB,
+                                    int max_context_len, float scale, void* workspace,
+                                    size_t workspace_bytes, pd_dtype dt, int32_t* dev_err,
+                                    cudaStream_t stream) {
+    DecodeArgs a{};
+    bool skip = false;
+    const pd_status st = decode_prepare(out, q, key_cache, value_cache, nullptr, nullptr, false,
+                                        block_tables, max_blocks_per_seq, context_lens, B, H, Hk,
+                                        D, S, NB, max_context_len, scale, workspace,
+                                        workspace_bytes, dt, dev_err, stream, &a, &skip, nq);
+    if (st != PD_OK || skip) return st;
+    return launch_decode(a);
 }
 
 pd_status pd_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,

@@ -219,21 +219,24 @@ __device__ __forceinline__ bool arrive_piece(unsigned long long* cnt, unsigned l
     }
 }
 
-// Merge the np pieces of a stream's GH rows (one warp, fixed piece order):
+// Merge the np pieces of a stream's rows (one warp, fixed piece order):
 // M = max_k m_k; out = sum_k o_k 2^(m_k - M) / sum_k l_k 2^(m_k - M).
-// Four lanes per row (row = lane / 4, a quarter of D each), so every row is
-// merged at once and the loads of all pieces are in flight together.
-// Pieces of other CTAs are read through L2 (ld.global.cg).
+// Four lanes per row (a quarter of D each), so every row is merged at once
+// and the loads of all pieces are in flight together.  Row n = col0 + lane / 4
+// is column n of the stream: head h0 + n / nq, query token n % nq of
+// sequence s (nq = 1 for decode).  Pieces of other CTAs are read through L2.
 template <typename T, int D>
 __device__ __forceinline__ void merge_stream(T* __restrict__ out, const float* ws_o,
-                                             const float* ws_m, const float* ws_l, int64_t row0,
-                                             int GH, int max_segs, int np, int lane) {
+                                             const float* ws_m, const float* ws_l, int s, int h0,
+                                             int H, int nq, int GH, int col0, int max_segs,
+                                             int np, int lane) {
     using E = Elem<T>;
     constexpr int kDpl = D / 4;          // values per lane
     constexpr int kCache = 8;            // pieces whose (m, l) stay in registers
-    const int h = lane >> 2;
-    if (h >= GH) return;
-    const int64_t row = row0 + h;
+    const int n = col0 + (lane >> 2);
+    const int hh = n / nq, j = n - hh * nq;
+    if (hh >= GH) return;
+    const int64_t row = ((int64_t)s * nq + j) * H + h0 + hh;
     const float* m = ws_m + row * max_segs;
     const float* l = ws_l + row * max_segs;
     const float* o = ws_o + row * max_segs * D + (lane & 3) * kDpl;
@@ -272,7 +275,7 @@ __device__ __forceinline__ void merge_stream(T* __restrict__ out, const float* w
             acc[4 * c + 3] += v.w * w;
         }
     }
-    const float inv = 1.f / lsum;
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;      // a query that saw no key: 0
     uint4* dst = reinterpret_cast<uint4*>(out + row * D + (lane & 3) * kDpl);
 #pragma unroll
     for (int c = 0; c < kDpl / 8; ++c)
@@ -283,18 +286,22 @@ __device__ __forceinline__ void merge_stream(T* __restrict__ out, const float* w
 }
 
 // Rows of empty contexts get zeros (no stream covers them); contexts outside
-// [0, cap] are flagged (the walk cuts them to cap).  CTA b takes sequences
-// b, b + grid, ...; called by one warp.
+// [0, cap], and non-empty ones shorter than the nq query tokens they hold,
+// are flagged (the walk cuts them to cap).  CTA b takes sequences b, b +
+// grid, ...; called by one warp.
 template <typename T, int D>
 __device__ __forceinline__ void zero_empty_rows(T* __restrict__ out,
                                                 const int32_t* __restrict__ context_lens, int B,
-                                                int H, int cap, int32_t* dev_err, int lane) {
+                                                int H, int nq, int cap, int32_t* dev_err,
+                                                int lane) {
     for (int s = blockIdx.x; s < B; s += gridDim.x) {
         const int raw = __ldg(context_lens + s);
-        if ((raw < 0 || raw > cap) && lane == 0) flag_error(dev_err, PD_DEVERR_CTX_RANGE);
+        if ((raw < 0 || raw > cap || (raw > 0 && raw < nq)) && lane == 0)
+            flag_error(dev_err, PD_DEVERR_CTX_RANGE);
         if (raw <= 0) {
-            uint4* dst = reinterpret_cast<uint4*>(out + (int64_t)s * H * D);
-            for (int i = lane; i < H * D * 2 / 16; i += 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+            uint4* dst = reinterpret_cast<uint4*>(out + (int64_t)s * nq * H * D);
+            for (int i = lane; i < nq * H * D * 2 / 16; i += 32)
+                dst[i] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
 }
@@ -342,13 +349,20 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // T: type of q and out.  kF8: the pools hold E4M3 codes with a K and a V scale
 // per kv head; the tensor-core products then run on fp16 (K and V widened
 // exactly, q rounded to fp16), and the scales are applied in fp32.
-template <typename T, int D, bool kF8>
+// kMQ: nq_arg query tokens per sequence (speculative verification), the last
+// nq_arg positions of its context, each attending causally.  The columns of a
+// stream are then (head, query token) pairs, GH * nq_arg <= 16: one tile of 8
+// columns is the decode layout (each consumer warp takes 16 tokens of a
+// stage); with two tiles, warp w takes tile w / 2 and tokens 32 (w % 2) ..
+// + 31 of each stage, so K/V of a kv head is still read once.
+template <typename T, int D, bool kF8, bool kMQ>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, T* __restrict__ out,
                           const T* __restrict__ q, const int32_t* __restrict__ block_tables,
                           int max_blocks_per_seq, const int32_t* __restrict__ context_lens,
-                          int B, int H, int Hk, int S, int NB, int GH, float scale_log2,
+                          int B, int H, int Hk, int S, int NB, int GH, int nq_arg,
+                          float scale_log2,
                           int max_segs, int cap, float* __restrict__ ws_o,
                           float* __restrict__ ws_m, float* __restrict__ ws_l,
                           unsigned long long* __restrict__ ws_cnt, unsigned long long tag,
@@ -373,6 +387,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int G = H / Hk;
     const int groups = G / GH;
     const int units = Hk * groups;
+    const int nq = kMQ ? nq_arg : 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -390,7 +405,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
 
     Walk w;
     if (!walk_begin(w, context_lens, B, units, cap)) {          // uniform: no range
-        if (warp == 0) zero_empty_rows<T, D>(out, context_lens, B, H, cap, dev_err, lane);
+        if (warp == 0) zero_empty_rows<T, D>(out, context_lens, B, H, nq, cap, dev_err, lane);
         return;
     }
 
@@ -472,13 +487,18 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             blk_cur = blk_next;
         }
         // all loads are issued: the producer has time for the empty rows
-        zero_empty_rows<T, D>(out, context_lens, B, H, cap, dev_err, lane);
+        zero_empty_rows<T, D>(out, context_lens, B, H, nq, cap, dev_err, lane);
         return;
     }
 
     // ---------------- consumer warps ----------------
     const int j8 = lane >> 3, r8 = lane & 7;     // ldmatrix: matrix index, row within it
-    const int tb = warp * 16;                    // this warp's tokens within a stage
+    // this warp's tokens within a stage (16, or 32 with two column tiles) and
+    // its first column
+    const int ctiles = kMQ ? (GH * nq + kHeadsN - 1) / kHeadsN : 1;
+    const int wpc = kConsumerWarps / ctiles;     // warps per column tile
+    const int tb = kMQ ? (warp % wpc) * 16 * ctiles : warp * 16;
+    const int col0 = kMQ ? (warp / wpc) * kHeadsN : 0;
     const uint32_t k_base0 = smem_u32(smem + L::kK);
     const uint32_t v_base0 = smem_u32(smem + L::kV);
     const float2 neg1 = make_float2(-1.f, -1.f);
@@ -499,24 +519,28 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         // (register 0) and the same + 8 (register 1); heads past GH are zero.
         uint32_t qb[KS][2];
         {
-            const int n = lane >> 2;
-            const T* qrow = q + ((int64_t)w.s * H + h0 + n) * D + 2 * (lane & 3);
+            // column n: head h0 + n / nq, query token n % nq
+            const int n = col0 + (lane >> 2);
+            const int qh = n / nq, qj = n - qh * nq;
+            const bool qv = qh < GH;
+            const int64_t qrow_i = ((int64_t)w.s * nq + qj) * H + h0 + qh;
+            const T* qrow = q + qrow_i * D + 2 * (lane & 3);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 if constexpr (kNative) {
                     // native FP8 path: k step ks pairs dims 16ks + 4t, +1 (register 0)
                     // and 16ks + 4t + 2, +3 (register 1), t = lane % 4, the order in
                     // which K comes out of its byte fragments
-                    const T* qr = q + ((int64_t)w.s * H + h0 + n) * D + 16 * ks + 4 * (lane & 3);
-                    const uint2 v = n < GH ? __ldg(reinterpret_cast<const uint2*>(qr))
-                                           : make_uint2(0u, 0u);
+                    const T* qr = q + qrow_i * D + 16 * ks + 4 * (lane & 3);
+                    const uint2 v = qv ? __ldg(reinterpret_cast<const uint2*>(qr))
+                                       : make_uint2(0u, 0u);
                     qb[ks][0] = v.x;
                     qb[ks][1] = v.y;
                 } else {
                     qb[ks][0] =
-                        n < GH ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks)) : 0u;
+                        qv ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks)) : 0u;
                     qb[ks][1] =
-                        n < GH ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8)) : 0u;
+                        qv ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8)) : 0u;
                 }
                 if constexpr (kF8 && !std::is_same<T, __half>::value) {
                     // q rounded to the fp16 operand type of the FP8 path
@@ -538,6 +562,11 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
         float m_run[2] = {-INFINITY, -INFINITY};
         float l_run[2] = {0.f, 0.f};
+        // columns 2(lane%4) + h: query token j sits nq - 1 - j positions
+        // before the context end and sees no key past itself
+        int dj[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) dj[h] = kMQ ? nq - 1 - (col0 + 2 * (lane & 3) + h) % nq : 0;
 
         for (int st = 0; st < piece_stages; ++st, ++gs) {
             const int slot = gs % kStages;
@@ -549,7 +578,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 aborted = true;
                 break;                   // skip the piece's other stages
             }
-            const int nt = min(kStageTokens, w.ctx - (w.off + st) * kStageTokens);
+            const int rem = w.ctx - (w.off + st) * kStageTokens;   // context from this stage on
+            const int nt = min(kStageTokens, rem);
             // FP8 pools: this warp widens its own 16 rows of K and V to fp16 in
             // the one 16-bit tile (no other warp reads them), then frees the raw
             // stage for the next copy right away.
@@ -631,7 +661,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int tok = tok0 + (i >> 1) * 8;
-                    x[i] = tok < nt ? (acc[0][i] + acc[1][i]) * sl2 : -INFINITY;
+                    x[i] = tok < (kMQ ? rem - dj[i & 1] : nt) ? (acc[0][i] + acc[1][i]) * sl2
+                                                                : -INFINITY;
                 }
                 float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
 #pragma unroll
@@ -652,8 +683,11 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         }
                     }
                 }
-                const float p0 = ex2(x[0] - m_run[0]), p1 = ex2(x[1] - m_run[1]);
-                const float p2 = ex2(x[2] - m_run[0]), p3 = ex2(x[3] - m_run[1]);
+                // a verify column may not have seen a key yet (m = -inf): its p are 0
+                const float mu0 = kMQ && m_run[0] == -INFINITY ? 0.f : m_run[0];
+                const float mu1 = kMQ && m_run[1] == -INFINITY ? 0.f : m_run[1];
+                const float p0 = ex2(x[0] - mu0), p1 = ex2(x[1] - mu1);
+                const float p2 = ex2(x[2] - mu0), p3 = ex2(x[3] - mu1);
                 l_run[0] += p0 + p2;
                 l_run[1] += p1 + p3;
                 const uint32_t hi0 = E::pack2(p0, p1), hi1 = E::pack2(p2, p3);
@@ -696,16 +730,19 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[slot]);
               }
-            } else if (tb < nt) {
+            } else {
+              for (int sub = 0; sub < (kMQ ? ctiles : 1); ++sub) {
+                const int tbs = tb + 16 * sub;           // 16 tokens of this warp
+                if (tbs >= nt) break;
                 const uint32_t kb = k_base0 + tslot * L::kTile;
                 const uint32_t vb = v_base0 + tslot * L::kTile;
-                const bool partial = tb + 16 > nt;
+                const bool partial = tbs + 16 > nt;
                 if (partial) {
                     // V rows past the context end hold other data or were never
                     // loaded this round: zero them so that 0 * v stays 0.
                     unsigned char* vrow = smem + L::kV + tslot * L::kTile;
                     for (int i = lane; i < 16 * kAtoms * 8; i += 32) {
-                        const int tok = tb + i / (kAtoms * 8);
+                        const int tok = tbs + i / (kAtoms * 8);
                         if (tok >= nt) {
                             const int a = (i / 8) % kAtoms, c = i % 8;
                             *reinterpret_cast<uint4*>(vrow + a * L::kAtom + tok * 128 + c * 16) =
@@ -719,16 +756,17 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
                     uint32_t a[4];
-                    wmma16::ldsm_x4(a, swz<D>(kb, tb + r8 + 8 * (j8 & 1), 2 * ks + (j8 >> 1)));
+                    wmma16::ldsm_x4(a, swz<D>(kb, tbs + r8 + 8 * (j8 & 1), 2 * ks + (j8 >> 1)));
                     wmma16::Mma<TM>::run(acc[ks & 1], a, qb[ks][0], qb[ks][1]);
                 }
-                // lane holds tokens tb + lane/4 (0,1) and + 8 (2,3); heads 2(lane%4) + {0,1}
-                const int tok0 = tb + (lane >> 2);
+                // lane holds tokens tbs + lane/4 (0,1) and + 8 (2,3); heads 2(lane%4) + {0,1}
+                const int tok0 = tbs + (lane >> 2);
                 float x[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int tok = tok0 + (i >> 1) * 8;
-                    x[i] = tok < nt ? (acc[0][i] + acc[1][i]) * sl2 : -INFINITY;
+                    x[i] = tok < (kMQ ? rem - dj[i & 1] : nt) ? (acc[0][i] + acc[1][i]) * sl2
+                                                                : -INFINITY;
                 }
                 // ---- online softmax per head (lane-local state, 3 shuffles per head)
                 float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
@@ -750,8 +788,11 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         }
                     }
                 }
-                const float p0 = ex2(x[0] - m_run[0]), p1 = ex2(x[1] - m_run[1]);
-                const float p2 = ex2(x[2] - m_run[0]), p3 = ex2(x[3] - m_run[1]);
+                // a verify column may not have seen a key yet (m = -inf): its p are 0
+                const float mu0 = kMQ && m_run[0] == -INFINITY ? 0.f : m_run[0];
+                const float mu1 = kMQ && m_run[1] == -INFINITY ? 0.f : m_run[1];
+                const float p0 = ex2(x[0] - mu0), p1 = ex2(x[1] - mu1);
+                const float p2 = ex2(x[2] - mu0), p3 = ex2(x[3] - mu1);
                 l_run[0] += p0 + p2;
                 l_run[1] += p1 + p3;
                 // P as hi + lo 16-bit pairs, transposed into B-operand layout
@@ -765,11 +806,12 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
                     uint32_t a[4];
-                    wmma16::ldsm_x4_t(a, swz<D>(vb, tb + r8 + 8 * (j8 >> 1), 2 * mt + (j8 & 1)));
+                    wmma16::ldsm_x4_t(a, swz<D>(vb, tbs + r8 + 8 * (j8 >> 1), 2 * mt + (j8 & 1)));
                     wmma16::Mma<TM>::run(o[mt], a, bh0, bh1);
                     wmma16::Mma<TM>::run(o[mt], a, bl0, bl1);
                 }
                 if (partial && !kF8) tc::fence_proxy_async_smem();   // zeros before the next TMA write
+              }
             }
             __syncwarp();
             if (!kF8 && lane == 0) mbar_arrive(&empty[slot]);
@@ -818,16 +860,24 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 for (int e = 0; e < 4; ++e)
                     o[mt][e] = o[mt][e] * c_mine[e & 1] + x[(mt * 4 + e) * 32] * c_other[e & 1];
         };
-        if (warp >= 2) put(warp - 2);
-        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-        if (warp < 2) take(warp);
-        if (warp == 1) {
-            __syncwarp();
-            put(1);                      // own partner slot, already read by this warp
+        // two column tiles: warp 1 hands over to 0 and warp 3 to 2 (same tile)
+        const bool two_tiles = kMQ && ctiles == 2;
+        if (!two_tiles) {
+            if (warp >= 2) put(warp - 2);
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+            if (warp < 2) take(warp);
+            if (warp == 1) {
+                __syncwarp();
+                put(1);                  // own partner slot, already read by this warp
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+            if (warp == 0) take(1);
+        } else {
+            if (warp & 1) put(warp >> 1);
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+            if (!(warp & 1)) take(warp >> 1);
         }
-        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-        if (warp == 0) {
-            take(1);
+        if (two_tiles ? (warp & 1) == 0 : warp == 0) {
             if constexpr (kF8) {
                 const float vs = __ldg(v_scale + kvh);
 #pragma unroll
@@ -842,12 +892,13 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             constexpr int kDd = kNative ? 1 : 8;     // dim step of registers 2, 3
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int hh = ha + h;
+                const int c = col0 + ha + h;          // column: head h0 + c / nq, query c % nq
+                const int hh = c / nq, jq = c - hh * nq;
                 if (hh >= GH) continue;
-                const int64_t row = (int64_t)w.s * H + h0 + hh;
+                const int64_t row = ((int64_t)w.s * nq + jq) * H + h0 + hh;
                 if (nseg == 1) {
                     // the whole stream was here: final, normalised output
-                    const float inv = 1.f / l_run[h];
+                    const float inv = kMQ && l_run[h] == 0.f ? 0.f : 1.f / l_run[h];
                     T* orow = out + row * D + d0;
 #pragma unroll
                     for (int mt = 0; mt < KS; ++mt) {
@@ -868,7 +919,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                     }
                 }
             }
-            if (nseg > 1) {
+            if (nseg > 1 && !two_tiles) {
                 // publish this piece, count it; the last of the stream's
                 // pieces to arrive merges them all
                 __threadfence();
@@ -879,9 +930,24 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
                     __threadfence();
-                    merge_stream<T, D>(out, ws_o, ws_m, ws_l, (int64_t)w.s * H + h0, GH, max_segs,
-                                       nseg, lane);
+                    merge_stream<T, D>(out, ws_o, ws_m, ws_l, w.s, h0, H, nq, GH, 0,
+                                       max_segs, nseg, lane);
                 }
+            }
+        }
+        if (two_tiles && nseg > 1) {
+            // both tile warps have written their rows of the piece before it
+            // is counted; then both merge their own tile if it was the last
+            volatile int32_t* last_flag = reinterpret_cast<int32_t*>(smem + L::kMisc + 8);
+            __threadfence();
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+            if (warp == 0 && lane == 0)
+                *last_flag = arrive_piece(ws_cnt + (int64_t)w.s * units + w.u, tag, nseg) ? 1 : 0;
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+            if ((warp & 1) == 0 && *last_flag) {
+                __threadfence();
+                merge_stream<T, D>(out, ws_o, ws_m, ws_l, w.s, h0, H, nq, GH, col0, max_segs,
+                                   nseg, lane);
             }
         }
         // the exchange buffer is rewritten by the next piece's merge
@@ -949,12 +1015,16 @@ int sm_count(int dev) {
     return counts[dev];
 }
 
-template <typename T, int D, bool kF8>
+template <typename T, int D, bool kF8, bool kMQ>
 pd_status launch_decode_t(const DecodeArgs& a) {
     using Lt = DecodeSmem<D, kF8>;
     const int G = a.H / a.Hk;
-    int GH = 1;                          // largest divisor of G that fits N = 8
-    for (int g = std::min(G, kHeadsN); g >= 1; --g)
+    const int nq = kMQ ? a.nq : 1;
+    // largest divisor of G whose columns fit: GH <= 8 for decode, GH * nq <= 16
+    // (two tiles of N = 8) for verification
+    const int max_cols = kMQ ? 2 * kHeadsN : kHeadsN;
+    int GH = 1;
+    for (int g = std::min(G, max_cols / nq); g >= 1; --g)
         if (G % g == 0) { GH = g; break; }
     CUtensorMap tm_k, tm_v;
     const unsigned long long rows = (unsigned long long)a.NB * a.Hk * a.S;
@@ -964,7 +1034,7 @@ pd_status launch_decode_t(const DecodeArgs& a) {
                              : (encode_pool_map(&tm_k, a.key_cache, D, rows, a.S, a.dt) &&
                                 encode_pool_map(&tm_v, a.value_cache, D, rows, a.S, a.dt));
     if (!maps_ok) return launch_result(cudaErrorInvalidValue);
-    auto kern = paged_decode_split_kernel<T, D, kF8>;
+    auto kern = paged_decode_split_kernel<T, D, kF8, kMQ>;
     static uint64_t attr_set = 0;   // one bit per device; benign if raced
     int dev = 0;
     cudaError_t e0 = cudaGetDevice(&dev);
@@ -976,7 +1046,7 @@ pd_status launch_decode_t(const DecodeArgs& a) {
         if (dev < 64) attr_set |= uint64_t(1) << dev;
     }
     const int P = decode_num_partitions(a.max_context_len);   // pieces per stream, at most
-    const WsLayout w = ws_layout(a.B, a.H, a.D, P);
+    const WsLayout w = ws_layout(a.B * nq, a.H, a.D, P);
     char* base = static_cast<char*>(a.workspace);
     float* ws_o = reinterpret_cast<float*>(base + w.o);
     float* ws_m = reinterpret_cast<float*>(base + w.m);
@@ -1000,16 +1070,17 @@ pd_status launch_decode_t(const DecodeArgs& a) {
     return launch_result(cudaLaunchKernelEx(
         &cfg, kern, tm_k, tm_v, static_cast<T*>(a.out), static_cast<const T*>(a.q),
         a.block_tables, a.max_blocks_per_seq, a.context_lens, a.B, a.H, a.Hk, a.S, a.NB, GH,
-        scale_log2, P, cap, ws_o, ws_m, ws_l, ws_cnt, next_launch_tag(), a.k_scale, a.v_scale,
+        nq, scale_log2, P, cap, ws_o, ws_m, ws_l, ws_cnt, next_launch_tag(), a.k_scale, a.v_scale,
         a.dev_err));
 }
 
-template <bool kF8>
+template <bool kF8, bool kMQ>
 pd_status launch_decode_dt(const DecodeArgs& a) {
     if (a.dt == PD_BF16)
-        return a.D == 128 ? launch_decode_t<__nv_bfloat16, 128, kF8>(a)
-                          : launch_decode_t<__nv_bfloat16, 64, kF8>(a);
-    return a.D == 128 ? launch_decode_t<__half, 128, kF8>(a) : launch_decode_t<__half, 64, kF8>(a);
+        return a.D == 128 ? launch_decode_t<__nv_bfloat16, 128, kF8, kMQ>(a)
+                          : launch_decode_t<__nv_bfloat16, 64, kF8, kMQ>(a);
+    return a.D == 128 ? launch_decode_t<__half, 128, kF8, kMQ>(a)
+                      : launch_decode_t<__half, 64, kF8, kMQ>(a);
 }
 
 }  // namespace
@@ -1032,7 +1103,8 @@ size_t decode_workspace_bytes(int B, int H, int D, int max_context_len) {
 }
 
 pd_status launch_decode(const DecodeArgs& a) {
-    return a.fp8 ? launch_decode_dt<true>(a) : launch_decode_dt<false>(a);
+    if (a.nq > 1) return a.fp8 ? PD_ERR_UNSUPPORTED : launch_decode_dt<false, true>(a);
+    return a.fp8 ? launch_decode_dt<true, false>(a) : launch_decode_dt<false, false>(a);
 }
 
 }  // namespace pd

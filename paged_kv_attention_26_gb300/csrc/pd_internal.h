@@ -45,6 +45,7 @@ struct DecodeArgs {
     const float* k_scale = nullptr;   // ... standing for code * scale[kv head]
     const float* v_scale = nullptr;
     bool pdl = false;            // launch as a programmatic dependent of the previous grid
+    int nq = 1;                  // query tokens per sequence (> 1: speculative verification)
 };
 pd_status launch_decode(const DecodeArgs& a);
 

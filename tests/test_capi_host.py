@@ -144,6 +144,33 @@ def test_decode_step_validation(lib):
     assert lib.pd_launch_count() == n0
 
 
+def test_verify_validation(lib):
+    f = lib.pd_paged_attention_verify
+    base = [P, P, P, P, P, 8, P, 4, 4, 8, 2, 64, 16, 64, 100, 0.125, None, 0, pd.PD_F16, None,
+            None]
+    cases = [
+        ({8: 0}, 2),           # nq < 1
+        ({8: 9}, 2),           # nq > 8
+        ({7: 20000}, 2),       # B * nq > 65535
+        ({9: 6}, 1),           # H % Hk
+        ({11: 80}, 2),         # D
+        ({0: 0}, 1),           # null out
+    ]
+    n0 = lib.pd_launch_count()
+    for change, want in cases:
+        a = list(base)
+        for k, v in change.items():
+            a[k] = v
+        assert f(*a) == want, change
+    # the workspace is sized for B * nq query rows
+    a = list(base)
+    a[14] = 5000
+    need = lib.pd_decode_workspace_bytes(4 * 4, 8, 64, 5000)
+    a[16], a[17] = P, lib.pd_decode_workspace_bytes(4, 8, 64, 5000)
+    assert a[17] < need and f(*a) == 5          # enough for decode, not for verify
+    assert lib.pd_launch_count() == n0
+
+
 def test_workspace_size_formula(lib):
     part = lib.pd_decode_partition_tokens(10000)
     assert part % 64 == 0
