@@ -504,6 +504,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     const float2 neg1 = make_float2(-1.f, -1.f);
     uint32_t gs = 0;                             // stages consumed so far
     bool aborted = false;
+    const bool two_tiles = kMQ && ctiles == 2;
 
     while (w.pos < w.end) {
         // ---- one stream piece: stages [w.off, min(w.L, w.off + w.end - w.pos)) of (s, u)
@@ -731,18 +732,21 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 if (lane == 0) mbar_arrive(&empty[slot]);
               }
             } else {
-              for (int sub = 0; sub < (kMQ ? ctiles : 1); ++sub) {
-                const int tbs = tb + 16 * sub;           // 16 tokens of this warp
-                if (tbs >= nt) break;
+              // NS sub-tiles of 16 tokens (tb .. tb + 16 NS - 1) processed together:
+              // their products interleave and share one max, rescale and shuffle
+              // round; NS = 1 is the decode layout, NS = 2 the two-tile verify one
+              auto body = [&](auto ns_c) {
+                constexpr int NS = decltype(ns_c)::value;
+                if (tb >= nt) return;
                 const uint32_t kb = k_base0 + tslot * L::kTile;
                 const uint32_t vb = v_base0 + tslot * L::kTile;
-                const bool partial = tbs + 16 > nt;
+                const bool partial = tb + 16 * NS > nt;
                 if (partial) {
                     // V rows past the context end hold other data or were never
                     // loaded this round: zero them so that 0 * v stays 0.
                     unsigned char* vrow = smem + L::kV + tslot * L::kTile;
-                    for (int i = lane; i < 16 * kAtoms * 8; i += 32) {
-                        const int tok = tbs + i / (kAtoms * 8);
+                    for (int i = lane; i < 16 * NS * kAtoms * 8; i += 32) {
+                        const int tok = tb + i / (kAtoms * 8);
                         if (tok >= nt) {
                             const int a = (i / 8) % kAtoms, c = i % 8;
                             *reinterpret_cast<uint4*>(vrow + a * L::kAtom + tok * 128 + c * 16) =
@@ -751,25 +755,40 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                     }
                     __syncwarp();
                 }
-                // ---- S^T[16 tokens][8 heads] = K q^T (two accumulators for ILP)
-                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                // ---- S^T[16 tokens][8 columns] = K q^T per sub-tile (two accumulators each)
+                float acc[NS][2][4];
+#pragma unroll
+                for (int sb = 0; sb < NS; ++sb)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[sb][0][e] = acc[sb][1][e] = 0.f;
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
-                    uint32_t a[4];
-                    wmma16::ldsm_x4(a, swz<D>(kb, tbs + r8 + 8 * (j8 & 1), 2 * ks + (j8 >> 1)));
-                    wmma16::Mma<TM>::run(acc[ks & 1], a, qb[ks][0], qb[ks][1]);
-                }
-                // lane holds tokens tbs + lane/4 (0,1) and + 8 (2,3); heads 2(lane%4) + {0,1}
-                const int tok0 = tbs + (lane >> 2);
-                float x[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int tok = tok0 + (i >> 1) * 8;
-                    x[i] = tok < (kMQ ? rem - dj[i & 1] : nt) ? (acc[0][i] + acc[1][i]) * sl2
-                                                                : -INFINITY;
+                    for (int sb = 0; sb < NS; ++sb) {
+                        uint32_t a[4];
+                        wmma16::ldsm_x4(a, swz<D>(kb, tb + 16 * sb + r8 + 8 * (j8 & 1),
+                                                  2 * ks + (j8 >> 1)));
+                        wmma16::Mma<TM>::run(acc[sb][ks & 1], a, qb[ks][0], qb[ks][1]);
+                    }
                 }
-                // ---- online softmax per head (lane-local state, 3 shuffles per head)
-                float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+                // lane holds tokens tb + 16 sb + lane/4 (0,1) and + 8 (2,3); columns
+                // 2(lane%4) + {0,1}
+                float x[NS][4];
+#pragma unroll
+                for (int sb = 0; sb < NS; ++sb)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int tok = tb + 16 * sb + (lane >> 2) + (i >> 1) * 8;
+                        x[sb][i] = tok < (kMQ ? rem - dj[i & 1] : nt)
+                                       ? (acc[sb][0][i] + acc[sb][1][i]) * sl2 : -INFINITY;
+                    }
+                // ---- online softmax per column (lane-local state, 3 shuffles per column)
+                float mx[2] = {fmaxf(x[0][0], x[0][2]), fmaxf(x[0][1], x[0][3])};
+#pragma unroll
+                for (int sb = 1; sb < NS; ++sb) {
+                    mx[0] = fmaxf(mx[0], fmaxf(x[sb][0], x[sb][2]));
+                    mx[1] = fmaxf(mx[1], fmaxf(x[sb][1], x[sb][3]));
+                }
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) {
                     mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
@@ -791,26 +810,49 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 // a verify column may not have seen a key yet (m = -inf): its p are 0
                 const float mu0 = kMQ && m_run[0] == -INFINITY ? 0.f : m_run[0];
                 const float mu1 = kMQ && m_run[1] == -INFINITY ? 0.f : m_run[1];
-                const float p0 = ex2(x[0] - mu0), p1 = ex2(x[1] - mu1);
-                const float p2 = ex2(x[2] - mu0), p3 = ex2(x[3] - mu1);
-                l_run[0] += p0 + p2;
-                l_run[1] += p1 + p3;
-                // P as hi + lo 16-bit pairs, transposed into B-operand layout
-                const uint32_t hi0 = E::pack2(p0, p1), hi1 = E::pack2(p2, p3);
-                const float2 lo0 = ffma2(E::unpack2(hi0), neg1, make_float2(p0, p1));
-                const float2 lo1 = ffma2(E::unpack2(hi1), neg1, make_float2(p2, p3));
-                const uint32_t bh0 = wmma16::movm_t(hi0), bh1 = wmma16::movm_t(hi1);
-                const uint32_t bl0 = wmma16::movm_t(E::pack2(lo0.x, lo0.y));
-                const uint32_t bl1 = wmma16::movm_t(E::pack2(lo1.x, lo1.y));
-                // ---- O^T[dims][heads] += V^T P^T
+                uint32_t bh0[NS], bh1[NS], bl0[NS], bl1[NS];
+                float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+                for (int sb = 0; sb < NS; ++sb) {
+                    const float p0 = ex2(x[sb][0] - mu0), p1 = ex2(x[sb][1] - mu1);
+                    const float p2 = ex2(x[sb][2] - mu0), p3 = ex2(x[sb][3] - mu1);
+                    if (sb == 0) {
+                        ls0 = p0 + p2;
+                        ls1 = p1 + p3;
+                    } else {
+                        ls0 += p0 + p2;
+                        ls1 += p1 + p3;
+                    }
+                    // P as hi + lo 16-bit pairs, transposed into B-operand layout
+                    const uint32_t hi0 = E::pack2(p0, p1), hi1 = E::pack2(p2, p3);
+                    const float2 lo0 = ffma2(E::unpack2(hi0), neg1, make_float2(p0, p1));
+                    const float2 lo1 = ffma2(E::unpack2(hi1), neg1, make_float2(p2, p3));
+                    bh0[sb] = wmma16::movm_t(hi0);
+                    bh1[sb] = wmma16::movm_t(hi1);
+                    bl0[sb] = wmma16::movm_t(E::pack2(lo0.x, lo0.y));
+                    bl1[sb] = wmma16::movm_t(E::pack2(lo1.x, lo1.y));
+                }
+                l_run[0] += ls0;
+                l_run[1] += ls1;
+                // ---- O^T[dims][columns] += V^T P^T
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
-                    uint32_t a[4];
-                    wmma16::ldsm_x4_t(a, swz<D>(vb, tbs + r8 + 8 * (j8 >> 1), 2 * mt + (j8 & 1)));
-                    wmma16::Mma<TM>::run(o[mt], a, bh0, bh1);
-                    wmma16::Mma<TM>::run(o[mt], a, bl0, bl1);
+#pragma unroll
+                    for (int sb = 0; sb < NS; ++sb) {
+                        uint32_t a[4];
+                        wmma16::ldsm_x4_t(a, swz<D>(vb, tb + 16 * sb + r8 + 8 * (j8 >> 1),
+                                                    2 * mt + (j8 & 1)));
+                        wmma16::Mma<TM>::run(o[mt], a, bh0[sb], bh1[sb]);
+                        wmma16::Mma<TM>::run(o[mt], a, bl0[sb], bl1[sb]);
+                    }
                 }
                 if (partial && !kF8) tc::fence_proxy_async_smem();   // zeros before the next TMA write
+              };
+              if constexpr (kMQ) {
+                  if (ctiles == 2) body(std::integral_constant<int, 2>{});
+                  else body(std::integral_constant<int, 1>{});
+              } else {
+                  body(std::integral_constant<int, 1>{});
               }
             }
             __syncwarp();
@@ -861,7 +903,6 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                     o[mt][e] = o[mt][e] * c_mine[e & 1] + x[(mt * 4 + e) * 32] * c_other[e & 1];
         };
         // two column tiles: warp 1 hands over to 0 and warp 3 to 2 (same tile)
-        const bool two_tiles = kMQ && ctiles == 2;
         if (!two_tiles) {
             if (warp >= 2) put(warp - 2);
             asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
@@ -877,6 +918,11 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
             if (!(warp & 1)) take(warp >> 1);
         }
+        // The exchange buffer has been read: the other warps go on to the next
+        // piece while the warp(s) holding the result write it, publish it and
+        // perhaps merge the stream. They fall behind by that much and catch up
+        // on stages already in the ring (consuming is faster than streaming).
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
         if (two_tiles ? (warp & 1) == 0 : warp == 0) {
             if constexpr (kF8) {
                 const float vs = __ldg(v_scale + kvh);
@@ -935,23 +981,22 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
             }
         }
-        if (two_tiles && nseg > 1) {
-            // both tile warps have written their rows of the piece before it
-            // is counted; then both merge their own tile if it was the last
+        if (two_tiles && nseg > 1 && (warp & 1) == 0) {
+            // both tile warps (0 and 2, named barrier 2) have written their rows
+            // of the piece before it is counted; then both merge their own tile
+            // if it was the last
             volatile int32_t* last_flag = reinterpret_cast<int32_t*>(smem + L::kMisc + 8);
             __threadfence();
-            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+            asm volatile("bar.sync 2, 64;" ::: "memory");
             if (warp == 0 && lane == 0)
                 *last_flag = arrive_piece(ws_cnt + (int64_t)w.s * units + w.u, tag, nseg) ? 1 : 0;
-            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-            if ((warp & 1) == 0 && *last_flag) {
+            asm volatile("bar.sync 2, 64;" ::: "memory");
+            if (*last_flag) {
                 __threadfence();
                 merge_stream<T, D>(out, ws_o, ws_m, ws_l, w.s, h0, H, nq, GH, col0, max_segs,
                                    nseg, lane);
             }
         }
-        // the exchange buffer is rewritten by the next piece's merge
-        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
         w.off += piece_stages;
         w.pos += piece_stages;
         if (w.off == w.L && w.pos < w.end) walk_next_stream(w, context_lens, B, units, cap);
