@@ -553,6 +553,24 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
             }
         }
+        // The next piece's q rows into L1 now, so that its loads at the piece
+        // switch hit instead of waiting on HBM: the next stream of the range is
+        // (s, u + 1), or unit 0 of sequence s + 1 (an empty one is skipped by
+        // the walk, so that prefetch is merely wasted).
+        if (piece_stages < w.end - w.pos) {
+            const int nu = w.u + 1 < units ? w.u + 1 : 0;
+            const int ns = w.u + 1 < units ? w.s : w.s + 1;
+            if (ns < B) {
+                const int n = col0 + (lane >> 2);
+                const int qh = n / nq, qj = n - qh * nq;
+                if (qh < GH) {
+                    const int nh0 = (nu / groups) * G + (nu % groups) * GH;
+                    const T* nrow = q + (((int64_t)ns * nq + qj) * H + nh0 + qh) * D;
+                    // the column's four lanes cover its row (D / 4 values each)
+                    asm volatile("prefetch.global.L1 [%0];" ::"l"(nrow + (lane & 3) * (D / 4)));
+                }
+            }
+        }
         // FP8 pools: the K scale joins the softmax scale, the V scale the output
         // (K is widened to fp16 scaled by 2^-8: the 2^8 comes back here)
         const float sl2 = kF8 ? scale_log2 * 256.f * __ldg(k_scale + kvh) : scale_log2;
