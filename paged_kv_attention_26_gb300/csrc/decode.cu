@@ -109,15 +109,22 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int tok, int chunk) {
            (((chunk & 7) ^ (tok & 7)) << 4);
 }
 
-// Stream walk shared by the producer and the consumers.  Streams are ordered
-// sequence-major, unit-minor; stream (s, u) has L_s = ceil(ctx_s / 64) stages
-// and starts at global stage units * (sum of L over earlier sequences) + u * L_s.
+// Stream walk shared by the producer and the consumers.  The grid is split
+// into one group of CTAs per unit (kv head, head group): CTA b works on unit
+// b % units as member b / units of that group.  Within a unit the streams are
+// ordered by sequence; stream (s, u) has L_s = ceil(ctx_s / 64) stages and
+// starts at stage (sum of L over earlier sequences) of the unit's order, and
+// the group cuts that order into equal contiguous ranges.  Members with the
+// same index in every group therefore walk the same blocks at the same time,
+// one head slab each, and a block's slabs lie side by side in the pool, so
+// DRAM sees its neighbouring slabs read together.
 struct Walk {
     int s, u, L, ctx;     // current stream and its sequence's stage count / tokens
-    long start;           // global stage index of the stream's first stage
+    long start;           // stage index (in the unit's order) of the stream's first stage
     int off;              // next stage within the stream
-    long pos, end;        // next global stage; end of this CTA's range
+    long pos, end;        // next stage; end of this CTA's range
     long per_cta;
+    int bi;               // this CTA's index within its unit group
 };
 
 __device__ __forceinline__ int stream_ctx(const int32_t* __restrict__ context_lens, int s,
@@ -130,25 +137,28 @@ __device__ __forceinline__ int stream_ctx(const int32_t* __restrict__ context_le
 __device__ __forceinline__ bool walk_begin(Walk& w, const int32_t* __restrict__ context_lens,
                                            int B, int units, int cap) {
     const int lane = threadIdx.x & 31;
-    long total = 0;
+    const int members = gridDim.x / units;          // CTAs per unit group (>= 1)
+    w.u = blockIdx.x % units;
+    w.bi = blockIdx.x / units;
+    long total = 0;                                 // stages of one unit
     for (int base = 0; base < B; base += 32) {
         const int s = base + lane;
-        const long v = s < B ? long(units) * ((stream_ctx(context_lens, s, cap) + 63) / 64) : 0;
+        const long v = s < B ? long((stream_ctx(context_lens, s, cap) + 63) / 64) : 0;
         total += v;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-    const long even = (total + gridDim.x - 1) / gridDim.x;
+    const long even = (total + members - 1) / members;
     w.per_cta = even > kMinStagesPerCta ? even : long(kMinStagesPerCta);
-    const long r0 = long(blockIdx.x) * w.per_cta;
+    const long r0 = long(w.bi) * w.per_cta;
     w.end = total < r0 + w.per_cta ? total : r0 + w.per_cta;
-    if (r0 >= total) return false;
-    // find the sequence whose streams contain r0
+    if (w.bi >= members || r0 >= total) return false;
+    // find the sequence whose stream contains r0
     long prefix = 0;
     for (int base = 0; base < B; base += 32) {
         const int s = base + lane;
         const int ctx = s < B ? stream_ctx(context_lens, s, cap) : 0;
-        const long v = long(units) * ((ctx + 63) / 64);
+        const long v = long((ctx + 63) / 64);
         long incl = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -161,10 +171,8 @@ __device__ __forceinline__ bool walk_begin(Walk& w, const int32_t* __restrict__ 
             const int src = __ffs(m) - 1;
             w.s = base + src;
             w.ctx = __shfl_sync(0xffffffffu, ctx, src);
-            const long before = prefix + __shfl_sync(0xffffffffu, incl - v, src);
+            w.start = prefix + __shfl_sync(0xffffffffu, incl - v, src);
             w.L = (w.ctx + 63) / 64;
-            w.u = int((r0 - before) / w.L);
-            w.start = before + long(w.u) * w.L;
             w.off = int(r0 - w.start);
             w.pos = r0;
             return true;
@@ -177,16 +185,14 @@ __device__ __forceinline__ bool walk_begin(Walk& w, const int32_t* __restrict__ 
 // After the current stream is exhausted, move to the next non-empty one.
 __device__ __forceinline__ void walk_next_stream(Walk& w, const int32_t* __restrict__ context_lens,
                                                  int B, int units, int cap) {
+    (void)units;
     w.start += w.L;
     w.off = 0;
-    if (++w.u == units) {
-        w.u = 0;
-        do {
-            ++w.s;
-            w.ctx = w.s < B ? stream_ctx(context_lens, w.s, cap) : 0;
-        } while (w.s < B && w.ctx == 0);
-        w.L = (w.ctx + 63) / 64;
-    }
+    do {
+        ++w.s;
+        w.ctx = w.s < B ? stream_ctx(context_lens, w.s, cap) : 0;
+    } while (w.s < B && w.ctx == 0);
+    w.L = (w.ctx + 63) / 64;
 }
 
 // OR of `pred` over the consumer warps (named barrier 1), uniform result.
@@ -515,7 +521,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         const long c_first = w.start / w.per_cta;
         const long c_last = (w.start + w.L - 1) / w.per_cta;
         const int nseg = int(c_last - c_first + 1);
-        const int seg = int(long(blockIdx.x) - c_first);
+        const int seg = int(long(w.bi) - c_first);
         // q^T as the MMA B operand: lane holds head lane/4, dims 16ks + 2(lane%4) + {0,1}
         // (register 0) and the same + 8 (register 1); heads past GH are zero.
         uint32_t qb[KS][2];
@@ -555,11 +561,11 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
         // The next piece's q rows into L1 now, so that its loads at the piece
         // switch hit instead of waiting on HBM: the next stream of the range is
-        // (s, u + 1), or unit 0 of sequence s + 1 (an empty one is skipped by
-        // the walk, so that prefetch is merely wasted).
+        // (s + 1, u) (an empty sequence is skipped by the walk, so that prefetch
+        // is merely wasted).
         if (piece_stages < w.end - w.pos) {
-            const int nu = w.u + 1 < units ? w.u + 1 : 0;
-            const int ns = w.u + 1 < units ? w.s : w.s + 1;
+            const int nu = w.u;                         // same unit, next sequence
+            const int ns = w.s + 1;
             if (ns < B) {
                 const int n = col0 + (lane >> 2);
                 const int qh = n / nq, qj = n - qh * nq;
@@ -587,9 +593,13 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
         for (int h = 0; h < 2; ++h) dj[h] = kMQ ? nq - 1 - (col0 + 2 * (lane & 3) + h) % nq : 0;
 
-        for (int st = 0; st < piece_stages; ++st, ++gs) {
+        for (int st = 0; st < piece_stages;) {
+            // the native FP8 path takes two stages of the piece at a time
+            const int nst = (kNative && st + 1 < piece_stages) ? 2 : 1;
             const int slot = gs % kStages;
-            if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (gs / kStages) & 1))) {
+            bool got = mbar_wait(&full[slot], (gs / kStages) & 1);
+            if (nst == 2) got = got && mbar_wait(&full[(gs + 1) % kStages], ((gs + 1) / kStages) & 1);
+            if (!__all_sync(0xffffffffu, got)) {
                 if (lane == 0) {
                     flag_error(dev_err, PD_DEVERR_TIMEOUT);
                     *abort_flag = 1;
@@ -645,45 +655,80 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 if (lane == 0) mbar_arrive(&empty[slot]);
             }
             if constexpr (kNative) {
-              if (tb < nt) {
-                // ---- fragments straight from the raw E4M3 stage (128-byte rows,
-                // swizzled): ldmatrix moves bytes, the conversion happens in registers
-                const uint32_t k8 = smem_u32(smem + L::kK8 + slot * L::kTile8);
-                const uint32_t v8 = smem_u32(smem + L::kV8 + slot * L::kTile8);
-                const int lrow = tb + r8 + 8 * (j8 & 1);
-                uint32_t kr[D / 32][4], vr[D / 32][4];
+              // NS consecutive stages of the piece (their slots are consecutive
+              // in the ring): this warp's 16 tokens of each, processed together
+              auto nbody = [&](auto ns_c) {
+                constexpr int NS = decltype(ns_c)::value;
+                int nts[NS];
+                uint32_t k8[NS], v8[NS];
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    wmma16::ldsm_x4(kr[c], swz128(k8, lrow, 2 * c + (j8 >> 1)));
-                    wmma16::ldsm_x4_t(vr[c], swz128(v8, lrow, 2 * c + (j8 >> 1)));
+                for (int sb = 0; sb < NS; ++sb) {
+                    const int sl = (gs + sb) % kStages;
+                    nts[sb] = min(kStageTokens, rem - sb * kStageTokens);
+                    k8[sb] = smem_u32(smem + L::kK8 + sl * L::kTile8);
+                    v8[sb] = smem_u32(smem + L::kV8 + sl * L::kTile8);
                 }
+                // a second stage exists only after a full first one, so a warp
+                // without tokens in the first stage has none in the second
+                if (tb >= nts[0]) {
+                    __syncwarp();
+                    if (lane == 0)
+                        for (int sb = 0; sb < NS; ++sb) mbar_arrive(&empty[(gs + sb) % kStages]);
+                    return;
+                }
+                // ---- fragments straight from the raw E4M3 stages (128-byte rows,
+                // swizzled): ldmatrix moves bytes, the conversion happens in registers
+                const int lrow = tb + r8 + 8 * (j8 & 1);
+                uint32_t kr[NS][D / 32][4], vr[NS][D / 32][4];
+#pragma unroll
+                for (int sb = 0; sb < NS; ++sb)
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        wmma16::ldsm_x4(kr[sb][c], swz128(k8[sb], lrow, 2 * c + (j8 >> 1)));
+                        wmma16::ldsm_x4_t(vr[sb][c], swz128(v8[sb], lrow, 2 * c + (j8 >> 1)));
+                    }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[slot]);     // the raw stage is free
+                if (lane == 0)                               // the raw stages are free
+                    for (int sb = 0; sb < NS; ++sb) mbar_arrive(&empty[(gs + sb) % kStages]);
                 // ---- S^T = K q^T: register j of block c holds row g (+8 for odd j),
                 // bytes 4t..4t+3 of dims 32c + 16 (j / 2) ..; K is widened as 2^-8 K
-                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                float acc[NS][2][4];
+#pragma unroll
+                for (int sb = 0; sb < NS; ++sb)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[sb][0][e] = acc[sb][1][e] = 0.f;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
-                        uint32_t a[4];
-                        a[0] = e4m3x2_to_f16x2_scaled<0x1404u>(kr[c][2 * h2]);
-                        a[1] = e4m3x2_to_f16x2_scaled<0x1404u>(kr[c][2 * h2 + 1]);
-                        a[2] = e4m3x2_to_f16x2_scaled<0x3424u>(kr[c][2 * h2]);
-                        a[3] = e4m3x2_to_f16x2_scaled<0x3424u>(kr[c][2 * h2 + 1]);
-                        const int ks = 2 * c + h2;
-                        wmma16::Mma<TM>::run(acc[ks & 1], a, qb[ks][0], qb[ks][1]);
+#pragma unroll
+                        for (int sb = 0; sb < NS; ++sb) {
+                            uint32_t a[4];
+                            a[0] = e4m3x2_to_f16x2_scaled<0x1404u>(kr[sb][c][2 * h2]);
+                            a[1] = e4m3x2_to_f16x2_scaled<0x1404u>(kr[sb][c][2 * h2 + 1]);
+                            a[2] = e4m3x2_to_f16x2_scaled<0x3424u>(kr[sb][c][2 * h2]);
+                            a[3] = e4m3x2_to_f16x2_scaled<0x3424u>(kr[sb][c][2 * h2 + 1]);
+                            const int ks = 2 * c + h2;
+                            wmma16::Mma<TM>::run(acc[sb][ks & 1], a, qb[ks][0], qb[ks][1]);
+                        }
                     }
                 }
                 const int tok0 = tb + (lane >> 2);
-                float x[4];
+                float x[NS][4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int tok = tok0 + (i >> 1) * 8;
-                    x[i] = tok < (kMQ ? rem - dj[i & 1] : nt) ? (acc[0][i] + acc[1][i]) * sl2
-                                                                : -INFINITY;
+                for (int sb = 0; sb < NS; ++sb)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int tok = tok0 + (i >> 1) * 8;
+                        x[sb][i] = tok < nts[sb] ? (acc[sb][0][i] + acc[sb][1][i]) * sl2
+                                                 : -INFINITY;
+                    }
+                float mx[2] = {fmaxf(x[0][0], x[0][2]), fmaxf(x[0][1], x[0][3])};
+#pragma unroll
+                for (int sb = 1; sb < NS; ++sb) {
+                    mx[0] = fmaxf(mx[0], fmaxf(x[sb][0], x[sb][2]));
+                    mx[1] = fmaxf(mx[1], fmaxf(x[sb][1], x[sb][3]));
                 }
-                float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
 #pragma unroll
                 for (int off = 4; off < 32; off <<= 1) {
                     mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
@@ -702,53 +747,65 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         }
                     }
                 }
-                // a verify column may not have seen a key yet (m = -inf): its p are 0
-                const float mu0 = kMQ && m_run[0] == -INFINITY ? 0.f : m_run[0];
-                const float mu1 = kMQ && m_run[1] == -INFINITY ? 0.f : m_run[1];
-                const float p0 = ex2(x[0] - mu0), p1 = ex2(x[1] - mu1);
-                const float p2 = ex2(x[2] - mu0), p3 = ex2(x[3] - mu1);
-                l_run[0] += p0 + p2;
-                l_run[1] += p1 + p3;
-                const uint32_t hi0 = E::pack2(p0, p1), hi1 = E::pack2(p2, p3);
-                const float2 lo0 = ffma2(E::unpack2(hi0), neg1, make_float2(p0, p1));
-                const float2 lo1 = ffma2(E::unpack2(hi1), neg1, make_float2(p2, p3));
-                const uint32_t bh0 = wmma16::movm_t(hi0), bh1 = wmma16::movm_t(hi1);
-                const uint32_t bl0 = wmma16::movm_t(E::pack2(lo0.x, lo0.y));
-                const uint32_t bl1 = wmma16::movm_t(E::pack2(lo1.x, lo1.y));
+                uint32_t bh0[NS], bh1[NS], bl0[NS], bl1[NS];
+                float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+                for (int sb = 0; sb < NS; ++sb) {
+                    const float p0 = ex2(x[sb][0] - m_run[0]), p1 = ex2(x[sb][1] - m_run[1]);
+                    const float p2 = ex2(x[sb][2] - m_run[0]), p3 = ex2(x[sb][3] - m_run[1]);
+                    if (sb == 0) {
+                        ls0 = p0 + p2;
+                        ls1 = p1 + p3;
+                    } else {
+                        ls0 += p0 + p2;
+                        ls1 += p1 + p3;
+                    }
+                    const uint32_t hi0 = E::pack2(p0, p1), hi1 = E::pack2(p2, p3);
+                    const float2 lo0 = ffma2(E::unpack2(hi0), neg1, make_float2(p0, p1));
+                    const float2 lo1 = ffma2(E::unpack2(hi1), neg1, make_float2(p2, p3));
+                    bh0[sb] = wmma16::movm_t(hi0);
+                    bh1[sb] = wmma16::movm_t(hi1);
+                    bl0[sb] = wmma16::movm_t(E::pack2(lo0.x, lo0.y));
+                    bl1[sb] = wmma16::movm_t(E::pack2(lo1.x, lo1.y));
+                }
+                l_run[0] += ls0;
+                l_run[1] += ls1;
                 // ---- O^T += V^T P^T: register j of block c holds tokens 2t, 2t+1
                 // (+8 for odd j) x dims 2g, 2g+1 of chunk 2c + j / 2; m-tile 2c + j/2
                 // has rows g -> dim 2g and g + 8 -> dim 2g + 1 of that chunk
-                const bool partial = tb + 16 > nt;
                 const int tk = tb + 2 * (lane & 3);
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
-                        uint32_t a[4];
-                        a[0] = e4m3_pair_to_f16x2<0x4420u>(vr[c][2 * h2]);
-                        a[1] = e4m3_pair_to_f16x2<0x4431u>(vr[c][2 * h2]);
-                        a[2] = e4m3_pair_to_f16x2<0x4420u>(vr[c][2 * h2 + 1]);
-                        a[3] = e4m3_pair_to_f16x2<0x4431u>(vr[c][2 * h2 + 1]);
-                        if (partial) {
-                            // tokens past the context: their V bytes are other data
-                            const uint32_t m01 = (tk < nt ? 0xffffu : 0u) |
-                                                 (tk + 1 < nt ? 0xffff0000u : 0u);
-                            const uint32_t m23 = (tk + 8 < nt ? 0xffffu : 0u) |
-                                                 (tk + 9 < nt ? 0xffff0000u : 0u);
-                            a[0] &= m01;
-                            a[1] &= m01;
-                            a[2] &= m23;
-                            a[3] &= m23;
+#pragma unroll
+                        for (int sb = 0; sb < NS; ++sb) {
+                            uint32_t a[4];
+                            a[0] = e4m3_pair_to_f16x2<0x4420u>(vr[sb][c][2 * h2]);
+                            a[1] = e4m3_pair_to_f16x2<0x4431u>(vr[sb][c][2 * h2]);
+                            a[2] = e4m3_pair_to_f16x2<0x4420u>(vr[sb][c][2 * h2 + 1]);
+                            a[3] = e4m3_pair_to_f16x2<0x4431u>(vr[sb][c][2 * h2 + 1]);
+                            if (tb + 16 > nts[sb]) {
+                                // tokens past the context: their V bytes are other data
+                                const int n = nts[sb];
+                                const uint32_t m01 = (tk < n ? 0xffffu : 0u) |
+                                                     (tk + 1 < n ? 0xffff0000u : 0u);
+                                const uint32_t m23 = (tk + 8 < n ? 0xffffu : 0u) |
+                                                     (tk + 9 < n ? 0xffff0000u : 0u);
+                                a[0] &= m01;
+                                a[1] &= m01;
+                                a[2] &= m23;
+                                a[3] &= m23;
+                            }
+                            const int mt = 2 * c + h2;
+                            wmma16::Mma<TM>::run(o[mt], a, bh0[sb], bh1[sb]);
+                            wmma16::Mma<TM>::run(o[mt], a, bl0[sb], bl1[sb]);
                         }
-                        const int mt = 2 * c + h2;
-                        wmma16::Mma<TM>::run(o[mt], a, bh0, bh1);
-                        wmma16::Mma<TM>::run(o[mt], a, bl0, bl1);
                     }
                 }
-              } else {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[slot]);
-              }
+              };
+              if (nst == 2) nbody(std::integral_constant<int, 2>{});
+              else nbody(std::integral_constant<int, 1>{});
             } else {
               // NS sub-tiles of 16 tokens (tb .. tb + 16 NS - 1) processed together:
               // their products interleave and share one max, rescale and shuffle
@@ -875,6 +932,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             }
             __syncwarp();
             if (!kF8 && lane == 0) mbar_arrive(&empty[slot]);
+            st += nst;
+            gs += nst;
         }
         // All four consumer warps decide together whether to go on: a warp
         // that gave up still arrives here, so named-barrier counts stay matched.
@@ -1118,8 +1177,11 @@ pd_status launch_decode_t(const DecodeArgs& a) {
     const float scale_log2 = a.scale * kLog2e;
     // contexts are cut to what the table holds and to the caller's promise
     const int cap = int(std::min<long>(long(a.max_blocks_per_seq) * a.S, a.max_context_len));
-    // persistent grid: two CTAs per SM (shared memory bound)
-    const unsigned grid = unsigned(2 * sm_count(dev));
+    // persistent grid: two CTAs per SM (shared memory bound), rounded down to
+    // a multiple of the units so that every unit group has the same size
+    const int units = a.Hk * (G / GH);
+    const int slots = 2 * sm_count(dev);
+    const unsigned grid = unsigned(units * std::max(1, slots / units));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kDecodeThreads);
