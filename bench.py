@@ -54,6 +54,9 @@ def parse_args():
                     "spec_verify,kv_handover",
                     help="comma-separated extra workloads to run after the headline")
     ap.add_argument("--extra-steps", type=int, default=10)
+    ap.add_argument("--only-extras", action="store_true",
+                    help="run only the --extras workloads and print their results (for "
+                         "profiling one kernel); not a benchmark line")
     return ap.parse_args()
 
 
@@ -280,31 +283,53 @@ def run_ours(args, rank, world, local_rank):
         result["cpu_baseline"] = cpu_baseline_decode(c, step_bytes, budget_s=10.0)
     wanted = [] if args.no_extras else [x for x in args.extras.split(",") if x]
     if world == 1 and wanted:
-        extras = {}
         del kc, vc
         torch.cuda.empty_cache()
-        if "chunked_prefill_mix" in wanted:
-            extras["chunked_prefill_mix"] = bench_prefill_mix(pd, pd_inputs, dev, args, flush,
-                                                              bf16_peak, hbm_peak, peak_src)
+        extras = run_extras(pd, pd_inputs, dev, args, flush, wanted, hbm_peak, bf16_peak,
+                            peak_src)
+        if "chunked_prefill_mix" in extras:
             pm = extras["chunked_prefill_mix"]
             result["prefill_tflops"] = pm["prefill_tflops"]
             result["prefill_pct_of_bf16_peak"] = round(100 * pm["prefill_frac"], 2)
-        if "long_context_32_layers" in wanted:
-            extras["long_context_32_layers"] = bench_long_context(pd, pd_inputs, dev, args,
-                                                                   flush, hbm_peak)
-        if "cow_fork_stress" in wanted:
-            extras["cow_fork_stress"] = bench_cow(pd, pd_inputs, dev, args, flush, hbm_peak)
-        if "fp8_decode" in wanted:
-            extras["fp8_decode"] = bench_fp8_decode(pd, pd_inputs, dev, args, flush, hbm_peak)
-        if "spec_verify" in wanted:
-            extras["spec_verify"] = bench_spec_verify(pd, pd_inputs, dev, args, flush, hbm_peak,
-                                                      bf16_peak)
-        if "kv_handover" in wanted:
-            extras["kv_handover"] = bench_kv_handover(pd, pd_inputs, dev, args, flush, hbm_peak)
         result["extras"] = extras
     if sampler is not None:
         result["clocks"] = sampler.stop()
     return result
+
+
+def run_extras(pd, pd_inputs, dev, args, flush, wanted, hbm_peak, bf16_peak, peak_src):
+    extras = {}
+    if "chunked_prefill_mix" in wanted:
+        extras["chunked_prefill_mix"] = bench_prefill_mix(pd, pd_inputs, dev, args, flush,
+                                                          bf16_peak, hbm_peak, peak_src)
+    if "long_context_32_layers" in wanted:
+        extras["long_context_32_layers"] = bench_long_context(pd, pd_inputs, dev, args,
+                                                               flush, hbm_peak)
+    if "cow_fork_stress" in wanted:
+        extras["cow_fork_stress"] = bench_cow(pd, pd_inputs, dev, args, flush, hbm_peak)
+    if "fp8_decode" in wanted:
+        extras["fp8_decode"] = bench_fp8_decode(pd, pd_inputs, dev, args, flush, hbm_peak)
+    if "spec_verify" in wanted:
+        extras["spec_verify"] = bench_spec_verify(pd, pd_inputs, dev, args, flush, hbm_peak,
+                                                  bf16_peak)
+    if "kv_handover" in wanted:
+        extras["kv_handover"] = bench_kv_handover(pd, pd_inputs, dev, args, flush, hbm_peak)
+    return extras
+
+
+def run_only_extras(args):
+    """The --extras workloads alone, on cuda:0 (a profiling aid)."""
+    import torch
+    import paged_kv_attention_26_gb300 as pd
+    import pd_inputs
+    pd.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    hbm_peak, bf16_peak, _, peak_src = peaks()
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    wanted = [x for x in args.extras.split(",") if x]
+    return {"only_extras": run_extras(pd, pd_inputs, dev, args, lambda: flush_buf.sum(), wanted,
+                                      hbm_peak, bf16_peak, peak_src)}
 
 
 def e2e_decode(pd, c, dev, args, step_bytes):
@@ -680,6 +705,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.only_extras:
+        print(json.dumps(run_only_extras(args)), flush=True)
+        return
     if args.impl == "reference":
         line = run_reference(args, rank, world)
         if line is not None:
