@@ -49,7 +49,8 @@ def test_single_token_context_returns_v_exactly(cuda_lib):
     assert torch.equal(out.cpu().view(torch.int16), want.view(torch.int16))
 
 
-@pytest.mark.parametrize("H,Hk", [(8, 8), (8, 1), (16, 2), (6, 2), (12, 2), (32, 8)])
+@pytest.mark.parametrize("H,Hk", [(8, 8), (8, 1), (16, 2), (6, 2), (12, 2), (32, 8), (12, 3),
+                                  (20, 5)])
 @pytest.mark.parametrize("D", [64, 128])
 def test_gqa_groupings(cuda_lib, H, Hk, D):
     c = pd_inputs.decode_case("gqa", 30 + H + Hk + D, [1, 31, 256, 257, 700], H, Hk, D, 16,
