@@ -147,6 +147,26 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------------
+# ranks: one replica of the workload per GPU (independent batches, no exchange)
+
+def rank_max(seconds: float, world: int, device) -> float:
+    """The slowest rank's timed seconds, on every rank (the job ends when the
+    last replica does)."""
+    if world <= 1:
+        return seconds
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(bytes_per_step: int, steps: int, seconds: float, world: int) -> float:
+    """GB/s of the whole job: every rank moved bytes_per_step per step of its
+    own batch, and the job took the slowest rank's time."""
+    return world * bytes_per_step * steps / seconds / 1e9
+
+
+# ---------------------------------------------------------------------------------
 # workload accounting
 
 def decode_alg_bytes(ctx, B, H, Hk, D, S, elem=2):
@@ -240,12 +260,9 @@ def run_ours(args, rank, world, local_rank):
         flush()
         decode_only()
     dec_s, _, _ = timed(decode_only)
-    if world > 1:
-        t = torch.tensor([step_s], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_s = float(t.item())
+    step_s = rank_max(step_s, world, dev)
     assert err.item() == 0, f"device error word {err.item()}"
-    value = world * step_bytes * args.steps / step_s / 1e9
+    value = whole_job_value(step_bytes, args.steps, step_s, world)
     ms_per_step = step_s / args.steps * 1e3
     dec_avg = dec_s / args.steps
     achieved = dec_bytes / dec_avg / 1e9
