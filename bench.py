@@ -254,12 +254,14 @@ def run_ours(args, rank, world, local_rank):
         return sum(a.elapsed_time(b) for a, b in ev) * 1e-3, wall, n
 
     # the headline: whole decode steps (store, then decode as a dependent grid)
-    step_s, t_wall, launches = timed(step)
+    with nvtx_range("decode_step"):
+        step_s, t_wall, launches = timed(step)
     # the roofline's kernel alone: the same decode launched by itself
-    for _ in range(args.warmup):
-        flush()
-        decode_only()
-    dec_s, _, _ = timed(decode_only)
+    with nvtx_range("decode_alone"):
+        for _ in range(args.warmup):
+            flush()
+            decode_only()
+        dec_s, _, _ = timed(decode_only)
     step_s = rank_max(step_s, world, dev)
     assert err.item() == 0, f"device error word {err.item()}"
     value = whole_job_value(step_bytes, args.steps, step_s, world)
@@ -296,7 +298,8 @@ def run_ours(args, rank, world, local_rank):
     }
 
     if rank == 0 and world == 1:
-        result["e2e"] = e2e_decode(pd, c, dev, args, step_bytes)
+        with nvtx_range("e2e"):
+            result["e2e"] = e2e_decode(pd, c, dev, args, step_bytes)
         result["cpu_baseline"] = cpu_baseline_decode(c, step_bytes, budget_s=10.0)
     wanted = [] if args.no_extras else [x for x in args.extras.split(",") if x]
     if world == 1 and wanted:
@@ -314,8 +317,31 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
+class nvtx_range:
+    """An NVTX range around one bench phase (seen by nsys/ncu timelines)."""
+
+    def __init__(self, name):
+        self.name = name
+
+    def __enter__(self):
+        import torch
+        torch.cuda.nvtx.range_push(self.name)
+
+    def __exit__(self, *exc):
+        import torch
+        torch.cuda.nvtx.range_pop()
+        return False
+
+
 def run_extras(pd, pd_inputs, dev, args, flush, wanted, hbm_peak, bf16_peak, peak_src):
     extras = {}
+    with nvtx_range("extras"):
+        _run_extras(extras, pd, pd_inputs, dev, args, flush, wanted, hbm_peak, bf16_peak,
+                    peak_src)
+    return extras
+
+
+def _run_extras(extras, pd, pd_inputs, dev, args, flush, wanted, hbm_peak, bf16_peak, peak_src):
     if "chunked_prefill_mix" in wanted:
         extras["chunked_prefill_mix"] = bench_prefill_mix(pd, pd_inputs, dev, args, flush,
                                                           bf16_peak, hbm_peak, peak_src)
@@ -331,7 +357,6 @@ def run_extras(pd, pd_inputs, dev, args, flush, wanted, hbm_peak, bf16_peak, pea
                                                   bf16_peak)
     if "kv_handover" in wanted:
         extras["kv_handover"] = bench_kv_handover(pd, pd_inputs, dev, args, flush, hbm_peak)
-    return extras
 
 
 def run_only_extras(args):

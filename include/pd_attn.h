@@ -251,6 +251,16 @@ PD_API pd_status pd_paged_attention_verify(void* out, const void* q,
                                            cudaStream_t stream);
 
 /* ---------------------------------------------------------------------- */
+/* pd_selftest_bounded_wait: exercises the in-kernel wait limit that every
+ * kernel of the library uses.  Launches one CTA that waits on a shared-memory
+ * barrier nothing completes; after limit_ns nanoseconds (1e3 .. 1e10) the
+ * wait gives up, PD_DEVERR_TIMEOUT is OR-ed into *dev_err (DEVICE int32,
+ * required) and the kernel returns, leaving the context usable.  For tests
+ * of failure detection; it faults, traps and hangs nothing. */
+PD_API pd_status pd_selftest_bounded_wait(int32_t* dev_err, uint64_t limit_ns,
+                                          cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
 /* One decode step of one layer: store the step's new K/V rows, then decode
  * attention that already sees them (nanoPD page, "模块结构与代码组织": the
  * attention layer writes the new token into its slot, then attends over the

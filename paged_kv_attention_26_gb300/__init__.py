@@ -65,6 +65,7 @@ SIGNATURES = {
                             _I, _I, _I, _I, _I, _F, _P, _SZ, _I, _P, _P]),
     "pd_decode_step_fp8": (_I, [_P, _P, _P, _I, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _I,
                                 _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _I, _P, _P]),
+    "pd_selftest_bounded_wait": (_I, [_P, ctypes.c_uint64, _P]),
     "pd_kv_pack": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pd_kv_unpack": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pd_paged_prefill_chunk": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
@@ -345,6 +346,16 @@ def pd_paged_attention_verify(out, q, key_cache, value_cache, block_tables, cont
 def verify_workspace(B, nq, H, D, max_context_len, device="cuda"):
     """Workspace for ``pd_paged_attention_verify`` (B sequences of nq queries)."""
     return decode_workspace(B * nq, H, D, max_context_len, device=device)
+
+
+def pd_selftest_bounded_wait(dev_err, limit_ns: int = 1_000_000, stream=None):
+    """One CTA waits on a barrier nothing completes; after ``limit_ns`` the
+    wait gives up and PD_DEVERR_TIMEOUT is OR-ed into ``dev_err`` (int32 CUDA
+    [1]), as in every kernel of the library.  A failure-detection test aid."""
+    torch = _torch()
+    st = load().pd_selftest_bounded_wait(_dev(dev_err, "dev_err", torch.int32), int(limit_ns),
+                                         _stream(stream))
+    _check("pd_selftest_bounded_wait", st)
 
 
 def pd_decode_step(out, q, key_cache, value_cache, block_tables, context_lens,

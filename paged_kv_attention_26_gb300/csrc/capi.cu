@@ -271,6 +271,11 @@ pd_status pd_paged_attention_verify(void* out, const void* q, const void* key_ca
     return launch_decode(a);
 }
 
+pd_status pd_selftest_bounded_wait(int32_t* dev_err, uint64_t limit_ns, cudaStream_t stream) {
+    if (!dev_err || limit_ns < 1000ull || limit_ns > 10000000000ull) return PD_ERR_INVALID_ARG;
+    return launch_bounded_wait_selftest(dev_err, (unsigned long long)limit_ns, stream);
+}
+
 pd_status pd_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,
                                    void* value_cache, const int64_t* slot_mapping, int T, int Hk,
                                    int D, int S, int NB, int64_t key_stride_tok,

@@ -60,14 +60,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete; false if the wait
-// ran past kWaitLimitNs (the caller then flags PD_DEVERR_TIMEOUT and leaves).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// ran past limit_ns (the caller then flags PD_DEVERR_TIMEOUT and leaves).
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+        if ((i & 255u) == 0 && globaltimer() - t0 > limit_ns) return false;
     }
+}
+
+// The wait every kernel of the library uses: bounded by kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 
 // ---- bulk copies (TMA engine, no tensor map) ---------------------------------

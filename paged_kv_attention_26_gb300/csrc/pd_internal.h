@@ -48,6 +48,8 @@ struct DecodeArgs {
     int nq = 1;                  // query tokens per sequence (> 1: speculative verification)
 };
 pd_status launch_decode(const DecodeArgs& a);
+pd_status launch_bounded_wait_selftest(int32_t* dev_err, unsigned long long limit_ns,
+                                       cudaStream_t stream);
 
 // ---- store / copy ----------------------------------------------------------------
 pd_status launch_reshape_and_cache(const void* key, const void* value, void* key_cache,

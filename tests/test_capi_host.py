@@ -171,6 +171,14 @@ def test_verify_validation(lib):
     assert lib.pd_launch_count() == n0
 
 
+def test_selftest_validation(lib):
+    n0 = lib.pd_launch_count()
+    assert lib.pd_selftest_bounded_wait(None, 1000000, None) == 1      # dev_err required
+    assert lib.pd_selftest_bounded_wait(P, 999, None) == 1             # limit too short
+    assert lib.pd_selftest_bounded_wait(P, 10**10 + 1, None) == 1      # limit too long
+    assert lib.pd_launch_count() == n0
+
+
 def test_workspace_size_formula(lib):
     part = lib.pd_decode_partition_tokens(10000)
     assert part % 64 == 0
