@@ -219,3 +219,14 @@ def test_workspace_contents_do_not_matter(cuda_lib):
     for o in outs[1:]:
         assert np.array_equal(o, outs[0])
     assert torch.isfinite(out.float()).all()
+
+
+def test_thousands_of_short_sequences(cuda_lib):
+    """3000 sequences of 0..40 tokens (a third empty): every CTA range crosses
+    many streams, and the walk scans the whole batch."""
+    g = torch.Generator().manual_seed(77)
+    ctx = torch.randint(0, 41, (3000,), generator=g)
+    ctx[::3] = 0
+    c = pd_inputs.decode_case("many", 77, ctx.tolist(), 8, 2, 64, 16, torch.bfloat16)
+    out = _check(cuda_lib, c, "3000 short")
+    assert (out[::3] == 0).all()

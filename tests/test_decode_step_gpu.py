@@ -204,3 +204,32 @@ def test_graph_replayed_decode_matches_eager(cuda_lib):
         graph.replay()
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+
+
+def test_step_with_padding_slots_and_more_tokens_than_sequences(cuda_lib):
+    """A step whose store carries padding slots (-1, skipped) and more rows
+    than sequences (T = 2B: each sequence's last two tokens), against the
+    separate calls and the oracle."""
+    pd = cuda_lib
+    c = pd_inputs.decode_case("pad", 69, [2, 40, 64, 65, 300], 16, 4, 128, 16, torch.float16,
+                              store_last=False)
+    B = c.B
+    g = torch.Generator().manual_seed(70)
+    seqs = torch.arange(B).repeat_interleave(2)
+    pos = (c.pool.context_lens.to(torch.int64) - 2).repeat_interleave(2) + torch.tensor([0, 1] * B)
+    slots = pd_inputs.slot_mapping_for(c.pool.block_tables, seqs, pos, 16)
+    slots[3] = -1                                     # a padding row: skipped
+    nk = torch.randn(2 * B, c.Hk, c.D, generator=g).to(torch.float16)
+    nv = torch.randn(2 * B, c.Hk, c.D, generator=g).to(torch.float16)
+    c.new_key, c.new_value, c.slot_mapping = nk, nv, slots
+    dev = torch.device("cuda")
+    err = device_err()
+    kc, vc = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
+    out = _step(pd, c, kc, vc, dev_err=err)
+    sep, kc2, vc2 = gpu_store_and_decode(pd, c)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.equal(out.view(torch.int16), sep.view(torch.int16))
+    ref, rk, rv = oracle_store_and_decode(c)
+    assert_close(out.cpu(), ref, "step with padding")
+    assert np.array_equal(u16(kc), rk) and np.array_equal(u16(vc), rv)
