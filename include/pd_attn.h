@@ -110,11 +110,13 @@ PD_API pd_status pd_reshape_and_cache(const void* key, const void* value,
  *   context_lens  int32 [B], each <= max_context_len (the caller's promise,
  *                 checked on device: PD_DEVERR_CTX_RANGE, the context is
  *                 then cut to max_context_len and to what the table holds)
- * One kernel launch.  The batch's work is cut into equal contiguous runs of
- * 64-token stages, one per resident CTA, so a long context may be split
- * across CTAs (online softmax per piece, pieces kept in `workspace`); the
- * CTA that finishes a context's last outstanding piece merges the pieces in
- * fixed order.  A context that one CTA finishes is written directly.
+ * One kernel launch.  The resident CTAs form one group per kv head (or
+ * head group); each group cuts that head's work over the batch into equal
+ * contiguous runs of 64-token stages, one per CTA, so a long context may be
+ * split across CTAs (online softmax per piece, pieces kept in `workspace`);
+ * the CTA that finishes a context's last outstanding piece merges the
+ * pieces in fixed order.  A context that one CTA finishes is written
+ * directly.
  *   workspace     device scratch of at least
  *                 pd_decode_workspace_bytes(B, H, D, max_context_len) bytes
  *                 (always > 0), 256-byte aligned.  Nothing in it needs to

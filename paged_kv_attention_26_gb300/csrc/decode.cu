@@ -9,19 +9,28 @@
 // Decode is HBM-bound (about one FLOP per byte per query head, tutorial page
 // section 1.1): the design streams every K/V byte once and keeps the
 // instruction count per byte low enough that issue never caps bandwidth.
-//  * work split (stream-K): each (sequence, kv head group) is a stream of
-//    64-token stages; the streams laid end to end are cut into equal
-//    contiguous ranges, one per persistent CTA (two per SM, at least 4
-//    stages each), so every CTA streams the same number of bytes.  A stream
-//    that fits inside one CTA's range is finished there; one that crosses
-//    range boundaries leaves one partial result per CTA for the reduce;
+//  * work split (stream-K per unit group): a unit is a kv head (or a group
+//    of its query heads); the persistent grid (two CTAs per SM) is split into
+//    one group of CTAs per unit, and each group cuts its unit's streams --
+//    one per sequence, 64-token stages, laid end to end -- into equal
+//    contiguous ranges of at least 4 stages, so every CTA streams the same
+//    number of bytes.  Members with the same index in every group walk the
+//    same blocks together, one head slab each (a block's slabs are adjacent
+//    in the pool).  A stream that fits inside one CTA's range is finished
+//    there; one that crosses range boundaries leaves one partial result per
+//    CTA for the merge;
 //  * one producer warp gathers K and V blocks with 2-D TMA boxes
 //    ([S tokens][64 dims], 128-byte swizzle) through the block table into a
-//    3-stage shared-memory ring, running ahead across stream boundaries;
+//    3-stage shared-memory ring (FP8 pools: raw one-byte stages, 6 deep),
+//    running ahead across stream boundaries; launched as a dependent of a
+//    store grid, it waits for that grid before its first copy;
 //  * four consumer warps take 16 tokens of each stage.  The G query heads
 //    that share the kv head form the N = 8 side of warp-level tensor-core
 //    products (mma.sync m16n8k16, fp32 accumulation): S^T = K q^T for 16
-//    tokens, then O^T += V^T P^T.  The fragment layouts line up so each lane
+//    tokens, then O^T += V^T P^T.  In verification mode the columns are
+//    (query head, query token) pairs with a causal limit per column, and
+//    with more than 8 columns the warps split into two column tiles of two
+//    warps, each warp taking 32 tokens of a stage.  The fragment layouts line up so each lane
 //    owns the same two heads in S and in O: the online softmax (log2 domain,
 //    lazy rescaling when a max grows by more than 2^8) needs only three
 //    shuffle steps per head pair and no broadcasts; P is transposed into
@@ -30,7 +39,8 @@
 //    (hi = rn(p), lo = rn(p - hi)), two MMAs per tile, so P carries about
 //    2^-17 relative error instead of the 2^-9 of a single bf16;
 //  * at the end of each stream piece the four warps merge through a small
-//    exchange buffer; a whole stream is normalised and written to `out`.
+//    exchange buffer (after which all but the result warp go on to the next
+//    piece); a whole stream is normalised and written to `out`.
 //    A piece of a longer stream leaves (max, sum, unnormalised o) in the
 //    workspace and counts itself on the stream's arrival counter; the CTA
 //    that brings the count to the number of pieces merges them all, in
