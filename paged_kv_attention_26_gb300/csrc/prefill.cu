@@ -131,11 +131,38 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
     volatile int32_t* v_issued = reinterpret_cast<volatile int32_t*>(smem + L::kMisc + 12);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int seq = blockIdx.z;
+    // Heaviest work first.  Blocks are dispatched in block-index order, so a
+    // block reads its z index as a rank among the batch's sequences sorted by
+    // causal work C (2P + C) (ties by index) and its x index from the last
+    // tile pair down: the last wave then holds the lightest tiles instead of
+    // whatever the batch order put there.  Every block ranks the batch
+    // itself (the ranks form a permutation whatever the values); batches of
+    // more than 256 sequences keep the launch order.
+    int seq = blockIdx.z;
+    if (gridDim.z > 1 && gridDim.z <= 256) {
+        __shared__ int picked;
+        auto work = [&](int j) -> long long {
+            const int c = __ldg(cu_q_lens + j + 1) - __ldg(cu_q_lens + j);
+            const int p = __ldg(context_lens + j) - c;
+            return (long long)c * (2LL * p + c);
+        };
+        const int t = threadIdx.x;
+        if (t < int(gridDim.z)) {
+            const long long wt = work(t);
+            int rank = 0;
+            for (int j = 0; j < int(gridDim.z); ++j) {
+                const long long wj = work(j);
+                rank += (wj > wt || (wj == wt && j < t)) ? 1 : 0;
+            }
+            if (rank == int(blockIdx.z)) picked = t;
+        }
+        __syncthreads();
+        seq = picked;
+    }
     const int TQ = kTileM / GP;                       // query tokens per tile
     const int q_begin = __ldg(cu_q_lens + seq);
     const int C = __ldg(cu_q_lens + seq + 1) - q_begin;
-    const int q0 = blockIdx.x * 2 * TQ;               // first chunk token of tile A
+    const int q0 = (gridDim.x - 1 - blockIdx.x) * 2 * TQ;   // first chunk token of tile A
     if (q0 >= C) return;
     const int ctx = __ldg(context_lens + seq);
     const int P = ctx - C;
