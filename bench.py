@@ -411,9 +411,10 @@ def e2e_decode(pd, c, dev, args, step_bytes):
     return {"value": round(step_bytes * args.steps / total / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(total / args.steps * 1e3, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "path": "DecodeStep replayed from a CUDA graph: one pinned host -> device copy of "
-                    "the step's inputs, pd_decode_step, device -> host copy of out, "
-                    "synchronize; host wall clock per step, L2 flushed before each",
+            "path": "DecodeStep replayed from a CUDA graph: pd_copy_bytes of the step's inputs "
+                    "from one pinned host buffer to the device, pd_decode_step, pd_copy_bytes of "
+                    "out to pinned host memory, synchronize; host wall clock per step, L2 "
+                    "flushed before each",
             "eager_value": round(step_bytes * args.steps / eager / 1e9, 2),
             "eager_ms_per_step": round(eager / args.steps * 1e3, 4)}
 

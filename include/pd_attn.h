@@ -253,6 +253,19 @@ PD_API pd_status pd_paged_attention_verify(void* out, const void* q,
                                            cudaStream_t stream);
 
 /* ---------------------------------------------------------------------- */
+/* pd_copy_bytes: copies `bytes` bytes from src to dst with an SM kernel on
+ * `stream`.  Each side may be device memory, managed memory, or pinned host
+ * memory mapped into the device's address space (cudaHostAlloc /
+ * cudaHostRegister); pageable host memory is refused.  Used to move a step's
+ * inputs and results between pinned host buffers and the device: many
+ * 16-byte loads in flight make a few-hundred-KB transfer link-bound rather
+ * than bound by a copy engine's per-transfer latency.
+ * Both pointers 16-byte aligned, bytes a multiple of 16; the ranges must not
+ * overlap.  PD_ERR_INVALID_ARG otherwise (nothing launched); bytes == 0
+ * launches nothing. */
+PD_API pd_status pd_copy_bytes(void* dst, const void* src, size_t bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
 /* pd_selftest_bounded_wait: exercises the in-kernel wait limit that every
  * kernel of the library uses.  Launches one CTA that waits on a shared-memory
  * barrier nothing completes; after limit_ns nanoseconds (1e3 .. 1e10) the

@@ -66,6 +66,7 @@ SIGNATURES = {
     "pd_decode_step_fp8": (_I, [_P, _P, _P, _I, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _I,
                                 _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _I, _P, _P]),
     "pd_selftest_bounded_wait": (_I, [_P, ctypes.c_uint64, _P]),
+    "pd_copy_bytes": (_I, [_P, _P, _SZ, _P]),
     "pd_kv_pack": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pd_kv_unpack": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pd_paged_prefill_chunk": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
@@ -348,6 +349,22 @@ def verify_workspace(B, nq, H, D, max_context_len, device="cuda"):
     return decode_workspace(B * nq, H, D, max_context_len, device=device)
 
 
+def pd_copy_bytes(dst, src, stream=None):
+    """Copy ``src`` into ``dst`` (same byte size, contiguous, 16-byte aligned,
+    a multiple of 16 bytes) with an SM kernel; either side may be a CUDA
+    tensor or a pinned host tensor."""
+    nb = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nb:
+        raise ValueError("size mismatch")
+    if not (dst.is_contiguous() and src.is_contiguous()):
+        raise ValueError("tensors must be contiguous")
+    for t in (dst, src):
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError("host tensors must be pinned")
+    st = load().pd_copy_bytes(dst.data_ptr(), src.data_ptr(), nb, _stream(stream))
+    _check("pd_copy_bytes", st)
+
+
 def pd_selftest_bounded_wait(dev_err, limit_ns: int = 1_000_000, stream=None):
     """One CTA waits on a barrier nothing completes; after ``limit_ns`` the
     wait gives up and PD_DEVERR_TIMEOUT is OR-ed into ``dev_err`` (int32 CUDA
@@ -419,7 +436,9 @@ class DecodeStep:
     int64 [T], ``block_tables`` int32 [B, max_blocks_per_seq],
     ``context_lens`` int32 [B]).  A call copies that buffer to the device in
     one transfer, runs ``pd_decode_step`` (store, then decode as a dependent
-    grid) and copies ``out`` back into the pinned ``host_out``.  With
+    grid) and copies ``out`` back into the pinned ``host_out``; both copies
+    are ``pd_copy_bytes`` (SM kernels reading and writing the pinned buffers
+    directly).  With
     ``graph=True`` those three operations are captured once in a CUDA graph
     and each call replays it; ``max_context_len`` and ``scale`` are fixed at
     construction (contexts may vary per call up to that bound).  One-byte
@@ -471,12 +490,12 @@ class DecodeStep:
 
     def _body(self):
         d = self.dev
-        self.dev_buf.copy_(self.host_buf, non_blocking=True)
+        pd_copy_bytes(self.dev_buf, self.host_buf)
         pd_decode_step(self.out, d["q"], self.key_cache, self.value_cache, d["block_tables"],
                        d["context_lens"], self.max_context_len, self.scale, d["key"], d["value"],
                        d["slot_mapping"], workspace=self.workspace, k_scale=self.k_scale,
                        v_scale=self.v_scale, dev_err=self.dev_err)
-        self.host_out.copy_(self.out, non_blocking=True)
+        pd_copy_bytes(self.host_out, self.out)
 
     def __call__(self):
         torch = _torch()

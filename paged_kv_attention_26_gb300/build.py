@@ -16,7 +16,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libpd_attn.so")
 
 CUDA_SOURCES = ["capi.cu", "store_copy.cu", "kv_pack.cu", "decode.cu", "decode_static.cu",
-                "selftest.cu",
+                "selftest.cu", "copy_bytes.cu",
                 "prefill.cu"]
 CXX_SOURCES = ["block_manager.cpp", "prefix_cache.cpp"]
 HEADERS = ["pd_device.cuh", "pd_internal.h", "pd_tcgen05.cuh", "pd_mma.cuh", "pd_tmap.h"]

@@ -271,6 +271,35 @@ pd_status pd_paged_attention_verify(void* out, const void* q, const void* key_ca
     return launch_decode(a);
 }
 
+// Device address of p if the device can reach it (device or managed memory,
+// or host memory registered / allocated pinned and mapped), else nullptr.
+static const void* device_view(const void* p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();                      // clear the sticky-free error
+        return nullptr;
+    }
+    switch (at.type) {
+        case cudaMemoryTypeDevice:
+        case cudaMemoryTypeManaged:
+            return p;
+        case cudaMemoryTypeHost:
+            return at.devicePointer;
+        default:
+            return nullptr;
+    }
+}
+
+pd_status pd_copy_bytes(void* dst, const void* src, size_t bytes, cudaStream_t stream) {
+    if (bytes == 0) return PD_OK;
+    if (!dst || !src || !aligned16(dst) || !aligned16(src) || (bytes & 15u))
+        return PD_ERR_INVALID_ARG;
+    const void* d = device_view(dst);
+    const void* s = device_view(src);
+    if (!d || !s || !aligned16(d) || !aligned16(s)) return PD_ERR_INVALID_ARG;
+    return launch_copy_bytes(const_cast<void*>(d), s, bytes, stream);
+}
+
 pd_status pd_selftest_bounded_wait(int32_t* dev_err, uint64_t limit_ns, cudaStream_t stream) {
     if (!dev_err || limit_ns < 1000ull || limit_ns > 10000000000ull) return PD_ERR_INVALID_ARG;
     return launch_bounded_wait_selftest(dev_err, (unsigned long long)limit_ns, stream);

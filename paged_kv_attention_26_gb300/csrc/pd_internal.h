@@ -50,6 +50,7 @@ struct DecodeArgs {
 pd_status launch_decode(const DecodeArgs& a);
 pd_status launch_bounded_wait_selftest(int32_t* dev_err, unsigned long long limit_ns,
                                        cudaStream_t stream);
+pd_status launch_copy_bytes(void* dst, const void* src, size_t bytes, cudaStream_t stream);
 
 // ---- store / copy ----------------------------------------------------------------
 pd_status launch_reshape_and_cache(const void* key, const void* value, void* key_cache,

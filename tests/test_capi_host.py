@@ -179,6 +179,18 @@ def test_selftest_validation(lib):
     assert lib.pd_launch_count() == n0
 
 
+def test_copy_bytes_validation(lib):
+    n0 = lib.pd_launch_count()
+    assert lib.pd_copy_bytes(P, P + 4096, 0, None) == 0          # nothing to copy
+    assert lib.pd_copy_bytes(None, P, 64, None) == 1             # null destination
+    assert lib.pd_copy_bytes(P + 8, P, 64, None) == 1            # misaligned
+    assert lib.pd_copy_bytes(P, P + 4096, 40, None) == 1         # not a multiple of 16
+    buf = (ctypes.c_uint8 * 256)()                               # pageable host memory
+    addr = (ctypes.addressof(buf) + 15) & ~15
+    assert lib.pd_copy_bytes(addr, addr + 128, 64, None) == 1    # refused: not device-visible
+    assert lib.pd_launch_count() == n0
+
+
 def test_workspace_size_formula(lib):
     part = lib.pd_decode_partition_tokens(10000)
     assert part % 64 == 0

@@ -233,3 +233,20 @@ def test_step_with_padding_slots_and_more_tokens_than_sequences(cuda_lib):
     ref, rk, rv = oracle_store_and_decode(c)
     assert_close(out.cpu(), ref, "step with padding")
     assert np.array_equal(u16(kc), rk) and np.array_equal(u16(vc), rv)
+
+
+def test_copy_bytes_pinned_and_device(cuda_lib):
+    """pd_copy_bytes moves bytes exactly between pinned host and device
+    buffers, in both directions and device to device."""
+    pd = cuda_lib
+    g = torch.Generator().manual_seed(71)
+    src = torch.randint(0, 256, (820 * 1024 + 48,), generator=g, dtype=torch.int32)
+    src = src.to(torch.uint8).pin_memory()
+    dev = torch.empty(src.shape, dtype=torch.uint8, device="cuda")
+    pd.pd_copy_bytes(dev, src)
+    dev2 = torch.empty_like(dev)
+    pd.pd_copy_bytes(dev2, dev)
+    back = torch.zeros_like(src).pin_memory()
+    pd.pd_copy_bytes(back, dev2)
+    torch.cuda.synchronize()
+    assert torch.equal(dev.cpu(), src) and torch.equal(back, src)
