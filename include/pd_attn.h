@@ -253,6 +253,23 @@ PD_API pd_status pd_paged_attention_verify(void* out, const void* q,
                                            cudaStream_t stream);
 
 /* ---------------------------------------------------------------------- */
+/* pd_verify_step: store the step's drafted tokens (key/value/slot_mapping/T
+ * as for pd_reshape_and_cache), then pd_paged_attention_verify over them
+ * (out/q [B][nq][H][D], workspace as for that call), the verify grid
+ * launched as a programmatic dependent of the store grid exactly as in
+ * pd_decode_step.  16-bit pools; nq 1 .. 8. */
+PD_API pd_status pd_verify_step(const void* key, const void* value,
+                                const int64_t* slot_mapping, int T,
+                                int64_t key_stride_tok, int64_t value_stride_tok,
+                                void* out, const void* q, void* key_cache,
+                                void* value_cache, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* context_lens,
+                                int B, int nq, int H, int Hk, int D, int S, int NB,
+                                int max_context_len, float scale, void* workspace,
+                                size_t workspace_bytes, pd_dtype dt,
+                                int32_t* dev_err, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
 /* pd_copy_bytes: copies `bytes` bytes from src to dst with an SM kernel on
  * `stream`.  Each side may be device memory, managed memory, or pinned host
  * memory mapped into the device's address space (cudaHostAlloc /

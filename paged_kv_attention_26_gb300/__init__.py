@@ -67,6 +67,8 @@ SIGNATURES = {
                                 _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _I, _P, _P]),
     "pd_selftest_bounded_wait": (_I, [_P, ctypes.c_uint64, _P]),
     "pd_copy_bytes": (_I, [_P, _P, _SZ, _P]),
+    "pd_verify_step": (_I, [_P, _P, _P, _I, _I64, _I64, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I,
+                            _I, _I, _I, _I, _I, _F, _P, _SZ, _I, _P, _P]),
     "pd_kv_pack": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pd_kv_unpack": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pd_paged_prefill_chunk": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
@@ -342,6 +344,43 @@ def pd_paged_attention_verify(out, q, key_cache, value_cache, block_tables, cont
         S, NB, int(max_context_len), float(scale), ws_ptr, ws_bytes, dt, _opt(dev_err),
         _stream(stream))
     _check("pd_paged_attention_verify", st)
+
+
+def pd_verify_step(out, q, key_cache, value_cache, block_tables, context_lens,
+                   max_context_len: int, scale: float, key, value, slot_mapping,
+                   workspace=None, dev_err=None, stream=None):
+    """Store the drafted tokens ``key``/``value`` [T, Hk, D] at ``slot_mapping``,
+    then verify ``q`` [B, nq, H, D] into ``out``: ``pd_reshape_and_cache``
+    followed by ``pd_paged_attention_verify``, the verify grid launched as a
+    dependent of the store grid."""
+    torch = _torch()
+    B, nq, H, D = q.shape
+    NB, Hk, S, D2 = key_cache.shape
+    T = key.shape[0]
+    if out.shape != q.shape or D2 != D or value_cache.shape != key_cache.shape:
+        raise ValueError("shape mismatch")
+    if key.shape != (T, Hk, D) or value.shape != key.shape or slot_mapping.shape != (T,):
+        raise ValueError("key / value / slot_mapping shape")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables / context_lens shape")
+    for t, n in ((key, "key"), (value, "value")):
+        if t.stride(2) != 1 or t.stride(1) != D:
+            raise ValueError(f"{n} must have contiguous heads and dims")
+    for t in (q, out, key, value, value_cache):
+        if t.dtype != key_cache.dtype:
+            raise TypeError("dtype mismatch")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    st = load().pd_verify_step(
+        _dev(key, "key", contiguous=False), _dev(value, "value", contiguous=False),
+        _dev(slot_mapping, "slot_mapping", torch.int64), T, key.stride(0), value.stride(0),
+        _dev(out, "out"), _dev(q, "q"), _dev(key_cache, "key_cache"),
+        _dev(value_cache, "value_cache"), _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), B, nq, H, Hk, D,
+        S, NB, int(max_context_len), float(scale), ws_ptr, ws_bytes, _dt(key_cache),
+        _opt(dev_err), _stream(stream))
+    _check("pd_verify_step", st)
 
 
 def verify_workspace(B, nq, H, D, max_context_len, device="cuda"):

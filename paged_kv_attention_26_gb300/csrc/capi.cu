@@ -176,13 +176,14 @@ static pd_status step_common(const void* key, const void* value, const int64_t* 
                              const int32_t* context_lens, int B, int H, int Hk, int D, int S,
                              int NB, int max_context_len, float scale, void* workspace,
                              size_t workspace_bytes, pd_dtype dt, int32_t* dev_err,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, int nq = 1) {
     DecodeArgs a{};
     bool skip_dec = false, skip_store = false;
+    if (fp8 && nq > 1) return PD_ERR_UNSUPPORTED;
     pd_status st = decode_prepare(out, q, key_cache, value_cache, k_scale, v_scale, fp8,
                                   block_tables, max_blocks_per_seq, context_lens, B, H, Hk, D, S,
                                   NB, max_context_len, scale, workspace, workspace_bytes, dt,
-                                  dev_err, stream, &a, &skip_dec);
+                                  dev_err, stream, &a, &skip_dec, nq);
     if (st != PD_OK) return st;
     st = store_check(key, value, key_cache, value_cache, slot_mapping, T, Hk, D, S, NB,
                      key_stride_tok, value_stride_tok, fp8, k_scale, v_scale, dt, &skip_store);
@@ -303,6 +304,20 @@ pd_status pd_copy_bytes(void* dst, const void* src, size_t bytes, cudaStream_t s
 pd_status pd_selftest_bounded_wait(int32_t* dev_err, uint64_t limit_ns, cudaStream_t stream) {
     if (!dev_err || limit_ns < 1000ull || limit_ns > 10000000000ull) return PD_ERR_INVALID_ARG;
     return launch_bounded_wait_selftest(dev_err, (unsigned long long)limit_ns, stream);
+}
+
+pd_status pd_verify_step(const void* key, const void* value, const int64_t* slot_mapping, int T,
+                         int64_t key_stride_tok, int64_t value_stride_tok, void* out,
+                         const void* q, void* key_cache, void* value_cache,
+                         const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* context_lens, int B, int nq, int H, int Hk, int D, int S,
+                         int NB, int max_context_len, float scale, void* workspace,
+                         size_t workspace_bytes, pd_dtype dt, int32_t* dev_err,
+                         cudaStream_t stream) {
+    return step_common(key, value, slot_mapping, T, key_stride_tok, value_stride_tok, out, q,
+                       key_cache, value_cache, nullptr, nullptr, false, block_tables,
+                       max_blocks_per_seq, context_lens, B, H, Hk, D, S, NB, max_context_len,
+                       scale, workspace, workspace_bytes, dt, dev_err, stream, nq);
 }
 
 pd_status pd_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,

@@ -191,6 +191,21 @@ def test_copy_bytes_validation(lib):
     assert lib.pd_launch_count() == n0
 
 
+def test_verify_step_validation(lib):
+    f = lib.pd_verify_step
+    base = [P, P, P, 16, 128, 128,           # key, value, slots, T, strides
+            P, P, P, P,                      # out, q, key_cache, value_cache
+            P, 8, P, 4, 4, 8, 2, 64, 16, 64,  # tables, mbps, lens, B, nq, H, Hk, D, S, NB
+            100, 0.125, None, 0, pd.PD_F16, None, None]
+    n0 = lib.pd_launch_count()
+    for change, want in [({14: 9}, 2), ({14: 0}, 2), ({3: -1}, 1), ({16: 3}, 1), ({17: 96}, 2)]:
+        a = list(base)
+        for k, v in change.items():
+            a[k] = v
+        assert f(*a) == want, change
+    assert lib.pd_launch_count() == n0
+
+
 def test_workspace_size_formula(lib):
     part = lib.pd_decode_partition_tokens(10000)
     assert part % 64 == 0

@@ -168,3 +168,28 @@ def test_verify_empty_and_short_contexts(cuda_lib):
     assert err.item() & 0x4
     assert (out[2, :2] == 0).all()        # queries at positions -2, -1
     assert torch.isfinite(out[2, 2:].float()).all()
+
+
+@pytest.mark.parametrize("n_q", [1, 4])
+def test_verify_step_equals_separate_calls_and_oracle(cuda_lib, n_q):
+    """pd_verify_step (store the drafts, then verify as a dependent grid) is
+    bit-identical to the store followed by the verify, and within tolerance
+    of the oracle."""
+    pd = cuda_lib
+    m = pd_inputs.spec_verify(seed=40 + n_q, B=9, n_q=n_q, lo=1, hi=900)
+    dev = torch.device("cuda")
+    kc, vc = m.pool.key_cache.to(dev), m.pool.value_cache.to(dev)
+    q = m.q_prefill.reshape(m.Bp, n_q, m.H, m.D).to(dev)
+    cl = m.pool.context_lens[:m.Bp]
+    mcl = int(cl.max())
+    out = torch.full_like(q, float("nan"))
+    err = device_err()
+    pd.pd_verify_step(out, q, kc, vc, m.pool.block_tables[:m.Bp].to(dev), cl.to(dev), mcl, m.scale,
+                      m.new_key.to(dev), m.new_value.to(dev), m.slot_mapping.to(dev),
+                      workspace=pd.verify_workspace(m.Bp, n_q, m.H, m.D, mcl), dev_err=err)
+    sep = _verify(pd, m)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    got = out.reshape(-1, m.H, m.D).cpu()
+    assert torch.equal(got.view(torch.int16), sep.view(torch.int16))
+    assert_close(got, _oracle(m), f"verify step n_q={n_q}")
