@@ -591,6 +591,9 @@ def bench_spec_verify(pd, pd_inputs, dev, args, flush, hbm_peak, bf16_peak):
     ws = pd.verify_workspace(m.Bp, nq, m.H, m.D, mcl, device=dev)
     t = _time_calls(lambda: pd.pd_paged_attention_verify(o4, q4, kc, vc, bt, cl, mcl, m.scale, ws),
                     args.extra_steps, flush)
+    nk, nv, sl = m.new_key.to(dev), m.new_value.to(dev), m.slot_mapping.to(dev)
+    tstep = _time_calls(lambda: pd.pd_verify_step(o4, q4, kc, vc, bt, cl, mcl, m.scale, nk, nv, sl,
+                                                  workspace=ws), args.extra_steps, flush)
     ctx = m.pool.context_lens[:m.Bp].double()
     kv = float(ctx.sum()) * m.Hk * m.D * 2 * 2
     P = m.prior_lens.double()
@@ -600,6 +603,8 @@ def bench_spec_verify(pd, pd_inputs, dev, args, flush, hbm_peak, bf16_peak):
            "ms": round(t * 1e3, 4), "kv_gbs": round(kv / t / 1e9, 1),
            "kv_frac": round(kv / t / 1e9 / hbm_peak, 4), "tflops": round(flops / t / 1e12, 2),
            "query_tokens_per_s": round(m.Bp * nq / t, 1),
+           "step_ms": round(tstep * 1e3, 4),
+           "step": "pd_verify_step: store the drafted tokens, then verify as a dependent grid",
            "via_prefill_chunk": {"ms": round(tp * 1e3, 4), "kv_gbs": round(kv / tp / 1e9, 1),
                                  "kv_frac": round(kv / tp / 1e9 / hbm_peak, 4)}}
     del kc, vc
