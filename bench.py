@@ -417,7 +417,7 @@ def e2e_decode(pd, c, dev, args, step_bytes, world=1):
     eager = rank_max(eager, world, dev)
     return {"value": round(whole_job_value(step_bytes, args.steps, total, world), 2), "unit": "GB/s",
             "ms_per_step": round(total / args.steps * 1e3, 4),
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world,
             "path": "DecodeStep replayed from a CUDA graph: pd_copy_bytes of the step's inputs "
                     "from one pinned host buffer to the device, pd_decode_step, pd_copy_bytes of "
                     "out to pinned host memory, synchronize; host wall clock per step, L2 "
