@@ -103,7 +103,7 @@ struct DecodeSmem {
     static constexpr int kV = kK + kTiles16 * kTile;
     static constexpr int kK8 = kV + kTiles16 * kTile;
     static constexpr int kV8 = kK8 + (kF8 ? kRing * kTile8 : 0);
-    static constexpr int kX = kV8 + (kF8 ? kRing * kTile8 : 0);    // merge exchange [2][kFrag][32]
+    static constexpr int kX = kV8 + (kF8 ? kRing * kTile8 : 0);    // merge exchange [2][32][kFrag]
     static constexpr int kBar = kX + 2 * kFrag * 32 * 4;
     static constexpr int kMisc = kBar + 2 * kRing * 8;     // abort flag, issued count
     static constexpr int kBytes = kMisc + 16;
@@ -960,23 +960,23 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 8);
             l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 16);
         }
+        // lane-major records (o, then m and l), 16-byte accesses: a quarter-warp's
+        // eight records start on distinct 4-bank groups, so no conflicts
         auto put = [&](int buf) {
-            float* x = xchg + buf * L::kFrag * 32 + lane;
+            float4* x = reinterpret_cast<float4*>(xchg + (buf * 32 + lane) * L::kFrag);
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) x[(mt * 4 + e) * 32] = o[mt][e];
-            x[(KS * 4 + 0) * 32] = m_run[0];
-            x[(KS * 4 + 1) * 32] = m_run[1];
-            x[(KS * 4 + 2) * 32] = l_run[0];
-            x[(KS * 4 + 3) * 32] = l_run[1];
+                x[mt] = make_float4(o[mt][0], o[mt][1], o[mt][2], o[mt][3]);
+            x[KS] = make_float4(m_run[0], m_run[1], l_run[0], l_run[1]);
         };
         auto take = [&](int buf) {
-            const float* x = xchg + buf * L::kFrag * 32 + lane;
+            const float4* x = reinterpret_cast<const float4*>(xchg + (buf * 32 + lane) * L::kFrag);
+            const float4 ml = x[KS];
+            const float mo2[2] = {ml.x, ml.y}, lo2[2] = {ml.z, ml.w};
             float c_mine[2], c_other[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const float mo = x[(KS * 4 + h) * 32], lo = x[(KS * 4 + 2 + h) * 32];
+                const float mo = mo2[h], lo = lo2[h];
                 const float M = fmaxf(m_run[h], mo);
                 c_mine[h] = m_run[h] == -INFINITY ? 0.f : ex2(m_run[h] - M);
                 c_other[h] = mo == -INFINITY ? 0.f : ex2(mo - M);
@@ -984,10 +984,13 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 m_run[h] = M;
             }
 #pragma unroll
-            for (int mt = 0; mt < KS; ++mt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    o[mt][e] = o[mt][e] * c_mine[e & 1] + x[(mt * 4 + e) * 32] * c_other[e & 1];
+            for (int mt = 0; mt < KS; ++mt) {
+                const float4 v = x[mt];
+                o[mt][0] = o[mt][0] * c_mine[0] + v.x * c_other[0];
+                o[mt][1] = o[mt][1] * c_mine[1] + v.y * c_other[1];
+                o[mt][2] = o[mt][2] * c_mine[0] + v.z * c_other[0];
+                o[mt][3] = o[mt][3] * c_mine[1] + v.w * c_other[1];
+            }
         };
         // two column tiles: warp 1 hands over to 0 and warp 3 to 2 (same tile)
         if (!two_tiles) {
