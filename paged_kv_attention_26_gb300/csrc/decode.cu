@@ -223,8 +223,8 @@ constexpr unsigned long long kCountBits = 20;
 constexpr unsigned long long kCountMask = (1ull << kCountBits) - 1;
 
 __device__ __forceinline__ bool arrive_piece(unsigned long long* cnt, unsigned long long tag,
-                                             int nseg) {
-    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(cnt);
+                                             int nseg, unsigned long long cur) {
+    // cur: the counter as read earlier (a stale value only costs one more CAS)
     for (;;) {
         const unsigned long long next =
             (cur >> kCountBits) == tag ? cur + 1 : (tag << kCountBits) | 1ull;
@@ -1013,6 +1013,12 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         // perhaps merge the stream. They fall behind by that much and catch up
         // on stages already in the ring (consuming is faster than streaming).
         asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+        // the arrival counter is read now, so that its latency overlaps the
+        // piece's writes and fence; a value changed meanwhile costs one more CAS
+        unsigned long long cnt0 = 0;
+        if (nseg > 1 && warp == 0 && lane == 0)
+            cnt0 = *reinterpret_cast<volatile unsigned long long*>(ws_cnt + (int64_t)w.s * units +
+                                                                    w.u);
         if (two_tiles ? (warp & 1) == 0 : warp == 0) {
             if constexpr (kF8) {
                 const float vs = __ldg(v_scale + kvh);
@@ -1062,7 +1068,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 __syncwarp();
                 uint32_t last = 0;
                 if (lane == 0)
-                    last = arrive_piece(ws_cnt + (int64_t)w.s * units + w.u, tag, nseg) ? 1u : 0u;
+                    last = arrive_piece(ws_cnt + (int64_t)w.s * units + w.u, tag, nseg, cnt0) ? 1u
+                                                                                              : 0u;
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
                     __threadfence();
@@ -1079,7 +1086,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             __threadfence();
             asm volatile("bar.sync 2, 64;" ::: "memory");
             if (warp == 0 && lane == 0)
-                *last_flag = arrive_piece(ws_cnt + (int64_t)w.s * units + w.u, tag, nseg) ? 1 : 0;
+                *last_flag =
+                    arrive_piece(ws_cnt + (int64_t)w.s * units + w.u, tag, nseg, cnt0) ? 1 : 0;
             asm volatile("bar.sync 2, 64;" ::: "memory");
             if (*last_flag) {
                 __threadfence();
