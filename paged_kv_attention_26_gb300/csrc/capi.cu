@@ -49,21 +49,40 @@ int pd_last_cuda_error(void) { return g_last_cuda_error; }
 
 uint64_t pd_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+// Argument checks of the store (16-bit or FP8 pools); *skip when T == 0.
+static pd_status store_check(const void* key, const void* value, const void* key_cache,
+                             const void* value_cache, const int64_t* slot_mapping, int T, int Hk,
+                             int D, int S, int NB, int64_t key_stride_tok,
+                             int64_t value_stride_tok, bool fp8, const float* k_scale,
+                             const float* v_scale, pd_dtype dt, bool* skip) {
+    *skip = false;
+    if (T < 0 || Hk < 1 || NB < 1) return PD_ERR_INVALID_ARG;
+    if (!supported_D(D) || !supported_S(S) || !supported_dt(dt)) return PD_ERR_UNSUPPORTED;
+    if (!key_cache || !value_cache || !aligned16(key_cache) || !aligned16(value_cache))
+        return PD_ERR_INVALID_ARG;
+    if (T == 0) {
+        *skip = true;
+        return PD_OK;
+    }
+    if (!key || !value || !slot_mapping || !aligned16(key) || !aligned16(value))
+        return PD_ERR_INVALID_ARG;
+    if (fp8 && (!k_scale || !v_scale)) return PD_ERR_INVALID_ARG;
+    if (key_stride_tok < int64_t(Hk) * D || value_stride_tok < int64_t(Hk) * D ||
+        key_stride_tok % 8 || value_stride_tok % 8)
+        return PD_ERR_INVALID_ARG;
+    return PD_OK;
+}
+
 pd_status pd_reshape_and_cache(const void* key, const void* value, void* key_cache,
                                void* value_cache, const int64_t* slot_mapping, int T, int Hk,
                                int D, int S, int NB, int64_t key_stride_tok,
                                int64_t value_stride_tok, pd_dtype dt, int32_t* dev_err,
                                cudaStream_t stream) {
-    if (T < 0 || Hk < 1 || NB < 1) return PD_ERR_INVALID_ARG;
-    if (!supported_D(D) || !supported_S(S) || !supported_dt(dt)) return PD_ERR_UNSUPPORTED;
-    if (!key_cache || !value_cache || !aligned16(key_cache) || !aligned16(value_cache))
-        return PD_ERR_INVALID_ARG;
-    if (T == 0) return PD_OK;
-    if (!key || !value || !slot_mapping || !aligned16(key) || !aligned16(value))
-        return PD_ERR_INVALID_ARG;
-    if (key_stride_tok < int64_t(Hk) * D || value_stride_tok < int64_t(Hk) * D ||
-        key_stride_tok % 8 || value_stride_tok % 8)
-        return PD_ERR_INVALID_ARG;
+    bool skip = false;
+    const pd_status st = store_check(key, value, key_cache, value_cache, slot_mapping, T, Hk, D, S,
+                                     NB, key_stride_tok, value_stride_tok, false, nullptr,
+                                     nullptr, dt, &skip);
+    if (st != PD_OK || skip) return st;
     return launch_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, T, Hk, D,
                                     S, NB, key_stride_tok, value_stride_tok, dev_err, stream);
 }
@@ -136,30 +155,6 @@ static pd_status decode_common(void* out, const void* q, const void* key_cache,
                                         workspace_bytes, dt, dev_err, stream, &a, &skip);
     if (st != PD_OK || skip) return st;
     return launch_decode(a);
-}
-
-// Argument checks of the store (16-bit or FP8 pools); *skip when T == 0.
-static pd_status store_check(const void* key, const void* value, const void* key_cache,
-                             const void* value_cache, const int64_t* slot_mapping, int T, int Hk,
-                             int D, int S, int NB, int64_t key_stride_tok,
-                             int64_t value_stride_tok, bool fp8, const float* k_scale,
-                             const float* v_scale, pd_dtype dt, bool* skip) {
-    *skip = false;
-    if (T < 0 || Hk < 1 || NB < 1) return PD_ERR_INVALID_ARG;
-    if (!supported_D(D) || !supported_S(S) || !supported_dt(dt)) return PD_ERR_UNSUPPORTED;
-    if (!key_cache || !value_cache || !aligned16(key_cache) || !aligned16(value_cache))
-        return PD_ERR_INVALID_ARG;
-    if (T == 0) {
-        *skip = true;
-        return PD_OK;
-    }
-    if (!key || !value || !slot_mapping || !aligned16(key) || !aligned16(value))
-        return PD_ERR_INVALID_ARG;
-    if (fp8 && (!k_scale || !v_scale)) return PD_ERR_INVALID_ARG;
-    if (key_stride_tok < int64_t(Hk) * D || value_stride_tok < int64_t(Hk) * D ||
-        key_stride_tok % 8 || value_stride_tok % 8)
-        return PD_ERR_INVALID_ARG;
-    return PD_OK;
 }
 
 // Store then decode on one stream.  The decode grid is launched as a
@@ -326,17 +321,11 @@ pd_status pd_reshape_and_cache_fp8(const void* key, const void* value, void* key
                                    int64_t value_stride_tok, const float* k_scale,
                                    const float* v_scale, pd_dtype in_dt, int32_t* dev_err,
                                    cudaStream_t stream) {
-    if (T < 0 || Hk < 1 || NB < 1) return PD_ERR_INVALID_ARG;
-    if (!supported_D(D) || !supported_S(S) || !supported_dt(in_dt)) return PD_ERR_UNSUPPORTED;
-    if (!key_cache || !value_cache || !aligned16(key_cache) || !aligned16(value_cache))
-        return PD_ERR_INVALID_ARG;
-    if (T == 0) return PD_OK;
-    if (!key || !value || !slot_mapping || !k_scale || !v_scale || !aligned16(key) ||
-        !aligned16(value))
-        return PD_ERR_INVALID_ARG;
-    if (key_stride_tok < int64_t(Hk) * D || value_stride_tok < int64_t(Hk) * D ||
-        key_stride_tok % 8 || value_stride_tok % 8)
-        return PD_ERR_INVALID_ARG;
+    bool skip = false;
+    const pd_status st = store_check(key, value, key_cache, value_cache, slot_mapping, T, Hk, D, S,
+                                     NB, key_stride_tok, value_stride_tok, true, k_scale, v_scale,
+                                     in_dt, &skip);
+    if (st != PD_OK || skip) return st;
     return launch_reshape_and_cache_fp8(key, value, key_cache, value_cache, slot_mapping, T, Hk,
                                         D, S, NB, key_stride_tok, value_stride_tok, k_scale,
                                         v_scale, in_dt, dev_err, stream);
