@@ -250,3 +250,42 @@ def test_copy_bytes_pinned_and_device(cuda_lib):
     pd.pd_copy_bytes(back, dev2)
     torch.cuda.synchronize()
     assert torch.equal(dev.cpu(), src) and torch.equal(back, src)
+
+
+def test_host_decode_step_fp8_pools(cuda_lib):
+    """DecodeStep over one-byte pools (quantising store, FP8 decode) replayed
+    from a CUDA graph: pools bit-exact with the oracle's store, outputs within
+    tolerance of the oracle's FP8 decode, over three steps."""
+    pd = cuda_lib
+    steps, B, H, Hk, D, S = 3, 6, 32, 8, 128, 16
+    ctx0 = torch.tensor([1, 30, 64, 65, 500, 1300])
+    c = pd_inputs.decode_case("hostfp8", 72, (ctx0 + steps).tolist(), H, Hk, D, S,
+                              torch.bfloat16, store_last=False, poison=False)
+    kc8, vc8, ks, vs = pd_inputs.fp8_pools(c.pool.key_cache, c.pool.value_cache)
+    dev = torch.device("cuda")
+    kg, vg = kc8.to(dev), vc8.to(dev)
+    rk, rv = kc8.numpy().copy(), vc8.numpy().copy()
+    bt = c.pool.block_tables
+    mcl = int(ctx0.max()) + steps
+    st = pd.DecodeStep(kg, vg, B, H, B, bt.shape[1], mcl, c.scale, torch.bfloat16,
+                       k_scale=ks.to(dev), v_scale=vs.to(dev), graph=True)
+    g = torch.Generator().manual_seed(73)
+    for i in range(steps):
+        lens = (ctx0 + i).to(torch.int32)
+        slots = pd_inputs.slot_mapping_for(bt, torch.arange(B), ctx0 - 1 + i, S)
+        nk = torch.randn(B, Hk, D, generator=g).to(torch.bfloat16)
+        nv = torch.randn(B, Hk, D, generator=g).to(torch.bfloat16)
+        q = torch.randn(B, H, D, generator=g).to(torch.bfloat16)
+        h = st.host
+        h["q"].copy_(q)
+        h["key"].copy_(nk)
+        h["value"].copy_(nv)
+        h["slot_mapping"].copy_(slots)
+        h["block_tables"].copy_(bt)
+        h["context_lens"].copy_(lens)
+        got = st().clone()
+        assert st.dev_err.item() == 0
+        oracle.reshape_and_cache_fp8(nk, nv, oracle.BF16, rk, rv, slots, ks, vs, S)
+        ref = oracle.decode_fp8(q, oracle.BF16, rk, rv, ks, vs, bt, lens, c.scale)
+        assert_close(got, ref, f"fp8 host step {i}")
+    assert np.array_equal(kg.cpu().numpy(), rk) and np.array_equal(vg.cpu().numpy(), rv)
