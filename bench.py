@@ -51,7 +51,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
     ap.add_argument("--extras", default="chunked_prefill_mix,long_context_32_layers,cow_fork_stress,fp8_decode,"
-                    "spec_verify,kv_handover",
+                    "spec_verify,kv_handover,prefix_cache",
                     help="comma-separated extra workloads to run after the headline")
     ap.add_argument("--extra-steps", type=int, default=10)
     ap.add_argument("--only-extras", action="store_true",
@@ -360,6 +360,8 @@ def _run_extras(extras, pd, pd_inputs, dev, args, flush, wanted, hbm_peak, bf16_
                                                   bf16_peak)
     if "kv_handover" in wanted:
         extras["kv_handover"] = bench_kv_handover(pd, pd_inputs, dev, args, flush, hbm_peak)
+    if "prefix_cache" in wanted:
+        extras["prefix_cache"] = bench_prefix_cache(pd, args)
 
 
 def run_only_extras(args):
@@ -622,6 +624,35 @@ def bench_spec_verify(pd, pd_inputs, dev, args, flush, hbm_peak, bf16_peak):
     del kc, vc
     torch.cuda.empty_cache()
     return res
+
+
+def bench_prefix_cache(pd, args):
+    """Host prefix cache (pd_pc_*): 64 requests of 2048 tokens (S 16, 128 full
+    blocks each) that share a 1024-token prefix; every request looks its
+    prompt up (hash chain over its blocks) and inserts what missed.  Reports
+    blocks hashed per second and the hit rate."""
+    import numpy as np
+    S, n_req, n_tok, shared = 16, 64, 2048, 1024
+    rng = np.random.default_rng(0)
+    prefix = rng.integers(0, 150000, shared)
+    prompts = [np.concatenate([prefix, rng.integers(0, 150000, n_tok - shared)]).tolist()
+               for _ in range(n_req)]
+    pc = pd.PrefixCache(capacity_blocks=n_req * n_tok // S, block_size=S)
+    next_block, hit_tokens = 0, 0
+    t0 = time.perf_counter()
+    for toks in prompts:
+        hit, keys, _ = pc.lookup(toks)
+        hit_tokens += hit
+        fresh = list(range(next_block, next_block + len(keys)))
+        next_block += len(keys)
+        pc.insert(keys, fresh)
+    dt = time.perf_counter() - t0
+    blocks = n_req * (n_tok // S)
+    return {"workload": f"{n_req} requests x {n_tok} tokens, {shared}-token shared prefix, S {S}",
+            "blocks_per_s": round(blocks / dt, 1), "us_per_request": round(dt / n_req * 1e6, 1),
+            "hit_rate": round(pc.hit_rate, 4),
+            "token_hit_fraction": round(hit_tokens / (n_req * n_tok), 4),
+            "note": "host C++ (SHA-256 chain, LRU) through the binding; no GPU work"}
 
 
 def bench_kv_handover(pd, pd_inputs, dev, args, flush, hbm_peak):
