@@ -54,6 +54,9 @@ def parse_args():
                     "spec_verify,kv_handover,prefix_cache",
                     help="comma-separated extra workloads to run after the headline")
     ap.add_argument("--extra-steps", type=int, default=10)
+    ap.add_argument("--long-context-layers", type=int, default=32,
+                    help="layers of the long-context extra (32 = the workload; fewer only "
+                         "to profile a layer's launch on a smaller device footprint)")
     ap.add_argument("--only-extras", action="store_true",
                     help="run only the --extras workloads and print their results (for "
                          "profiling one kernel); not a benchmark line")
@@ -303,7 +306,10 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0:
         result["e2e"] = e2e
     if rank == 0 and world == 1:
-        result["cpu_baseline"] = cpu_baseline_decode(c, step_bytes, budget_s=10.0)
+        step()                                   # the output of one whole step, for parity
+        torch.cuda.synchronize()
+        result["cpu_baseline"] = cpu_baseline_decode(c, step_bytes, gpu_out=out)
+        result["parity"] = result["cpu_baseline"].pop("parity")
     wanted = [] if args.no_extras else [x for x in args.extras.split(",") if x]
     if world == 1 and wanted:
         del kc, vc
@@ -428,28 +434,52 @@ def e2e_decode(pd, c, dev, args, step_bytes, world=1):
             "eager_ms_per_step": round(eager / args.steps * 1e3, 4)}
 
 
-def cpu_baseline_decode(c, step_bytes, budget_s=10.0):
+def cpu_baseline_decode(c, step_bytes, gpu_out=None, budget_s=8.0):
     """The float64 oracle (as it stands) on this host's cores, on the same step:
-    store + decode of all 64 sequences, repeated until ``budget_s`` elapsed."""
+    store + decode of all 64 sequences, repeated until ``budget_s`` elapsed, on
+    all cores and then on one core.  When ``gpu_out`` (the GPU step's output)
+    is given, the oracle's result of the same step also gives the headline's
+    parity record: max-abs and max-rel error and the count of elements outside
+    |gpu - oracle| <= 2e-3 + 1e-2 |oracle|."""
     import numpy as np
     import torch
     import oracle
     threads = oracle.default_threads()
     kc0 = c.pool.key_cache.view(torch.int16).numpy().view(np.uint16)
     vc0 = c.pool.value_cache.view(torch.int16).numpy().view(np.uint16)
-    reps, total = 0, 0.0
-    while total < budget_s and reps < 50:
-        kc, vc = kc0.copy(), vc0.copy()
-        t0 = time.perf_counter()
-        oracle.reshape_and_cache(c.new_key, c.new_value, kc, vc, c.slot_mapping, c.pool.S)
-        oracle.decode(c.q, kc, vc, c.pool.block_tables, c.pool.context_lens, c.scale,
-                      oracle.BF16, threads=threads)
-        total += time.perf_counter() - t0
-        reps += 1
-    return {"value": round(step_bytes * reps / total / 1e9, 4), "unit": "GB/s",
-            "cores": threads, "kind": "oracle",
-            "sample": f"{reps} full steps (store + decode of all 64 sequences), "
-                      f"{total:.1f} s on {threads} threads"}
+
+    def run(nthreads, max_reps):
+        reps, total, ref = 0, 0.0, None
+        while (total < budget_s or reps == 0) and reps < max_reps:
+            kc, vc = kc0.copy(), vc0.copy()
+            t0 = time.perf_counter()
+            oracle.reshape_and_cache(c.new_key, c.new_value, kc, vc, c.slot_mapping, c.pool.S)
+            ref = oracle.decode(c.q, kc, vc, c.pool.block_tables, c.pool.context_lens, c.scale,
+                                oracle.BF16, threads=nthreads)
+            total += time.perf_counter() - t0
+            reps += 1
+        return reps, total, ref
+
+    reps, total, ref = run(threads, 50)
+    reps1, total1, _ = run(1, 10)
+    res = {"value": round(step_bytes * reps / total / 1e9, 4), "unit": "GB/s",
+           "cores": threads, "kind": "oracle",
+           "sample": f"{reps} full steps (store + decode of all 64 sequences), "
+                     f"{total:.1f} s on {threads} threads",
+           "one_core": {"value": round(step_bytes * reps1 / total1 / 1e9, 4), "unit": "GB/s",
+                        "cores": 1,
+                        "sample": f"{reps1} full steps, {total1:.1f} s on 1 thread"}}
+    if gpu_out is not None:
+        g = gpu_out.detach().cpu().double().numpy().reshape(ref.shape)
+        err = np.abs(g - ref)
+        big = np.abs(ref) >= 1e-3                 # relative error where it means something
+        res["parity"] = {
+            "elements": int(err.size),
+            "max_abs": float(err.max()),
+            "max_rel": float((err[big] / np.abs(ref[big])).max()) if big.any() else 0.0,
+            "failing": int((~(err <= 2e-3 + 1e-2 * np.abs(ref))).sum()),
+            "tolerance": "|gpu - oracle| <= 2e-3 + 1e-2 |oracle|; max_rel over |oracle| >= 1e-3"}
+    return res
 
 
 def _time_calls(fn, n, flush, warm=3):
@@ -522,9 +552,10 @@ def bench_prefill_mix(pd, pd_inputs, dev, args, flush, bf16_peak, hbm_peak, peak
 def bench_long_context(pd, pd_inputs, dev, args, flush, hbm_peak):
     import torch
     res = {}
+    nl = args.long_context_layers
     for point, (B, ctx) in enumerate(pd_inputs.LONG_CONTEXT_POINTS):
         layers = []
-        for layer in range(32):
+        for layer in range(nl):
             lc = pd_inputs.long_context_layer(point, layer, device=dev)
             layers.append((lc.pool.key_cache, lc.pool.value_cache, lc.q))
         bt = lc.pool.block_tables.to(dev)
@@ -538,10 +569,10 @@ def bench_long_context(pd, pd_inputs, dev, args, flush, hbm_peak):
 
         t = _time_calls(step, max(3, args.extra_steps // 2), flush, warm=2)
         kv, alg = decode_alg_bytes([ctx] * B, B, lc.H, lc.Hk, lc.D, lc.pool.S)
-        res[f"{B}x{ctx}"] = {"step_ms": round(t * 1e3, 3),
-                             "gbs": round(32 * alg / t / 1e9, 1),
-                             "frac": round(32 * alg / t / 1e9 / hbm_peak, 4),
-                             "kv_tokens_per_s": round(32 * B * ctx / t, 1),
+        res[f"{B}x{ctx}"] = {"layers": nl, "step_ms": round(t * 1e3, 3),
+                             "gbs": round(nl * alg / t / 1e9, 1),
+                             "frac": round(nl * alg / t / 1e9 / hbm_peak, 4),
+                             "kv_tokens_per_s": round(nl * B * ctx / t, 1),
                              "partitions": -(-ctx // pd.pd_decode_partition_tokens(ctx))}
         del layers, outs
         torch.cuda.empty_cache()

@@ -159,13 +159,21 @@ PD_API pd_status pd_paged_attention_decode(void* out, const void* q,
  *   whose pd_decode_workspace_bytes(B, H, D, max_context_len) exceeds
  *   32 MiB (33554432 bytes) is rejected with PD_ERR_WORKSPACE_TOO_SMALL and
  *   nothing is launched.
- * - The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture on the device.
+ * - The array's device address is looked up (cudaGetSymbolAddress, with the
+ *   calling device current) on every call made outside stream capture, so a
+ *   module reloaded after cudaDeviceReset is never reached through a stale
+ *   address.  A call made while `stream` is capturing uses the address found
+ *   by the last call outside capture on that device: make the first call on
+ *   a device before any stream capture on it (otherwise PD_ERR_CUDA).
  * - Nothing in the scratch needs to start at zero (as for the workspace of
- *   pd_paged_attention_decode).
- * - All calls share the one array: calls that may overlap on the GPU (other
- *   streams, other host threads) race and must be serialised by the caller.
+ *   pd_paged_attention_decode): every call tags its arrival counters with a
+ *   tag of its own, so counts left behind by an earlier call, including one
+ *   that flagged PD_DEVERR_TIMEOUT, read as zero.  A launch repeated with an
+ *   unchanged tag would meet them; the caller has no address for the array
+ *   and cannot clear it.
+ * - All calls share the one array and it keeps what the last call wrote:
+ *   calls that may overlap on the GPU (other streams, other host threads)
+ *   race and must be serialised by the caller.
  * - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
 PD_API pd_status pd_paged_attention_decode_noalloc(void* out, const void* q,
                                            const void* key_cache,

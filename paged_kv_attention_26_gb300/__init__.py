@@ -18,6 +18,7 @@ step, one copy out), optionally replayed from a CUDA graph.
 """
 from __future__ import annotations
 
+import collections
 import ctypes
 import os
 import threading
@@ -581,18 +582,27 @@ def pd_paged_attention_decode_noalloc(out, q, key_cache, value_cache, block_tabl
     _check("pd_paged_attention_decode_noalloc", st)
 
 
-_ptr_arrays: dict = {}
+_ptr_arrays: "collections.OrderedDict" = collections.OrderedDict()
+_PTR_ARRAYS_MAX = 64
 
 
 def pointer_array(tensors, device=None):
-    """Device int64 array of the tensors' data pointers (cached per pointer tuple)."""
+    """Device int64 array of the tensors' data pointers, cached per (device,
+    pointer tuple); the cache keeps the _PTR_ARRAYS_MAX most recently used
+    arrays, so callers that reallocate their pools do not grow it without
+    bound.  An evicted array is freed through torch's stream-ordered caching
+    allocator, so a launch already enqueued with it still reads it."""
     torch = _torch()
-    key = tuple(t.data_ptr() for t in tensors)
+    dev = torch.device(device) if device is not None else tensors[0].device
+    key = (str(dev),) + tuple(t.data_ptr() for t in tensors)
     arr = _ptr_arrays.get(key)
     if arr is None:
-        dev = device or tensors[0].device
-        arr = torch.tensor(key, dtype=torch.int64).to(dev)
+        arr = torch.tensor(key[1:], dtype=torch.int64).to(dev)
         _ptr_arrays[key] = arr
+        while len(_ptr_arrays) > _PTR_ARRAYS_MAX:
+            _ptr_arrays.popitem(last=False)
+    else:
+        _ptr_arrays.move_to_end(key)
     return arr
 
 

@@ -26,6 +26,53 @@ pd_status launch_result(cudaError_t e) {
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+// Checks the decode arguments and fills *a; *skip is set when there is
+// nothing to launch (B == 0).  check_workspace_ptr == false skips the checks
+// of the workspace pointer (not its size): the caller supplies the address
+// after validation (the library's own scratch array).
+pd_status decode_prepare(void* out, const void* q, const void* key_cache,
+                         const void* value_cache, const float* k_scale, const float* v_scale,
+                         bool fp8, const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* context_lens, int B, int H, int Hk, int D, int S, int NB,
+                         int max_context_len, float scale, void* workspace,
+                         size_t workspace_bytes, pd_dtype dt, int32_t* dev_err,
+                         cudaStream_t stream, DecodeArgs* a, bool* skip, int nq,
+                         bool check_workspace_ptr) {
+    *skip = false;
+    if (nq < 1 || nq > 8) return PD_ERR_UNSUPPORTED;
+    if (B < 0 || H < 1 || Hk < 1 || NB < 1 || max_blocks_per_seq < 1 || max_context_len < 0)
+        return PD_ERR_INVALID_ARG;
+    if (H % Hk != 0) return PD_ERR_INVALID_ARG;
+    if (!supported_D(D) || !supported_S(S) || !supported_dt(dt)) return PD_ERR_UNSUPPORTED;
+    if (B == 0) {
+        *skip = true;
+        return PD_OK;
+    }
+    if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens)
+        return PD_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
+        return PD_ERR_INVALID_ARG;
+    if (int64_t(B) * nq > 65535 || int64_t(max_blocks_per_seq) * S > (int64_t(1) << 30) ||
+        decode_num_partitions(max_context_len) > 65535)
+        return PD_ERR_UNSUPPORTED;
+    const size_t need = decode_workspace_bytes(B * nq, H, D, max_context_len);
+    if (need > 0) {
+        if (check_workspace_ptr &&
+            (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+            return PD_ERR_INVALID_ARG;
+        if (workspace_bytes < need) return PD_ERR_WORKSPACE_TOO_SMALL;
+    }
+    if (fp8 && (!k_scale || !v_scale)) return PD_ERR_INVALID_ARG;
+    *a = DecodeArgs{out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
+                    context_lens, B, H, Hk, D, S, NB, max_context_len, scale, workspace, dt,
+                    dev_err, stream};
+    a->fp8 = fp8;
+    a->k_scale = k_scale;
+    a->v_scale = v_scale;
+    a->nq = nq;
+    return PD_OK;
+}
+
 }  // namespace pd
 
 using namespace pd;
@@ -94,50 +141,6 @@ size_t pd_decode_workspace_bytes(int B, int H, int D, int max_context_len) {
 
 int pd_decode_partition_tokens(int max_context_len) {
     return decode_partition_tokens(max_context_len);
-}
-
-// Checks the decode arguments and fills *a; *skip is set when there is
-// nothing to launch (B == 0).
-static pd_status decode_prepare(void* out, const void* q, const void* key_cache,
-                                const void* value_cache, const float* k_scale,
-                                const float* v_scale, bool fp8, const int32_t* block_tables,
-                                int max_blocks_per_seq, const int32_t* context_lens, int B, int H,
-                                int Hk, int D, int S, int NB, int max_context_len, float scale,
-                                void* workspace, size_t workspace_bytes, pd_dtype dt,
-                                int32_t* dev_err, cudaStream_t stream, DecodeArgs* a,
-                                bool* skip, int nq = 1) {
-    *skip = false;
-    if (nq < 1 || nq > 8) return PD_ERR_UNSUPPORTED;
-    if (B < 0 || H < 1 || Hk < 1 || NB < 1 || max_blocks_per_seq < 1 || max_context_len < 0)
-        return PD_ERR_INVALID_ARG;
-    if (H % Hk != 0) return PD_ERR_INVALID_ARG;
-    if (!supported_D(D) || !supported_S(S) || !supported_dt(dt)) return PD_ERR_UNSUPPORTED;
-    if (B == 0) {
-        *skip = true;
-        return PD_OK;
-    }
-    if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens)
-        return PD_ERR_INVALID_ARG;
-    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
-        return PD_ERR_INVALID_ARG;
-    if (int64_t(B) * nq > 65535 || int64_t(max_blocks_per_seq) * S > (int64_t(1) << 30) ||
-        decode_num_partitions(max_context_len) > 65535)
-        return PD_ERR_UNSUPPORTED;
-    const size_t need = decode_workspace_bytes(B * nq, H, D, max_context_len);
-    if (need > 0) {
-        if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-            return PD_ERR_INVALID_ARG;
-        if (workspace_bytes < need) return PD_ERR_WORKSPACE_TOO_SMALL;
-    }
-    if (fp8 && (!k_scale || !v_scale)) return PD_ERR_INVALID_ARG;
-    *a = DecodeArgs{out, q, key_cache, value_cache, block_tables, max_blocks_per_seq,
-                    context_lens, B, H, Hk, D, S, NB, max_context_len, scale, workspace, dt,
-                    dev_err, stream};
-    a->fp8 = fp8;
-    a->k_scale = k_scale;
-    a->v_scale = v_scale;
-    a->nq = nq;
-    return PD_OK;
 }
 
 static pd_status decode_common(void* out, const void* q, const void* key_cache,

@@ -10,9 +10,13 @@
 // The scratch is a file-scope __device__ array of kStaticScratchBytes
 // (32 MiB).  Every GPU that loads this library keeps it until the process
 // exits.  Host code cannot use the array's name as a device address (on the
-// host it names a stand-in object), so the address is looked up once per
-// device with cudaGetSymbolAddress, with that device current, the first time
-// the entry point runs on it.
+// host it names a stand-in object), so the address comes from
+// cudaGetSymbolAddress with the calling device current.  Outside stream
+// capture the lookup is repeated on every call (a host-side lookup, cheap),
+// so an address that changed -- the module loaded again after
+// cudaDeviceReset -- is never used stale; during capture the address found
+// by the last call outside capture on that device is used, which is why the
+// first call on a device must come before any capture.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -30,11 +34,11 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
 std::mutex g_setup_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+void* g_scratch_ptr[kMaxDevices] = {};   // last address looked up per device
 
-// Device address of the scratch array on the current device (looked up once
-// per device).  nullptr with *err set on failure.
-void* scratch_for_current_device(cudaError_t* err) {
+// Device address of the scratch array on the current device.  nullptr with
+// *err set on failure.
+void* scratch_for_current_device(cudaStream_t stream, cudaError_t* err) {
     int dev = 0;
     *err = cudaGetDevice(&dev);
     if (*err != cudaSuccess) return nullptr;
@@ -42,14 +46,21 @@ void* scratch_for_current_device(cudaError_t* err) {
         *err = cudaErrorInvalidDevice;
         return nullptr;
     }
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    *err = cudaStreamIsCapturing(stream, &cap);
+    if (*err != cudaSuccess) return nullptr;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        *err = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (*err != cudaSuccess) return nullptr;
-        g_scratch_ptr[dev] = p;
+    if (cap != cudaStreamCaptureStatusNone) {
+        // no lookup while capturing: a device whose address was never looked
+        // up outside capture is refused
+        if (g_scratch_ptr[dev] == nullptr) *err = cudaErrorStreamCaptureUnsupported;
+        return g_scratch_ptr[dev];
     }
-    return g_scratch_ptr[dev];
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    g_scratch_ptr[dev] = p;
+    return p;
 }
 
 }  // namespace
@@ -67,26 +78,21 @@ pd_status pd_paged_attention_decode_noalloc(void* out, const void* q, const void
                                             int D, int S, int NB, int max_context_len,
                                             float scale, pd_dtype dt, int32_t* dev_err,
                                             cudaStream_t stream) {
-    if (B < 0 || H < 1 || Hk < 1 || NB < 1 || max_blocks_per_seq < 1 || max_context_len < 0)
-        return PD_ERR_INVALID_ARG;
-    if (H % Hk != 0) return PD_ERR_INVALID_ARG;
-    if (!supported_D(D) || !supported_S(S) || !supported_dt(dt)) return PD_ERR_UNSUPPORTED;
-    if (B == 0) return PD_OK;
-    if (!out || !q || !key_cache || !value_cache || !block_tables || !context_lens)
-        return PD_ERR_INVALID_ARG;
-    if (!aligned16(out) || !aligned16(q) || !aligned16(key_cache) || !aligned16(value_cache))
-        return PD_ERR_INVALID_ARG;
-    if (B > 65535 || int64_t(max_blocks_per_seq) * S > (int64_t(1) << 30) ||
-        decode_num_partitions(max_context_len) > 65535)
-        return PD_ERR_UNSUPPORTED;
-    // The batch's partition scratch must fit the fixed array.
-    if (decode_workspace_bytes(B, H, D, max_context_len) > kStaticScratchBytes)
-        return PD_ERR_WORKSPACE_TOO_SMALL;
+    // The checks of pd_paged_attention_decode, with the array's size as the
+    // workspace size: a batch whose partition scratch does not fit gets
+    // PD_ERR_WORKSPACE_TOO_SMALL.  The address is filled in afterwards.
+    DecodeArgs a{};
+    bool skip = false;
+    const pd_status st = decode_prepare(out, q, key_cache, value_cache, nullptr, nullptr, false,
+                                        block_tables, max_blocks_per_seq, context_lens, B, H, Hk,
+                                        D, S, NB, max_context_len, scale, nullptr,
+                                        kStaticScratchBytes, dt, dev_err, stream, &a, &skip, 1,
+                                        /*check_workspace_ptr=*/false);
+    if (st != PD_OK || skip) return st;
     cudaError_t e = cudaSuccess;
-    void* scratch = scratch_for_current_device(&e);
+    void* scratch = scratch_for_current_device(stream, &e);
     if (scratch == nullptr) return launch_result(e);
-    DecodeArgs a{out, q, key_cache, value_cache, block_tables, max_blocks_per_seq, context_lens,
-                 B, H, Hk, D, S, NB, max_context_len, scale, scratch, dt, dev_err, stream};
+    a.workspace = scratch;
     return launch_decode(a);
 }
 

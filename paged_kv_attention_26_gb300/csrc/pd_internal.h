@@ -48,6 +48,17 @@ struct DecodeArgs {
     int nq = 1;                  // query tokens per sequence (> 1: speculative verification)
 };
 pd_status launch_decode(const DecodeArgs& a);
+// Argument checks shared by every decode entry point (defined with the C
+// ABI); fills *a, sets *skip when B == 0.  check_workspace_ptr == false
+// leaves the workspace address to the caller (checked size only).
+pd_status decode_prepare(void* out, const void* q, const void* key_cache,
+                         const void* value_cache, const float* k_scale, const float* v_scale,
+                         bool fp8, const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* context_lens, int B, int H, int Hk, int D, int S, int NB,
+                         int max_context_len, float scale, void* workspace,
+                         size_t workspace_bytes, pd_dtype dt, int32_t* dev_err,
+                         cudaStream_t stream, DecodeArgs* a, bool* skip, int nq = 1,
+                         bool check_workspace_ptr = true);
 pd_status launch_bounded_wait_selftest(int32_t* dev_err, unsigned long long limit_ns,
                                        cudaStream_t stream);
 pd_status launch_copy_bytes(void* dst, const void* src, size_t bytes, cudaStream_t stream);

@@ -24,12 +24,24 @@ def u16(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16).copy()
 
 
+# One record per comparison made in this process: (what, elements, max abs
+# error, max rel error over |oracle| >= 1e-3, failing elements, largest
+# err / (atol + rtol |oracle|)).  The conftest prints them at the end of a run,
+# so a passing run still shows how close each case came to the bound.
+RECORDS: list = []
+
+
 def assert_close(gpu: torch.Tensor, ref: np.ndarray, what: str, atol=ATOL, rtol=RTOL):
     g = gpu.detach().cpu().to(torch.float64).numpy()
     assert g.shape == ref.shape, (g.shape, ref.shape)
     assert np.isfinite(ref).all(), f"{what}: oracle produced non-finite values"
     err = np.abs(g - ref)
     bad = ~(err <= atol + rtol * np.abs(ref))       # NaN counts as bad
+    if err.size:
+        big = np.abs(ref) >= 1e-3
+        RECORDS.append((what, int(err.size), float(np.nanmax(err)),
+                        float(np.nanmax(err[big] / np.abs(ref[big]))) if big.any() else 0.0,
+                        int(bad.sum()), float(np.nanmax(err / (atol + rtol * np.abs(ref))))))
     if bad.any():
         idx = np.argwhere(bad)[:5].tolist()
         rel = err / np.maximum(np.abs(ref), 1e-30)
