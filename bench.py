@@ -765,13 +765,20 @@ def bench_cow(pd, pd_inputs, dev, args, flush, hbm_peak):
         unique_blocks = len({b for t in tables for b in t})
         unique = unique_blocks * S * fc.Hk * fc.D * 2 * 2
         copy_bytes = 2 * len(pairs) * 2 * fc.Hk * S * fc.D * 2
+        # DRAM bytes of one decode launch from the committed ncu capture of this
+        # source (None once the kernel changed since)
+        dram = profiled_traffic(f"paged_decode_cow_S{S}", source_sha("decode.cu", "pd_device.cuh"))
         res[f"S{S}"] = {"pairs": len(pairs), "step_ms": round(t_step * 1e3, 4),
                         "copy_ms": round(t_copy * 1e3, 4),
                         "copy_gbs": round(copy_bytes / t_copy / 1e9, 1),
                         "decode_ms": round(t_dec * 1e3, 4),
                         "decode_logical_gbs": round(logical / t_dec / 1e9, 1),
                         "decode_unique_gbs": round(unique / t_dec / 1e9, 1),
-                        "decode_unique_frac": round(unique / t_dec / 1e9 / hbm_peak, 4)}
+                        "decode_unique_frac": round(unique / t_dec / 1e9 / hbm_peak, 4),
+                        "decode_dram_bytes": dram,
+                        "decode_dram_over_unique": round(dram / unique, 3) if dram else None,
+                        "decode_dram_frac": (round(dram / t_dec / 1e9 / hbm_peak, 4)
+                                             if dram else None)}
     return res
 
 
