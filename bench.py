@@ -761,6 +761,28 @@ def bench_cow(pd, pd_inputs, dev, args, flush, hbm_peak):
             pd.pd_paged_attention_decode(out, q, kc, vc, bt, cl, mcl, fc.scale, ws)
 
         t_step = _time_calls(whole, n, flush)
+        # the same decode with each prompt's shared blocks read once for its
+        # forks: groups from the host helper (outside the timing)
+        grp_starts, grp_shared = pd.find_shared_prefixes(bt.cpu(), cl.cpu(), S,
+                                                         max_group=fc.n_fork)
+        gs_d, sl_d = grp_starts.to(dev), grp_shared.to(dev)
+        ws_sh = pd.decode_shared_workspace(grp_shared.numel(), fc.n_fork, fc.H, fc.Hk, fc.D,
+                                           device=dev)
+
+        def shared_decode():
+            pd.pd_paged_attention_decode_shared(out, q, kc, vc, bt, cl, mcl, fc.scale, gs_d, sl_d,
+                                                fc.n_fork, ws_sh)
+
+        t_sh = _time_calls(shared_decode, n, flush)
+
+        def whole_shared():
+            pd.pd_copy_blocks([kc], [vc], pr)
+            pd.pd_reshape_and_cache(nk, nv, kc, vc, sl)
+            shared_decode()
+
+        t_step_sh = _time_calls(whole_shared, n, flush)
+        sha = source_sha("decode.cu", "pd_device.cuh")
+        dram_sh = profiled_traffic(f"paged_decode_shared_cow_S{S}", sha)
         _, logical = decode_alg_bytes(ctxs, len(tables), fc.H, fc.Hk, fc.D, S)
         unique_blocks = len({b for t in tables for b in t})
         unique = unique_blocks * S * fc.Hk * fc.D * 2 * 2
@@ -768,7 +790,8 @@ def bench_cow(pd, pd_inputs, dev, args, flush, hbm_peak):
         # DRAM bytes of one decode launch from the committed ncu capture of this
         # source (None once the kernel changed since)
         dram = profiled_traffic(f"paged_decode_cow_S{S}", source_sha("decode.cu", "pd_device.cuh"))
-        res[f"S{S}"] = {"pairs": len(pairs), "step_ms": round(t_step * 1e3, 4),
+        res[f"S{S}"] = {"pairs": len(pairs), "groups": grp_shared.numel(),
+                        "step_ms": round(t_step * 1e3, 4),
                         "copy_ms": round(t_copy * 1e3, 4),
                         "copy_gbs": round(copy_bytes / t_copy / 1e9, 1),
                         "decode_ms": round(t_dec * 1e3, 4),
@@ -778,7 +801,20 @@ def bench_cow(pd, pd_inputs, dev, args, flush, hbm_peak):
                         "decode_dram_bytes": dram,
                         "decode_dram_over_unique": round(dram / unique, 3) if dram else None,
                         "decode_dram_frac": (round(dram / t_dec / 1e9 / hbm_peak, 4)
-                                             if dram else None)}
+                                             if dram else None),
+                        "shared": {
+                            "path": "pd_paged_attention_decode_shared (each prompt's shared "
+                                    "blocks read once for its 8 forks)",
+                            "decode_ms": round(t_sh * 1e3, 4),
+                            "step_ms": round(t_step_sh * 1e3, 4),
+                            "decode_unique_gbs": round(unique / t_sh / 1e9, 1),
+                            "decode_unique_frac": round(unique / t_sh / 1e9 / hbm_peak, 4),
+                            "decode_logical_gbs": round(logical / t_sh / 1e9, 1),
+                            "decode_dram_bytes": dram_sh,
+                            "decode_dram_over_unique": (round(dram_sh / unique, 3)
+                                                        if dram_sh else None),
+                            "decode_dram_frac": (round(dram_sh / t_sh / 1e9 / hbm_peak, 4)
+                                                 if dram_sh else None)}}
     return res
 
 

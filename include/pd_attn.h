@@ -71,6 +71,8 @@ typedef enum pd_dtype { PD_F16 = 0, PD_BF16 = 1, PD_FP8_E4M3 = 2 } pd_dtype;
 #define PD_DEVERR_BLOCK_RANGE 0x2 /* block id outside [0, NB)                */
 #define PD_DEVERR_CTX_RANGE 0x4   /* context longer than table / promise     */
 #define PD_DEVERR_TIMEOUT 0x8     /* a bounded wait inside a kernel expired  */
+#define PD_DEVERR_SHARED_PREFIX 0x10 /* shared-prefix groups malformed, or a
+                                        member's table differs in the prefix */
 
 /* Text for a status code (static storage). */
 PD_API const char* pd_status_string(pd_status s);
@@ -185,6 +187,78 @@ PD_API pd_status pd_paged_attention_decode_noalloc(void* out, const void* q,
                                            int max_context_len, float scale,
                                            pd_dtype dt, int32_t* dev_err,
                                            cudaStream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Decode attention for forks that share a prompt's blocks (tutorial page "LLM
+ * 推理服务引擎深度拆解", section 2.3: parallel sampling forks a sequence n ways,
+ * every fork keeps the prompt's blocks, with zero copies, and only a written
+ * shared block is copied; nanoPD page "分页KV缓存": CoW for beam search and
+ * speculative branches).  Same operation and result as
+ * pd_paged_attention_decode on the same arguments; the work is arranged so
+ * that each shared block is read from memory once for all the forks that
+ * hold it, instead of once per fork.
+ *   group_starts  DEVICE int32 [n_groups + 1]: group g is sequences
+ *                 group_starts[g] .. group_starts[g+1] - 1 (consecutive);
+ *                 group_starts[0] == 0, non-decreasing, group_starts[n_groups]
+ *                 == B, at most max_group members per group
+ *   shared_lens   DEVICE int32 [n_groups]: the caller's promise that every
+ *                 member's block table holds the first member's block ids
+ *                 over its first shared_lens[g] tokens.  The kernel uses
+ *                 sh = shared_lens[g] rounded down to a multiple of S and cut
+ *                 to the shortest member's context, reads tokens [0, sh) of
+ *                 every member through the FIRST member's table and the rest
+ *                 through each member's own.  A group layout that breaks the
+ *                 rules above, or a member whose table differs from the first
+ *                 member's within [0, sh), flags PD_DEVERR_SHARED_PREFIX
+ *                 (checked on the device; results of that group unspecified).
+ *                 shared_lens[g] == 0 is allowed (no sharing).
+ *   max_group     1 .. 32 (sizes the column layout; (H / Hk) heads of up to
+ *                 32 / max_group forks go through one pass over a kv head)
+ *   workspace     device scratch of at least
+ *                 pd_decode_shared_workspace_bytes(n_groups, max_group, H, Hk,
+ *                 D) bytes, 256-byte aligned, same rules as the workspace of
+ *                 pd_paged_attention_decode (nothing needs to start at zero)
+ * every other argument as for pd_paged_attention_decode (16-bit pools).
+ * With fp16 elements, probabilities enter the P.V product as one fp16 value
+ * (2^-11 relative rounding); with bf16 as a hi + lo pair as in decode.
+ * PD_ERR_UNSUPPORTED: max_group outside 1 .. 32, n_groups < 1 or > 65535. */
+PD_API size_t pd_decode_shared_workspace_bytes(int n_groups, int max_group, int H, int Hk,
+                                               int D);
+PD_API pd_status pd_paged_attention_decode_shared(void* out, const void* q,
+                                                  const void* key_cache,
+                                                  const void* value_cache,
+                                                  const int32_t* block_tables,
+                                                  int max_blocks_per_seq,
+                                                  const int32_t* context_lens, int B, int H,
+                                                  int Hk, int D, int S, int NB,
+                                                  int max_context_len, float scale,
+                                                  const int32_t* group_starts,
+                                                  const int32_t* shared_lens, int n_groups,
+                                                  int max_group, void* workspace,
+                                                  size_t workspace_bytes, pd_dtype dt,
+                                                  int32_t* dev_err, cudaStream_t stream);
+/* Host helper for the call above (no CUDA calls): cut sequences 0 .. B-1 into
+ * groups of consecutive sequences that share leading blocks.  block_tables and
+ * context_lens are HOST arrays laid out as for the decode calls.  For each
+ * sequence i, its shared prefix with the first member f of the current group
+ * is n * S tokens, n = the number of leading entries with
+ * block_tables[i][b] == block_tables[f][b], counting only blocks b that are
+ * full in both (b < min(ctx_i, ctx_f) / S).  Sequence i joins the group when
+ * the group has fewer than max_group members and that prefix is at least
+ * max(min_shared_tokens, S) tokens and at least the group's current shared
+ * length (a later member never shortens what the earlier ones share); else
+ * it starts a new group.  A group's shared_lens entry is its members' common
+ * prefix (0 for a group of one).
+ *   group_starts_out  [B + 1] (n_groups + 1 entries written)
+ *   shared_lens_out   [B]     (n_groups entries written)
+ * PD_ERR_INVALID_ARG on NULL pointers (block_tables, context_lens and
+ * shared_lens_out may be NULL when B == 0), B < 0, max_blocks_per_seq < 1,
+ * S < 1, or max_group outside 1 .. 32. */
+PD_API pd_status pd_find_shared_prefixes(const int32_t* block_tables, int max_blocks_per_seq,
+                                         const int32_t* context_lens, int B, int S,
+                                         int max_group, int min_shared_tokens,
+                                         int32_t* group_starts_out, int32_t* shared_lens_out,
+                                         int* n_groups_out);
 
 /* ---------------------------------------------------------------------- */
 /* FP8 (E4M3) KV cache (essay page "LLM推理PD分离架构深度工程实践", section

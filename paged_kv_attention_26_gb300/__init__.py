@@ -33,6 +33,7 @@ PD_DEVERR_SLOT_RANGE = 0x1
 PD_DEVERR_BLOCK_RANGE = 0x2
 PD_DEVERR_CTX_RANGE = 0x4
 PD_DEVERR_TIMEOUT = 0x8
+PD_DEVERR_SHARED_PREFIX = 0x10
 
 STATUS_NAMES = {0: "PD_OK", 1: "PD_ERR_INVALID_ARG", 2: "PD_ERR_UNSUPPORTED", 3: "PD_ERR_CUDA",
                 4: "PD_ERR_NO_FREE_BLOCK", 5: "PD_ERR_WORKSPACE_TOO_SMALL",
@@ -55,6 +56,14 @@ SIGNATURES = {
                                        _F, _P, _SZ, _I, _P, _P]),
     "pd_paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
                                                _I, _I, _F, _I, _P, _P]),
+    "pd_decode_shared_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "pd_paged_attention_decode_shared": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
+                                              _I, _I, _F, _P, _P, _I, _I, _P, _SZ, _I, _P, _P]),
+    "pd_find_shared_prefixes": (_I, [ctypes.POINTER(ctypes.c_int32), _I,
+                                     ctypes.POINTER(ctypes.c_int32), _I, _I, _I, _I,
+                                     ctypes.POINTER(ctypes.c_int32),
+                                     ctypes.POINTER(ctypes.c_int32),
+                                     ctypes.POINTER(ctypes.c_int)]),
     "pd_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pd_reshape_and_cache_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I64, _I64,
                                       _P, _P, _I, _P, _P]),
@@ -315,6 +324,77 @@ def pd_paged_attention_decode(out, q, key_cache, value_cache, block_tables, cont
         NB, int(max_context_len), float(scale), ws_ptr, ws_bytes, dt, _opt(dev_err),
         _stream(stream))
     _check("pd_paged_attention_decode", st)
+
+
+def pd_decode_shared_workspace_bytes(n_groups: int, max_group: int, H: int, Hk: int,
+                                     D: int) -> int:
+    return int(load().pd_decode_shared_workspace_bytes(n_groups, max_group, H, Hk, D))
+
+
+def decode_shared_workspace(n_groups, max_group, H, Hk, D, device="cuda"):
+    """Allocate the workspace of ``pd_paged_attention_decode_shared``."""
+    torch = _torch()
+    n = pd_decode_shared_workspace_bytes(n_groups, max_group, H, Hk, D)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def find_shared_prefixes(block_tables, context_lens, S: int, max_group: int = 8,
+                         min_shared_tokens: int = 0):
+    """Groups of consecutive sequences sharing leading blocks (host tensors in,
+    ``pd_find_shared_prefixes``): returns (group_starts int32 [n_groups + 1],
+    shared_lens int32 [n_groups]) as CPU tensors."""
+    torch = _torch()
+    bt = block_tables.detach().to("cpu", torch.int32).contiguous()
+    cl = context_lens.detach().to("cpu", torch.int32).contiguous()
+    B, mb = bt.shape
+    if cl.shape != (B,):
+        raise ValueError("context_lens shape")
+    gs = torch.zeros(B + 1, dtype=torch.int32)
+    sl = torch.zeros(max(B, 1), dtype=torch.int32)
+    n = ctypes.c_int(0)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    st = load().pd_find_shared_prefixes(
+        ctypes.cast(bt.data_ptr(), i32p), mb, ctypes.cast(cl.data_ptr(), i32p), B, int(S),
+        int(max_group), int(min_shared_tokens), ctypes.cast(gs.data_ptr(), i32p),
+        ctypes.cast(sl.data_ptr(), i32p), ctypes.byref(n))
+    _check("pd_find_shared_prefixes", st)
+    return gs[:n.value + 1].clone(), sl[:n.value].clone()
+
+
+def pd_paged_attention_decode_shared(out, q, key_cache, value_cache, block_tables,
+                                     context_lens, max_context_len: int, scale: float,
+                                     group_starts, shared_lens, max_group: int,
+                                     workspace=None, dev_err=None, stream=None):
+    """Decode for groups of forks that share leading blocks: the result of
+    ``pd_paged_attention_decode``, each shared block read once per group.
+    group_starts int32 CUDA [n_groups + 1], shared_lens int32 CUDA [n_groups]
+    (from ``find_shared_prefixes``); ``workspace`` from
+    ``decode_shared_workspace``."""
+    torch = _torch()
+    B, H, D = q.shape
+    NB, Hk, S, D2 = key_cache.shape
+    if out.shape != q.shape or D2 != D or value_cache.shape != key_cache.shape:
+        raise ValueError("shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables / context_lens shape")
+    n_groups = shared_lens.numel()
+    if group_starts.shape != (n_groups + 1,):
+        raise ValueError("group_starts must have n_groups + 1 entries")
+    dt = _dt(key_cache)
+    for t in (q, out, value_cache):
+        if t.dtype != key_cache.dtype:
+            raise TypeError("dtype mismatch")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    st = load().pd_paged_attention_decode_shared(
+        _dev(out, "out"), _dev(q, "q"), _dev(key_cache, "key_cache"),
+        _dev(value_cache, "value_cache"), _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), B, H, Hk, D, S,
+        NB, int(max_context_len), float(scale), _dev(group_starts, "group_starts", torch.int32),
+        _dev(shared_lens, "shared_lens", torch.int32), n_groups, int(max_group), ws_ptr,
+        ws_bytes, dt, _opt(dev_err), _stream(stream))
+    _check("pd_paged_attention_decode_shared", st)
 
 
 def pd_paged_attention_verify(out, q, key_cache, value_cache, block_tables, context_lens,

@@ -8,6 +8,7 @@
 // by a fresh copy (copy-on-write) and a private one is written in place; fork
 // shares every block and copies nothing.  The allocation order is part of the
 // contract so a replay of the same operations yields the same ids.
+#include <algorithm>
 #include <cstdint>
 #include <new>
 #include <unordered_map>
@@ -181,3 +182,53 @@ pd_status pd_bm_drop(pd_bm* bm, int block_id) {
 }
 
 }  // extern "C"
+
+// Groups of consecutive sequences sharing leading blocks, for the
+// shared-prefix decode (pd_attn.h states the rule).  Pure host code.
+extern "C" pd_status pd_find_shared_prefixes(const int32_t* block_tables, int max_blocks_per_seq,
+                                             const int32_t* context_lens, int B, int S,
+                                             int max_group, int min_shared_tokens,
+                                             int32_t* group_starts_out, int32_t* shared_lens_out,
+                                             int* n_groups_out) {
+    if ((B > 0 && (!block_tables || !context_lens || !shared_lens_out)) || !group_starts_out ||
+        !n_groups_out || B < 0 || max_blocks_per_seq < 1 || S < 1 || max_group < 1 ||
+        max_group > 32)
+        return PD_ERR_INVALID_ARG;
+    const int64_t cap = int64_t(max_blocks_per_seq) * S;
+    auto ctx_of = [&](int i) -> int64_t {
+        const int64_t c = context_lens[i];
+        return c < 0 ? 0 : (c > cap ? cap : c);
+    };
+    // tokens of the leading full blocks that sequences i and f share
+    auto common = [&](int i, int f) -> int64_t {
+        const int64_t full = std::min(ctx_of(i), ctx_of(f)) / S;
+        const int32_t* ti = block_tables + int64_t(i) * max_blocks_per_seq;
+        const int32_t* tf = block_tables + int64_t(f) * max_blocks_per_seq;
+        int64_t n = 0;
+        while (n < full && ti[n] == tf[n]) ++n;
+        return n * S;
+    };
+    const int64_t need = std::max<int64_t>(min_shared_tokens, S);
+    int ng = 0, first = 0, members = B > 0 ? 1 : 0;
+    int64_t shared = 0;
+    group_starts_out[0] = 0;
+    for (int i = 1; i < B; ++i) {
+        const int64_t c = common(i, first);
+        if (members < max_group && c >= need && (members == 1 || c >= shared)) {
+            if (members == 1) shared = c;
+            ++members;
+            continue;
+        }
+        shared_lens_out[ng] = members > 1 ? int32_t(shared) : 0;
+        group_starts_out[++ng] = i;
+        first = i;
+        members = 1;
+        shared = 0;
+    }
+    if (B > 0) {
+        shared_lens_out[ng] = members > 1 ? int32_t(shared) : 0;
+        group_starts_out[++ng] = B;
+    }
+    *n_groups_out = ng;
+    return PD_OK;
+}

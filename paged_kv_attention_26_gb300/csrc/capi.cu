@@ -37,9 +37,12 @@ pd_status decode_prepare(void* out, const void* q, const void* key_cache,
                          int max_context_len, float scale, void* workspace,
                          size_t workspace_bytes, pd_dtype dt, int32_t* dev_err,
                          cudaStream_t stream, DecodeArgs* a, bool* skip, int nq,
-                         bool check_workspace_ptr) {
+                         bool check_workspace_ptr, const SharedGroups* grp) {
     *skip = false;
     if (nq < 1 || nq > 8) return PD_ERR_UNSUPPORTED;
+    if (grp && (grp->max_group < 1 || grp->max_group > 32 || grp->n_groups < 1 ||
+                grp->n_groups > 65535 || nq != 1))
+        return PD_ERR_UNSUPPORTED;
     if (B < 0 || H < 1 || Hk < 1 || NB < 1 || max_blocks_per_seq < 1 || max_context_len < 0)
         return PD_ERR_INVALID_ARG;
     if (H % Hk != 0) return PD_ERR_INVALID_ARG;
@@ -55,7 +58,10 @@ pd_status decode_prepare(void* out, const void* q, const void* key_cache,
     if (int64_t(B) * nq > 65535 || int64_t(max_blocks_per_seq) * S > (int64_t(1) << 30) ||
         decode_num_partitions(max_context_len) > 65535)
         return PD_ERR_UNSUPPORTED;
-    const size_t need = decode_workspace_bytes(B * nq, H, D, max_context_len);
+    if (grp && (!grp->start || !grp->shared)) return PD_ERR_INVALID_ARG;
+    const size_t need = grp ? decode_shared_workspace_bytes(grp->n_groups, grp->max_group, H,
+                                                            Hk, D)
+                            : decode_workspace_bytes(B * nq, H, D, max_context_len);
     if (need > 0) {
         if (check_workspace_ptr &&
             (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
@@ -70,6 +76,12 @@ pd_status decode_prepare(void* out, const void* q, const void* key_cache,
     a->k_scale = k_scale;
     a->v_scale = v_scale;
     a->nq = nq;
+    if (grp) {
+        a->grp_start = grp->start;
+        a->grp_shared = grp->shared;
+        a->n_groups = grp->n_groups;
+        a->max_group = grp->max_group;
+    }
     return PD_OK;
 }
 
@@ -251,6 +263,35 @@ pd_status pd_decode_step_fp8(const void* key, const void* value, const int64_t* 
                        key_cache, value_cache, k_scale, v_scale, true, block_tables,
                        max_blocks_per_seq, context_lens, B, H, Hk, D, S, NB, max_context_len,
                        scale, workspace, workspace_bytes, dt, dev_err, stream);
+}
+
+size_t pd_decode_shared_workspace_bytes(int n_groups, int max_group, int H, int Hk, int D) {
+    if (n_groups < 1 || n_groups > 65535 || max_group < 1 || max_group > 32 || H < 1 ||
+        Hk < 1 || H % Hk != 0 || !supported_D(D))
+        return 0;
+    return decode_shared_workspace_bytes(n_groups, max_group, H, Hk, D);
+}
+
+pd_status pd_paged_attention_decode_shared(void* out, const void* q, const void* key_cache,
+                                           const void* value_cache, const int32_t* block_tables,
+                                           int max_blocks_per_seq, const int32_t* context_lens,
+                                           int B, int H, int Hk, int D, int S, int NB,
+                                           int max_context_len, float scale,
+                                           const int32_t* group_starts,
+                                           const int32_t* shared_lens, int n_groups,
+                                           int max_group, void* workspace,
+                                           size_t workspace_bytes, pd_dtype dt, int32_t* dev_err,
+                                           cudaStream_t stream) {
+    DecodeArgs a{};
+    bool skip = false;
+    const SharedGroups grp{group_starts, shared_lens, n_groups, max_group};
+    const pd_status st = decode_prepare(out, q, key_cache, value_cache, nullptr, nullptr, false,
+                                        block_tables, max_blocks_per_seq, context_lens, B, H, Hk,
+                                        D, S, NB, max_context_len, scale, workspace,
+                                        workspace_bytes, dt, dev_err, stream, &a, &skip, 1, true,
+                                        &grp);
+    if (st != PD_OK || skip) return st;
+    return launch_decode(a);
 }
 
 pd_status pd_paged_attention_verify(void* out, const void* q, const void* key_cache,

@@ -128,13 +128,35 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int tok, int chunk) {
 // same index in every group therefore walk the same blocks at the same time,
 // one head slab each, and a block's slabs lie side by side in the pool, so
 // DRAM sees its neighbouring slabs read together.
+//
+// Shared-prefix mode: a stream is a group of consecutive sequences (forks of
+// one prompt) whose block tables agree on their first blocks.  Its stages are
+// the shared prefix, read once through the first member's table, followed by
+// each member's own remaining tokens ("tails"), read through that member's
+// table; a tail stage is seen only by that member's columns.
 struct Walk {
-    int s, u, L, ctx;     // current stream and its sequence's stage count / tokens
+    int s, u, L, ctx;     // current stream and its stage count / tokens (decode, verify)
     long start;           // stage index (in the unit's order) of the stream's first stage
     int off;              // next stage within the stream
     long pos, end;        // next stage; end of this CTA's range
     long per_cta;
     int bi;               // this CTA's index within its unit group
+    // shared-prefix mode: the group (first sequence, members, shared tokens)
+    // and the part the next stage falls in (pj = -1: the shared prefix, else
+    // member pj's tail; stage pk of the part's plen, tokens [pt0, pend))
+    int lead, nmem, sh;
+    int pj, pk, plen, pt0, pend;
+};
+
+// Groups of the shared-prefix mode: sequences start[k] .. start[k+1]-1 share
+// their first shared[k] tokens' blocks (rounded down to whole blocks and to
+// the shortest member's context); at most Mmax members.
+struct ForkArgs {
+    const int32_t* start;     // [n_groups + 1]
+    const int32_t* shared;    // [n_groups]
+    int nseq;                 // sequences (rows of q / out)
+    int Mmax;                 // most members a group may have (column layout)
+    int ppu;                  // workspace pieces per unit: n_groups + CTAs per unit
 };
 
 __device__ __forceinline__ int stream_ctx(const int32_t* __restrict__ context_lens, int s,
@@ -143,9 +165,123 @@ __device__ __forceinline__ int stream_ctx(const int32_t* __restrict__ context_le
     return c < 0 ? 0 : (c > cap ? cap : c);
 }
 
+// Group k: first sequence, member count (0 for a malformed group), shared
+// tokens (a multiple of S, at most every member's context) and, if L is
+// given, its stages.  The members' context lengths are loaded eight at a
+// time, so a group costs about one load latency, not one per member.
+__device__ __forceinline__ void group_info(const ForkArgs& f,
+                                           const int32_t* __restrict__ context_lens, int k,
+                                           int cap, int S, int& lead, int& n, int& sh,
+                                           long* L = nullptr) {
+    const int a = __ldg(f.start + k), b = __ldg(f.start + k + 1);
+    const int want = __ldg(f.shared + k);
+    const bool bad = a < 0 || b < a || b > f.nseq || b - a > f.Mmax;
+    lead = a;
+    n = bad ? 0 : b - a;
+    int c[8];
+    int mn = cap;
+    long tail_sum = 0;                 // stages of the members' tails, once sh is known
+    for (int j0 = 0; j0 < n; j0 += 8) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = j0 + i < n ? stream_ctx(context_lens, a + j0 + i, cap) : cap;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mn = min(mn, c[i]);
+    }
+    sh = n > 0 ? (max(0, min(want, mn)) & ~(S - 1)) : 0;
+    if (L == nullptr) return;
+    for (int j0 = 0; j0 < n; j0 += 8) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            c[i] = j0 + i < n ? stream_ctx(context_lens, a + j0 + i, cap) : sh;   // L1 hits
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tail_sum += (c[i] - sh + 63) / 64;
+    }
+    *L = n > 0 ? (sh + 63) / 64 + tail_sum : 0;
+}
+
+__device__ __forceinline__ long group_stages(const ForkArgs& f,
+                                             const int32_t* __restrict__ context_lens, int k,
+                                             int cap, int S) {
+    int lead, n, sh;
+    long L;
+    group_info(f, context_lens, k, cap, S, lead, n, sh, &L);
+    return L;
+}
+
+// Stages of stream k: ceil(ctx / 64) for a sequence; shared prefix plus tails
+// for a group.
+template <bool kFork>
+__device__ __forceinline__ long stream_stages(const int32_t* __restrict__ context_lens, int k,
+                                              int cap, int S, const ForkArgs& f) {
+    if constexpr (kFork) return group_stages(f, context_lens, k, cap, S);
+    return long((stream_ctx(context_lens, k, cap) + 63) / 64);
+}
+
+// Shared-prefix mode: place the part walk at stage `off` of the group stream.
+__device__ __forceinline__ void part_seek(Walk& w, const int32_t* __restrict__ context_lens,
+                                          int cap, int off) {
+    const int ls = (w.sh + 63) / 64;
+    w.pj = -1;
+    w.pk = off;
+    w.plen = ls;
+    w.pt0 = 0;
+    w.pend = w.sh;
+    if (off < ls) return;
+    off -= ls;
+    for (int j = 0; j < w.nmem; ++j) {
+        const int c = stream_ctx(context_lens, w.lead + j, cap);
+        const int l = (c - w.sh + 63) / 64;
+        if (off < l) {
+            w.pj = j;
+            w.pk = off;
+            w.plen = l;
+            w.pt0 = w.sh;
+            w.pend = c;
+            return;
+        }
+        off -= l;
+    }
+}
+
+// Shared-prefix mode: the next stage of the group stream (the next member
+// with a non-empty tail once a part is used up; nothing past the stream).
+__device__ __forceinline__ void part_next(Walk& w, const int32_t* __restrict__ context_lens,
+                                          int cap) {
+    if (++w.pk < w.plen) return;
+    for (int j = w.pj + 1; j < w.nmem; ++j) {
+        const int c = stream_ctx(context_lens, w.lead + j, cap);
+        const int l = (c - w.sh + 63) / 64;
+        if (l > 0) {
+            w.pj = j;
+            w.pk = 0;
+            w.plen = l;
+            w.pt0 = w.sh;
+            w.pend = c;
+            return;
+        }
+    }
+}
+
+// Load stream w.s's description (every lane) and place the part walk at w.off.
+template <bool kFork>
+__device__ __forceinline__ void stream_setup(Walk& w, const int32_t* __restrict__ context_lens,
+                                             int cap, int S, const ForkArgs& f) {
+    if constexpr (kFork) {
+        long L;
+        group_info(f, context_lens, w.s, cap, S, w.lead, w.nmem, w.sh, &L);
+        w.L = int(L);
+        part_seek(w, context_lens, cap, w.off);
+    } else {
+        w.ctx = stream_ctx(context_lens, w.s, cap);
+        w.L = (w.ctx + 63) / 64;
+    }
+}
+
 // Position the walk at the start of this CTA's range (every warp computes it).
+// B is the number of streams: sequences, or groups in shared-prefix mode.
+template <bool kFork>
 __device__ __forceinline__ bool walk_begin(Walk& w, const int32_t* __restrict__ context_lens,
-                                           int B, int units, int cap) {
+                                           int B, int units, int cap, int S, const ForkArgs& f) {
     const int lane = threadIdx.x & 31;
     const int members = gridDim.x / units;          // CTAs per unit group (>= 1)
     w.u = blockIdx.x % units;
@@ -153,8 +289,7 @@ __device__ __forceinline__ bool walk_begin(Walk& w, const int32_t* __restrict__ 
     long total = 0;                                 // stages of one unit
     for (int base = 0; base < B; base += 32) {
         const int s = base + lane;
-        const long v = s < B ? long((stream_ctx(context_lens, s, cap) + 63) / 64) : 0;
-        total += v;
+        total += s < B ? stream_stages<kFork>(context_lens, s, cap, S, f) : 0;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
@@ -163,12 +298,11 @@ __device__ __forceinline__ bool walk_begin(Walk& w, const int32_t* __restrict__ 
     const long r0 = long(w.bi) * w.per_cta;
     w.end = total < r0 + w.per_cta ? total : r0 + w.per_cta;
     if (w.bi >= members || r0 >= total) return false;
-    // find the sequence whose stream contains r0
+    // find the stream that contains r0
     long prefix = 0;
     for (int base = 0; base < B; base += 32) {
         const int s = base + lane;
-        const int ctx = s < B ? stream_ctx(context_lens, s, cap) : 0;
-        const long v = long((ctx + 63) / 64);
+        const long v = s < B ? stream_stages<kFork>(context_lens, s, cap, S, f) : 0;
         long incl = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -180,11 +314,10 @@ __device__ __forceinline__ bool walk_begin(Walk& w, const int32_t* __restrict__ 
         if (m) {
             const int src = __ffs(m) - 1;
             w.s = base + src;
-            w.ctx = __shfl_sync(0xffffffffu, ctx, src);
             w.start = prefix + __shfl_sync(0xffffffffu, incl - v, src);
-            w.L = (w.ctx + 63) / 64;
             w.off = int(r0 - w.start);
             w.pos = r0;
+            stream_setup<kFork>(w, context_lens, cap, S, f);
             return true;
         }
         prefix += __shfl_sync(0xffffffffu, incl, 31);
@@ -193,16 +326,38 @@ __device__ __forceinline__ bool walk_begin(Walk& w, const int32_t* __restrict__ 
 }
 
 // After the current stream is exhausted, move to the next non-empty one.
+template <bool kFork>
 __device__ __forceinline__ void walk_next_stream(Walk& w, const int32_t* __restrict__ context_lens,
-                                                 int B, int units, int cap) {
-    (void)units;
+                                                 int B, int cap, int S, const ForkArgs& f) {
     w.start += w.L;
     w.off = 0;
-    do {
-        ++w.s;
-        w.ctx = w.s < B ? stream_ctx(context_lens, w.s, cap) : 0;
-    } while (w.s < B && w.ctx == 0);
-    w.L = (w.ctx + 63) / 64;
+    if constexpr (kFork) {
+        do {
+            ++w.s;
+            w.L = w.s < B ? int(group_stages(f, context_lens, w.s, cap, S)) : 0;
+        } while (w.s < B && w.L == 0);
+        if (w.s < B) stream_setup<kFork>(w, context_lens, cap, S, f);
+    } else {
+        do {
+            ++w.s;
+            w.ctx = w.s < B ? stream_ctx(context_lens, w.s, cap) : 0;
+        } while (w.s < B && w.ctx == 0);
+        w.L = (w.ctx + 63) / 64;
+    }
+}
+
+// One stage forward (producer): within the stream, or on to the next stream
+// when this one is used up and the range goes on.
+template <bool kFork>
+__device__ __forceinline__ void walk_step(Walk& w, const int32_t* __restrict__ context_lens,
+                                          int B, int cap, int S, const ForkArgs& f) {
+    ++w.off;
+    ++w.pos;
+    if (w.off == w.L) {
+        if (w.pos < w.end) walk_next_stream<kFork>(w, context_lens, B, cap, S, f);
+    } else if constexpr (kFork) {
+        part_next(w, context_lens, cap);
+    }
 }
 
 // OR of `pred` over the consumer warps (named barrier 1), uniform result.
@@ -238,33 +393,31 @@ __device__ __forceinline__ bool arrive_piece(unsigned long long* cnt, unsigned l
 // Merge the np pieces of a stream's rows (one warp, fixed piece order):
 // M = max_k m_k; out = sum_k o_k 2^(m_k - M) / sum_k l_k 2^(m_k - M).
 // Four lanes per row (a quarter of D each), so every row is merged at once
-// and the loads of all pieces are in flight together.  Row n = col0 + lane / 4
-// is column n of the stream: head h0 + n / nq, query token n % nq of
-// sequence s (nq = 1 for decode).  Pieces of other CTAs are read through L2.
+// and the loads of all pieces are in flight together.  The caller gives each
+// lane its row's output index orow (< 0: nothing to write) and the workspace
+// index of the row's first piece; later pieces follow at stride pstride.
+// Pieces of other CTAs are read through L2.
 template <typename T, int D>
-__device__ __forceinline__ void merge_stream(T* __restrict__ out, const float* ws_o,
-                                             const float* ws_m, const float* ws_l, int s, int h0,
-                                             int H, int nq, int GH, int col0, int max_segs,
-                                             int np, int lane) {
+__device__ __forceinline__ void merge_rows(T* __restrict__ out, const float* ws_o,
+                                           const float* ws_m, const float* ws_l, int64_t orow,
+                                           int64_t base, int pstride, int np, int lane) {
     using E = Elem<T>;
     constexpr int kDpl = D / 4;          // values per lane
     constexpr int kCache = 8;            // pieces whose (m, l) stay in registers
-    const int n = col0 + (lane >> 2);
-    const int hh = n / nq, j = n - hh * nq;
-    if (hh >= GH) return;
-    const int64_t row = ((int64_t)s * nq + j) * H + h0 + hh;
-    const float* m = ws_m + row * max_segs;
-    const float* l = ws_l + row * max_segs;
-    const float* o = ws_o + row * max_segs * D + (lane & 3) * kDpl;
+    if (orow < 0) return;
+    const int64_t row = orow;
+    const float* m = ws_m + base;
+    const float* l = ws_l + base;
+    const float* o = ws_o + base * D + (lane & 3) * kDpl;
     float mc[kCache], lc[kCache];
     float M = -INFINITY;
 #pragma unroll
     for (int p = 0; p < kCache; ++p) {
-        mc[p] = p < np ? __ldcg(m + p) : -INFINITY;
-        lc[p] = p < np ? __ldcg(l + p) : 0.f;
+        mc[p] = p < np ? __ldcg(m + int64_t(p) * pstride) : -INFINITY;
+        lc[p] = p < np ? __ldcg(l + int64_t(p) * pstride) : 0.f;
         M = fmaxf(M, mc[p]);
     }
-    for (int p = kCache; p < np; ++p) M = fmaxf(M, __ldcg(m + p));
+    for (int p = kCache; p < np; ++p) M = fmaxf(M, __ldcg(m + int64_t(p) * pstride));
     float acc[kDpl];
 #pragma unroll
     for (int e = 0; e < kDpl; ++e) acc[e] = 0.f;
@@ -276,12 +429,12 @@ __device__ __forceinline__ void merge_stream(T* __restrict__ out, const float* w
             for (int k = 0; k < kCache; ++k)
                 if (k == p) { mp = mc[k]; lp = lc[k]; }
         } else {
-            mp = __ldcg(m + p);
-            lp = __ldcg(l + p);
+            mp = __ldcg(m + int64_t(p) * pstride);
+            lp = __ldcg(l + int64_t(p) * pstride);
         }
         const float w = mp != -INFINITY ? ex2(mp - M) : 0.f;
         lsum += lp * w;
-        const float4* src = reinterpret_cast<const float4*>(o + int64_t(p) * D);
+        const float4* src = reinterpret_cast<const float4*>(o + int64_t(p) * pstride * D);
 #pragma unroll
         for (int c = 0; c < kDpl / 4; ++c) {
             const float4 v = __ldcg(src + c);
@@ -319,6 +472,40 @@ __device__ __forceinline__ void zero_empty_rows(T* __restrict__ out,
             for (int i = lane; i < nq * H * D * 2 / 16; i += 32)
                 dst[i] = make_uint4(0u, 0u, 0u, 0u);
         }
+    }
+}
+
+// Shared-prefix mode: the groups must cover sequences 0 .. nseq - 1 in order
+// and every member's table must hold the first member's block ids over the
+// group's shared prefix; otherwise PD_DEVERR_SHARED_PREFIX (the results of
+// such a group are unspecified).  CTA b checks groups b, b + grid, ...;
+// called by one warp.
+__device__ __forceinline__ void check_groups(const ForkArgs& f, int n_groups,
+                                             const int32_t* __restrict__ block_tables,
+                                             int max_blocks_per_seq,
+                                             const int32_t* __restrict__ context_lens, int cap,
+                                             int S, int32_t* dev_err, int lane) {
+    if (blockIdx.x == 0 && lane == 0 &&
+        (__ldg(f.start) != 0 || __ldg(f.start + n_groups) != f.nseq))
+        flag_error(dev_err, PD_DEVERR_SHARED_PREFIX);
+    const int log2S = __ffs(S) - 1;
+    for (int k = blockIdx.x; k < n_groups; k += gridDim.x) {
+        const int a = __ldg(f.start + k), b = __ldg(f.start + k + 1);
+        if (a < 0 || b < a || b > f.nseq || b - a > f.Mmax) {
+            if (lane == 0) flag_error(dev_err, PD_DEVERR_SHARED_PREFIX);
+            continue;
+        }
+        int lead, n, sh;
+        group_info(f, context_lens, k, cap, S, lead, n, sh);
+        const int nb = sh >> log2S;
+        const int32_t* first = block_tables + (int64_t)lead * max_blocks_per_seq;
+        bool bad = false;
+        for (int i = lane; i < (n - 1) * nb; i += 32) {
+            const int j = 1 + i / nb, blk = i - (i / nb) * nb;
+            bad |= __ldg(block_tables + (int64_t)(lead + j) * max_blocks_per_seq + blk) !=
+                   __ldg(first + blk);
+        }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) flag_error(dev_err, PD_DEVERR_SHARED_PREFIX);
     }
 }
 
@@ -365,13 +552,19 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // T: type of q and out.  kF8: the pools hold E4M3 codes with a K and a V scale
 // per kv head; the tensor-core products then run on fp16 (K and V widened
 // exactly, q rounded to fp16), and the scales are applied in fp32.
-// kMQ: nq_arg query tokens per sequence (speculative verification), the last
-// nq_arg positions of its context, each attending causally.  The columns of a
-// stream are then (head, query token) pairs, GH * nq_arg <= 16: one tile of 8
-// columns is the decode layout (each consumer warp takes 16 tokens of a
-// stage); with two tiles, warp w takes tile w / 2 and tokens 32 (w % 2) ..
-// + 31 of each stage, so K/V of a kv head is still read once.
-template <typename T, int D, bool kF8, bool kMQ>
+// kMQ: several columns per kv-head unit beyond its query heads, in tiles of 8
+// (MMA N): one tile is the decode layout (each consumer warp takes 16 tokens
+// of a stage, the four warps merge per piece); with two tiles, warp w takes
+// tile w / 2 and tokens 32 (w % 2) .. + 31 of each stage; with four tiles
+// (shared-prefix mode only), warp w takes tile w and all 64 tokens, so K/V of
+// a kv head is still read once whatever the column count (<= 16 for verify,
+// <= 32 for shared prefixes).  Verification (nq_arg query tokens per
+// sequence, the last nq_arg positions of its context, each attending
+// causally): columns are (head, query token) pairs, head-major.
+// kFork (with kMQ): shared-prefix mode, B = groups of sequences; columns are
+// (member, head) pairs, member-major (member j of the group: columns
+// j GH .. j GH + GH - 1), so a member's tail stage involves one tile.
+template <typename T, int D, bool kF8, bool kMQ, bool kFork>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, T* __restrict__ out,
@@ -383,7 +576,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                           float* __restrict__ ws_m, float* __restrict__ ws_l,
                           unsigned long long* __restrict__ ws_cnt, unsigned long long tag,
                           const float* __restrict__ k_scale, const float* __restrict__ v_scale,
-                          int32_t* dev_err) {
+                          ForkArgs fk, int32_t* dev_err) {
+    static_assert(!kFork || (kMQ && !kF8), "shared-prefix mode: 16-bit pools, column tiles");
     using L = DecodeSmem<D, kF8>;
     constexpr bool kNative = L::kNative;
     using TM = typename std::conditional<kF8, __half, T>::type;   // tensor-core operand type
@@ -403,7 +597,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int G = H / Hk;
     const int groups = G / GH;
     const int units = Hk * groups;
-    const int nq = kMQ ? nq_arg : 1;
+    const int nq = kMQ && !kFork ? nq_arg : 1;
+    const int nseq = kFork ? fk.nseq : B;          // rows of q / out are sequences
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -420,8 +615,13 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     __syncthreads();
 
     Walk w;
-    if (!walk_begin(w, context_lens, B, units, cap)) {          // uniform: no range
-        if (warp == 0) zero_empty_rows<T, D>(out, context_lens, B, H, nq, cap, dev_err, lane);
+    if (!walk_begin<kFork>(w, context_lens, B, units, cap, S, fk)) {   // uniform: no range
+        if (warp == 0) {
+            zero_empty_rows<T, D>(out, context_lens, nseq, H, nq, cap, dev_err, lane);
+            if constexpr (kFork)
+                check_groups(fk, B, block_tables, max_blocks_per_seq, context_lens, cap, S,
+                             dev_err, lane);
+        }
         return;
     }
 
@@ -437,10 +637,15 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         // copies instead of sitting in front of every stage.
         const int log2S = __ffs(S) - 1;                    // S is a power of two
         auto stage_blk = [&](const Walk& x) -> int {
-            const int t0 = x.off * kStageTokens;
-            const int nt = min(kStageTokens, x.ctx - t0);
+            // the stage's first token, its end, and whose table holds it
+            // (shared-prefix mode: the group's first member for the shared
+            // part, the member itself for its tail; both start on a block)
+            const int t0 = kFork ? x.pt0 + x.pk * kStageTokens : x.off * kStageTokens;
+            const int tend = kFork ? x.pend : x.ctx;
+            const int seq = kFork ? (x.pj < 0 ? x.lead : x.lead + x.pj) : x.s;
+            const int nt = min(kStageTokens, tend - t0);
             const int nblk = (nt + S - 1) >> log2S;        // <= 64 / S <= 8
-            const int32_t* p = block_tables + (int64_t)x.s * max_blocks_per_seq +
+            const int32_t* p = block_tables + (int64_t)seq * max_blocks_per_seq +
                                (t0 >> log2S) + lane;
             int v = -2;
             // issued here, consumed one stage later
@@ -467,9 +672,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 break;
             }
             // start loading the next stage's block ids
-            ++wn.off;
-            ++wn.pos;
-            if (wn.off == wn.L && wn.pos < wn.end) walk_next_stream(wn, context_lens, B, units, cap);
+            walk_step<kFork>(wn, context_lens, B, cap, S, fk);
             const int blk_next = wn.pos < wn.end ? stage_blk(wn) : -2;
             const int kvh = w.u / groups;
             int row = -1;
@@ -503,24 +706,45 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             blk_cur = blk_next;
         }
         // all loads are issued: the producer has time for the empty rows
-        zero_empty_rows<T, D>(out, context_lens, B, H, nq, cap, dev_err, lane);
+        zero_empty_rows<T, D>(out, context_lens, nseq, H, nq, cap, dev_err, lane);
+        if constexpr (kFork)
+            check_groups(fk, B, block_tables, max_blocks_per_seq, context_lens, cap, S, dev_err,
+                         lane);
         return;
     }
 
     // ---------------- consumer warps ----------------
     const int j8 = lane >> 3, r8 = lane & 7;     // ldmatrix: matrix index, row within it
-    // this warp's tokens within a stage (16, or 32 with two column tiles) and
-    // its first column
-    const int ctiles = kMQ ? (GH * nq + kHeadsN - 1) / kHeadsN : 1;
+    // columns of a stream, in 1, 2 or 4 tiles of 8; this warp's tokens within
+    // a stage (16, 32 or all 64) and its first column
+    const int ncols = kFork ? GH * fk.Mmax : GH * nq;
+    const int ctiles = kMQ ? (ncols <= kHeadsN ? 1 : ncols <= 2 * kHeadsN ? 2 : 4) : 1;
     const int wpc = kConsumerWarps / ctiles;     // warps per column tile
     const int tb = kMQ ? (warp % wpc) * 16 * ctiles : warp * 16;
     const int col0 = kMQ ? (warp / wpc) * kHeadsN : 0;
+    const bool tile_live = col0 < ncols;         // four tiles may leave the last one empty
+    const int cstride = ctiles * kHeadsN;        // shared-prefix workspace: columns per piece
     const uint32_t k_base0 = smem_u32(smem + L::kK);
     const uint32_t v_base0 = smem_u32(smem + L::kV);
     const float2 neg1 = make_float2(-1.f, -1.f);
     uint32_t gs = 0;                             // stages consumed so far
     bool aborted = false;
-    const bool two_tiles = kMQ && ctiles == 2;
+    // fp16 shared-prefix mode: P enters PV as one fp16 value (2^-11 relative
+    // rounding); otherwise as the hi + lo pair
+    constexpr bool kLoP = !(kFork && std::is_same<T, __half>::value);
+
+    // output row of column n of stream x whose unit starts at head h0 (-1: a
+    // padding column, or a member without context, whose rows others write)
+    auto col_row = [&](const Walk& x, int h0, int n) -> int64_t {
+        if constexpr (kFork) {
+            const int j = n / GH, hh = n - j * GH;
+            if (j >= x.nmem || stream_ctx(context_lens, x.lead + j, cap) == 0) return -1;
+            return (int64_t)(x.lead + j) * H + h0 + hh;
+        } else {
+            const int hh = n / nq, j = n - hh * nq;
+            return hh < GH ? ((int64_t)x.s * nq + j) * H + h0 + hh : -1;
+        }
+    };
 
     while (w.pos < w.end) {
         // ---- one stream piece: stages [w.off, min(w.L, w.off + w.end - w.pos)) of (s, u)
@@ -536,11 +760,11 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         // (register 0) and the same + 8 (register 1); heads past GH are zero.
         uint32_t qb[KS][2];
         {
-            // column n: head h0 + n / nq, query token n % nq
-            const int n = col0 + (lane >> 2);
-            const int qh = n / nq, qj = n - qh * nq;
-            const bool qv = qh < GH;
-            const int64_t qrow_i = ((int64_t)w.s * nq + qj) * H + h0 + qh;
+            // column n: head h0 + n / nq, query token n % nq (verify); member
+            // n / GH, head h0 + n % GH (shared-prefix mode)
+            const int64_t qrow_c = col_row(w, h0, col0 + (lane >> 2));
+            const bool qv = qrow_c >= 0;
+            const int64_t qrow_i = qv ? qrow_c : 0;
             const T* qrow = q + qrow_i * D + 2 * (lane & 3);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
@@ -573,7 +797,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         // switch hit instead of waiting on HBM: the next stream of the range is
         // (s + 1, u) (an empty sequence is skipped by the walk, so that prefetch
         // is merely wasted).
-        if (piece_stages < w.end - w.pos) {
+        if (!kFork && piece_stages < w.end - w.pos) {
             const int nu = w.u;                         // same unit, next sequence
             const int ns = w.s + 1;
             if (ns < B) {
@@ -602,6 +826,13 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         int dj[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) dj[h] = kMQ ? nq - 1 - (col0 + 2 * (lane & 3) + h) % nq : 0;
+        // shared-prefix mode: the members of this lane's two columns, the
+        // members this warp's tile spans, and the walk over the piece's parts
+        int mem[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) mem[h] = kFork ? (col0 + 2 * (lane & 3) + h) / GH : 0;
+        const int tile_m0 = kFork ? col0 / GH : 0, tile_m1 = kFork ? (col0 + kHeadsN - 1) / GH : 0;
+        Walk pw = w;
 
         for (int st = 0; st < piece_stages;) {
             // the native FP8 path takes two stages of the piece at a time
@@ -617,8 +848,17 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 aborted = true;
                 break;                   // skip the piece's other stages
             }
-            const int rem = w.ctx - (w.off + st) * kStageTokens;   // context from this stage on
-            const int nt = min(kStageTokens, rem);
+            // context from this stage on (decode, verify); shared-prefix mode:
+            // the stage's tokens and the member whose tail it is (-1: shared)
+            int rem, nt, act = -1;
+            if constexpr (kFork) {
+                rem = pw.pend - (pw.pt0 + pw.pk * kStageTokens);
+                nt = min(kStageTokens, rem);
+                act = pw.pj;
+            } else {
+                rem = w.ctx - (w.off + st) * kStageTokens;
+                nt = min(kStageTokens, rem);
+            }
             // FP8 pools: this warp widens its own 16 rows of K and V to fp16 in
             // the one 16-bit tile (no other warp reads them), then frees the raw
             // stage for the next copy right away.
@@ -822,15 +1062,20 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
               // round; NS = 1 is the decode layout, NS = 2 the two-tile verify one
               auto body = [&](auto ns_c) {
                 constexpr int NS = decltype(ns_c)::value;
-                if (tb >= nt) return;
+                if (tb >= nt || !tile_live) return;
+                // a member's tail stage concerns only the tile holding its columns
+                if (kFork && act >= 0 && (act < tile_m0 || act > tile_m1)) return;
+                // sub-tiles of this warp that hold tokens (shared-prefix mode,
+                // whose short tail stages would otherwise run all NS)
+                const int nsb = (NS == 1 || !kFork) ? NS : min(NS, (nt - tb + 15) >> 4);
                 const uint32_t kb = k_base0 + tslot * L::kTile;
                 const uint32_t vb = v_base0 + tslot * L::kTile;
-                const bool partial = tb + 16 * NS > nt;
+                const bool partial = tb + 16 * nsb > nt;
                 if (partial) {
                     // V rows past the context end hold other data or were never
                     // loaded this round: zero them so that 0 * v stays 0.
                     unsigned char* vrow = smem + L::kV + tslot * L::kTile;
-                    for (int i = lane; i < 16 * NS * kAtoms * 8; i += 32) {
+                    for (int i = lane; i < 16 * nsb * kAtoms * 8; i += 32) {
                         const int tok = tb + i / (kAtoms * 8);
                         if (tok >= nt) {
                             const int a = (i / 8) % kAtoms, c = i % 8;
@@ -850,6 +1095,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 for (int ks = 0; ks < KS; ++ks) {
 #pragma unroll
                     for (int sb = 0; sb < NS; ++sb) {
+                        if (sb >= nsb) continue;
                         uint32_t a[4];
                         wmma16::ldsm_x4(a, swz<D>(kb, tb + 16 * sb + r8 + 8 * (j8 & 1),
                                                   2 * ks + (j8 >> 1)));
@@ -857,14 +1103,22 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                     }
                 }
                 // lane holds tokens tb + 16 sb + lane/4 (0,1) and + 8 (2,3); columns
-                // 2(lane%4) + {0,1}
+                // 2(lane%4) + {0,1}.  Tokens past a column's limit are masked: the
+                // stage's end (decode); the query's causal limit (verify); in
+                // shared-prefix mode, the whole stage for columns of other members
+                // when it is a member's tail.
+                int lim[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    lim[h] = kFork ? ((act < 0 || mem[h] == act) ? nt : 0)
+                                   : (kMQ ? rem - dj[h] : nt);
                 float x[NS][4];
 #pragma unroll
                 for (int sb = 0; sb < NS; ++sb)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int tok = tb + 16 * sb + (lane >> 2) + (i >> 1) * 8;
-                        x[sb][i] = tok < (kMQ ? rem - dj[i & 1] : nt)
+                        x[sb][i] = (sb < nsb && tok < lim[i & 1])
                                        ? (acc[sb][0][i] + acc[sb][1][i]) * sl2 : -INFINITY;
                     }
                 // ---- online softmax per column (lane-local state, 3 shuffles per column)
@@ -895,7 +1149,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 // a verify column may not have seen a key yet (m = -inf): its p are 0
                 const float mu0 = kMQ && m_run[0] == -INFINITY ? 0.f : m_run[0];
                 const float mu1 = kMQ && m_run[1] == -INFINITY ? 0.f : m_run[1];
-                uint32_t bh0[NS], bh1[NS], bl0[NS], bl1[NS];
+                uint32_t bh0[NS], bh1[NS];
+                [[maybe_unused]] uint32_t bl0[NS], bl1[NS];   // the lo half (kLoP only)
                 float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
                 for (int sb = 0; sb < NS; ++sb) {
@@ -910,12 +1165,14 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                     }
                     // P as hi + lo 16-bit pairs, transposed into B-operand layout
                     const uint32_t hi0 = E::pack2(p0, p1), hi1 = E::pack2(p2, p3);
-                    const float2 lo0 = ffma2(E::unpack2(hi0), neg1, make_float2(p0, p1));
-                    const float2 lo1 = ffma2(E::unpack2(hi1), neg1, make_float2(p2, p3));
                     bh0[sb] = wmma16::movm_t(hi0);
                     bh1[sb] = wmma16::movm_t(hi1);
-                    bl0[sb] = wmma16::movm_t(E::pack2(lo0.x, lo0.y));
-                    bl1[sb] = wmma16::movm_t(E::pack2(lo1.x, lo1.y));
+                    if constexpr (kLoP) {
+                        const float2 lo0 = ffma2(E::unpack2(hi0), neg1, make_float2(p0, p1));
+                        const float2 lo1 = ffma2(E::unpack2(hi1), neg1, make_float2(p2, p3));
+                        bl0[sb] = wmma16::movm_t(E::pack2(lo0.x, lo0.y));
+                        bl1[sb] = wmma16::movm_t(E::pack2(lo1.x, lo1.y));
+                    }
                 }
                 l_run[0] += ls0;
                 l_run[1] += ls1;
@@ -924,16 +1181,21 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 for (int mt = 0; mt < KS; ++mt) {
 #pragma unroll
                     for (int sb = 0; sb < NS; ++sb) {
+                        if (sb >= nsb) continue;
                         uint32_t a[4];
                         wmma16::ldsm_x4_t(a, swz<D>(vb, tb + 16 * sb + r8 + 8 * (j8 >> 1),
                                                     2 * mt + (j8 & 1)));
                         wmma16::Mma<TM>::run(o[mt], a, bh0[sb], bh1[sb]);
-                        wmma16::Mma<TM>::run(o[mt], a, bl0[sb], bl1[sb]);
+                        if constexpr (kLoP) wmma16::Mma<TM>::run(o[mt], a, bl0[sb], bl1[sb]);
                     }
                 }
                 if (partial && !kF8) tc::fence_proxy_async_smem();   // zeros before the next TMA write
               };
-              if constexpr (kMQ) {
+              if constexpr (kFork) {
+                  if (ctiles == 4) body(std::integral_constant<int, 4>{});
+                  else if (ctiles == 2) body(std::integral_constant<int, 2>{});
+                  else body(std::integral_constant<int, 1>{});
+              } else if constexpr (kMQ) {
                   if (ctiles == 2) body(std::integral_constant<int, 2>{});
                   else body(std::integral_constant<int, 1>{});
               } else {
@@ -944,6 +1206,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             if (!kF8 && lane == 0) mbar_arrive(&empty[slot]);
             st += nst;
             gs += nst;
+            if constexpr (kFork) part_next(pw, context_lens, cap);
         }
         // All four consumer warps decide together whether to go on: a warp
         // that gave up still arrives here, so named-barrier counts stay matched.
@@ -992,8 +1255,10 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 o[mt][3] = o[mt][3] * c_mine[1] + v.w * c_other[1];
             }
         };
-        // two column tiles: warp 1 hands over to 0 and warp 3 to 2 (same tile)
-        if (!two_tiles) {
+        // one tile: warps 2, 3 hand over to 0, 1, then warp 1 to 0; two tiles:
+        // warp 1 hands over to 0 and warp 3 to 2 (same tile); four tiles: each
+        // warp holds its own columns whole
+        if (ctiles == 1) {
             if (warp >= 2) put(warp - 2);
             asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
             if (warp < 2) take(warp);
@@ -1003,7 +1268,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             }
             asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
             if (warp == 0) take(1);
-        } else {
+        } else if (ctiles == 2) {
             if (warp & 1) put(warp >> 1);
             asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
             if (!(warp & 1)) take(warp >> 1);
@@ -1013,13 +1278,28 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         // perhaps merge the stream. They fall behind by that much and catch up
         // on stages already in the ring (consuming is faster than streaming).
         asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+        const bool leader = (warp % wpc) == 0;   // holds its tile's result
+        // workspace index of column c's partial for piece `p` of this stream:
+        // per output row (decode, verify), or compact per (unit, piece, column)
+        // in shared-prefix mode (piece k + c_first + p < n_groups + CTAs per unit)
+        auto ws_index = [&](int64_t row, int c, long p) -> int64_t {
+            if constexpr (kFork)
+                return ((int64_t)w.u * fk.ppu + w.s + c_first + p) * cstride + c;
+            return row * max_segs + p;
+        };
+        auto merge_tile = [&]() {
+            const int n = col0 + (lane >> 2);
+            const int64_t orow = col_row(w, h0, n);
+            merge_rows<T, D>(out, ws_o, ws_m, ws_l, orow, orow < 0 ? 0 : ws_index(orow, n, 0),
+                             kFork ? cstride : 1, nseg, lane);
+        };
         // the arrival counter is read now, so that its latency overlaps the
         // piece's writes and fence; a value changed meanwhile costs one more CAS
         unsigned long long cnt0 = 0;
         if (nseg > 1 && warp == 0 && lane == 0)
             cnt0 = *reinterpret_cast<volatile unsigned long long*>(ws_cnt + (int64_t)w.s * units +
                                                                     w.u);
-        if (two_tiles ? (warp & 1) == 0 : warp == 0) {
+        if (leader && tile_live) {
             if constexpr (kF8) {
                 const float vs = __ldg(v_scale + kvh);
 #pragma unroll
@@ -1027,17 +1307,16 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
                     for (int e = 0; e < 4; ++e) o[mt][e] *= vs;
             }
-            // lane: heads ha, ha + 1; dims 16mt + lane/4 and + 8 (native FP8: the
+            // lane: columns ha, ha + 1; dims 16mt + lane/4 and + 8 (native FP8: the
             // m-tile rows g, g + 8 are dims 2g, 2g + 1)
             const int ha = 2 * (lane & 3);
             const int d0 = kNative ? 2 * (lane >> 2) : (lane >> 2);
             constexpr int kDd = kNative ? 1 : 8;     // dim step of registers 2, 3
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int c = col0 + ha + h;          // column: head h0 + c / nq, query c % nq
-                const int hh = c / nq, jq = c - hh * nq;
-                if (hh >= GH) continue;
-                const int64_t row = ((int64_t)w.s * nq + jq) * H + h0 + hh;
+                const int c = col0 + ha + h;
+                const int64_t row = col_row(w, h0, c);
+                if (row < 0) continue;
                 if (nseg == 1) {
                     // the whole stream was here: final, normalised output
                     const float inv = kMQ && l_run[h] == 0.f ? 0.f : 1.f / l_run[h];
@@ -1048,7 +1327,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         orow[16 * mt + kDd] = T(o[mt][2 + h] * inv);
                     }
                 } else {
-                    const int64_t r = row * max_segs + seg;
+                    const int64_t r = ws_index(row, c, seg);
                     float* wrow = ws_o + r * D + d0;
 #pragma unroll
                     for (int mt = 0; mt < KS; ++mt) {
@@ -1061,7 +1340,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                     }
                 }
             }
-            if (nseg > 1 && !two_tiles) {
+            if (nseg > 1 && ctiles == 1) {
                 // publish this piece, count it; the last of the stream's
                 // pieces to arrive merges them all
                 __threadfence();
@@ -1073,31 +1352,29 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
                     __threadfence();
-                    merge_stream<T, D>(out, ws_o, ws_m, ws_l, w.s, h0, H, nq, GH, 0,
-                                       max_segs, nseg, lane);
+                    merge_tile();
                 }
             }
         }
-        if (two_tiles && nseg > 1 && (warp & 1) == 0) {
-            // both tile warps (0 and 2, named barrier 2) have written their rows
-            // of the piece before it is counted; then both merge their own tile
-            // if it was the last
+        if (ctiles > 1 && nseg > 1 && leader) {
+            // every tile's leader (named barrier 2) has written its rows of the
+            // piece before it is counted; then each merges its own tile if the
+            // piece was the last
             volatile int32_t* last_flag = reinterpret_cast<int32_t*>(smem + L::kMisc + 8);
             __threadfence();
-            asm volatile("bar.sync 2, 64;" ::: "memory");
+            asm volatile("bar.sync 2, %0;" ::"r"(ctiles * 32) : "memory");
             if (warp == 0 && lane == 0)
                 *last_flag =
                     arrive_piece(ws_cnt + (int64_t)w.s * units + w.u, tag, nseg, cnt0) ? 1 : 0;
-            asm volatile("bar.sync 2, 64;" ::: "memory");
-            if (*last_flag) {
+            asm volatile("bar.sync 2, %0;" ::"r"(ctiles * 32) : "memory");
+            if (*last_flag && tile_live) {
                 __threadfence();
-                merge_stream<T, D>(out, ws_o, ws_m, ws_l, w.s, h0, H, nq, GH, col0, max_segs,
-                                   nseg, lane);
+                merge_tile();
             }
         }
         w.off += piece_stages;
         w.pos += piece_stages;
-        if (w.off == w.L && w.pos < w.end) walk_next_stream(w, context_lens, B, units, cap);
+        if (w.off == w.L && w.pos < w.end) walk_next_stream<kFork>(w, context_lens, B, cap, S, fk);
     }
 
     if (aborted) {
@@ -1158,17 +1435,48 @@ int sm_count(int dev) {
     return counts[dev];
 }
 
-template <typename T, int D, bool kF8, bool kMQ>
+// Largest divisor of G whose columns fit max_cols: 8 heads for decode; 16
+// (two tiles of N = 8) for verification, GH * nq; 32 (four tiles) in
+// shared-prefix mode, GH * Mmax.
+int heads_per_unit(int G, int cols_per_head, int max_cols) {
+    for (int g = std::min(G, max_cols / cols_per_head); g >= 1; --g)
+        if (G % g == 0) return g;
+    return 1;
+}
+
+// Most CTAs a decode launch uses: two per SM, at most kMaxGrid (so that the
+// shared-prefix workspace can be sized without asking the device).
+constexpr int kMaxGrid = 1024;
+
+// Shared-prefix workspace: partials of (unit, piece, column) with at most
+// n_groups + kMaxGrid / units pieces per unit, then per-(group, unit) counters.
+WsLayout fork_ws_layout(int n_groups, int max_group, int H, int Hk, int D, int* units_out,
+                        int* ppu_max_out) {
+    const int G = H / Hk;
+    const int GH = heads_per_unit(G, max_group, 4 * kHeadsN);
+    const int units = Hk * (G / GH);
+    const int ncols = GH * max_group;
+    const int cstride = (ncols <= kHeadsN ? 1 : ncols <= 2 * kHeadsN ? 2 : 4) * kHeadsN;
+    const int ppu = n_groups + std::max(1, kMaxGrid / units);
+    const size_t rows = size_t(units) * ppu * cstride;
+    WsLayout w;
+    w.o = 0;
+    w.m = align256(rows * D * sizeof(float));
+    w.l = w.m + align256(rows * sizeof(float));
+    w.cnt = w.l + align256(rows * sizeof(float));
+    w.total = w.cnt + align256(size_t(n_groups) * units * sizeof(unsigned long long));
+    if (units_out) *units_out = units;
+    if (ppu_max_out) *ppu_max_out = ppu;
+    return w;
+}
+
+template <typename T, int D, bool kF8, bool kMQ, bool kFork>
 pd_status launch_decode_t(const DecodeArgs& a) {
     using Lt = DecodeSmem<D, kF8>;
     const int G = a.H / a.Hk;
-    const int nq = kMQ ? a.nq : 1;
-    // largest divisor of G whose columns fit: GH <= 8 for decode, GH * nq <= 16
-    // (two tiles of N = 8) for verification
-    const int max_cols = kMQ ? 2 * kHeadsN : kHeadsN;
-    int GH = 1;
-    for (int g = std::min(G, max_cols / nq); g >= 1; --g)
-        if (G % g == 0) { GH = g; break; }
+    const int nq = kMQ && !kFork ? a.nq : 1;
+    const int GH = kFork ? heads_per_unit(G, a.max_group, 4 * kHeadsN)
+                         : heads_per_unit(G, nq, kMQ ? 2 * kHeadsN : kHeadsN);
     CUtensorMap tm_k, tm_v;
     const unsigned long long rows = (unsigned long long)a.NB * a.Hk * a.S;
     if (rows > 0x7fffffffull) return PD_ERR_UNSUPPORTED;   // TMA row coordinate is int32
@@ -1177,7 +1485,7 @@ pd_status launch_decode_t(const DecodeArgs& a) {
                              : (encode_pool_map(&tm_k, a.key_cache, D, rows, a.S, a.dt) &&
                                 encode_pool_map(&tm_v, a.value_cache, D, rows, a.S, a.dt));
     if (!maps_ok) return launch_result(cudaErrorInvalidValue);
-    auto kern = paged_decode_split_kernel<T, D, kF8, kMQ>;
+    auto kern = paged_decode_split_kernel<T, D, kF8, kMQ, kFork>;
     static uint64_t attr_set = 0;   // one bit per device; benign if raced
     int dev = 0;
     cudaError_t e0 = cudaGetDevice(&dev);
@@ -1188,9 +1496,24 @@ pd_status launch_decode_t(const DecodeArgs& a) {
         if (e != cudaSuccess) return launch_result(e);
         if (dev < 64) attr_set |= uint64_t(1) << dev;
     }
-    const int P = decode_num_partitions(a.max_context_len);   // pieces per stream, at most
-    const WsLayout w = ws_layout(a.B * nq, a.H, a.D, P);
+    // persistent grid: two CTAs per SM (shared memory bound), at most
+    // kMaxGrid, rounded down to a multiple of the units so that every unit
+    // group has the same size
+    const int units = a.Hk * (G / GH);
+    const int slots = std::min(2 * sm_count(dev), kMaxGrid);
+    const int members = std::max(1, slots / units);
+    const unsigned grid = unsigned(units * members);
     char* base = static_cast<char*>(a.workspace);
+    WsLayout w;
+    int P = 1;
+    ForkArgs fk{a.grp_start, a.grp_shared, a.B, a.max_group, 0};
+    if constexpr (kFork) {
+        w = fork_ws_layout(a.n_groups, a.max_group, a.H, a.Hk, a.D, nullptr, nullptr);
+        fk.ppu = a.n_groups + members;
+    } else {
+        P = decode_num_partitions(a.max_context_len);   // pieces per stream, at most
+        w = ws_layout(a.B * nq, a.H, a.D, P);
+    }
     float* ws_o = reinterpret_cast<float*>(base + w.o);
     float* ws_m = reinterpret_cast<float*>(base + w.m);
     float* ws_l = reinterpret_cast<float*>(base + w.l);
@@ -1198,11 +1521,7 @@ pd_status launch_decode_t(const DecodeArgs& a) {
     const float scale_log2 = a.scale * kLog2e;
     // contexts are cut to what the table holds and to the caller's promise
     const int cap = int(std::min<long>(long(a.max_blocks_per_seq) * a.S, a.max_context_len));
-    // persistent grid: two CTAs per SM (shared memory bound), rounded down to
-    // a multiple of the units so that every unit group has the same size
-    const int units = a.Hk * (G / GH);
-    const int slots = 2 * sm_count(dev);
-    const unsigned grid = unsigned(units * std::max(1, slots / units));
+    const int streams = kFork ? a.n_groups : a.B;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kDecodeThreads);
@@ -1215,18 +1534,18 @@ pd_status launch_decode_t(const DecodeArgs& a) {
     cfg.numAttrs = a.pdl ? 1 : 0;
     return launch_result(cudaLaunchKernelEx(
         &cfg, kern, tm_k, tm_v, static_cast<T*>(a.out), static_cast<const T*>(a.q),
-        a.block_tables, a.max_blocks_per_seq, a.context_lens, a.B, a.H, a.Hk, a.S, a.NB, GH,
+        a.block_tables, a.max_blocks_per_seq, a.context_lens, streams, a.H, a.Hk, a.S, a.NB, GH,
         nq, scale_log2, P, cap, ws_o, ws_m, ws_l, ws_cnt, next_launch_tag(), a.k_scale, a.v_scale,
-        a.dev_err));
+        fk, a.dev_err));
 }
 
-template <bool kF8, bool kMQ>
+template <bool kF8, bool kMQ, bool kFork>
 pd_status launch_decode_dt(const DecodeArgs& a) {
     if (a.dt == PD_BF16)
-        return a.D == 128 ? launch_decode_t<__nv_bfloat16, 128, kF8, kMQ>(a)
-                          : launch_decode_t<__nv_bfloat16, 64, kF8, kMQ>(a);
-    return a.D == 128 ? launch_decode_t<__half, 128, kF8, kMQ>(a)
-                      : launch_decode_t<__half, 64, kF8, kMQ>(a);
+        return a.D == 128 ? launch_decode_t<__nv_bfloat16, 128, kF8, kMQ, kFork>(a)
+                          : launch_decode_t<__nv_bfloat16, 64, kF8, kMQ, kFork>(a);
+    return a.D == 128 ? launch_decode_t<__half, 128, kF8, kMQ, kFork>(a)
+                      : launch_decode_t<__half, 64, kF8, kMQ, kFork>(a);
 }
 
 }  // namespace
@@ -1248,9 +1567,15 @@ size_t decode_workspace_bytes(int B, int H, int D, int max_context_len) {
     return ws_layout(B, H, D, decode_num_partitions(max_context_len)).total;
 }
 
+size_t decode_shared_workspace_bytes(int n_groups, int max_group, int H, int Hk, int D) {
+    return fork_ws_layout(n_groups, max_group, H, Hk, D, nullptr, nullptr).total;
+}
+
 pd_status launch_decode(const DecodeArgs& a) {
-    if (a.nq > 1) return a.fp8 ? PD_ERR_UNSUPPORTED : launch_decode_dt<false, true>(a);
-    return a.fp8 ? launch_decode_dt<true, false>(a) : launch_decode_dt<false, false>(a);
+    if (a.n_groups > 0)
+        return a.fp8 || a.nq > 1 ? PD_ERR_UNSUPPORTED : launch_decode_dt<false, true, true>(a);
+    if (a.nq > 1) return a.fp8 ? PD_ERR_UNSUPPORTED : launch_decode_dt<false, true, false>(a);
+    return a.fp8 ? launch_decode_dt<true, false, false>(a) : launch_decode_dt<false, false, false>(a);
 }
 
 }  // namespace pd

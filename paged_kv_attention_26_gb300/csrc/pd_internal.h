@@ -25,6 +25,8 @@ inline int elem_bytes(pd_dtype dt) { return dt == PD_FP8_E4M3 ? 1 : 2; }
 int decode_partition_tokens(int max_context_len);
 int decode_num_partitions(int max_context_len);
 size_t decode_workspace_bytes(int B, int H, int D, int max_context_len);
+// Workspace of the shared-prefix mode (H % Hk == 0, 1 <= max_group <= 32).
+size_t decode_shared_workspace_bytes(int n_groups, int max_group, int H, int Hk, int D);
 
 struct DecodeArgs {
     void* out;
@@ -46,11 +48,26 @@ struct DecodeArgs {
     const float* v_scale = nullptr;
     bool pdl = false;            // launch as a programmatic dependent of the previous grid
     int nq = 1;                  // query tokens per sequence (> 1: speculative verification)
+    // shared-prefix mode (n_groups > 0): groups of consecutive sequences whose
+    // tables agree on their first blocks
+    const int32_t* grp_start = nullptr;    // device [n_groups + 1]
+    const int32_t* grp_shared = nullptr;   // device [n_groups], tokens
+    int n_groups = 0;
+    int max_group = 1;           // most members a group may have (<= 32)
 };
 pd_status launch_decode(const DecodeArgs& a);
-// Argument checks shared by every decode entry point (defined with the C
-// ABI); fills *a, sets *skip when B == 0.  check_workspace_ptr == false
-// leaves the workspace address to the caller (checked size only).
+// Groups of the shared-prefix decode (device arrays, see
+// pd_paged_attention_decode_shared).
+struct SharedGroups {
+    const int32_t* start;
+    const int32_t* shared;
+    int n_groups;
+    int max_group;
+};
+// Argument checks shared by every decode entry point (defined in capi.cu);
+// fills *a, sets *skip when B == 0.  check_workspace_ptr == false leaves the
+// workspace address to the caller (checked size only); grp != nullptr selects
+// the shared-prefix mode and its workspace size.
 pd_status decode_prepare(void* out, const void* q, const void* key_cache,
                          const void* value_cache, const float* k_scale, const float* v_scale,
                          bool fp8, const int32_t* block_tables, int max_blocks_per_seq,
@@ -58,7 +75,7 @@ pd_status decode_prepare(void* out, const void* q, const void* key_cache,
                          int max_context_len, float scale, void* workspace,
                          size_t workspace_bytes, pd_dtype dt, int32_t* dev_err,
                          cudaStream_t stream, DecodeArgs* a, bool* skip, int nq = 1,
-                         bool check_workspace_ptr = true);
+                         bool check_workspace_ptr = true, const SharedGroups* grp = nullptr);
 pd_status launch_bounded_wait_selftest(int32_t* dev_err, unsigned long long limit_ns,
                                        cudaStream_t stream);
 pd_status launch_copy_bytes(void* dst, const void* src, size_t bytes, cudaStream_t stream);

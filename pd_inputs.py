@@ -173,6 +173,79 @@ def decode_case(name, seed, ctx, H, Hk, D, S, dtype, NB=None, pool_factor=1.5,
     return DecodeCase(name, q, pool, nk, nv, slots, H, Hk, D, 1.0 / math.sqrt(D), dtype)
 
 
+@dataclass
+class ForkedDecodeCase(DecodeCase):
+    """A decode batch made of groups of forks: group g is sequences
+    group_starts[g] .. group_starts[g+1]-1, whose block tables hold the same
+    physical blocks for the first prefix_lens[g] // S blocks."""
+    group_starts: torch.Tensor = None    # int32 [n_groups + 1]
+    shared_lens: torch.Tensor = None     # int32 [n_groups], tokens (the prompt length)
+
+
+def forked_decode(name: str, seed: int, groups, H: int, Hk: int, D: int, S: int, dtype,
+                  pool_factor: float = 1.25, poison: bool = True) -> ForkedDecodeCase:
+    """groups: list of (prompt_len, [ctx of each fork]).  The prompt's full
+    blocks are shared by all forks of the group (one set of physical blocks);
+    from there on each fork owns its blocks, and the prompt's partial last
+    block is copied into every fork's first own block (as copy-on-write leaves
+    it).  Blocks are scattered over a random permutation of the pool; slots no
+    fork may read are NaN.  Each fork whose last token lies in an own block
+    gets that token as a new K/V to store before the attention."""
+    g = _gen(seed)
+    nshared = [P // S for P, _ in groups]
+    own = [[max(0, (c + S - 1) // S - ns) for c in ctxs] for ns, (_, ctxs) in zip(nshared, groups)]
+    needed = sum(nshared) + sum(sum(o) for o in own)
+    NB = max(needed + 1, int(math.ceil(pool_factor * needed)))
+    perm = torch.randperm(NB, generator=g, dtype=torch.int64).to(torch.int32)
+    ctx_all = [c for _, ctxs in groups for c in ctxs]
+    B = len(ctx_all)
+    max_blocks = max(1, max((c + S - 1) // S for c in ctx_all) if ctx_all else 1)
+    pad = int(perm[needed])
+    bt = torch.full((B, max_blocks), pad, dtype=torch.int32)
+    nxt, row, starts = 0, 0, [0]
+    copies = []                       # (src block, dst block, tokens) of the prompt's partial block
+    for (P, ctxs), ns, ow in zip(groups, nshared, own):
+        shared_ids = perm[nxt:nxt + ns]
+        nxt += ns
+        first_own = None
+        for c, n_own in zip(ctxs, ow):
+            bt[row, :ns] = shared_ids[:min(ns, (c + S - 1) // S)]
+            bt[row, ns:ns + n_own] = perm[nxt:nxt + n_own]
+            if n_own > 0 and P % S:
+                if first_own is None:
+                    first_own = int(perm[nxt])
+                else:
+                    copies.append((first_own, int(perm[nxt]), P % S))
+            nxt += n_own
+            row += 1
+        starts.append(row)
+    ctx = torch.tensor(ctx_all, dtype=torch.int64)
+    valid = valid_slots(bt, ctx, S, NB)
+    k, v = fill_pool(g, NB, Hk, S, D, dtype, valid if poison else None)
+    for src, dst, n in copies:
+        k[dst, :, :n] = k[src, :, :n]
+        v[dst, :, :n] = v[src, :, :n]
+    pool = PagedPool(k, v, bt, ctx.to(torch.int32), S, NB, pad, valid)
+    q = torch.randn(B, H, D, generator=g).to(dtype)
+    seqs, pos = [], []
+    r = 0
+    for (P, ctxs), ns in zip(groups, nshared):
+        for c in ctxs:
+            if c > ns * S:            # the last token sits in an own block
+                seqs.append(r)
+                pos.append(c - 1)
+            r += 1
+    slots = slot_mapping_for(bt, seqs, pos, S) if seqs else torch.zeros(0, dtype=torch.int64)
+    nk = torch.randn(len(seqs), Hk, D, generator=g).to(dtype)
+    nv = torch.randn(len(seqs), Hk, D, generator=g).to(dtype)
+    if poison and seqs:
+        pool.key_cache[slots // S, :, slots % S] = float("nan")
+        pool.value_cache[slots // S, :, slots % S] = float("nan")
+    return ForkedDecodeCase(name, q, pool, nk, nv, slots, H, Hk, D, 1.0 / math.sqrt(D), dtype,
+                            torch.tensor(starts, dtype=torch.int32),
+                            torch.tensor([P for P, _ in groups], dtype=torch.int32))
+
+
 # ---- the five workloads -----------------------------------------------------
 
 def tiny_decode(seed: int = 0) -> DecodeCase:
