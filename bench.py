@@ -776,9 +776,10 @@ def bench_cow(pd, pd_inputs, dev, args, flush, hbm_peak):
         t_sh = _time_calls(shared_decode, n, flush)
 
         def whole_shared():
-            pd.pd_copy_blocks([kc], [vc], pr)
-            pd.pd_reshape_and_cache(nk, nv, kc, vc, sl)
-            shared_decode()
+            # copies -> store -> shared-prefix decode as one chain of dependent grids
+            pd.pd_decode_step_shared(out, q, kc, vc, bt, cl, mcl, fc.scale, gs_d, sl_d, fc.n_fork,
+                                     key=nk, value=nv, slot_mapping=sl, block_mapping=pr,
+                                     workspace=ws_sh)
 
         t_step_sh = _time_calls(whole_shared, n, flush)
         sha = source_sha("decode.cu", "pd_device.cuh")
@@ -807,6 +808,8 @@ def bench_cow(pd, pd_inputs, dev, args, flush, hbm_peak):
                                     "blocks read once for its 8 forks)",
                             "decode_ms": round(t_sh * 1e3, 4),
                             "step_ms": round(t_step_sh * 1e3, 4),
+                            "step": "pd_decode_step_shared: copy_blocks -> store -> shared-prefix "
+                                    "decode, each grid a programmatic dependent of the last",
                             "decode_unique_gbs": round(unique / t_sh / 1e9, 1),
                             "decode_unique_frac": round(unique / t_sh / 1e9 / hbm_peak, 4),
                             "decode_logical_gbs": round(logical / t_sh / 1e9, 1),

@@ -237,7 +237,37 @@ PD_API pd_status pd_paged_attention_decode_shared(void* out, const void* q,
                                                   int max_group, void* workspace,
                                                   size_t workspace_bytes, pd_dtype dt,
                                                   int32_t* dev_err, cudaStream_t stream);
-/* Host helper for the call above (no CUDA calls): cut sequences 0 .. B-1 into
+/* pd_decode_step_shared: one copy-on-write decode step of one layer over
+ * forks that share blocks (tutorial page "LLM 推理服务引擎深度拆解", section
+ * 2.3: a fork about to write a shared block first gets a copy of it, then
+ * appends its token): the block copies, then the store of the new tokens,
+ * then pd_paged_attention_decode_shared.  The result is exactly that of
+ * pd_copy_blocks (this layer's pools only), pd_reshape_and_cache and
+ * pd_paged_attention_decode_shared on the same stream.
+ *   block_mapping  DEVICE int64 [npairs][2] (src, dst) copied in key_cache
+ *                  and value_cache as by pd_copy_blocks; npairs == 0: none
+ * every other argument as for pd_reshape_and_cache (key, value,
+ * slot_mapping, T, strides; T == 0 skips the store) and for
+ * pd_paged_attention_decode_shared.  Each grid is launched as a programmatic
+ * dependent of the one before it: the store waits for the copies before it
+ * writes, the decode waits for the store (and so for the copies) before it
+ * reads the pools; prologues overlap.  Reads of q, block_tables,
+ * context_lens and the group arrays may happen while the copies and the
+ * store run.  All checks are made before anything is launched. */
+PD_API pd_status pd_decode_step_shared(const int64_t* block_mapping, int npairs,
+                                       const void* key, const void* value,
+                                       const int64_t* slot_mapping, int T,
+                                       int64_t key_stride_tok, int64_t value_stride_tok,
+                                       void* out, const void* q, void* key_cache,
+                                       void* value_cache, const int32_t* block_tables,
+                                       int max_blocks_per_seq, const int32_t* context_lens,
+                                       int B, int H, int Hk, int D, int S, int NB,
+                                       int max_context_len, float scale,
+                                       const int32_t* group_starts, const int32_t* shared_lens,
+                                       int n_groups, int max_group, void* workspace,
+                                       size_t workspace_bytes, pd_dtype dt, int32_t* dev_err,
+                                       cudaStream_t stream);
+/* Host helper for the shared-prefix calls (no CUDA calls): cut sequences 0 .. B-1 into
  * groups of consecutive sequences that share leading blocks.  block_tables and
  * context_lens are HOST arrays laid out as for the decode calls.  For each
  * sequence i, its shared prefix with the first member f of the current group

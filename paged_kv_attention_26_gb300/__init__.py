@@ -59,6 +59,9 @@ SIGNATURES = {
     "pd_decode_shared_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "pd_paged_attention_decode_shared": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
                                               _I, _I, _F, _P, _P, _I, _I, _P, _SZ, _I, _P, _P]),
+    "pd_decode_step_shared": (_I, [_P, _I, _P, _P, _P, _I, _I64, _I64, _P, _P, _P, _P, _P, _I,
+                                   _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _I, _I, _P, _SZ,
+                                   _I, _P, _P]),
     "pd_find_shared_prefixes": (_I, [ctypes.POINTER(ctypes.c_int32), _I,
                                      ctypes.POINTER(ctypes.c_int32), _I, _I, _I, _I,
                                      ctypes.POINTER(ctypes.c_int32),
@@ -395,6 +398,61 @@ def pd_paged_attention_decode_shared(out, q, key_cache, value_cache, block_table
         _dev(shared_lens, "shared_lens", torch.int32), n_groups, int(max_group), ws_ptr,
         ws_bytes, dt, _opt(dev_err), _stream(stream))
     _check("pd_paged_attention_decode_shared", st)
+
+
+def pd_decode_step_shared(out, q, key_cache, value_cache, block_tables, context_lens,
+                          max_context_len: int, scale: float, group_starts, shared_lens,
+                          max_group: int, key=None, value=None, slot_mapping=None,
+                          block_mapping=None, workspace=None, dev_err=None, stream=None):
+    """One copy-on-write decode step of one layer over forks sharing blocks:
+    ``block_mapping`` (int64 CUDA [npairs, 2], or None) block copies in these
+    pools, then the store of ``key``/``value`` [T, Hk, D] at ``slot_mapping``
+    (or None), then ``pd_paged_attention_decode_shared``; each grid a
+    programmatic dependent of the one before it."""
+    torch = _torch()
+    B, H, D = q.shape
+    NB, Hk, S, D2 = key_cache.shape
+    if out.shape != q.shape or D2 != D or value_cache.shape != key_cache.shape:
+        raise ValueError("shape mismatch")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables / context_lens shape")
+    n_groups = shared_lens.numel()
+    if group_starts.shape != (n_groups + 1,):
+        raise ValueError("group_starts must have n_groups + 1 entries")
+    dt = _dt(key_cache)
+    for t in (q, out, value_cache):
+        if t.dtype != key_cache.dtype:
+            raise TypeError("dtype mismatch")
+    npairs, bm = 0, None
+    if block_mapping is not None and block_mapping.numel():
+        if block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
+            raise ValueError("block_mapping must be [npairs, 2]")
+        npairs, bm = block_mapping.shape[0], _dev(block_mapping, "block_mapping", torch.int64)
+    T, kp, vp, sp, ks, vs = 0, None, None, None, 0, 0
+    if key is not None and key.shape[0]:
+        T = key.shape[0]
+        if key.shape != (T, Hk, D) or value.shape != key.shape or slot_mapping.shape != (T,):
+            raise ValueError("key / value / slot_mapping shape")
+        for t, n in ((key, "key"), (value, "value")):
+            if t.stride(2) != 1 or t.stride(1) != D:
+                raise ValueError(f"{n} must have contiguous heads and dims")
+            if t.dtype != key_cache.dtype:
+                raise TypeError("dtype mismatch")
+        kp, vp = _dev(key, "key", contiguous=False), _dev(value, "value", contiguous=False)
+        sp = _dev(slot_mapping, "slot_mapping", torch.int64)
+        ks, vs = key.stride(0), value.stride(0)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    st = load().pd_decode_step_shared(
+        bm, npairs, kp, vp, sp, T, ks, vs, _dev(out, "out"), _dev(q, "q"),
+        _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), B, H, Hk, D, S, NB,
+        int(max_context_len), float(scale), _dev(group_starts, "group_starts", torch.int32),
+        _dev(shared_lens, "shared_lens", torch.int32), n_groups, int(max_group), ws_ptr,
+        ws_bytes, dt, _opt(dev_err), _stream(stream))
+    _check("pd_decode_step_shared", st)
 
 
 def pd_paged_attention_verify(out, q, key_cache, value_cache, block_tables, context_lens,

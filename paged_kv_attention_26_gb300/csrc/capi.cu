@@ -294,6 +294,51 @@ pd_status pd_paged_attention_decode_shared(void* out, const void* q, const void*
     return launch_decode(a);
 }
 
+pd_status pd_decode_step_shared(const int64_t* block_mapping, int npairs, const void* key,
+                                const void* value, const int64_t* slot_mapping, int T,
+                                int64_t key_stride_tok, int64_t value_stride_tok, void* out,
+                                const void* q, void* key_cache, void* value_cache,
+                                const int32_t* block_tables, int max_blocks_per_seq,
+                                const int32_t* context_lens, int B, int H, int Hk, int D, int S,
+                                int NB, int max_context_len, float scale,
+                                const int32_t* group_starts, const int32_t* shared_lens,
+                                int n_groups, int max_group, void* workspace,
+                                size_t workspace_bytes, pd_dtype dt, int32_t* dev_err,
+                                cudaStream_t stream) {
+    DecodeArgs a{};
+    bool skip_dec = false, skip_store = false;
+    if (npairs < 0 || (npairs > 0 && !block_mapping)) return PD_ERR_INVALID_ARG;
+    const SharedGroups grp{group_starts, shared_lens, n_groups, max_group};
+    pd_status st = decode_prepare(out, q, key_cache, value_cache, nullptr, nullptr, false,
+                                  block_tables, max_blocks_per_seq, context_lens, B, H, Hk, D, S,
+                                  NB, max_context_len, scale, workspace, workspace_bytes, dt,
+                                  dev_err, stream, &a, &skip_dec, 1, true, &grp);
+    if (st != PD_OK) return st;
+    st = store_check(key, value, key_cache, value_cache, slot_mapping, T, Hk, D, S, NB,
+                     key_stride_tok, value_stride_tok, false, nullptr, nullptr, dt, &skip_store);
+    if (st != PD_OK) return st;
+    // copy -> store -> decode, each grid a programmatic dependent of the one
+    // before it: the store waits for the copy before writing, the decode for
+    // the store (and so for the copy) before reading the pools
+    bool launched = false;
+    if (npairs > 0) {
+        st = launch_copy_blocks(nullptr, nullptr, 1, block_mapping, npairs, Hk, D, S, NB, 2,
+                                dev_err, stream, key_cache, value_cache);
+        if (st != PD_OK) return st;
+        launched = true;
+    }
+    if (!skip_store) {
+        st = launch_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, T, Hk, D,
+                                      S, NB, key_stride_tok, value_stride_tok, dev_err, stream,
+                                      launched);
+        if (st != PD_OK) return st;
+        launched = true;
+    }
+    if (skip_dec) return PD_OK;
+    a.pdl = launched;
+    return launch_decode(a);
+}
+
 pd_status pd_paged_attention_verify(void* out, const void* q, const void* key_cache,
                                     const void* value_cache, const int32_t* block_tables,
                                     int max_blocks_per_seq, const int32_t* context_lens, int B,

@@ -85,16 +85,18 @@ pd_status launch_reshape_and_cache(const void* key, const void* value, void* key
                                    void* value_cache, const int64_t* slot_mapping, int T,
                                    int Hk, int D, int S, int NB, int64_t key_stride_tok,
                                    int64_t value_stride_tok, int32_t* dev_err,
-                                   cudaStream_t stream);
+                                   cudaStream_t stream, bool pdl = false);
 pd_status launch_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,
                                        void* value_cache, const int64_t* slot_mapping, int T,
                                        int Hk, int D, int S, int NB, int64_t key_stride_tok,
                                        int64_t value_stride_tok, const float* k_scale,
                                        const float* v_scale, pd_dtype in_dt, int32_t* dev_err,
                                        cudaStream_t stream);
+// key_caches == nullptr: one layer whose pools are k_pool / v_pool.
 pd_status launch_copy_blocks(void* const* key_caches, void* const* value_caches, int L,
                              const int64_t* block_mapping, int npairs, int Hk, int D, int S,
-                             int NB, int esize, int32_t* dev_err, cudaStream_t stream);
+                             int NB, int esize, int32_t* dev_err, cudaStream_t stream,
+                             void* k_pool = nullptr, void* v_pool = nullptr);
 
 // ---- KV pack / unpack ------------------------------------------------------------------
 pd_status launch_kv_pack(bool unpack, void* staging, void* const* key_caches,

@@ -36,6 +36,10 @@ reshape_and_cache_kernel(const uint4* __restrict__ key, const uint4* __restrict_
     const uint4 kv = __ldg(key + n * key_stride_vec + int64_t(h) * vec_per_row + c);
     const uint4 vv = __ldg(value + n * value_stride_vec + int64_t(h) * vec_per_row + c);
     const int64_t slot = __ldg(slot_mapping + n);
+    // Launched as a dependent of a block-copy grid, the writes wait for that
+    // grid (the slot may lie in a block it is copying); returns at once for
+    // an ordinary launch.
+    pdl_wait_primary();
     if (slot < 0) return;                       // padding token
     if (slot >= int64_t(NB) * S) {
         if (c == 0) flag_error(dev_err, PD_DEVERR_SLOT_RANGE);
@@ -72,6 +76,7 @@ reshape_and_cache_fp8_kernel(const uint4* __restrict__ key, const uint4* __restr
     const uint4 k0 = __ldg(key + src_k), k1 = __ldg(key + src_k + 1);
     const uint4 v0 = __ldg(value + src_v), v1 = __ldg(value + src_v + 1);
     const int64_t slot = __ldg(slot_mapping + n);
+    pdl_wait_primary();                         // as in the 16-bit store
     if (slot < 0) return;                       // padding token
     if (slot >= int64_t(NB) * S) {
         if (c == 0) flag_error(dev_err, PD_DEVERR_SLOT_RANGE);
@@ -105,11 +110,16 @@ constexpr int kCopyThreads = 256;
 constexpr int kCopyUnroll = 4;
 
 // blockIdx.x = pair, blockIdx.y = layer, blockIdx.z = 0 for K, 1 for V.
-// The whole block (Hk * S * D elements) is contiguous in the pool.
+// The whole block (Hk * S * D elements) is contiguous in the pool.  The pools
+// come from the device pointer arrays, or (key_caches == nullptr, one layer)
+// are the pools k_pool / v_pool themselves.
 __global__ void __launch_bounds__(kCopyThreads)
 copy_blocks_kernel(void* const* __restrict__ key_caches, void* const* __restrict__ value_caches,
-                   const int64_t* __restrict__ block_mapping, int NB, int64_t block_vecs,
-                   int32_t* dev_err) {
+                   void* k_pool, void* v_pool, const int64_t* __restrict__ block_mapping, int NB,
+                   int64_t block_vecs, int32_t* dev_err) {
+    // a store grid launched as our dependent may start now; it waits for
+    // this grid before it writes
+    pdl_launch_dependents();
     const int64_t src = __ldg(block_mapping + 2 * blockIdx.x);
     const int64_t dst = __ldg(block_mapping + 2 * blockIdx.x + 1);
     if (src < 0 || src >= NB || dst < 0 || dst >= NB) {
@@ -117,8 +127,13 @@ copy_blocks_kernel(void* const* __restrict__ key_caches, void* const* __restrict
             flag_error(dev_err, PD_DEVERR_BLOCK_RANGE);
         return;
     }
-    void* const* pools = blockIdx.z == 0 ? key_caches : value_caches;
-    uint4* pool = static_cast<uint4*>(pools[blockIdx.y]);
+    uint4* pool;
+    if (key_caches != nullptr) {
+        void* const* pools = blockIdx.z == 0 ? key_caches : value_caches;
+        pool = static_cast<uint4*>(pools[blockIdx.y]);
+    } else {
+        pool = static_cast<uint4*>(blockIdx.z == 0 ? k_pool : v_pool);
+    }
     if (reinterpret_cast<uintptr_t>(pool) & 15u) {     // pointer table is device data
         if (threadIdx.x == 0) flag_error(dev_err, PD_DEVERR_BLOCK_RANGE);
         return;
@@ -146,15 +161,24 @@ pd_status launch_reshape_and_cache(const void* key, const void* value, void* key
                                    void* value_cache, const int64_t* slot_mapping, int T,
                                    int Hk, int D, int S, int NB, int64_t key_stride_tok,
                                    int64_t value_stride_tok, int32_t* dev_err,
-                                   cudaStream_t stream) {
+                                   cudaStream_t stream, bool pdl) {
     if (T == 0) return PD_OK;
     const int64_t threads = int64_t(T) * Hk * (D / 8);
     const int64_t blocks = (threads + kStoreThreads - 1) / kStoreThreads;
-    reshape_and_cache_kernel<<<unsigned(blocks), kStoreThreads, 0, stream>>>(
-        static_cast<const uint4*>(key), static_cast<const uint4*>(value),
-        static_cast<uint4*>(key_cache), static_cast<uint4*>(value_cache), slot_mapping, T, Hk,
-        D, S, NB, key_stride_tok / 8, value_stride_tok / 8, dev_err);
-    return launch_result(cudaGetLastError());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(kStoreThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return launch_result(cudaLaunchKernelEx(
+        &cfg, reshape_and_cache_kernel, static_cast<const uint4*>(key),
+        static_cast<const uint4*>(value), static_cast<uint4*>(key_cache),
+        static_cast<uint4*>(value_cache), slot_mapping, T, Hk, D, S, NB, key_stride_tok / 8,
+        value_stride_tok / 8, dev_err));
 }
 
 pd_status launch_reshape_and_cache_fp8(const void* key, const void* value, void* key_cache,
@@ -177,12 +201,13 @@ pd_status launch_reshape_and_cache_fp8(const void* key, const void* value, void*
 
 pd_status launch_copy_blocks(void* const* key_caches, void* const* value_caches, int L,
                              const int64_t* block_mapping, int npairs, int Hk, int D, int S,
-                             int NB, int esize, int32_t* dev_err, cudaStream_t stream) {
+                             int NB, int esize, int32_t* dev_err, cudaStream_t stream,
+                             void* k_pool, void* v_pool) {
     if (npairs == 0 || L == 0) return PD_OK;
     const int64_t block_vecs = int64_t(Hk) * S * D * esize / 16;
     dim3 grid(unsigned(npairs), unsigned(L), 2);
-    copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(key_caches, value_caches,
-                                                          block_mapping, NB, block_vecs,
+    copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(key_caches, value_caches, k_pool,
+                                                          v_pool, block_mapping, NB, block_vecs,
                                                           dev_err);
     return launch_result(cudaGetLastError());
 }

@@ -195,3 +195,60 @@ def test_declared_prefix_longer_than_a_member(cuda_lib):
                                 16, torch.bfloat16)
     sl = torch.tensor([5000, 45], dtype=torch.int32)
     _check(cuda_lib, c, "declared prefix cut", groups=(c.group_starts, sl))
+
+
+@pytest.mark.parametrize("S", [8, 16, 64])
+def test_step_shared_matches_separate_calls(cuda_lib, S):
+    """pd_decode_step_shared (copies -> store -> decode as dependent grids)
+    leaves the pools bit-exact as the oracle's copy and store do, and its
+    output bit-identical to pd_copy_blocks + pd_reshape_and_cache +
+    pd_paged_attention_decode_shared on the same stream; also with no copies
+    and with no stored tokens."""
+    pd = cuda_lib
+    fc = pd_inputs.cow_fork_stress(S, n_prompts=12)
+    tables, ctx, slots, pairs = fork_flow(fc, OracleBM)
+    dev = torch.device("cuda")
+    mb = max(len(t) for t in tables)
+    bt = torch.zeros(len(tables), mb, dtype=torch.int32)
+    for i, t in enumerate(tables):
+        bt[i, :len(t)] = torch.tensor(t, dtype=torch.int32)
+    cl = torch.tensor(ctx, dtype=torch.int32)
+    gs, sl = pd.find_shared_prefixes(bt, cl, S, max_group=8)
+    n, mcl = len(tables), max(ctx)
+    q = fc.q.to(dev)
+    nk, nv = fc.new_key.to(dev), fc.new_value.to(dev)
+    sm = torch.tensor(slots, dtype=torch.int64, device=dev)
+    pr = torch.tensor(pairs, dtype=torch.int64, device=dev).view(-1, 2)
+    btd, cld, gsd, sld = bt.to(dev), cl.to(dev), gs.to(dev), sl.to(dev)
+    ws = pd.decode_shared_workspace(sl.numel(), 8, fc.H, fc.Hk, fc.D)
+    err = device_err()
+    for with_pairs, with_store in ((True, True), (False, True), (True, False)):
+        k1, v1 = fc.key_cache.to(dev), fc.value_cache.to(dev)
+        k2, v2 = fc.key_cache.to(dev), fc.value_cache.to(dev)
+        o1, o2 = torch.full_like(q, float("nan")), torch.full_like(q, float("nan"))
+        if with_pairs:
+            pd.pd_copy_blocks([k1], [v1], pr, dev_err=err)
+        if with_store:
+            pd.pd_reshape_and_cache(nk, nv, k1, v1, sm, dev_err=err)
+        pd.pd_paged_attention_decode_shared(o1, q, k1, v1, btd, cld, mcl, fc.scale, gsd, sld, 8,
+                                            ws, dev_err=err)
+        pd.pd_decode_step_shared(o2, q, k2, v2, btd, cld, mcl, fc.scale, gsd, sld, 8,
+                                 key=nk if with_store else None,
+                                 value=nv if with_store else None,
+                                 slot_mapping=sm if with_store else None,
+                                 block_mapping=pr if with_pairs else None, workspace=ws,
+                                 dev_err=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        assert np.array_equal(u16(k1), u16(k2))
+        assert np.array_equal(u16(v1), u16(v2))
+        assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+        if with_pairs and with_store:
+            rk, rv = u16(fc.key_cache), u16(fc.value_cache)
+            oracle.copy_blocks([rk], [rv], np.array(pairs, dtype=np.int64))
+            oracle.reshape_and_cache(fc.new_key, fc.new_value, rk, rv, torch.tensor(slots), S)
+            assert np.array_equal(u16(k2), rk) and np.array_equal(u16(v2), rv)
+            rows = (0, 16 * fc.H)
+            ref = oracle.decode(fc.q, rk, rv, bt, cl, fc.scale, odt(fc.dtype), rows=rows)
+            assert_close(o2.cpu().reshape(-1, fc.D)[rows[0]:rows[1]],
+                         ref.reshape(-1, fc.D)[rows[0]:rows[1]], f"cow step S{S}")
