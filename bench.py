@@ -40,6 +40,9 @@ METRIC = ("Paged decode-attn achieved HBM GB/s (% of GB300 peak); KV tokens/s; "
           "prefill TFLOP/s")
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+# GB300's nominal figures (context beside the measured denominators)
+NOMINAL_HBM_GBS = 7900.0
+NOMINAL_BF16_TFLOPS = 2250.0
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -288,10 +291,13 @@ def run_ours(args, rank, world, local_rank):
                          "before every timed step by reading a 256 MiB buffer",
                    "parallelism": f"replicas x{world}"},
         "pct_of_hbm_peak": round(100 * value / world / hbm_peak, 2),
+        "pct_of_nominal_hbm_peak": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "kv_tokens_per_s": round(world * sum(ctx) * args.steps / step_s, 1),
         "roofline": {"kernel": "paged_decode_split_kernel", "bound": "hbm",
                      "achieved": round(achieved, 2), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
+                     "nominal_peak": NOMINAL_HBM_GBS,
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                      "alg_bytes_per_launch": dec_bytes,
                      "timing": "the decode launched alone, steps x (L2 flush, launch), CUDA "
                                "events on the launching stream",
@@ -387,10 +393,11 @@ def run_only_extras(args):
 
 def e2e_decode(pd, c, dev, args, step_bytes, world=1):
     """The same step through the public API from pinned host memory:
-    ``DecodeStep`` (one pinned staging buffer holding q, the new K/V, slots,
-    block tables and context lengths; one copy in, ``pd_decode_step``, one copy
-    of ``out`` back, synchronize), replayed from a CUDA graph; the same object
-    run eagerly is reported beside it."""
+    ``DecodeStep`` (one pinned buffer holding q, the new K/V, slots, block
+    tables and context lengths; the tables and lengths copied in, q / K/V /
+    slots read and ``out`` written by the kernels over the host link,
+    synchronize), replayed from a CUDA graph; the same object run eagerly is
+    reported beside it."""
     import torch
     kc, vc = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -426,10 +433,12 @@ def e2e_decode(pd, c, dev, args, step_bytes, world=1):
     return {"value": round(whole_job_value(step_bytes, args.steps, total, world), 2), "unit": "GB/s",
             "ms_per_step": round(total / args.steps * 1e3, 4),
             "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world,
-            "path": "DecodeStep replayed from a CUDA graph: pd_copy_bytes of the step's inputs "
-                    "from one pinned host buffer to the device, pd_decode_step, pd_copy_bytes of "
-                    "out to pinned host memory, synchronize; host wall clock per step, L2 "
-                    "flushed before each",
+            "path": "DecodeStep replayed from a CUDA graph: pd_copy_bytes of the block tables "
+                    "and context lengths from the pinned host buffer to the device, then "
+                    "pd_decode_step reading q, the new K/V and the slots from that pinned "
+                    "buffer and writing out into pinned host memory over the host link, "
+                    "synchronize; host wall clock per step, L2 flushed before each; the byte "
+                    "counts are every input and output byte that crosses the link",
             "eager_value": round(whole_job_value(step_bytes, args.steps, eager, world), 2),
             "eager_ms_per_step": round(eager / args.steps * 1e3, 4)}
 
@@ -543,6 +552,7 @@ def bench_prefill_mix(pd, pd_inputs, dev, args, flush, bf16_peak, hbm_peak, peak
             "prefill_ms": round(t_pre * 1e3, 4), "prefill_gflop": round(flops / 1e9, 2),
             "prefill_tflops": round(flops / t_pre / 1e12, 2),
             "prefill_frac": round(flops / t_pre / 1e12 / bf16_peak, 4),
+            "prefill_frac_of_nominal": round(flops / t_pre / 1e12 / NOMINAL_BF16_TFLOPS, 4),
             "prefill_peak_tflops": bf16_peak, "peak_source": peak_src,
             "store_tokens": sl.numel(), "store_gbs": round(sbytes / t_store / 1e9, 1),
             "decode_ms": round(t_dec * 1e3, 4), "decode_gbs": round(dbytes / t_dec / 1e9, 1),

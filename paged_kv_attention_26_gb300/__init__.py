@@ -177,9 +177,12 @@ def _is_fp8(t) -> bool:
     return _dt(t) == PD_FP8_E4M3
 
 
-def _dev(t, name, dtype=None, contiguous=True):
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+def _dev(t, name, dtype=None, contiguous=True, host_ok=False):
+    # host_ok: pinned host memory is accepted too (with unified addressing its
+    # host address is the address the kernels use, over the host link)
+    if not t.is_cuda and not (host_ok and t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor" +
+                         (" or pinned host memory" if host_ok else ""))
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if contiguous and not t.is_contiguous():
@@ -561,7 +564,9 @@ def pd_decode_step(out, q, key_cache, value_cache, block_tables, context_lens,
     ``out``.  The same result as ``pd_reshape_and_cache`` (``_fp8`` with
     scales) followed by ``pd_paged_attention_decode`` (``_fp8``); the decode
     grid's prologue overlaps the store.  One-byte pools need ``k_scale`` and
-    ``v_scale`` (float32 [Hk])."""
+    ``v_scale`` (float32 [Hk]).  ``q``, ``key``, ``value``, ``slot_mapping``
+    and ``out`` may be pinned host tensors: the kernels then read and write
+    them over the host link, with no separate copy."""
     torch = _torch()
     B, H, D = q.shape
     NB, Hk, S, D2 = key_cache.shape
@@ -584,10 +589,11 @@ def pd_decode_step(out, q, key_cache, value_cache, block_tables, context_lens,
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
-    head = (_dev(key, "key", contiguous=False), _dev(value, "value", contiguous=False),
-            _dev(slot_mapping, "slot_mapping", torch.int64), T, key.stride(0), value.stride(0),
-            _dev(out, "out"), _dev(q, "q"), _dev(key_cache, "key_cache"),
-            _dev(value_cache, "value_cache"))
+    head = (_dev(key, "key", contiguous=False, host_ok=True),
+            _dev(value, "value", contiguous=False, host_ok=True),
+            _dev(slot_mapping, "slot_mapping", torch.int64, host_ok=True), T, key.stride(0),
+            value.stride(0), _dev(out, "out", host_ok=True), _dev(q, "q", host_ok=True),
+            _dev(key_cache, "key_cache"), _dev(value_cache, "value_cache"))
     tail = (_dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
             _dev(context_lens, "context_lens", torch.int32), B, H, Hk, D, S, NB,
             int(max_context_len), float(scale), ws_ptr, ws_bytes, _dt(q), _opt(dev_err),
@@ -612,16 +618,18 @@ class DecodeStep:
     The step's inputs live in one pinned host buffer, exposed as views in
     ``host`` (``q`` [B, H, D], ``key``/``value`` [T, Hk, D], ``slot_mapping``
     int64 [T], ``block_tables`` int32 [B, max_blocks_per_seq],
-    ``context_lens`` int32 [B]).  A call copies that buffer to the device in
-    one transfer, runs ``pd_decode_step`` (store, then decode as a dependent
-    grid) and copies ``out`` back into the pinned ``host_out``; both copies
-    are ``pd_copy_bytes`` (SM kernels reading and writing the pinned buffers
-    directly).  With
-    ``graph=True`` those three operations are captured once in a CUDA graph
-    and each call replays it; ``max_context_len`` and ``scale`` are fixed at
-    construction (contexts may vary per call up to that bound).  One-byte
-    pools take ``k_scale``/``v_scale`` (float32 CUDA [Hk]).  The device error
-    word of the last call is ``dev_err``."""
+    ``context_lens`` int32 [B]); the result lands in the pinned ``host_out``.
+    A call copies the block tables and context lengths (the part that every
+    CTA of the decode reads) to the device in one ``pd_copy_bytes`` and runs
+    ``pd_decode_step`` (store, then decode as a dependent grid) with q, the
+    new K/V, the slots and ``out`` passed as the pinned host buffers
+    themselves: the store and the decode read those and write the result over
+    the host link, so there is no other copy.  With ``graph=True`` the two
+    operations are captured once in a CUDA graph and each call replays it;
+    ``max_context_len`` and ``scale`` are fixed at construction (contexts may
+    vary per call up to that bound).  One-byte pools take
+    ``k_scale``/``v_scale`` (float32 CUDA [Hk]).  The device error word of the
+    last call is ``dev_err``."""
 
     def __init__(self, key_cache, value_cache, B: int, H: int, T: int, max_blocks_per_seq: int,
                  max_context_len: int, scale: float, dtype, k_scale=None, v_scale=None,
@@ -629,6 +637,8 @@ class DecodeStep:
         torch = _torch()
         dev = key_cache.device
         NB, Hk, S, D = key_cache.shape
+        # read by the kernels in place, then copied: tables and lengths last,
+        # so the copied part is one contiguous span
         fields = (("q", (B, H, D), dtype), ("key", (T, Hk, D), dtype),
                   ("value", (T, Hk, D), dtype), ("slot_mapping", (T,), torch.int64),
                   ("block_tables", (B, max_blocks_per_seq), torch.int32),
@@ -637,14 +647,17 @@ class DecodeStep:
         for name, shape, dt in fields:
             n = torch.empty(shape, dtype=dt, device="meta").numel() * \
                 torch.empty((), dtype=dt, device="meta").element_size()
+            if name == "block_tables":
+                self._copy_from = off
             spans.append((name, shape, dt, off, n))
             off += (n + 255) // 256 * 256
         self.host_buf = torch.zeros(max(off, 256), dtype=torch.uint8).pin_memory()
-        self.dev_buf = torch.zeros(self.host_buf.shape, dtype=torch.uint8, device=dev)
+        self._copy_host = self.host_buf[self._copy_from:]
+        self._copy_dev = torch.zeros(self._copy_host.shape, dtype=torch.uint8, device=dev)
         self.host = {n: self.host_buf[o:o + b].view(dt).view(shape) for n, shape, dt, o, b in spans}
-        self.dev = {n: self.dev_buf[o:o + b].view(dt).view(shape) for n, shape, dt, o, b in spans}
+        self.dev = {n: self._copy_dev[o - self._copy_from:o - self._copy_from + b]
+                    .view(dt).view(shape) for n, shape, dt, o, b in spans if o >= self._copy_from}
         self.host["slot_mapping"].fill_(-1)      # until the caller writes it: store nothing
-        self.out = torch.zeros((B, H, D), dtype=dtype, device=dev)
         self.host_out = torch.zeros((B, H, D), dtype=dtype).pin_memory()
         self.workspace = decode_workspace(B, H, D, max_context_len, device=dev)
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -667,13 +680,12 @@ class DecodeStep:
             self.graph = g
 
     def _body(self):
-        d = self.dev
-        pd_copy_bytes(self.dev_buf, self.host_buf)
-        pd_decode_step(self.out, d["q"], self.key_cache, self.value_cache, d["block_tables"],
-                       d["context_lens"], self.max_context_len, self.scale, d["key"], d["value"],
-                       d["slot_mapping"], workspace=self.workspace, k_scale=self.k_scale,
-                       v_scale=self.v_scale, dev_err=self.dev_err)
-        pd_copy_bytes(self.host_out, self.out)
+        h, d = self.host, self.dev
+        pd_copy_bytes(self._copy_dev, self._copy_host)
+        pd_decode_step(self.host_out, h["q"], self.key_cache, self.value_cache,
+                       d["block_tables"], d["context_lens"], self.max_context_len, self.scale,
+                       h["key"], h["value"], h["slot_mapping"], workspace=self.workspace,
+                       k_scale=self.k_scale, v_scale=self.v_scale, dev_err=self.dev_err)
 
     def __call__(self):
         torch = _torch()
@@ -686,6 +698,8 @@ class DecodeStep:
 
     @property
     def h2d_bytes(self) -> int:
+        """Input bytes that cross the host link per call: the copied tables
+        and lengths plus q, the new K/V and the slots read in place."""
         return self.host_buf.numel()
 
     @property
