@@ -35,9 +35,11 @@
 //    lazy rescaling when a max grows by more than 2^8) needs only three
 //    shuffle steps per head pair and no broadcasts; P is transposed into
 //    operand layout with movmatrix;
-//  * P enters the product as an unevaluated pair of 16-bit values
-//    (hi = rn(p), lo = rn(p - hi)), two MMAs per tile, so P carries about
-//    2^-17 relative error instead of the 2^-9 of a single bf16;
+//  * with bf16 operands P enters the product as an unevaluated pair of
+//    16-bit values (hi = rn(p), lo = rn(p - hi)), two MMAs per tile, so P
+//    carries about 2^-17 relative error instead of the 2^-9 of a single bf16;
+//    fp16 operands (fp16 pools, FP8 pools widened to fp16) take one fp16 P
+//    (2^-11, the size of q's own rounding in the FP8 path);
 //  * at the end of each stream piece the four warps merge through a small
 //    exchange buffer (after which all but the result warp go on to the next
 //    piece); a whole stream is normalised and written to `out`.
@@ -729,9 +731,10 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     const float2 neg1 = make_float2(-1.f, -1.f);
     uint32_t gs = 0;                             // stages consumed so far
     bool aborted = false;
-    // fp16 shared-prefix mode: P enters PV as one fp16 value (2^-11 relative
-    // rounding); otherwise as the hi + lo pair
-    constexpr bool kLoP = !(kFork && std::is_same<T, __half>::value);
+    // P enters PV as one 16-bit value when the products run on fp16 (fp16
+    // pools, FP8 pools, whose codes widen to fp16): 2^-11 relative rounding,
+    // as small as q's own; with bf16 operands (2^-9) as the hi + lo pair
+    constexpr bool kLoP = !std::is_same<TM, __half>::value;
 
     // output row of column n of stream x whose unit starts at head h0 (-1: a
     // padding column, or a member without context, whose rows others write)
@@ -997,7 +1000,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         }
                     }
                 }
-                uint32_t bh0[NS], bh1[NS], bl0[NS], bl1[NS];
+                uint32_t bh0[NS], bh1[NS];
+                [[maybe_unused]] uint32_t bl0[NS], bl1[NS];   // the lo half (kLoP only)
                 float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
                 for (int sb = 0; sb < NS; ++sb) {
@@ -1011,12 +1015,14 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         ls1 += p1 + p3;
                     }
                     const uint32_t hi0 = E::pack2(p0, p1), hi1 = E::pack2(p2, p3);
-                    const float2 lo0 = ffma2(E::unpack2(hi0), neg1, make_float2(p0, p1));
-                    const float2 lo1 = ffma2(E::unpack2(hi1), neg1, make_float2(p2, p3));
                     bh0[sb] = wmma16::movm_t(hi0);
                     bh1[sb] = wmma16::movm_t(hi1);
-                    bl0[sb] = wmma16::movm_t(E::pack2(lo0.x, lo0.y));
-                    bl1[sb] = wmma16::movm_t(E::pack2(lo1.x, lo1.y));
+                    if constexpr (kLoP) {
+                        const float2 lo0 = ffma2(E::unpack2(hi0), neg1, make_float2(p0, p1));
+                        const float2 lo1 = ffma2(E::unpack2(hi1), neg1, make_float2(p2, p3));
+                        bl0[sb] = wmma16::movm_t(E::pack2(lo0.x, lo0.y));
+                        bl1[sb] = wmma16::movm_t(E::pack2(lo1.x, lo1.y));
+                    }
                 }
                 l_run[0] += ls0;
                 l_run[1] += ls1;
@@ -1049,7 +1055,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                             }
                             const int mt = 2 * c + h2;
                             wmma16::Mma<TM>::run(o[mt], a, bh0[sb], bh1[sb]);
-                            wmma16::Mma<TM>::run(o[mt], a, bl0[sb], bl1[sb]);
+                            if constexpr (kLoP) wmma16::Mma<TM>::run(o[mt], a, bl0[sb], bl1[sb]);
                         }
                     }
                 }
