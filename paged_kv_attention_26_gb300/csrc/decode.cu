@@ -519,18 +519,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
     return r;
 }
 
-// Two E4M3 codes -> two fp16 values times 2^-8, exactly, with integer
-// operations only (no conversion unit): an E4M3 code s.eeee.mmm placed as
-// fp16 bits s.0eeee.mmm0000000 reads as its value times 2^-8 (the exponent
-// biases differ by 8; subnormal codes land on fp16 subnormals).  sel picks
-// the two bytes of w (0x1404: bytes 0, 1; 0x3424: bytes 2, 3).
-template <uint32_t kSel>
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t w) {
-    uint32_t t;
-    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(t) : "r"(w), "n"(kSel));
-    return (t & 0x80008000u) | ((t >> 1) & 0x3F803F80u);
-}
-
 // Two E4M3 codes at bytes (i, j) of w -> fp16x2 exactly (byte i low).
 template <uint32_t kSel>
 __device__ __forceinline__ uint32_t e4m3_pair_to_f16x2(uint32_t w) {
@@ -815,8 +803,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             }
         }
         // FP8 pools: the K scale joins the softmax scale, the V scale the output
-        // (K is widened to fp16 scaled by 2^-8: the 2^8 comes back here)
-        const float sl2 = kF8 ? scale_log2 * 256.f * __ldg(k_scale + kvh) : scale_log2;
+        const float sl2 = kF8 ? scale_log2 * __ldg(k_scale + kvh) : scale_log2;
         // O^T fragments: m-tile mt covers dims 16mt..16mt+15; lane holds dims
         // 16mt + lane/4 (regs 0,1) and + 8 (regs 2,3), heads 2(lane%4) and + 1.
         float o[KS][4];
@@ -868,8 +855,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int tslot = kF8 ? 0 : slot;
             if constexpr (kF8 && !kNative) {
                 if (tb < nt) {
-                    // K through integer operations (times 2^-8), V through the
-                    // conversion unit (exact): the two halves run on different pipes.
+                    // K and V widened exactly by the E4M3 -> fp16 conversion
                     constexpr int kChunks = D / 16;          // 16-byte chunks per FP8 row
                     const unsigned char* srck = smem + L::kK8 + slot * L::kTile8 + tb * D;
                     const unsigned char* srcv = smem + L::kV8 + slot * L::kTile8 + tb * D;
@@ -891,8 +877,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         uint32_t hk[8], hv[8];
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            hk[2 * j] = e4m3x2_to_f16x2_scaled<0x1404u>(wk[j]);
-                            hk[2 * j + 1] = e4m3x2_to_f16x2_scaled<0x3424u>(wk[j]);
+                            hk[2 * j] = e4m3x2_to_f16x2(uint16_t(wk[j] & 0xffffu));
+                            hk[2 * j + 1] = e4m3x2_to_f16x2(uint16_t(wk[j] >> 16));
                             hv[2 * j] = e4m3x2_to_f16x2(uint16_t(wv[j] & 0xffffu));
                             hv[2 * j + 1] = e4m3x2_to_f16x2(uint16_t(wv[j] >> 16));
                         }
@@ -944,7 +930,10 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 if (lane == 0)                               // the raw stages are free
                     for (int sb = 0; sb < NS; ++sb) mbar_arrive(&empty[(gs + sb) % kStages]);
                 // ---- S^T = K q^T: register j of block c holds row g (+8 for odd j),
-                // bytes 4t..4t+3 of dims 32c + 16 (j / 2) ..; K is widened as 2^-8 K
+                // bytes 4t..4t+3 of dims 32c + 16 (j / 2) ..; bytes 0, 1 and 2, 3
+                // widen exactly to the two fp16 pairs of the A fragment (one
+                // conversion each: fewer integer instructions than assembling the
+                // fp16 bits by hand, which kept the ALU pipe the busiest)
                 float acc[NS][2][4];
 #pragma unroll
                 for (int sb = 0; sb < NS; ++sb)
@@ -957,10 +946,10 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
                         for (int sb = 0; sb < NS; ++sb) {
                             uint32_t a[4];
-                            a[0] = e4m3x2_to_f16x2_scaled<0x1404u>(kr[sb][c][2 * h2]);
-                            a[1] = e4m3x2_to_f16x2_scaled<0x1404u>(kr[sb][c][2 * h2 + 1]);
-                            a[2] = e4m3x2_to_f16x2_scaled<0x3424u>(kr[sb][c][2 * h2]);
-                            a[3] = e4m3x2_to_f16x2_scaled<0x3424u>(kr[sb][c][2 * h2 + 1]);
+                            a[0] = e4m3x2_to_f16x2(uint16_t(kr[sb][c][2 * h2] & 0xffffu));
+                            a[1] = e4m3x2_to_f16x2(uint16_t(kr[sb][c][2 * h2 + 1] & 0xffffu));
+                            a[2] = e4m3x2_to_f16x2(uint16_t(kr[sb][c][2 * h2] >> 16));
+                            a[3] = e4m3x2_to_f16x2(uint16_t(kr[sb][c][2 * h2 + 1] >> 16));
                             const int ks = 2 * c + h2;
                             wmma16::Mma<TM>::run(acc[sb][ks & 1], a, qb[ks][0], qb[ks][1]);
                         }
