@@ -497,15 +497,18 @@ def _time_calls(fn, n, flush, warm=3):
         flush()
         fn()
     torch.cuda.synchronize()
-    ts = []
-    for _ in range(n):
+    # every call is enqueued behind its L2 flush before any is waited for, so
+    # the host's launch overhead hides behind the flush and the events time the
+    # device work alone
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for a, b in ev:
         flush()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         fn()
         b.record()
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b) * 1e-3)
+    torch.cuda.synchronize()
+    ts = [a.elapsed_time(b) * 1e-3 for a, b in ev]
     # mean without the slowest tenth of the calls (at least one when n >= 5): a
     # single call held up by something else on the machine should not move the
     # figure of a workload that runs in tens of microseconds

@@ -107,8 +107,12 @@ struct DecodeSmem {
     static constexpr int kV8 = kK8 + (kF8 ? kRing * kTile8 : 0);
     static constexpr int kX = kV8 + (kF8 ? kRing * kTile8 : 0);    // merge exchange [2][32][kFrag]
     static constexpr int kBar = kX + 2 * kFrag * 32 * 4;
-    static constexpr int kMisc = kBar + 2 * kRing * 8;     // abort flag, issued count
-    static constexpr int kBytes = kMisc + 16;
+    // ring barriers (full, empty), then the two tail-merge barriers
+    static constexpr int kMisc = kBar + (2 * kRing + 2) * 8;   // abort flag, issued count, flags
+    // tail merge: the other piece of the range's last stream, [8][D] of o,
+    // then m[8], l[8]
+    static constexpr int kTl = kMisc + 16;
+    static constexpr int kBytes = kTl + (kHeadsN * D + 2 * kHeadsN) * 4;
     static constexpr int kAlloc = kBytes + 1024;           // base aligned to 1 KB in-kernel
 };
 
@@ -288,10 +292,26 @@ __device__ __forceinline__ bool walk_begin(Walk& w, const int32_t* __restrict__ 
     const int members = gridDim.x / units;          // CTAs per unit group (>= 1)
     w.u = blockIdx.x % units;
     w.bi = blockIdx.x / units;
+    // Up to 128 streams: every lane's context lengths are loaded at once (one
+    // round trip to memory instead of one per 32 streams) and kept for the
+    // search below.
+    constexpr int kHeld = 4;
+    const bool held = !kFork && B <= 32 * kHeld;
+    long sv[kHeld];
     long total = 0;                                 // stages of one unit
-    for (int base = 0; base < B; base += 32) {
-        const int s = base + lane;
-        total += s < B ? stream_stages<kFork>(context_lens, s, cap, S, f) : 0;
+    if (held) {
+#pragma unroll
+        for (int i = 0; i < kHeld; ++i) {
+            const int s = 32 * i + lane;
+            sv[i] = s < B ? stream_stages<kFork>(context_lens, s, cap, S, f) : 0;
+        }
+#pragma unroll
+        for (int i = 0; i < kHeld; ++i) total += sv[i];
+    } else {
+        for (int base = 0; base < B; base += 32) {
+            const int s = base + lane;
+            total += s < B ? stream_stages<kFork>(context_lens, s, cap, S, f) : 0;
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
@@ -304,7 +324,14 @@ __device__ __forceinline__ bool walk_begin(Walk& w, const int32_t* __restrict__ 
     long prefix = 0;
     for (int base = 0; base < B; base += 32) {
         const int s = base + lane;
-        const long v = s < B ? stream_stages<kFork>(context_lens, s, cap, S, f) : 0;
+        long v = 0;
+        if (held) {
+#pragma unroll
+            for (int i = 0; i < kHeld; ++i)
+                if (32 * i == base) v = sv[i];
+        } else {
+            v = s < B ? stream_stages<kFork>(context_lens, s, cap, S, f) : 0;
+        }
         long incl = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -394,56 +421,76 @@ __device__ __forceinline__ bool arrive_piece(unsigned long long* cnt, unsigned l
 
 // Merge the np pieces of a stream's rows (one warp, fixed piece order):
 // M = max_k m_k; out = sum_k o_k 2^(m_k - M) / sum_k l_k 2^(m_k - M).
-// Four lanes per row (a quarter of D each), so every row is merged at once
-// and the loads of all pieces are in flight together.  The caller gives each
-// lane its row's output index orow (< 0: nothing to write) and the workspace
-// index of the row's first piece; later pieces follow at stride pstride.
-// Pieces of other CTAs are read through L2.
-template <typename T, int D>
+// Four lanes per row (a quarter of D each), so every row is merged at once.
+// With kAhead = 2 the o loads of the first two pieces go out together with
+// the pieces' (m, l), later pieces two at a time, so a two-piece stream (the
+// usual case) costs one L2 round trip; kAhead = 1 (kernels with no registers
+// to spare) loads one piece at a time once M is known.  The caller gives each lane its row's output index
+// orow (< 0: nothing to write) and the workspace index of the row's first
+// piece; later pieces follow at stride pstride.  Pieces of other CTAs are
+// read through L2.
+template <typename T, int D, int kAhead>
 __device__ __forceinline__ void merge_rows(T* __restrict__ out, const float* ws_o,
                                            const float* ws_m, const float* ws_l, int64_t orow,
                                            int64_t base, int pstride, int np, int lane) {
     using E = Elem<T>;
     constexpr int kDpl = D / 4;          // values per lane
-    constexpr int kCache = 8;            // pieces whose (m, l) stay in registers
+    constexpr int kV = kDpl / 4;         // float4 per lane and piece
+    constexpr int kCache = kAhead > 1 ? 4 : 8;   // pieces whose (m, l) stay in registers
     if (orow < 0) return;
     const int64_t row = orow;
     const float* m = ws_m + base;
     const float* l = ws_l + base;
-    const float* o = ws_o + base * D + (lane & 3) * kDpl;
+    const float4* o = reinterpret_cast<const float4*>(ws_o + base * D + (lane & 3) * kDpl);
+    const int64_t ostep = int64_t(pstride) * (D / 4);     // float4 from one piece to the next
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     float mc[kCache], lc[kCache];
-    float M = -INFINITY;
+    float4 v[kAhead][kV];
+    auto load_o = [&](int p0) {
+#pragma unroll
+        for (int a = 0; a < kAhead; ++a)
+#pragma unroll
+            for (int c = 0; c < kV; ++c)
+                v[a][c] = p0 + a < np ? __ldcg(o + int64_t(p0 + a) * ostep + c) : z4;
+    };
 #pragma unroll
     for (int p = 0; p < kCache; ++p) {
         mc[p] = p < np ? __ldcg(m + int64_t(p) * pstride) : -INFINITY;
         lc[p] = p < np ? __ldcg(l + int64_t(p) * pstride) : 0.f;
-        M = fmaxf(M, mc[p]);
     }
+    if constexpr (kAhead > 1) load_o(0);
+    float M = -INFINITY;
+#pragma unroll
+    for (int p = 0; p < kCache; ++p) M = fmaxf(M, mc[p]);
     for (int p = kCache; p < np; ++p) M = fmaxf(M, __ldcg(m + int64_t(p) * pstride));
     float acc[kDpl];
 #pragma unroll
     for (int e = 0; e < kDpl; ++e) acc[e] = 0.f;
     float lsum = 0.f;
-    for (int p = 0; p < np; ++p) {
-        float mp, lp;
-        if (p < kCache) {
+    for (int p0 = 0; p0 < np; p0 += kAhead) {
+        if (kAhead == 1 || p0 > 0) load_o(p0);
 #pragma unroll
-            for (int k = 0; k < kCache; ++k)
-                if (k == p) { mp = mc[k]; lp = lc[k]; }
-        } else {
-            mp = __ldcg(m + int64_t(p) * pstride);
-            lp = __ldcg(l + int64_t(p) * pstride);
-        }
-        const float w = mp != -INFINITY ? ex2(mp - M) : 0.f;
-        lsum += lp * w;
-        const float4* src = reinterpret_cast<const float4*>(o + int64_t(p) * pstride * D);
+        for (int a = 0; a < kAhead; ++a) {
+            const int p = p0 + a;
+            if (p >= np) break;
+            float mp = 0.f, lp = 0.f;
+            if (p < kCache) {
 #pragma unroll
-        for (int c = 0; c < kDpl / 4; ++c) {
-            const float4 v = __ldcg(src + c);
-            acc[4 * c + 0] += v.x * w;
-            acc[4 * c + 1] += v.y * w;
-            acc[4 * c + 2] += v.z * w;
-            acc[4 * c + 3] += v.w * w;
+                for (int k = 0; k < kCache; ++k)
+                    if (k == p) { mp = mc[k]; lp = lc[k]; }
+            } else {
+                mp = __ldcg(m + int64_t(p) * pstride);
+                lp = __ldcg(l + int64_t(p) * pstride);
+            }
+            const float w = mp != -INFINITY ? ex2(mp - M) : 0.f;
+            lsum += lp * w;
+#pragma unroll
+            for (int c = 0; c < kV; ++c) {
+                acc[4 * c + 0] += v[a][c].x * w;
+                acc[4 * c + 1] += v[a][c].y * w;
+                acc[4 * c + 2] += v[a][c].z * w;
+                acc[4 * c + 3] += v[a][c].w * w;
+            }
         }
     }
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;      // a query that saw no key: 0
@@ -454,6 +501,47 @@ __device__ __forceinline__ void merge_rows(T* __restrict__ out, const float* ws_
                             E::pack2(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv),
                             E::pack2(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv),
                             E::pack2(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv));
+}
+
+// Tail merge of a two-piece stream's GH rows (one warp): pieces p0, p1 in
+// shared memory as [8][D] of o, then m[8], l[8].  The arithmetic and piece
+// order are merge_rows', so either path gives the same bits.
+template <typename T, int D>
+__device__ __forceinline__ void tail_merge_rows(T* __restrict__ out, const float* p0,
+                                             const float* p1, int GH, int lane) {
+    using E = Elem<T>;
+    constexpr int kDpl = D / 32;         // values per lane
+    for (int k = 0; k < GH; ++k) {
+        float v0[kDpl], v1[kDpl];
+#pragma unroll
+        for (int e = 0; e < kDpl; ++e) {
+            v0[e] = p0[k * D + lane * kDpl + e];
+            v1[e] = p1[k * D + lane * kDpl + e];
+        }
+        const float m0 = p0[kHeadsN * D + k], l0 = p0[kHeadsN * D + kHeadsN + k];
+        const float m1 = p1[kHeadsN * D + k], l1 = p1[kHeadsN * D + kHeadsN + k];
+        const float M = fmaxf(fmaxf(-INFINITY, m0), m1);
+        float acc[kDpl];
+#pragma unroll
+        for (int e = 0; e < kDpl; ++e) acc[e] = 0.f;
+        float lsum = 0.f;
+        const float w0 = m0 != -INFINITY ? ex2(m0 - M) : 0.f;
+        lsum += l0 * w0;
+#pragma unroll
+        for (int e = 0; e < kDpl; ++e) acc[e] += v0[e] * w0;
+        const float w1 = m1 != -INFINITY ? ex2(m1 - M) : 0.f;
+        lsum += l1 * w1;
+#pragma unroll
+        for (int e = 0; e < kDpl; ++e) acc[e] += v1[e] * w1;
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;      // a query that saw no key: 0
+        T* orow = out + k * D + lane * kDpl;
+        if constexpr (kDpl == 4) {
+            *reinterpret_cast<uint2*>(orow) = make_uint2(E::pack2(acc[0] * inv, acc[1] * inv),
+                                                         E::pack2(acc[2] * inv, acc[3] * inv));
+        } else {
+            *reinterpret_cast<uint32_t*>(orow) = E::pack2(acc[0] * inv, acc[1] * inv);
+        }
+    }
 }
 
 // Rows of empty contexts get zeros (no stream covers them); contexts outside
@@ -581,8 +669,13 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     float* xchg = reinterpret_cast<float*>(smem + L::kX);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
     uint64_t* empty = full + kStages;
+    // tail merge: the producer's decision (tail_flag) is ready / warp 0's own
+    // piece is in the exchange buffer
+    uint64_t* tail_ready = full + 2 * kStages;
+    uint64_t* tail_own = tail_ready + 1;
     volatile int32_t* abort_flag = reinterpret_cast<int32_t*>(smem + L::kMisc);
     volatile int32_t* issued = reinterpret_cast<int32_t*>(smem + L::kMisc + 4);
+    volatile int32_t* tail_flag = reinterpret_cast<int32_t*>(smem + L::kMisc + 12);
 
     const int G = H / Hk;
     const int groups = G / GH;
@@ -596,6 +689,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
+        mbar_init(tail_ready, 1);
+        mbar_init(tail_own, 1);
         *abort_flag = 0;
         *issued = 0;
         fence_mbar_init();
@@ -644,6 +739,9 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         };
         Walk wn = w;                                       // one stage ahead of w
         int blk_cur = stage_blk(w);
+        // the stream of the last stage issued (tail merge)
+        int tl_s = -1, tl_u = 0, tl_L = 0;
+        long tl_start = 0;
         // Launched as a dependent of the store grid, the CTA got here while
         // the store may still run: wait for its writes before the first K/V
         // copy (returns at once for an ordinary launch).
@@ -692,14 +790,91 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
             }
             if (lane == 0) *issued = int(gs + 1);
+            tl_s = w.s;
+            tl_u = w.u;
+            tl_L = w.L;
+            tl_start = w.start;
             w = wn;
             blk_cur = blk_next;
+        }
+        // ---- tail merge (one query per sequence).  The range's last stream
+        // usually goes on in the next CTA's range, whose first piece was
+        // counted long ago.  If so (two pieces, the other one counted), this
+        // warp loads the other piece now, while the consumers finish theirs;
+        // warp 0 then hands its piece over in shared memory instead of
+        // publishing it, and this warp writes the merged rows (same arithmetic
+        // and piece order as merge_rows).
+        [[maybe_unused]] float* tl = reinterpret_cast<float*>(smem + L::kTl);
+        [[maybe_unused]] int t_seg = 0, t_h0 = 0;
+        int tail = 0;
+        if constexpr (!kMQ) {
+            // two pieces: the stream starts in this range and ends in the
+            // next one (this is piece 0), or starts in the previous range and
+            // ends in this one (piece 1); comparisons, no 64-bit division
+            const long r0 = long(w.bi) * w.per_cta, s_end = tl_start + tl_L;
+            const bool starts_here = tl_start >= r0;
+            const bool starts_prev = !starts_here && tl_start >= r0 - w.per_cta;
+            const bool ends_here = s_end <= w.end;
+            const bool ends_next = !ends_here && s_end <= w.end + w.per_cta;
+            const bool two = (starts_here && ends_next) || (starts_prev && ends_here);
+            if (tl_s >= 0 && two && *abort_flag == 0) {
+                t_seg = starts_here ? 0 : 1;
+                const unsigned long long c =
+                    ld_acquire_u64(ws_cnt + (int64_t)tl_s * units + tl_u);
+                tail = __all_sync(0xffffffffu,
+                                  (c >> kCountBits) == tag && int(c & kCountMask) == 1) ? 1 : 0;
+            }
+            // warp 0 waits for this decision at the end of its last piece
+            if (lane == 0) *tail_flag = tail;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tail_ready);
+            if (tail) {
+                t_h0 = (tl_u / groups) * G + (tl_u % groups) * GH;
+                // into shared memory by asynchronous copies, all in flight at
+                // once (lane: D / 32 values of each row; lanes < GH: m and l
+                // of row lane); ordered after the acquire load above
+                for (int k = 0; k < GH; ++k) {
+                    const int64_t r = ((int64_t)tl_s * H + t_h0 + k) * max_segs + (1 - t_seg);
+                    cp_async<D / 8>(tl + k * D + lane * (D / 32), ws_o + r * D + lane * (D / 32));
+                }
+                if (lane < GH) {
+                    const int64_t r = ((int64_t)tl_s * H + t_h0 + lane) * max_segs + (1 - t_seg);
+                    cp_async<4>(tl + kHeadsN * D + lane, ws_m + r);
+                    cp_async<4>(tl + kHeadsN * D + kHeadsN + lane, ws_l + r);
+                }
+            }
         }
         // all loads are issued: the producer has time for the empty rows
         zero_empty_rows<T, D>(out, context_lens, nseq, H, nq, cap, dev_err, lane);
         if constexpr (kFork)
             check_groups(fk, B, block_tables, max_blocks_per_seq, context_lens, cap, S, dev_err,
                          lane);
+        if constexpr (!kMQ) {
+            if (tail) {
+                // warp 0's piece: rows [k][D] of o, then m[8], l[8] (exchange buffer)
+                bool got = false;
+                const uint64_t t0 = globaltimer();
+                for (uint32_t i = 0;; ++i) {
+                    if (mbar_try_wait(tail_own, 0)) { got = true; break; }
+                    if (*abort_flag != 0) break;
+                    if ((i & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) break;
+                }
+                got = __all_sync(0xffffffffu, got);
+                if (!got) {
+                    if (lane == 0 && *abort_flag == 0) {
+                        flag_error(dev_err, PD_DEVERR_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    return;
+                }
+                cp_async_wait_all();
+                __syncwarp();                    // m, l of the other piece, from other lanes
+                tail_merge_rows<T, D>(out + ((int64_t)tl_s * H + t_h0) * D, t_seg == 0 ? xchg : tl,
+                                      t_seg == 0 ? tl : xchg, GH, lane);
+                // the stream is complete: its counter back to zero
+                if (lane == 0) st_relaxed_u64(ws_cnt + (int64_t)tl_s * units + tl_u, 0ull);
+            }
+        }
         return;
     }
 
@@ -1285,7 +1460,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         auto merge_tile = [&]() {
             const int n = col0 + (lane >> 2);
             const int64_t orow = col_row(w, h0, n);
-            merge_rows<T, D>(out, ws_o, ws_m, ws_l, orow, orow < 0 ? 0 : ws_index(orow, n, 0),
+            merge_rows<T, D, kMQ ? 1 : 2>(out, ws_o, ws_m, ws_l, orow, orow < 0 ? 0 : ws_index(orow, n, 0),
                              kFork ? cstride : 1, nseg, lane);
         };
         // the arrival counter is read now, so that its latency overlaps the
@@ -1294,6 +1469,20 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         if (nseg > 1 && warp == 0 && lane == 0)
             cnt0 = *reinterpret_cast<volatile unsigned long long*>(ws_cnt + (int64_t)w.s * units +
                                                                     w.u);
+        // The range's final piece, split in two: the producer warp has decided
+        // whether it merges the stream (tail merge; its decision follows its
+        // last copy, so warp 0 seldom waits here).
+        bool handoff = false;
+        if constexpr (!kMQ) {
+            if (warp == 0 && nseg == 2 && long(piece_stages) == left) {
+                const bool ok = __all_sync(0xffffffffu, mbar_wait(tail_ready, 0));
+                if (!ok && lane == 0) {
+                    flag_error(dev_err, PD_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                handoff = ok && *tail_flag != 0;
+            }
+        }
         if (leader && tile_live) {
             if constexpr (kF8) {
                 const float vs = __ldg(v_scale + kvh);
@@ -1307,11 +1496,33 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             const int ha = 2 * (lane & 3);
             const int d0 = kNative ? 2 * (lane >> 2) : (lane >> 2);
             constexpr int kDd = kNative ? 1 : 8;     // dim step of registers 2, 3
+            if (handoff) {
+                // this piece goes to the producer warp through the exchange
+                // buffer (every warp has read it): rows [c][D] of o, then
+                // m[8], l[8]
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c = ha + h;
+                    if (c >= GH) continue;
+                    float* xr = xchg + c * D + d0;
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        xr[16 * mt] = o[mt][h];
+                        xr[16 * mt + kDd] = o[mt][2 + h];
+                    }
+                    if (d0 == 0) {
+                        xchg[kHeadsN * D + c] = m_run[h];
+                        xchg[kHeadsN * D + kHeadsN + c] = l_run[h];
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tail_own);
+            }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int c = col0 + ha + h;
                 const int64_t row = col_row(w, h0, c);
-                if (row < 0) continue;
+                if (row < 0 || handoff) continue;
                 if (nseg == 1) {
                     // the whole stream was here: final, normalised output
                     const float inv = kMQ && l_run[h] == 0.f ? 0.f : 1.f / l_run[h];
@@ -1335,7 +1546,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                     }
                 }
             }
-            if (nseg > 1 && ctiles == 1) {
+            if (!handoff && nseg > 1 && ctiles == 1) {
                 // publish this piece, count it; the last of the stream's
                 // pieces to arrive merges them all
                 __threadfence();

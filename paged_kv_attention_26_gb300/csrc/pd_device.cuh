@@ -25,8 +25,30 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
+// Acquire 64-bit global load and relaxed store, GPU scope.
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Asynchronous global -> shared copies of 4, 8 or 16 bytes (no registers held
+// while in flight); cp_async_wait_all waits for this thread's copies.
+template <int N>
+__device__ __forceinline__ void cp_async(void* dst, const void* src) {
+    static_assert(N == 4 || N == 8 || N == 16, "cp.async sizes");
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ---- mbarrier ---------------------------------------------------------------
