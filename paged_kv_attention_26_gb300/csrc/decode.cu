@@ -80,7 +80,9 @@ constexpr int kSegTokens = kMinStagesPerCta * 64;   // bounds pieces per stream
 constexpr int kStageTokens = 64;    // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;   // 16 tokens of each stage per warp
 constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kPublisherWarp = kConsumerWarps + 1;   // one query per sequence only
+constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;     // verify, shared prefix
+constexpr int kDecodeThreadsPub = (kConsumerWarps + 2) * 32;  // single-query decode
 constexpr int kHeadsN = 8;          // MMA N: query heads per CTA, padded
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows > 2^8
 constexpr float kLog2e = 1.4426950408889634f;
@@ -106,11 +108,14 @@ struct DecodeSmem {
     static constexpr int kK8 = kV + kTiles16 * kTile;
     static constexpr int kV8 = kK8 + (kF8 ? kRing * kTile8 : 0);
     static constexpr int kX = kV8 + (kF8 ? kRing * kTile8 : 0);    // merge exchange [2][32][kFrag]
-    static constexpr int kBar = kX + 2 * kFrag * 32 * 4;
-    // ring barriers (full, empty), then the two tail-merge barriers
-    static constexpr int kMisc = kBar + (2 * kRing + 2) * 8;   // abort flag, issued count, flags
-    // tail merge: the other piece of the range's last stream, [8][D] of o,
-    // then m[8], l[8]
+    // a finished piece's stream, unit, piece count and index, and whether it
+    // is the range's last (single-query decode: read by the publisher warp)
+    static constexpr int kMeta = kX + 2 * kFrag * 32 * 4;
+    static constexpr int kBar = kMeta + 32;
+    // ring barriers (full, empty), then the tail-merge and hand-off barriers
+    static constexpr int kMisc = kBar + (2 * kRing + 4) * 8;   // abort flag, issued count, flags
+    // tail merge: the other piece of the range's last stream, [8 rows][D] of
+    // o, then m[8], l[8]
     static constexpr int kTl = kMisc + 16;
     static constexpr int kBytes = kTl + (kHeadsN * D + 2 * kHeadsN) * 4;
     static constexpr int kAlloc = kBytes + 1024;           // base aligned to 1 KB in-kernel
@@ -503,44 +508,32 @@ __device__ __forceinline__ void merge_rows(T* __restrict__ out, const float* ws_
                             E::pack2(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv));
 }
 
-// Tail merge of a two-piece stream's GH rows (one warp): pieces p0, p1 in
-// shared memory as [8][D] of o, then m[8], l[8].  The arithmetic and piece
-// order are merge_rows', so either path gives the same bits.
-template <typename T, int D>
-__device__ __forceinline__ void tail_merge_rows(T* __restrict__ out, const float* p0,
-                                             const float* p1, int GH, int lane) {
-    using E = Elem<T>;
-    constexpr int kDpl = D / 32;         // values per lane
-    for (int k = 0; k < GH; ++k) {
-        float v0[kDpl], v1[kDpl];
+// Combine a lane's partial (o fragments, and m, l of its two columns) with
+// another share of the same columns stored as a lane record (o fragments,
+// then m[2], l[2]): M = max(m, m'); o = o 2^(m - M) + o' 2^(m' - M), and l
+// likewise.
+template <int KS>
+__device__ __forceinline__ void frag_combine(float (&o)[KS][4], float (&m_run)[2],
+                                             float (&l_run)[2], const float4* x) {
+    const float4 ml = x[KS];
+    const float mo2[2] = {ml.x, ml.y}, lo2[2] = {ml.z, ml.w};
+    float c_mine[2], c_other[2];
 #pragma unroll
-        for (int e = 0; e < kDpl; ++e) {
-            v0[e] = p0[k * D + lane * kDpl + e];
-            v1[e] = p1[k * D + lane * kDpl + e];
-        }
-        const float m0 = p0[kHeadsN * D + k], l0 = p0[kHeadsN * D + kHeadsN + k];
-        const float m1 = p1[kHeadsN * D + k], l1 = p1[kHeadsN * D + kHeadsN + k];
-        const float M = fmaxf(fmaxf(-INFINITY, m0), m1);
-        float acc[kDpl];
+    for (int h = 0; h < 2; ++h) {
+        const float mo = mo2[h], lo = lo2[h];
+        const float M = fmaxf(m_run[h], mo);
+        c_mine[h] = m_run[h] == -INFINITY ? 0.f : ex2(m_run[h] - M);
+        c_other[h] = mo == -INFINITY ? 0.f : ex2(mo - M);
+        l_run[h] = l_run[h] * c_mine[h] + lo * c_other[h];
+        m_run[h] = M;
+    }
 #pragma unroll
-        for (int e = 0; e < kDpl; ++e) acc[e] = 0.f;
-        float lsum = 0.f;
-        const float w0 = m0 != -INFINITY ? ex2(m0 - M) : 0.f;
-        lsum += l0 * w0;
-#pragma unroll
-        for (int e = 0; e < kDpl; ++e) acc[e] += v0[e] * w0;
-        const float w1 = m1 != -INFINITY ? ex2(m1 - M) : 0.f;
-        lsum += l1 * w1;
-#pragma unroll
-        for (int e = 0; e < kDpl; ++e) acc[e] += v1[e] * w1;
-        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;      // a query that saw no key: 0
-        T* orow = out + k * D + lane * kDpl;
-        if constexpr (kDpl == 4) {
-            *reinterpret_cast<uint2*>(orow) = make_uint2(E::pack2(acc[0] * inv, acc[1] * inv),
-                                                         E::pack2(acc[2] * inv, acc[3] * inv));
-        } else {
-            *reinterpret_cast<uint32_t*>(orow) = E::pack2(acc[0] * inv, acc[1] * inv);
-        }
+    for (int mt = 0; mt < KS; ++mt) {
+        const float4 v = x[mt];
+        o[mt][0] = o[mt][0] * c_mine[0] + v.x * c_other[0];
+        o[mt][1] = o[mt][1] * c_mine[1] + v.y * c_other[1];
+        o[mt][2] = o[mt][2] * c_mine[0] + v.z * c_other[0];
+        o[mt][3] = o[mt][3] * c_mine[1] + v.w * c_other[1];
     }
 }
 
@@ -643,7 +636,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // (member, head) pairs, member-major (member j of the group: columns
 // j GH .. j GH + GH - 1), so a member's tail stage involves one tile.
 template <typename T, int D, bool kF8, bool kMQ, bool kFork>
-__global__ void __launch_bounds__(kDecodeThreads, 2)
+__global__ void __launch_bounds__(kMQ ? kDecodeThreads : kDecodeThreadsPub, 2)
 paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, T* __restrict__ out,
                           const T* __restrict__ q, const int32_t* __restrict__ block_tables,
@@ -669,10 +662,14 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     float* xchg = reinterpret_cast<float*>(smem + L::kX);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);
     uint64_t* empty = full + kStages;
-    // tail merge: the producer's decision (tail_flag) is ready / warp 0's own
-    // piece is in the exchange buffer
+    // tail merge: the producer's decision (tail_flag) is made / the other
+    // piece is in shared memory
     uint64_t* tail_ready = full + 2 * kStages;
-    uint64_t* tail_own = tail_ready + 1;
+    uint64_t* tail_data = tail_ready + 1;
+    // single-query decode: warps 0 and 1 have handed a piece over / the
+    // publisher warp has taken it
+    uint64_t* pub_full = tail_ready + 2;
+    uint64_t* pub_free = tail_ready + 3;
     volatile int32_t* abort_flag = reinterpret_cast<int32_t*>(smem + L::kMisc);
     volatile int32_t* issued = reinterpret_cast<int32_t*>(smem + L::kMisc + 4);
     volatile int32_t* tail_flag = reinterpret_cast<int32_t*>(smem + L::kMisc + 12);
@@ -690,7 +687,9 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             mbar_init(&empty[s], kConsumerWarps);
         }
         mbar_init(tail_ready, 1);
-        mbar_init(tail_own, 1);
+        mbar_init(tail_data, 1);
+        mbar_init(pub_full, 2);
+        mbar_init(pub_free, 1);
         *abort_flag = 0;
         *issued = 0;
         fence_mbar_init();
@@ -742,6 +741,18 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         // the stream of the last stage issued (tail merge)
         int tl_s = -1, tl_u = 0, tl_L = 0;
         long tl_start = 0;
+        // The first block ids of a stream come from a table row no other
+        // stage has touched, a full memory round trip that the one-stage
+        // lookahead does not cover: while a stream is walked, the next
+        // stream's first table line is fetched into L1 ahead of time.
+        auto prefetch_next_row = [&](int s_cur) {
+            if constexpr (!kFork) {
+                if (lane == 0 && s_cur + 1 < B)
+                    asm volatile("prefetch.global.L1 [%0];" ::"l"(
+                        block_tables + (int64_t)(s_cur + 1) * max_blocks_per_seq));
+            }
+        };
+        prefetch_next_row(w.s);
         // Launched as a dependent of the store grid, the CTA got here while
         // the store may still run: wait for its writes before the first K/V
         // copy (returns at once for an ordinary launch).
@@ -760,7 +771,9 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 break;
             }
             // start loading the next stage's block ids
+            const int s_before = wn.s;
             walk_step<kFork>(wn, context_lens, B, cap, S, fk);
+            if (wn.s != s_before) prefetch_next_row(wn.s);
             const int blk_next = wn.pos < wn.end ? stage_blk(wn) : -2;
             const int kvh = w.u / groups;
             int row = -1;
@@ -800,12 +813,10 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         // ---- tail merge (one query per sequence).  The range's last stream
         // usually goes on in the next CTA's range, whose first piece was
         // counted long ago.  If so (two pieces, the other one counted), this
-        // warp loads the other piece now, while the consumers finish theirs;
-        // warp 0 then hands its piece over in shared memory instead of
-        // publishing it, and this warp writes the merged rows (same arithmetic
-        // and piece order as merge_rows).
+        // warp loads the other piece into shared memory now, while the
+        // consumers finish theirs, and the publisher warp merges the stream
+        // from there instead of publishing the last piece.
         [[maybe_unused]] float* tl = reinterpret_cast<float*>(smem + L::kTl);
-        [[maybe_unused]] int t_seg = 0, t_h0 = 0;
         int tail = 0;
         if constexpr (!kMQ) {
             // two pieces: the stream starts in this range and ends in the
@@ -817,19 +828,19 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             const bool ends_here = s_end <= w.end;
             const bool ends_next = !ends_here && s_end <= w.end + w.per_cta;
             const bool two = (starts_here && ends_next) || (starts_prev && ends_here);
+            const int t_seg = starts_here ? 0 : 1;
             if (tl_s >= 0 && two && *abort_flag == 0) {
-                t_seg = starts_here ? 0 : 1;
                 const unsigned long long c =
                     ld_acquire_u64(ws_cnt + (int64_t)tl_s * units + tl_u);
                 tail = __all_sync(0xffffffffu,
                                   (c >> kCountBits) == tag && int(c & kCountMask) == 1) ? 1 : 0;
             }
-            // warp 0 waits for this decision at the end of its last piece
+            // the publisher waits for this decision with the last piece
             if (lane == 0) *tail_flag = tail;
             __syncwarp();
             if (lane == 0) mbar_arrive(tail_ready);
             if (tail) {
-                t_h0 = (tl_u / groups) * G + (tl_u % groups) * GH;
+                const int t_h0 = (tl_u / groups) * G + (tl_u % groups) * GH;
                 // into shared memory by asynchronous copies, all in flight at
                 // once (lane: D / 32 values of each row; lanes < GH: m and l
                 // of row lane); ordered after the acquire load above
@@ -851,28 +862,173 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                          lane);
         if constexpr (!kMQ) {
             if (tail) {
-                // warp 0's piece: rows [k][D] of o, then m[8], l[8] (exchange buffer)
+                cp_async_wait_all();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tail_data);     // the other piece has landed
+            }
+        }
+        return;
+    }
+
+    if (warp == kPublisherWarp) {
+        // ---------------- publisher warp (one query per sequence) ----------------
+        // Warps 0 and 1 hand each finished piece over as two partial results
+        // in the exchange buffer (the four consumer warps' shares combined in
+        // pairs).  This warp combines the two and does what follows, so that
+        // the consumers go straight on to the next piece: the normalised rows
+        // of a whole stream; or the piece's partial, its fence and arrival
+        // count, and the stream's merge when the piece completes it; or, for
+        // the range's last piece when the producer has fetched the stream's
+        // other piece, the merged rows (the tail merge, with merge_rows'
+        // arithmetic and piece order).
+        if constexpr (!kMQ) {
+            constexpr int KS = D / 16;
+            const int32_t* meta = reinterpret_cast<const int32_t*>(smem + L::kMeta);
+            const float* tl = reinterpret_cast<const float*>(smem + L::kTl);
+            // lane: columns ha, ha + 1; dims 16mt + d0 and + kDd (the
+            // consumers' fragment layout; native FP8: the m-tile rows g, g + 8
+            // are dims 2g, 2g + 1)
+            const int ha = 2 * (lane & 3);
+            const int d0 = kNative ? 2 * (lane >> 2) : (lane >> 2);
+            constexpr int kDd = kNative ? 1 : 8;
+            // bounded wait on a barrier phase that also gives up on an abort
+            auto wait_phase = [&](uint64_t* bar, uint32_t parity) -> bool {
                 bool got = false;
                 const uint64_t t0 = globaltimer();
                 for (uint32_t i = 0;; ++i) {
-                    if (mbar_try_wait(tail_own, 0)) { got = true; break; }
+                    if (mbar_try_wait(bar, parity)) { got = true; break; }
                     if (*abort_flag != 0) break;
                     if ((i & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) break;
                 }
                 got = __all_sync(0xffffffffu, got);
-                if (!got) {
-                    if (lane == 0 && *abort_flag == 0) {
-                        flag_error(dev_err, PD_DEVERR_TIMEOUT);
-                        *abort_flag = 1;
-                    }
-                    return;
+                if (!got && lane == 0 && *abort_flag == 0) {
+                    flag_error(dev_err, PD_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
                 }
-                cp_async_wait_all();
-                __syncwarp();                    // m, l of the other piece, from other lanes
-                tail_merge_rows<T, D>(out + ((int64_t)tl_s * H + t_h0) * D, t_seg == 0 ? xchg : tl,
-                                      t_seg == 0 ? tl : xchg, GH, lane);
-                // the stream is complete: its counter back to zero
-                if (lane == 0) st_relaxed_u64(ws_cnt + (int64_t)tl_s * units + tl_u, 0ull);
+                return got;
+            };
+            for (uint32_t job = 0;; ++job) {
+                if (!wait_phase(pub_full, job & 1)) return;
+                const int js = meta[0], ju = meta[1], jn = meta[2], jseg = meta[3];
+                const bool jfinal = meta[4] != 0;
+                float o[KS][4], m_run[2], l_run[2];
+                {
+                    const float4* x = reinterpret_cast<const float4*>(xchg + lane * L::kFrag);
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        const float4 v = x[mt];
+                        o[mt][0] = v.x; o[mt][1] = v.y; o[mt][2] = v.z; o[mt][3] = v.w;
+                    }
+                    const float4 ml = x[KS];
+                    m_run[0] = ml.x; m_run[1] = ml.y; l_run[0] = ml.z; l_run[1] = ml.w;
+                }
+                frag_combine<KS>(o, m_run, l_run, reinterpret_cast<const float4*>(
+                                                      xchg + (32 + lane) * L::kFrag));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pub_free);    // the buffer is free again
+                const int jkvh = ju / groups;
+                if constexpr (kF8) {
+                    const float vs = __ldg(v_scale + jkvh);
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) o[mt][e] *= vs;
+                }
+                const int jh0 = jkvh * G + (ju % groups) * GH;
+                const int64_t row0 = (int64_t)js * H + jh0;      // one query per sequence
+                unsigned long long* cnt = ws_cnt + (int64_t)js * units + ju;
+                bool merged = false;
+                if (jfinal && jn == 2) {
+                    // the producer decided after its last copy (long before
+                    // this piece ended, as a rule)
+                    if (!wait_phase(tail_ready, 0)) return;
+                    if (*tail_flag != 0) {
+                        if (!wait_phase(tail_data, 0)) return;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int c = ha + h;
+                            if (c >= GH) continue;
+                            const float mo = tl[kHeadsN * D + c], lo = tl[kHeadsN * D + kHeadsN + c];
+                            // pieces in order: 0, then 1 (this one is jseg)
+                            const float m0 = jseg == 0 ? m_run[h] : mo, m1 = jseg == 0 ? mo : m_run[h];
+                            const float l0 = jseg == 0 ? l_run[h] : lo, l1 = jseg == 0 ? lo : l_run[h];
+                            const float M = fmaxf(fmaxf(-INFINITY, m0), m1);
+                            const float w0 = m0 != -INFINITY ? ex2(m0 - M) : 0.f;
+                            const float w1 = m1 != -INFINITY ? ex2(m1 - M) : 0.f;
+                            float lsum = 0.f;
+                            lsum += l0 * w0;
+                            lsum += l1 * w1;
+                            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+                            T* orow = out + (row0 + c) * D;
+                            const float* trow = tl + c * D;
+#pragma unroll
+                            for (int mt = 0; mt < KS; ++mt) {
+#pragma unroll
+                                for (int r = 0; r < 2; ++r) {
+                                    const int d = 16 * mt + d0 + r * kDd;
+                                    const float vm = o[mt][h + 2 * r], vt = trow[d];
+                                    float acc = 0.f;
+                                    acc += (jseg == 0 ? vm : vt) * w0;
+                                    acc += (jseg == 0 ? vt : vm) * w1;
+                                    orow[d] = T(acc * inv);
+                                }
+                            }
+                        }
+                        // the stream is complete: its counter back to zero
+                        if (lane == 0) st_relaxed_u64(cnt, 0ull);
+                        merged = true;
+                    }
+                }
+                if (!merged) {
+                    // read now, so that its latency overlaps the writes and fence
+                    unsigned long long c0 = 0;
+                    if (jn > 1 && lane == 0) c0 = *reinterpret_cast<volatile unsigned long long*>(cnt);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int c = ha + h;
+                        if (c >= GH) continue;
+                        const int64_t row = row0 + c;
+                        if (jn == 1) {
+                            // the whole stream was in this CTA: final, normalised rows
+                            const float inv = 1.f / l_run[h];
+                            T* orow = out + row * D + d0;
+#pragma unroll
+                            for (int mt = 0; mt < KS; ++mt) {
+                                orow[16 * mt] = T(o[mt][h] * inv);
+                                orow[16 * mt + kDd] = T(o[mt][2 + h] * inv);
+                            }
+                        } else {
+                            const int64_t r = row * max_segs + jseg;
+                            float* wrow = ws_o + r * D + d0;
+#pragma unroll
+                            for (int mt = 0; mt < KS; ++mt) {
+                                wrow[16 * mt] = o[mt][h];
+                                wrow[16 * mt + kDd] = o[mt][2 + h];
+                            }
+                            if (d0 == 0) {
+                                ws_m[r] = m_run[h];
+                                ws_l[r] = l_run[h];
+                            }
+                        }
+                    }
+                    if (jn > 1) {
+                        // publish the piece, count it; the last of the stream's
+                        // pieces to arrive merges them all
+                        __threadfence();
+                        __syncwarp();
+                        uint32_t last = 0;
+                        if (lane == 0) last = arrive_piece(cnt, tag, jn, c0) ? 1u : 0u;
+                        last = __shfl_sync(0xffffffffu, last, 0);
+                        if (last) {
+                            __threadfence();
+                            const int n = lane >> 2;
+                            const int64_t orow = n < GH ? row0 + n : -1;
+                            merge_rows<T, D, 2>(out, ws_o, ws_m, ws_l, orow,
+                                                orow < 0 ? 0 : orow * max_segs, 1, jn, lane);
+                        }
+                    }
+                }
+                if (jfinal) return;
             }
         }
         return;
@@ -912,6 +1068,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         }
     };
 
+    uint32_t npub = 0;                           // pieces handed to the publisher warp
     while (w.pos < w.end) {
         // ---- one stream piece: stages [w.off, min(w.L, w.off + w.end - w.pos)) of (s, u)
         const int kvh = w.u / groups;
@@ -1403,179 +1560,148 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             x[KS] = make_float4(m_run[0], m_run[1], l_run[0], l_run[1]);
         };
         auto take = [&](int buf) {
-            const float4* x = reinterpret_cast<const float4*>(xchg + (buf * 32 + lane) * L::kFrag);
-            const float4 ml = x[KS];
-            const float mo2[2] = {ml.x, ml.y}, lo2[2] = {ml.z, ml.w};
-            float c_mine[2], c_other[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float mo = mo2[h], lo = lo2[h];
-                const float M = fmaxf(m_run[h], mo);
-                c_mine[h] = m_run[h] == -INFINITY ? 0.f : ex2(m_run[h] - M);
-                c_other[h] = mo == -INFINITY ? 0.f : ex2(mo - M);
-                l_run[h] = l_run[h] * c_mine[h] + lo * c_other[h];
-                m_run[h] = M;
-            }
-#pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                const float4 v = x[mt];
-                o[mt][0] = o[mt][0] * c_mine[0] + v.x * c_other[0];
-                o[mt][1] = o[mt][1] * c_mine[1] + v.y * c_other[1];
-                o[mt][2] = o[mt][2] * c_mine[0] + v.z * c_other[0];
-                o[mt][3] = o[mt][3] * c_mine[1] + v.w * c_other[1];
-            }
+            frag_combine<KS>(o, m_run, l_run, reinterpret_cast<const float4*>(
+                                                  xchg + (buf * 32 + lane) * L::kFrag));
         };
-        // one tile: warps 2, 3 hand over to 0, 1, then warp 1 to 0; two tiles:
-        // warp 1 hands over to 0 and warp 3 to 2 (same tile); four tiles: each
-        // warp holds its own columns whole
-        if (ctiles == 1) {
-            if (warp >= 2) put(warp - 2);
-            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-            if (warp < 2) take(warp);
-            if (warp == 1) {
-                __syncwarp();
-                put(1);                  // own partner slot, already read by this warp
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-            if (warp == 0) take(1);
-        } else if (ctiles == 2) {
-            if (warp & 1) put(warp >> 1);
-            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-            if (!(warp & 1)) take(warp >> 1);
-        }
-        // The exchange buffer has been read: the other warps go on to the next
-        // piece while the warp(s) holding the result write it, publish it and
-        // perhaps merge the stream. They fall behind by that much and catch up
-        // on stages already in the ring (consuming is faster than streaming).
-        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-        const bool leader = (warp % wpc) == 0;   // holds its tile's result
-        // workspace index of column c's partial for piece `p` of this stream:
-        // per output row (decode, verify), or compact per (unit, piece, column)
-        // in shared-prefix mode (piece k + c_first + p < n_groups + CTAs per unit)
-        auto ws_index = [&](int64_t row, int c, long p) -> int64_t {
-            if constexpr (kFork)
-                return ((int64_t)w.u * fk.ppu + w.s + c_first + p) * cstride + c;
-            return row * max_segs + p;
-        };
-        auto merge_tile = [&]() {
-            const int n = col0 + (lane >> 2);
-            const int64_t orow = col_row(w, h0, n);
-            merge_rows<T, D, kMQ ? 1 : 2>(out, ws_o, ws_m, ws_l, orow, orow < 0 ? 0 : ws_index(orow, n, 0),
-                             kFork ? cstride : 1, nseg, lane);
-        };
-        // the arrival counter is read now, so that its latency overlaps the
-        // piece's writes and fence; a value changed meanwhile costs one more CAS
-        unsigned long long cnt0 = 0;
-        if (nseg > 1 && warp == 0 && lane == 0)
-            cnt0 = *reinterpret_cast<volatile unsigned long long*>(ws_cnt + (int64_t)w.s * units +
-                                                                    w.u);
-        // The range's final piece, split in two: the producer warp has decided
-        // whether it merges the stream (tail merge; its decision follows its
-        // last copy, so warp 0 seldom waits here).
-        bool handoff = false;
         if constexpr (!kMQ) {
-            if (warp == 0 && nseg == 2 && long(piece_stages) == left) {
-                const bool ok = __all_sync(0xffffffffu, mbar_wait(tail_ready, 0));
+            // Warps 2, 3 hand their shares to 0, 1, which combine them and hand
+            // the two partials to the publisher warp with the piece's
+            // description; then all four go straight on.  The buffer is the
+            // only thing shared with the publisher, which frees it as soon as
+            // it has read it.
+            if (npub > 0 && warp >= 2) {
+                const bool ok = __all_sync(0xffffffffu, mbar_wait(pub_free, (npub - 1) & 1));
                 if (!ok && lane == 0) {
                     flag_error(dev_err, PD_DEVERR_TIMEOUT);
                     *abort_flag = 1;
                 }
-                handoff = ok && *tail_flag != 0;
             }
-        }
-        if (leader && tile_live) {
-            if constexpr (kF8) {
-                const float vs = __ldg(v_scale + kvh);
-#pragma unroll
-                for (int mt = 0; mt < KS; ++mt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) o[mt][e] *= vs;
+            if (warp >= 2) put(warp - 2);
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+            if (warp < 2) {
+                take(warp);
+                __syncwarp();
+                put(warp);                     // own slot, already read by this lane
+                if (warp == 0 && lane == 0) {
+                    int32_t* meta = reinterpret_cast<int32_t*>(smem + L::kMeta);
+                    meta[0] = w.s;
+                    meta[1] = w.u;
+                    meta[2] = nseg;
+                    meta[3] = seg;
+                    meta[4] = long(piece_stages) == left ? 1 : 0;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pub_full);
             }
-            // lane: columns ha, ha + 1; dims 16mt + lane/4 and + 8 (native FP8: the
-            // m-tile rows g, g + 8 are dims 2g, 2g + 1)
-            const int ha = 2 * (lane & 3);
-            const int d0 = kNative ? 2 * (lane >> 2) : (lane >> 2);
-            constexpr int kDd = kNative ? 1 : 8;     // dim step of registers 2, 3
-            if (handoff) {
-                // this piece goes to the producer warp through the exchange
-                // buffer (every warp has read it): rows [c][D] of o, then
-                // m[8], l[8]
+            ++npub;
+        } else {
+            // one tile: warps 2, 3 hand over to 0, 1, then warp 1 to 0; two
+            // tiles: warp 1 hands over to 0 and warp 3 to 2 (same tile); four
+            // tiles: each warp holds its own columns whole
+            if (ctiles == 1) {
+                if (warp >= 2) put(warp - 2);
+                asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+                if (warp < 2) take(warp);
+                if (warp == 1) {
+                    __syncwarp();
+                    put(1);                  // own partner slot, already read by this warp
+                }
+                asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+                if (warp == 0) take(1);
+            } else if (ctiles == 2) {
+                if (warp & 1) put(warp >> 1);
+                asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+                if (!(warp & 1)) take(warp >> 1);
+            }
+            // The exchange buffer has been read: the other warps go on to the
+            // next piece while the warp(s) holding the result write it, publish
+            // it and perhaps merge the stream. They fall behind by that much and
+            // catch up on stages already in the ring (consuming is faster than
+            // streaming).
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+            const bool leader = (warp % wpc) == 0;   // holds its tile's result
+            // workspace index of column c's partial for piece `p` of this
+            // stream: per output row (verify), or compact per (unit, piece,
+            // column) in shared-prefix mode (piece k + c_first + p < n_groups +
+            // CTAs per unit)
+            auto ws_index = [&](int64_t row, int c, long p) -> int64_t {
+                if constexpr (kFork)
+                    return ((int64_t)w.u * fk.ppu + w.s + c_first + p) * cstride + c;
+                return row * max_segs + p;
+            };
+            auto merge_tile = [&]() {               // verify, shared prefix
+                const int n = col0 + (lane >> 2);
+                const int64_t orow = col_row(w, h0, n);
+                merge_rows<T, D, 1>(out, ws_o, ws_m, ws_l, orow,
+                                    orow < 0 ? 0 : ws_index(orow, n, 0), kFork ? cstride : 1,
+                                    nseg, lane);
+            };
+            // the arrival counter is read now, so that its latency overlaps the
+            // piece's writes and fence; a value changed meanwhile costs one more CAS
+            unsigned long long* cnt = ws_cnt + (int64_t)w.s * units + w.u;
+            unsigned long long cnt0 = 0;
+            if (nseg > 1 && warp == 0 && lane == 0)
+                cnt0 = *reinterpret_cast<volatile unsigned long long*>(cnt);
+            if (leader && tile_live) {
+                // lane: columns ha, ha + 1; dims 16mt + lane/4 and + 8
+                const int ha = 2 * (lane & 3);
+                const int d0 = lane >> 2;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int c = ha + h;
-                    if (c >= GH) continue;
-                    float* xr = xchg + c * D + d0;
+                    const int c = col0 + ha + h;
+                    const int64_t row = col_row(w, h0, c);
+                    if (row < 0) continue;
+                    if (nseg == 1) {
+                        // the whole stream was here: final, normalised output
+                        // (0 for a query that saw no key)
+                        const float inv = l_run[h] == 0.f ? 0.f : 1.f / l_run[h];
+                        T* orow = out + row * D + d0;
 #pragma unroll
-                    for (int mt = 0; mt < KS; ++mt) {
-                        xr[16 * mt] = o[mt][h];
-                        xr[16 * mt + kDd] = o[mt][2 + h];
-                    }
-                    if (d0 == 0) {
-                        xchg[kHeadsN * D + c] = m_run[h];
-                        xchg[kHeadsN * D + kHeadsN + c] = l_run[h];
+                        for (int mt = 0; mt < KS; ++mt) {
+                            orow[16 * mt] = T(o[mt][h] * inv);
+                            orow[16 * mt + 8] = T(o[mt][2 + h] * inv);
+                        }
+                    } else {
+                        const int64_t r = ws_index(row, c, seg);
+                        float* wrow = ws_o + r * D + d0;
+#pragma unroll
+                        for (int mt = 0; mt < KS; ++mt) {
+                            wrow[16 * mt] = o[mt][h];
+                            wrow[16 * mt + 8] = o[mt][2 + h];
+                        }
+                        if (d0 == 0) {
+                            ws_m[r] = m_run[h];
+                            ws_l[r] = l_run[h];
+                        }
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tail_own);
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int c = col0 + ha + h;
-                const int64_t row = col_row(w, h0, c);
-                if (row < 0 || handoff) continue;
-                if (nseg == 1) {
-                    // the whole stream was here: final, normalised output
-                    const float inv = kMQ && l_run[h] == 0.f ? 0.f : 1.f / l_run[h];
-                    T* orow = out + row * D + d0;
-#pragma unroll
-                    for (int mt = 0; mt < KS; ++mt) {
-                        orow[16 * mt] = T(o[mt][h] * inv);
-                        orow[16 * mt + kDd] = T(o[mt][2 + h] * inv);
-                    }
-                } else {
-                    const int64_t r = ws_index(row, c, seg);
-                    float* wrow = ws_o + r * D + d0;
-#pragma unroll
-                    for (int mt = 0; mt < KS; ++mt) {
-                        wrow[16 * mt] = o[mt][h];
-                        wrow[16 * mt + kDd] = o[mt][2 + h];
-                    }
-                    if (d0 == 0) {
-                        ws_m[r] = m_run[h];
-                        ws_l[r] = l_run[h];
+                if (nseg > 1 && ctiles == 1) {
+                    // publish this piece, count it; the last of the stream's
+                    // pieces to arrive merges them all
+                    __threadfence();
+                    __syncwarp();
+                    uint32_t last = 0;
+                    if (lane == 0) last = arrive_piece(cnt, tag, nseg, cnt0) ? 1u : 0u;
+                    last = __shfl_sync(0xffffffffu, last, 0);
+                    if (last) {
+                        __threadfence();
+                        merge_tile();
                     }
                 }
             }
-            if (!handoff && nseg > 1 && ctiles == 1) {
-                // publish this piece, count it; the last of the stream's
-                // pieces to arrive merges them all
+            if (ctiles > 1 && nseg > 1 && leader) {
+                // every tile's leader (named barrier 2) has written its rows of
+                // the piece before it is counted; then each merges its own tile
+                // if the piece was the last
+                volatile int32_t* last_flag = reinterpret_cast<int32_t*>(smem + L::kMisc + 8);
                 __threadfence();
-                __syncwarp();
-                uint32_t last = 0;
-                if (lane == 0)
-                    last = arrive_piece(ws_cnt + (int64_t)w.s * units + w.u, tag, nseg, cnt0) ? 1u
-                                                                                              : 0u;
-                last = __shfl_sync(0xffffffffu, last, 0);
-                if (last) {
+                asm volatile("bar.sync 2, %0;" ::"r"(ctiles * 32) : "memory");
+                if (warp == 0 && lane == 0) *last_flag = arrive_piece(cnt, tag, nseg, cnt0) ? 1 : 0;
+                asm volatile("bar.sync 2, %0;" ::"r"(ctiles * 32) : "memory");
+                if (*last_flag && tile_live) {
                     __threadfence();
                     merge_tile();
                 }
-            }
-        }
-        if (ctiles > 1 && nseg > 1 && leader) {
-            // every tile's leader (named barrier 2) has written its rows of the
-            // piece before it is counted; then each merges its own tile if the
-            // piece was the last
-            volatile int32_t* last_flag = reinterpret_cast<int32_t*>(smem + L::kMisc + 8);
-            __threadfence();
-            asm volatile("bar.sync 2, %0;" ::"r"(ctiles * 32) : "memory");
-            if (warp == 0 && lane == 0)
-                *last_flag =
-                    arrive_piece(ws_cnt + (int64_t)w.s * units + w.u, tag, nseg, cnt0) ? 1 : 0;
-            asm volatile("bar.sync 2, %0;" ::"r"(ctiles * 32) : "memory");
-            if (*last_flag && tile_live) {
-                __threadfence();
-                merge_tile();
             }
         }
         w.off += piece_stages;
@@ -1730,7 +1856,7 @@ pd_status launch_decode_t(const DecodeArgs& a) {
     const int streams = kFork ? a.n_groups : a.B;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kDecodeThreads);
+    cfg.blockDim = dim3(kMQ ? kDecodeThreads : kDecodeThreadsPub);
     cfg.dynamicSmemBytes = Lt::kAlloc;
     cfg.stream = a.stream;
     cudaLaunchAttribute attr[1];
