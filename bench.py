@@ -394,10 +394,9 @@ def run_only_extras(args):
 def e2e_decode(pd, c, dev, args, step_bytes, world=1):
     """The same step through the public API from pinned host memory:
     ``DecodeStep`` (one pinned buffer holding q, the new K/V, slots, block
-    tables and context lengths; the tables and lengths copied in, q / K/V /
-    slots read and ``out`` written by the kernels over the host link,
-    synchronize), replayed from a CUDA graph; the same object run eagerly is
-    reported beside it."""
+    tables and context lengths, all read by the kernels over the host link,
+    and ``out`` written back the same way, synchronize), replayed from a CUDA
+    graph; the same object run eagerly is reported beside it."""
     import torch
     kc, vc = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -433,12 +432,11 @@ def e2e_decode(pd, c, dev, args, step_bytes, world=1):
     return {"value": round(whole_job_value(step_bytes, args.steps, total, world), 2), "unit": "GB/s",
             "ms_per_step": round(total / args.steps * 1e3, 4),
             "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world,
-            "path": "DecodeStep replayed from a CUDA graph: pd_copy_bytes of the block tables "
-                    "and context lengths from the pinned host buffer to the device, then "
-                    "pd_decode_step reading q, the new K/V and the slots from that pinned "
-                    "buffer and writing out into pinned host memory over the host link, "
-                    "synchronize; host wall clock per step, L2 flushed before each; the byte "
-                    "counts are every input and output byte that crosses the link",
+            "path": "DecodeStep replayed from a CUDA graph: pd_decode_step reading q, the "
+                    "new K/V, the slots, the block tables and the context lengths from one "
+                    "pinned host buffer and writing out into pinned host memory over the "
+                    "host link, synchronize; host wall clock per step, L2 flushed before "
+                    "each; the byte counts are every input and output byte of the step",
             "eager_value": round(whole_job_value(step_bytes, args.steps, eager, world), 2),
             "eager_ms_per_step": round(eager / args.steps * 1e3, 4)}
 

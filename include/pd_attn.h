@@ -422,14 +422,15 @@ PD_API pd_status pd_selftest_bounded_wait(int32_t* dev_err, uint64_t limit_ns,
  * All checks of both calls are made before anything is launched; on an error
  * nothing is launched.  T == 0 skips the store (the decode then launches
  * normally); B == 0 skips the decode.
- * Host-to-host steps: key, value, slot_mapping, q and out may be pinned host
- * memory mapped into the device's address space (cudaHostAlloc, or
- * cudaHostRegister with cudaHostRegisterMapped), given by its device
- * address (with unified addressing, the host address): the store and the
- * decode then read the step's inputs and write its result over the host
- * link, each byte once, with no separate copy.  block_tables and
- * context_lens are read by every CTA of the decode and belong in device
- * memory. */
+ * Host-to-host steps: key, value, slot_mapping, q, block_tables,
+ * context_lens and out may be pinned host memory mapped into the device's
+ * address space (cudaHostAlloc, or cudaHostRegister with
+ * cudaHostRegisterMapped), given by its device address (with unified
+ * addressing, the host address): the store and the decode then read the
+ * step's inputs and write its result over the host link, with no separate
+ * copy.  Each CTA of the decode reads the context lengths and its streams'
+ * table rows, so those cross the link more than once; measured on a batch
+ * of 64 that costs no more than copying them to the device first. */
 PD_API pd_status pd_decode_step(const void* key, const void* value,
                                 const int64_t* slot_mapping, int T,
                                 int64_t key_stride_tok, int64_t value_stride_tok,
