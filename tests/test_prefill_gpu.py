@@ -173,3 +173,37 @@ def test_repeat_runs_identical(cuda_lib):
         again, _, _ = _run(pd, m, kc=kc, vc=vc)
         assert torch.equal(first.view(torch.int16), again.view(torch.int16))
     assert_close(first.cpu(), _oracle(m), "repeat mix")
+
+
+def test_repeated_launches_and_graph_replays(cuda_lib):
+    """Many launches in a row, and a launch captured in a CUDA graph and
+    replayed, give the eager launch's bits every time, over a batch of many
+    short chunks (more tile pairs than SMs, some tile pairs empty)."""
+    pd = cuda_lib
+    dev = torch.device("cuda")
+    m = pd_inputs.mixed_case(96, [0, 40, 300, 900] * 12, [130, 64, 200, 65] * 12, [], 8, 2, 128,
+                             16, torch.bfloat16)
+    eager, kc, vc = _run(pd, m)
+    assert_close(eager.cpu(), _oracle(m), "many items")
+    q = m.q_prefill.to(dev)
+    cu = m.cu_q_lens.to(dev)
+    bt, cl = m.pool.block_tables[:m.Bp].to(dev), m.pool.context_lens[:m.Bp].to(dev)
+    err = device_err()
+    for _ in range(70):
+        out = torch.full_like(q, float("nan"))
+        pd.pd_paged_prefill_chunk(out, q, cu, m.max_q_len, kc, vc, bt, cl, m.scale, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    gout = torch.full_like(q, float("nan"))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        pd.pd_paged_prefill_chunk(gout, q, cu, m.max_q_len, kc, vc, bt, cl, m.scale, dev_err=err)
+    for _ in range(4):
+        gout.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(gout.view(torch.int16), eager.view(torch.int16))
+    assert err.item() == 0
