@@ -92,7 +92,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 // bytes); each consumer warp widens its own 16 rows of a stage (exactly) to
 // fp16 into one 16-bit tile of the same layout, releases the raw stage at
 // once, and runs the 16-bit code on fp16 operands.
-template <int D, bool kF8 = false>
+// kTc: shared-prefix mode, whose consumers run on the tensor cores: the
+// piece's q rows lie ahead of the ring, and there is no warp exchange.
+template <int D, bool kF8 = false, bool kTc = false>
 struct DecodeSmem {
     // FP8 with D = 128: consumers take MMA fragments straight from the raw
     // (128-byte swizzled) tiles, so there is no 16-bit tile and the ring is deeper.
@@ -103,21 +105,28 @@ struct DecodeSmem {
     static constexpr int kTile = (D / 64) * kAtom;     // one stage of K (or of V)
     static constexpr int kTile8 = kStageTokens * D;    // one FP8 stage of K (or of V)
     static constexpr int kFrag = (D / 16) * 4 + 4;     // per-lane merge record: o, m[2], l[2]
-    static constexpr int kK = 0;
+    // kTc: q of the piece's (up to 32) columns at offset 0, K-major in
+    // 64-value swizzle atoms of 32 rows (4 KB); the MMA reads 128 rows from
+    // each atom's start, so rows 32.. fall on the atoms and tiles behind it
+    // and are never used
+    static constexpr int kQAtom = 32 * 128;
+    static constexpr int kK = kTc ? (D / 64) * kQAtom : 0;
     static constexpr int kV = kK + kTiles16 * kTile;
     static constexpr int kK8 = kV + kTiles16 * kTile;
     static constexpr int kV8 = kK8 + (kF8 ? kRing * kTile8 : 0);
     static constexpr int kX = kV8 + (kF8 ? kRing * kTile8 : 0);    // merge exchange [2][32][kFrag]
     // a finished piece's stream, unit, piece count and index, and whether it
     // is the range's last (single-query decode: read by the publisher warp)
-    static constexpr int kMeta = kX + 2 * kFrag * 32 * 4;
+    static constexpr int kMeta = kX + (kTc ? 0 : 2 * kFrag * 32 * 4);
     static constexpr int kBar = kMeta + 32;
     // ring barriers (full, empty), then the tail-merge and hand-off barriers
-    static constexpr int kMisc = kBar + (2 * kRing + 4) * 8;   // abort flag, issued count, flags
+    // (kTc: the tensor-core and publisher hand-offs, fourteen)
+    // abort flag, issued count, flags (kTc: and the tensor-memory address)
+    static constexpr int kMisc = kBar + (2 * kRing + (kTc ? 14 : 4)) * 8;
     // tail merge: the other piece of the range's last stream, [8 rows][D] of
-    // o, then m[8], l[8]
-    static constexpr int kTl = kMisc + 16;
-    static constexpr int kBytes = kTl + (kHeadsN * D + 2 * kHeadsN) * 4;
+    // o, then m[8], l[8]; kTc: the walk position of the next piece instead
+    static constexpr int kTl = kMisc + (kTc ? 32 : 16);
+    static constexpr int kBytes = kTl + (kTc ? 128 : (kHeadsN * D + 2 * kHeadsN) * 4);
     static constexpr int kAlloc = kBytes + 1024;           // base aligned to 1 KB in-kernel
 };
 
@@ -158,6 +167,9 @@ struct Walk {
     int lead, nmem, sh;
     int pj, pk, plen, pt0, pend;
 };
+
+// the shared-prefix consumers park one in shared memory (128 bytes)
+static_assert(sizeof(Walk) <= 128 && alignof(Walk) <= 8, "walk record");
 
 // Groups of the shared-prefix mode: sequences start[k] .. start[k+1]-1 share
 // their first shared[k] tokens' blocks (rounded down to whole blocks and to
@@ -649,7 +661,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const float* __restrict__ k_scale, const float* __restrict__ v_scale,
                           ForkArgs fk, int32_t* dev_err) {
     static_assert(!kFork || (kMQ && !kF8), "shared-prefix mode: 16-bit pools, column tiles");
-    using L = DecodeSmem<D, kF8>;
+    using L = DecodeSmem<D, kF8, kFork>;
     constexpr bool kNative = L::kNative;
     using TM = typename std::conditional<kF8, __half, T>::type;   // tensor-core operand type
     using E = Elem<TM>;
@@ -684,12 +696,20 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+            // shared-prefix mode: freed by the MMA commit after the stage's P V
+            mbar_init(&empty[s], kFork ? 1 : kConsumerWarps);
         }
-        mbar_init(tail_ready, 1);
-        mbar_init(tail_data, 1);
-        mbar_init(pub_full, 2);
-        mbar_init(pub_free, 1);
+        if constexpr (kFork) {
+            // the tensor-core and publisher hand-offs; the publishers' release
+            // of a piece (the eleventh and twelfth) takes both publisher warps
+            for (int i = 0; i < 14; ++i)
+                mbar_init(full + 2 * kStages + i, (i == 10 || i == 11) ? 2 : 1);
+        } else {
+            mbar_init(tail_ready, 1);
+            mbar_init(tail_data, 1);
+            mbar_init(pub_full, 2);
+            mbar_init(pub_free, 1);
+        }
         *abort_flag = 0;
         *issued = 0;
         fence_mbar_init();
@@ -1034,17 +1054,481 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         return;
     }
 
+    if constexpr (kFork) {
+        // ---------------- shared-prefix mode: consumers on the tensor cores ----------------
+        // A stream's (member, head) columns are the M rows 0..31 of 128-row
+        // tcgen05 MMAs; rows 32.. read whatever lies behind the q rows and are
+        // never looked at.  Per stage g:
+        //   S^T = q K^T   [column][64 tokens], fp32 in tensor memory (two buffers)
+        //   P = exp2(S^T - m), written over S as 16 bits (bf16: hi, then lo)
+        //   O^T += P V    [column][D] in tensor memory, V the MN-major operand
+        // Warp 0 owns tensor-memory lanes 0..31, one column per lane: it writes
+        // each piece's q rows, runs the online softmax and writes the piece's
+        // result (final rows, or partials to the workspace).  Warp 1 issues
+        // the MMAs.  Warps 2 and 3 count finished pieces on the stream's
+        // arrival counter and merge the stream when its last piece is in.
+        uint64_t* s_full = full + 2 * kStages;    // S of stage g is in tensor memory
+        uint64_t* p_full = s_full + 2;            // P of stage g (and any O rescale) written
+        uint64_t* pv_done = p_full + 2;           // O += P V of stage g has finished
+        uint64_t* q_ready = pv_done + 2;          // the piece's q rows are written
+        uint64_t* drained = q_ready + 1;          // every MMA issued has finished
+        // by job parity: a piece's partials are written / taken by both
+        // publishers / counted by warp 2
+        uint64_t* pub_full_f = drained + 1;
+        uint64_t* pub_free_f = pub_full_f + 2;
+        uint64_t* last_ready = pub_free_f + 2;
+        uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc + 16);
+        // whether the piece completed its stream, by job parity
+        volatile int32_t* last_f = reinterpret_cast<int32_t*>(smem + L::kMisc + 20);
+        constexpr uint32_t kTmemCols = 256;       // S: 2 x 64 columns, then O: D columns
+        constexpr bool kBf = std::is_same<T, __nv_bfloat16>::value;
+        const int ncols = GH * fk.Mmax;
+        const int cstride = (ncols <= kHeadsN ? 1 : ncols <= 2 * kHeadsN ? 2 : 4) * kHeadsN;
+        // bounded wait that also gives up on an abort; warp-uniform result
+        auto wait_tc = [&](uint64_t* bar, uint32_t parity) -> bool {
+            bool got = false;
+            const uint64_t t0 = globaltimer();
+            for (uint32_t i = 0;; ++i) {
+                if (mbar_try_wait(bar, parity)) { got = true; break; }
+                if (*abort_flag != 0) break;
+                if ((i & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) break;
+            }
+            got = __all_sync(0xffffffffu, got);
+            if (!got && lane == 0 && *abort_flag == 0) {
+                flag_error(dev_err, PD_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            return got;
+        };
+        // the piece at a walk position: its unit's first head, its stages, and
+        // its place among the stream's pieces (c_first: the CTA index where
+        // the stream begins)
+        struct Piece {
+            int h0, stages, nseg, seg;
+            long c_first;
+        };
+        auto piece_at = [&](const Walk& x) {
+            Piece p;
+            p.h0 = (x.u / groups) * G + (x.u % groups) * GH;
+            const long left = x.end - x.pos;
+            p.stages = int(left < long(x.L - x.off) ? left : long(x.L - x.off));
+            p.c_first = x.start / x.per_cta;
+            p.nseg = int((x.start + x.L - 1) / x.per_cta - p.c_first + 1);
+            p.seg = int(long(x.bi) - p.c_first);
+            return p;
+        };
+        auto next_piece = [&](Walk& x, int stages) {
+            x.off += stages;
+            x.pos += stages;
+            if (x.off == x.L && x.pos < x.end) walk_next_stream<kFork>(x, context_lens, B, cap, S, fk);
+        };
+        const int mem = lane / GH, hh = lane - (lane / GH) * GH;   // lane's column (warp 0)
+        // output row of column lane in the group at x (-1: padding, or a member
+        // without context, whose rows the producer zeroes)
+        auto out_row = [&](const Walk& x, int h0) -> int64_t {
+            if (lane >= ncols || mem >= x.nmem || stream_ctx(context_lens, x.lead + mem, cap) == 0)
+                return -1;
+            return (int64_t)(x.lead + mem) * H + h0 + hh;
+        };
+        // partials per (unit, piece, column): piece k + c_first + seg of group k
+        auto ws_base = [&](const Walk& x, const Piece& p) -> int64_t {
+            return ((int64_t)x.u * fk.ppu + x.s + p.c_first) * cstride;
+        };
+        if (warp >= 2) {
+            // ------------------------------ publishers ------------------------------
+            // For each piece of several: take it once warp 0 has written its
+            // partials, count it (warp 2), and if it was the stream's last,
+            // merge the stream's pieces, columns split between the two warps.
+            uint32_t job = 0;
+            while (w.pos < w.end) {
+                const Piece pc = piece_at(w);
+                if (pc.nseg > 1) {
+                    if (!wait_tc(&pub_full_f[job & 1], (job >> 1) & 1)) return;
+                    uint32_t last = 0;
+                    if (warp == 2) {
+                        unsigned long long* cnt = ws_cnt + (int64_t)w.s * units + w.u;
+                        if (lane == 0) {
+                            const unsigned long long cnt0 =
+                                *reinterpret_cast<volatile unsigned long long*>(cnt);
+                            // warp 0's writes, seen through the barrier, go out
+                            // before the count
+                            __threadfence();
+                            last = arrive_piece(cnt, tag, pc.nseg, cnt0) ? 1u : 0u;
+                            last_f[job & 1] = int32_t(last);
+                        }
+                        last = __shfl_sync(0xffffffffu, last, 0);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&last_ready[job & 1]);
+                    } else {
+                        if (!wait_tc(&last_ready[job & 1], (job >> 1) & 1)) return;
+                        last = uint32_t(last_f[job & 1]);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&pub_free_f[job & 1]);
+                    ++job;
+                    if (last) {
+                        __threadfence();
+                        const int64_t wb = ws_base(w, pc);
+                        for (int n0 = (warp - 2) * 8; n0 < ncols; n0 += 16) {
+                            const int n = n0 + (lane >> 2);
+                            int64_t rn = -1;
+                            if (n < ncols && n / GH < w.nmem &&
+                                stream_ctx(context_lens, w.lead + n / GH, cap) > 0)
+                                rn = (int64_t)(w.lead + n / GH) * H + pc.h0 + (n - (n / GH) * GH);
+                            merge_rows<T, D, 1>(out, ws_o, ws_m, ws_l, rn, wb + n, cstride, pc.nseg,
+                                                lane);
+                        }
+                    }
+                }
+                next_piece(w, pc.stages);
+            }
+            return;
+        }
+        if (warp == 1) {
+            tc::tmem_alloc(tmem_slot, kTmemCols);
+            tc::tmem_relinquish();
+        }
+        tc::fence_before_sync();
+        asm volatile("bar.sync 3, 64;" ::: "memory");
+        tc::fence_after_sync();
+        const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+        const uint32_t o_tm = tmem + 2 * kStageTokens;
+        bool ok = true;
+        uint32_t g = 0;         // stages consumed by this CTA: ring slot, buffer and phases
+        uint32_t npc = 0;       // pieces begun
+        if (warp == 1) {
+            // ------------------------------ MMA issuer ------------------------------
+            // The whole warp runs the loop in step; one elected lane issues.
+            constexpr uint32_t kHi = tc::sw128_desc_hi(1024);
+            constexpr uint32_t kTile16 = uint32_t(L::kTile) >> 4;
+            constexpr uint32_t kIdQK = tc::idesc_f16(kBf, 128, kStageTokens, false, false);
+            constexpr uint32_t kIdPV = tc::idesc_f16(kBf, 128, D, false, true);
+            const uint32_t q_lo = tc::smem_desc_sw128_lo(smem_u32(smem), 16);   // q tile
+            const uint32_t k_lo = tc::smem_desc_sw128_lo(smem_u32(smem + L::kK), 16);
+            // V as the MN-major operand: N = D in 64-value atoms (LBO between
+            // them), K = tokens at 128 B (SBO per 8 tokens)
+            const uint32_t v_lo = tc::smem_desc_sw128_lo(smem_u32(smem + L::kV), L::kAtom);
+            // O += P V of stage gg (nt tokens: only the 16-token steps holding
+            // some); the piece's first product overwrites O.  P of tokens
+            // 32c..32c+31 sits over S as 16 columns of hi, then 16 of lo.
+            auto pv = [&](uint32_t gg, int nt, bool first) -> bool {
+                if (!wait_tc(&p_full[gg & 1], (gg >> 1) & 1)) return false;
+                tc::fence_after_sync();
+                const uint32_t slot = gg % kStages;
+                const uint32_t p0 = tmem + (gg & 1) * kStageTokens;
+                const uint32_t b0 = v_lo + slot * kTile16;
+                const int nk = (nt + 15) >> 4;
+#pragma unroll
+                for (int pass = 0; pass < (kBf ? 2 : 1); ++pass)
+                    for (int kk = 0; kk < nk; ++kk)
+                        tc::mma_ts_warp(o_tm, p0 + uint32_t(32 * (kk >> 1) + 8 * (kk & 1) + 16 * pass),
+                                        b0 + uint32_t(kk * 16 * 128 / 16), kHi, kIdPV,
+                                        uint32_t(!first || kk > 0 || pass > 0));
+                tc::commit_warp(&pv_done[gg & 1]);
+                tc::commit_warp(&empty[slot]);       // K and V of the stage are used up
+                return true;
+            };
+            while (ok && w.pos < w.end) {
+                const Piece pc = piece_at(w);
+                Walk pw = w;
+                if (!(ok = wait_tc(q_ready, npc & 1))) break;
+                tc::fence_after_sync();
+                int nt_prev = 0;
+                for (int st = 0; st < pc.stages; ++st, ++g) {
+                    const uint32_t slot = g % kStages;
+                    if (!(ok = wait_tc(&full[slot], (g / kStages) & 1))) break;
+                    tc::fence_after_sync();
+                    const uint32_t d_s = tmem + (g & 1) * kStageTokens;
+                    const uint32_t b0 = k_lo + slot * kTile16;
+#pragma unroll
+                    for (int kk = 0; kk < KS; ++kk) {
+                        const uint32_t qo = uint32_t((kk >> 2) * L::kQAtom + (kk & 3) * 32) >> 4;
+                        const uint32_t ko = uint32_t((kk >> 2) * L::kAtom + (kk & 3) * 32) >> 4;
+                        if (kk == 0)
+                            tc::mma_ss_warp<false>(d_s, q_lo + qo, kHi, b0 + ko, kHi, kIdQK);
+                        else
+                            tc::mma_ss_warp<true>(d_s, q_lo + qo, kHi, b0 + ko, kHi, kIdQK);
+                    }
+                    tc::commit_warp(&s_full[g & 1]);
+                    const int nt = min(kStageTokens, pw.pend - (pw.pt0 + pw.pk * kStageTokens));
+                    part_next(pw, context_lens, cap);
+                    // the previous stage's P V goes in behind this stage's S
+                    if (st > 0 && !(ok = pv(g - 1, nt_prev, st == 1))) break;
+                    nt_prev = nt;
+                }
+                if (!ok || !(ok = pv(g - 1, nt_prev, pc.stages == 1))) break;
+                ++npc;
+                next_piece(w, pc.stages);
+            }
+            // nothing may still write tensor memory when it is freed
+            tc::commit_warp(drained);
+            (void)__all_sync(0xffffffffu, mbar_wait(drained, 0));
+        } else {
+            // ------------------------- softmax and results -------------------------
+            const uint32_t q_base = smem_u32(smem);      // q tile
+            const uint32_t v_base = smem_u32(smem + L::kV);
+            uint32_t njob = 0;      // pieces handed to the publishers
+            // q rows of the piece at x into the q tile (K-major, 128-byte
+            // swizzle, lane = row), then hand them to the issuer
+            auto write_q = [&](const Walk& x, int h0) -> int64_t {
+                const int64_t r = out_row(x, h0);
+                const uint4* src = reinterpret_cast<const uint4*>(q + (r < 0 ? 0 : r) * D);
+#pragma unroll
+                for (int a = 0; a < kAtoms; ++a) {
+                    uint4 v[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        v[c] = r >= 0 ? __ldg(src + 8 * a + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        st_shared_v4(q_base + a * L::kQAtom + lane * 128 + ((c ^ (lane & 7)) << 4),
+                                     v[c].x, v[c].y, v[c].z, v[c].w);
+                }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(q_ready);
+                return r;
+            };
+            int64_t orow = w.pos < w.end ? write_q(w, piece_at(w).h0) : -1;
+            while (ok && w.pos < w.end) {
+                const Piece pc = piece_at(w);
+                Walk pw = w;
+                // the next piece, found now: its q rows go to L2 at once and
+                // into the q tile during this piece's last stage (no product
+                // reads q once that stage's S is in)
+                bool has_next;
+                int64_t rn;
+                {
+                    // kept in shared memory until the piece ends (registers are scarce)
+                    Walk wn = w;
+                    next_piece(wn, pc.stages);
+                    has_next = wn.pos < wn.end;
+                    rn = has_next ? out_row(wn, piece_at(wn).h0) : -1;
+                    __syncwarp();
+                    if (lane == 0) *reinterpret_cast<Walk*>(smem + L::kTl) = wn;
+                }
+                if (rn >= 0)
+                    for (int b = 0; b < D * 2; b += 128)
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(
+                            reinterpret_cast<const unsigned char*>(q + rn * D) + b));
+                float m_run = -INFINITY, l_run = 0.f;
+                for (int st = 0; st < pc.stages; ++st, ++g) {
+                    const int nt = min(kStageTokens, pw.pend - (pw.pt0 + pw.pk * kStageTokens));
+                    const int act = pw.pj;            // -1: shared prefix, else member act's tail
+                    part_next(pw, context_lens, cap);
+                    if (!(ok = wait_tc(&s_full[g & 1], (g >> 1) & 1))) break;
+                    tc::fence_after_sync();
+                    if (st == pc.stages - 1 && has_next) {
+                        // the piece's last S is in: the next piece's q rows
+                        // (zeros for a padding column) copy in behind it
+                        const uint4* src = reinterpret_cast<const uint4*>(q + (rn < 0 ? 0 : rn) * D);
+#pragma unroll
+                        for (int c = 0; c < D / 8; ++c) {
+                            const uint32_t dst = q_base + (c >> 3) * L::kQAtom + lane * 128 +
+                                                 (((c & 7) ^ (lane & 7)) << 4);
+                            if (rn >= 0)
+                                asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst),
+                                             "l"(src + c) : "memory");
+                            else
+                                st_shared_v4(dst, 0u, 0u, 0u, 0u);
+                        }
+                    }
+                    const uint32_t s_tm = tmem + (g & 1) * kStageTokens;
+                    // a member's tail is seen only by that member's columns
+                    const int lim = (orow >= 0 && (act < 0 || act == mem)) ? nt : 0;
+                    // S is read twice, 32 tokens at a time (the maximum, then
+                    // P), which keeps the registers to one chunk; chunks past
+                    // the stage's tokens are skipped (no product reads them).
+                    // kDense: a full stage of the shared prefix, which every
+                    // column sees whole (no per-token masks).
+                    auto softmax = [&](auto dense_c) -> bool {
+                        constexpr bool kDense = decltype(dense_c)::value;
+                        float mx = -INFINITY;
+#pragma unroll
+                        for (int c = 0; c < kStageTokens / 32; ++c) {
+                            if (!kDense && 32 * c >= nt) break;
+                            uint32_t r[32];
+                            tc::tmem_ld32(s_tm + 32 * c, r);
+                            tc::tmem_ld_wait();
+                            tc::tmem_ld_fence(r);
+                            float m8[8];
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (kDense || 32 * c + j < lim)
+                                    m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(r[j]));
+                            mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))));
+                        }
+                        mx = mx == -INFINITY ? mx : mx * scale_log2;
+                        // lazy rescale: only when the maximum grows by more than 2^8
+                        const bool grow = mx > m_run + kRescaleThreshold;
+                        float alpha = 1.f;
+                        if (grow) {
+                            alpha = ex2(m_run - mx);      // 0 the first time
+                            m_run = mx;
+                            l_run *= alpha;
+                        }
+                        if (st > 0 && __any_sync(0xffffffffu, grow)) {
+                            // O holds the stages before g: let the last of them finish
+                            if (!wait_tc(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1)) return false;
+                            tc::fence_after_sync();
+#pragma unroll
+                            for (int c = 0; c < D / 32; ++c) {
+                                uint32_t r[32];
+                                tc::tmem_ld32(o_tm + 32 * c, r);
+                                tc::tmem_ld_wait();
+                                tc::tmem_ld_fence(r);
+#pragma unroll
+                                for (int e = 0; e < 32; ++e)
+                                    r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                                tc::tmem_st32(o_tm + 32 * c, r);
+                            }
+                        }
+                        const float mu = m_run == -INFINITY ? 0.f : m_run;
+                        // P over S, per 32 tokens c: hi in columns 32c..32c+15
+                        // and (bf16) lo in 32c+16..32c+31
+                        const float2 sc2 = make_float2(scale_log2, scale_log2);
+                        const float2 nm2 = make_float2(-mu, -mu);
+                        float2 ls4[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) ls4[k] = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int c = 0; c < kStageTokens / 32; ++c) {
+                            if (!kDense && 32 * c >= nt) break;
+                            uint32_t r[32];
+                            tc::tmem_ld32(s_tm + 32 * c, r);
+                            tc::tmem_ld_wait();
+                            tc::tmem_ld_fence(r);
+                            uint32_t hi[16];
+                            [[maybe_unused]] uint32_t lo[16];
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const float2 xv = ffma2(make_float2(__uint_as_float(r[2 * e]),
+                                                                    __uint_as_float(r[2 * e + 1])),
+                                                        sc2, nm2);
+                                const float p0 = kDense || 32 * c + 2 * e < lim ? ex2(xv.x) : 0.f;
+                                const float p1 = kDense || 32 * c + 2 * e + 1 < lim ? ex2(xv.y) : 0.f;
+                                ls4[e & 3] = fadd2(ls4[e & 3], make_float2(p0, p1));
+                                hi[e] = E::pack2(p0, p1);
+                                if constexpr (kBf) {
+                                    const float2 d = fsub2(make_float2(p0, p1), E::unpack2(hi[e]));
+                                    lo[e] = E::pack2(d.x, d.y);
+                                }
+                            }
+                            tc::tmem_st16(s_tm + 32 * c, hi);
+                            if constexpr (kBf) tc::tmem_st16(s_tm + 32 * c + 16, lo);
+                        }
+                        const float2 l01 = fadd2(fadd2(ls4[0], ls4[1]), fadd2(ls4[2], ls4[3]));
+                        l_run += l01.x + l01.y;
+                        return true;
+                    };
+                    // uniform: a full stage of the shared prefix
+                    const bool dense = act < 0 && nt == kStageTokens;
+                    if (!(ok = dense ? softmax(std::true_type{}) : softmax(std::false_type{}))) break;
+                    if (nt & 15) {
+                        // V rows nt .. 16 ceil(nt / 16) - 1 hold other data (or
+                        // none yet): zeroed, so that 0 * v stays 0 in the last step
+                        const uint32_t vb = v_base + (g % kStages) * L::kTile;
+                        const int zr = 16 - (nt & 15);
+                        for (int i = lane; i < zr * kAtoms * 8; i += 32) {
+                            const int r = nt + i / (kAtoms * 8);
+                            const int a = (i >> 3) % kAtoms;
+                            st_shared_v4(vb + a * L::kAtom + r * 128 + (i & 7) * 16, 0u, 0u, 0u, 0u);
+                        }
+                        tc::fence_proxy_async_smem();
+                    }
+                    tc::tmem_st_wait();
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&p_full[g & 1]);
+                }
+                if (!ok) break;
+                // the piece's last product, then O out of tensor memory, 32
+                // values at a time, straight to the output or the workspace
+                if (!(ok = wait_tc(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1))) break;
+                tc::fence_after_sync();
+                const int64_t wr = ws_base(w, pc) + int64_t(pc.seg) * cstride + lane;
+                // the whole stream was here: final, normalised output
+                const float inv = l_run == 0.f ? 0.f : 1.f / l_run;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(o_tm + 32 * c, o);
+                    tc::tmem_ld_wait();
+                    tc::tmem_ld_fence(o);
+                    if (orow >= 0 && pc.nseg == 1) {
+                        uint4* dst = reinterpret_cast<uint4*>(out + orow * D + 32 * c);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float* f = reinterpret_cast<const float*>(&o[8 * j]);
+                            dst[j] = make_uint4(E::pack2(f[0] * inv, f[1] * inv),
+                                                E::pack2(f[2] * inv, f[3] * inv),
+                                                E::pack2(f[4] * inv, f[5] * inv),
+                                                E::pack2(f[6] * inv, f[7] * inv));
+                        }
+                    } else if (orow >= 0) {
+                        float4* dst = reinterpret_cast<float4*>(ws_o + wr * D + 32 * c);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_float4(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]),
+                                                 __uint_as_float(o[4 * j + 2]),
+                                                 __uint_as_float(o[4 * j + 3]));
+                    }
+                }
+                if (orow >= 0 && pc.nseg > 1) {
+                    ws_m[wr] = m_run;
+                    ws_l[wr] = l_run;
+                }
+                tc::fence_before_sync();
+                if (pc.nseg > 1) {
+                    // hand the partials to the publishers (once they have
+                    // taken the piece before last, which used the same barriers)
+                    if (njob > 1 && !(ok = wait_tc(&pub_free_f[njob & 1], ((njob - 2) >> 1) & 1)))
+                        break;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&pub_full_f[njob & 1]);
+                    ++njob;
+                }
+                // every product of the piece is done and O is read: the next
+                // piece's q rows (copied during the last stage) go to the issuer
+                if (has_next) {
+                    cp_async_wait_all();
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(q_ready);
+                }
+                ++npc;
+                __syncwarp();
+                w = *reinterpret_cast<const Walk*>(smem + L::kTl);
+                orow = rn;
+            }
+            if (*abort_flag != 0 && lane == 0) {
+                // let copies already issued into the ring land before the CTA exits
+                const int n_issued = *issued;
+                for (int s2 = int(g); s2 < n_issued; ++s2)
+                    if (!mbar_wait(&full[s2 % kStages], (s2 / kStages) & 1)) break;
+            }
+        }
+        tc::fence_before_sync();
+        asm volatile("bar.sync 3, 64;" ::: "memory");
+        if (warp == 1) {
+            tc::fence_after_sync();
+            tc::tmem_dealloc(tmem, kTmemCols);
+        }
+        return;
+    }
+
     // ---------------- consumer warps ----------------
     const int j8 = lane >> 3, r8 = lane & 7;     // ldmatrix: matrix index, row within it
-    // columns of a stream, in 1, 2 or 4 tiles of 8; this warp's tokens within
-    // a stage (16, 32 or all 64) and its first column
-    const int ncols = kFork ? GH * fk.Mmax : GH * nq;
-    const int ctiles = kMQ ? (ncols <= kHeadsN ? 1 : ncols <= 2 * kHeadsN ? 2 : 4) : 1;
+    // columns of a stream, in 1 or 2 tiles of 8; this warp's tokens within a
+    // stage (16 or 32) and its first column
+    const int ncols = GH * nq;
+    const int ctiles = kMQ ? (ncols <= kHeadsN ? 1 : 2) : 1;
     const int wpc = kConsumerWarps / ctiles;     // warps per column tile
     const int tb = kMQ ? (warp % wpc) * 16 * ctiles : warp * 16;
     const int col0 = kMQ ? (warp / wpc) * kHeadsN : 0;
-    const bool tile_live = col0 < ncols;         // four tiles may leave the last one empty
-    const int cstride = ctiles * kHeadsN;        // shared-prefix workspace: columns per piece
     const uint32_t k_base0 = smem_u32(smem + L::kK);
     const uint32_t v_base0 = smem_u32(smem + L::kV);
     const float2 neg1 = make_float2(-1.f, -1.f);
@@ -1055,17 +1539,11 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
     // as small as q's own; with bf16 operands (2^-9) as the hi + lo pair
     constexpr bool kLoP = !std::is_same<TM, __half>::value;
 
-    // output row of column n of stream x whose unit starts at head h0 (-1: a
-    // padding column, or a member without context, whose rows others write)
+    // output row of column n (head h0 + n / nq, query n % nq) of stream x
+    // whose unit starts at head h0 (-1: a padding column)
     auto col_row = [&](const Walk& x, int h0, int n) -> int64_t {
-        if constexpr (kFork) {
-            const int j = n / GH, hh = n - j * GH;
-            if (j >= x.nmem || stream_ctx(context_lens, x.lead + j, cap) == 0) return -1;
-            return (int64_t)(x.lead + j) * H + h0 + hh;
-        } else {
-            const int hh = n / nq, j = n - hh * nq;
-            return hh < GH ? ((int64_t)x.s * nq + j) * H + h0 + hh : -1;
-        }
+        const int hh = n / nq, j = n - hh * nq;
+        return hh < GH ? ((int64_t)x.s * nq + j) * H + h0 + hh : -1;
     };
 
     uint32_t npub = 0;                           // pieces handed to the publisher warp
@@ -1120,7 +1598,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         // switch hit instead of waiting on HBM: the next stream of the range is
         // (s + 1, u) (an empty sequence is skipped by the walk, so that prefetch
         // is merely wasted).
-        if (!kFork && piece_stages < w.end - w.pos) {
+        if (piece_stages < w.end - w.pos) {
             const int nu = w.u;                         // same unit, next sequence
             const int ns = w.s + 1;
             if (ns < B) {
@@ -1148,13 +1626,6 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         int dj[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) dj[h] = kMQ ? nq - 1 - (col0 + 2 * (lane & 3) + h) % nq : 0;
-        // shared-prefix mode: the members of this lane's two columns, the
-        // members this warp's tile spans, and the walk over the piece's parts
-        int mem[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) mem[h] = kFork ? (col0 + 2 * (lane & 3) + h) / GH : 0;
-        const int tile_m0 = kFork ? col0 / GH : 0, tile_m1 = kFork ? (col0 + kHeadsN - 1) / GH : 0;
-        Walk pw = w;
 
         for (int st = 0; st < piece_stages;) {
             // the native FP8 path takes two stages of the piece at a time
@@ -1170,17 +1641,9 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 aborted = true;
                 break;                   // skip the piece's other stages
             }
-            // context from this stage on (decode, verify); shared-prefix mode:
-            // the stage's tokens and the member whose tail it is (-1: shared)
-            int rem, nt, act = -1;
-            if constexpr (kFork) {
-                rem = pw.pend - (pw.pt0 + pw.pk * kStageTokens);
-                nt = min(kStageTokens, rem);
-                act = pw.pj;
-            } else {
-                rem = w.ctx - (w.off + st) * kStageTokens;
-                nt = min(kStageTokens, rem);
-            }
+            // context from this stage on, and the stage's tokens
+            const int rem = w.ctx - (w.off + st) * kStageTokens;
+            const int nt = min(kStageTokens, rem);
             // FP8 pools: this warp widens its own 16 rows of K and V to fp16 in
             // the one 16-bit tile (no other warp reads them), then frees the raw
             // stage for the next copy right away.
@@ -1389,20 +1852,15 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
               // round; NS = 1 is the decode layout, NS = 2 the two-tile verify one
               auto body = [&](auto ns_c) {
                 constexpr int NS = decltype(ns_c)::value;
-                if (tb >= nt || !tile_live) return;
-                // a member's tail stage concerns only the tile holding its columns
-                if (kFork && act >= 0 && (act < tile_m0 || act > tile_m1)) return;
-                // sub-tiles of this warp that hold tokens (shared-prefix mode,
-                // whose short tail stages would otherwise run all NS)
-                const int nsb = (NS == 1 || !kFork) ? NS : min(NS, (nt - tb + 15) >> 4);
+                if (tb >= nt) return;
                 const uint32_t kb = k_base0 + tslot * L::kTile;
                 const uint32_t vb = v_base0 + tslot * L::kTile;
-                const bool partial = tb + 16 * nsb > nt;
+                const bool partial = tb + 16 * NS > nt;
                 if (partial) {
                     // V rows past the context end hold other data or were never
                     // loaded this round: zero them so that 0 * v stays 0.
                     unsigned char* vrow = smem + L::kV + tslot * L::kTile;
-                    for (int i = lane; i < 16 * nsb * kAtoms * 8; i += 32) {
+                    for (int i = lane; i < 16 * NS * kAtoms * 8; i += 32) {
                         const int tok = tb + i / (kAtoms * 8);
                         if (tok >= nt) {
                             const int a = (i / 8) % kAtoms, c = i % 8;
@@ -1422,7 +1880,6 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 for (int ks = 0; ks < KS; ++ks) {
 #pragma unroll
                     for (int sb = 0; sb < NS; ++sb) {
-                        if (sb >= nsb) continue;
                         uint32_t a[4];
                         wmma16::ldsm_x4(a, swz<D>(kb, tb + 16 * sb + r8 + 8 * (j8 & 1),
                                                   2 * ks + (j8 >> 1)));
@@ -1431,21 +1888,17 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
                 // lane holds tokens tb + 16 sb + lane/4 (0,1) and + 8 (2,3); columns
                 // 2(lane%4) + {0,1}.  Tokens past a column's limit are masked: the
-                // stage's end (decode); the query's causal limit (verify); in
-                // shared-prefix mode, the whole stage for columns of other members
-                // when it is a member's tail.
+                // stage's end (decode); the query's causal limit (verify).
                 int lim[2];
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    lim[h] = kFork ? ((act < 0 || mem[h] == act) ? nt : 0)
-                                   : (kMQ ? rem - dj[h] : nt);
+                for (int h = 0; h < 2; ++h) lim[h] = kMQ ? rem - dj[h] : nt;
                 float x[NS][4];
 #pragma unroll
                 for (int sb = 0; sb < NS; ++sb)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int tok = tb + 16 * sb + (lane >> 2) + (i >> 1) * 8;
-                        x[sb][i] = (sb < nsb && tok < lim[i & 1])
+                        x[sb][i] = tok < lim[i & 1]
                                        ? (acc[sb][0][i] + acc[sb][1][i]) * sl2 : -INFINITY;
                     }
                 // ---- online softmax per column (lane-local state, 3 shuffles per column)
@@ -1508,7 +1961,6 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 for (int mt = 0; mt < KS; ++mt) {
 #pragma unroll
                     for (int sb = 0; sb < NS; ++sb) {
-                        if (sb >= nsb) continue;
                         uint32_t a[4];
                         wmma16::ldsm_x4_t(a, swz<D>(vb, tb + 16 * sb + r8 + 8 * (j8 >> 1),
                                                     2 * mt + (j8 & 1)));
@@ -1518,11 +1970,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 }
                 if (partial && !kF8) tc::fence_proxy_async_smem();   // zeros before the next TMA write
               };
-              if constexpr (kFork) {
-                  if (ctiles == 4) body(std::integral_constant<int, 4>{});
-                  else if (ctiles == 2) body(std::integral_constant<int, 2>{});
-                  else body(std::integral_constant<int, 1>{});
-              } else if constexpr (kMQ) {
+              if constexpr (kMQ) {
                   if (ctiles == 2) body(std::integral_constant<int, 2>{});
                   else body(std::integral_constant<int, 1>{});
               } else {
@@ -1533,7 +1981,6 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             if (!kF8 && lane == 0) mbar_arrive(&empty[slot]);
             st += nst;
             gs += nst;
-            if constexpr (kFork) part_next(pw, context_lens, cap);
         }
         // All four consumer warps decide together whether to go on: a warp
         // that gave up still arrives here, so named-barrier counts stay matched.
@@ -1620,20 +2067,13 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             // streaming).
             asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
             const bool leader = (warp % wpc) == 0;   // holds its tile's result
-            // workspace index of column c's partial for piece `p` of this
-            // stream: per output row (verify), or compact per (unit, piece,
-            // column) in shared-prefix mode (piece k + c_first + p < n_groups +
-            // CTAs per unit)
-            auto ws_index = [&](int64_t row, int c, long p) -> int64_t {
-                if constexpr (kFork)
-                    return ((int64_t)w.u * fk.ppu + w.s + c_first + p) * cstride + c;
-                return row * max_segs + p;
-            };
-            auto merge_tile = [&]() {               // verify, shared prefix
+            // workspace index of a column's partial for piece `p` of this
+            // stream: per output row
+            auto ws_index = [&](int64_t row, long p) -> int64_t { return row * max_segs + p; };
+            auto merge_tile = [&]() {               // verify
                 const int n = col0 + (lane >> 2);
                 const int64_t orow = col_row(w, h0, n);
-                merge_rows<T, D, 1>(out, ws_o, ws_m, ws_l, orow,
-                                    orow < 0 ? 0 : ws_index(orow, n, 0), kFork ? cstride : 1,
+                merge_rows<T, D, 1>(out, ws_o, ws_m, ws_l, orow, orow < 0 ? 0 : ws_index(orow, 0), 1,
                                     nseg, lane);
             };
             // the arrival counter is read now, so that its latency overlaps the
@@ -1642,7 +2082,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             unsigned long long cnt0 = 0;
             if (nseg > 1 && warp == 0 && lane == 0)
                 cnt0 = *reinterpret_cast<volatile unsigned long long*>(cnt);
-            if (leader && tile_live) {
+            if (leader) {
                 // lane: columns ha, ha + 1; dims 16mt + lane/4 and + 8
                 const int ha = 2 * (lane & 3);
                 const int d0 = lane >> 2;
@@ -1662,7 +2102,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                             orow[16 * mt + 8] = T(o[mt][2 + h] * inv);
                         }
                     } else {
-                        const int64_t r = ws_index(row, c, seg);
+                        const int64_t r = ws_index(row, seg);
                         float* wrow = ws_o + r * D + d0;
 #pragma unroll
                         for (int mt = 0; mt < KS; ++mt) {
@@ -1698,7 +2138,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 asm volatile("bar.sync 2, %0;" ::"r"(ctiles * 32) : "memory");
                 if (warp == 0 && lane == 0) *last_flag = arrive_piece(cnt, tag, nseg, cnt0) ? 1 : 0;
                 asm volatile("bar.sync 2, %0;" ::"r"(ctiles * 32) : "memory");
-                if (*last_flag && tile_live) {
+                if (*last_flag) {
                     __threadfence();
                     merge_tile();
                 }
@@ -1804,7 +2244,7 @@ WsLayout fork_ws_layout(int n_groups, int max_group, int H, int Hk, int D, int* 
 
 template <typename T, int D, bool kF8, bool kMQ, bool kFork>
 pd_status launch_decode_t(const DecodeArgs& a) {
-    using Lt = DecodeSmem<D, kF8>;
+    using Lt = DecodeSmem<D, kF8, kFork>;
     const int G = a.H / a.Hk;
     const int nq = kMQ && !kFork ? a.nq : 1;
     const int GH = kFork ? heads_per_unit(G, a.max_group, 4 * kHeadsN)
