@@ -1439,10 +1439,20 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         }
                         tc::fence_proxy_async_smem();
                     }
+                    const bool q_in = st == pc.stages - 1 && has_next;
+                    if (q_in) {
+                        // the next piece's q rows are in: its first S can be
+                        // computed while this piece's O is read out
+                        cp_async_wait_all();
+                        tc::fence_proxy_async_smem();
+                    }
                     tc::tmem_st_wait();
                     tc::fence_before_sync();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&p_full[g & 1]);
+                    if (lane == 0) {
+                        mbar_arrive(&p_full[g & 1]);
+                        if (q_in) mbar_arrive(q_ready);
+                    }
                 }
                 if (!ok) break;
                 // the piece's last product, then O out of tensor memory, 32
@@ -1490,14 +1500,6 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&pub_full_f[njob & 1]);
                     ++njob;
-                }
-                // every product of the piece is done and O is read: the next
-                // piece's q rows (copied during the last stage) go to the issuer
-                if (has_next) {
-                    cp_async_wait_all();
-                    tc::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(q_ready);
                 }
                 ++npc;
                 __syncwarp();
