@@ -77,11 +77,38 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def code_text(src: str) -> str:
+    """C++/CUDA source without its comments, whitespace runs folded to one
+    space: two sources with the same code_text compile to the same kernels."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == "/" and src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif c == "/" and src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_sha(*names) -> str:
+    """First 16 hex digits of sha256 over the code (comments and whitespace
+    aside) of the named files under csrc/, in order."""
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "paged_kv_attention_26_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "paged_kv_attention_26_gb300", "csrc", n)) as f:
+            h.update(code_text(f.read()).encode())
     return h.hexdigest()[:16]
 
 

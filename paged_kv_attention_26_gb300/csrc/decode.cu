@@ -40,6 +40,11 @@
 //    carries about 2^-17 relative error instead of the 2^-9 of a single bf16;
 //    fp16 operands (fp16 pools, FP8 pools widened to fp16) take one fp16 P
 //    (2^-11, the size of q's own rounding in the FP8 path);
+//  * shared-prefix mode (fork groups) runs its consumers on the 5th-generation
+//    tensor cores instead: the group's (member, head) columns are the rows of
+//    128-row tcgen05 products, S^T = q K^T and O^T += P V, with S, P and O in
+//    tensor memory; one warp runs the softmax over the columns (one per lane),
+//    one issues the products, one counts and merges pieces;
 //  * at the end of each stream piece the four warps merge through a small
 //    exchange buffer (after which all but the result warp go on to the next
 //    piece); a whole stream is normalised and written to `out`.
@@ -637,16 +642,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // exactly, q rounded to fp16), and the scales are applied in fp32.
 // kMQ: several columns per kv-head unit beyond its query heads, in tiles of 8
 // (MMA N): one tile is the decode layout (each consumer warp takes 16 tokens
-// of a stage, the four warps merge per piece); with two tiles, warp w takes
-// tile w / 2 and tokens 32 (w % 2) .. + 31 of each stage; with four tiles
-// (shared-prefix mode only), warp w takes tile w and all 64 tokens, so K/V of
-// a kv head is still read once whatever the column count (<= 16 for verify,
-// <= 32 for shared prefixes).  Verification (nq_arg query tokens per
-// sequence, the last nq_arg positions of its context, each attending
-// causally): columns are (head, query token) pairs, head-major.
+// of a stage, the four warps merge per piece); with two tiles (verify, up to
+// 16 columns), warp w takes tile w / 2 and tokens 32 (w % 2) .. + 31 of each
+// stage, so K/V of a kv head is still read once.  Verification (nq_arg query
+// tokens per sequence, the last nq_arg positions of its context, each
+// attending causally): columns are (head, query token) pairs, head-major.
 // kFork (with kMQ): shared-prefix mode, B = groups of sequences; columns are
 // (member, head) pairs, member-major (member j of the group: columns
-// j GH .. j GH + GH - 1), so a member's tail stage involves one tile.
+// j GH .. j GH + GH - 1), up to 32, the M rows of the tensor-core consumers.
 template <typename T, int D, bool kF8, bool kMQ, bool kFork>
 __global__ void __launch_bounds__(kMQ ? kDecodeThreads : kDecodeThreadsPub, 2)
 paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -2210,8 +2213,8 @@ int sm_count(int dev) {
 }
 
 // Largest divisor of G whose columns fit max_cols: 8 heads for decode; 16
-// (two tiles of N = 8) for verification, GH * nq; 32 (four tiles) in
-// shared-prefix mode, GH * Mmax.
+// (two tiles of N = 8) for verification, GH * nq; 32 (the tensor-core rows
+// read) in shared-prefix mode, GH * Mmax.
 int heads_per_unit(int G, int cols_per_head, int max_cols) {
     for (int g = std::min(G, max_cols / cols_per_head); g >= 1; --g)
         if (G % g == 0) return g;
