@@ -129,9 +129,12 @@ struct DecodeSmem {
     // abort flag, issued count, flags (kTc: and the tensor-memory address)
     static constexpr int kMisc = kBar + (2 * kRing + (kTc ? 14 : 4)) * 8;
     // tail merge: the other piece of the range's last stream, [8 rows][D] of
-    // o, then m[8], l[8]; kTc: the walk position of the next piece instead
+    // o, then m[8], l[8]; kTc: a ring of kWalks walk positions (128 bytes
+    // each) and the pieces each reading warp is done with, instead
+    static constexpr int kWalks = 4;
     static constexpr int kTl = kMisc + (kTc ? 32 : 16);
-    static constexpr int kBytes = kTl + (kTc ? 128 : (kHeadsN * D + 2 * kHeadsN) * 4);
+    static constexpr int kBytes =
+        kTl + (kTc ? kWalks * 128 + 16 : (kHeadsN * D + 2 * kHeadsN) * 4);
     static constexpr int kAlloc = kBytes + 1024;           // base aligned to 1 KB in-kernel
 };
 
@@ -651,7 +654,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // (member, head) pairs, member-major (member j of the group: columns
 // j GH .. j GH + GH - 1), up to 32, the M rows of the tensor-core consumers.
 template <typename T, int D, bool kF8, bool kMQ, bool kFork>
-__global__ void __launch_bounds__(kMQ ? kDecodeThreads : kDecodeThreadsPub, 2)
+__global__ void __launch_bounds__(kMQ && !kFork ? kDecodeThreads : kDecodeThreadsPub, 2)
 paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, T* __restrict__ out,
                           const T* __restrict__ q, const int32_t* __restrict__ block_tables,
@@ -707,6 +710,9 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             // of a piece (the eleventh and twelfth) takes both publisher warps
             for (int i = 0; i < 14; ++i)
                 mbar_init(full + 2 * kStages + i, (i == 10 || i == 11) ? 2 : 1);
+            *reinterpret_cast<volatile int32_t*>(smem + L::kMisc + 28) = 0;   // walks ready
+            for (int i = 0; i < 4; ++i)                                       // ... and read
+                reinterpret_cast<volatile int32_t*>(smem + L::kTl + L::kWalks * 128)[i] = 0;
         } else {
             mbar_init(tail_ready, 1);
             mbar_init(tail_data, 1);
@@ -893,7 +899,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         return;
     }
 
-    if (warp == kPublisherWarp) {
+    if (!kFork && warp == kPublisherWarp) {
         // ---------------- publisher warp (one query per sequence) ----------------
         // Warps 0 and 1 hand each finished piece over as two partial results
         // in the exchange buffer (the four consumer warps' shares combined in
@@ -1070,6 +1076,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         // result (final rows, or partials to the workspace).  Warp 1 issues
         // the MMAs.  Warps 2 and 3 count finished pieces on the stream's
         // arrival counter and merge the stream when its last piece is in.
+        // Warp 5 walks the CTA's pieces ahead of the others.
         uint64_t* s_full = full + 2 * kStages;    // S of stage g is in tensor memory
         uint64_t* p_full = s_full + 2;            // P of stage g (and any O rescale) written
         uint64_t* pv_done = p_full + 2;           // O += P V of stage g has finished
@@ -1137,13 +1144,74 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         auto ws_base = [&](const Walk& x, const Piece& p) -> int64_t {
             return ((int64_t)x.u * fk.ppu + x.s + p.c_first) * cstride;
         };
+        // The walk position after each of the CTA's pieces, found ahead by
+        // warp 5 (each is a chain of dependent loads: the next group's bounds,
+        // then its members' context lengths) into a ring of kWalks slots; the
+        // other warps read it from shared memory when they move on, and mark
+        // each piece they are done with, which frees its slot.
+        volatile int32_t* walks_ready = reinterpret_cast<int32_t*>(smem + L::kMisc + 28);
+        Walk* walks = reinterpret_cast<Walk*>(smem + L::kTl);
+        volatile int32_t* walks_done = reinterpret_cast<int32_t*>(smem + L::kTl + L::kWalks * 128);
+        // bounded wait until *v >= want; false (with the abort flag set) when
+        // it runs out or another warp gave up
+        auto wait_at_least = [&](auto probe, int32_t want) -> bool {
+            bool got = probe() >= want;
+            if (!got) {
+                const uint64_t t0 = globaltimer();
+                for (uint32_t i = 0;; ++i) {
+                    if (probe() >= want) { got = true; break; }
+                    if (*abort_flag != 0) break;
+                    if ((i & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) break;
+                }
+            }
+            got = __all_sync(0xffffffffu, got);
+            if (!got && lane == 0 && *abort_flag == 0) {
+                flag_error(dev_err, PD_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            return got;
+        };
+        // x = the walk after piece k; `last` marks piece k done for this warp
+        auto piece_after = [&](Walk& x, uint32_t k, bool last) -> bool {
+            if (!wait_at_least([&] { return *walks_ready; }, int32_t(k + 1))) return false;
+            __threadfence_block();
+            x = walks[k % L::kWalks];
+            if (last) {
+                __threadfence_block();
+                __syncwarp();
+                if (lane == 0) walks_done[warp] = int32_t(k + 1);
+            }
+            return true;
+        };
+        if (warp == kPublisherWarp) {
+            // ------------------------------- walker -------------------------------
+            Walk x = w;
+            for (int k = 0; x.pos < x.end; ++k) {
+                // the slot's previous walk has been read by warps 0-3
+                if (k >= L::kWalks &&
+                    !wait_at_least([&] {
+                        return min(min(walks_done[0], walks_done[1]),
+                                   min(walks_done[2], walks_done[3]));
+                    }, int32_t(k - L::kWalks + 1)))
+                    return;
+                __threadfence_block();              // their reads before this write
+                next_piece(x, piece_at(x).stages);
+                if (lane == 0) {
+                    walks[k % L::kWalks] = x;
+                    __threadfence_block();
+                    *walks_ready = k + 1;
+                }
+                __syncwarp();
+            }
+            return;
+        }
         if (warp >= 2) {
             // ------------------------------ publishers ------------------------------
             // For each piece of several: take it once warp 0 has written its
             // partials, count it (warp 2), and if it was the stream's last,
             // merge the stream's pieces, columns split between the two warps.
             uint32_t job = 0;
-            while (w.pos < w.end) {
+            for (uint32_t k = 0; w.pos < w.end; ++k) {
                 const Piece pc = piece_at(w);
                 if (pc.nseg > 1) {
                     if (!wait_tc(&pub_full_f[job & 1], (job >> 1) & 1)) return;
@@ -1183,7 +1251,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         }
                     }
                 }
-                next_piece(w, pc.stages);
+                if (!piece_after(w, k, true)) return;
             }
             return;
         }
@@ -1260,8 +1328,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                     nt_prev = nt;
                 }
                 if (!ok || !(ok = pv(g - 1, nt_prev, pc.stages == 1))) break;
+                if (!(ok = piece_after(w, npc, true))) break;
                 ++npc;
-                next_piece(w, pc.stages);
             }
             // nothing may still write tensor memory when it is freed
             tc::commit_warp(drained);
@@ -1302,13 +1370,10 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 bool has_next;
                 int64_t rn;
                 {
-                    // kept in shared memory until the piece ends (registers are scarce)
                     Walk wn = w;
-                    next_piece(wn, pc.stages);
+                    if (!(ok = piece_after(wn, npc, false))) break;
                     has_next = wn.pos < wn.end;
                     rn = has_next ? out_row(wn, piece_at(wn).h0) : -1;
-                    __syncwarp();
-                    if (lane == 0) *reinterpret_cast<Walk*>(smem + L::kTl) = wn;
                 }
                 if (rn >= 0)
                     for (int b = 0; b < D * 2; b += 128)
@@ -1504,9 +1569,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                     if (lane == 0) mbar_arrive(&pub_full_f[njob & 1]);
                     ++njob;
                 }
+                if (!(ok = piece_after(w, npc, true))) break;
                 ++npc;
-                __syncwarp();
-                w = *reinterpret_cast<const Walk*>(smem + L::kTl);
                 orow = rn;
             }
             if (*abort_flag != 0 && lane == 0) {
@@ -2301,7 +2365,7 @@ pd_status launch_decode_t(const DecodeArgs& a) {
     const int streams = kFork ? a.n_groups : a.B;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kMQ ? kDecodeThreads : kDecodeThreadsPub);
+    cfg.blockDim = dim3(kMQ && !kFork ? kDecodeThreads : kDecodeThreadsPub);
     cfg.dynamicSmemBytes = Lt::kAlloc;
     cfg.stream = a.stream;
     cudaLaunchAttribute attr[1];
