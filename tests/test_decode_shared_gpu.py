@@ -6,7 +6,8 @@ prompt's blocks (tutorial page "LLM 推理服务引擎深度拆解", section 2.3
 shares every block, a written shared block is copied first).  Covers the
 copy-on-write fork stress at every block size, random groups (sizes 1-32, no
 sharing, empty contexts, tails of 0..several stages), every column layout
-(1, 2 and 4 tiles), both element types and head dims, block-permutation
+(group sizes giving 8 to 32 columns), both element types and head dims, many
+small groups per CTA (the walk ring wrapping), block-permutation
 bit-identity, and the device check of the caller's sharing promise.
 """
 import numpy as np
@@ -139,6 +140,21 @@ def test_column_layouts(cuda_lib, G, M):
     c = pd_inputs.forked_decode(f"layout G{G} M{M}", 7, groups, G * Hk, Hk, 128, 16,
                                 torch.bfloat16)
     _check(cuda_lib, c, f"layout G{G} M{M}", max_group=M)
+
+
+@pytest.mark.parametrize("members", [1, 2])
+def test_many_small_groups_per_cta(cuda_lib, members):
+    """400 groups of one or two short contexts (at most two 64-token stages
+    each): every CTA's range spans about ten groups, so the per-CTA walk ring
+    (four positions) wraps several times and most stages start a new piece."""
+    rng = np.random.default_rng(400 + members)
+    groups = []
+    for _ in range(400):
+        P = int(rng.integers(0, 48)) if members > 1 else 0
+        groups.append((P, [P + int(rng.integers(1, 60)) for _ in range(members)]))
+    c = pd_inputs.forked_decode(f"small groups x{members}", 11 + members, groups, 32, 8, 128,
+                                16, torch.float16)
+    _check(cuda_lib, c, f"400 small groups x{members}", max_group=members)
 
 
 def test_bit_identical_under_block_permutation(cuda_lib):
