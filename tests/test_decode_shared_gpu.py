@@ -8,7 +8,8 @@ copy-on-write fork stress at every block size, random groups (sizes 1-32, no
 sharing, empty contexts, tails of 0..several stages), every column layout
 (group sizes giving 8 to 32 columns), both element types and head dims, many
 small groups per CTA (the walk ring wrapping), block-permutation
-bit-identity, and the device check of the caller's sharing promise.
+bit-identity, the device check of the caller's sharing promise, and the
+chained step eagerly and replayed from a CUDA graph.
 """
 import numpy as np
 import pytest
@@ -268,3 +269,57 @@ def test_step_shared_matches_separate_calls(cuda_lib, S):
             ref = oracle.decode(fc.q, rk, rv, bt, cl, fc.scale, odt(fc.dtype), rows=rows)
             assert_close(o2.cpu().reshape(-1, fc.D)[rows[0]:rows[1]],
                          ref.reshape(-1, fc.D)[rows[0]:rows[1]], f"cow step S{S}")
+
+
+def test_step_shared_in_a_cuda_graph(cuda_lib):
+    """pd_decode_step_shared captured once in a CUDA graph and replayed over
+    fresh pools (the copies and the store rewrite them each time): every
+    replay gives the bits of the eager step (tensor memory is allocated and
+    freed inside each launch, the arrival counters are left at zero)."""
+    pd = cuda_lib
+    S = 16
+    fc = pd_inputs.cow_fork_stress(S, n_prompts=8)
+    tables, ctx, slots, pairs = fork_flow(fc, OracleBM)
+    dev = torch.device("cuda")
+    mb = max(len(t) for t in tables)
+    bt = torch.zeros(len(tables), mb, dtype=torch.int32)
+    for i, t in enumerate(tables):
+        bt[i, :len(t)] = torch.tensor(t, dtype=torch.int32)
+    cl = torch.tensor(ctx, dtype=torch.int32)
+    gs, sl = pd.find_shared_prefixes(bt, cl, S, max_group=8)
+    q = fc.q.to(dev)
+    nk, nv = fc.new_key.to(dev), fc.new_value.to(dev)
+    sm = torch.tensor(slots, dtype=torch.int64, device=dev)
+    pr = torch.tensor(pairs, dtype=torch.int64, device=dev).view(-1, 2)
+    btd, cld, gsd, sld = bt.to(dev), cl.to(dev), gs.to(dev), sl.to(dev)
+    ws = pd.decode_shared_workspace(sl.numel(), 8, fc.H, fc.Hk, fc.D)
+    err = device_err()
+    kc, vc = fc.key_cache.to(dev), fc.value_cache.to(dev)
+    out = torch.full_like(q, float("nan"))
+
+    def step():
+        pd.pd_decode_step_shared(out, q, kc, vc, btd, cld, max(ctx), fc.scale, gsd, sld, 8,
+                                 key=nk, value=nv, slot_mapping=sm, block_mapping=pr,
+                                 workspace=ws, dev_err=err)
+
+    step()                                           # eager reference
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    ref = out.clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        kc.copy_(fc.key_cache)
+        vc.copy_(fc.value_cache)
+        with torch.cuda.graph(g, stream=side):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        kc.copy_(fc.key_cache.to(dev))
+        vc.copy_(fc.value_cache.to(dev))
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
