@@ -99,6 +99,65 @@ def test_consecutive_steps_see_their_own_tokens(cuda_lib):
     assert np.array_equal(u16(kc), rk) and np.array_equal(u16(vc), rv)
 
 
+@pytest.mark.parametrize("T", [48, 256, 300])
+def test_step_storing_early_tokens(cuda_lib, T):
+    """The store writes T tokens at random positions of the sequences (early
+    blocks included, several per sequence), each slot NaN in the pool until
+    then: the decode grid, started while the store grid runs, must not read
+    any of them before the store has written it (a read ahead would give
+    NaN), and three runs of the step give the same bits."""
+    B, H, Hk, D, S = 64, 32, 8, 128, 16
+    g = torch.Generator().manual_seed(90 + T)
+    ctx = torch.randint(64, 2049, (B,), generator=g)
+    c = pd_inputs.decode_case("early", 91, ctx.tolist(), H, Hk, D, S, torch.bfloat16,
+                              store_last=False, poison=False)
+    bt = c.pool.block_tables
+    # T distinct (sequence, position) pairs, position 0 of the first sequences included
+    seqs = torch.randint(0, B, (T,), generator=g)
+    pos = (torch.rand(T, generator=g) * ctx[seqs]).long()
+    pos[: min(T, 16)] = 0
+    seqs[: min(T, 16)] = torch.arange(min(T, 16))
+    slots = pd_inputs.slot_mapping_for(bt, seqs, pos, S)
+    keep = torch.ones(T, dtype=torch.bool)
+    seen = set()
+    for i, sl in enumerate(slots.tolist()):
+        keep[i] = sl not in seen
+        seen.add(sl)
+    slots = torch.where(keep, slots, torch.full_like(slots, -1))
+    w = slots[slots >= 0]
+    c.pool.key_cache[w // S, :, w % S] = float("nan")
+    c.pool.value_cache[w // S, :, w % S] = float("nan")
+    nk = torch.randn(T, Hk, D, generator=g).to(torch.bfloat16)
+    nv = torch.randn(T, Hk, D, generator=g).to(torch.bfloat16)
+    dev = torch.device("cuda")
+    kc, vc = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
+    rk, rv = u16(c.pool.key_cache), u16(c.pool.value_cache)
+    err = device_err()
+    ws = cuda_lib.decode_workspace(B, H, D, c.max_context_len)
+    outs = []
+    for _ in range(3):           # the same step again: the store rewrites the same values
+        out = torch.empty(B, H, D, dtype=torch.bfloat16, device=dev)
+        cuda_lib.pd_decode_step(out, c.q.to(dev), kc, vc, bt.to(dev),
+                                c.pool.context_lens.to(dev), c.max_context_len, c.scale,
+                                nk.to(dev), nv.to(dev), slots.to(dev), workspace=ws, dev_err=err)
+        outs.append(out)
+        if len(outs) == 1:       # the next steps start from the poisoned pool again
+            torch.cuda.synchronize()
+            kc.copy_(c.pool.key_cache.to(dev))
+            vc.copy_(c.pool.value_cache.to(dev))
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    oracle.reshape_and_cache(nk, nv, rk, rv, slots, S)
+    assert np.array_equal(u16(kc), rk) and np.array_equal(u16(vc), rv)
+    ref = oracle.decode(c.q, rk, rv, bt, c.pool.context_lens, c.scale, oracle.BF16,
+                        rows=(0, 64))
+    for i, out in enumerate(outs):
+        assert not out.isnan().any()
+        assert_close(out.cpu().reshape(-1, D)[0:64], ref.reshape(-1, D)[0:64],
+                     f"early store T{T} #{i}")
+        assert torch.equal(out.view(torch.int16), outs[0].view(torch.int16))
+
+
 @pytest.mark.parametrize("D", [64, 128])
 def test_fp8_step_equals_separate_calls_and_oracle(cuda_lib, D):
     c = pd_inputs.decode_case("fp8step", 64 + D, [1, 17, 64, 65, 700, 2049], 32, 8, D, 16,
