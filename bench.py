@@ -255,6 +255,12 @@ def run_ours(args, rank, world, local_rank):
     step_bytes = dec_bytes + st_bytes
 
     def step():
+        # one kernel: each sequence's new row is stored by the decode CTA that
+        # copies its block, right before the copy
+        pd.pd_decode_step_fused(out, q, kc, vc, bt, cl, mcl, c.scale, nk, nv, slots,
+                                workspace=ws, dev_err=err)
+
+    def two_kernel_step():
         pd.pd_decode_step(out, q, kc, vc, bt, cl, mcl, c.scale, nk, nv, slots, workspace=ws,
                           dev_err=err)
 
@@ -286,9 +292,15 @@ def run_ours(args, rank, world, local_rank):
             torch.distributed.barrier()
         return sum(a.elapsed_time(b) for a, b in ev) * 1e-3, wall, n
 
-    # the headline: whole decode steps (store, then decode as a dependent grid)
+    # the headline: whole decode steps (the store inside the decode)
     with nvtx_range("decode_step"):
         step_s, t_wall, launches = timed(step)
+    # the same step as two grids (store, then decode as a programmatic dependent)
+    with nvtx_range("decode_step_two_kernels"):
+        for _ in range(args.warmup):
+            flush()
+            two_kernel_step()
+        two_s, _, _ = timed(two_kernel_step)
     # the roofline's kernel alone: the same decode launched by itself
     with nvtx_range("decode_alone"):
         for _ in range(args.warmup):
@@ -312,8 +324,10 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": "qwen3_8b_decode_step", "batch": B, "q_heads": H, "kv_heads": Hk,
                    "head_dim": D, "block_size": S, "context_lens": "uniform [128, 2048], seed 0",
                    "kv_tokens": int(sum(ctx)), "pool_blocks": c.pool.NB,
-                   "step": "pd_decode_step: store 64 tokens, then split-context decode (one "
-                           "launch, in-kernel merge) as a programmatic dependent of the store",
+                   "step": "pd_decode_step_fused: one launch; the decode CTA that copies a "
+                           "sequence's last block first stores the sequence's new K/V row at "
+                           "its slot (the slot is checked against the table), then the "
+                           "split-context decode with its in-kernel merge",
                    "l2": "inputs larger than L2 (KV 321 MB vs 129 MB L2), and L2 flushed "
                          "before every timed step by reading a 256 MiB buffer",
                    "parallelism": f"replicas x{world}"},
@@ -331,6 +345,9 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": traffic, "traffic_source_sha": sha},
         "gpu_launches": launches,
         "wall_s_timed_loop": round(t_wall, 4),
+        "two_kernel_step_ms": round(rank_max(two_s, world, dev) / args.steps * 1e3, 5),
+        "two_kernel_step": "pd_decode_step: the store grid, then the decode as its "
+                           "programmatic dependent (same result, same bytes)",
     }
 
     # every rank runs its replica host to host; the job takes the slowest
@@ -420,17 +437,17 @@ def run_only_extras(args):
 
 def e2e_decode(pd, c, dev, args, step_bytes, world=1):
     """The same step through the public API from pinned host memory:
-    ``DecodeStep`` (one pinned buffer holding q, the new K/V, slots, block
-    tables and context lengths, all read by the kernels over the host link,
-    and ``out`` written back the same way, synchronize), replayed from a CUDA
-    graph; the same object run eagerly is reported beside it."""
+    ``DecodeStep(fused=True)`` (one pinned buffer holding q, the new K/V,
+    slots, block tables and context lengths, all read by the kernel over the
+    host link, and ``out`` written back the same way, synchronize), replayed
+    from a CUDA graph; the same object run eagerly is reported beside it."""
     import torch
     kc, vc = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     res = {}
     for graph in (True, False):
         st = pd.DecodeStep(kc, vc, c.B, c.H, c.B, c.pool.block_tables.shape[1],
-                           c.max_context_len, c.scale, c.dtype, graph=graph)
+                           c.max_context_len, c.scale, c.dtype, graph=graph, fused=True)
         h = st.host
         h["q"].copy_(c.q)
         h["key"].copy_(c.new_key)
@@ -459,7 +476,7 @@ def e2e_decode(pd, c, dev, args, step_bytes, world=1):
     return {"value": round(whole_job_value(step_bytes, args.steps, total, world), 2), "unit": "GB/s",
             "ms_per_step": round(total / args.steps * 1e3, 4),
             "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world,
-            "path": "DecodeStep replayed from a CUDA graph: pd_decode_step reading q, the "
+            "path": "DecodeStep replayed from a CUDA graph: pd_decode_step_fused reading q, the "
                     "new K/V, the slots, the block tables and the context lengths from one "
                     "pinned host buffer and writing out into pinned host memory over the "
                     "host link, synchronize; host wall clock per step, L2 flushed before "

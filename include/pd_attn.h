@@ -73,6 +73,8 @@ typedef enum pd_dtype { PD_F16 = 0, PD_BF16 = 1, PD_FP8_E4M3 = 2 } pd_dtype;
 #define PD_DEVERR_TIMEOUT 0x8     /* a bounded wait inside a kernel expired  */
 #define PD_DEVERR_SHARED_PREFIX 0x10 /* shared-prefix groups malformed, or a
                                         member's table differs in the prefix */
+#define PD_DEVERR_STEP_SLOT 0x20  /* fused step: a slot that is not the one of
+                                     the sequence's last token (not stored) */
 
 /* Text for a status code (static storage). */
 PD_API const char* pd_status_string(pd_status s);
@@ -441,6 +443,31 @@ PD_API pd_status pd_decode_step(const void* key, const void* value,
                                 int max_context_len, float scale, void* workspace,
                                 size_t workspace_bytes, pd_dtype dt,
                                 int32_t* dev_err, cudaStream_t stream);
+/* pd_decode_step_fused: the same step as pd_decode_step (same arguments, the
+ * same result) in ONE kernel, for the usual shape of a decode step: T == B,
+ * row i of key/value is the new token of sequence i, the last of its
+ * context (position context_lens[i] - 1), and slot_mapping[i] is that
+ * token's slot through the sequence's table (or < 0: nothing stored for it).
+ * The decode CTA that copies a sequence's last 64-token stage for a kv head
+ * writes the row into the pool right before that copy; no other CTA reads
+ * the block.  So the block holding a sequence's new token must be read by
+ * no other sequence of the batch (the copy-on-write rule of the tutorial
+ * page, section 2.3, gives every appended-to block a single owner).
+ * A slot that is not the one of the sequence's last token (or a context cut
+ * short by the table or max_context_len) is not stored and flags
+ * PD_DEVERR_STEP_SLOT.  16-bit pools, G = H / Hk <= 8 (else
+ * PD_ERR_UNSUPPORTED); T != B is PD_ERR_INVALID_ARG; T == B == 0 does
+ * nothing.  Inputs may be pinned host memory as for pd_decode_step. */
+PD_API pd_status pd_decode_step_fused(const void* key, const void* value,
+                                      const int64_t* slot_mapping, int T,
+                                      int64_t key_stride_tok, int64_t value_stride_tok,
+                                      void* out, const void* q, void* key_cache,
+                                      void* value_cache, const int32_t* block_tables,
+                                      int max_blocks_per_seq, const int32_t* context_lens,
+                                      int B, int H, int Hk, int D, int S, int NB,
+                                      int max_context_len, float scale, void* workspace,
+                                      size_t workspace_bytes, pd_dtype dt,
+                                      int32_t* dev_err, cudaStream_t stream);
 /* pd_decode_step_fp8: the same over E4M3 pools with per-kv-head float32
  * k_scale / v_scale [Hk] (DEVICE), used by both the store and the decode. */
 PD_API pd_status pd_decode_step_fp8(const void* key, const void* value,

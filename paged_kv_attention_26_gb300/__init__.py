@@ -34,6 +34,7 @@ PD_DEVERR_BLOCK_RANGE = 0x2
 PD_DEVERR_CTX_RANGE = 0x4
 PD_DEVERR_TIMEOUT = 0x8
 PD_DEVERR_SHARED_PREFIX = 0x10
+PD_DEVERR_STEP_SLOT = 0x20
 
 STATUS_NAMES = {0: "PD_OK", 1: "PD_ERR_INVALID_ARG", 2: "PD_ERR_UNSUPPORTED", 3: "PD_ERR_CUDA",
                 4: "PD_ERR_NO_FREE_BLOCK", 5: "PD_ERR_WORKSPACE_TOO_SMALL",
@@ -76,6 +77,8 @@ SIGNATURES = {
                                        _I, _F, _P, _SZ, _I, _P, _P]),
     "pd_decode_step": (_I, [_P, _P, _P, _I, _I64, _I64, _P, _P, _P, _P, _P, _I, _P, _I, _I,
                             _I, _I, _I, _I, _I, _F, _P, _SZ, _I, _P, _P]),
+    "pd_decode_step_fused": (_I, [_P, _P, _P, _I, _I64, _I64, _P, _P, _P, _P, _P, _I, _P, _I, _I,
+                                  _I, _I, _I, _I, _I, _F, _P, _SZ, _I, _P, _P]),
     "pd_decode_step_fp8": (_I, [_P, _P, _P, _I, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _I,
                                 _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _SZ, _I, _P, _P]),
     "pd_selftest_bounded_wait": (_I, [_P, ctypes.c_uint64, _P]),
@@ -556,9 +559,23 @@ def pd_selftest_bounded_wait(dev_err, limit_ns: int = 1_000_000, stream=None):
     _check("pd_selftest_bounded_wait", st)
 
 
+def pd_decode_step_fused(out, q, key_cache, value_cache, block_tables, context_lens,
+                         max_context_len: int, scale: float, key, value, slot_mapping,
+                         workspace=None, dev_err=None, stream=None):
+    """``pd_decode_step`` in one kernel, for a step whose row i of
+    ``key``/``value`` [B, Hk, D] is the last token of sequence i (its slot in
+    ``slot_mapping``, or < 0 for none): the decode stores each row right
+    before it copies the row's block.  16-bit pools, G <= 8; a slot that is
+    not the last token's flags ``PD_DEVERR_STEP_SLOT`` and is not stored."""
+    pd_decode_step(out, q, key_cache, value_cache, block_tables, context_lens, max_context_len,
+                   scale, key, value, slot_mapping, workspace=workspace, dev_err=dev_err,
+                   stream=stream, _fused=True)
+
+
 def pd_decode_step(out, q, key_cache, value_cache, block_tables, context_lens,
                    max_context_len: int, scale: float, key, value, slot_mapping,
-                   workspace=None, k_scale=None, v_scale=None, dev_err=None, stream=None):
+                   workspace=None, k_scale=None, v_scale=None, dev_err=None, stream=None,
+                   _fused=False):
     """One decode step of one layer: store ``key``/``value`` [T, Hk, D] at
     ``slot_mapping``, then decode ``q`` [B, H, D] over the paged caches into
     ``out``.  The same result as ``pd_reshape_and_cache`` (``_fp8`` with
@@ -599,6 +616,8 @@ def pd_decode_step(out, q, key_cache, value_cache, block_tables, context_lens,
             _dev(context_lens, "context_lens", torch.int32, host_ok=True), B, H, Hk, D, S, NB,
             int(max_context_len), float(scale), ws_ptr, ws_bytes, _dt(q), _opt(dev_err),
             _stream(stream))
+    if fp8 and _fused:
+        raise TypeError("the fused step takes 16-bit pools")
     if fp8:
         if k_scale is None or v_scale is None:
             raise ValueError("one-byte pools need k_scale and v_scale")
@@ -608,6 +627,9 @@ def pd_decode_step(out, q, key_cache, value_cache, block_tables, context_lens,
         st = load().pd_decode_step_fp8(*head, _dev(k_scale, "k_scale", torch.float32),
                                        _dev(v_scale, "v_scale", torch.float32), *tail)
         _check("pd_decode_step_fp8", st)
+    elif _fused:
+        st = load().pd_decode_step_fused(*head, *tail)
+        _check("pd_decode_step_fused", st)
     else:
         st = load().pd_decode_step(*head, *tail)
         _check("pd_decode_step", st)
@@ -628,13 +650,15 @@ class DecodeStep:
     step).  With ``graph=True`` the step is captured once in a CUDA graph and
     each call replays it;
     ``max_context_len`` and ``scale`` are fixed at construction (contexts may
-    vary per call up to that bound).  One-byte pools take
+    vary per call up to that bound).  ``fused=True`` runs
+    ``pd_decode_step_fused`` instead (T == B, row i the last token of
+    sequence i; 16-bit pools).  One-byte pools take
     ``k_scale``/``v_scale`` (float32 CUDA [Hk]).  The device error word of the
     last call is ``dev_err``."""
 
     def __init__(self, key_cache, value_cache, B: int, H: int, T: int, max_blocks_per_seq: int,
                  max_context_len: int, scale: float, dtype, k_scale=None, v_scale=None,
-                 graph: bool = True):
+                 graph: bool = True, fused: bool = False):
         torch = _torch()
         dev = key_cache.device
         NB, Hk, S, D = key_cache.shape
@@ -658,6 +682,7 @@ class DecodeStep:
         self.key_cache, self.value_cache = key_cache, value_cache
         self.k_scale, self.v_scale = k_scale, v_scale
         self.max_context_len, self.scale = int(max_context_len), float(scale)
+        self.fused = bool(fused)
         self.device = dev
         self.graph = None
         # one eager run on the harmless initial inputs (no slot stored, empty
@@ -675,6 +700,12 @@ class DecodeStep:
 
     def _body(self):
         h = self.host
+        if self.fused:
+            pd_decode_step_fused(self.host_out, h["q"], self.key_cache, self.value_cache,
+                                 h["block_tables"], h["context_lens"], self.max_context_len,
+                                 self.scale, h["key"], h["value"], h["slot_mapping"],
+                                 workspace=self.workspace, dev_err=self.dev_err)
+            return
         pd_decode_step(self.host_out, h["q"], self.key_cache, self.value_cache,
                        h["block_tables"], h["context_lens"], self.max_context_len, self.scale,
                        h["key"], h["value"], h["slot_mapping"], workspace=self.workspace,

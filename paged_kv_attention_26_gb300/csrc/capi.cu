@@ -250,6 +250,38 @@ pd_status pd_decode_step(const void* key, const void* value, const int64_t* slot
                        scale, workspace, workspace_bytes, dt, dev_err, stream);
 }
 
+pd_status pd_decode_step_fused(const void* key, const void* value, const int64_t* slot_mapping,
+                               int T, int64_t key_stride_tok, int64_t value_stride_tok,
+                               void* out, const void* q, void* key_cache, void* value_cache,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int B, int H, int Hk, int D, int S,
+                               int NB, int max_context_len, float scale, void* workspace,
+                               size_t workspace_bytes, pd_dtype dt, int32_t* dev_err,
+                               cudaStream_t stream) {
+    DecodeArgs a{};
+    bool skip_dec = false, skip_store = false;
+    pd_status st = decode_prepare(out, q, key_cache, value_cache, nullptr, nullptr, false,
+                                  block_tables, max_blocks_per_seq, context_lens, B, H, Hk, D, S,
+                                  NB, max_context_len, scale, workspace, workspace_bytes, dt,
+                                  dev_err, stream, &a, &skip_dec, 1);
+    if (st != PD_OK) return st;
+    st = store_check(key, value, key_cache, value_cache, slot_mapping, T, Hk, D, S, NB,
+                     key_stride_tok, value_stride_tok, false, nullptr, nullptr, dt, &skip_store);
+    if (st != PD_OK) return st;
+    if (T != B) return PD_ERR_INVALID_ARG;              // one new row per sequence
+    // every kv head must be read by one CTA group alone (G <= 8 query heads)
+    if (H / Hk > 8) return PD_ERR_UNSUPPORTED;
+    if (skip_dec) return PD_OK;
+    if (!skip_store) {
+        a.row_k = key;
+        a.row_v = value;
+        a.row_ks = key_stride_tok;
+        a.row_vs = value_stride_tok;
+        a.row_slots = slot_mapping;
+    }
+    return launch_decode(a);
+}
+
 pd_status pd_decode_step_fp8(const void* key, const void* value, const int64_t* slot_mapping,
                              int T, int64_t key_stride_tok, int64_t value_stride_tok, void* out,
                              const void* q, void* key_cache, void* value_cache,

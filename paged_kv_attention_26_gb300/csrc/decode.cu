@@ -176,6 +176,19 @@ struct Walk {
     int pj, pk, plen, pt0, pend;
 };
 
+// A decode step's new rows stored by the decode itself (one per sequence:
+// row i is token context_lens[i] - 1 of sequence i, at slots[i]); k == null:
+// nothing to store.  The pools are written through kc / vc and read through
+// the tensor maps.
+struct StepRows {
+    const void* k;
+    const void* v;
+    int64_t ks, vs;          // elements between consecutive rows
+    const int64_t* slots;
+    void* kc;
+    void* vc;
+};
+
 // the shared-prefix consumers park one in shared memory (128 bytes)
 static_assert(sizeof(Walk) <= 128 && alignof(Walk) <= 8, "walk record");
 
@@ -665,7 +678,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                           float* __restrict__ ws_m, float* __restrict__ ws_l,
                           unsigned long long* __restrict__ ws_cnt, unsigned long long tag,
                           const float* __restrict__ k_scale, const float* __restrict__ v_scale,
-                          ForkArgs fk, int32_t* dev_err) {
+                          ForkArgs fk, StepRows sr, int32_t* dev_err) {
     static_assert(!kFork || (kMQ && !kF8), "shared-prefix mode: 16-bit pools, column tiles");
     using L = DecodeSmem<D, kF8, kFork>;
     constexpr bool kNative = L::kNative;
@@ -767,6 +780,30 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
         };
         Walk wn = w;                                       // one stage ahead of w
         int blk_cur = stage_blk(w);
+        // Fused step (single-query decode on 16-bit pools, one unit per kv
+        // head): the new row of a stream is stored by the CTA that copies the
+        // stream's last stage, the only one that reads its block, right
+        // before that copy.  The row and its slot are loaded one stage ahead.
+        constexpr bool kRows = !kMQ && !kFork && !kF8;
+        auto row_load = [&](const Walk& x, uint4& r, int64_t& sl) {
+            r = make_uint4(0u, 0u, 0u, 0u);
+            sl = -1;
+            if constexpr (kRows) {
+                if (sr.k == nullptr || x.pos >= x.end || x.off != x.L - 1) return;
+                sl = __ldg(sr.slots + x.s);
+                const int c = lane & 15;             // 16-byte chunk: lanes 0.. K, 16.. V
+                if (c < D / 8) {
+                    const int64_t kvh_x = x.u / groups;
+                    const T* src = lane < 16
+                                       ? static_cast<const T*>(sr.k) + x.s * sr.ks + kvh_x * D
+                                       : static_cast<const T*>(sr.v) + x.s * sr.vs + kvh_x * D;
+                    r = __ldg(reinterpret_cast<const uint4*>(src) + c);
+                }
+            }
+        };
+        uint4 row_cur, row_next;
+        int64_t rs_cur, rs_next;
+        row_load(w, row_cur, rs_cur);
         // the stream of the last stage issued (tail merge)
         int tl_s = -1, tl_u = 0, tl_L = 0;
         long tl_start = 0;
@@ -804,6 +841,7 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             walk_step<kFork>(wn, context_lens, B, cap, S, fk);
             if (wn.s != s_before) prefetch_next_row(wn.s);
             const int blk_next = wn.pos < wn.end ? stage_blk(wn) : -2;
+            row_load(wn, row_next, rs_next);
             const int kvh = w.u / groups;
             int row = -1;
             if (blk_cur != -2) {
@@ -812,6 +850,33 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                 } else {
                     flag_error(dev_err, PD_DEVERR_BLOCK_RANGE);
                 }
+            }
+            if (kRows && rs_cur >= 0) {          // uniform: every lane loaded the slot
+                // the stream's new row goes into its last block (the stage's
+                // last, lane nblk - 1) before the copy: only the slot of the
+                // sequence's last token is taken
+                const int nt_w = w.ctx - w.off * kStageTokens;   // <= 64: the last stage
+                const int blast = __shfl_sync(0xffffffffu, blk_cur, ((nt_w + S - 1) >> log2S) - 1);
+                const int off_new = (w.ctx - 1) & (S - 1);
+                const bool whole = __ldg(context_lens + w.s) == w.ctx;   // not cut short
+                if (whole && blast >= 0 && blast < NB &&
+                    rs_cur == int64_t(blast) * S + off_new) {
+                    if ((lane & 15) < D / 8) {
+                        T* dst = (lane < 16 ? static_cast<T*>(sr.kc) : static_cast<T*>(sr.vc)) +
+                                 ((int64_t(blast) * Hk + kvh) * S + off_new) * D;
+                        reinterpret_cast<uint4*>(dst)[lane & 15] = row_cur;
+                        // each writer orders its store before the async
+                        // proxy's accesses (the tensor copy reads the block)
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                    }
+                } else if (lane == 0) {
+                    flag_error(dev_err, PD_DEVERR_STEP_SLOT);
+                }
+                // ... and the warp barrier orders the writers before the lanes
+                // that issue the copies (a global membar here cost ~2 us a
+                // launch, one per stream end on the producer's path)
+                __syncwarp();
+                asm volatile("fence.proxy.async.global;" ::: "memory");
             }
             const uint32_t ok_mask = __ballot_sync(0xffffffffu, row >= 0);
             if (lane == 0) mbar_arrive_expect_tx(&p_full[slot], 2u * block_bytes * __popc(ok_mask));
@@ -838,6 +903,8 @@ paged_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
             tl_start = w.start;
             w = wn;
             blk_cur = blk_next;
+            row_cur = row_next;
+            rs_cur = rs_next;
         }
         // ---- tail merge (one query per sequence).  The range's last stream
         // usually goes on in the next CTA's range, whose first piece was
@@ -2377,7 +2444,10 @@ pd_status launch_decode_t(const DecodeArgs& a) {
         &cfg, kern, tm_k, tm_v, static_cast<T*>(a.out), static_cast<const T*>(a.q),
         a.block_tables, a.max_blocks_per_seq, a.context_lens, streams, a.H, a.Hk, a.S, a.NB, GH,
         nq, scale_log2, P, cap, ws_o, ws_m, ws_l, ws_cnt, next_launch_tag(), a.k_scale, a.v_scale,
-        fk, a.dev_err));
+        fk,
+        StepRows{a.row_k, a.row_v, a.row_ks, a.row_vs, a.row_slots,
+                 const_cast<void*>(a.key_cache), const_cast<void*>(a.value_cache)},
+        a.dev_err));
 }
 
 template <bool kF8, bool kMQ, bool kFork>

@@ -47,6 +47,12 @@ struct DecodeArgs {
     const float* k_scale = nullptr;   // ... standing for code * scale[kv head]
     const float* v_scale = nullptr;
     bool pdl = false;            // launch as a programmatic dependent of the previous grid
+    // pd_decode_step_fused: row i of row_k / row_v (row_ks / row_vs elements
+    // between rows) is stored at row_slots[i] by the decode itself (null: none)
+    const void* row_k = nullptr;
+    const void* row_v = nullptr;
+    int64_t row_ks = 0, row_vs = 0;
+    const int64_t* row_slots = nullptr;
     int nq = 1;                  // query tokens per sequence (> 1: speculative verification)
     // shared-prefix mode (n_groups > 0): groups of consecutive sequences whose
     // tables agree on their first blocks

@@ -142,6 +142,20 @@ def test_decode_step_validation(lib):
     a[10], a[11] = P, None     # v_scale missing
     assert g(*a) == 1
     assert lib.pd_launch_count() == n0
+    # the one-kernel step: the same checks, then one row per sequence and a
+    # kv head read by one CTA group alone
+    h = lib.pd_decode_step_fused
+    for change, want in cases + [({3: 3}, 1),             # T != B
+                                 ({14: 40, 15: 4, 4: 256, 5: 256, 21: P, 22: 1 << 30},
+                                  2)]:                    # G = 10 > 8
+        a = list(base)
+        for k, v in change.items():
+            a[k] = v
+        assert h(*a) == want, change
+    a = list(base)
+    a[3], a[13] = 0, 0
+    assert h(*a) == 0
+    assert lib.pd_launch_count() == n0
 
 
 def test_verify_validation(lib):

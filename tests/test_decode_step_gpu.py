@@ -56,10 +56,12 @@ def test_step_equals_separate_calls_and_oracle(cuda_lib, which):
     assert np.array_equal(u16(kc), rk) and np.array_equal(u16(vc), rv)
 
 
-def test_consecutive_steps_see_their_own_tokens(cuda_lib):
+@pytest.mark.parametrize("fused", [False, True])
+def test_consecutive_steps_see_their_own_tokens(cuda_lib, fused):
     """20 decode steps of 8 sequences, one new token each per step.  Every
     slot a step stores is NaN in the pool until then, so a decode that read
-    it before the store grid finished would return NaN."""
+    it before the store grid finished (or, fused, before its own store of
+    the row) would return NaN."""
     steps = 20
     ctx0 = torch.tensor([1, 15, 16, 17, 63, 64, 300, 1100])
     H, Hk, D, S = 16, 4, 128, 16
@@ -86,9 +88,9 @@ def test_consecutive_steps_see_their_own_tokens(cuda_lib):
         nv = torch.randn(B, Hk, D, generator=g).to(torch.bfloat16)
         q = torch.randn(B, H, D, generator=g).to(torch.bfloat16)
         out = torch.empty(B, H, D, dtype=torch.bfloat16, device=dev)
-        cuda_lib.pd_decode_step(out, q.to(dev), kc, vc, btd, lens.to(dev), int(lens.max()),
-                                c.scale, nk.to(dev), nv.to(dev), slots.to(dev), workspace=ws,
-                                dev_err=err)
+        step = cuda_lib.pd_decode_step_fused if fused else cuda_lib.pd_decode_step
+        step(out, q.to(dev), kc, vc, btd, lens.to(dev), int(lens.max()), c.scale, nk.to(dev),
+             nv.to(dev), slots.to(dev), workspace=ws, dev_err=err)
         outs.append(out)
         oracle.reshape_and_cache(nk, nv, rk, rv, slots, S)
         refs.append(oracle.decode(q, rk, rv, bt, lens, c.scale, oracle.BF16))
@@ -96,6 +98,89 @@ def test_consecutive_steps_see_their_own_tokens(cuda_lib):
     assert err.item() == 0
     for i in range(steps):
         assert_close(outs[i].cpu(), refs[i], f"step {i}")
+    assert np.array_equal(u16(kc), rk) and np.array_equal(u16(vc), rv)
+
+
+def _rows_per_sequence(c):
+    """The case's new rows as one row per sequence (zeros and slot -1 for an
+    empty context), the layout of the fused step."""
+    ctx = c.pool.context_lens.to(torch.int64)
+    B = ctx.shape[0]
+    seqs = torch.nonzero(ctx > 0).flatten()
+    nk = torch.zeros(B, c.Hk, c.D, dtype=c.dtype)
+    nv = torch.zeros(B, c.Hk, c.D, dtype=c.dtype)
+    sl = torch.full((B,), -1, dtype=torch.int64)
+    nk[seqs], nv[seqs], sl[seqs] = c.new_key, c.new_value, c.slot_mapping
+    return nk, nv, sl
+
+
+@pytest.mark.parametrize("which", ["tiny", "qwen3_8b", "ragged", "f16_d64"])
+def test_fused_step_equals_step_and_oracle(cuda_lib, which):
+    """pd_decode_step_fused (the decode stores each sequence's new row right
+    before copying its block) gives the bits of pd_decode_step, the same
+    pools, and the oracle's store-then-decode result."""
+    if which == "tiny":
+        c = pd_inputs.tiny_decode()
+    elif which == "qwen3_8b":
+        c = pd_inputs.qwen3_8b_decode()
+    elif which == "ragged":
+        c = pd_inputs.decode_case("fragged", 92, [1, 0, 16, 17, 64, 65, 999, 2048, 5000], 16, 4,
+                                  128, 16, torch.bfloat16, key_outlier_frac=0.05)
+    else:
+        c = pd_inputs.decode_case("f16d64", 93, [1, 8, 9, 63, 64, 65, 129, 700], 8, 2, 64, 8,
+                                  torch.float16)
+    dev = torch.device("cuda")
+    nk, nv, sl = _rows_per_sequence(c)
+    q, bt, cl = c.q.to(dev), c.pool.block_tables.to(dev), c.pool.context_lens.to(dev)
+    ws = cuda_lib.decode_workspace(c.B, c.H, c.D, c.max_context_len)
+    err = device_err()
+    kc, vc = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
+    out = torch.empty_like(q)
+    cuda_lib.pd_decode_step_fused(out, q, kc, vc, bt, cl, c.max_context_len, c.scale,
+                                  nk.to(dev), nv.to(dev), sl.to(dev), workspace=ws, dev_err=err)
+    kc2, vc2 = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
+    ref_out = torch.empty_like(q)
+    cuda_lib.pd_decode_step(ref_out, q, kc2, vc2, bt, cl, c.max_context_len, c.scale,
+                            c.new_key.to(dev), c.new_value.to(dev), c.slot_mapping.to(dev),
+                            workspace=ws, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(kc.view(torch.int16), kc2.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), vc2.view(torch.int16))
+    rows = (0, 64) if which == "qwen3_8b" else None
+    ref, rk, rv = oracle_store_and_decode(c, rows=rows)
+    g = out.cpu()
+    if rows:
+        g = g.reshape(-1, c.D)[rows[0]:rows[1]]
+        ref = ref.reshape(-1, c.D)[rows[0]:rows[1]]
+    assert_close(g, ref, f"fused step {which}")
+    assert np.array_equal(u16(kc), rk) and np.array_equal(u16(vc), rv)
+
+
+def test_fused_step_flags_a_slot_off_the_last_token(cuda_lib):
+    """A slot that is not the one of the sequence's last token is not stored
+    and flags PD_DEVERR_STEP_SLOT; the other sequences' rows are stored."""
+    c = pd_inputs.decode_case("fbad", 94, [40, 100, 300], 8, 2, 128, 16, torch.bfloat16,
+                              poison=False)
+    dev = torch.device("cuda")
+    nk, nv, sl = _rows_per_sequence(c)
+    bad = sl.clone()
+    bad[1] = pd_inputs.slot_mapping_for(c.pool.block_tables, [1], [10], 16)[0]   # token 10
+    kc, vc = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
+    err = device_err()
+    out = torch.empty_like(c.q.to(dev))
+    cuda_lib.pd_decode_step_fused(out, c.q.to(dev), kc, vc, c.pool.block_tables.to(dev),
+                                  c.pool.context_lens.to(dev), c.max_context_len, c.scale,
+                                  nk.to(dev), nv.to(dev), bad.to(dev),
+                                  workspace=cuda_lib.decode_workspace(c.B, c.H, c.D,
+                                                                      c.max_context_len),
+                                  dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == cuda_lib.PD_DEVERR_STEP_SLOT
+    rk, rv = u16(c.pool.key_cache), u16(c.pool.value_cache)
+    keep = torch.tensor([0, 2])
+    oracle.reshape_and_cache(nk[keep], nv[keep], rk, rv, sl[keep], 16)
     assert np.array_equal(u16(kc), rk) and np.array_equal(u16(vc), rv)
 
 
@@ -200,8 +285,8 @@ def test_step_without_new_tokens_is_plain_decode(cuda_lib):
     assert torch.equal(out.view(torch.int16), sep.view(torch.int16))
 
 
-@pytest.mark.parametrize("graph", [False, True])
-def test_host_decode_step_replays(cuda_lib, graph):
+@pytest.mark.parametrize("graph,fused", [(False, False), (True, False), (True, True)])
+def test_host_decode_step_replays(cuda_lib, graph, fused):
     """DecodeStep: inputs written into its pinned views, one call per step.
     Six steps with new tokens, queries and context lengths each time; with a
     CUDA graph the decode replays with its launch tag fixed at capture, so
@@ -216,7 +301,8 @@ def test_host_decode_step_replays(cuda_lib, graph):
     kc, vc = c.pool.key_cache.to(dev), c.pool.value_cache.to(dev)
     rk, rv = u16(c.pool.key_cache), u16(c.pool.value_cache)
     mcl = int(ctx0.max()) + steps
-    st = pd.DecodeStep(kc, vc, B, H, B, bt.shape[1], mcl, c.scale, torch.bfloat16, graph=graph)
+    st = pd.DecodeStep(kc, vc, B, H, B, bt.shape[1], mcl, c.scale, torch.bfloat16, graph=graph,
+                       fused=fused)
     assert (graph and st.graph is not None) or (not graph and st.graph is None)
     g = torch.Generator().manual_seed(67)
     for i in range(steps):
@@ -236,7 +322,7 @@ def test_host_decode_step_replays(cuda_lib, graph):
         assert st.dev_err.item() == 0
         oracle.reshape_and_cache(nk, nv, rk, rv, slots, S)
         ref = oracle.decode(q, rk, rv, bt, lens, c.scale, oracle.BF16)
-        assert_close(got, ref, f"host step {i} graph={graph}")
+        assert_close(got, ref, f"host step {i} graph={graph} fused={fused}")
     assert np.array_equal(u16(kc), rk) and np.array_equal(u16(vc), rv)
     assert st.h2d_bytes >= (B * H * D + 2 * B * Hk * D) * 2 + B * 8 + bt.numel() * 4 + B * 4
     assert st.d2h_bytes == B * H * D * 2
