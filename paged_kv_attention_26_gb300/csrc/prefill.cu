@@ -32,11 +32,11 @@
 //    S row from tensor memory in 32-column chunks (a max pass, then an
 //    exponential pass), and write P over S for the PV product;
 //  * P is rounded to 16 bits for the tensor cores.  Where one key can carry a
-//    large share of a row's softmax mass (its weight may exceed 1/16), the
+//    large share of a row's softmax mass (its weight may exceed 1/8), the
 //    16-bit rounding error (2^-9 relative for bf16) is not averaged away, so
 //    that tile also gets the residual lo = rn(p - hi) as a second PV pass (a
-//    key of weight w <= 1/16 moves the output by at most 2^-13 |v| without it,
-//    a sixteenth of the output's own bf16 rounding);
+//    key of weight w <= 1/8 moves the output by at most 2^-12 |v| without it,
+//    an eighth of the output's own bf16 rounding);
 //    rows vote per warp, and the MMA issuer runs the second pass only when
 //    some row of the tile asked for it.
 // Every wait is bounded; a wait that runs out flags PD_DEVERR_TIMEOUT and the
@@ -65,7 +65,7 @@ constexpr int kPrefillThreads = 384;   // warp 0 TMA, 1 MMA, 2-3 spare, 4-7 / 8-
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kTmemCols = 512;    // S_A [0,128) O_A [128,256) S_B [256,384) O_B [384,512)
 constexpr float kRescaleThreshold = 8.0f;
-constexpr float kLoWeight = 1.0f / 16.0f;   // weight above which P's rounding is corrected
+constexpr float kLoWeight = 1.0f / 8.0f;   // weight above which P's rounding is corrected
 constexpr float kLog2e = 1.4426950408889634f;
 // Register split (384 threads launched at 168 each = 64512): the TMA/MMA
 // warpgroup keeps 80, the two softmax warpgroups take 208, which holds a
